@@ -1,0 +1,400 @@
+"""Benchmark of the spectral KV-cache codec hot path on one B300.
+
+One step = one pass of the whole path over one synthetic Llama-3.1-8B-shaped
+layer cache (8 KV heads x 32768 tokens x head_dim 128, bf16 K and V):
+  calibrate K and V (Gram + Jacobi eigenbasis on the first 2048 tokens)
+  -> allocate 2.0 bits/value by reverse water-filling
+  -> encode K and V (rotate, uniform +-3 sigma quantize, bit-pack)
+  -> decode K and V
+  -> one decode-step attention (32 query heads, GQA over the 8 KV heads)
+     read straight from the packed K/V streams.
+value = codec tokens per second over whole steps (a token = one position,
+all 8 heads, K and V), summed over ranks; inputs are resident in HBM and four
+rotating copies (512 MiB of inputs) keep every step's reads out of L2.
+
+--impl reference times the CPU oracle (the fp64 restatement in oracle/) on a
+bounded sample of the same workload and scales it to the same unit.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+T_TOK, H_KV, D = 32768, 8, 128
+N_CAL = 2048
+AVG_BITS = 2.0
+HQ = 32
+NCOPY = 4
+METRIC = "KV codec tokens/s (encode, decode)"
+UNIT = "tokens/s"
+WORKLOAD = ("llama3.1-8b-shaped layer: K,V [32768 tok, 8 kv heads, d 128] bf16, spiked+outlier "
+            "Student-t(4) synthetic; calibrate 2048 tok, 2.0 bits/value water-filled, uniform "
+            "+-3 sigma; encode+decode K,V; attn_decode 32 q heads over the packed cache")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import kv_cache_transform_encode_b300 as spx
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    seed = 1000 + rank
+    # rotating input copies (K, V) and outputs
+    K = [synth.spiked_t_torch(seed + 10 * c, T_TOK, H_KV, D, role=synth.ROLE_K, device=dev) for c in range(NCOPY)]
+    V = [synth.spiked_t_torch(seed + 10 * c, T_TOK, H_KV, D, role=synth.ROLE_V, device=dev) for c in range(NCOPY)]
+    q = torch.from_numpy(synth.queries(seed, 1, HQ, D)).to(torch.bfloat16).to(dev)
+    kp, vp = spx.Plan(H_KV, D, device=dev), spx.Plan(H_KV, D, device=dev)
+    # one allocation sizes the streams (2.0 bits/value -> R = 256 bits)
+    R = int(min(np.floor(AVG_BITS * D + 1e-9), 8 * D))
+    sbytes = spx.spectra_stream_bytes(R, T_TOK)
+    kc = [torch.zeros((H_KV, sbytes), dtype=torch.uint8, device=dev) for _ in range(NCOPY)]
+    vc = [torch.zeros((H_KV, sbytes), dtype=torch.uint8, device=dev) for _ in range(NCOPY)]
+    ko = [torch.empty((T_TOK, H_KV, D), dtype=torch.bfloat16, device=dev) for _ in range(NCOPY)]
+    vo = [torch.empty((T_TOK, H_KV, D), dtype=torch.bfloat16, device=dev) for _ in range(NCOPY)]
+    att = torch.empty((1, HQ, D), dtype=torch.float32, device=dev)
+    cws = torch.empty((spx.spectra_calibrate_workspace_bytes(H_KV, D, N_CAL),), dtype=torch.uint8, device=dev)
+    cws2 = torch.empty_like(cws)
+    aws = torch.empty((spx.spectra_attn_workspace_bytes(1, HQ, D, T_TOK) + 256,), dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    phases = ["calibrate", "alloc", "encode", "decode", "attn"]
+
+    def step(i, ev=None):
+        c = i % NCOPY
+        mark = (lambda k: ev[k].record(s)) if ev is not None else (lambda k: None)
+        mark(0)
+        spx.spectra_calibrate(kp, K[c], n_cal=N_CAL, workspace=cws)
+        spx.spectra_calibrate(vp, V[c], n_cal=N_CAL, workspace=cws2)
+        mark(1)
+        spx.spectra_alloc_bits(kp, AVG_BITS)
+        spx.spectra_alloc_bits(vp, AVG_BITS)
+        mark(2)
+        spx.spectra_encode(kp, K[c], kc[c])
+        spx.spectra_encode(vp, V[c], vc[c])
+        mark(3)
+        spx.spectra_decode(kp, kc[c], T_TOK, ko[c])
+        spx.spectra_decode(vp, vc[c], T_TOK, vo[c])
+        mark(4)
+        spx.spectra_attn_decode(kp, vp, q, kc[c], vc[c], T_TOK, 1.0, att, workspace=aws)
+        mark(5)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert np.all(kp.status.cpu().numpy() >= 0) and np.all(vp.status.cpu().numpy() >= 0)
+
+    # ---- timed region (device time)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    clk = ClockSampler(local_rank)
+    clk.start()
+    time.sleep(0.3)
+    _barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    for i in range(args.steps):
+        step(i, evs[i])
+    t1.record(s)
+    torch.cuda.synchronize()
+    _barrier(world)
+    clocks = clk.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    ms = _max_over_ranks(ms, world)
+    ph = {p: statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evs) for k, p in enumerate(phases)}
+
+    # ---- end to end through the API with host buffers (pinned), per step:
+    # H2D of K and V, the whole path, D2H of the packed codes and the output
+    hK = K[0].cpu().pin_memory()
+    hV = V[0].cpu().pin_memory()
+    hkc = torch.empty_like(kc[0], device="cpu").pin_memory()
+    hvc = torch.empty_like(vc[0], device="cpu").pin_memory()
+    hatt = torch.empty_like(att, device="cpu").pin_memory()
+
+    def e2e_step(i):
+        c = i % NCOPY
+        K[c].copy_(hK, non_blocking=True)
+        V[c].copy_(hV, non_blocking=True)
+        step(i)
+        hkc.copy_(kc[c], non_blocking=True)
+        hvc.copy_(vc[c], non_blocking=True)
+        hatt.copy_(att, non_blocking=True)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    _barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    n_e2e = max(3, args.steps // 2)
+    for i in range(n_e2e):
+        e2e_step(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
+    h2d = hK.numel() * 2 + hV.numel() * 2
+    d2h = hkc.numel() + hvc.numel() + hatt.numel() * 4
+
+    # ---- roofline of the dominant HBM kernel (encode or decode, whichever
+    # takes longer; each phase is two launches, K and V)
+    import json as _json
+    peaks = _peaks()
+    enc_bytes = 2 * (T_TOK * H_KV * D * 2 + H_KV * sbytes)      # per phase (K+V)
+    dec_bytes = enc_bytes
+    dom = "encode" if ph["encode"] >= ph["decode"] else "decode"
+    per_launch_bytes = (enc_bytes if dom == "encode" else dec_bytes) / 2
+    per_launch_ms = ph[dom] / 2
+    achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "peak_source": peaks["source"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": None}
+
+    tokens = T_TOK * world
+    res = {
+        "metric": METRIC, "value": round(tokens / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded spiked-covariance multivariate Student-t, bf16)",
+        "config": {"workload": WORKLOAD, "tokens": T_TOK, "kv_heads": H_KV, "head_dim": D,
+                   "avg_bits": AVG_BITS, "n_cal": N_CAL, "q_heads": HQ, "parallelism": f"replicas x{world}",
+                   "l2": f"{NCOPY} rotating input/output copies, {NCOPY * 2 * T_TOK * H_KV * D * 2 >> 20} MiB of inputs > L2"},
+        "phases_ms": {k: round(v, 4) for k, v in ph.items()},
+        "codec_tokens_per_s": round(T_TOK / ((ph["encode"] + ph["decode"]) * 1e-3), 1),
+        "roofline": roof,
+        "clocks": clocks,
+        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps * launches_per_step(),
+    }
+    return res
+
+
+def launches_per_step():
+    """Kernels this library launches per step (counted from the dispatch in
+    csrc/api.cu): calibrate = Gram partials + Jacobi; alloc = water-filling +
+    finalize; encode 1; decode 1 -- each for K and V; attention = query
+    rotation + split kernel + combine."""
+    per_side = 2 + 2 + 1 + 1
+    return 2 * per_side + 3
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle
+def oracle_sample(seconds_budget: float = 20.0):
+    """Time the CPU oracle on a bounded sample of the workload: calibrate K
+    and V (2048 tokens, 8 heads), allocate, encode+decode a slice of tokens
+    for all heads, attention over that slice; scale the per-token parts to
+    32768 tokens.  Heads run on a thread pool (ctypes releases the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle as orc
+    import synth
+
+    cores = min(2 * H_KV, os.cpu_count() or 1)
+    n_tok = 8192
+    Kx = synth.to_bf16_exact(synth.spiked_t(7, N_CAL, H_KV, D, role=synth.ROLE_K)).astype(np.float64)
+    Vx = synth.to_bf16_exact(synth.spiked_t(7, N_CAL, H_KV, D, role=synth.ROLE_V)).astype(np.float64)
+    orc.lloyd_max_tables()
+    pool = ThreadPoolExecutor(cores)
+    t0 = time.perf_counter()
+    # calibrate: per head in parallel
+    def cal(job):
+        x, h = job
+        lam, Q, _ = orc.jacobi_eigh(orc.gram(x[:, h, :]))
+        return lam, Q
+    res = list(pool.map(cal, [(x, h) for x in (Kx, Vx) for h in range(H_KV)]))
+    t_cal = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    plans = []
+    for side in range(2):
+        lam = np.stack([res[side * H_KV + h][0] for h in range(H_KV)]).astype(np.float32).astype(np.float64)
+        Q = np.stack([res[side * H_KV + h][1] for h in range(H_KV)]).astype(np.float32).astype(np.float64)
+        R = orc.total_bits(AVG_BITS, D)
+        bits = np.stack([orc.alloc(lam[h], R) for h in range(H_KV)])
+        plans.append(orc.Plan(orc.BASIS_EIGEN, orc.QUANT_UNIFORM, bits, basis=Q, eigvals=lam))
+    t_alloc = time.perf_counter() - t1
+    t2 = time.perf_counter()
+    xs = (Kx[:n_tok], Vx[:n_tok])
+
+    def encdec(job):
+        side, h = job
+        e = orc.encode_head(plans[side], h, xs[side][:, h, :])
+        return orc.decode_head(plans[side], h, e["stream"], n_tok)
+    rec = list(pool.map(encdec, [(s, h) for s in range(2) for h in range(H_KV)]))
+    t_encdec = time.perf_counter() - t2
+    t3 = time.perf_counter()
+    q = synth.queries(1, 1, HQ, D).astype(np.float64)
+    Kh = np.stack([rec[h] for h in range(H_KV)], 1)[None]
+    Vh = np.stack([rec[H_KV + h] for h in range(H_KV)], 1)[None]
+    orc.attn_decode(q, Kh, Vh, 1.0)
+    t_attn = time.perf_counter() - t3
+    scale = T_TOK / n_tok
+    est = t_cal + t_alloc + (t_encdec + t_attn) * scale
+    return {"value": round(T_TOK / est, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"calibrate K,V (2048 tok x 8 heads) + alloc measured in full; encode+decode "
+                       f"and attention measured on {n_tok} of {T_TOK} tokens (all heads) and scaled "
+                       f"x{scale:g}; wall {t_cal + t_alloc + t_encdec + t_attn:.1f} s"),
+            "seconds": {"calibrate": round(t_cal, 3), "alloc": round(t_alloc, 4),
+                        "encode_decode_sample": round(t_encdec, 3), "attn_sample": round(t_attn, 3)},
+            "est_step_s": round(est, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    vals = []
+    t_all = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample()
+        if i >= args.warmup:
+            vals.append(r)
+        if time.perf_counter() - t_all > 240 and len(vals) >= 1:
+            break
+    v = statistics.mean(r["value"] for r in vals)
+    est = statistics.mean(r["est_step_s"] for r in vals)
+    cb = dict(vals[-1])
+    cb["value"] = round(v, 2)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": UNIT, "n_gpus": world,
+            "steps": len(vals), "warmup": args.warmup, "ms_per_step": round(est * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded spiked-covariance multivariate Student-t, bf16-rounded)",
+            "config": {"workload": WORKLOAD, "tokens": T_TOK, "kv_heads": H_KV, "head_dim": D,
+                       "avg_bits": AVG_BITS, "n_cal": N_CAL, "q_heads": HQ},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = oracle_sample()
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,242 @@
+/*
+ * spectra.h -- C ABI of the spectral transform codec for transformer KV
+ * caches (sm_103a).
+ *
+ * Method (page titles and sections):
+ *  - "Sintesi Tecnica: SPECTRA" (gist.science, paper 2608.07915):
+ *      "Metodologia" items 1-3 -- rotate the cache into the eigenbasis of
+ *      its own second-moment (Gram) matrix G = E[h^T h], where channels are
+ *      uncorrelated and energy concentrates; importance-weighted bit
+ *      allocation; zero-bit channels are dropped.
+ *      "La Pipeline di SPECTRA" phase 2 -- reverse water-filling of bits on
+ *      the measured marginal variances; phase 3 -- tokens are projected,
+ *      quantized per token and appended to a latent cache; full keys and
+ *      values are rebuilt on the fly.  "Significato e Rivendicazioni" --
+ *      attention directly in the latent space (here: spectra_attn_decode).
+ *  - "Technisch Overzicht: Ablatie, Statistische Inferentie en Validatie
+ *      voor KV-Cache Compressie" (gist.science, paper 2607.09683),
+ *      "Experimentele Opstelling": randomized Walsh-Hadamard rotation with a
+ *      data-independent Lloyd-Max codebook (the RWHT basis here), and the
+ *      per-head eigenbasis calibrated on representative tokens.
+ *
+ * Conventions shared by every call:
+ *  - All pointers are DEVICE pointers unless stated, caller-allocated and
+ *    caller-owned.  The library allocates and frees nothing and keeps no
+ *    state between calls: every table it needs lives in the plan.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy
+ *    default stream).  Host-detectable argument errors return a non-OK
+ *    status before anything is launched.  Conditions only the device can
+ *    see (a non-finite Gram matrix, an unconverged eigensolve, a stream
+ *    buffer too small for a head's record) are written to plan->status[h]
+ *    and read by the caller after synchronising.
+ *  - Caches are row-major [tokens][heads][head_dim]: element (t, h, i) of x
+ *    is at x[t * token_stride + h * head_dim + i] (token_stride in
+ *    elements, >= heads * head_dim).  head_dim is 64 or 128.
+ *  - A "head" is one (layer, kv-head) pair: a multi-layer cache laid out as
+ *    [tokens][layers * kv_heads][head_dim] is one call with
+ *    heads = layers * kv_heads.
+ *
+ * Packed-code stream (one per head; the pages print no bit layout, this is
+ * the library's own): tokens in groups of 32; with R = sum_c bits[c] and
+ * o_c = sum_{c' < c} bits[c'], group g holds R little-endian 32-bit words,
+ * and bit (t mod 32) of word g*R + o_c + k is bit k of the code of channel c
+ * of token t.  Channels are in eigenvalue-descending order; 0-bit channels
+ * take no space.  A stream of T tokens takes spectra_stream_bytes(R, T)
+ * bytes (zero-padded to a multiple of 16).
+ */
+#ifndef SPECTRA_H
+#define SPECTRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPECTRA_API __attribute__((visibility("default")))
+#else
+#define SPECTRA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* spectra_stream_t; /* == cudaStream_t */
+
+typedef enum {
+    SPECTRA_OK = 0,
+    SPECTRA_ERR_INVALID_ARG = 1,   /* bad pointer, size, stride or enum   */
+    SPECTRA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d)   */
+    SPECTRA_ERR_CUDA = 3,          /* a CUDA runtime call failed           */
+    SPECTRA_ERR_NOT_CONVERGED = 4, /* device status: eigensolve gave up    */
+    SPECTRA_ERR_TIMEOUT = 5,       /* device status: a bounded wait ran out*/
+    SPECTRA_ERR_NONFINITE = 6,     /* device status: NaN/Inf in the input  */
+    SPECTRA_ERR_BUFFER = 7         /* device status: stream buffer too small */
+} spectra_status;
+
+typedef enum { SPECTRA_BF16 = 0, SPECTRA_F32 = 1 } spectra_dtype;
+typedef enum { SPECTRA_BASIS_EIGEN = 0, SPECTRA_BASIS_RWHT = 1 } spectra_basis;
+typedef enum { SPECTRA_Q_UNIFORM3S = 0, SPECTRA_Q_LLOYD_GAUSS = 1 } spectra_quant;
+
+/*
+ * Per-head codec plan.  Host-side ints describe the shape; every pointer is
+ * a caller-owned device buffer of the stated size.
+ *   basis_mat [heads][d][d] f32  EIGEN: basis_mat[h][i][c] = component i of
+ *                                the eigenvector of channel c (channels in
+ *                                eigenvalue-descending order).  Unused by RWHT.
+ *   eigvals   [heads][d]    f32  EIGEN: marginal variance of channel c.
+ *   signs     [heads][d]    i8   RWHT: the +-1 diagonal D of y = H D x / sqrt(d)
+ *                                (random draws supplied by the caller).
+ *   bits      [heads][d]    u8   width of channel c, 0..8 (0 = dropped).
+ *   rec_bits  [heads]       i32  R_h = sum_c bits[h][c].
+ *   derived   spectra_plan_derived_bytes(heads, d) bytes, 256-B aligned:
+ *                                tables written by spectra_plan_finalize.
+ *   status    [heads]       i32  device status words (see above).
+ *   max_rec_bits                 host-side upper bound on every R_h, set by
+ *                                spectra_alloc_bits (or by the caller before
+ *                                spectra_plan_finalize); sizes the streams.
+ */
+typedef struct {
+    int32_t heads;
+    int32_t head_dim;
+    int32_t basis;          /* spectra_basis */
+    int32_t quant;          /* spectra_quant */
+    int32_t max_rec_bits;
+    int32_t reserved;
+    float* basis_mat;
+    float* eigvals;
+    int8_t* signs;
+    uint8_t* bits;
+    int32_t* rec_bits;
+    void* derived;
+    int32_t* status;
+} spectra_plan;
+
+/* Library version (major*10000 + minor*100 + patch). */
+SPECTRA_API int spectra_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+SPECTRA_API const char* spectra_status_string(spectra_status st);
+
+/* Bytes of the plan's `derived` buffer for `heads` heads of width d. */
+SPECTRA_API size_t spectra_plan_derived_bytes(int heads, int head_dim);
+
+/* Bytes of one packed stream of T tokens at R bits per token (zero-padded
+ * to a multiple of 16).  0 when R == 0 or T == 0. */
+SPECTRA_API size_t spectra_stream_bytes(int32_t rec_bits, int64_t T);
+
+/*
+ * spectra_calibrate -- per-head Gram matrix and its eigenbasis.
+ * ("Sintesi Tecnica: SPECTRA", "Metodologia" items 1 and 3; "Technisch
+ * Overzicht ...", "Experimentele Opstelling": per-head eigenbasis calibrated
+ * on representative tokens.)
+ *   G_h = (1/n_cal) sum_{t < n_cal} x[t,h,:] x[t,h,:]^T   (uncentred), then
+ *   G_h = Q diag(lam) Q^T by cyclic Jacobi, one thread block per head, lam
+ *   descending (ties: lower index first), each eigenvector's largest-|.|
+ *   component positive (ties: lowest row).
+ * x: [n_cal][heads][d] of dtype `dt`, token_stride in elements (for BF16 a
+ *   multiple of 8, for F32 a multiple of 4; x 16-byte aligned).
+ * Writes plan->basis_mat, plan->eigvals and plan->status[h] (= sweeps used,
+ *   or -SPECTRA_ERR_NOT_CONVERGED / -SPECTRA_ERR_NONFINITE).
+ * workspace: spectra_calibrate_workspace_bytes(heads, d, n_cal) bytes.
+ * gram_out: optional [heads][d][d] f32 copy of G (NULL to skip).
+ * max_sweeps: 1..100 (Jacobi sweeps before giving up).
+ */
+SPECTRA_API size_t spectra_calibrate_workspace_bytes(int heads, int head_dim, int64_t n_cal);
+SPECTRA_API spectra_status spectra_calibrate(spectra_plan* plan, const void* x, spectra_dtype dt,
+                                 int64_t n_cal, int64_t token_stride, int max_sweeps,
+                                 void* workspace, size_t workspace_bytes, float* gram_out,
+                                 spectra_stream_t stream);
+
+/*
+ * spectra_alloc_bits -- integer reverse water-filling, then finalize.
+ * ("Sintesi Tecnica: SPECTRA", "La Pipeline di SPECTRA" phase 2; zero-bit
+ * channels dropped, "Metodologia" item 2.)
+ * fixed_bits == 0: R_tot = min(floor(avg_bits * d + 1e-9), 8 d) one-bit
+ *   increments, each to the channel with the largest eigvals[c] * 4^-b_c
+ *   among channels below 8 bits (lowest index on ties; negative eigenvalues
+ *   count as 0).  Every head gets exactly R_tot bits.
+ * fixed_bits in 1..8: every channel gets fixed_bits (no water-filling; the
+ *   RWHT variant and uniform-allocation variants).
+ * Writes plan->bits, plan->rec_bits and the derived tables; sets
+ * plan->max_rec_bits on the host.
+ */
+SPECTRA_API spectra_status spectra_alloc_bits(spectra_plan* plan, double avg_bits, int fixed_bits,
+                                  spectra_stream_t stream);
+
+/*
+ * spectra_plan_finalize -- recompute rec_bits and the derived tables from a
+ * plan whose bits (and eigvals / basis_mat / signs) the caller filled in.
+ * plan->max_rec_bits must already bound every R_h.
+ */
+SPECTRA_API spectra_status spectra_plan_finalize(spectra_plan* plan, spectra_stream_t stream);
+
+/*
+ * spectra_encode -- rotate, quantize and bit-pack T tokens of every head.
+ * ("Sintesi Tecnica: SPECTRA", "La Pipeline di SPECTRA" phase 3: tokens are
+ * projected down, quantized per token and appended to the latent cache.)
+ * EIGEN: y_c = sum_i basis_mat[i][c] x_i for channels with bits > 0.
+ * RWHT:  y = H D x / sqrt(d) (Sylvester Hadamard, natural order).
+ * UNIFORM3S: sigma_c = sqrt(max(eigvals[c], 0)), Delta = 6 sigma_c / 2^b,
+ *   code = clamp(floor((y + 3 sigma_c) / Delta), 0, 2^b - 1).
+ * LLOYD_GAUSS: code = #{Gaussian Lloyd-Max thresholds tau_k <= y / sigma},
+ *   sigma = sigma_c (EIGEN) or ||x|| / sqrt(d) per token (RWHT).
+ * x: [T][heads][d] of dtype `dt` (token_stride as in spectra_calibrate).
+ * codes: head h's stream starts at codes + h * stream_stride_bytes (16-byte
+ *   aligned; stride >= spectra_stream_bytes(plan->max_rec_bits, T)); token 0
+ *   of the call is written at the start of that stream.  To append after t0
+ *   tokens (t0 a multiple of 128), pass codes + t0 / 32 * 4 * R.
+ * norms: RWHT only, f32, norms[h * norms_stride + t] = ||x[t,h,:]||;
+ *   NULL otherwise.
+ */
+SPECTRA_API spectra_status spectra_encode(const spectra_plan* plan, const void* x, spectra_dtype dt,
+                              int64_t T, int64_t token_stride, uint8_t* codes,
+                              int64_t stream_stride_bytes, float* norms, int64_t norms_stride,
+                              spectra_stream_t stream);
+
+/*
+ * spectra_decode -- unpack, dequantize, rotate back.
+ * ("Sintesi Tecnica: SPECTRA", "La Pipeline di SPECTRA" phase 3: full keys
+ * and values rebuilt on the fly.)
+ * UNIFORM3S: y_c = -3 sigma_c + (code + 1/2) Delta; LLOYD_GAUSS:
+ *   y_c = sigma * level[b][code]; dropped channels y_c = 0.
+ * EIGEN: x_i = sum_c basis_mat[i][c] y_c.   RWHT: x = D H y / sqrt(d).
+ * codes/norms as in spectra_encode; x_out: [T][heads][d] of out_dt with
+ * token_stride in elements.
+ */
+SPECTRA_API spectra_status spectra_decode(const spectra_plan* plan, const uint8_t* codes,
+                              int64_t stream_stride_bytes, const float* norms,
+                              int64_t norms_stride, int64_t T, void* x_out, spectra_dtype out_dt,
+                              int64_t token_stride, spectra_stream_t stream);
+
+/*
+ * spectra_attn_decode -- one decode step of grouped-query attention read
+ * straight from packed K/V streams, computed in the latent basis.
+ * ("Sintesi Tecnica: SPECTRA", "Significato e Rivendicazioni": attention
+ * directly in the latent space.)
+ * For batch b and query head j (kv head h = j / (Hq / Hkv), Hkv =
+ * kplan->heads = vplan->heads):
+ *   s_t = softmax_scale * <q[b,j], khat_t>,  p = softmax(s),
+ *   out[b,j] = sum_t p_t vhat_t,
+ * with khat/vhat the spectra_decode reconstructions of the streams; the
+ * rotation of q into the K basis and of the latent output back out of the
+ * V basis are done by the library (khat, vhat are never written).
+ * q: [B][Hq][d] of q_dt.  Streams of (b, h) at k_codes / v_codes +
+ *   (b * Hkv + h) * stream_stride_bytes, each holding ctx tokens.
+ * norms (RWHT plans only): k_norms / v_norms[(b * Hkv + h) * norms_stride + t].
+ * out: [B][Hq][d] f32.
+ * workspace: spectra_attn_workspace_bytes(B, Hq, d, ctx) bytes (split-context
+ *   partials).
+ */
+SPECTRA_API size_t spectra_attn_workspace_bytes(int B, int Hq, int head_dim, int64_t ctx);
+SPECTRA_API spectra_status spectra_attn_decode(const spectra_plan* kplan, const spectra_plan* vplan,
+                                   const void* q, spectra_dtype q_dt, int B, int Hq,
+                                   const uint8_t* k_codes, const uint8_t* v_codes,
+                                   int64_t stream_stride_bytes, const float* k_norms,
+                                   const float* v_norms, int64_t norms_stride, int64_t ctx,
+                                   float softmax_scale, float* out, void* workspace,
+                                   size_t workspace_bytes, spectra_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECTRA_H */

@@ -1,0 +1,245 @@
+"""Spectral transform coding of transformer KV caches on B300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/spectra.h``: the functions
+below carry the same names and only marshal arguments (torch tensors ->
+device pointers, the current torch stream -> cudaStream_t).  Every step of
+the codec runs in the CUDA library ``libspectra.so`` built in-tree by
+``kv_cache_transform_encode_b300.build``; importing this module on a machine
+where that library cannot be loaded raises, and there is no CPU fallback.
+
+Method: "Sintesi Tecnica: SPECTRA" (gist.science 2608.07915) -- Gram-matrix
+eigenbasis, reverse water-filling of bits, zero-bit channels dropped,
+per-token quantize-and-append, on-the-fly reconstruction, attention in the
+latent space; "Technisch Overzicht ... KV-Cache Compressie" (gist.science
+2607.09683) -- randomized Walsh-Hadamard rotation with a Lloyd-Max codebook.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from . import build as _build
+
+SPECTRA_OK = 0
+SPECTRA_BF16, SPECTRA_F32 = 0, 1
+SPECTRA_BASIS_EIGEN, SPECTRA_BASIS_RWHT = 0, 1
+SPECTRA_Q_UNIFORM3S, SPECTRA_Q_LLOYD_GAUSS = 0, 1
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
+                4: "eigensolve not converged", 5: "bounded wait timed out",
+                6: "non-finite input", 7: "stream buffer too small"}
+
+EXPORTS = ("spectra_version", "spectra_status_string", "spectra_plan_derived_bytes",
+           "spectra_stream_bytes", "spectra_calibrate_workspace_bytes", "spectra_calibrate",
+           "spectra_alloc_bits", "spectra_plan_finalize", "spectra_encode", "spectra_decode",
+           "spectra_attn_workspace_bytes", "spectra_attn_decode")
+
+
+class SpectraError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status})")
+        self.status = status
+
+
+class spectra_plan(C.Structure):
+    _fields_ = [("heads", C.c_int32), ("head_dim", C.c_int32), ("basis", C.c_int32),
+                ("quant", C.c_int32), ("max_rec_bits", C.c_int32), ("reserved", C.c_int32),
+                ("basis_mat", C.c_void_p), ("eigvals", C.c_void_p), ("signs", C.c_void_p),
+                ("bits", C.c_void_p), ("rec_bits", C.c_void_p), ("derived", C.c_void_p),
+                ("status", C.c_void_p)]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> C.CDLL:
+    """Load libspectra.so (built in-tree); raise if it is missing."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise ImportError(f"libspectra.so is not built ({path}); run "
+                              "python -m kv_cache_transform_encode_b300.build")
+        h = C.CDLL(path)
+        vp, i32, i64, sz, f32, f64 = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t, C.c_float, C.c_double
+        P = C.POINTER(spectra_plan)
+        sig = {
+            "spectra_version": (C.c_int, []),
+            "spectra_status_string": (C.c_char_p, [C.c_int]),
+            "spectra_plan_derived_bytes": (sz, [C.c_int, C.c_int]),
+            "spectra_stream_bytes": (sz, [i32, i64]),
+            "spectra_calibrate_workspace_bytes": (sz, [C.c_int, C.c_int, i64]),
+            "spectra_calibrate": (C.c_int, [P, vp, C.c_int, i64, i64, C.c_int, vp, sz, vp, vp]),
+            "spectra_alloc_bits": (C.c_int, [P, f64, C.c_int, vp]),
+            "spectra_plan_finalize": (C.c_int, [P, vp]),
+            "spectra_encode": (C.c_int, [P, vp, C.c_int, i64, i64, vp, i64, vp, i64, vp]),
+            "spectra_decode": (C.c_int, [P, vp, i64, vp, i64, i64, vp, C.c_int, i64, vp]),
+            "spectra_attn_workspace_bytes": (sz, [C.c_int, C.c_int, C.c_int, i64]),
+            "spectra_attn_decode": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp, vp,
+                                              i64, i64, f32, vp, vp, sz, vp]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(h, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = h
+    return _LIB
+
+
+def _check(st: int, what: str):
+    if st != SPECTRA_OK:
+        raise SpectraError(st, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPECTRA_BF16
+    if t.dtype == torch.float32:
+        return SPECTRA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+class Plan:
+    """Device buffers of one codec plan (caller-owned, allocated through
+    torch) and the matching C struct."""
+
+    def __init__(self, heads: int, head_dim: int, basis: int = SPECTRA_BASIS_EIGEN,
+                 quant: int = SPECTRA_Q_UNIFORM3S, device="cuda"):
+        self.heads, self.head_dim, self.basis, self.quant = heads, head_dim, basis, quant
+        H, d = heads, head_dim
+        kw = dict(device=device)
+        self.basis_mat = torch.zeros((H, d, d), dtype=torch.float32, **kw)
+        self.eigvals = torch.zeros((H, d), dtype=torch.float32, **kw)
+        self.signs = torch.ones((H, d), dtype=torch.int8, **kw)
+        self.bits = torch.zeros((H, d), dtype=torch.uint8, **kw)
+        self.rec_bits = torch.zeros((H,), dtype=torch.int32, **kw)
+        nbytes = spectra_plan_derived_bytes(H, d)
+        self._derived = torch.zeros((nbytes + 256,), dtype=torch.uint8, **kw)
+        off = (-self._derived.data_ptr()) % 256
+        self.derived = self._derived[off: off + nbytes]
+        self.status = torch.zeros((H,), dtype=torch.int32, **kw)
+        self.max_rec_bits = 0
+
+    def c(self) -> spectra_plan:
+        return spectra_plan(self.heads, self.head_dim, self.basis, self.quant, self.max_rec_bits, 0,
+                            self.basis_mat.data_ptr(), self.eigvals.data_ptr(), self.signs.data_ptr(),
+                            self.bits.data_ptr(), self.rec_bits.data_ptr(), self.derived.data_ptr(),
+                            self.status.data_ptr())
+
+    def stream_bytes(self, T: int) -> int:
+        return spectra_stream_bytes(self.max_rec_bits, T)
+
+    def new_streams(self, T: int, n: int | None = None) -> torch.Tensor:
+        """uint8 [n, stream_bytes] (n defaults to heads), zero-filled."""
+        n = self.heads if n is None else n
+        return torch.zeros((n, max(self.stream_bytes(T), 16)), dtype=torch.uint8,
+                           device=self.bits.device)
+
+
+# ----------------------------------------------------------------- C ABI
+def spectra_version() -> int:
+    return lib().spectra_version()
+
+
+def spectra_status_string(st: int) -> str:
+    return lib().spectra_status_string(st).decode()
+
+
+def spectra_plan_derived_bytes(heads: int, head_dim: int) -> int:
+    return lib().spectra_plan_derived_bytes(heads, head_dim)
+
+
+def spectra_stream_bytes(rec_bits: int, T: int) -> int:
+    return lib().spectra_stream_bytes(rec_bits, T)
+
+
+def spectra_calibrate_workspace_bytes(heads: int, head_dim: int, n_cal: int) -> int:
+    return lib().spectra_calibrate_workspace_bytes(heads, head_dim, n_cal)
+
+
+def spectra_attn_workspace_bytes(B: int, Hq: int, head_dim: int, ctx: int) -> int:
+    return lib().spectra_attn_workspace_bytes(B, Hq, head_dim, ctx)
+
+
+def spectra_calibrate(plan: Plan, x: torch.Tensor, n_cal: int | None = None, max_sweeps: int = 30,
+                      workspace: torch.Tensor | None = None, gram_out: torch.Tensor | None = None,
+                      stream=None):
+    """x: [T, H, d] bf16/f32 cuda tensor (token stride = x.stride(0))."""
+    n_cal = x.shape[0] if n_cal is None else n_cal
+    need = spectra_calibrate_workspace_bytes(plan.heads, plan.head_dim, n_cal)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=x.device)
+    p = plan.c()
+    st = lib().spectra_calibrate(C.byref(p), _ptr(x), _dt(x), n_cal, x.stride(0), max_sweeps,
+                                 _ptr(workspace), workspace.numel(), _ptr(gram_out), _stream(stream))
+    _check(st, "spectra_calibrate")
+
+
+def spectra_alloc_bits(plan: Plan, avg_bits: float, fixed_bits: int = 0, stream=None):
+    p = plan.c()
+    st = lib().spectra_alloc_bits(C.byref(p), float(avg_bits), int(fixed_bits), _stream(stream))
+    _check(st, "spectra_alloc_bits")
+    plan.max_rec_bits = p.max_rec_bits
+
+
+def spectra_plan_finalize(plan: Plan, stream=None):
+    p = plan.c()
+    _check(lib().spectra_plan_finalize(C.byref(p), _stream(stream)), "spectra_plan_finalize")
+
+
+def spectra_encode(plan: Plan, x: torch.Tensor, codes: torch.Tensor, norms: torch.Tensor | None = None,
+                   T: int | None = None, stream=None):
+    """x: [T, H, d]; codes: uint8 [H, stride]; norms (RWHT): f32 [H, >=T]."""
+    T = x.shape[0] if T is None else T
+    p = plan.c()
+    st = lib().spectra_encode(C.byref(p), _ptr(x), _dt(x), T, x.stride(0), _ptr(codes),
+                              codes.stride(0) if codes.dim() > 1 else 0, _ptr(norms),
+                              norms.stride(0) if norms is not None and norms.dim() > 1 else 0,
+                              _stream(stream))
+    _check(st, "spectra_encode")
+
+
+def spectra_decode(plan: Plan, codes: torch.Tensor, T: int, out: torch.Tensor,
+                   norms: torch.Tensor | None = None, stream=None):
+    """codes: uint8 [H, stride]; out: [T, H, d] bf16/f32."""
+    p = plan.c()
+    st = lib().spectra_decode(C.byref(p), _ptr(codes), codes.stride(0) if codes.dim() > 1 else 0,
+                              _ptr(norms), norms.stride(0) if norms is not None and norms.dim() > 1 else 0,
+                              T, _ptr(out), _dt(out), out.stride(0), _stream(stream))
+    _check(st, "spectra_decode")
+
+
+def spectra_attn_decode(kplan: Plan, vplan: Plan, q: torch.Tensor, k_codes: torch.Tensor,
+                        v_codes: torch.Tensor, ctx: int, softmax_scale: float, out: torch.Tensor,
+                        workspace: torch.Tensor | None = None, k_norms: torch.Tensor | None = None,
+                        v_norms: torch.Tensor | None = None, stream=None):
+    """q: [B, Hq, d]; k_codes/v_codes: uint8 [B*Hkv, stride]; out: f32 [B, Hq, d]."""
+    B, Hq, d = q.shape
+    if workspace is None:
+        workspace = torch.empty((max(spectra_attn_workspace_bytes(B, Hq, d, ctx), 16) + 256,),
+                                dtype=torch.uint8, device=q.device)
+    off = (-workspace.data_ptr()) % 256
+    ws = workspace[off:]
+    kp, vp = kplan.c(), vplan.c()
+    nstride = k_norms.stride(0) if k_norms is not None else 0
+    st = lib().spectra_attn_decode(C.byref(kp), C.byref(vp), _ptr(q), _dt(q), B, Hq, _ptr(k_codes),
+                                   _ptr(v_codes), k_codes.stride(0), _ptr(k_norms), _ptr(v_norms),
+                                   nstride, ctx, float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(),
+                                   _stream(stream))
+    _check(st, "spectra_attn_decode")

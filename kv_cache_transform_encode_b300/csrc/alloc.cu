@@ -1,0 +1,241 @@
+// alloc.cu -- integer reverse water-filling, plan finalization and the
+// Gaussian Lloyd-Max tables.
+//
+// "Sintesi Tecnica: SPECTRA", "La Pipeline di SPECTRA" phase 2: reverse
+// water-filling on the measured marginal variances -- more bits to
+// high-variance latent coordinates, fewer (down to zero) to the rest;
+// "Metodologia" item 2: zero-bit channels are dropped.
+//
+// The greedy rule (R_tot one-bit steps, each to the channel with the largest
+// lam_c * 4^-b_c, lowest index on ties) picks, in order, the R_tot largest
+// keys of the multiset {lam_c 4^-k : c < d, 0 <= k < 8}: every channel's keys
+// fall with k, so a channel's chosen keys are a prefix.  alloc_kernel selects
+// those keys directly: one thread per key (thread c*8+k), a bisection on the
+// fp64 bit pattern of the R_tot-th largest key (64 block-wide counts), then
+// ties at that value broken in thread order, which is (c asc, k asc) -- the
+// greedy's tie order.  Keys are exact powers-of-two scalings of fp32
+// eigenvalues, so the result is bit-identical to the sequential greedy.
+#include "spectra_internal.cuh"
+
+#include <math.h>
+
+namespace spectra {
+
+namespace {
+
+template <int D>
+__global__ void __launch_bounds__(D * 8)
+alloc_kernel(const float* __restrict__ eig, int R, int fixed_bits, uint8_t* __restrict__ bits_out)
+{
+    __shared__ int warp_tot[32];
+    const int h = blockIdx.x, tid = threadIdx.x;
+    const int c = tid >> 3, k = tid & 7;
+    const int lane = tid & 31, warp = tid >> 5;
+    uint8_t* bo = bits_out + size_t(h) * D;
+    if (fixed_bits > 0) {
+        if (k == 0) bo[c] = uint8_t(fixed_bits);
+        return;
+    }
+    float lf = eig[size_t(h) * D + c];
+    lf = (lf > 0.f) ? lf : 0.f;     // negative or NaN -> 0
+    const double key = ldexp(double(lf), -2 * k);
+    const unsigned long long kb = static_cast<unsigned long long>(__double_as_longlong(key));
+
+    bool sel = false;
+    if (R > 0) {
+        // smallest u with #{keys > u} < R  ==  the R-th largest key
+        unsigned long long lo = 0ull, hi = 0x7FF0000000000000ull;
+        while (lo < hi) {
+            const unsigned long long mid = lo + ((hi - lo) >> 1);
+            const int gt = __syncthreads_count(kb > mid);
+            if (gt < R) hi = mid; else lo = mid + 1;
+        }
+        const bool gt = kb > lo, eq = kb == lo;
+        const int n_gt = __syncthreads_count(gt);
+        const int need = R - n_gt;
+        // rank of this key among equal keys, in thread order
+        const unsigned m = __ballot_sync(0xffffffffu, eq);
+        if (lane == 0) warp_tot[warp] = __popc(m);
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += warp_tot[w];
+        before += __popc(m & ((1u << lane) - 1u));
+        sel = gt || (eq && before < need);
+    }
+    const unsigned sm = __ballot_sync(0xffffffffu, sel);
+    if (k == 0) bo[c] = uint8_t(__popc((sm >> (lane & ~7)) & 0xFFu));
+}
+
+// Per-head offsets, record size and quantizer scales.
+template <int D>
+__global__ void __launch_bounds__(D)
+finalize_kernel(int basis, int quant, int max_rec_bits, const float* __restrict__ eig,
+                const uint8_t* __restrict__ bits, int32_t* __restrict__ rec_bits,
+                uint16_t* __restrict__ chan_off, float* __restrict__ qscale,
+                float* __restrict__ rscale, int32_t* __restrict__ status)
+{
+    __shared__ int wsum[D / 32];
+    const int h = blockIdx.x, c = threadIdx.x, lane = c & 31, warp = c >> 5;
+    const int b = bits[size_t(h) * D + c];
+    int incl = b;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int base = 0, total = 0;
+    for (int w = 0; w < D / 32; ++w) {
+        if (w < warp) base += wsum[w];
+        total += wsum[w];
+    }
+    chan_off[size_t(h) * D + c] = uint16_t(base + incl - b);
+    float qs = 1.f, rs = 1.f;
+    if (basis == SPECTRA_BASIS_EIGEN && b > 0) {
+        float lam = eig[size_t(h) * D + c];
+        lam = (lam > 0.f) ? lam : 0.f;
+        const float sig = sqrtf(lam);
+        if (quant == SPECTRA_Q_UNIFORM3S) {
+            const float levels = float(1 << b);
+            qs = (sig > 0.f) ? levels / (6.f * sig) : 0.f;
+            rs = 6.f * sig / levels;
+        } else {
+            qs = (sig > 0.f) ? 1.f / sig : 0.f;
+            rs = sig;
+        }
+    }
+    qscale[size_t(h) * D + c] = qs;
+    rscale[size_t(h) * D + c] = rs;
+    if (c == 0) {
+        rec_bits[h] = total;
+        if (total > max_rec_bits || b > 8) status[h] = -SPECTRA_ERR_BUFFER;
+    }
+}
+
+// Gaussian Lloyd-Max codebooks for widths 1..8 (one warp per width).
+// The optimal levels of N(0,1) satisfy l_k = E[X | t_k < X < t_{k+1}] with
+// t the midpoints of adjacent levels (the Lloyd-Max conditions).  Solved by
+// Newton's method on F_k = l_k P_k - M_k (P_k the cell mass, M_k the cell's
+// first moment), whose Jacobian is tridiagonal; by symmetry only the L/2
+// positive levels are unknowns.  Start: Panter-Dite companding points
+// sqrt(3) * Phi^-1((j + 1/2) / L).
+constexpr int kHalfMax = 128;
+
+__global__ void __launch_bounds__(256)
+lm_tables_kernel(float* __restrict__ levels, float* __restrict__ thresh)
+{
+    __shared__ double a_s[8][kHalfMax], f_s[8][kHalfMax], dg_s[8][kHalfMax],
+        lo_s[8][kHalfMax], up_s[8][kHalfMax];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = w + 1, L = 1 << b, H = L >> 1;
+    double* a = a_s[w];
+    const double inv_sqrt2 = 0.70710678118654752440;
+    const double inv_sqrt2pi = 0.39894228040143267794;
+    for (int k = lane; k < H; k += 32)
+        a[k] = sqrt(3.0) * normcdfinv((H + k + 0.5) / double(L));
+    __syncwarp();
+    for (int it = 0; it < 80; ++it) {
+        for (int k = lane; k < H; k += 32) {
+            const double ak = a[k];
+            const double tk = (k == 0) ? 0.0 : 0.5 * (a[k - 1] + ak);
+            const bool last = (k == H - 1);
+            const double tk1 = last ? 0.0 : 0.5 * (ak + a[k + 1]);
+            const double Qk = 0.5 * erfc(tk * inv_sqrt2);
+            const double Qk1 = last ? 0.0 : 0.5 * erfc(tk1 * inv_sqrt2);
+            const double phk = inv_sqrt2pi * exp(-0.5 * tk * tk);
+            const double phk1 = last ? 0.0 : inv_sqrt2pi * exp(-0.5 * tk1 * tk1);
+            const double P = Qk - Qk1, M = phk - phk1;
+            const double low = (k >= 1) ? 0.5 * (tk - ak) * phk : 0.0;
+            const double upp = last ? 0.0 : 0.5 * (ak - tk1) * phk1;
+            f_s[w][k] = ak * P - M;
+            lo_s[w][k] = low;
+            up_s[w][k] = upp;
+            dg_s[w][k] = P + low + upp;
+        }
+        __syncwarp();
+        double maxd = 0.0;
+        if (lane == 0) {
+            // Thomas solve J delta = -F (in place: up <- c', f <- d')
+            double* dg = dg_s[w]; double* lo = lo_s[w]; double* up = up_s[w]; double* f = f_s[w];
+            double m = dg[0];
+            up[0] /= m;
+            f[0] = -f[0] / m;
+            for (int k = 1; k < H; ++k) {
+                m = dg[k] - lo[k] * up[k - 1];
+                up[k] /= m;
+                f[k] = (-f[k] - lo[k] * f[k - 1]) / m;
+            }
+            for (int k = H - 2; k >= 0; --k) f[k] -= up[k] * f[k + 1];
+            // damped step keeping 0 < a_0 < a_1 < ...
+            double lam = 1.0;
+            for (int tries = 0; tries < 40; ++tries) {
+                bool ok = (a[0] + lam * f[0]) > 0.0;
+                for (int k = 1; k < H && ok; ++k)
+                    ok = (a[k] + lam * f[k]) > (a[k - 1] + lam * f[k - 1]);
+                if (ok) break;
+                lam *= 0.5;
+            }
+            for (int k = 0; k < H; ++k) {
+                const double st = lam * f[k];
+                a[k] += st;
+                maxd = fmax(maxd, fabs(st));
+            }
+        }
+        maxd = __shfl_sync(0xffffffffu, maxd, 0);
+        __syncwarp();
+        if (maxd < 1e-15) break;
+    }
+    float* lv = levels + (b - 1) * kLmStride;
+    float* th = thresh + (b - 1) * kLmStride;
+    for (int k = lane; k < H; k += 32) {
+        lv[H + k] = float(a[k]);
+        lv[H - 1 - k] = float(-a[k]);
+    }
+    for (int j = lane; j < L; j += 32) {
+        double t;
+        if (j == 0) { th[0] = -INFINITY; continue; }
+        if (j == H) t = 0.0;
+        else if (j > H) t = 0.5 * (a[j - H - 1] + a[j - H]);
+        else t = -0.5 * (a[L - j - H - 1] + a[L - j - H]);
+        th[j] = float(t);
+    }
+}
+
+}  // namespace
+
+spectra_status launch_alloc(const spectra_plan* plan, int R_tot, int fixed_bits, cudaStream_t s)
+{
+    if (plan->head_dim == 128)
+        alloc_kernel<128><<<plan->heads, 128 * 8, 0, s>>>(plan->eigvals, R_tot, fixed_bits, plan->bits);
+    else
+        alloc_kernel<64><<<plan->heads, 64 * 8, 0, s>>>(plan->eigvals, R_tot, fixed_bits, plan->bits);
+    return cuda_status(cudaGetLastError());
+}
+
+spectra_status launch_tc_images(const spectra_plan* plan, cudaStream_t s);   // codec_tc.cu
+
+spectra_status launch_finalize(const spectra_plan* plan, cudaStream_t s)
+{
+    const PlanView v = make_view(plan);
+    uint16_t* co = const_cast<uint16_t*>(v.chan_off);
+    float* qs = const_cast<float*>(v.qscale);
+    float* rs = const_cast<float*>(v.rscale);
+    if (plan->head_dim == 128)
+        finalize_kernel<128><<<plan->heads, 128, 0, s>>>(plan->basis, plan->quant, plan->max_rec_bits,
+                                                         plan->eigvals, plan->bits, plan->rec_bits, co,
+                                                         qs, rs, plan->status);
+    else
+        finalize_kernel<64><<<plan->heads, 64, 0, s>>>(plan->basis, plan->quant, plan->max_rec_bits,
+                                                       plan->eigvals, plan->bits, plan->rec_bits, co,
+                                                       qs, rs, plan->status);
+    spectra_status st = cuda_status(cudaGetLastError());
+    if (st != SPECTRA_OK) return st;
+    if (plan->quant == SPECTRA_Q_LLOYD_GAUSS) {
+        lm_tables_kernel<<<1, 256, 0, s>>>(const_cast<float*>(v.lm_level), const_cast<float*>(v.lm_thresh));
+        st = cuda_status(cudaGetLastError());
+        if (st != SPECTRA_OK) return st;
+    }
+    return launch_tc_images(plan, s);
+}
+
+}  // namespace spectra

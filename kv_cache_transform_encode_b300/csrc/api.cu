@@ -1,0 +1,245 @@
+// api.cu -- the exported C ABI (include/spectra.h): argument validation on
+// the host, then launches on the caller's stream.  Nothing here allocates
+// device memory or synchronises.
+#include "spectra_internal.cuh"
+
+#include <math.h>
+
+using namespace spectra;
+
+namespace spectra {
+spectra_status launch_encode_generic(const spectra_plan*, const void*, int, int64_t, int64_t,
+                                     uint8_t*, int64_t, float*, int64_t, cudaStream_t);
+spectra_status launch_decode_generic(const spectra_plan*, const uint8_t*, int64_t, const float*,
+                                     int64_t, int64_t, void*, int, int64_t, cudaStream_t);
+spectra_status launch_encode_tc(const spectra_plan*, const void*, int, int64_t, int64_t,
+                                uint8_t*, int64_t, float*, int64_t, cudaStream_t, bool*);
+spectra_status launch_decode_tc(const spectra_plan*, const uint8_t*, int64_t, const float*,
+                                int64_t, int64_t, void*, int, int64_t, cudaStream_t, bool*);
+}  // namespace spectra
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_size(int dt) { return dt == SPECTRA_BF16 ? 2 : 4; }
+
+bool valid_dtype(int dt) { return dt == SPECTRA_BF16 || dt == SPECTRA_F32; }
+
+spectra_status check_plan(const spectra_plan* p, bool need_tables)
+{
+    if (!p) return SPECTRA_ERR_INVALID_ARG;
+    if (p->heads <= 0 || p->heads > (1 << 20)) return SPECTRA_ERR_INVALID_ARG;
+    if (p->head_dim != 64 && p->head_dim != 128) return SPECTRA_ERR_UNSUPPORTED;
+    if (p->basis != SPECTRA_BASIS_EIGEN && p->basis != SPECTRA_BASIS_RWHT) return SPECTRA_ERR_INVALID_ARG;
+    if (p->quant != SPECTRA_Q_UNIFORM3S && p->quant != SPECTRA_Q_LLOYD_GAUSS) return SPECTRA_ERR_INVALID_ARG;
+    if (p->basis == SPECTRA_BASIS_RWHT && p->quant != SPECTRA_Q_LLOYD_GAUSS) return SPECTRA_ERR_UNSUPPORTED;
+    if (p->basis == SPECTRA_BASIS_EIGEN && (!p->basis_mat || !p->eigvals)) return SPECTRA_ERR_INVALID_ARG;
+    if (p->basis == SPECTRA_BASIS_RWHT && !p->signs) return SPECTRA_ERR_INVALID_ARG;
+    if (!p->bits || !p->rec_bits || !p->status) return SPECTRA_ERR_INVALID_ARG;
+    if (need_tables) {
+        if (!p->derived || (reinterpret_cast<uintptr_t>(p->derived) & 255u)) return SPECTRA_ERR_INVALID_ARG;
+        if (p->max_rec_bits < 0 || p->max_rec_bits > 8 * p->head_dim) return SPECTRA_ERR_INVALID_ARG;
+    }
+    return SPECTRA_OK;
+}
+
+spectra_status check_cache(const void* x, int dt, int64_t T, int64_t tstride, int heads, int d)
+{
+    if (!valid_dtype(dt)) return SPECTRA_ERR_INVALID_ARG;
+    if (T < 0) return SPECTRA_ERR_INVALID_ARG;
+    if (T == 0) return SPECTRA_OK;
+    if (!x || !aligned16(x)) return SPECTRA_ERR_INVALID_ARG;
+    if (tstride < int64_t(heads) * d) return SPECTRA_ERR_INVALID_ARG;
+    if ((tstride * elem_size(dt)) % 16 != 0) return SPECTRA_ERR_INVALID_ARG;
+    return SPECTRA_OK;
+}
+
+spectra_status check_streams(const spectra_plan* p, const uint8_t* codes, int64_t sstride, int64_t T,
+                             int64_t nstreams)
+{
+    const int64_t need = stream_bytes(p->max_rec_bits, T);
+    if (need == 0) return SPECTRA_OK;
+    if (!codes || !aligned16(codes)) return SPECTRA_ERR_INVALID_ARG;
+    if (nstreams > 1 && (sstride < need || sstride % 16 != 0)) return SPECTRA_ERR_INVALID_ARG;
+    if (nstreams == 1 && sstride != 0 && sstride < need) return SPECTRA_ERR_INVALID_ARG;
+    return SPECTRA_OK;
+}
+
+bool force_generic()
+{
+    static const int v = [] {
+        const char* e = getenv("SPECTRA_FORCE_GENERIC");
+        return (e && e[0] == '1') ? 1 : 0;
+    }();
+    return v != 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spectra_version(void) { return 100; }
+
+const char* spectra_status_string(spectra_status st)
+{
+    switch (st) {
+    case SPECTRA_OK: return "ok";
+    case SPECTRA_ERR_INVALID_ARG: return "invalid argument";
+    case SPECTRA_ERR_UNSUPPORTED: return "unsupported";
+    case SPECTRA_ERR_CUDA: return "CUDA error";
+    case SPECTRA_ERR_NOT_CONVERGED: return "eigensolve not converged";
+    case SPECTRA_ERR_TIMEOUT: return "bounded wait timed out";
+    case SPECTRA_ERR_NONFINITE: return "non-finite input";
+    case SPECTRA_ERR_BUFFER: return "stream buffer too small";
+    }
+    return "unknown status";
+}
+
+size_t spectra_plan_derived_bytes(int heads, int head_dim)
+{
+    if (heads <= 0 || (head_dim != 64 && head_dim != 128)) return 0;
+    return derived_layout(heads, head_dim).total;
+}
+
+size_t spectra_stream_bytes(int32_t rec_bits, int64_t T) { return size_t(stream_bytes(rec_bits, T)); }
+
+size_t spectra_calibrate_workspace_bytes(int heads, int head_dim, int64_t n_cal)
+{
+    if (heads <= 0 || n_cal <= 0 || (head_dim != 64 && head_dim != 128)) return 0;
+    return sizeof(float) * size_t(heads) * gram_chunks(heads, n_cal) * head_dim * head_dim;
+}
+
+spectra_status spectra_calibrate(spectra_plan* plan, const void* x, spectra_dtype dt, int64_t n_cal,
+                                 int64_t token_stride, int max_sweeps, void* workspace,
+                                 size_t workspace_bytes, float* gram_out, spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, false);
+    if (st) return st;
+    if (plan->basis != SPECTRA_BASIS_EIGEN) return SPECTRA_ERR_INVALID_ARG;
+    if (n_cal <= 0 || max_sweeps < 1 || max_sweeps > 100) return SPECTRA_ERR_INVALID_ARG;
+    if ((st = check_cache(x, dt, n_cal, token_stride, plan->heads, plan->head_dim))) return st;
+    const size_t need = spectra_calibrate_workspace_bytes(plan->heads, plan->head_dim, n_cal);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SPECTRA_ERR_INVALID_ARG;
+    const int nch = gram_chunks(plan->heads, n_cal);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = launch_gram(plan, x, dt, n_cal, token_stride, static_cast<float*>(workspace), nch, s)))
+        return st;
+    return launch_jacobi(plan, static_cast<float*>(workspace), nch, n_cal, max_sweeps, gram_out, s);
+}
+
+spectra_status spectra_plan_finalize(spectra_plan* plan, spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, true);
+    if (st) return st;
+    return launch_finalize(plan, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spectra_status spectra_alloc_bits(spectra_plan* plan, double avg_bits, int fixed_bits,
+                                  spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, false);
+    if (st) return st;
+    if (!plan->derived || (reinterpret_cast<uintptr_t>(plan->derived) & 255u)) return SPECTRA_ERR_INVALID_ARG;
+    const int d = plan->head_dim;
+    int R;
+    if (fixed_bits != 0) {
+        if (fixed_bits < 1 || fixed_bits > 8) return SPECTRA_ERR_INVALID_ARG;
+        R = fixed_bits * d;
+    } else {
+        if (!(avg_bits >= 0.0) || !isfinite(avg_bits)) return SPECTRA_ERR_INVALID_ARG;
+        if (plan->basis != SPECTRA_BASIS_EIGEN) return SPECTRA_ERR_INVALID_ARG;
+        const double r = floor(avg_bits * d + 1e-9);
+        R = int(r < 8.0 * d ? r : 8.0 * d);
+    }
+    plan->max_rec_bits = R;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = launch_alloc(plan, R, fixed_bits, s))) return st;
+    return launch_finalize(plan, s);
+}
+
+spectra_status spectra_encode(const spectra_plan* plan, const void* x, spectra_dtype dt, int64_t T,
+                              int64_t token_stride, uint8_t* codes, int64_t stream_stride_bytes,
+                              float* norms, int64_t norms_stride, spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, true);
+    if (st) return st;
+    if ((st = check_cache(x, dt, T, token_stride, plan->heads, plan->head_dim))) return st;
+    if ((st = check_streams(plan, codes, stream_stride_bytes, T, plan->heads))) return st;
+    if (plan->basis == SPECTRA_BASIS_RWHT && T > 0) {
+        if (!norms || (plan->heads > 1 && norms_stride < T)) return SPECTRA_ERR_INVALID_ARG;
+    }
+    if (T == 0 || plan->max_rec_bits == 0) {
+        if (plan->basis != SPECTRA_BASIS_RWHT || T == 0) return SPECTRA_OK;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!force_generic()) {
+        bool done = false;
+        st = launch_encode_tc(plan, x, dt, T, token_stride, codes, stream_stride_bytes, norms,
+                              norms_stride, s, &done);
+        if (st || done) return st;
+    }
+    return launch_encode_generic(plan, x, dt, T, token_stride, codes, stream_stride_bytes, norms,
+                                 norms_stride, s);
+}
+
+spectra_status spectra_decode(const spectra_plan* plan, const uint8_t* codes, int64_t stream_stride_bytes,
+                              const float* norms, int64_t norms_stride, int64_t T, void* x_out,
+                              spectra_dtype out_dt, int64_t token_stride, spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, true);
+    if (st) return st;
+    if ((st = check_cache(x_out, out_dt, T, token_stride, plan->heads, plan->head_dim))) return st;
+    if ((st = check_streams(plan, codes, stream_stride_bytes, T, plan->heads))) return st;
+    if (plan->basis == SPECTRA_BASIS_RWHT && T > 0) {
+        if (!norms || (plan->heads > 1 && norms_stride < T)) return SPECTRA_ERR_INVALID_ARG;
+    }
+    if (T == 0) return SPECTRA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!force_generic()) {
+        bool done = false;
+        st = launch_decode_tc(plan, codes, stream_stride_bytes, norms, norms_stride, T, x_out, out_dt,
+                              token_stride, s, &done);
+        if (st || done) return st;
+    }
+    return launch_decode_generic(plan, codes, stream_stride_bytes, norms, norms_stride, T, x_out,
+                                 out_dt, token_stride, s);
+}
+
+size_t spectra_attn_workspace_bytes(int B, int Hq, int head_dim, int64_t ctx)
+{
+    if (B <= 0 || Hq <= 0 || ctx < 0 || (head_dim != 64 && head_dim != 128)) return 0;
+    return attn_workspace_bytes(B, Hq, head_dim, ctx);
+}
+
+spectra_status spectra_attn_decode(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
+                                   spectra_dtype q_dt, int B, int Hq, const uint8_t* k_codes,
+                                   const uint8_t* v_codes, int64_t stream_stride_bytes,
+                                   const float* k_norms, const float* v_norms, int64_t norms_stride,
+                                   int64_t ctx, float softmax_scale, float* out, void* workspace,
+                                   size_t workspace_bytes, spectra_stream_t stream)
+{
+    spectra_status st;
+    if ((st = check_plan(kplan, true))) return st;
+    if ((st = check_plan(vplan, true))) return st;
+    if (kplan->heads != vplan->heads || kplan->head_dim != vplan->head_dim) return SPECTRA_ERR_INVALID_ARG;
+    const int Hkv = kplan->heads, d = kplan->head_dim;
+    if (B <= 0 || Hq <= 0 || Hq % Hkv != 0 || ctx < 0) return SPECTRA_ERR_INVALID_ARG;
+    if (!q || !out || !valid_dtype(q_dt) || !isfinite(softmax_scale)) return SPECTRA_ERR_INVALID_ARG;
+    if ((st = check_streams(kplan, k_codes, stream_stride_bytes, ctx, int64_t(B) * Hkv))) return st;
+    if ((st = check_streams(vplan, v_codes, stream_stride_bytes, ctx, int64_t(B) * Hkv))) return st;
+    if (kplan->basis == SPECTRA_BASIS_RWHT && ctx > 0 && (!k_norms || norms_stride < ctx))
+        return SPECTRA_ERR_INVALID_ARG;
+    if (vplan->basis == SPECTRA_BASIS_RWHT && ctx > 0 && (!v_norms || norms_stride < ctx))
+        return SPECTRA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (ctx == 0)
+        return cuda_status(cudaMemsetAsync(out, 0, sizeof(float) * size_t(B) * Hq * d, s));
+    const size_t need = attn_workspace_bytes(B, Hq, d, ctx);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return SPECTRA_ERR_INVALID_ARG;
+    return launch_attn(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes, k_norms,
+                       v_norms, norms_stride, ctx, softmax_scale, out, workspace, workspace_bytes, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,295 @@
+// attn.cu -- decode-step attention read straight from packed K/V streams,
+// computed in the latent bases (CUDA-core path; any plan kind).
+//
+// "Sintesi Tecnica: SPECTRA", "Significato e Rivendicazioni": the latent
+// space opens the way to attention computed directly in it.  With
+// khat = B_K yk and vhat = B_V yv (the decode reconstructions),
+//   <q, khat_t> = <B_K^T q, yk_t>   and   sum_t p_t vhat_t = B_V sum_t p_t yv_t,
+// so scores use the rotated query qt = scale * B_K^T q against the latent
+// K coordinates, the softmax-weighted sum runs over latent V coordinates,
+// and one rotation by B_V at the end gives the output.
+//
+// Three launches: (1) qt for every (b, query head); (2) one block per
+// (context split, kv head, batch) -- online softmax over tiles of 64 tokens
+// for the Hq/Hkv query heads that share the kv head, partial (m, l, acc)
+// to the workspace; (3) per (b, query head) merge the splits and rotate back.
+#include "spectra_internal.cuh"
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+namespace spectra {
+
+namespace {
+
+constexpr int kSplitLen = 2048;     // tokens per context split
+constexpr int kTile = 64;           // tokens per tile (two bit-plane groups)
+constexpr int kThreads = 256;
+constexpr int kMaxGroup = 8;        // query heads per kv head
+
+__device__ __forceinline__ float basis_entry(const PlanView& pv, int h, int i, int c, int D)
+{
+    if (pv.basis == SPECTRA_BASIS_EIGEN) return pv.basis_mat[(size_t(h) * D + i) * D + c];
+    return float(pv.signs[size_t(h) * D + i] * hadamard_sign(i, c)) * rsqrtf(float(D));
+}
+
+__global__ void attn_qrot_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, int Hkv,
+                                 float scale, float* __restrict__ qt)
+{
+    const int D = kp.d;
+    const int bj = blockIdx.x, j = bj % Hq;
+    const int h = j / (Hq / Hkv);
+    extern __shared__ float qs[];
+    for (int i = threadIdx.x; i < D; i += blockDim.x) qs[i] = load_elem(q, q_dt, int64_t(bj) * D + i);
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        float a = 0.f;
+        for (int i = 0; i < D; ++i) a = fmaf(basis_entry(kp, h, i, c, D), qs[i], a);
+        qt[int64_t(bj) * D + c] = scale * a;
+    }
+}
+
+struct Side {            // per-plan tables staged in shared memory
+    int* bits;
+    int* off;
+    float* rsc;
+    uint32_t* words;     // [2][R]
+};
+
+template <int D>
+__device__ void unpack_tile(const PlanView& pv, const Side& sd, int h, int R, const uint32_t* stream,
+                            const float* norms, int64_t t0, int64_t tend, float* y, const float* lv)
+{
+    constexpr int LD = D + 1;
+    // stage the two groups' words
+    const int64_t g0 = t0 / kGroup;
+    for (int e = threadIdx.x; e < 2 * R; e += blockDim.x) {
+        const int64_t gg = g0 + e / R;
+        sd.words[e] = (gg * kGroup < tend) ? stream[gg * R + (e % R)] : 0u;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kTile * D; e += blockDim.x) {
+        const int t = e / D, c = e % D;
+        const int b = sd.bits[c];
+        float v = 0.f;
+        if (b > 0 && t0 + t < tend) {
+            const uint32_t* w = sd.words + (t >> 5) * R + sd.off[c];
+            int code = 0;
+            for (int k = 0; k < b; ++k) code |= int((w[k] >> (t & 31)) & 1u) << k;
+            if (pv.quant == SPECTRA_Q_UNIFORM3S)
+                v = sd.rsc[c] * (float(code) + 0.5f - float(1 << (b - 1)));
+            else {
+                const float s = (pv.basis == SPECTRA_BASIS_RWHT)
+                                    ? norms[t0 + t] * rsqrtf(float(D)) : sd.rsc[c];
+                v = s * lv[(b - 1) * kLmStride + code];
+            }
+        }
+        y[t * LD + c] = v;
+    }
+    __syncthreads();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq, int64_t ctx,
+                  const uint8_t* __restrict__ kc, const uint8_t* __restrict__ vc, int64_t sstride,
+                  const float* __restrict__ kn, const float* __restrict__ vn, int64_t nstride,
+                  int nsplit, float* __restrict__ part)
+{
+    constexpr int LD = D + 1;
+    extern __shared__ float smem[];
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int Hkv = kp.heads, G = Hq / Hkv;
+    const int RK = kp.rec_bits[h], RV = vp.rec_bits[h];
+
+    float* qs = smem;                       // [G][D]
+    float* yk = qs + kMaxGroup * D;         // [kTile][LD]
+    float* yv = yk + kTile * LD;            // [kTile][LD]
+    float* S = yv + kTile * LD;             // [G][kTile]
+    float* mrow = S + kMaxGroup * kTile;    // [G]
+    float* lrow = mrow + kMaxGroup;         // [G]
+    float* alpha = lrow + kMaxGroup;        // [G]
+    float* lvK = alpha + kMaxGroup;         // [8][256]
+    float* lvV = lvK + kMaxBits * kLmStride;
+    Side sk, sv;
+    sk.rsc = lvV + kMaxBits * kLmStride;
+    sv.rsc = sk.rsc + D;
+    sk.bits = reinterpret_cast<int*>(sv.rsc + D);
+    sv.bits = sk.bits + D;
+    sk.off = sv.bits + D;
+    sv.off = sk.off + D;
+    sk.words = reinterpret_cast<uint32_t*>(sv.off + D);
+    sv.words = sk.words + 2 * 8 * D;
+
+    for (int e = threadIdx.x; e < G * D; e += blockDim.x)
+        qs[e] = qt[(int64_t(b) * Hq + h * G) * D + e];
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        sk.bits[c] = kp.bits[size_t(h) * D + c];
+        sv.bits[c] = vp.bits[size_t(h) * D + c];
+        sk.off[c] = kp.chan_off[size_t(h) * D + c];
+        sv.off[c] = vp.chan_off[size_t(h) * D + c];
+        sk.rsc[c] = kp.rscale[size_t(h) * D + c];
+        sv.rsc[c] = vp.rscale[size_t(h) * D + c];
+    }
+    for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) {
+        lvK[e] = kp.lm_level[e];
+        lvV[e] = vp.lm_level[e];
+    }
+    if (threadIdx.x < kMaxGroup) { mrow[threadIdx.x] = -INFINITY; lrow[threadIdx.x] = 0.f; }
+
+    const int64_t sid = int64_t(b) * Hkv + h;
+    const uint32_t* ks = reinterpret_cast<const uint32_t*>(kc + sid * sstride);
+    const uint32_t* vs = reinterpret_cast<const uint32_t*>(vc + sid * sstride);
+    const float* knr = kn ? kn + sid * nstride : nullptr;
+    const float* vnr = vn ? vn + sid * nstride : nullptr;
+    const int64_t s0 = int64_t(split) * kSplitLen;
+    const int64_t s1 = min(ctx, s0 + kSplitLen);
+
+    // each thread owns outputs (j, c) for e = tid + k*blockDim
+    constexpr int kOwn = kMaxGroup * D / kThreads;
+    float acc[kOwn];
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k) acc[k] = 0.f;
+    __syncthreads();
+
+    for (int64_t t0 = s0; t0 < s1; t0 += kTile) {
+        unpack_tile<D>(kp, sk, h, RK, ks, knr, t0, s1, yk, lvK);
+        for (int e = threadIdx.x; e < G * kTile; e += blockDim.x) {
+            const int j = e / kTile, t = e % kTile;
+            float a = 0.f;
+            for (int c = 0; c < D; ++c) a = fmaf(qs[j * D + c], yk[t * LD + c], a);
+            S[j * kTile + t] = (t0 + t < s1) ? a : -INFINITY;
+        }
+        __syncthreads();
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (warp < G) {
+            float mx = fmaxf(S[warp * kTile + lane], S[warp * kTile + lane + 32]);
+            for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float mold = mrow[warp];
+            const float mnew = fmaxf(mold, mx);
+            const float p0 = __expf(S[warp * kTile + lane] - mnew);
+            const float p1 = __expf(S[warp * kTile + lane + 32] - mnew);
+            S[warp * kTile + lane] = p0;
+            S[warp * kTile + lane + 32] = p1;
+            float ps = p0 + p1;
+            for (int o = 16; o; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+            if (lane == 0) {
+                const float al = (mold == -INFINITY) ? 0.f : __expf(mold - mnew);
+                alpha[warp] = al;
+                lrow[warp] = lrow[warp] * al + ps;
+                mrow[warp] = mnew;
+            }
+        }
+        unpack_tile<D>(vp, sv, h, RV, vs, vnr, t0, s1, yv, lvV);   // syncs inside
+#pragma unroll
+        for (int k = 0; k < kOwn; ++k) {
+            const int e = threadIdx.x + k * kThreads;
+            const int j = e / D, c = e % D;
+            if (j < G) {
+                float a = acc[k] * alpha[j];
+                for (int t = 0; t < kTile; ++t) a = fmaf(S[j * kTile + t], yv[t * LD + c], a);
+                acc[k] = a;
+            }
+        }
+        __syncthreads();
+    }
+    float* out = part + ((int64_t(b) * Hq + h * G) * nsplit + split) * (D + 2);
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k) {
+        const int e = threadIdx.x + k * kThreads;
+        const int j = e / D, c = e % D;
+        if (j < G) out[int64_t(j) * nsplit * (D + 2) + 2 + c] = acc[k];
+    }
+    if (threadIdx.x < G) {
+        out[int64_t(threadIdx.x) * nsplit * (D + 2) + 0] = mrow[threadIdx.x];
+        out[int64_t(threadIdx.x) * nsplit * (D + 2) + 1] = lrow[threadIdx.x];
+    }
+}
+
+__global__ void attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsplit,
+                                    float* __restrict__ out)
+{
+    const int D = vp.d;
+    const int bj = blockIdx.x, j = bj % Hq;
+    const int h = j / (Hq / vp.heads);
+    extern __shared__ float os[];
+    __shared__ float sM, sL;
+    const float* pp = part + int64_t(bj) * nsplit * (D + 2);
+    if (threadIdx.x == 0) {
+        float M = -INFINITY;
+        for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pp[int64_t(s) * (D + 2)]);
+        float L = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const float m = pp[int64_t(s) * (D + 2)];
+            if (m != -INFINITY) L += pp[int64_t(s) * (D + 2) + 1] * __expf(m - M);
+        }
+        sM = M;
+        sL = L;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        float a = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const float m = pp[int64_t(s) * (D + 2)];
+            if (m != -INFINITY) a += pp[int64_t(s) * (D + 2) + 2 + c] * __expf(m - sM);
+        }
+        os[c] = (sL > 0.f) ? a / sL : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        float a = 0.f;
+        for (int c = 0; c < D; ++c) a = fmaf(basis_entry(vp, h, i, c, D), os[c], a);
+        out[int64_t(bj) * D + i] = a;
+    }
+}
+
+template <int D>
+size_t split_smem()
+{
+    return sizeof(float) * (kMaxGroup * D + 2 * kTile * (D + 1) + kMaxGroup * kTile + 3 * kMaxGroup +
+                            2 * kMaxBits * kLmStride + 2 * D) +
+           sizeof(int) * 4 * D + sizeof(uint32_t) * 2 * 2 * 8 * D;
+}
+
+int nsplit_of(int64_t ctx) { return int((ctx + kSplitLen - 1) / kSplitLen); }
+
+}  // namespace
+
+size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx)
+{
+    const size_t qt = align256(sizeof(float) * size_t(B) * Hq * d);
+    const size_t part = align256(sizeof(float) * size_t(B) * Hq * nsplit_of(ctx) * (d + 2));
+    return qt + part;
+}
+
+spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
+                           int q_dt, int B, int Hq, const uint8_t* kc, const uint8_t* vc,
+                           int64_t sstride, const float* kn, const float* vn, int64_t nstride,
+                           int64_t ctx, float scale, float* out, void* ws, size_t ws_bytes,
+                           cudaStream_t s)
+{
+    const int D = kplan->head_dim, Hkv = kplan->heads;
+    if (Hq / Hkv > kMaxGroup) return SPECTRA_ERR_UNSUPPORTED;
+    const PlanView kp = make_view(kplan), vp = make_view(vplan);
+    const int nsplit = nsplit_of(ctx);
+    float* qt = static_cast<float*>(ws);
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                           align256(sizeof(float) * size_t(B) * Hq * D));
+    attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt);
+    dim3 grid(nsplit, Hkv, B);
+    if (D == 128) {
+        const size_t sm = split_smem<128>();
+        cudaFuncSetAttribute(attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        attn_split_kernel<128><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
+                                                          nstride, nsplit, part);
+    } else {
+        const size_t sm = split_smem<64>();
+        cudaFuncSetAttribute(attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        attn_split_kernel<64><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
+                                                         nstride, nsplit, part);
+    }
+    attn_combine_kernel<<<B * Hq, D, D * sizeof(float), s>>>(vp, part, Hq, nsplit, out);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace spectra

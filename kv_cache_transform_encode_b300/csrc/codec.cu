@@ -1,0 +1,250 @@
+// codec.cu -- encode/decode on CUDA cores (any dtype, d in {64, 128}, both
+// bases, both quantizers).  The bf16 d=128 hot configurations go through the
+// tensor-core kernels in codec_tc.cu; this file serves every other case.
+//
+// "Sintesi Tecnica: SPECTRA", "La Pipeline di SPECTRA" phase 3: tokens are
+// projected into the latent basis, quantized per token and appended to the
+// latent cache; keys and values are rebuilt on the fly.  "Technisch
+// Overzicht ...", "Experimentele Opstelling": randomized Walsh-Hadamard
+// rotation (y = H D x / sqrt(d)) with a Lloyd-Max codebook.
+//
+// One warp per 32-token group (lane = token).  The d x d rotation matrix of
+// the head sits in shared memory (rows padded to d+1 floats); EIGEN uses the
+// plan's basis, RWHT builds M[i][c] = s_i H[i][c] / sqrt(d), so that both
+// bases share y_c = sum_i M[i][c] x_i and x_i = sum_c M[i][c] y_c.  Codes are
+// packed with one warp ballot per bit-column, which yields exactly the
+// group's bit-plane word.
+#include "spectra_internal.cuh"
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+namespace spectra {
+
+namespace {
+
+constexpr int kWarps = 8;
+
+template <int D>
+__device__ void load_matrix(const PlanView& pv, int h, float* M)
+{
+    constexpr int LD = D + 1;
+    if (pv.basis == SPECTRA_BASIS_EIGEN) {
+        for (int e = threadIdx.x; e < D * D; e += blockDim.x)
+            M[(e / D) * LD + (e % D)] = pv.basis_mat[size_t(h) * D * D + e];
+    } else {
+        const float inv = rsqrtf(float(D));
+        for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
+            const int i = e / D, c = e % D;
+            M[i * LD + c] = float(pv.signs[size_t(h) * D + i] * hadamard_sign(i, c)) * inv;
+        }
+    }
+}
+
+// count of thresholds tau_1..tau_{L-1} that are <= u (ascending table)
+__device__ __forceinline__ int lm_code(const float* th, int b, float u)
+{
+    int lo = 0;                        // answer in [0, L-1]
+    for (int step = 1 << (b - 1); step; step >>= 1)
+        if (th[lo + step] <= u) lo += step;
+    return lo;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+encode_generic_kernel(PlanView pv, const void* __restrict__ x, int dt, int64_t T, int64_t tstride,
+                      uint8_t* __restrict__ codes, int64_t sstride, float* __restrict__ norms,
+                      int64_t nstride)
+{
+    constexpr int LD = D + 1;
+    extern __shared__ float smem[];
+    float* M = smem;                               // [D][LD]
+    float* xs = M + D * LD;                        // [kWarps][32][LD]
+    float* th = xs + kWarps * 32 * LD;             // [8][256] Lloyd-Max thresholds
+    float* qsc = th + kMaxBits * kLmStride;        // [D]
+    int* bsh = reinterpret_cast<int*>(qsc + D);    // [D]
+
+    const int h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = pv.rec_bits[h];
+    if (R > pv.max_rec_bits) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) pv.status[h] = -SPECTRA_ERR_BUFFER;
+        return;
+    }
+    load_matrix<D>(pv, h, M);
+    for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) th[e] = pv.lm_thresh[e];
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        qsc[c] = pv.qscale[size_t(h) * D + c];
+        bsh[c] = pv.bits[size_t(h) * D + c];
+    }
+    __syncthreads();
+
+    const int64_t ngroups = (T + kGroup - 1) / kGroup;
+    const int64_t g = int64_t(blockIdx.x) * kWarps + warp;
+    if (g >= ngroups) return;
+    float* xw = xs + warp * 32 * LD;
+    for (int r = 0; r < 32; ++r) {
+        const int64_t t = g * kGroup + r;
+        for (int i = lane; i < D; i += 32)
+            xw[r * LD + i] = (t < T) ? load_elem(x, dt, t * tstride + int64_t(h) * D + i) : 0.f;
+    }
+    __syncwarp();
+    const int64_t t = g * kGroup + lane;
+    const bool live = t < T;
+    float inv_sig = 0.f;
+    if (pv.basis == SPECTRA_BASIS_RWHT) {
+        float n2 = 0.f;
+        for (int i = 0; i < D; ++i) n2 = fmaf(xw[lane * LD + i], xw[lane * LD + i], n2);
+        const float nrm = sqrtf(n2);
+        if (live) norms[int64_t(h) * nstride + t] = nrm;
+        const float sig = nrm * rsqrtf(float(D));
+        inv_sig = (sig > 0.f) ? 1.f / sig : 0.f;
+    }
+    uint32_t* out = reinterpret_cast<uint32_t*>(codes + int64_t(h) * sstride) + g * R;
+    uint32_t myword = 0;
+    int bc = 0;
+    for (int c = 0; c < D; ++c) {
+        const int b = bsh[c];
+        if (b == 0) continue;
+        float y = 0.f;
+        for (int i = 0; i < D; ++i) y = fmaf(M[i * LD + c], xw[lane * LD + i], y);
+        int code;
+        if (pv.quant == SPECTRA_Q_UNIFORM3S) {
+            const float u = fmaf(y, qsc[c], float(1 << (b - 1)));
+            code = min(max(__float2int_rd(u), 0), (1 << b) - 1);
+        } else {
+            const float s = (pv.basis == SPECTRA_BASIS_RWHT) ? inv_sig : qsc[c];
+            code = lm_code(th + (b - 1) * kLmStride, b, y * s);
+        }
+        if (!live) code = 0;
+        for (int k = 0; k < b; ++k, ++bc) {
+            const uint32_t wv = __ballot_sync(0xffffffffu, (code >> k) & 1);
+            if ((bc & 31) == lane) myword = wv;
+            if ((bc & 31) == 31) out[(bc & ~31) + lane] = myword;
+        }
+    }
+    if ((bc & 31) != 0 && lane < (bc & 31)) out[(bc & ~31) + lane] = myword;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+decode_generic_kernel(PlanView pv, const uint8_t* __restrict__ codes, int64_t sstride,
+                      const float* __restrict__ norms, int64_t nstride, int64_t T,
+                      void* __restrict__ xo, int out_dt, int64_t tstride)
+{
+    constexpr int LD = D + 1;
+    extern __shared__ float smem[];
+    float* M = smem;                               // [D][LD]
+    float* ys = M + D * LD;                        // [kWarps][32][LD]
+    float* lv = ys + kWarps * 32 * LD;             // [8][256] Lloyd-Max levels
+    float* rsc = lv + kMaxBits * kLmStride;        // [D]
+    int* bsh = reinterpret_cast<int*>(rsc + D);    // [D]
+    uint32_t* wsh = reinterpret_cast<uint32_t*>(bsh + D);   // [kWarps][8*D]
+
+    const int h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = pv.rec_bits[h];
+    if (R > pv.max_rec_bits) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) pv.status[h] = -SPECTRA_ERR_BUFFER;
+        return;
+    }
+    load_matrix<D>(pv, h, M);
+    for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) lv[e] = pv.lm_level[e];
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        rsc[c] = pv.rscale[size_t(h) * D + c];
+        bsh[c] = pv.bits[size_t(h) * D + c];
+    }
+    __syncthreads();
+
+    const int64_t ngroups = (T + kGroup - 1) / kGroup;
+    const int64_t g = int64_t(blockIdx.x) * kWarps + warp;
+    if (g >= ngroups) return;
+    const uint32_t* in = reinterpret_cast<const uint32_t*>(codes + int64_t(h) * sstride) + g * R;
+    uint32_t* ww = wsh + warp * 8 * D;
+    for (int e = lane; e < R; e += 32) ww[e] = in[e];
+    __syncwarp();
+    const int64_t t = g * kGroup + lane;
+    float sig_t = 0.f;
+    if (pv.basis == SPECTRA_BASIS_RWHT && t < T)
+        sig_t = norms[int64_t(h) * nstride + t] * rsqrtf(float(D));
+    float* yw = ys + warp * 32 * LD;
+    int bc = 0;
+    for (int c = 0; c < D; ++c) {
+        const int b = bsh[c];
+        float y = 0.f;
+        if (b > 0) {
+            int code = 0;
+            for (int k = 0; k < b; ++k, ++bc) code |= int((ww[bc] >> lane) & 1u) << k;
+            if (pv.quant == SPECTRA_Q_UNIFORM3S)
+                y = rsc[c] * (float(code) + 0.5f - float(1 << (b - 1)));
+            else
+                y = ((pv.basis == SPECTRA_BASIS_RWHT) ? sig_t : rsc[c]) * lv[(b - 1) * kLmStride + code];
+        }
+        yw[lane * LD + c] = y;
+    }
+    __syncwarp();
+    for (int r = 0; r < 32; ++r) {
+        const int64_t tt = g * kGroup + r;
+        if (tt >= T) break;
+        for (int i = lane; i < D; i += 32) {
+            float acc = 0.f;
+            for (int c = 0; c < D; ++c) acc = fmaf(M[i * LD + c], yw[r * LD + c], acc);
+            const int64_t o = tt * tstride + int64_t(h) * D + i;
+            if (out_dt == SPECTRA_BF16) static_cast<__nv_bfloat16*>(xo)[o] = __float2bfloat16_rn(acc);
+            else static_cast<float*>(xo)[o] = acc;
+        }
+    }
+}
+
+template <int D>
+size_t enc_smem() { return sizeof(float) * (D * (D + 1) + kWarps * 32 * (D + 1) + kMaxBits * kLmStride + D) + sizeof(int) * D; }
+template <int D>
+size_t dec_smem() { return enc_smem<D>() + sizeof(uint32_t) * kWarps * 8 * D; }
+
+}  // namespace
+
+spectra_status launch_encode_generic(const spectra_plan* plan, const void* x, int dt, int64_t T,
+                                     int64_t token_stride, uint8_t* codes, int64_t sstride,
+                                     float* norms, int64_t nstride, cudaStream_t s)
+{
+    const PlanView pv = make_view(plan);
+    const int64_t ngroups = (T + kGroup - 1) / kGroup;
+    if (ngroups == 0) return SPECTRA_OK;
+    dim3 grid(unsigned((ngroups + kWarps - 1) / kWarps), plan->heads);
+    if (plan->head_dim == 128) {
+        const size_t sm = enc_smem<128>();
+        cudaFuncSetAttribute(encode_generic_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        encode_generic_kernel<128><<<grid, kWarps * 32, sm, s>>>(pv, x, dt, T, token_stride, codes,
+                                                                 sstride, norms, nstride);
+    } else {
+        const size_t sm = enc_smem<64>();
+        cudaFuncSetAttribute(encode_generic_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        encode_generic_kernel<64><<<grid, kWarps * 32, sm, s>>>(pv, x, dt, T, token_stride, codes,
+                                                                sstride, norms, nstride);
+    }
+    return cuda_status(cudaGetLastError());
+}
+
+spectra_status launch_decode_generic(const spectra_plan* plan, const uint8_t* codes, int64_t sstride,
+                                     const float* norms, int64_t nstride, int64_t T, void* x_out,
+                                     int out_dt, int64_t token_stride, cudaStream_t s)
+{
+    const PlanView pv = make_view(plan);
+    const int64_t ngroups = (T + kGroup - 1) / kGroup;
+    if (ngroups == 0) return SPECTRA_OK;
+    dim3 grid(unsigned((ngroups + kWarps - 1) / kWarps), plan->heads);
+    if (plan->head_dim == 128) {
+        const size_t sm = dec_smem<128>();
+        cudaFuncSetAttribute(decode_generic_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        decode_generic_kernel<128><<<grid, kWarps * 32, sm, s>>>(pv, codes, sstride, norms, nstride, T,
+                                                                 x_out, out_dt, token_stride);
+    } else {
+        const size_t sm = dec_smem<64>();
+        cudaFuncSetAttribute(decode_generic_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        decode_generic_kernel<64><<<grid, kWarps * 32, sm, s>>>(pv, codes, sstride, norms, nstride, T,
+                                                                x_out, out_dt, token_stride);
+    }
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace spectra

@@ -1,0 +1,157 @@
+// spectra_internal.cuh -- shared declarations of the CUDA library (not part
+// of the public ABI; see include/spectra.h for the contract).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spectra.h"
+
+namespace spectra {
+
+constexpr int kGroup = 32;          // tokens per bit-plane group (one warp)
+constexpr int kMaxBits = 8;         // widest channel code
+constexpr int kLmStride = 256;      // row stride of the Lloyd-Max tables
+
+// ---------------------------------------------------------------------------
+// Layout of a plan's `derived` buffer.  Each table starts on a 256-byte
+// boundary.  Per head h:
+//   chan_off[h][c]  u16  bit offset o_c of channel c inside a token's R bits
+//   qscale[h][c]    f32  encode scale: UNIFORM3S 2^b/(6 sigma_c); LLOYD 1/sigma_c
+//   rscale[h][c]    f32  decode scale: UNIFORM3S Delta_c;        LLOYD sigma_c
+// Shared by every head:
+//   lm_level[b-1][k] f32 Gaussian Lloyd-Max level k of width b (ascending)
+//   lm_thresh[b-1][k] f32 threshold between levels k-1 and k (k >= 1)
+// Tensor-core operand images (see codec_tc.cu / attn_tc.cu):
+//   enc_img[h]  bf16/f16 basis image for the encode contraction
+//   dec_img[h]  f16 basis image for the decode contraction
+// ---------------------------------------------------------------------------
+struct DerivedLayout {
+    size_t chan_off, qscale, rscale, lm_level, lm_thresh, enc_img, dec_img, total;
+    size_t enc_img_head_bytes, dec_img_head_bytes;
+};
+
+__host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Per-head tensor-core image sizes (bytes).  Encode: two K-major f16 terms
+// (hi, lo) of the d x d basis, or one bf16 +-1 Hadamard image for RWHT.
+// Decode: two f16 terms of (basis * rscale).
+__host__ __device__ inline size_t enc_img_bytes(int d) { return size_t(2) * d * d * 2; }
+__host__ __device__ inline size_t dec_img_bytes(int d) { return size_t(2) * d * d * 2; }
+
+__host__ __device__ inline DerivedLayout derived_layout(int heads, int d)
+{
+    DerivedLayout L;
+    size_t o = 0;
+    const size_t hd = size_t(heads) * d;
+    L.chan_off = o;  o = align256(o + hd * sizeof(uint16_t));
+    L.qscale = o;    o = align256(o + hd * sizeof(float));
+    L.rscale = o;    o = align256(o + hd * sizeof(float));
+    L.lm_level = o;  o = align256(o + kMaxBits * kLmStride * sizeof(float));
+    L.lm_thresh = o; o = align256(o + kMaxBits * kLmStride * sizeof(float));
+    L.enc_img_head_bytes = enc_img_bytes(d);
+    L.dec_img_head_bytes = dec_img_bytes(d);
+    L.enc_img = o;   o = align256(o + size_t(heads) * L.enc_img_head_bytes);
+    L.dec_img = o;   o = align256(o + size_t(heads) * L.dec_img_head_bytes);
+    L.total = o;
+    return L;
+}
+
+// Device-side view of a plan with derived tables resolved.
+struct PlanView {
+    int heads, d, basis, quant, max_rec_bits;
+    const float* basis_mat;
+    const float* eigvals;
+    const int8_t* signs;
+    const uint8_t* bits;
+    const int32_t* rec_bits;
+    const uint16_t* chan_off;
+    const float* qscale;
+    const float* rscale;
+    const float* lm_level;
+    const float* lm_thresh;
+    const uint8_t* enc_img;
+    const uint8_t* dec_img;
+    int32_t* status;
+};
+
+inline PlanView make_view(const spectra_plan* p)
+{
+    const DerivedLayout L = derived_layout(p->heads, p->head_dim);
+    const uint8_t* base = static_cast<const uint8_t*>(p->derived);
+    PlanView v;
+    v.heads = p->heads;
+    v.d = p->head_dim;
+    v.basis = p->basis;
+    v.quant = p->quant;
+    v.max_rec_bits = p->max_rec_bits;
+    v.basis_mat = p->basis_mat;
+    v.eigvals = p->eigvals;
+    v.signs = p->signs;
+    v.bits = p->bits;
+    v.rec_bits = p->rec_bits;
+    v.chan_off = reinterpret_cast<const uint16_t*>(base + L.chan_off);
+    v.qscale = reinterpret_cast<const float*>(base + L.qscale);
+    v.rscale = reinterpret_cast<const float*>(base + L.rscale);
+    v.lm_level = reinterpret_cast<const float*>(base + L.lm_level);
+    v.lm_thresh = reinterpret_cast<const float*>(base + L.lm_thresh);
+    v.enc_img = base + L.enc_img;
+    v.dec_img = base + L.dec_img;
+    v.status = p->status;
+    return v;
+}
+
+// Bytes of a packed stream: ceil(T/32) groups of R words, padded to 16 B.
+__host__ __device__ inline int64_t stream_bytes(int64_t R, int64_t T)
+{
+    if (R <= 0 || T <= 0) return 0;
+    const int64_t raw = ((T + kGroup - 1) / kGroup) * 4 * R;
+    return (raw + 15) / 16 * 16;
+}
+
+// Sylvester Hadamard entry H[i][j] = (-1)^popcount(i & j).
+__host__ __device__ inline int hadamard_sign(int i, int j)
+{
+#ifdef __CUDA_ARCH__
+    return (__popc(i & j) & 1) ? -1 : 1;
+#else
+    return (__builtin_popcount(unsigned(i & j)) & 1) ? -1 : 1;
+#endif
+}
+
+__device__ __forceinline__ float load_elem(const void* p, int dt, int64_t idx)
+{
+    if (dt == SPECTRA_BF16) {
+        const uint16_t u = static_cast<const uint16_t*>(p)[idx];
+        return __uint_as_float(uint32_t(u) << 16);
+    }
+    return static_cast<const float*>(p)[idx];
+}
+
+// ----- launchers (defined in the .cu files) --------------------------------
+spectra_status launch_gram(const spectra_plan* plan, const void* x, int dt, int64_t n_cal,
+                           int64_t token_stride, float* partials, int nchunks, cudaStream_t s);
+spectra_status launch_jacobi(const spectra_plan* plan, const float* partials, int nchunks,
+                             int64_t n_cal, int max_sweeps, float* gram_out, cudaStream_t s);
+spectra_status launch_alloc(const spectra_plan* plan, int R_tot, int fixed_bits, cudaStream_t s);
+spectra_status launch_finalize(const spectra_plan* plan, cudaStream_t s);
+spectra_status launch_encode(const spectra_plan* plan, const void* x, int dt, int64_t T,
+                             int64_t token_stride, uint8_t* codes, int64_t sstride, float* norms,
+                             int64_t nstride, cudaStream_t s);
+spectra_status launch_decode(const spectra_plan* plan, const uint8_t* codes, int64_t sstride,
+                             const float* norms, int64_t nstride, int64_t T, void* x_out,
+                             int out_dt, int64_t token_stride, cudaStream_t s);
+spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
+                           int q_dt, int B, int Hq, const uint8_t* kc, const uint8_t* vc,
+                           int64_t sstride, const float* kn, const float* vn, int64_t nstride,
+                           int64_t ctx, float scale, float* out, void* ws, size_t ws_bytes,
+                           cudaStream_t s);
+size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx);
+int gram_chunks(int heads, int64_t n_cal);
+
+inline spectra_status cuda_status(cudaError_t e)
+{
+    return e == cudaSuccess ? SPECTRA_OK : SPECTRA_ERR_CUDA;
+}
+
+}  // namespace spectra

@@ -1,0 +1,105 @@
+"""GPU parity of the packed-cache decode-step attention against the oracle's
+fp64 attention over the same reconstructed cache (identical plans, streams
+and queries on both sides).  Shapes span several context splits, 64-token
+tiles and a ragged tail, with grouped-query heads."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from parity import ATTN_TOL, gpu_plan, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def spx():
+    import kv_cache_transform_encode_b300 as spx
+    spx.lib()
+    return spx
+
+
+def _setup(orc, B, Hkv, ctx, d=128, kind="eigen", B_bits=2.0, quant=0, seed=11):
+    """Oracle plans from batch element 0's first tokens; per-batch caches."""
+    kx = [synth.to_bf16_exact(synth.spiked_t(seed + b, ctx, Hkv, d, role=synth.ROLE_K)).astype(np.float64)
+          for b in range(B)]
+    vx = [synth.to_bf16_exact(synth.spiked_t(seed + b, ctx, Hkv, d, role=synth.ROLE_V)).astype(np.float64)
+          for b in range(B)]
+    if kind == "eigen":
+        kp = orc.make_eigen_plan(kx[0][: min(ctx, 2048)], B_bits, quant)
+        vp = orc.make_eigen_plan(vx[0][: min(ctx, 2048)], B_bits, quant)
+    else:
+        kp = orc.make_rwht_plan(synth.rwht_signs(seed, Hkv, d), 3)
+        vp = orc.make_rwht_plan(synth.rwht_signs(seed + 1, Hkv, d), 3)
+    return kx, vx, kp, vp
+
+
+def _streams(orc, plan, xs, ctx):
+    """Oracle-encoded streams [B*Hkv] (+ norms) and reconstructions."""
+    encs = [orc.encode(plan, x) for x in xs]
+    rec = np.stack([orc.decode(plan, [e["stream"] for e in en], ctx,
+                               [e["norms"] for e in en] if plan.basis_kind == orc.BASIS_RWHT else None)
+                    for en in encs])                      # [B, ctx, Hkv, d]
+    flat = [e for en in encs for e in en]
+    sb = max(len(e["stream"]) for e in flat)
+    st = np.zeros((len(flat), max(sb, 16)), dtype=np.uint8)
+    for i, e in enumerate(flat):
+        st[i, : len(e["stream"])] = e["stream"]
+    norms = (np.stack([e["norms"] for e in flat]) if plan.basis_kind == orc.BASIS_RWHT else None)
+    return st, norms, rec
+
+
+def _run(spx, orc, B, Hq, Hkv, ctx, kind="eigen", quant=0, B_bits=2.0, scale=1.0, q=None):
+    kx, vx, kp, vp = _setup(orc, B, Hkv, ctx, kind=kind, quant=quant, B_bits=B_bits)
+    ks, kn, krec = _streams(orc, kp, kx, ctx)
+    vs, vn, vrec = _streams(orc, vp, vx, ctx)
+    if q is None:
+        q = synth.to_bf16_exact(synth.queries(5, B, Hq, 128))
+    want = orc.attn_decode(q.astype(np.float64), krec, vrec, scale)
+    gk, gv = gpu_plan(spx, kp), gpu_plan(spx, vp)
+    stride = max(ks.shape[1], vs.shape[1])
+    kd = torch.zeros((ks.shape[0], stride), dtype=torch.uint8)
+    vd = torch.zeros((vs.shape[0], stride), dtype=torch.uint8)
+    kd[:, : ks.shape[1]] = torch.from_numpy(ks)
+    vd[:, : vs.shape[1]] = torch.from_numpy(vs)
+    out = torch.zeros((B, Hq, 128), device="cuda")
+    spx.spectra_attn_decode(gk, gv, torch.from_numpy(q).to(torch.bfloat16).cuda(), kd.cuda(), vd.cuda(),
+                            ctx, scale, out,
+                            k_norms=None if kn is None else torch.from_numpy(kn).cuda(),
+                            v_norms=None if vn is None else torch.from_numpy(vn).cuda())
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), want
+
+
+@pytest.mark.parametrize("ctx", [1, 100, 2048, 4500])
+def test_attn_uniform_gqa(spx, orc, ctx):
+    got, want = _run(spx, orc, B=2, Hq=8, Hkv=2, ctx=ctx)
+    assert rel_l2(got, want) <= ATTN_TOL, rel_l2(got, want)
+
+
+def test_attn_lloyd_and_budgets(spx, orc):
+    got, want = _run(spx, orc, B=1, Hq=4, Hkv=1, ctx=3000, quant=1, B_bits=1.33)
+    assert rel_l2(got, want) <= ATTN_TOL
+    got, want = _run(spx, orc, B=1, Hq=4, Hkv=1, ctx=1500, quant=0, B_bits=4.0)
+    assert rel_l2(got, want) <= ATTN_TOL
+
+
+def test_attn_rwht(spx, orc):
+    got, want = _run(spx, orc, B=2, Hq=4, Hkv=2, ctx=1200, kind="rwht")
+    assert rel_l2(got, want) <= ATTN_TOL
+
+
+def test_attn_peaky_scores(spx, orc):
+    """Sharper softmax (scale 4 on N(0,1/d) queries): still within tolerance."""
+    got, want = _run(spx, orc, B=1, Hq=8, Hkv=2, ctx=2500, scale=4.0)
+    assert rel_l2(got, want) <= ATTN_TOL
+
+
+def test_attn_empty_context(spx, orc):
+    kx, vx, kp, vp = _setup(orc, 1, 2, 64)
+    gk, gv = gpu_plan(spx, kp), gpu_plan(spx, vp)
+    out = torch.full((1, 4, 128), 7.0, device="cuda")
+    codes = torch.zeros((2, 16), dtype=torch.uint8, device="cuda")
+    spx.spectra_attn_decode(gk, gv, torch.zeros((1, 4, 128), device="cuda"), codes, codes, 0, 1.0, out)
+    torch.cuda.synchronize()
+    assert out.abs().max().item() == 0.0
