@@ -112,51 +112,63 @@ finalize_kernel(int basis, int quant, int max_rec_bits, const float* __restrict_
     }
 }
 
-// Gaussian Lloyd-Max codebooks for widths 1..8 (one warp per width).
-// The optimal levels of N(0,1) satisfy l_k = E[X | t_k < X < t_{k+1}] with
-// t the midpoints of adjacent levels (the Lloyd-Max conditions).  Solved by
-// Newton's method on F_k = l_k P_k - M_k (P_k the cell mass, M_k the cell's
-// first moment), whose Jacobian is tridiagonal; by symmetry only the L/2
-// positive levels are unknowns.  Start: Panter-Dite companding points
-// sqrt(3) * Phi^-1((j + 1/2) / L).
+// Gaussian Lloyd-Max codebooks for widths 1..8 (one warp per width, one
+// block per width).  The optimal levels of N(0,1) are the fixed point of
+// Lloyd's map: each level equals the centroid of its cell,
+//   c_k = (phi(t_k) - phi(t_{k+1})) / (Phi(t_{k+1}) - Phi(t_k)),
+// with thresholds t at the midpoints of adjacent levels.  Solved here by
+// Newton's method on G(a) = a - c(a) (tridiagonal Jacobian, Thomas solve)
+// with a backtracking line search on max|G| that keeps the levels ordered --
+// a different solver from plain Lloyd iteration, reaching the same fixed
+// point.  By symmetry only the L/2 positive levels are unknowns.
 constexpr int kHalfMax = 128;
 
-__global__ void __launch_bounds__(256)
-lm_tables_kernel(float* __restrict__ levels, float* __restrict__ thresh)
+// Evaluates G = a - c(a) over the positive half; optionally the Jacobian
+// bands.  Returns max |G| over the warp.
+__device__ double lm_eval(const double* a, int H, int lane, double* G, double* lo, double* up, double* dg)
 {
-    __shared__ double a_s[8][kHalfMax], f_s[8][kHalfMax], dg_s[8][kHalfMax],
-        lo_s[8][kHalfMax], up_s[8][kHalfMax];
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = w + 1, L = 1 << b, H = L >> 1;
-    double* a = a_s[w];
     const double inv_sqrt2 = 0.70710678118654752440;
     const double inv_sqrt2pi = 0.39894228040143267794;
-    for (int k = lane; k < H; k += 32)
-        a[k] = sqrt(3.0) * normcdfinv((H + k + 0.5) / double(L));
-    __syncwarp();
-    for (int it = 0; it < 80; ++it) {
-        for (int k = lane; k < H; k += 32) {
-            const double ak = a[k];
-            const double tk = (k == 0) ? 0.0 : 0.5 * (a[k - 1] + ak);
-            const bool last = (k == H - 1);
-            const double tk1 = last ? 0.0 : 0.5 * (ak + a[k + 1]);
-            const double Qk = 0.5 * erfc(tk * inv_sqrt2);
-            const double Qk1 = last ? 0.0 : 0.5 * erfc(tk1 * inv_sqrt2);
-            const double phk = inv_sqrt2pi * exp(-0.5 * tk * tk);
-            const double phk1 = last ? 0.0 : inv_sqrt2pi * exp(-0.5 * tk1 * tk1);
-            const double P = Qk - Qk1, M = phk - phk1;
-            const double low = (k >= 1) ? 0.5 * (tk - ak) * phk : 0.0;
-            const double upp = last ? 0.0 : 0.5 * (ak - tk1) * phk1;
-            f_s[w][k] = ak * P - M;
-            lo_s[w][k] = low;
-            up_s[w][k] = upp;
-            dg_s[w][k] = P + low + upp;
+    double gmax = 0.0;
+    for (int k = lane; k < H; k += 32) {
+        const double ak = a[k];
+        const bool last = (k == H - 1);
+        const double tk = (k == 0) ? 0.0 : 0.5 * (a[k - 1] + ak);
+        const double tk1 = last ? 0.0 : 0.5 * (ak + a[k + 1]);
+        const double Qk = 0.5 * erfc(tk * inv_sqrt2);
+        const double Qk1 = last ? 0.0 : 0.5 * erfc(tk1 * inv_sqrt2);
+        const double phk = inv_sqrt2pi * exp(-0.5 * tk * tk);
+        const double phk1 = last ? 0.0 : inv_sqrt2pi * exp(-0.5 * tk1 * tk1);
+        const double P = Qk - Qk1;
+        const double c = (phk - phk1) / P;
+        const double g = ak - c;
+        gmax = fmax(gmax, fabs(g));
+        if (G) {
+            const double dck = (k >= 1) ? phk * (c - tk) / P : 0.0;      // dc/dt_k
+            const double dck1 = last ? 0.0 : phk1 * (tk1 - c) / P;       // dc/dt_{k+1}
+            G[k] = g;
+            lo[k] = -0.5 * dck;
+            up[k] = -0.5 * dck1;
+            dg[k] = 1.0 - 0.5 * dck - 0.5 * dck1;
         }
+    }
+    for (int o = 16; o; o >>= 1) gmax = fmax(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+    return gmax;
+}
+
+__global__ void __launch_bounds__(32)
+lm_tables_kernel(float* __restrict__ levels, float* __restrict__ thresh)
+{
+    __shared__ double a[kHalfMax], tr[kHalfMax], f[kHalfMax], lo[kHalfMax], up[kHalfMax], dg[kHalfMax];
+    const int lane = threadIdx.x;
+    const int b = blockIdx.x + 1, L = 1 << b, H = L >> 1;
+    for (int k = lane; k < H; k += 32) a[k] = normcdfinv((H + k + 0.5) / double(L));
+    __syncwarp();
+    for (int it = 0; it < 100; ++it) {
+        const double g0 = lm_eval(a, H, lane, f, lo, up, dg);
         __syncwarp();
-        double maxd = 0.0;
-        if (lane == 0) {
-            // Thomas solve J delta = -F (in place: up <- c', f <- d')
-            double* dg = dg_s[w]; double* lo = lo_s[w]; double* up = up_s[w]; double* f = f_s[w];
+        if (g0 < 1e-13) break;
+        if (lane == 0) {   // Thomas solve J delta = -G (in place: up <- c', f <- d')
             double m = dg[0];
             up[0] /= m;
             f[0] = -f[0] / m;
@@ -166,24 +178,22 @@ lm_tables_kernel(float* __restrict__ levels, float* __restrict__ thresh)
                 f[k] = (-f[k] - lo[k] * f[k - 1]) / m;
             }
             for (int k = H - 2; k >= 0; --k) f[k] -= up[k] * f[k + 1];
-            // damped step keeping 0 < a_0 < a_1 < ...
-            double lam = 1.0;
-            for (int tries = 0; tries < 40; ++tries) {
-                bool ok = (a[0] + lam * f[0]) > 0.0;
-                for (int k = 1; k < H && ok; ++k)
-                    ok = (a[k] + lam * f[k]) > (a[k - 1] + lam * f[k - 1]);
-                if (ok) break;
-                lam *= 0.5;
-            }
-            for (int k = 0; k < H; ++k) {
-                const double st = lam * f[k];
-                a[k] += st;
-                maxd = fmax(maxd, fabs(st));
-            }
         }
-        maxd = __shfl_sync(0xffffffffu, maxd, 0);
         __syncwarp();
-        if (maxd < 1e-15) break;
+        double lam = 1.0;
+        bool accepted = false;
+        for (int ls = 0; ls < 50 && !accepted; ++ls, lam *= 0.5) {
+            for (int k = lane; k < H; k += 32) tr[k] = a[k] + lam * f[k];
+            __syncwarp();
+            bool mono = true;
+            for (int k = lane; k < H; k += 32) mono = mono && (tr[k] > ((k == 0) ? 0.0 : tr[k - 1]));
+            mono = __all_sync(0xffffffffu, mono);
+            if (mono) accepted = lm_eval(tr, H, lane, nullptr, nullptr, nullptr, nullptr) < g0;
+            __syncwarp();
+        }
+        if (!accepted) break;
+        for (int k = lane; k < H; k += 32) a[k] = tr[k];
+        __syncwarp();
     }
     float* lv = levels + (b - 1) * kLmStride;
     float* th = thresh + (b - 1) * kLmStride;
@@ -231,7 +241,7 @@ spectra_status launch_finalize(const spectra_plan* plan, cudaStream_t s)
     spectra_status st = cuda_status(cudaGetLastError());
     if (st != SPECTRA_OK) return st;
     if (plan->quant == SPECTRA_Q_LLOYD_GAUSS) {
-        lm_tables_kernel<<<1, 256, 0, s>>>(const_cast<float*>(v.lm_level), const_cast<float*>(v.lm_thresh));
+        lm_tables_kernel<<<kMaxBits, 32, 0, s>>>(const_cast<float*>(v.lm_level), const_cast<float*>(v.lm_thresh));
         st = cuda_status(cudaGetLastError());
         if (st != SPECTRA_OK) return st;
     }

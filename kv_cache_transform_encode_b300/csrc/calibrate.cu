@@ -183,7 +183,7 @@ jacobi_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int 
                     const float at = fabsf(theta);
                     float t = (at > 1e18f) ? 0.5f / at : 1.f / (at + sqrtf(fmaf(at, at, 1.f)));
                     t = (theta >= 0.f) ? t : -t;
-                    c = rsqrtf(fmaf(t, t, 1.f));
+                    c = 1.f / sqrtf(fmaf(t, t, 1.f));   // correctly rounded: no drift in |J|
                     s = t * c;
                 }
                 cs[tid] = c; sn[tid] = s; pp[tid] = p; qq[tid] = q;

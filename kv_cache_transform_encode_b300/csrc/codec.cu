@@ -23,7 +23,8 @@ namespace spectra {
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 8;       // encode: warps (32-token groups) per block
+constexpr int kDecWarps = 4;    // decode: fewer, to fit the staged words
 
 template <int D>
 __device__ void load_matrix(const PlanView& pv, int h, float* M)
@@ -127,7 +128,7 @@ encode_generic_kernel(PlanView pv, const void* __restrict__ x, int dt, int64_t T
 }
 
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kDecWarps * 32)
 decode_generic_kernel(PlanView pv, const uint8_t* __restrict__ codes, int64_t sstride,
                       const float* __restrict__ norms, int64_t nstride, int64_t T,
                       void* __restrict__ xo, int out_dt, int64_t tstride)
@@ -135,11 +136,11 @@ decode_generic_kernel(PlanView pv, const uint8_t* __restrict__ codes, int64_t ss
     constexpr int LD = D + 1;
     extern __shared__ float smem[];
     float* M = smem;                               // [D][LD]
-    float* ys = M + D * LD;                        // [kWarps][32][LD]
-    float* lv = ys + kWarps * 32 * LD;             // [8][256] Lloyd-Max levels
+    float* ys = M + D * LD;                        // [kDecWarps][32][LD]
+    float* lv = ys + kDecWarps * 32 * LD;             // [8][256] Lloyd-Max levels
     float* rsc = lv + kMaxBits * kLmStride;        // [D]
     int* bsh = reinterpret_cast<int*>(rsc + D);    // [D]
-    uint32_t* wsh = reinterpret_cast<uint32_t*>(bsh + D);   // [kWarps][8*D]
+    uint32_t* wsh = reinterpret_cast<uint32_t*>(bsh + D);   // [kDecWarps][8*D]
 
     const int h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,7 +158,7 @@ decode_generic_kernel(PlanView pv, const uint8_t* __restrict__ codes, int64_t ss
     __syncthreads();
 
     const int64_t ngroups = (T + kGroup - 1) / kGroup;
-    const int64_t g = int64_t(blockIdx.x) * kWarps + warp;
+    const int64_t g = int64_t(blockIdx.x) * kDecWarps + warp;
     if (g >= ngroups) return;
     const uint32_t* in = reinterpret_cast<const uint32_t*>(codes + int64_t(h) * sstride) + g * R;
     uint32_t* ww = wsh + warp * 8 * D;
@@ -199,7 +200,11 @@ decode_generic_kernel(PlanView pv, const uint8_t* __restrict__ codes, int64_t ss
 template <int D>
 size_t enc_smem() { return sizeof(float) * (D * (D + 1) + kWarps * 32 * (D + 1) + kMaxBits * kLmStride + D) + sizeof(int) * D; }
 template <int D>
-size_t dec_smem() { return enc_smem<D>() + sizeof(uint32_t) * kWarps * 8 * D; }
+size_t dec_smem()
+{
+    return sizeof(float) * (D * (D + 1) + kDecWarps * 32 * (D + 1) + kMaxBits * kLmStride + D) +
+           sizeof(int) * D + sizeof(uint32_t) * kDecWarps * 8 * D;
+}
 
 }  // namespace
 
@@ -232,16 +237,16 @@ spectra_status launch_decode_generic(const spectra_plan* plan, const uint8_t* co
     const PlanView pv = make_view(plan);
     const int64_t ngroups = (T + kGroup - 1) / kGroup;
     if (ngroups == 0) return SPECTRA_OK;
-    dim3 grid(unsigned((ngroups + kWarps - 1) / kWarps), plan->heads);
+    dim3 grid(unsigned((ngroups + kDecWarps - 1) / kDecWarps), plan->heads);
     if (plan->head_dim == 128) {
         const size_t sm = dec_smem<128>();
         cudaFuncSetAttribute(decode_generic_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-        decode_generic_kernel<128><<<grid, kWarps * 32, sm, s>>>(pv, codes, sstride, norms, nstride, T,
+        decode_generic_kernel<128><<<grid, kDecWarps * 32, sm, s>>>(pv, codes, sstride, norms, nstride, T,
                                                                  x_out, out_dt, token_stride);
     } else {
         const size_t sm = dec_smem<64>();
         cudaFuncSetAttribute(decode_generic_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-        decode_generic_kernel<64><<<grid, kWarps * 32, sm, s>>>(pv, codes, sstride, norms, nstride, T,
+        decode_generic_kernel<64><<<grid, kDecWarps * 32, sm, s>>>(pv, codes, sstride, norms, nstride, T,
                                                                 x_out, out_dt, token_stride);
     }
     return cuda_status(cudaGetLastError());
