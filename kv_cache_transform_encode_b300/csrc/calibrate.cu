@@ -12,10 +12,12 @@
 //   per thread) and writes it to the workspace.  Deterministic: the Jacobi
 //   kernel sums the chunk partials in a fixed order.
 // jacobi_kernel: one block per head.  The matrix and the rotation
-//   accumulator live in shared memory (rows padded to d+1 floats so both row
-//   and column sweeps are bank-conflict free).  Each round applies d/2
-//   disjoint rotations chosen by the round-robin ("circle") tournament, so a
-//   sweep of d-1 rounds visits every pair once.
+//   accumulator live in shared memory (rows padded to d+1 floats so column
+//   accesses are bank-conflict free).  Each round applies d/2 disjoint
+//   rotations chosen by the round-robin ("circle") tournament, so a sweep of
+//   d-1 rounds visits every pair once; the two-sided update J^T A J is done
+//   one 2x2 block at a time in registers (one pass over A per round), the
+//   accumulator V J in the same phase.
 #include "spectra_internal.cuh"
 
 #include <math.h>
@@ -112,9 +114,10 @@ jacobi_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int 
     extern __shared__ float smem[];
     float* A = smem;                 // [D][LD]
     float* V = A + D * LD;           // [D][LD]
-    float* cs = V + D * LD;          // [NP] cos
-    float* sn = cs + NP;             // [NP] sin
-    int* pp = reinterpret_cast<int*>(sn + NP);   // [NP]
+    float* sn = V + D * LD;          // [NP] sin
+    float* ta = sn + NP;             // [NP] tau = s / (1 + c)
+    float* tt = ta + NP;             // [NP] tan
+    int* pp = reinterpret_cast<int*>(tt + NP);   // [NP]
     int* qq = pp + NP;                           // [NP]
     float* red = reinterpret_cast<float*>(qq + NP);   // [33]
     int* flag = reinterpret_cast<int*>(red + 33);
@@ -172,51 +175,67 @@ jacobi_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int 
         prev_off = off;
         ++sweeps;
         for (int r = 0; r < D - 1; ++r) {
+            // rotation k annihilates A[p][q] (p = top, q = bottom of pair k).
+            // Rutishauser's form: with tau = s / (1 + c), c*x - s*y is
+            // evaluated as x - s (y + tau x), which keeps every rotation
+            // orthogonal to working precision even when c rounds to 1.
             if (tid < NP) {
                 int p, q;
                 rr_pair(D, r, tid, p, q);
                 const float apq = A[p * LD + q];
                 const float app = A[p * LD + p], aqq = A[q * LD + q];
-                float c = 1.f, s = 0.f;
+                float t = 0.f, s = 0.f, tau = 0.f;
                 if (fabsf(apq) > 1e-30f && fabsf(apq) > 1e-10f * sqrtf(fabsf(app * aqq))) {
                     const float theta = (aqq - app) / (2.f * apq);
                     const float at = fabsf(theta);
-                    float t = (at > 1e18f) ? 0.5f / at : 1.f / (at + sqrtf(fmaf(at, at, 1.f)));
+                    t = (at > 1e18f) ? 0.5f / at : 1.f / (at + sqrtf(fmaf(at, at, 1.f)));
                     t = (theta >= 0.f) ? t : -t;
-                    c = 1.f / sqrtf(fmaf(t, t, 1.f));   // correctly rounded: no drift in |J|
+                    const float c = 1.f / sqrtf(fmaf(t, t, 1.f));
                     s = t * c;
+                    tau = s / (1.f + c);
                 }
-                cs[tid] = c; sn[tid] = s; pp[tid] = p; qq[tid] = q;
+                sn[tid] = s; ta[tid] = tau; tt[tid] = t; pp[tid] = p; qq[tid] = q;
             }
             __syncthreads();
-            // rows: A <- J^T A
-            for (int e = tid; e < NP * D; e += blockDim.x) {
-                const int k = e / D, j = e % D;
-                const int p = pp[k], q = qq[k];
-                const float c = cs[k], s = sn[k];
-                const float ap = A[p * LD + j], aq = A[q * LD + j];
-                A[p * LD + j] = c * ap - s * aq;
-                A[q * LD + j] = s * ap + c * aq;
+            // A <- J^T A J, one 2x2 block (pair k rows, pair l cols) at a time
+            for (int e = tid; e < NP * NP; e += blockDim.x) {
+                const int k = e / NP, l = e % NP;
+                const int p = pp[k], q = qq[k], u = pp[l], w = qq[l];
+                float a = A[p * LD + u], b = A[p * LD + w], c = A[q * LD + u], d = A[q * LD + w];
+                if (k == l) {
+                    const float tk = tt[k];
+                    a = a - tk * b;          // a_pp - t a_pq
+                    d = d + tk * b;          // a_qq + t a_pq
+                    b = 0.f;
+                    c = 0.f;
+                } else {
+                    const float sl = sn[l], tl = ta[l], sk = sn[k], tk = ta[k];
+                    // columns (u, w) by rotation l
+                    float a1 = a - sl * (b + tl * a), b1 = b + sl * (a - tl * b);
+                    float c1 = c - sl * (d + tl * c), d1 = d + sl * (c - tl * d);
+                    // rows (p, q) by rotation k
+                    a = a1 - sk * (c1 + tk * a1);
+                    c = c1 + sk * (a1 - tk * c1);
+                    b = b1 - sk * (d1 + tk * b1);
+                    d = d1 + sk * (b1 - tk * d1);
+                }
+                A[p * LD + u] = a; A[p * LD + w] = b; A[q * LD + u] = c; A[q * LD + w] = d;
             }
-            __syncthreads();
-            // columns: A <- A J, V <- V J
+            // V <- V J
             for (int e = tid; e < NP * D; e += blockDim.x) {
                 const int k = e / D, i = e % D;
                 const int p = pp[k], q = qq[k];
-                const float c = cs[k], s = sn[k];
-                const float ap = A[i * LD + p], aq = A[i * LD + q];
-                A[i * LD + p] = c * ap - s * aq;
-                A[i * LD + q] = s * ap + c * aq;
+                const float s = sn[k], tau = ta[k];
                 const float vp = V[i * LD + p], vq = V[i * LD + q];
-                V[i * LD + p] = c * vp - s * vq;
-                V[i * LD + q] = s * vp + c * vq;
+                V[i * LD + p] = vp - s * (vq + tau * vp);
+                V[i * LD + q] = vq + s * (vp - tau * vq);
             }
             __syncthreads();
         }
     }
 
     // 3. Sort descending (ties: lower index first), sign-fix, write out.
-    int* rank = reinterpret_cast<int*>(cs);   // reuse: needs D ints (cs..qq span 2D floats)
+    int* rank = reinterpret_cast<int*>(sn);   // reuse: needs D ints (sn..ta span 2 NP floats)
     if (tid < D) {
         const float li = A[tid * LD + tid];
         int rk = 0;
@@ -253,7 +272,7 @@ jacobi_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int 
 template <int D>
 size_t jacobi_smem()
 {
-    return sizeof(float) * (2 * D * (D + 1) + D) + sizeof(int) * D + sizeof(float) * 33 + 16;
+    return sizeof(float) * (2 * D * (D + 1) + 3 * (D / 2)) + sizeof(int) * D + sizeof(float) * 33 + 16;
 }
 
 }  // namespace
