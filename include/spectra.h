@@ -236,6 +236,33 @@ SPECTRA_API spectra_status spectra_attn_decode(const spectra_plan* kplan, const 
                                    float softmax_scale, float* out, void* workspace,
                                    size_t workspace_bytes, spectra_stream_t stream);
 
+/*
+ * spectra_attn_decode_noalloc -- spectra_attn_decode for callers that cannot
+ * allocate device memory when they run a decode step (code inside an
+ * allocator or memory-pool callback, hosts whose device memory belongs to
+ * another framework's pool, deployments that forbid allocation after
+ * start-up).  The pages have no counterpart: this is a packaging variant of
+ * spectra_attn_decode, with the same arguments minus the workspace and the
+ * same results.
+ * Scratch: a static device array of SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES inside
+ *   the library, held by every GPU that loads the library until the process
+ *   exits.  A call whose spectra_attn_workspace_bytes(B, Hq, d, ctx) exceeds
+ *   it returns SPECTRA_ERR_UNSUPPORTED and launches nothing.  Nothing in the
+ *   array needs clearing between calls.
+ * The first call on a device looks up the array's device address and caches
+ *   it (make that first call before any stream capture).  Every call shares
+ *   the one array: calls whose kernels overlap on the GPU race on it.
+ * This call allocates nothing (no cudaMalloc / cudaFree, no allocating
+ *   library routine).
+ */
+#define SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+SPECTRA_API spectra_status spectra_attn_decode_noalloc(const spectra_plan* kplan, const spectra_plan* vplan,
+                                   const void* q, spectra_dtype q_dt, int B, int Hq,
+                                   const uint8_t* k_codes, const uint8_t* v_codes,
+                                   int64_t stream_stride_bytes, const float* k_norms,
+                                   const float* v_norms, int64_t norms_stride, int64_t ctx,
+                                   float softmax_scale, float* out, spectra_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

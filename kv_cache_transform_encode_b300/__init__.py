@@ -33,7 +33,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error
 EXPORTS = ("spectra_version", "spectra_status_string", "spectra_plan_derived_bytes",
            "spectra_stream_bytes", "spectra_calibrate_workspace_bytes", "spectra_calibrate",
            "spectra_alloc_bits", "spectra_plan_finalize", "spectra_encode", "spectra_decode",
-           "spectra_attn_workspace_bytes", "spectra_attn_decode")
+           "spectra_attn_workspace_bytes", "spectra_attn_decode", "spectra_attn_decode_noalloc")
 
 
 class SpectraError(RuntimeError):
@@ -82,6 +82,8 @@ def lib() -> C.CDLL:
             "spectra_attn_workspace_bytes": (sz, [C.c_int, C.c_int, C.c_int, i64]),
             "spectra_attn_decode": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp, vp,
                                               i64, i64, f32, vp, vp, sz, vp]),
+            "spectra_attn_decode_noalloc": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp,
+                                                      vp, i64, i64, f32, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(h, name)
@@ -243,3 +245,25 @@ def spectra_attn_decode(kplan: Plan, vplan: Plan, q: torch.Tensor, k_codes: torc
                                    nstride, ctx, float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(),
                                    _stream(stream))
     _check(st, "spectra_attn_decode")
+
+
+SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def spectra_attn_decode_noalloc(kplan: Plan, vplan: Plan, q: torch.Tensor, k_codes: torch.Tensor,
+                                v_codes: torch.Tensor, ctx: int, softmax_scale: float, out: torch.Tensor,
+                                k_norms: torch.Tensor | None = None, v_norms: torch.Tensor | None = None,
+                                stream=None):
+    """spectra_attn_decode for callers that cannot allocate device memory:
+    the split-context scratch comes from a static buffer inside the library
+    (SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES), so neither this binding nor the
+    library allocates anything.  Calls that overlap on the GPU race on that
+    shared buffer; make the first call on a device before any stream
+    capture."""
+    B, Hq, d = q.shape
+    kp, vp = kplan.c(), vplan.c()
+    nstride = k_norms.stride(0) if k_norms is not None else 0
+    st = lib().spectra_attn_decode_noalloc(C.byref(kp), C.byref(vp), _ptr(q), _dt(q), B, Hq, _ptr(k_codes),
+                                           _ptr(v_codes), k_codes.stride(0), _ptr(k_norms), _ptr(v_norms),
+                                           nstride, ctx, float(softmax_scale), _ptr(out), _stream(stream))
+    _check(st, "spectra_attn_decode_noalloc")
