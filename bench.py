@@ -50,6 +50,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=T_TOK,
+                    help="tokens per head (default: the Llama-shaped layer's 32768); other values are "
+                         "for profiling captures, not bench lines")
+    ap.add_argument("--copies", type=int, default=NCOPY,
+                    help="rotating input/output copies (L2 defeat); fewer for profiling captures")
     return ap.parse_args()
 
 
@@ -110,6 +115,8 @@ class ClockSampler:
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
+
+    T_TOK, NCOPY = args.tokens, args.copies
 
     import kv_cache_transform_encode_b300 as spx
     import synth

@@ -4,6 +4,7 @@
 #include "spectra_internal.cuh"
 
 #include <math.h>
+#include <stdlib.h>
 
 using namespace spectra;
 
@@ -66,13 +67,20 @@ spectra_status check_streams(const spectra_plan* p, const uint8_t* codes, int64_
     return SPECTRA_OK;
 }
 
-bool force_generic()
+// Kernel-family selection for encode/decode, read on every call so a test
+// process can switch it: SPECTRA_PATH=generic sends every call to the
+// CUDA-core kernels; SPECTRA_PATH=tc requires the tensor-core kernels (a call
+// they do not cover returns SPECTRA_ERR_UNSUPPORTED); unset = tensor cores
+// where they apply (bf16 cache, head_dim 128), CUDA cores elsewhere.
+enum PathChoice { PATH_AUTO, PATH_GENERIC, PATH_TC };
+
+PathChoice path_choice()
 {
-    static const int v = [] {
-        const char* e = getenv("SPECTRA_FORCE_GENERIC");
-        return (e && e[0] == '1') ? 1 : 0;
-    }();
-    return v != 0;
+    const char* e = getenv("SPECTRA_PATH");
+    if (!e) return PATH_AUTO;
+    if (e[0] == 'g') return PATH_GENERIC;
+    if (e[0] == 't') return PATH_TC;
+    return PATH_AUTO;
 }
 
 }  // namespace
@@ -173,11 +181,13 @@ spectra_status spectra_encode(const spectra_plan* plan, const void* x, spectra_d
         if (plan->basis != SPECTRA_BASIS_RWHT || T == 0) return SPECTRA_OK;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (!force_generic()) {
+    const PathChoice pc = path_choice();
+    if (pc != PATH_GENERIC) {
         bool done = false;
         st = launch_encode_tc(plan, x, dt, T, token_stride, codes, stream_stride_bytes, norms,
                               norms_stride, s, &done);
         if (st || done) return st;
+        if (pc == PATH_TC) return SPECTRA_ERR_UNSUPPORTED;
     }
     return launch_encode_generic(plan, x, dt, T, token_stride, codes, stream_stride_bytes, norms,
                                  norms_stride, s);
@@ -196,11 +206,13 @@ spectra_status spectra_decode(const spectra_plan* plan, const uint8_t* codes, in
     }
     if (T == 0) return SPECTRA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (!force_generic()) {
+    const PathChoice pc = path_choice();
+    if (pc != PATH_GENERIC) {
         bool done = false;
         st = launch_decode_tc(plan, codes, stream_stride_bytes, norms, norms_stride, T, x_out, out_dt,
                               token_stride, s, &done);
         if (st || done) return st;
+        if (pc == PATH_TC) return SPECTRA_ERR_UNSUPPORTED;
     }
     return launch_decode_generic(plan, codes, stream_stride_bytes, norms, norms_stride, T, x_out,
                                  out_dt, token_stride, s);

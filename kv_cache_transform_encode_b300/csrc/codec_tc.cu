@@ -1,22 +1,972 @@
-// codec_tc.cu -- tensor-core (tcgen05) encode/decode for bf16, d = 128.
+// codec_tc.cu -- tensor-core (tcgen05) encode and decode for bf16 caches
+// with head_dim 128, both bases, both quantizers.
+//
+// "Sintesi Tecnica: SPECTRA", "La Pipeline di SPECTRA" phase 3: tokens are
+// projected into the latent basis, quantized per token and appended to the
+// latent cache; keys and values are rebuilt on the fly.  "Technisch
+// Overzicht ...", "Experimentele Opstelling": randomized Walsh-Hadamard
+// rotation with a Lloyd-Max codebook.
+//
+// Both kernels are persistent (one CTA per SM) and warp-specialised; the
+// work list is the (head, 128-token tile) pairs in head-major order, split
+// into one contiguous range per CTA, so a CTA reloads its head's operand
+// image at most a few times.
+//
+// Encode, per tile: TMA brings x [128 tokens][128] bf16 into shared memory
+// (128-byte swizzle); one thread issues tcgen05.mma with A = the plan's basis
+// image (M = 128 channels, K = 128) and B = x (N = 128 tokens) into a TMEM
+// accumulator (double-buffered), so TMEM lane = channel, column = token.
+// The basis is fp32; it enters the bf16 tensor cores as three bf16 terms
+// (hi + mid + lo, 24 significand bits in all) accumulated into the same fp32
+// accumulator, so y carries fp32-grade accuracy, which the code-parity band
+// (3e-5 sigma) needs.  RWHT uses one exact +-1 term.  Eight epilogue warps
+// (lane = channel, two 32-token groups each) quantize without branches (two
+// FMAs per value for the uniform quantizer, all channel constants in
+// registers), gather each token's code into a byte, and turn the 32 codes
+// of a group into the channel's bit-plane words with four 8x8 bit
+// transposes -- exactly the stream layout.
+//
+// Decode, per tile: a bulk copy brings the tile's code words into shared
+// memory; eight unpack warps (lane = a pair of channels, one 32-token group
+// each) invert the bit transposes, dequantize and write the A operand
+// (bf16; for the uniform quantizer the exact odd integer 2 code + 1 - 2^b,
+// the scale Delta/2 being folded into the image) in the swizzled layout;
+// tcgen05.mma forms x = A * image^T (M = 128 tokens; image = basis * scale
+// as bf16 hi + lo; Lloyd-Max levels enter as bf16 hi + lo too); four
+// epilogue warps (lane = token) convert the accumulator to the output dtype
+// in a swizzled staging buffer that a TMA store writes out (rows past T are
+// clipped by the TMA unit).
 #include "spectra_internal.cuh"
+#include "tc_common.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
 
 namespace spectra {
 
-spectra_status launch_tc_images(const spectra_plan*, cudaStream_t) { return SPECTRA_OK; }
+namespace {
 
-spectra_status launch_encode_tc(const spectra_plan*, const void*, int, int64_t, int64_t, uint8_t*,
-                                int64_t, float*, int64_t, cudaStream_t, bool* done)
+using namespace tc;
+
+constexpr int D = 128;
+constexpr int TILE = 128;                 // tokens per tile (MMA M)
+constexpr uint32_t OPND = TILE * D * 2;   // one bf16 operand tile: 32 KB
+constexpr uint32_t KBLK = TILE * 128;     // one 64-element K block: 16 KB
+constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
+constexpr int kEncThreads = 320;          // producer, MMA, 8 epilogue warps
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// ------------------------------------------------------------------ helpers
+struct Work {
+    int begin, end;        // this CTA's item range
+};
+
+__device__ __forceinline__ Work cta_work(int total)
 {
-    *done = false;
-    return SPECTRA_OK;
+    Work w;
+    w.begin = int((int64_t(total) * blockIdx.x) / gridDim.x);
+    w.end = int((int64_t(total) * (blockIdx.x + 1)) / gridDim.x);
+    return w;
 }
 
-spectra_status launch_decode_tc(const spectra_plan*, const uint8_t*, int64_t, const float*, int64_t,
-                                int64_t, void*, int, int64_t, cudaStream_t, bool* done)
+// ------------------------------------------------------------------ pack helpers
+// 8x8 bit transpose of a 64-bit block held as (lo, hi): byte i, bit j
+// <-> byte j, bit i.  Three delta swaps (exchange distances 7, 14, 28).
+__device__ __forceinline__ void transpose8(uint32_t& lo, uint32_t& hi)
+{
+    uint32_t t;
+    t = (lo ^ (lo >> 7)) & 0x00AA00AAu;  lo ^= t ^ (t << 7);
+    t = (hi ^ (hi >> 7)) & 0x00AA00AAu;  hi ^= t ^ (t << 7);
+    t = (lo ^ (lo >> 14)) & 0x0000CCCCu; lo ^= t ^ (t << 14);
+    t = (hi ^ (hi >> 14)) & 0x0000CCCCu; hi ^= t ^ (t << 14);
+    t = (lo ^ (hi << 4)) & 0xF0F0F0F0u;  lo ^= t;  hi ^= t >> 4;
+}
+
+// bytes k of four words, in order, as one word
+__device__ __forceinline__ uint32_t gather_byte(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int k)
+{
+    const uint32_t sel = ((4u + k) << 4) | uint32_t(k);
+    return __byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410);
+}
+
+// low bytes of four words, in order, as one word
+__device__ __forceinline__ uint32_t low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+// Uniform quantizer in two FMA-pipe instructions.  With s = sat(y/(6 sigma)
+// + 1/2 + 2^-22) and v = RD(s * L(1 - 2^-22) + 1.5 * 2^23), the low byte of
+// v's bit pattern is clamp(floor((y + 3 sigma) / Delta), 0, L - 1): the
+// saturation does the clamp, the magic addend puts floor(.) in the low
+// mantissa bits, the factor (1 - 2^-22) maps s = 1 to L - 1 and the 2^-22
+// offset keeps y = 0 with sigma = 0 in the middle cell.  Decision
+// boundaries move by at most 6 sigma 2^-22 (1.4e-6 sigma).
+constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
+
+__device__ __forceinline__ uint32_t quant_uniform(float y, float qk, float cl)
+{
+    const float s = __saturatef(fmaf(y, qk, 0.5f + 0x1p-22f));
+    return __float_as_uint(__fmaf_rd(s, cl, kMagic));
+}
+
+// Lloyd-Max code: number of thresholds <= u among th[1 .. 2^b - 1]
+// (ascending), for a per-lane width b <= bmax (bmax warp-uniform).
+__device__ __forceinline__ uint32_t quant_lm(const float* th, int b, int bmax, float u)
+{
+    int lo = 0;
+    for (int s = bmax - 1; s >= 0; --s) {
+        if (s < b) {
+            const int step = 1 << s;
+            if (th[lo + step] <= u) lo += step;
+        }
+    }
+    return uint32_t(lo);
+}
+
+// ------------------------------------------------------------------ encode
+struct EncParams {
+    PlanView pv;
+    int64_t T;
+    int tiles_per_head;
+    int total;             // heads * tiles_per_head
+    int nterms;            // 3 (EIGEN) or 1 (RWHT)
+    int stages;
+    uint8_t* codes;
+    int64_t sstride;
+    float* norms;
+    int64_t nstride;
+};
+
+struct EncSmem {            // offsets into dynamic shared memory (1024-aligned base)
+    uint32_t img, xs, th, red, bars, total;
+};
+
+__host__ __device__ inline EncSmem enc_smem_layout(int nterms, int stages, bool lm)
+{
+    EncSmem L;
+    uint32_t o = 0;
+    L.img = o;  o += nterms * OPND;
+    L.xs = o;   o += stages * OPND;
+    L.th = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
+    L.red = o;  o += 2 * (4 * 32 + 8 * 32) * 4;      // RWHT norm partials and inverses
+    L.bars = o; o += 256;
+    L.total = o;
+    return L;
+}
+
+constexpr int kEncEpiWarps = 8;
+
+// D[c][t] = sum_i img[c][i] x[t][i]: TMEM lane = channel, column = token.
+// Epilogue warp e (warps 2..9): lane quadrant q = warp & 3 (channels
+// 32q .. 32q+31), token groups 2*half, 2*half+1 of each 128-token tile.
+__global__ void __launch_bounds__(64 + 32 * kEncEpiWarps, 1)
+encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const bool lm = P.pv.quant == SPECTRA_Q_LLOYD_GAUSS;
+    const bool rwht = P.pv.basis == SPECTRA_BASIS_RWHT;
+    const EncSmem L = enc_smem_layout(P.nterms, P.stages, lm);
+    uint8_t* img = smem + L.img;
+    uint8_t* xs = smem + L.xs;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* full = bars;                 // [stages <= 4]
+    uint64_t* empty = bars + 4;            // [stages]
+    uint64_t* accfull = bars + 8;          // [2]
+    uint64_t* accempty = bars + 10;        // [2]
+    uint64_t* imgfull = bars + 12;
+    uint64_t* imgempty = bars + 13;
+    uint64_t* drain = bars + 14;
+    uint64_t* rbar = bars + 15;            // [2] RWHT norm rendezvous, one per half
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 19);
+    volatile int* drain_flag = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Work W = cta_work(P.total);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P.stages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], 1); mbar_init(&accempty[a], kEncEpiWarps); }
+        mbar_init(imgfull, 1);
+        mbar_init(imgempty, 1);
+        mbar_init(drain, 1);
+        mbar_init(&rbar[0], 4);
+        mbar_init(&rbar[1], 4);
+        *abort_flag = 0;
+        *drain_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 256);
+        tmem_relinquish();
+    }
+    if (lm) {
+        float* th = reinterpret_cast<float*>(smem + L.th);
+        for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) th[e] = P.pv.lm_thresh[e];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int k = 0, j = 0, cur_h = -1;
+            int last_issued[4] = {-1, -1, -1, -1};
+            int img_issued = 0;
+            for (int w = W.begin; w < W.end; ++w, ++k) {
+                const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+                if (h != cur_h) {
+                    if (j > 0 && !mbar_wait(imgempty, (j - 1) & 1, abort_flag, kWaitNs)) break;
+                    const uint32_t bytes = P.nterms * OPND;
+                    mbar_arrive_expect_tx(imgfull, bytes);
+                    const uint8_t* src = P.pv.enc_img + size_t(h) * enc_img_bytes(D);
+                    for (uint32_t o = 0; o < bytes; o += 32768u) bulk_load(img + o, src + o, 32768u, imgfull);
+                    img_issued = j + 1;
+                    cur_h = h;
+                    ++j;
+                }
+                const int s = k % P.stages;
+                if (k >= P.stages && !mbar_wait(&empty[s], ((k / P.stages) - 1) & 1, abort_flag, kWaitNs)) break;
+                mbar_arrive_expect_tx(&full[s], OPND);
+                uint8_t* dst = xs + s * OPND;
+                tma_load_3d(dst, &tmap_x, &full[s], 0, h, tile * TILE);
+                tma_load_3d(dst + KBLK, &tmap_x, &full[s], 64, h, tile * TILE);
+                last_issued[s] = k;
+            }
+            if (*abort_flag) {   // let copies in flight land before the CTA exits
+                for (int s = 0; s < P.stages; ++s)
+                    if (last_issued[s] >= 0)
+                        mbar_wait(&full[s], (last_issued[s] / P.stages) & 1, drain_flag, 100000000ull);
+                if (img_issued > 0) mbar_wait(imgfull, (img_issued - 1) & 1, drain_flag, 100000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA
+        if (lane == 0) {
+            int k = 0, j = 0, cur_h = -1;
+            bool issued = false;
+            for (int w = W.begin; w < W.end; ++w, ++k) {
+                const int h = w / P.tiles_per_head;
+                if (h != cur_h) {
+                    if (!mbar_wait(imgfull, j & 1, abort_flag, kWaitNs)) break;
+                    cur_h = h;
+                    ++j;
+                }
+                const int s = k % P.stages, a = k & 1;
+                if (!mbar_wait(&full[s], (k / P.stages) & 1, abort_flag, kWaitNs)) break;
+                if (k >= 2 && !mbar_wait(&accempty[a], ((k >> 1) - 1) & 1, abort_flag, kWaitNs)) break;
+                tc_fence_after();
+                const uint32_t xa = smem_u32(xs + s * OPND);
+                const uint32_t ia = smem_u32(img);
+                const uint32_t d_tmem = tmem + a * 128;
+                for (int t = 0; t < P.nterms; ++t)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * KBLK + (kk & 3) * 32;
+                        mma_bf16_ss(d_tmem, sdesc_sw128(ia + t * OPND + koff), sdesc_sw128(xa + koff), IDESC,
+                                    (t | kk) ? 1u : 0u);
+                    }
+                issued = true;
+                mma_commit(&empty[s]);
+                mma_commit(&accfull[a]);
+                const bool head_ends = (w + 1 == W.end) || ((w + 1) / P.tiles_per_head != h);
+                if (head_ends) mma_commit(imgempty);
+            }
+            if (issued) {   // every MMA of this CTA done before TMEM is released
+                mma_commit(drain);
+                mbar_wait(drain, 0, drain_flag, 100000000ull);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;                        // TMEM lane quadrant: channels 32q..
+        const int half = (warp - 2) >> 2;              // token groups 2 half, 2 half + 1
+        const int c = q * 32 + lane;                   // this thread's channel
+        const float* th = reinterpret_cast<const float*>(smem + L.th);
+        float* part = reinterpret_cast<float*>(smem + L.red) + half * (4 * 32);        // [4 q][32 t]
+        float* invs = reinterpret_cast<float*>(smem + L.red) + 2 * 4 * 32 + (warp - 2) * 32;
+        int k = 0, cur_h = -1, R = 0, b = 0, o = 0, bmax = 0, ruse = 0;
+        float qk = 0.f, cl = 0.f;
+        bool head_ok = true;
+        for (int w = W.begin; w < W.end; ++w, ++k) {
+            const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+            if (h != cur_h) {
+                cur_h = h;
+                R = P.pv.rec_bits[h];
+                head_ok = R <= P.pv.max_rec_bits;
+                if (!head_ok && lane == 0) P.pv.status[h] = -SPECTRA_ERR_BUFFER;
+                b = P.pv.bits[size_t(h) * D + c];
+                o = P.pv.chan_off[size_t(h) * D + c];
+                const float qs = P.pv.qscale[size_t(h) * D + c];
+                // UNIFORM3S: qscale = 2^b / (6 sigma) -> qk = 1 / (6 sigma); LLOYD: 1 / sigma
+                qk = lm ? qs : qs / float(1 << b);
+                cl = float(1 << b) * (1.0f - 0x1p-22f);
+                bmax = __reduce_max_sync(0xffffffffu, b);
+            }
+            const int a = k & 1;
+            if (!mbar_wait(&accfull[a], (k >> 1) & 1, abort_flag, kWaitNs)) break;
+            tc_fence_after();
+            uint32_t* out = reinterpret_cast<uint32_t*>(P.codes + int64_t(h) * P.sstride);
+            bool ok = true;
+            for (int gg = 0; gg < 2; ++gg) {
+                const int gi = 2 * half + gg;                       // group inside the tile
+                const int64_t t0 = int64_t(tile) * TILE + gi * 32;
+                const bool glive = t0 < P.T;
+                uint32_t r[32];
+                tmem_ld32(tmem + a * 128 + (uint32_t(q * 32) << 16) + gi * 32, r);
+                tmem_ld_wait();
+                if (rwht) {
+                    // ||x_t||^2 = (1/d) sum_c D[c][t]^2: reduce the 32 columns
+                    // over this warp's lanes (lane t ends with token t), then
+                    // over the four lane quadrants through shared memory.
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * __uint_as_float(r[i]);
+#pragma unroll
+                    for (int s = 16; s >= 1; s >>= 1) {
+                        const bool up = lane & s;
+#pragma unroll
+                        for (int i = 0; i < s; ++i) {
+                            const float send = up ? v[i] : v[i + s];
+                            const float keep = up ? v[i + s] : v[i];
+                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+                        }
+                    }
+                    part[q * 32 + lane] = v[0];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&rbar[half]);
+                    if (!(ok = mbar_wait(&rbar[half], ruse & 1, abort_flag, kWaitNs))) break;
+                    ++ruse;
+                    const float n2 = part[lane] + part[32 + lane] + part[64 + lane] + part[96 + lane];
+                    const float nrm = sqrtf(n2 * (1.0f / float(D)));
+                    if (q == 0 && head_ok && t0 + lane < P.T) P.norms[int64_t(h) * P.nstride + t0 + lane] = nrm;
+                    invs[lane] = (nrm > 0.f) ? 1.f / nrm : 0.f;
+                    __syncwarp();
+                    // everyone has read part[] before it is written again
+                    if (lane == 0) mbar_arrive(&rbar[half]);
+                    if (!(ok = mbar_wait(&rbar[half], ruse & 1, abort_flag, kWaitNs))) break;
+                    ++ruse;
+                }
+                if (!glive || !head_ok || R == 0) continue;
+                // codes of 32 tokens (low byte of each word)
+                uint32_t cw[32];
+                if (!lm) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) cw[i] = quant_uniform(__uint_as_float(r[i]), qk, cl);
+                } else {
+                    const float* tb = th + (b > 0 ? (b - 1) * kLmStride : 0);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float u = __uint_as_float(r[i]) * (rwht ? invs[i] : qk);
+                        cw[i] = quant_lm(tb, b, bmax, u);
+                    }
+                }
+                uint32_t Y[8];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    Y[2 * m] = low_bytes(cw[8 * m], cw[8 * m + 1], cw[8 * m + 2], cw[8 * m + 3]);
+                    Y[2 * m + 1] = low_bytes(cw[8 * m + 4], cw[8 * m + 5], cw[8 * m + 6], cw[8 * m + 7]);
+                    transpose8(Y[2 * m], Y[2 * m + 1]);
+                }
+                const int64_t nt = P.T - t0;
+                const uint32_t live = nt >= 32 ? 0xffffffffu : ((1u << nt) - 1u);
+                uint32_t* dst = out + (int64_t(tile) * 4 + gi) * R + o;
+#pragma unroll
+                for (int kb = 0; kb < 8; ++kb) {
+                    if (kb < bmax) {
+                        const int hs = kb >> 2;
+                        const uint32_t pw = gather_byte(Y[hs], Y[2 + hs], Y[4 + hs], Y[6 + hs], kb & 3) & live;
+                        if (kb < b) dst[kb] = pw;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty[a]);
+            if (!ok) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        for (int w = W.begin; w < W.end; w += P.tiles_per_head)
+            P.pv.status[w / P.tiles_per_head] = -SPECTRA_ERR_TIMEOUT;
+        if (W.end > W.begin) P.pv.status[(W.end - 1) / P.tiles_per_head] = -SPECTRA_ERR_TIMEOUT;
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// ------------------------------------------------------------------ decode
+struct DecParams {
+    PlanView pv;
+    int64_t T;
+    int tiles_per_head;
+    int total;
+    int nterms;            // image terms: 2 (EIGEN) or 1 (RWHT)
+    int na;                // A tiles per stage: 1 (uniform) or 2 (Lloyd-Max hi + lo)
+    int astages;           // A stages (1 or 2)
+    int cstages;           // code-word stages
+    uint32_t cbytes;       // bytes of one code-word stage (16 * max R)
+    int out_f32;
+    const uint8_t* codes;
+    int64_t sstride;
+    const float* norms;
+    int64_t nstride;
+};
+
+struct DecSmem {
+    uint32_t img, as, cs, stg, lv, bars, total;
+};
+
+__host__ __device__ inline DecSmem dec_smem_layout(int nterms, int na, int astages, int cstages, uint32_t cbytes,
+                                                   bool lm)
+{
+    DecSmem L;
+    uint32_t o = 0;
+    L.img = o;  o += nterms * OPND;
+    L.as = o;   o += astages * na * OPND;
+    L.stg = o;  o += 2 * OPND;
+    L.cs = o;   o += cstages * cbytes;
+    o = (o + 15) & ~15u;
+    L.lv = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
+    L.bars = o; o += 256;
+    L.total = o;
+    return L;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+constexpr int kDecUnpackWarps = 8;
+constexpr int kDecEpiWarps = 4;
+constexpr int kDecThreads = 32 * (2 + kDecUnpackWarps + kDecEpiWarps);
+
+// Unpack one channel's codes of a 32-token group: planes -> code bytes.
+// X[2m], X[2m+1] hold the codes of tokens 8m .. 8m+7, one per byte.
+__device__ __forceinline__ void unpack_channel(const uint32_t* words, int o, int b, int bmax, uint32_t (&X)[8])
+{
+    uint32_t pl[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pl[k] = (k < bmax && k < b) ? words[o + k] : 0u;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        X[2 * m] = gather_byte(pl[0], pl[1], pl[2], pl[3], m);
+        X[2 * m + 1] = gather_byte(pl[4], pl[5], pl[6], pl[7], m);
+        transpose8(X[2 * m], X[2 * m + 1]);
+    }
+}
+
+// byte i of the 32 codes in X as a float (exact): M + code - M
+__device__ __forceinline__ float code_byte(const uint32_t (&X)[8], int t)
+{
+    return __uint_as_float(__byte_perm(X[t >> 2], 0x4B400000u, 0x7650u | uint32_t(t & 3))) - kMagic;
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const bool lm = P.pv.quant == SPECTRA_Q_LLOYD_GAUSS;
+    const bool rwht = P.pv.basis == SPECTRA_BASIS_RWHT;
+    const DecSmem L = dec_smem_layout(P.nterms, P.na, P.astages, P.cstages, P.cbytes, lm);
+    uint8_t* img = smem + L.img;
+    uint8_t* as = smem + L.as;
+    uint8_t* cs = smem + L.cs;
+    uint8_t* stg = smem + L.stg;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* cfull = bars;          // [cstages <= 4]
+    uint64_t* cempty = bars + 4;     // [cstages]
+    uint64_t* afull = bars + 8;      // [astages <= 2]
+    uint64_t* aempty = bars + 10;    // [astages]
+    uint64_t* accfull = bars + 12;   // [2]
+    uint64_t* accempty = bars + 14;  // [2]
+    uint64_t* imgfull = bars + 16;
+    uint64_t* imgempty = bars + 17;
+    uint64_t* drain = bars + 18;
+    uint64_t* ebar = bars + 19;      // epilogue-warp rendezvous (bounded, unlike bar.sync)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 20);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
+    volatile int* drain_flag = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Work W = cta_work(P.total);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P.cstages; ++s) { mbar_init(&cfull[s], 1); mbar_init(&cempty[s], kDecUnpackWarps); }
+        for (int s = 0; s < P.astages; ++s) { mbar_init(&afull[s], kDecUnpackWarps); mbar_init(&aempty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], 1); mbar_init(&accempty[a], kDecEpiWarps); }
+        mbar_init(imgfull, 1);
+        mbar_init(imgempty, 1);
+        mbar_init(drain, 1);
+        mbar_init(ebar, kDecEpiWarps);
+        *abort_flag = 0;
+        *drain_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 256);
+        tmem_relinquish();
+    }
+    if (lm) {
+        float* lv = reinterpret_cast<float*>(smem + L.lv);
+        for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) lv[e] = P.pv.lm_level[e];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int k = 0, j = 0, cur_h = -1, R = 0;
+            int last_issued[4] = {-1, -1, -1, -1};
+            int img_issued = 0;
+            for (int w = W.begin; w < W.end; ++w, ++k) {
+                const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+                if (h != cur_h) {
+                    if (j > 0 && !mbar_wait(imgempty, (j - 1) & 1, abort_flag, kWaitNs)) break;
+                    const uint32_t bytes = P.nterms * OPND;
+                    mbar_arrive_expect_tx(imgfull, bytes);
+                    const uint8_t* src = P.pv.dec_img + size_t(h) * dec_img_bytes(D);
+                    for (uint32_t o = 0; o < bytes; o += 32768u) bulk_load(img + o, src + o, 32768u, imgfull);
+                    img_issued = j + 1;
+                    cur_h = h;
+                    R = P.pv.rec_bits[h];
+                    if (R > P.pv.max_rec_bits) {
+                        P.pv.status[h] = -SPECTRA_ERR_BUFFER;
+                        R = 0;
+                    }
+                    ++j;
+                }
+                const int s = k % P.cstages;
+                if (k >= P.cstages && !mbar_wait(&cempty[s], ((k / P.cstages) - 1) & 1, abort_flag, kWaitNs)) break;
+                const int64_t t0 = int64_t(tile) * TILE;
+                const int64_t ngroups = min(int64_t(4), (P.T - t0 + 31) / 32);
+                const uint32_t bytes = uint32_t((ngroups * 4 * R + 15) / 16 * 16);
+                if (bytes > 0) {
+                    mbar_arrive_expect_tx(&cfull[s], bytes);
+                    bulk_load(cs + s * P.cbytes, P.codes + int64_t(h) * P.sstride + (t0 / 32) * 4 * R, bytes,
+                              &cfull[s]);
+                    last_issued[s] = k;
+                } else {
+                    mbar_arrive(&cfull[s]);
+                }
+            }
+            if (*abort_flag) {
+                for (int s = 0; s < P.cstages; ++s)
+                    if (last_issued[s] >= 0)
+                        mbar_wait(&cfull[s], (last_issued[s] / P.cstages) & 1, drain_flag, 100000000ull);
+                if (img_issued > 0) mbar_wait(imgfull, (img_issued - 1) & 1, drain_flag, 100000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA
+        if (lane == 0) {
+            int k = 0, j = 0, cur_h = -1;
+            bool issued = false;
+            // products (A term, image term): uniform 2 (ell x hi, ell x lo);
+            // EIGEN Lloyd-Max 3 (hi x hi, lo x hi, hi x lo); RWHT 2 (hi, lo x +-1)
+            const int npr = !lm ? P.nterms : (!rwht ? 3 : 2);
+            const uint32_t pa = !lm ? 0u : (!rwht ? 0x010u : 0x10u);    // nibble pr: A term
+            const uint32_t pb = !lm ? 0x10u : (!rwht ? 0x100u : 0x00u); // nibble pr: image term
+            for (int w = W.begin; w < W.end; ++w, ++k) {
+                const int h = w / P.tiles_per_head;
+                if (h != cur_h) {
+                    if (!mbar_wait(imgfull, j & 1, abort_flag, kWaitNs)) break;
+                    cur_h = h;
+                    ++j;
+                }
+                const int s = k % P.astages, a = k & 1;
+                if (!mbar_wait(&afull[s], (k / P.astages) & 1, abort_flag, kWaitNs)) break;
+                if (k >= 2 && !mbar_wait(&accempty[a], ((k >> 1) - 1) & 1, abort_flag, kWaitNs)) break;
+                tc_fence_after();
+                const uint32_t aa = smem_u32(as + s * P.na * OPND);
+                const uint32_t ia = smem_u32(img);
+                const uint32_t d_tmem = tmem + a * 128;
+                for (int pr = 0; pr < npr; ++pr) {
+                    const uint32_t at = (pa >> (4 * pr)) & 15u, bt = (pb >> (4 * pr)) & 15u;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * KBLK + (kk & 3) * 32;
+                        mma_bf16_ss(d_tmem, sdesc_sw128(aa + at * OPND + koff), sdesc_sw128(ia + bt * OPND + koff),
+                                    IDESC, (pr | kk) ? 1u : 0u);
+                    }
+                }
+                issued = true;
+                mma_commit(&aempty[s]);
+                mma_commit(&accfull[a]);
+                const bool head_ends = (w + 1 == W.end) || ((w + 1) / P.tiles_per_head != h);
+                if (head_ends) mma_commit(imgempty);
+            }
+            if (issued) {
+                mma_commit(drain);
+                mbar_wait(drain, 0, drain_flag, 100000000ull);
+            }
+        }
+    } else if (warp < 2 + kDecUnpackWarps) {
+        // ---------------------------------------------------------- unpack
+        // unit = (group gi, channel half hc); lane handles channels c0 = 64 hc + 2 lane, c0 + 1
+        const int u = warp - 2, gi = u >> 1, hc = u & 1;
+        const int c0 = 64 * hc + 2 * lane;
+        const float* lv = reinterpret_cast<const float*>(smem + L.lv);
+        int k = 0, cur_h = -1, R = 0, b0 = 0, b1 = 0, o0 = 0, o1 = 0, bmax = 0;
+        float off0 = 0.f, off1 = 0.f;
+        for (int w = W.begin; w < W.end; ++w, ++k) {
+            const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+            if (h != cur_h) {
+                cur_h = h;
+                R = P.pv.rec_bits[h];
+                if (R > P.pv.max_rec_bits) R = 0;
+                b0 = P.pv.bits[size_t(h) * D + c0];
+                b1 = P.pv.bits[size_t(h) * D + c0 + 1];
+                o0 = P.pv.chan_off[size_t(h) * D + c0];
+                o1 = P.pv.chan_off[size_t(h) * D + c0 + 1];
+                off0 = 1.0f - float(1 << b0);
+                off1 = 1.0f - float(1 << b1);
+                bmax = __reduce_max_sync(0xffffffffu, max(b0, b1));
+            }
+            const int sc = k % P.cstages, sa = k % P.astages;
+            if (!mbar_wait(&cfull[sc], (k / P.cstages) & 1, abort_flag, kWaitNs)) break;
+            if (k >= P.astages && !mbar_wait(&aempty[sa], ((k / P.astages) - 1) & 1, abort_flag, kWaitNs)) break;
+            const int64_t t0 = int64_t(tile) * TILE + gi * 32;
+            if (t0 < P.T && R > 0) {
+                const uint32_t* words = reinterpret_cast<const uint32_t*>(cs + sc * P.cbytes) + gi * R;
+                uint32_t X0[8], X1[8];
+                unpack_channel(words, o0, b0, bmax, X0);
+                unpack_channel(words, o1, b1, bmax, X1);
+                const uint32_t abase = smem_u32(as + sa * P.na * OPND) + hc * KBLK;
+                const float* lv0 = lv + (b0 > 0 ? (b0 - 1) * kLmStride : 0);
+                const float* lv1 = lv + (b1 > 0 ? (b1 - 1) * kLmStride : 0);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const uint32_t row = uint32_t(gi * 32 + t);
+                    const uint32_t addr = abase + row * 128u + ((uint32_t(lane >> 2) ^ (row & 7u)) << 4) +
+                                          4u * uint32_t(lane & 3);
+                    const float k0 = code_byte(X0, t), k1 = code_byte(X1, t);
+                    if (!lm) {
+                        // 2 code + 1 - 2^b (odd integer, exact in bf16); 0 for dropped channels
+                        const float v0 = b0 ? fmaf(k0, 2.f, off0) : 0.f;
+                        const float v1 = b1 ? fmaf(k1, 2.f, off1) : 0.f;
+                        st_shared_u32(addr, pack_bf16x2(v0, v1));
+                    } else {
+                        const float v0 = b0 ? lv0[int(k0)] : 0.f;
+                        const float v1 = b1 ? lv1[int(k1)] : 0.f;
+                        const uint32_t hv = pack_bf16x2(v0, v1);
+                        const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hv);
+                        st_shared_u32(addr, hv);
+                        st_shared_u32(addr + OPND, pack_bf16x2(v0 - __low2float(hb), v1 - __high2float(hb)));
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&afull[sa]);
+                mbar_arrive(&cempty[sc]);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const bool leader = (warp == 2 + kDecUnpackWarps && lane == 0);
+        int k = 0, euse = 0;
+        bool ok = true;
+        auto rendezvous = [&]() -> bool {   // all four epilogue warps
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ebar);
+            const bool r = mbar_wait(ebar, euse & 1, abort_flag, kWaitNs);
+            ++euse;
+            return r;
+        };
+        for (int w = W.begin; w < W.end && ok; ++w, ++k) {
+            const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+            const int a = k & 1;
+            if (!mbar_wait(&accfull[a], (k >> 1) & 1, abort_flag, kWaitNs)) break;
+            tc_fence_after();
+            const int64_t t = int64_t(tile) * TILE + q * 32 + lane;
+            float scale = 1.f;
+            if (rwht) scale = (t < P.T) ? P.norms[int64_t(h) * P.nstride + t] * (1.0f / float(D)) : 0.f;
+            const uint32_t tm = tmem + a * 128 + (uint32_t(q * 32) << 16);
+            const uint32_t row = uint32_t(q * 32 + lane);
+            const int nrounds = P.out_f32 ? 2 : 1;
+            for (int rd = 0; rd < nrounds; ++rd) {
+                // staging slot(s) must be free: the stores issued from them earlier have read them
+                const int slot = P.out_f32 ? rd : (k & 1);
+                if (leader) tma_store_wait_read<1>();
+                if (!(ok = rendezvous())) break;
+                uint8_t* sb = stg + slot * OPND;
+                const uint32_t sba = smem_u32(sb);
+                if (!P.out_f32) {
+#pragma unroll 1
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t r[32];
+                        tmem_ld32(tm + 32 * j, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                pk[e] = pack_bf16x2(__uint_as_float(r[c4 * 8 + 2 * e]) * scale,
+                                                    __uint_as_float(r[c4 * 8 + 2 * e + 1]) * scale);
+                            const uint32_t off = (j >> 1) * KBLK + sw128_offset(row, (j & 1) * 64 + c4 * 16);
+                            st_shared_v4(sba + off, pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                } else {
+#pragma unroll 1
+                    for (int j = 0; j < 2; ++j) {
+                        uint32_t r[32];
+                        tmem_ld32(tm + 64 * rd + 32 * j, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const uint32_t off = j * KBLK + sw128_offset(row, c4 * 16);
+                            st_shared_v4(sba + off, __float_as_uint(__uint_as_float(r[4 * c4]) * scale),
+                                         __float_as_uint(__uint_as_float(r[4 * c4 + 1]) * scale),
+                                         __float_as_uint(__uint_as_float(r[4 * c4 + 2]) * scale),
+                                         __float_as_uint(__uint_as_float(r[4 * c4 + 3]) * scale));
+                        }
+                    }
+                }
+                if (rd == nrounds - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&accempty[a]);
+                }
+                fence_proxy_async_smem();
+                if (!(ok = rendezvous())) break;
+                if (leader) {
+                    if (!P.out_f32) {
+                        tma_store_3d(&tmap_out, sb, 0, h, tile * TILE);
+                        tma_store_3d(&tmap_out, sb + KBLK, 64, h, tile * TILE);
+                    } else {
+                        tma_store_3d(&tmap_out, sb, 64 * rd, h, tile * TILE);
+                        tma_store_3d(&tmap_out, sb + KBLK, 64 * rd + 32, h, tile * TILE);
+                    }
+                    tma_store_commit();
+                }
+            }
+        }
+        if (leader) tma_store_wait_all<0>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        for (int w = W.begin; w < W.end; w += P.tiles_per_head)
+            P.pv.status[w / P.tiles_per_head] = -SPECTRA_ERR_TIMEOUT;
+        if (W.end > W.begin) P.pv.status[(W.end - 1) / P.tiles_per_head] = -SPECTRA_ERR_TIMEOUT;
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// ------------------------------------------------------------------ images
+// Operand images of one head, in the swizzled K-major layout the MMAs read.
+//  encode (B operand, rows = channel c, K = input index i):
+//    EIGEN: three bf16 terms of basis[i][c] (hi, mid, lo);  RWHT: s_i H[i][c].
+//  decode (B operand, rows = output index i, K = channel c):
+//    EIGEN uniform: basis[i][c] * Delta_c / 2;  EIGEN Lloyd-Max: basis[i][c] *
+//    sigma_c -- two bf16 terms (hi, lo);  RWHT: s_i H[i][c].
+__global__ void tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t* __restrict__ dec)
+{
+    const int h = blockIdx.x;
+    const bool rwht = pv.basis == SPECTRA_BASIS_RWHT;
+    uint8_t* e = enc + size_t(h) * enc_img_bytes(D);
+    uint8_t* dd = dec + size_t(h) * dec_img_bytes(D);
+    for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) {
+        const int r = idx / D, kk = idx % D;   // row, K index
+        const uint32_t off = (kk >> 6) * KBLK + sw128_offset(r, (kk & 63) * 2);
+        // encode: row = channel r, K = input i = kk
+        {
+            float v;
+            if (rwht) v = float(pv.signs[size_t(h) * D + kk] * hadamard_sign(kk, r));
+            else v = pv.basis_mat[(size_t(h) * D + kk) * D + r];
+            const int nt = rwht ? 1 : 3;
+            float rem = v;
+            for (int t = 0; t < nt; ++t) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(rem);
+                *reinterpret_cast<__nv_bfloat16*>(e + t * OPND + off) = b;
+                rem -= __bfloat162float(b);
+            }
+        }
+        // decode: row = output i = r, K = channel c = kk
+        {
+            float v;
+            if (rwht) v = float(pv.signs[size_t(h) * D + r] * hadamard_sign(r, kk));
+            else {
+                const float sc = pv.rscale[size_t(h) * D + kk];
+                v = pv.basis_mat[(size_t(h) * D + r) * D + kk] *
+                    (pv.quant == SPECTRA_Q_UNIFORM3S ? 0.5f * sc : sc);
+            }
+            const int nt = rwht ? 1 : 2;
+            float rem = v;
+            for (int t = 0; t < nt; ++t) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(rem);
+                *reinterpret_cast<__nv_bfloat16*>(dd + t * OPND + off) = b;
+                rem -= __bfloat162float(b);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+int sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    static int cache[64] = {0};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && cache[dev]) return cache[dev];
+    int n = 148;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+// [T][heads][128] cache of 2- or 4-byte elements, box [128 tokens][1][64 or 32]
+bool make_cache_map(CUtensorMap* m, const void* base, bool f32, int heads, int64_t T, int64_t tstride)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int es = f32 ? 4 : 2;
+    cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(heads), cuuint64_t(T)};
+    cuuint64_t strides[2] = {cuuint64_t(D) * es, cuuint64_t(tstride) * es};
+    cuuint32_t box[3] = {cuuint32_t(128 / es), 1u, cuuint32_t(TILE)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+constexpr uint32_t kSmemMax = 227 * 1024;
+
+}  // namespace
+
+spectra_status launch_tc_images(const spectra_plan* plan, cudaStream_t s)
+{
+    if (plan->head_dim != D) return SPECTRA_OK;
+    const PlanView pv = make_view(plan);
+    tc_images_kernel<<<plan->heads, 256, 0, s>>>(pv, const_cast<uint8_t*>(pv.enc_img), const_cast<uint8_t*>(pv.dec_img));
+    return cuda_status(cudaGetLastError());
+}
+
+spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt, int64_t T, int64_t token_stride,
+                                uint8_t* codes, int64_t sstride, float* norms, int64_t nstride, cudaStream_t s,
+                                bool* done)
 {
     *done = false;
-    return SPECTRA_OK;
+    if (dt != SPECTRA_BF16 || plan->head_dim != D || T <= 0) return SPECTRA_OK;
+    if (T > (int64_t(1) << 31) - TILE) return SPECTRA_OK;
+    CUtensorMap m;
+    if (!make_cache_map(&m, x, false, plan->heads, T, token_stride)) return SPECTRA_OK;
+    EncParams P;
+    P.pv = make_view(plan);
+    P.T = T;
+    P.tiles_per_head = int((T + TILE - 1) / TILE);
+    if (int64_t(P.tiles_per_head) * plan->heads > (int64_t(1) << 31) - 1) return SPECTRA_OK;
+    P.total = P.tiles_per_head * plan->heads;
+    P.nterms = plan->basis == SPECTRA_BASIS_RWHT ? 1 : 3;
+    const bool lm = plan->quant == SPECTRA_Q_LLOYD_GAUSS;
+    P.stages = 4;
+    while (P.stages > 2 && enc_smem_layout(P.nterms, P.stages, lm).total + 1024 > kSmemMax) --P.stages;
+    P.codes = codes;
+    P.sstride = sstride;
+    P.norms = norms;
+    P.nstride = nstride;
+    const uint32_t sm = enc_smem_layout(P.nterms, P.stages, lm).total + 1024;
+    cudaFuncSetAttribute(encode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    const int grid = min(sm_count(), P.total);
+    encode_tc_kernel<<<grid, kEncThreads, sm, s>>>(m, P);
+    *done = true;
+    return cuda_status(cudaGetLastError());
+}
+
+spectra_status launch_decode_tc(const spectra_plan* plan, const uint8_t* codes, int64_t sstride, const float* norms,
+                                int64_t nstride, int64_t T, void* x_out, int out_dt, int64_t token_stride,
+                                cudaStream_t s, bool* done)
+{
+    *done = false;
+    if (plan->head_dim != D || T <= 0) return SPECTRA_OK;
+    if (T > (int64_t(1) << 31) - TILE) return SPECTRA_OK;
+    const bool f32 = out_dt == SPECTRA_F32;
+    CUtensorMap m;
+    if (!make_cache_map(&m, x_out, f32, plan->heads, T, token_stride)) return SPECTRA_OK;
+    DecParams P;
+    P.pv = make_view(plan);
+    P.T = T;
+    P.tiles_per_head = int((T + TILE - 1) / TILE);
+    if (int64_t(P.tiles_per_head) * plan->heads > (int64_t(1) << 31) - 1) return SPECTRA_OK;
+    P.total = P.tiles_per_head * plan->heads;
+    const bool lm = plan->quant == SPECTRA_Q_LLOYD_GAUSS;
+    P.nterms = plan->basis == SPECTRA_BASIS_RWHT ? 1 : 2;
+    P.na = lm ? 2 : 1;
+    P.cbytes = uint32_t(16 * ((plan->max_rec_bits > 0) ? plan->max_rec_bits : 1));
+    P.astages = 2;
+    P.cstages = 3;
+    auto total = [&] { return dec_smem_layout(P.nterms, P.na, P.astages, P.cstages, P.cbytes, lm).total + 1024; };
+    while (total() > kSmemMax && P.cstages > 2) --P.cstages;
+    while (total() > kSmemMax && P.astages > 1) --P.astages;
+    if (total() > kSmemMax) return SPECTRA_OK;
+    P.out_f32 = f32 ? 1 : 0;
+    P.codes = codes;
+    P.sstride = sstride;
+    P.norms = norms;
+    P.nstride = nstride;
+    const uint32_t sm = total();
+    cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    const int grid = min(sm_count(), P.total);
+    decode_tc_kernel<<<grid, kDecThreads, sm, s>>>(m, P);
+    *done = true;
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace spectra

@@ -22,9 +22,9 @@ constexpr int kLmStride = 256;      // row stride of the Lloyd-Max tables
 // Shared by every head:
 //   lm_level[b-1][k] f32 Gaussian Lloyd-Max level k of width b (ascending)
 //   lm_thresh[b-1][k] f32 threshold between levels k-1 and k (k >= 1)
-// Tensor-core operand images (see codec_tc.cu / attn_tc.cu):
-//   enc_img[h]  bf16/f16 basis image for the encode contraction
-//   dec_img[h]  f16 basis image for the decode contraction
+// Tensor-core operand images (codec_tc.cu):
+//   enc_img[h]  bf16 basis image for the encode contraction
+//   dec_img[h]  bf16 basis image for the decode contraction
 // ---------------------------------------------------------------------------
 struct DerivedLayout {
     size_t chan_off, qscale, rscale, lm_level, lm_thresh, enc_img, dec_img, total;
@@ -33,11 +33,13 @@ struct DerivedLayout {
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Per-head tensor-core image sizes (bytes).  Encode: two K-major f16 terms
-// (hi, lo) of the d x d basis, or one bf16 +-1 Hadamard image for RWHT.
-// Decode: two f16 terms of (basis * rscale).
-__host__ __device__ inline size_t enc_img_bytes(int d) { return size_t(2) * d * d * 2; }
-__host__ __device__ inline size_t dec_img_bytes(int d) { return size_t(2) * d * d * 2; }
+// Per-head tensor-core operand images (bytes; head_dim 128 only, the
+// tensor-core kernels' width).  Encode: three bf16 terms (hi, mid, lo) of
+// the transposed basis, or one exact +-1 Hadamard term for RWHT.  Decode:
+// two bf16 terms of basis * scale, or one +-1 term for RWHT.  Each term is
+// a 128 x 128 bf16 tile in the 128-byte-swizzled K-major layout.
+__host__ __device__ inline size_t enc_img_bytes(int d) { return d == 128 ? size_t(3) * d * d * 2 : 0; }
+__host__ __device__ inline size_t dec_img_bytes(int d) { return d == 128 ? size_t(2) * d * d * 2 : 0; }
 
 __host__ __device__ inline DerivedLayout derived_layout(int heads, int d)
 {

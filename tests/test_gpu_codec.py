@@ -15,6 +15,15 @@ from parity import (ATTN_TOL, BAND_SIGMA, FLIP_FRAC, REC_TOL, bf16, compare_code
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["tc", "generic"])
+def path(request, monkeypatch):
+    """Kernel family for bf16 head_dim-128 encode/decode: the tensor-core
+    kernels (required: a call they do not cover fails) or the CUDA-core
+    kernels."""
+    monkeypatch.setenv("SPECTRA_PATH", request.param)
+    return request.param
+
+
 @pytest.fixture(scope="module")
 def spx():
     import kv_cache_transform_encode_b300 as spx
@@ -171,19 +180,19 @@ def test_codec_tiny_fp32_d64(spx, orc):
 
 
 @pytest.mark.parametrize("B,quant", [(2.0, 0), (4.0, 1), (2.0, 1), (1.33, 1), (16.0, 0)])
-def test_codec_llama_bf16(spx, orc, B, quant):
+def test_codec_llama_bf16(spx, orc, path, B, quant):
     x, xd, x64 = llama_case(T=1000)
     oplan = orc.make_eigen_plan(x64[:512], B, quant)
     _check_codec(spx, orc, oplan, x64, xd, 1000)
 
 
-def test_codec_rwht_lloyd3(spx, orc):
+def test_codec_rwht_lloyd3(spx, orc, path):
     x, xd, x64 = llama_case(T=700, H=6, seed=3)
     oplan = orc.make_rwht_plan(synth.rwht_signs(3, 6, 128), 3)
     _check_codec(spx, orc, oplan, x64, xd, 700)
 
 
-def test_codec_zero_bit_channels(spx, orc):
+def test_codec_zero_bit_channels(spx, orc, path):
     """0.5 bits/value on a steep spectrum: dropped channels take no bits and
     decode to exactly their zero latent coordinate."""
     x, xd, x64 = llama_case(T=300, H=2)
@@ -192,15 +201,15 @@ def test_codec_zero_bit_channels(spx, orc):
     _check_codec(spx, orc, oplan, x64, xd, 300)
 
 
-@pytest.mark.parametrize("T", [1, 31, 32, 33, 127, 129])
-def test_codec_ragged_lengths(spx, orc, T):
+@pytest.mark.parametrize("T", [1, 31, 32, 33, 127, 129, 255, 257, 1000])
+def test_codec_ragged_lengths(spx, orc, path, T):
     x, xd, x64 = llama_case(T=T, H=2, seed=5)
     x2, _, x642 = llama_case(T=256, H=2, seed=5)
     oplan = orc.make_eigen_plan(x642, 2.0)
     _check_codec(spx, orc, oplan, x64, xd, T)
 
 
-def test_codec_empty(spx, orc):
+def test_codec_empty(spx, orc, path):
     x, xd, x64 = llama_case(T=64, H=2)
     oplan = orc.make_eigen_plan(x64, 2.0)
     p = gpu_plan(spx, oplan)
@@ -212,7 +221,7 @@ def test_codec_empty(spx, orc):
     assert codes.sum().item() == 0
 
 
-def test_end_to_end_device_plan(spx, orc):
+def test_end_to_end_device_plan(spx, orc, path):
     """Whole path on the device (calibrate -> alloc -> encode -> decode) vs
     the oracle's whole path: allocations agree and reconstruction errors
     match.  A differing width may only come from a near-tie in the greedy
@@ -233,3 +242,52 @@ def test_end_to_end_device_plan(spx, orc):
     xo = orc.decode(oplan, [e["stream"] for e in orc.encode(oplan, x64)], 4096)
     e_gpu, e_orc = orc.relmse(x64, out.cpu().numpy()), orc.relmse(x64, xo)
     assert abs(e_gpu - e_orc) <= 0.05 * e_orc, (e_gpu, e_orc)
+
+
+def test_codec_multi_head_tiles(spx, orc, path):
+    """More (head, tile) work items than SMs: persistent CTAs walk ranges
+    that cross head boundaries and reload the head's operand image."""
+    x, xd, x64 = llama_case(T=5000, H=8, seed=11)
+    oplan = orc.make_eigen_plan(x64[:1024], 2.0)
+    _check_codec(spx, orc, oplan, x64, xd, 5000)
+
+
+def test_codec_full_size_sampled(spx, orc, path):
+    """Llama-shaped layer at full size (32768 tokens x 8 heads, 2.0
+    bits/value), the launch the benchmark times: codes of 2048 sampled tokens
+    per head against the oracle's encode of those tokens (band rule), and the
+    decode of the device's own codes against the oracle's decode of the same
+    codes on those tokens."""
+    T, H = 32768, 8
+    x = synth.to_bf16_exact(synth.spiked_t(21, T, H, 128))
+    x64 = x.astype(np.float64)
+    oplan = orc.make_eigen_plan(x64[:2048], 2.0)
+    p = gpu_plan(spx, oplan)
+    xd = bf16(x).cuda()
+    codes = p.new_streams(T)
+    spx.spectra_encode(p, xd, codes)
+    out = torch.zeros((T, H, 128), device="cuda", dtype=torch.bfloat16)
+    spx.spectra_decode(p, codes, T, out)
+    torch.cuda.synchronize()
+    assert np.all(p.status.cpu().numpy() >= 0)
+    g = np.random.default_rng(5)
+    idx = np.sort(g.choice(T, size=2048, replace=False))
+    idx[:2] = [0, T - 1]
+    cc = codes.cpu().numpy()
+    outn = out.float().cpu().numpy()
+    flips = total = 0
+    for h in range(H):
+        R = int(oplan.rec_bits()[h])
+        got = orc.unpack(np.ascontiguousarray(cc[h, : orc.stream_bytes(T, R)]), T, oplan.bits[h])[idx]
+        enc = orc.encode_head(oplan, h, x64[idx, h, :])
+        diff = got != enc["codes"]
+        if diff.any():
+            assert orc.decision_margin(oplan, h, enc)[diff].max() <= BAND_SIGMA
+        flips += int(diff.sum())
+        total += diff.size
+        # decode of the device's codes for the sampled tokens
+        sub = orc.pack(got, oplan.bits[h])
+        xh = orc.decode_head(oplan, h, sub, len(idx))
+        want = synth.to_bf16_exact(xh.astype(np.float32))
+        assert rel_l2(outn[idx, h, :], want) <= REC_TOL
+    assert flips <= FLIP_FRAC * total, (flips, total)
