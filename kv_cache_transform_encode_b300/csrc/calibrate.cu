@@ -269,6 +269,354 @@ jacobi_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int 
     if (tid == 0) status[h] = converged ? sweeps : -SPECTRA_ERR_NOT_CONVERGED;
 }
 
+// ---------------------------------------------------------------------------
+// jacobi128_kernel: cyclic Jacobi for head_dim 128 with the odd-even
+// ("caterpillar") ordering, register-blocked.  Round r pairs adjacent
+// positions: (2k, 2k+1) when r is even, (2k+1, 2k+2) when r is odd.  Every
+// pair's transform is the Jacobi rotation that annihilates A[p][q] followed
+// by a swap of the two positions, so after 128 rounds (one sweep) every pair
+// of eigen-indices has met exactly once -- the odd-even transposition
+// network run with every comparator exchanging.  Because pairs are always
+// adjacent, the 128x128 matrix A and the accumulator V stay in registers:
+// thread (warp w, lane l) owns the 4x4 blocks A[4w..4w+3][4l..4l+3] and
+// V[4w..][4l..].  Column rotations that straddle two blocks take the
+// neighbour lane's column by shuffle; row rotations that straddle two warps
+// take the neighbour block row from shared memory.  The 64 rotations of a
+// round come from the diagonal band (A[i][i], A[i][i+1]), which the owners
+// of the diagonal and super-diagonal blocks publish after each round; two
+// warps turn the band into rotations while the other thirty apply the
+// previous round's rotations to V (V trails A by one round).
+// Rutishauser's form (c x - s y evaluated as x - s (y + tau x), tau =
+// s / (1 + c)) keeps the transforms orthogonal to working precision.
+constexpr int kJ2 = 128;
+
+struct Rot { float s, tau, t; };
+
+__device__ __forceinline__ Rot load_rot(const float4* prm, int k)
+{
+    const float4 v = prm[k];
+    Rot r;
+    r.s = v.x;
+    r.tau = v.y;
+    r.t = v.z;
+    return r;
+}
+
+// (x, y) <- (s x + c y, c x - s y): rotation then swap, in Rutishauser form
+__device__ __forceinline__ void rotswap(float& x, float& y, float s, float tau)
+{
+    const float xn = fmaf(s, fmaf(-tau, y, x), y);
+    const float yn = fmaf(-s, fmaf(tau, x, y), x);
+    x = xn;
+    y = yn;
+}
+
+// the same on two rows at once (packed fp32x2 FMAs)
+__device__ __forceinline__ void rotswap2(float2& x, float2& y, float s, float tau)
+{
+    const float2 S = make_float2(s, s), NS = make_float2(-s, -s);
+    const float2 T = make_float2(tau, tau), NT = make_float2(-tau, -tau);
+    const float2 u = __ffma2_rn(NT, y, x);
+    const float2 v = __ffma2_rn(T, x, y);
+    const float2 xn = __ffma2_rn(S, u, y);
+    const float2 yn = __ffma2_rn(NS, v, x);
+    x = xn;
+    y = yn;
+}
+
+// Rotation of pair (p, q) from the band: fast-math reciprocal and square
+// roots (the rotation only has to be orthogonal, which c = rsqrt(1 + t^2),
+// s = t c guarantees to a few ulp whatever small error t carries).
+__device__ __forceinline__ float4 band_rotation(float app, float aqq, float apq)
+{
+    float s = 0.f, tau = 0.f, t = 0.f;
+    if (fabsf(apq) > 1e-30f && apq * apq > 1e-20f * fabsf(app * aqq)) {
+        const float theta = __fdividef(aqq - app, 2.f * apq);
+        const float at = fabsf(theta);
+        if (at > 1e18f) {
+            t = __fdividef(0.5f, at);
+        } else {
+            const float q1 = fmaf(at, at, 1.f);
+            t = __fdividef(1.f, fmaf(q1, rsqrtf(q1), at));     // 1 / (|theta| + sqrt(theta^2 + 1))
+        }
+        t = (theta >= 0.f) ? t : -t;
+        const float c = rsqrtf(fmaf(t, t, 1.f));
+        s = t * c;
+        tau = __fdividef(s, 1.f + c);
+    }
+    return make_float4(s, tau, t, 0.f);
+}
+
+// V <- V Q for round parity `par` (columns only; V rows are independent).
+__device__ __forceinline__ void v_update(float2 (&v)[2][4], const float4* pr, bool E, int l)
+{
+    if (E) {
+        const Rot c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
+#pragma unroll
+        for (int ip = 0; ip < 2; ++ip) {
+            rotswap2(v[ip][0], v[ip][1], c0.s, c0.tau);
+            rotswap2(v[ip][2], v[ip][3], c1.s, c1.tau);
+        }
+    } else {
+        const bool lf = l > 0, rt = l < 31;
+        const Rot cm = load_rot(pr, lf ? 2 * l - 1 : 0), c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
+#pragma unroll
+        for (int ip = 0; ip < 2; ++ip) {
+            float2 vr, vl;
+            vr.x = __shfl_down_sync(0xffffffffu, v[ip][0].x, 1);
+            vr.y = __shfl_down_sync(0xffffffffu, v[ip][0].y, 1);
+            vl.x = __shfl_up_sync(0xffffffffu, v[ip][3].x, 1);
+            vl.y = __shfl_up_sync(0xffffffffu, v[ip][3].y, 1);
+            if (rt) {
+                float2 x = v[ip][3], y = vr;
+                rotswap2(x, y, c1.s, c1.tau);
+                v[ip][3] = x;
+            }
+            if (lf) {
+                float2 x = vl, y = v[ip][0];
+                rotswap2(x, y, cm.s, cm.tau);
+                v[ip][0] = y;
+            }
+            rotswap2(v[ip][1], v[ip][2], c0.s, c0.tau);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(1024, 1)
+jacobi128_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int max_sweeps,
+                 float* __restrict__ basis_out, float* __restrict__ eig_out, int32_t* __restrict__ status,
+                 float* __restrict__ gram_out)
+{
+    constexpr int D = kJ2;
+    extern __shared__ float smem[];
+    float* rowx = smem;                                   // [32][2][D] exchanged block rows
+    float* band = rowx + 32 * 2 * D;                      // [2 parity][2][D]: diag, super-diag
+    float4* prm = reinterpret_cast<float4*>(band + 4 * D);  // [2 parity][64]
+    float* red = reinterpret_cast<float*>(prm + 128);     // [33]
+
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, h = blockIdx.x;
+    // a[ip][j] = (A[4w + 2ip][4l + j], A[4w + 2ip + 1][4l + j]); v likewise
+    float2 a[2][4], v[2][4];
+#define AE(i, j) ((i) & 1 ? a[(i) >> 1][j].y : a[(i) >> 1][j].x)
+
+    // 1. G = (1/n) sum of the chunk partials (fixed order), V = I.
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = 4 * w + i, c = 4 * l + j;
+            const float* src = partials + size_t(h) * nchunks * D * D + size_t(r) * D + c;
+            float sum = 0.f;
+            for (int ch = 0; ch < nchunks; ++ch) sum += src[size_t(ch) * D * D];
+            sum *= inv_n;
+            AE(i, j) = sum;
+            ((i & 1) ? v[i >> 1][j].y : v[i >> 1][j].x) = (r == c) ? 1.f : 0.f;
+            if (gram_out) gram_out[size_t(h) * D * D + size_t(r) * D + c] = sum;
+            bad |= !isfinite(sum);
+        }
+    if (__syncthreads_or(bad)) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                basis_out[size_t(h) * D * D + size_t(4 * w + i) * D + 4 * l + j] = (4 * w + i == 4 * l + j) ? 1.f : 0.f;
+        if (tid < D) eig_out[size_t(h) * D + tid] = 0.f;
+        if (tid == 0) status[h] = -SPECTRA_ERR_NONFINITE;
+        return;
+    }
+    auto publish_band = [&](int par) {
+        float* dg = band + par * 2 * D;
+        float* sp = dg + D;
+        if (w == l) {
+            dg[4 * w + 0] = a[0][0].x; dg[4 * w + 1] = a[0][1].y;
+            dg[4 * w + 2] = a[1][2].x; dg[4 * w + 3] = a[1][3].y;
+            sp[4 * w + 0] = a[0][1].x; sp[4 * w + 1] = a[0][2].y; sp[4 * w + 2] = a[1][3].x;
+        }
+        if (l == w + 1) sp[4 * w + 3] = a[1][0].y;
+    };
+    publish_band(0);
+
+    float loc = 0.f;
+#pragma unroll
+    for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) loc += a[ip][j].x * a[ip][j].x + a[ip][j].y * a[ip][j].y;
+    const float fro = sqrtf(block_sum(loc, red));
+
+    int sweeps = 0, converged = 0, rounds = 0;
+    float prev_off = INFINITY;
+    for (;;) {
+        loc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (4 * w + i != 4 * l + j) loc = fmaf(AE(i, j), AE(i, j), loc);
+        const float off = sqrtf(block_sum(loc, red));
+        if (off <= 1e-6f * fro || fro == 0.f || (off > 0.5f * prev_off && off <= 1e-4f * fro)) {
+            converged = 1;
+            break;
+        }
+        if (sweeps >= max_sweeps) break;
+        prev_off = off;
+        ++sweeps;
+        for (int r = 0; r < D; ++r, ++rounds) {
+            const int par = r & 1;
+            const bool E = par == 0;   // pairs (2k, 2k+1)
+            __syncthreads();           // band[par] published
+            if (w < 2) {
+                const int k = tid, p = E ? 2 * k : 2 * k + 1, q = p + 1;
+                float4 rt = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q < D) {
+                    const float* dg = band + par * 2 * D;
+                    rt = band_rotation(dg[p], dg[q], dg[D + p]);
+                }
+                prm[par * 64 + k] = rt;
+            } else if (rounds > 0) {
+                v_update(v, prm + (par ^ 1) * 64, !E, l);   // previous round's rotations
+            }
+            __syncthreads();
+            if (w < 2 && rounds > 0) v_update(v, prm + (par ^ 1) * 64, !E, l);
+            const float4* pr = prm + par * 64;
+            if (E) {
+                const Rot r0 = load_rot(pr, 2 * w), r1 = load_rot(pr, 2 * w + 1);     // rows
+                const Rot c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);     // columns
+                float d00 = 0.f, d11 = 0.f, d01 = 0.f, d22 = 0.f, d33 = 0.f, d23 = 0.f;
+                if (w == l) {
+                    d00 = a[0][0].x; d11 = a[0][1].y; d01 = a[0][1].x;
+                    d22 = a[1][2].x; d33 = a[1][3].y; d23 = a[1][3].x;
+                }
+#pragma unroll
+                for (int ip = 0; ip < 2; ++ip) {
+                    rotswap2(a[ip][0], a[ip][1], c0.s, c0.tau);
+                    rotswap2(a[ip][2], a[ip][3], c1.s, c1.tau);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    rotswap(a[0][j].x, a[0][j].y, r0.s, r0.tau);
+                    rotswap(a[1][j].x, a[1][j].y, r1.s, r1.tau);
+                }
+                if (w == l) {   // diagonal sub-blocks: exact values
+                    a[0][0].x = fmaf(r0.t, d01, d11); a[0][1].y = fmaf(-r0.t, d01, d00);
+                    a[0][1].x = 0.f; a[0][0].y = 0.f;
+                    a[1][2].x = fmaf(r1.t, d23, d33); a[1][3].y = fmaf(-r1.t, d23, d22);
+                    a[1][3].x = 0.f; a[1][2].y = 0.f;
+                }
+            } else {
+                const bool up = w > 0, dn = w < 31, lf = l > 0, rt = l < 31;
+                const Rot cm = load_rot(pr, lf ? 2 * l - 1 : 0), c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
+                float d11 = 0.f, d22 = 0.f, d12 = 0.f;
+                if (w == l) { d11 = a[0][1].y; d22 = a[1][2].x; d12 = a[0][2].y; }
+                // columns: (4l-1, 4l) with the left lane, (4l+1, 4l+2) inside, (4l+3, 4l+4) with the right lane
+#pragma unroll
+                for (int ip = 0; ip < 2; ++ip) {
+                    float2 ar, al;
+                    ar.x = __shfl_down_sync(0xffffffffu, a[ip][0].x, 1);
+                    ar.y = __shfl_down_sync(0xffffffffu, a[ip][0].y, 1);
+                    al.x = __shfl_up_sync(0xffffffffu, a[ip][3].x, 1);
+                    al.y = __shfl_up_sync(0xffffffffu, a[ip][3].y, 1);
+                    if (rt) {
+                        float2 x = a[ip][3], y = ar;
+                        rotswap2(x, y, c1.s, c1.tau);
+                        a[ip][3] = x;
+                    }
+                    if (lf) {
+                        float2 x = al, y = a[ip][0];
+                        rotswap2(x, y, cm.s, cm.tau);
+                        a[ip][0] = y;
+                    }
+                    rotswap2(a[ip][1], a[ip][2], c0.s, c0.tau);
+                }
+                // rows: (4w-1, 4w) and (4w+3, 4w+4) through shared memory
+                float* mine = rowx + w * 2 * D + 4 * l;
+                *reinterpret_cast<float4*>(mine) = make_float4(a[0][0].x, a[0][1].x, a[0][2].x, a[0][3].x);
+                *reinterpret_cast<float4*>(mine + D) = make_float4(a[1][0].y, a[1][1].y, a[1][2].y, a[1][3].y);
+                __syncthreads();
+                const Rot rm = load_rot(pr, up ? 2 * w - 1 : 0), r0 = load_rot(pr, 2 * w), r1 = load_rot(pr, 2 * w + 1);
+                if (dn) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(rowx + (w + 1) * 2 * D + 4 * l);
+                    const float bl[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a[1][j].y = fmaf(r1.s, fmaf(-r1.tau, bl[j], a[1][j].y), bl[j]);
+                }
+                if (up) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(rowx + (w - 1) * 2 * D + D + 4 * l);
+                    const float ab[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a[0][j].x = fmaf(-rm.s, fmaf(rm.tau, ab[j], a[0][j].x), ab[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) rotswap(a[0][j].y, a[1][j].x, r0.s, r0.tau);
+                if (w == l) {
+                    a[0][1].y = fmaf(r0.t, d12, d22); a[1][2].x = fmaf(-r0.t, d12, d11);
+                    a[0][2].y = 0.f; a[1][1].x = 0.f;
+                }
+            }
+            publish_band(par ^ 1);
+        }
+    }
+    if (rounds > 0) {   // V trails A by one round: apply the last one
+        __syncthreads();
+        v_update(v, prm + ((rounds - 1) & 1) * 64, ((rounds - 1) & 1) == 0, l);
+    }
+
+    // 2. Sort descending (ties: lower position first), sign-fix, write out.
+    __syncthreads();
+    constexpr int LD = D + 1;
+    float* Vs = smem;                 // [D][LD]
+    float* lam = Vs + D * LD;         // [D]
+    int* rank = reinterpret_cast<int*>(lam + D);
+#pragma unroll
+    for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            Vs[(4 * w + 2 * ip) * LD + 4 * l + j] = v[ip][j].x;
+            Vs[(4 * w + 2 * ip + 1) * LD + 4 * l + j] = v[ip][j].y;
+        }
+    if (w == l) {
+        lam[4 * w + 0] = a[0][0].x; lam[4 * w + 1] = a[0][1].y;
+        lam[4 * w + 2] = a[1][2].x; lam[4 * w + 3] = a[1][3].y;
+    }
+#undef AE
+    __syncthreads();
+    if (tid < D) {
+        const float li = lam[tid];
+        int rk = 0;
+        for (int j = 0; j < D; ++j) {
+            const float lj = lam[j];
+            rk += (lj > li) || (lj == li && j < tid);
+        }
+        rank[tid] = rk;
+    }
+    __syncthreads();
+    for (int i = w; i < D; i += 32) {
+        float best = -1.f;
+        int br = 0;
+        for (int rr = l; rr < D; rr += 32) {
+            const float av = fabsf(Vs[rr * LD + i]);
+            if (av > best) { best = av; br = rr; }
+        }
+        for (int o = 16; o; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int orr = __shfl_xor_sync(0xffffffffu, br, o);
+            if (ob > best || (ob == best && orr < br)) { best = ob; br = orr; }
+        }
+        const float sgn = (Vs[br * LD + i] < 0.f) ? -1.f : 1.f;
+        const int c = rank[i];
+        for (int rr = l; rr < D; rr += 32) basis_out[size_t(h) * D * D + size_t(rr) * D + c] = sgn * Vs[rr * LD + i];
+        if (l == 0) eig_out[size_t(h) * D + c] = lam[i];
+    }
+    if (tid == 0) status[h] = converged ? sweeps : -SPECTRA_ERR_NOT_CONVERGED;
+}
+
+size_t jacobi128_smem()
+{
+    const size_t work = sizeof(float) * (32 * 2 * kJ2 + 4 * kJ2) + sizeof(float4) * 128 + sizeof(float) * 33;
+    const size_t fin = sizeof(float) * (kJ2 * (kJ2 + 1) + kJ2) + sizeof(int) * kJ2;
+    return (work > fin ? work : fin) + 16;
+}
+
 template <int D>
 size_t jacobi_smem()
 {
@@ -303,10 +651,10 @@ spectra_status launch_jacobi(const spectra_plan* plan, const float* partials, in
 {
     const float inv_n = 1.0f / float(n_cal);
     if (plan->head_dim == 128) {
-        const size_t sm = jacobi_smem<128>();
-        cudaFuncSetAttribute(jacobi_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-        jacobi_kernel<128><<<plan->heads, kJacobiThreads, sm, s>>>(
-            partials, nchunks, inv_n, max_sweeps, plan->basis_mat, plan->eigvals, plan->status, gram_out);
+        const size_t sm = jacobi128_smem();
+        cudaFuncSetAttribute(jacobi128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        jacobi128_kernel<<<plan->heads, 1024, sm, s>>>(partials, nchunks, inv_n, max_sweeps, plan->basis_mat,
+                                                       plan->eigvals, plan->status, gram_out);
     } else {
         const size_t sm = jacobi_smem<64>();
         cudaFuncSetAttribute(jacobi_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
