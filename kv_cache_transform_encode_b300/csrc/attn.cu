@@ -17,6 +17,7 @@
 
 #include <cuda_bf16.h>
 #include <math.h>
+#include <stdlib.h>
 
 namespace spectra {
 
@@ -206,8 +207,11 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
     }
 }
 
+// code_domain: the partials hold sum_t p_t code_c(t) (tensor-core path,
+// uniform quantizer); the merged value is dequantized as
+// Delta_c (code_mean + (1 - 2^b) / 2) before the rotation.
 __global__ void attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsplit,
-                                    float* __restrict__ out)
+                                    int code_domain, float* __restrict__ out)
 {
     const int D = vp.d;
     const int bj = blockIdx.x, j = bj % Hq;
@@ -233,7 +237,12 @@ __global__ void attn_combine_kernel(PlanView vp, const float* __restrict__ part,
             const float m = pp[int64_t(s) * (D + 2)];
             if (m != -INFINITY) a += pp[int64_t(s) * (D + 2) + 2 + c] * __expf(m - sM);
         }
-        os[c] = (sL > 0.f) ? a / sL : 0.f;
+        float y = (sL > 0.f) ? a / sL : 0.f;
+        if (code_domain) {
+            const int bc = vp.bits[size_t(h) * D + c];
+            y = (bc > 0) ? vp.rscale[size_t(h) * D + c] * (y + 0.5f * (1.f - float(1 << bc))) : 0.f;
+        }
+        os[c] = y;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < D; i += blockDim.x) {
@@ -253,13 +262,27 @@ size_t split_smem()
 
 int nsplit_of(int64_t ctx) { return int((ctx + kSplitLen - 1) / kSplitLen); }
 
+// kernel family, as for encode/decode: SPECTRA_PATH=generic / tc / unset
+char attn_path()
+{
+    const char* e = getenv("SPECTRA_PATH");
+    return (e && (e[0] == 'g' || e[0] == 't')) ? e[0] : 'a';
+}
+
 }  // namespace
 
+size_t attn_tc_extra_bytes(int B, int Hkv);   // attn_tc.cu
+spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vplan, const void* q, int q_dt,
+                              int B, int Hq, const uint8_t* kc, const uint8_t* vc, int64_t sstride, int64_t ctx,
+                              float scale, float* part, int nsplit, int split_len, void* extra,
+                              cudaStream_t s, bool* done);
+
+// [qt (B Hq d f32) | split partials | tensor-core operands (sized for Hkv <= Hq)]
 size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx)
 {
     const size_t qt = align256(sizeof(float) * size_t(B) * Hq * d);
     const size_t part = align256(sizeof(float) * size_t(B) * Hq * nsplit_of(ctx) * (d + 2));
-    return qt + part;
+    return qt + part + attn_tc_extra_bytes(B, Hq);
 }
 
 spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
@@ -275,6 +298,18 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
     float* qt = static_cast<float*>(ws);
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                            align256(sizeof(float) * size_t(B) * Hq * D));
+    void* extra = reinterpret_cast<uint8_t*>(part) + align256(sizeof(float) * size_t(B) * Hq * nsplit * (D + 2));
+    if (attn_path() != 'g') {
+        bool done = false;
+        spectra_status st = launch_attn_tc(kplan, vplan, q, q_dt, B, Hq, kc, vc, sstride, ctx, scale, part, nsplit,
+                                           kSplitLen, extra, s, &done);
+        if (st) return st;
+        if (done) {
+            attn_combine_kernel<<<B * Hq, D, D * sizeof(float), s>>>(vp, part, Hq, nsplit, 1, out);
+            return cuda_status(cudaGetLastError());
+        }
+        if (attn_path() == 't') return SPECTRA_ERR_UNSUPPORTED;
+    }
     attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt);
     dim3 grid(nsplit, Hkv, B);
     if (D == 128) {
@@ -288,7 +323,7 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
         attn_split_kernel<64><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
                                                          nstride, nsplit, part);
     }
-    attn_combine_kernel<<<B * Hq, D, D * sizeof(float), s>>>(vp, part, Hq, nsplit, out);
+    attn_combine_kernel<<<B * Hq, D, D * sizeof(float), s>>>(vp, part, Hq, nsplit, 0, out);
     return cuda_status(cudaGetLastError());
 }
 

@@ -1,0 +1,468 @@
+// attn_tc.cu -- decode-step attention over packed K/V streams on the tensor
+// cores (uniform quantizer, eigenbasis plans, head_dim 128, at most four
+// query heads per kv head).
+//
+// "Sintesi Tecnica: SPECTRA", "Significato e Rivendicazioni": attention
+// computed directly in the latent space.  With the uniform quantizer a
+// latent coordinate is yhat_c = (Delta_c / 2)(2 code_c + 1 - 2^b_c), affine
+// in the code, so
+//   s_j(t) = sum_c qt_jc yhat_c(t) = sum_c W_jc code_c(t) + K0_j,
+//   W_jc = qt_jc Delta_c,   K0_j = sum_c qt_jc (Delta_c / 2)(1 - 2^b_c),
+//   sum_t p_j(t) yhat_c(t) = Delta_c (sum_t p_j(t) code_c(t) + (1 - 2^b_c) l_j / 2),
+// and both contractions run on integer codes.  A code enters the tensor
+// core as the fp16 number 1024 + code (exact: the code lands in the low
+// mantissa bits, one byte-permute per two codes); after every 16-wide MMA
+// step the 1024 offsets are taken out again with the sums of the other
+// operand, so rounding stays relative to a 16-term partial sum.  W and P enter as fp16
+// hi + lo pairs (22 significand bits), so the products carry fp32-grade
+// accuracy.
+//
+// One CTA per (context split, kv head, batch).  Per 128-token tile:
+//  1. the tile's K and V code words arrive in shared memory (cp.async,
+//     double-buffered);
+//  2. eight warps unpack them, one channel per lane (the bit-plane words of
+//     a 32-token group become 32 code bytes through four 8x8 bit
+//     transposes), into fp16 tiles L[c][t];
+//  3. scores: mma.sync m16n8k16, A = L_K^T (ldmatrix.trans), B = [W_hi; W_lo]
+//     (n = head, hi/lo), one 16-token slice per warp;
+//  4. online softmax per head (warps 0..3);
+//  5. P V: mma.sync, A = L_V (channels x tokens), B = [P_hi; P_lo], one
+//     16-channel slice per warp, accumulated over the split in registers.
+// The split's (m, l, sum_t p code) go to the workspace; the combine kernel
+// of attn.cu merges splits, dequantizes and rotates by the V basis.
+#include "spectra_internal.cuh"
+
+#include <cuda_fp16.h>
+#include <math.h>
+
+namespace spectra {
+
+namespace {
+
+constexpr int D = 128;
+constexpr int TT = 128;                  // tokens per tile
+constexpr int LROW = TT * 2 + 16;        // bytes per L row (padded: conflict-free ldmatrix)
+constexpr int kThreads = 256;
+constexpr int kGmax = 4;                 // query heads per kv head
+constexpr float kOff = 1024.f;           // fp16 1024 + code
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void transpose8(uint32_t& lo, uint32_t& hi)
+{
+    uint32_t t;
+    t = (lo ^ (lo >> 7)) & 0x00AA00AAu;  lo ^= t ^ (t << 7);
+    t = (hi ^ (hi >> 7)) & 0x00AA00AAu;  hi ^= t ^ (t << 7);
+    t = (lo ^ (lo >> 14)) & 0x0000CCCCu; lo ^= t ^ (t << 14);
+    t = (hi ^ (hi >> 14)) & 0x0000CCCCu; hi ^= t ^ (t << 14);
+    t = (lo ^ (hi << 4)) & 0xF0F0F0F0u;  lo ^= t;  hi ^= t >> 4;
+}
+
+__device__ __forceinline__ uint32_t gather_byte(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int k)
+{
+    const uint32_t sel = ((4u + k) << 4) | uint32_t(k);
+    return __byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410);
+}
+
+// bit planes of one channel for a 32-token group -> 32 code bytes
+__device__ __forceinline__ void planes_to_codes(const uint32_t* words, int o, int b, int bmax, uint32_t (&X)[8])
+{
+    uint32_t pl[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pl[k] = (k < bmax && k < b) ? words[o + k] : 0u;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        X[2 * m] = gather_byte(pl[0], pl[1], pl[2], pl[3], m);
+        X[2 * m + 1] = gather_byte(pl[4], pl[5], pl[6], pl[7], m);
+        transpose8(X[2 * m], X[2 * m + 1]);
+    }
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// D (16x8 f32) = A (16x16 f16, row) * B (16x8 f16, col) + C
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                         const float (&c)[4])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
+{
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------ prep
+// Per (batch, kv head): qt_j = scale * B_K^T q_j, W_jc = qt_jc Delta_c as fp16
+// hi/lo rows ([8][D]: rows 0..3 hi, 4..7 lo; heads >= G zero), the sums of
+// each row over every 16-channel chunk (the 1024 offsets removed per MMA
+// step), and K0_j.
+__global__ void __launch_bounds__(D)
+attn_tc_prep_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, int G, float scale,
+                    __half* __restrict__ wimg, float* __restrict__ bias, float* __restrict__ wsum16)
+{
+    const int bh = blockIdx.x, Hkv = kp.heads, h = bh % Hkv, b = bh / Hkv;
+    const int c = threadIdx.x;
+    __shared__ float qs[kGmax][D];
+    __shared__ float red[kGmax][4];
+    for (int e = c; e < G * D; e += D) qs[e / D][e % D] = load_elem(q, q_dt, (int64_t(b) * Hq + h * G + e / D) * D + e % D);
+    __syncthreads();
+    const int bits = kp.bits[size_t(h) * D + c];
+    const float delta = kp.rscale[size_t(h) * D + c];
+    __half* wr = wimg + size_t(bh) * 8 * D;
+    float* wsr = wsum16 + size_t(bh) * 8 * 8;           // [kb][n]
+    for (int j = 0; j < kGmax; ++j) {
+        float qt = 0.f;
+        if (j < G)
+            for (int i = 0; i < D; ++i) qt = fmaf(kp.basis_mat[(size_t(h) * D + i) * D + c], qs[j][i], qt);
+        qt *= scale;
+        const float w = (bits > 0 && j < G) ? qt * delta : 0.f;
+        const __half hi = __float2half_rn(w);
+        const __half lo = __float2half_rn(w - __half2float(hi));
+        wr[j * D + c] = hi;
+        wr[(kGmax + j) * D + c] = lo;
+        float sh = __half2float(hi), sl = __half2float(lo);
+        for (int o = 8; o; o >>= 1) {            // 16-channel chunk sums
+            sh += __shfl_xor_sync(0xffffffffu, sh, o);
+            sl += __shfl_xor_sync(0xffffffffu, sl, o);
+        }
+        if ((c & 15) == 0) {
+            wsr[(c >> 4) * 8 + j] = sh;
+            wsr[(c >> 4) * 8 + kGmax + j] = sl;
+        }
+        float k0 = (bits > 0 && j < G) ? qt * 0.5f * delta * (1.f - float(1 << bits)) : 0.f;
+        for (int o = 16; o; o >>= 1) k0 += __shfl_xor_sync(0xffffffffu, k0, o);
+        if ((c & 31) == 0) red[j][c >> 5] = k0;
+    }
+    __syncthreads();
+    if (c < kGmax) bias[size_t(bh) * kGmax + c] = red[c][0] + red[c][1] + red[c][2] + red[c][3];
+}
+
+// ------------------------------------------------------------------ split
+struct AttnTcParams {
+    PlanView kp, vp;
+    int Hq, G, nsplit, split_len;
+    int64_t ctx;
+    const uint8_t* kc;
+    const uint8_t* vc;
+    int64_t sstride;
+    const __half* wimg;
+    const float* bias;
+    const float* wsum16;
+    float* part;
+    uint32_t kbytes, vbytes;   // code-word bytes of one tile (16 R)
+};
+
+__global__ void __launch_bounds__(kThreads, 2)
+attn_tc_split_kernel(AttnTcParams P)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int Hkv = P.kp.heads, G = P.G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int bh = b * Hkv + h;
+
+    uint8_t* cw = smem;                                          // [2][kbytes + vbytes]
+    const uint32_t cwb = P.kbytes + P.vbytes;
+    uint8_t* Lk = cw + 2 * cwb;                                  // [D][LROW]
+    uint8_t* Lv = Lk + D * LROW;                                 // [D][LROW]
+    float* S = reinterpret_cast<float*>(Lv + D * LROW);          // [kGmax][TT]
+    __half* Pm = reinterpret_cast<__half*>(S + kGmax * TT);      // [8][TT + 8]
+    float* st_m = reinterpret_cast<float*>(Pm + 8 * (TT + 8));   // [kGmax]
+    float* st_l = st_m + kGmax;
+    float* st_a = st_l + kGmax;                                  // alpha of this tile
+    float* ps16 = st_a + kGmax;                                  // [8 chunks][8 rows] p sums
+
+    const int64_t t_begin = int64_t(split) * P.split_len;
+    const int64_t t_end = min(P.ctx, t_begin + P.split_len);
+    const int ntiles = int((t_end - t_begin + TT - 1) / TT);
+    // records larger than the plans' bound are not read (their streams were sized by the bound)
+    const int RK0 = P.kp.rec_bits[h], RV0 = P.vp.rec_bits[h];
+    const int RK = RK0 <= P.kp.max_rec_bits ? RK0 : 0, RV = RV0 <= P.vp.max_rec_bits ? RV0 : 0;
+    const int64_t sid = int64_t(b) * Hkv + h;
+    const uint8_t* ks = P.kc + sid * P.sstride;
+    const uint8_t* vs = P.vc + sid * P.sstride;
+
+    // unpack role: side (K for warps 0-3, V for 4-7), channel
+    const int side = warp >> 2, uc = (warp & 3) * 32 + lane;
+    const PlanView& up = side ? P.vp : P.kp;
+    const int ub = up.bits[size_t(h) * D + uc];
+    const int uo = up.chan_off[size_t(h) * D + uc];
+    const int ubmax = __reduce_max_sync(0xffffffffu, ub);
+    const int uR = side ? RV : RK;
+
+    // score operand B: W rows (n = g8: 0..3 hi, 4..7 lo), k = 16 kb + 2 tig (+8)
+    uint32_t wf[8][2];
+    {
+        const __half* wr = P.wimg + size_t(bh) * 8 * D + g8 * D;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+            wf[kb][0] = *reinterpret_cast<const uint32_t*>(wr + kb * 16 + 2 * tig);
+            wf[kb][1] = *reinterpret_cast<const uint32_t*>(wr + kb * 16 + 8 + 2 * tig);
+        }
+    }
+    const float bias0 = P.bias[size_t(bh) * kGmax + ((2 * tig) & 3)];
+    const float bias1 = P.bias[size_t(bh) * kGmax + ((2 * tig + 1) & 3)];
+    float oacc[4] = {0.f, 0.f, 0.f, 0.f};     // (channel g8 / g8+8, column n = 2 tig / 2 tig + 1)
+    if (tid < kGmax) { st_m[tid] = -INFINITY; st_l[tid] = 0.f; }
+
+    auto issue_load = [&](int tile, int buf) {
+        const int64_t t0 = t_begin + int64_t(tile) * TT;
+        const int64_t ng = min(int64_t(4), (t_end - t0 + 31) / 32);
+        const uint32_t nk = uint32_t((ng * 4 * RK + 15) / 16), nv = uint32_t((ng * 4 * RV + 15) / 16);
+        uint8_t* dst = cw + buf * cwb;
+        const uint8_t* srck = ks + (t0 / 32) * 4 * RK;
+        const uint8_t* srcv = vs + (t0 / 32) * 4 * RV;
+        for (uint32_t i = tid; i < nk + nv; i += kThreads) {
+            if (i < nk) cp_async16(dst + 16 * i, srck + 16 * i);
+            else cp_async16(dst + P.kbytes + 16 * (i - nk), srcv + 16 * (i - nk));
+        }
+        cp_async_commit();
+    };
+    if (ntiles > 0) issue_load(0, 0);
+
+    for (int tile = 0; tile < ntiles; ++tile) {
+        const int buf = tile & 1;
+        const int64_t t0 = t_begin + int64_t(tile) * TT;
+        cp_async_wait_all();
+        __syncthreads();                                   // code words landed; previous tile done
+        if (tile + 1 < ntiles) issue_load(tile + 1, buf ^ 1);
+
+        // ---- unpack: one channel per lane, four 32-token groups
+        {
+            const uint32_t* words = reinterpret_cast<const uint32_t*>(cw + buf * cwb + (side ? P.kbytes : 0));
+            uint8_t* L = side ? Lv : Lk;
+            uint8_t* row = L + uc * LROW;
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+                uint32_t X[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if (t0 + 32 * g < t_end && uR > 0) planes_to_codes(words + g * uR, uo, ub, ubmax, X);
+                uint32_t v[16];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    v[2 * m] = __byte_perm(X[m], 0x6464u, 0x5140);       // tokens 4m, 4m+1 -> fp16 1024 + code
+                    v[2 * m + 1] = __byte_perm(X[m], 0x6464u, 0x5342);   // tokens 4m+2, 4m+3
+                }
+                uint4* dst = reinterpret_cast<uint4*>(row + g * 64);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            }
+        }
+        __syncthreads();
+
+        // ---- scores: warp -> tokens 16 warp .. +15
+        {
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+            const int mi = lane >> 3, ri = lane & 7;
+            const float* wsr = P.wsum16 + size_t(bh) * 64;
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) {
+                uint32_t a[4];
+                const int k = kb * 16 + (mi >> 1) * 8 + ri, m = warp * 16 + (mi & 1) * 8;
+                ldsm_x4_t(smem_addr(Lk + k * LROW + m * 2), a);
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(d, a, wf[kb][0], wf[kb][1], d);
+                const float o0 = kOff * wsr[kb * 8 + 2 * tig], o1 = kOff * wsr[kb * 8 + 2 * tig + 1];
+                sacc[0] += d[0] - o0; sacc[1] += d[1] - o1; sacc[2] += d[2] - o0; sacc[3] += d[3] - o1;
+            }
+            // lanes tig 0/1 hold hi heads 2 tig, 2 tig + 1; lanes tig 2/3 the lo parts
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[e] += __shfl_xor_sync(0xffffffffu, sacc[e], 2);
+            if (tig < 2) {
+                const int j0 = 2 * tig, j1 = 2 * tig + 1;
+                const int ta = warp * 16 + g8, tb = ta + 8;
+                const bool la = t0 + ta < t_end, lb = t0 + tb < t_end;
+                if (j0 < G) {
+                    S[j0 * TT + ta] = la ? sacc[0] + bias0 : -INFINITY;
+                    S[j0 * TT + tb] = lb ? sacc[2] + bias0 : -INFINITY;
+                }
+                if (j1 < G) {
+                    S[j1 * TT + ta] = la ? sacc[1] + bias1 : -INFINITY;
+                    S[j1 * TT + tb] = lb ? sacc[3] + bias1 : -INFINITY;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- online softmax: warp j < G handles head j
+        if (warp < kGmax) {
+            const int j = warp;
+            float s[4];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                s[i] = (j < G) ? S[j * TT + lane + 32 * i] : -INFINITY;
+                mx = fmaxf(mx, s[i]);
+            }
+            for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float mold = st_m[j];
+            const float mnew = fmaxf(mold, mx);
+            const float alpha = (mold == -INFINITY) ? 0.f : __expf(mold - mnew);
+            float ptot = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float p = (s[i] == -INFINITY) ? 0.f : __expf(s[i] - mnew);
+                const __half ph = __float2half_rn(p);
+                const __half pl = __float2half_rn(p - __half2float(ph));
+                const int t = lane + 32 * i;
+                Pm[j * (TT + 8) + t] = ph;
+                Pm[(kGmax + j) * (TT + 8) + t] = pl;
+                float sh = __half2float(ph), sl = __half2float(pl);
+                ptot += sh + sl;
+                // per 16-token chunk sums of the hi and lo rows (chunk = t / 16)
+                for (int o = 8; o; o >>= 1) {
+                    sh += __shfl_xor_sync(0xffffffffu, sh, o);
+                    sl += __shfl_xor_sync(0xffffffffu, sl, o);
+                }
+                if ((lane & 15) == 0) {
+                    ps16[(2 * i + (lane >> 4)) * 8 + j] = sh;
+                    ps16[(2 * i + (lane >> 4)) * 8 + kGmax + j] = sl;
+                }
+            }
+            for (int o = 16; o; o >>= 1) ptot += __shfl_xor_sync(0xffffffffu, ptot, o);
+            if (lane == 0) {
+                st_l[j] = st_l[j] * alpha + ptot;
+                st_m[j] = mnew;
+                st_a[j] = alpha;
+            }
+        } else if (warp < 2 * kGmax && warp - kGmax >= 0) {
+            // zero P rows of absent heads (G < 4) so the MMA sees zeros
+            const int j = warp - kGmax;
+            if (j >= G) {
+                for (int t = lane; t < TT; t += 32) {
+                    Pm[j * (TT + 8) + t] = __float2half_rn(0.f);
+                    Pm[(kGmax + j) * (TT + 8) + t] = __float2half_rn(0.f);
+                }
+                if (lane < 8) { ps16[lane * 8 + j] = 0.f; ps16[lane * 8 + kGmax + j] = 0.f; }
+                if (lane == 0) st_a[j] = 0.f;
+            }
+        }
+        __syncthreads();
+
+        // ---- P V: warp -> channels 16 warp .. +15; each column n (head hi/lo)
+        // accumulated on its own, offsets removed per 16-token chunk
+        {
+            const int mi = lane >> 3, ri = lane & 7;
+            const float a0 = st_a[(2 * tig) & 3], a1 = st_a[(2 * tig + 1) & 3];
+            oacc[0] *= a0; oacc[1] *= a1; oacc[2] *= a0; oacc[3] *= a1;
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) {
+                uint32_t a[4];
+                const int m = warp * 16 + (mi & 1) * 8 + ri, k = kb * 16 + (mi >> 1) * 8;
+                ldsm_x4(smem_addr(Lv + m * LROW + k * 2), a);
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(Pm + g8 * (TT + 8) + kb * 16 + 2 * tig);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(Pm + g8 * (TT + 8) + kb * 16 + 8 + 2 * tig);
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(d, a, b0, b1, d);
+                const float s0 = kOff * ps16[kb * 8 + 2 * tig], s1 = kOff * ps16[kb * 8 + 2 * tig + 1];
+                oacc[0] += d[0] - s0; oacc[1] += d[1] - s1; oacc[2] += d[2] - s0; oacc[3] += d[3] - s1;
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 4; ++e) oacc[e] += __shfl_xor_sync(0xffffffffu, oacc[e], 2);   // hi + lo
+
+    // partials: [(b Hq + h G + j) nsplit + split][2 + D]: m, l, sum_t p code
+    if (tig < 2) {
+        const int j0 = 2 * tig, j1 = 2 * tig + 1;
+        const int c0 = warp * 16 + g8, c1 = c0 + 8;
+        auto base = [&](int j) { return P.part + ((int64_t(b) * P.Hq + h * G + j) * P.nsplit + split) * (D + 2); };
+        if (j0 < G) { base(j0)[2 + c0] = oacc[0]; base(j0)[2 + c1] = oacc[2]; }
+        if (j1 < G) { base(j1)[2 + c0] = oacc[1]; base(j1)[2 + c1] = oacc[3]; }
+    }
+    if (tid < G) {
+        float* bp = P.part + ((int64_t(b) * P.Hq + h * G + tid) * P.nsplit + split) * (D + 2);
+        bp[0] = ntiles > 0 ? st_m[tid] : -INFINITY;
+        bp[1] = ntiles > 0 ? st_l[tid] : 0.f;
+    }
+}
+
+size_t tc_split_smem(uint32_t kbytes, uint32_t vbytes)
+{
+    return 2 * size_t(kbytes + vbytes) + 2 * size_t(D) * LROW + sizeof(float) * kGmax * TT +
+           sizeof(__half) * 8 * (TT + 8) + sizeof(float) * (3 * kGmax + 8 * 8) + 64;
+}
+
+}  // namespace
+
+// Workspace layout of the tensor-core path (inside attn_workspace_bytes):
+// [partials | wimg (B Hkv 8 D fp16) | bias (B Hkv 4 f32) | wsum16 (B Hkv 64 f32)].
+size_t attn_tc_extra_bytes(int B, int Hkv)
+{
+    return align256(sizeof(__half) * size_t(B) * Hkv * 8 * D) + align256(sizeof(float) * size_t(B) * Hkv * kGmax) +
+           align256(sizeof(float) * size_t(B) * Hkv * 64);
+}
+
+spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vplan, const void* q, int q_dt, int B,
+                              int Hq, const uint8_t* kc, const uint8_t* vc, int64_t sstride, int64_t ctx,
+                              float scale, float* part, int nsplit, int split_len, void* extra,
+                              cudaStream_t s, bool* done)
+{
+    *done = false;
+    const int Hkv = kplan->heads, G = Hq / Hkv;
+    if (kplan->head_dim != D || G > kGmax) return SPECTRA_OK;
+    if (kplan->basis != SPECTRA_BASIS_EIGEN || vplan->basis != SPECTRA_BASIS_EIGEN) return SPECTRA_OK;
+    if (kplan->quant != SPECTRA_Q_UNIFORM3S || vplan->quant != SPECTRA_Q_UNIFORM3S) return SPECTRA_OK;
+    if (split_len % TT != 0) return SPECTRA_OK;
+    AttnTcParams P;
+    P.kp = make_view(kplan);
+    P.vp = make_view(vplan);
+    P.Hq = Hq;
+    P.G = G;
+    P.nsplit = nsplit;
+    P.split_len = split_len;
+    P.ctx = ctx;
+    P.kc = kc;
+    P.vc = vc;
+    P.sstride = sstride;
+    __half* wimg = static_cast<__half*>(extra);
+    float* bias = reinterpret_cast<float*>(static_cast<uint8_t*>(extra) +
+                                           align256(sizeof(__half) * size_t(B) * Hkv * 8 * D));
+    float* wsum16 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bias) +
+                                             align256(sizeof(float) * size_t(B) * Hkv * kGmax));
+    P.wimg = wimg;
+    P.bias = bias;
+    P.wsum16 = wsum16;
+    P.part = part;
+    P.kbytes = uint32_t(16 * (kplan->max_rec_bits > 0 ? kplan->max_rec_bits : 1));
+    P.vbytes = uint32_t(16 * (vplan->max_rec_bits > 0 ? vplan->max_rec_bits : 1));
+    const size_t sm = tc_split_smem(P.kbytes, P.vbytes);
+    if (sm > 227 * 1024) return SPECTRA_OK;
+    attn_tc_prep_kernel<<<B * Hkv, D, 0, s>>>(P.kp, q, q_dt, Hq, G, scale, wimg, bias, wsum16);
+    cudaFuncSetAttribute(attn_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    dim3 grid(nsplit, Hkv, B);
+    attn_tc_split_kernel<<<grid, kThreads, sm, s>>>(P);
+    *done = true;
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace spectra

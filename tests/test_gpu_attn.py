@@ -12,6 +12,14 @@ from parity import ATTN_TOL, gpu_plan, rel_l2
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["tc", "generic"])
+def path(request, monkeypatch):
+    """Kernel family for uniform-quantizer eigenbasis plans: the tensor-core
+    kernels (required) or the CUDA-core kernels."""
+    monkeypatch.setenv("SPECTRA_PATH", request.param)
+    return request.param
+
+
 @pytest.fixture(scope="module")
 def spx():
     import kv_cache_transform_encode_b300 as spx
@@ -72,15 +80,27 @@ def _run(spx, orc, B, Hq, Hkv, ctx, kind="eigen", quant=0, B_bits=2.0, scale=1.0
 
 
 @pytest.mark.parametrize("ctx", [1, 100, 2048, 4500])
-def test_attn_uniform_gqa(spx, orc, ctx):
+def test_attn_uniform_gqa(spx, orc, path, ctx):
     got, want = _run(spx, orc, B=2, Hq=8, Hkv=2, ctx=ctx)
     assert rel_l2(got, want) <= ATTN_TOL, rel_l2(got, want)
 
 
-def test_attn_lloyd_and_budgets(spx, orc):
+def test_attn_lloyd(spx, orc):
     got, want = _run(spx, orc, B=1, Hq=4, Hkv=1, ctx=3000, quant=1, B_bits=1.33)
     assert rel_l2(got, want) <= ATTN_TOL
-    got, want = _run(spx, orc, B=1, Hq=4, Hkv=1, ctx=1500, quant=0, B_bits=4.0)
+
+
+@pytest.mark.parametrize("B_bits", [4.0, 1.33, 8.0])
+def test_attn_uniform_budgets(spx, orc, path, B_bits):
+    """Other budgets, including 8-bit channels (codes up to 255)."""
+    got, want = _run(spx, orc, B=1, Hq=4, Hkv=1, ctx=1500, quant=0, B_bits=B_bits)
+    assert rel_l2(got, want) <= ATTN_TOL
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_attn_small_groups(spx, orc, path, G):
+    """Fewer query heads per kv head than the tensor-core tile holds."""
+    got, want = _run(spx, orc, B=2, Hq=2 * G, Hkv=2, ctx=700)
     assert rel_l2(got, want) <= ATTN_TOL
 
 
@@ -89,10 +109,43 @@ def test_attn_rwht(spx, orc):
     assert rel_l2(got, want) <= ATTN_TOL
 
 
-def test_attn_peaky_scores(spx, orc):
+def test_attn_peaky_scores(spx, orc, path):
     """Sharper softmax (scale 4 on N(0,1/d) queries): still within tolerance."""
     got, want = _run(spx, orc, B=1, Hq=8, Hkv=2, ctx=2500, scale=4.0)
     assert rel_l2(got, want) <= ATTN_TOL
+
+
+def test_attn_full_layer_sampled(spx, orc, monkeypatch):
+    """The benchmark's attention launch (1 x 32 query heads over 8 kv heads,
+    32768 tokens at 2.0 bits/value) on the tensor-core kernels; the oracle's
+    fp64 attention checked on the query heads of kv heads 0 and 5."""
+    monkeypatch.setenv("SPECTRA_PATH", "tc")
+    B, Hq, Hkv, ctx = 1, 32, 8, 32768
+    kx = [synth.to_bf16_exact(synth.spiked_t(31, ctx, Hkv, 128, role=synth.ROLE_K)).astype(np.float64)]
+    vx = [synth.to_bf16_exact(synth.spiked_t(31, ctx, Hkv, 128, role=synth.ROLE_V)).astype(np.float64)]
+    kp = orc.make_eigen_plan(kx[0][:2048], 2.0)
+    vp = orc.make_eigen_plan(vx[0][:2048], 2.0)
+    kenc, venc = orc.encode(kp, kx[0]), orc.encode(vp, vx[0])
+    stride = max(max(len(e["stream"]) for e in kenc), max(len(e["stream"]) for e in venc))
+    kd = torch.zeros((Hkv, stride), dtype=torch.uint8)
+    vd = torch.zeros((Hkv, stride), dtype=torch.uint8)
+    for h in range(Hkv):
+        kd[h, : len(kenc[h]["stream"])] = torch.from_numpy(kenc[h]["stream"])
+        vd[h, : len(venc[h]["stream"])] = torch.from_numpy(venc[h]["stream"])
+    q = synth.to_bf16_exact(synth.queries(9, B, Hq, 128))
+    gk, gv = gpu_plan(spx, kp), gpu_plan(spx, vp)
+    out = torch.zeros((B, Hq, 128), device="cuda")
+    spx.spectra_attn_decode(gk, gv, torch.from_numpy(q).to(torch.bfloat16).cuda(), kd.cuda(), vd.cuda(),
+                            ctx, 1.0, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    G = Hq // Hkv
+    for h in (0, 5):
+        kr = orc.decode_head(kp, h, kenc[h]["stream"], ctx)
+        vr = orc.decode_head(vp, h, venc[h]["stream"], ctx)
+        for j in range(G):
+            want = orc.attention(q[0, h * G + j].astype(np.float64), kr, vr, 1.0)
+            assert rel_l2(got[0, h * G + j], want) <= ATTN_TOL, (h, j)
 
 
 def test_attn_empty_context(spx, orc):
