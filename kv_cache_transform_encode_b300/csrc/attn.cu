@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads)
 attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq, int64_t ctx,
                   const uint8_t* __restrict__ kc, const uint8_t* __restrict__ vc, int64_t sstride,
                   const float* __restrict__ kn, const float* __restrict__ vn, int64_t nstride,
-                  int nsplit, float* __restrict__ part)
+                  int nsplit, int split_len, float* __restrict__ part)
 {
     constexpr int LD = D + 1;
     extern __shared__ float smem[];
@@ -143,8 +143,8 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
     const uint32_t* vs = reinterpret_cast<const uint32_t*>(vc + sid * sstride);
     const float* knr = kn ? kn + sid * nstride : nullptr;
     const float* vnr = vn ? vn + sid * nstride : nullptr;
-    const int64_t s0 = int64_t(split) * kSplitLen;
-    const int64_t s1 = min(ctx, s0 + kSplitLen);
+    const int64_t s0 = int64_t(split) * split_len;
+    const int64_t s1 = min(ctx, s0 + split_len);
 
     // each thread owns outputs (j, c) for e = tid + k*blockDim
     constexpr int kOwn = kMaxGroup * D / kThreads;
@@ -219,16 +219,17 @@ __global__ void attn_combine_kernel(PlanView vp, const float* __restrict__ part,
     extern __shared__ float os[];
     __shared__ float sM, sL;
     const float* pp = part + int64_t(bj) * nsplit * (D + 2);
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
         float M = -INFINITY;
-        for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pp[int64_t(s) * (D + 2)]);
+        for (int s = threadIdx.x; s < nsplit; s += 32) M = fmaxf(M, pp[int64_t(s) * (D + 2)]);
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float L = 0.f;
-        for (int s = 0; s < nsplit; ++s) {
+        for (int s = threadIdx.x; s < nsplit; s += 32) {
             const float m = pp[int64_t(s) * (D + 2)];
             if (m != -INFINITY) L += pp[int64_t(s) * (D + 2) + 1] * __expf(m - M);
         }
-        sM = M;
-        sL = L;
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (threadIdx.x == 0) { sM = M; sL = L; }
     }
     __syncthreads();
     for (int c = threadIdx.x; c < D; c += blockDim.x) {
@@ -245,10 +246,17 @@ __global__ void attn_combine_kernel(PlanView vp, const float* __restrict__ part,
         os[c] = y;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    // out_i = sum_c B_V[i][c] os[c]: one warp per output row (coalesced row reads)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int i = warp; i < D; i += nw) {
         float a = 0.f;
-        for (int c = 0; c < D; ++c) a = fmaf(basis_entry(vp, h, i, c, D), os[c], a);
-        out[int64_t(bj) * D + i] = a;
+        for (int c = lane; c < D; c += 32) {
+            const float bic = (vp.basis == SPECTRA_BASIS_EIGEN) ? vp.basis_mat[(size_t(h) * D + i) * D + c]
+                                                                : basis_entry(vp, h, i, c, D);
+            a = fmaf(bic, os[c], a);
+        }
+        for (int o = 16; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) out[int64_t(bj) * D + i] = a;
     }
 }
 
@@ -260,7 +268,14 @@ size_t split_smem()
            sizeof(int) * 4 * D + sizeof(uint32_t) * 2 * 2 * 8 * D;
 }
 
-int nsplit_of(int64_t ctx) { return int((ctx + kSplitLen - 1) / kSplitLen); }
+// context split length: 2048 tokens, or 1024 when few (batch, query head)
+// pairs would leave SMs idle
+int split_len_of(int B, int Hq) { return (int64_t(B) * Hq >= 256) ? kSplitLen : kSplitLen / 2; }
+int nsplit_of(int B, int Hq, int64_t ctx)
+{
+    const int L = split_len_of(B, Hq);
+    return int((ctx + L - 1) / L);
+}
 
 // kernel family, as for encode/decode: SPECTRA_PATH=generic / tc / unset
 char attn_path()
@@ -281,7 +296,7 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
 size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx)
 {
     const size_t qt = align256(sizeof(float) * size_t(B) * Hq * d);
-    const size_t part = align256(sizeof(float) * size_t(B) * Hq * nsplit_of(ctx) * (d + 2));
+    const size_t part = align256(sizeof(float) * size_t(B) * Hq * nsplit_of(B, Hq, ctx) * (d + 2));
     return qt + part + attn_tc_extra_bytes(B, Hq);
 }
 
@@ -294,7 +309,8 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
     const int D = kplan->head_dim, Hkv = kplan->heads;
     if (Hq / Hkv > kMaxGroup) return SPECTRA_ERR_UNSUPPORTED;
     const PlanView kp = make_view(kplan), vp = make_view(vplan);
-    const int nsplit = nsplit_of(ctx);
+    const int nsplit = nsplit_of(B, Hq, ctx);
+    const int split_len = split_len_of(B, Hq);
     float* qt = static_cast<float*>(ws);
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                            align256(sizeof(float) * size_t(B) * Hq * D));
@@ -302,7 +318,7 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
     if (attn_path() != 'g') {
         bool done = false;
         spectra_status st = launch_attn_tc(kplan, vplan, q, q_dt, B, Hq, kc, vc, sstride, ctx, scale, part, nsplit,
-                                           kSplitLen, extra, s, &done);
+                                           split_len, extra, s, &done);
         if (st) return st;
         if (done) {
             attn_combine_kernel<<<B * Hq, D, D * sizeof(float), s>>>(vp, part, Hq, nsplit, 1, out);
@@ -316,12 +332,12 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
         const size_t sm = split_smem<128>();
         cudaFuncSetAttribute(attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
         attn_split_kernel<128><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
-                                                          nstride, nsplit, part);
+                                                          nstride, nsplit, split_len, part);
     } else {
         const size_t sm = split_smem<64>();
         cudaFuncSetAttribute(attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
         attn_split_kernel<64><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
-                                                         nstride, nsplit, part);
+                                                         nstride, nsplit, split_len, part);
     }
     attn_combine_kernel<<<B * Hq, D, D * sizeof(float), s>>>(vp, part, Hq, nsplit, 0, out);
     return cuda_status(cudaGetLastError());

@@ -130,20 +130,31 @@ attn_tc_prep_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, i
 {
     const int bh = blockIdx.x, Hkv = kp.heads, h = bh % Hkv, b = bh / Hkv;
     const int c = threadIdx.x;
+    extern __shared__ float Bs[];                 // [D][D] basis of head h (staged: coalesced 16-B loads)
     __shared__ float qs[kGmax][D];
     __shared__ float red[kGmax][4];
-    for (int e = c; e < G * D; e += D) qs[e / D][e % D] = load_elem(q, q_dt, (int64_t(b) * Hq + h * G + e / D) * D + e % D);
+    {
+        const float4* src = reinterpret_cast<const float4*>(kp.basis_mat + size_t(h) * D * D);
+        float4* dst = reinterpret_cast<float4*>(Bs);
+        for (int e = c; e < D * D / 4; e += D) dst[e] = src[e];
+    }
+    for (int e = c; e < kGmax * D; e += D)
+        qs[e / D][e % D] = (e / D < G) ? load_elem(q, q_dt, (int64_t(b) * Hq + h * G + e / D) * D + e % D) : 0.f;
     __syncthreads();
+    float qt[kGmax] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < D; ++i) {
+        const float bic = Bs[i * D + c];
+#pragma unroll
+        for (int j = 0; j < kGmax; ++j) qt[j] = fmaf(bic, qs[j][i], qt[j]);
+    }
     const int bits = kp.bits[size_t(h) * D + c];
     const float delta = kp.rscale[size_t(h) * D + c];
     __half* wr = wimg + size_t(bh) * 8 * D;
     float* wsr = wsum16 + size_t(bh) * 8 * 8;           // [kb][n]
+#pragma unroll
     for (int j = 0; j < kGmax; ++j) {
-        float qt = 0.f;
-        if (j < G)
-            for (int i = 0; i < D; ++i) qt = fmaf(kp.basis_mat[(size_t(h) * D + i) * D + c], qs[j][i], qt);
-        qt *= scale;
-        const float w = (bits > 0 && j < G) ? qt * delta : 0.f;
+        const float qj = qt[j] * scale;
+        const float w = (bits > 0 && j < G) ? qj * delta : 0.f;
         const __half hi = __float2half_rn(w);
         const __half lo = __float2half_rn(w - __half2float(hi));
         wr[j * D + c] = hi;
@@ -157,7 +168,7 @@ attn_tc_prep_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, i
             wsr[(c >> 4) * 8 + j] = sh;
             wsr[(c >> 4) * 8 + kGmax + j] = sl;
         }
-        float k0 = (bits > 0 && j < G) ? qt * 0.5f * delta * (1.f - float(1 << bits)) : 0.f;
+        float k0 = (bits > 0 && j < G) ? qj * 0.5f * delta * (1.f - float(1 << bits)) : 0.f;
         for (int o = 16; o; o >>= 1) k0 += __shfl_xor_sync(0xffffffffu, k0, o);
         if ((c & 31) == 0) red[j][c >> 5] = k0;
     }
@@ -457,7 +468,8 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
     P.vbytes = uint32_t(16 * (vplan->max_rec_bits > 0 ? vplan->max_rec_bits : 1));
     const size_t sm = tc_split_smem(P.kbytes, P.vbytes);
     if (sm > 227 * 1024) return SPECTRA_OK;
-    attn_tc_prep_kernel<<<B * Hkv, D, 0, s>>>(P.kp, q, q_dt, Hq, G, scale, wimg, bias, wsum16);
+    cudaFuncSetAttribute(attn_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(float) * D * D));
+    attn_tc_prep_kernel<<<B * Hkv, D, sizeof(float) * D * D, s>>>(P.kp, q, q_dt, Hq, G, scale, wimg, bias, wsum16);
     cudaFuncSetAttribute(attn_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
     dim3 grid(nsplit, Hkv, B);
     attn_tc_split_kernel<<<grid, kThreads, sm, s>>>(P);

@@ -20,6 +20,7 @@
 //   accumulator V J in the same phase.
 #include "spectra_internal.cuh"
 
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include <algorithm>
@@ -289,6 +290,7 @@ jacobi_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int 
 // Rutishauser's form (c x - s y evaluated as x - s (y + tau x), tau =
 // s / (1 + c)) keeps the transforms orthogonal to working precision.
 constexpr int kJ2 = 128;
+constexpr int kJacCluster = 8;   // CTAs per head in the cluster Jacobi
 
 struct Rot { float s, tau, t; };
 
@@ -617,6 +619,330 @@ size_t jacobi128_smem()
     return (work > fin ? work : fin) + 16;
 }
 
+// ---------------------------------------------------------------------------
+// jacobi128c_kernel<C>: the same odd-even Jacobi spread over a cluster of C
+// CTAs per head (distributed shared memory).  CTA r owns block rows
+// [NW r, NW r + NW) (NW = 32 / C warps, 4 rows each) of A and V; thread
+// (warp, lane) still owns one 4x4 block of each.  Once per round, after a
+// cluster barrier, every CTA holds the whole diagonal band (each CTA writes
+// its band entries into all CTAs' shared memory) and computes the round's 64
+// rotations itself; the block rows that straddle two CTAs in odd rounds are
+// sent ahead (as they stand after the previous round) and each receiver
+// applies the column rotations to its copy.  Every CTA runs the same rounds
+// and takes the same convergence decision (cluster-reduced in a fixed
+// order), so every barrier is met by all CTAs.
+template <int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(1024 / C, 1)
+jacobi128c_kernel(const float* partials, int nchunks, float inv_n, int max_sweeps,
+                  float* __restrict__ basis_out, float* __restrict__ eig_out, int32_t* __restrict__ status,
+                  float* __restrict__ gram_out, float* scratch)
+{
+    namespace cg = cooperative_groups;
+    constexpr int D = kJ2;
+    constexpr int NW = 32 / C;                // warps per CTA
+    constexpr int NT = 32 * NW;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = int(cluster.block_rank());
+    const int hd = blockIdx.x / C;
+
+    extern __shared__ float smem[];
+    float* rowx = smem;                                    // [NW][2][D]
+    float* band = rowx + NW * 2 * D;                       // [2][2][D]
+    float* nbr = band + 4 * D;                             // [2 parity][2: up, down][D]
+    float4* prm = reinterpret_cast<float4*>(nbr + 4 * D);  // [2][64]
+    float* red = reinterpret_cast<float*>(prm + 128);      // [33]
+    float* csum = red + 33;                                // [2][C] cluster partial sums
+    float* lamall = csum + 2 * C;                          // [D]
+    int* cflag = reinterpret_cast<int*>(lamall + D);       // [C]
+
+    const int tid = threadIdx.x, wl = tid >> 5, l = tid & 31;
+    const int w = rank * NW + wl;                          // global block row
+    cluster.sync();    // every CTA of the cluster runs before any shared memory is touched remotely
+    float2 a[2][4], v[2][4];
+#define AE(i, j) ((i) & 1 ? a[(i) >> 1][j].y : a[(i) >> 1][j].x)
+
+    // cluster-wide sum of one float per CTA, identical in every CTA
+    int cuse = 0;
+    auto cluster_sum = [&](float part) -> float {
+        const float tot = block_sum(part, red);
+        if (tid < C) *cluster.map_shared_rank(csum + (cuse & 1) * C + rank, tid) = tot;
+        cluster.sync();
+        float s = 0.f;
+        for (int k = 0; k < C; ++k) s += csum[(cuse & 1) * C + k];
+        ++cuse;
+        return s;
+    };
+
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = 4 * w + i, c = 4 * l + j;
+            const float* src = partials + size_t(hd) * nchunks * D * D + size_t(r) * D + c;
+            float sum = 0.f;
+            for (int ch = 0; ch < nchunks; ++ch) sum += src[size_t(ch) * D * D];
+            sum *= inv_n;
+            AE(i, j) = sum;
+            ((i & 1) ? v[i >> 1][j].y : v[i >> 1][j].x) = (r == c) ? 1.f : 0.f;
+            if (gram_out) gram_out[size_t(hd) * D * D + size_t(r) * D + c] = sum;
+            bad |= !isfinite(sum);
+        }
+    {
+        const int bl = __syncthreads_or(bad);
+        if (tid < C) *cluster.map_shared_rank(cflag + rank, tid) = bl;
+        cluster.sync();
+        int any = 0;
+        for (int k = 0; k < C; ++k) any |= cflag[k];
+        if (any) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    basis_out[size_t(hd) * D * D + size_t(4 * w + i) * D + 4 * l + j] = (4 * w + i == 4 * l + j) ? 1.f : 0.f;
+            if (rank == 0 && tid < D) eig_out[size_t(hd) * D + tid] = 0.f;
+            if (rank == 0 && tid == 0) status[hd] = -SPECTRA_ERR_NONFINITE;
+            return;
+        }
+    }
+    // publish this CTA's band entries (all CTAs) and, before odd rounds, the
+    // block rows the neighbour CTAs need
+    auto publish = [&](int par, bool rows) {
+        if (w == l) {
+            const float dv[4] = {a[0][0].x, a[0][1].y, a[1][2].x, a[1][3].y};
+            const float sv[3] = {a[0][1].x, a[0][2].y, a[1][3].x};
+            for (int k = 0; k < C; ++k) {
+                float* dg = cluster.map_shared_rank(band + par * 2 * D, k);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dg[4 * w + i] = dv[i];
+#pragma unroll
+                for (int i = 0; i < 3; ++i) dg[D + 4 * w + i] = sv[i];
+            }
+        }
+        if (l == w + 1) {
+            for (int k = 0; k < C; ++k) cluster.map_shared_rank(band + par * 2 * D, k)[D + 4 * w + 3] = a[1][0].y;
+        }
+        if (rows) {
+            if (wl == 0 && rank > 0) {          // my row 0 -> rank-1's "down" row
+                float* dst = cluster.map_shared_rank(nbr + (par * 2 + 1) * D, rank - 1) + 4 * l;
+                *reinterpret_cast<float4*>(dst) = make_float4(a[0][0].x, a[0][1].x, a[0][2].x, a[0][3].x);
+            }
+            if (wl == NW - 1 && rank < C - 1) { // my row 3 -> rank+1's "up" row
+                float* dst = cluster.map_shared_rank(nbr + (par * 2 + 0) * D, rank + 1) + 4 * l;
+                *reinterpret_cast<float4*>(dst) = make_float4(a[1][0].y, a[1][1].y, a[1][2].y, a[1][3].y);
+            }
+        }
+    };
+    publish(0, false);
+
+    float loc = 0.f;
+#pragma unroll
+    for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) loc += a[ip][j].x * a[ip][j].x + a[ip][j].y * a[ip][j].y;
+    const float fro = sqrtf(cluster_sum(loc));
+
+    // column rotations of one 4-wide row segment (odd round): (4l-1, 4l) with
+    // the left lane, (4l+1, 4l+2) inside, (4l+3, 4l+4) with the right lane
+    auto col_odd = [&](float (&x)[4], const Rot& cm, const Rot& c0, const Rot& c1) {
+        const float xr = __shfl_down_sync(0xffffffffu, x[0], 1);
+        const float xl = __shfl_up_sync(0xffffffffu, x[3], 1);
+        if (l < 31) x[3] = fmaf(c1.s, fmaf(-c1.tau, xr, x[3]), xr);
+        if (l > 0) x[0] = fmaf(-cm.s, fmaf(cm.tau, xl, x[0]), xl);
+        rotswap(x[1], x[2], c0.s, c0.tau);
+    };
+
+    int sweeps = 0, converged = 0, rounds = 0;
+    float prev_off = INFINITY;
+    for (;;) {
+        loc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (4 * w + i != 4 * l + j) loc = fmaf(AE(i, j), AE(i, j), loc);
+        const float off = sqrtf(cluster_sum(loc));
+        if (off <= 1e-6f * fro || fro == 0.f || (off > 0.5f * prev_off && off <= 1e-4f * fro)) {
+            converged = 1;
+            break;
+        }
+        if (sweeps >= max_sweeps) break;
+        prev_off = off;
+        ++sweeps;
+        for (int r = 0; r < D; ++r, ++rounds) {
+            const int par = r & 1;
+            const bool E = par == 0;
+            cluster.sync();                        // band[par] (and rows) from every CTA visible
+            if (wl < 2) {
+                const int k = tid, p = E ? 2 * k : 2 * k + 1, q = p + 1;
+                float4 rt = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q < D) {
+                    const float* dg = band + par * 2 * D;
+                    rt = band_rotation(dg[p], dg[q], dg[D + p]);
+                }
+                prm[par * 64 + k] = rt;
+            } else if (rounds > 0) {
+                v_update(v, prm + (par ^ 1) * 64, !E, l);
+            }
+            __syncthreads();
+            if (wl < 2 && rounds > 0) v_update(v, prm + (par ^ 1) * 64, !E, l);
+            const float4* pr = prm + par * 64;
+            if (E) {
+                const Rot r0 = load_rot(pr, 2 * w), r1 = load_rot(pr, 2 * w + 1);
+                const Rot c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
+                float d00 = 0.f, d11 = 0.f, d01 = 0.f, d22 = 0.f, d33 = 0.f, d23 = 0.f;
+                if (w == l) {
+                    d00 = a[0][0].x; d11 = a[0][1].y; d01 = a[0][1].x;
+                    d22 = a[1][2].x; d33 = a[1][3].y; d23 = a[1][3].x;
+                }
+#pragma unroll
+                for (int ip = 0; ip < 2; ++ip) {
+                    rotswap2(a[ip][0], a[ip][1], c0.s, c0.tau);
+                    rotswap2(a[ip][2], a[ip][3], c1.s, c1.tau);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    rotswap(a[0][j].x, a[0][j].y, r0.s, r0.tau);
+                    rotswap(a[1][j].x, a[1][j].y, r1.s, r1.tau);
+                }
+                if (w == l) {
+                    a[0][0].x = fmaf(r0.t, d01, d11); a[0][1].y = fmaf(-r0.t, d01, d00);
+                    a[0][1].x = 0.f; a[0][0].y = 0.f;
+                    a[1][2].x = fmaf(r1.t, d23, d33); a[1][3].y = fmaf(-r1.t, d23, d22);
+                    a[1][3].x = 0.f; a[1][2].y = 0.f;
+                }
+            } else {
+                const bool up = w > 0, dn = w < 31, lf = l > 0, rt = l < 31;
+                const Rot cm = load_rot(pr, lf ? 2 * l - 1 : 0), c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
+                float d11 = 0.f, d22 = 0.f, d12 = 0.f;
+                if (w == l) { d11 = a[0][1].y; d22 = a[1][2].x; d12 = a[0][2].y; }
+#pragma unroll
+                for (int ip = 0; ip < 2; ++ip) {
+                    float2 ar, al;
+                    ar.x = __shfl_down_sync(0xffffffffu, a[ip][0].x, 1);
+                    ar.y = __shfl_down_sync(0xffffffffu, a[ip][0].y, 1);
+                    al.x = __shfl_up_sync(0xffffffffu, a[ip][3].x, 1);
+                    al.y = __shfl_up_sync(0xffffffffu, a[ip][3].y, 1);
+                    if (rt) {
+                        float2 x = a[ip][3], y = ar;
+                        rotswap2(x, y, c1.s, c1.tau);
+                        a[ip][3] = x;
+                    }
+                    if (lf) {
+                        float2 x = al, y = a[ip][0];
+                        rotswap2(x, y, cm.s, cm.tau);
+                        a[ip][0] = y;
+                    }
+                    rotswap2(a[ip][1], a[ip][2], c0.s, c0.tau);
+                }
+                // rows across warps of this CTA: shared memory; across CTAs:
+                // the neighbour's row as it stood, column-rotated here
+                float* mine = rowx + wl * 2 * D + 4 * l;
+                *reinterpret_cast<float4*>(mine) = make_float4(a[0][0].x, a[0][1].x, a[0][2].x, a[0][3].x);
+                *reinterpret_cast<float4*>(mine + D) = make_float4(a[1][0].y, a[1][1].y, a[1][2].y, a[1][3].y);
+                float ab[4] = {0.f, 0.f, 0.f, 0.f}, bl[4] = {0.f, 0.f, 0.f, 0.f};
+                if (wl == 0 && up) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(nbr + (par * 2 + 0) * D + 4 * l);
+                    ab[0] = t4.x; ab[1] = t4.y; ab[2] = t4.z; ab[3] = t4.w;
+                    col_odd(ab, cm, c0, c1);
+                }
+                if (wl == NW - 1 && dn) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(nbr + (par * 2 + 1) * D + 4 * l);
+                    bl[0] = t4.x; bl[1] = t4.y; bl[2] = t4.z; bl[3] = t4.w;
+                    col_odd(bl, cm, c0, c1);
+                }
+                __syncthreads();
+                const Rot rm = load_rot(pr, up ? 2 * w - 1 : 0), r0 = load_rot(pr, 2 * w), r1 = load_rot(pr, 2 * w + 1);
+                if (dn) {
+                    if (wl < NW - 1) {
+                        const float4 b4 = *reinterpret_cast<const float4*>(rowx + (wl + 1) * 2 * D + 4 * l);
+                        bl[0] = b4.x; bl[1] = b4.y; bl[2] = b4.z; bl[3] = b4.w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a[1][j].y = fmaf(r1.s, fmaf(-r1.tau, bl[j], a[1][j].y), bl[j]);
+                }
+                if (up) {
+                    if (wl > 0) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(rowx + (wl - 1) * 2 * D + D + 4 * l);
+                        ab[0] = a4.x; ab[1] = a4.y; ab[2] = a4.z; ab[3] = a4.w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a[0][j].x = fmaf(-rm.s, fmaf(rm.tau, ab[j], a[0][j].x), ab[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) rotswap(a[0][j].y, a[1][j].x, r0.s, r0.tau);
+                if (w == l) {
+                    a[0][1].y = fmaf(r0.t, d12, d22); a[1][2].x = fmaf(-r0.t, d12, d11);
+                    a[0][2].y = 0.f; a[1][1].x = 0.f;
+                }
+            }
+            publish(par ^ 1, E);
+        }
+    }
+    if (rounds > 0) {
+        __syncthreads();
+        v_update(v, prm + ((rounds - 1) & 1) * 64, ((rounds - 1) & 1) == 0, l);
+    }
+
+    // Sort descending (ties: lower position first), sign-fix, write out.  V
+    // rows go through global scratch, eigenvalues to every CTA.
+    float* Vg = scratch + size_t(hd) * nchunks * D * D;    // [D][D] position-ordered columns
+#pragma unroll
+    for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            Vg[size_t(4 * w + 2 * ip) * D + 4 * l + j] = v[ip][j].x;
+            Vg[size_t(4 * w + 2 * ip + 1) * D + 4 * l + j] = v[ip][j].y;
+        }
+    if (w == l) {
+        const float dv[4] = {a[0][0].x, a[0][1].y, a[1][2].x, a[1][3].y};
+        for (int k = 0; k < C; ++k) {
+            float* lm = cluster.map_shared_rank(lamall, k);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) lm[4 * w + i] = dv[i];
+        }
+    }
+#undef AE
+    __threadfence();
+    cluster.sync();
+    constexpr int CPC = D / C;                 // columns per CTA
+    for (int ci = wl; ci < CPC; ci += NW) {
+        const int i = rank * CPC + ci;         // position
+        const float li = lamall[i];
+        int rk = 0;
+        for (int j = l; j < D; j += 32) {
+            const float lj = lamall[j];
+            rk += (lj > li) || (lj == li && j < i);
+        }
+        for (int o = 16; o; o >>= 1) rk += __shfl_xor_sync(0xffffffffu, rk, o);
+        float best = -1.f;
+        int br = 0;
+        for (int rr = l; rr < D; rr += 32) {
+            const float av = fabsf(__ldcg(Vg + size_t(rr) * D + i));   // written by other CTAs: skip L1
+            if (av > best) { best = av; br = rr; }
+        }
+        for (int o = 16; o; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int orr = __shfl_xor_sync(0xffffffffu, br, o);
+            if (ob > best || (ob == best && orr < br)) { best = ob; br = orr; }
+        }
+        const float sgn = (__ldcg(Vg + size_t(br) * D + i) < 0.f) ? -1.f : 1.f;
+        for (int rr = l; rr < D; rr += 32)
+            basis_out[size_t(hd) * D * D + size_t(rr) * D + rk] = sgn * __ldcg(Vg + size_t(rr) * D + i);
+        if (l == 0) eig_out[size_t(hd) * D + rk] = li;
+    }
+    if (rank == 0 && tid == 0) status[hd] = converged ? sweeps : -SPECTRA_ERR_NOT_CONVERGED;
+    cluster.sync();   // no CTA leaves while others may still write into its shared memory
+}
+
+template <int C>
+size_t jacobi128c_smem()
+{
+    constexpr int NW = 32 / C;
+    return sizeof(float) * (NW * 2 * kJ2 + 4 * kJ2 + 4 * kJ2) + sizeof(float4) * 128 +
+           sizeof(float) * (33 + 2 * C + kJ2) + sizeof(int) * C + 16;
+}
+
 template <int D>
 size_t jacobi_smem()
 {
@@ -651,10 +977,14 @@ spectra_status launch_jacobi(const spectra_plan* plan, const float* partials, in
 {
     const float inv_n = 1.0f / float(n_cal);
     if (plan->head_dim == 128) {
-        const size_t sm = jacobi128_smem();
-        cudaFuncSetAttribute(jacobi128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-        jacobi128_kernel<<<plan->heads, 1024, sm, s>>>(partials, nchunks, inv_n, max_sweeps, plan->basis_mat,
-                                                       plan->eigvals, plan->status, gram_out);
+        // one cluster of kJacCluster CTAs per head; the Gram partials of the
+        // head (at least D x D floats) double as the scratch of the final sort
+        constexpr int C = kJacCluster;
+        const size_t sm = jacobi128c_smem<C>();
+        cudaFuncSetAttribute(jacobi128c_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        jacobi128c_kernel<C><<<plan->heads * C, 1024 / C, sm, s>>>(partials, nchunks, inv_n, max_sweeps,
+                                                                   plan->basis_mat, plan->eigvals, plan->status,
+                                                                   gram_out, const_cast<float*>(partials));
     } else {
         const size_t sm = jacobi_smem<64>();
         cudaFuncSetAttribute(jacobi_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
