@@ -57,7 +57,7 @@ constexpr int TILE = 128;                 // tokens per tile (MMA M)
 constexpr uint32_t OPND = TILE * D * 2;   // one bf16 operand tile: 32 KB
 constexpr uint32_t KBLK = TILE * 128;     // one 64-element K block: 16 KB
 constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
-constexpr int kEncThreads = 320;          // producer, MMA, 8 epilogue warps
+constexpr int kEncThreads = 576;          // producer, MMA, 16 epilogue warps
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // ------------------------------------------------------------------ helpers
@@ -153,24 +153,26 @@ __host__ __device__ inline EncSmem enc_smem_layout(int nterms, int stages, bool 
     L.img = o;  o += nterms * OPND;
     L.xs = o;   o += stages * OPND;
     L.th = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
-    L.red = o;  o += 2 * (4 * 32 + 8 * 32) * 4;      // RWHT norm partials and inverses
+    L.red = o;  o += (4 * 4 * 32 + 16 * 32) * 4;     // RWHT norm partials and inverses
     L.bars = o; o += 256;
     L.total = o;
     return L;
 }
 
-constexpr int kEncEpiWarps = 8;
+constexpr int kEncEpiWarps = 16;
 
 // D[c][t] = sum_i img[c][i] x[t][i]: TMEM lane = channel, column = token.
-// Epilogue warp e (warps 2..9): lane quadrant q = warp & 3 (channels
-// 32q .. 32q+31), token groups 2*half, 2*half+1 of each 128-token tile.
+// Epilogue warp e (warps 2..17): lane quadrant q = warp & 3 (channels
+// 32q .. 32q+31), token group gi = (warp - 2) / 4 of each 128-token tile.
+// LM: Lloyd-Max quantizer; RWHT: Hadamard basis (per-token scale).
+template <bool LM, bool RWHT>
 __global__ void __launch_bounds__(64 + 32 * kEncEpiWarps, 1)
 encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const bool lm = P.pv.quant == SPECTRA_Q_LLOYD_GAUSS;
-    const bool rwht = P.pv.basis == SPECTRA_BASIS_RWHT;
+    constexpr bool lm = LM;
+    constexpr bool rwht = RWHT;
     const EncSmem L = enc_smem_layout(P.nterms, P.stages, lm);
     uint8_t* img = smem + L.img;
     uint8_t* xs = smem + L.xs;
@@ -182,9 +184,9 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     uint64_t* imgfull = bars + 12;
     uint64_t* imgempty = bars + 13;
     uint64_t* drain = bars + 14;
-    uint64_t* rbar = bars + 15;            // [2] RWHT norm rendezvous, one per half
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 19);
+    uint64_t* rbar = bars + 15;            // [4] RWHT norm rendezvous, one per token group
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 20);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
     volatile int* drain_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -196,8 +198,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         mbar_init(imgfull, 1);
         mbar_init(imgempty, 1);
         mbar_init(drain, 1);
-        mbar_init(&rbar[0], 4);
-        mbar_init(&rbar[1], 4);
+        for (int g = 0; g < 4; ++g) mbar_init(&rbar[g], 4);
         *abort_flag = 0;
         *drain_flag = 0;
         fence_mbar_init();
@@ -288,11 +289,11 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;                        // TMEM lane quadrant: channels 32q..
-        const int half = (warp - 2) >> 2;              // token groups 2 half, 2 half + 1
+        const int gi = (warp - 2) >> 2;                // token group inside each tile
         const int c = q * 32 + lane;                   // this thread's channel
         const float* th = reinterpret_cast<const float*>(smem + L.th);
-        float* part = reinterpret_cast<float*>(smem + L.red) + half * (4 * 32);        // [4 q][32 t]
-        float* invs = reinterpret_cast<float*>(smem + L.red) + 2 * 4 * 32 + (warp - 2) * 32;
+        float* part = reinterpret_cast<float*>(smem + L.red) + gi * (4 * 32);          // [4 q][32 t]
+        float* invs = reinterpret_cast<float*>(smem + L.red) + 4 * 4 * 32 + (warp - 2) * 32;
         int k = 0, cur_h = -1, R = 0, b = 0, o = 0, bmax = 0, ruse = 0;
         float qk = 0.f, cl = 0.f;
         bool head_ok = true;
@@ -316,82 +317,77 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
             tc_fence_after();
             uint32_t* out = reinterpret_cast<uint32_t*>(P.codes + int64_t(h) * P.sstride);
             bool ok = true;
-            for (int gg = 0; gg < 2; ++gg) {
-                const int gi = 2 * half + gg;                       // group inside the tile
-                const int64_t t0 = int64_t(tile) * TILE + gi * 32;
-                const bool glive = t0 < P.T;
-                uint32_t r[32];
-                tmem_ld32(tmem + a * 128 + (uint32_t(q * 32) << 16) + gi * 32, r);
-                tmem_ld_wait();
-                if (rwht) {
-                    // ||x_t||^2 = (1/d) sum_c D[c][t]^2: reduce the 32 columns
-                    // over this warp's lanes (lane t ends with token t), then
-                    // over the four lane quadrants through shared memory.
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * __uint_as_float(r[i]);
-#pragma unroll
-                    for (int s = 16; s >= 1; s >>= 1) {
-                        const bool up = lane & s;
-#pragma unroll
-                        for (int i = 0; i < s; ++i) {
-                            const float send = up ? v[i] : v[i + s];
-                            const float keep = up ? v[i + s] : v[i];
-                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-                        }
-                    }
-                    part[q * 32 + lane] = v[0];
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&rbar[half]);
-                    if (!(ok = mbar_wait(&rbar[half], ruse & 1, abort_flag, kWaitNs))) break;
-                    ++ruse;
-                    const float n2 = part[lane] + part[32 + lane] + part[64 + lane] + part[96 + lane];
-                    const float nrm = sqrtf(n2 * (1.0f / float(D)));
-                    if (q == 0 && head_ok && t0 + lane < P.T) P.norms[int64_t(h) * P.nstride + t0 + lane] = nrm;
-                    invs[lane] = (nrm > 0.f) ? 1.f / nrm : 0.f;
-                    __syncwarp();
-                    // everyone has read part[] before it is written again
-                    if (lane == 0) mbar_arrive(&rbar[half]);
-                    if (!(ok = mbar_wait(&rbar[half], ruse & 1, abort_flag, kWaitNs))) break;
-                    ++ruse;
-                }
-                if (!glive || !head_ok || R == 0) continue;
-                // codes of 32 tokens (low byte of each word)
-                uint32_t cw[32];
-                if (!lm) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) cw[i] = quant_uniform(__uint_as_float(r[i]), qk, cl);
-                } else {
-                    const float* tb = th + (b > 0 ? (b - 1) * kLmStride : 0);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float u = __uint_as_float(r[i]) * (rwht ? invs[i] : qk);
-                        cw[i] = quant_lm(tb, b, bmax, u);
-                    }
-                }
-                uint32_t Y[8];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    Y[2 * m] = low_bytes(cw[8 * m], cw[8 * m + 1], cw[8 * m + 2], cw[8 * m + 3]);
-                    Y[2 * m + 1] = low_bytes(cw[8 * m + 4], cw[8 * m + 5], cw[8 * m + 6], cw[8 * m + 7]);
-                    transpose8(Y[2 * m], Y[2 * m + 1]);
-                }
-                const int64_t nt = P.T - t0;
-                const uint32_t live = nt >= 32 ? 0xffffffffu : ((1u << nt) - 1u);
-                uint32_t* dst = out + (int64_t(tile) * 4 + gi) * R + o;
-#pragma unroll
-                for (int kb = 0; kb < 8; ++kb) {
-                    if (kb < bmax) {
-                        const int hs = kb >> 2;
-                        const uint32_t pw = gather_byte(Y[hs], Y[2 + hs], Y[4 + hs], Y[6 + hs], kb & 3) & live;
-                        if (kb < b) dst[kb] = pw;
-                    }
-                }
-            }
+            const int64_t t0 = int64_t(tile) * TILE + gi * 32;
+            const bool glive = t0 < P.T;
+            uint32_t r[32];
+            tmem_ld32(tmem + a * 128 + (uint32_t(q * 32) << 16) + gi * 32, r);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&accempty[a]);
-            if (!ok) break;
+            if (lane == 0) mbar_arrive(&accempty[a]);      // accumulator columns read: MMA may reuse them
+            if (rwht) {
+                // ||x_t||^2 = (1/d) sum_c D[c][t]^2: reduce the 32 columns
+                // over this warp's lanes (lane t ends with token t), then over
+                // the four lane quadrants through shared memory.
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * __uint_as_float(r[i]);
+#pragma unroll
+                for (int s = 16; s >= 1; s >>= 1) {
+                    const bool up = lane & s;
+#pragma unroll
+                    for (int i = 0; i < s; ++i) {
+                        const float send = up ? v[i] : v[i + s];
+                        const float keep = up ? v[i + s] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+                    }
+                }
+                part[q * 32 + lane] = v[0];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rbar[gi]);
+                if (!(ok = mbar_wait(&rbar[gi], ruse & 1, abort_flag, kWaitNs))) break;
+                ++ruse;
+                const float n2 = part[lane] + part[32 + lane] + part[64 + lane] + part[96 + lane];
+                const float nrm = sqrtf(n2 * (1.0f / float(D)));
+                if (q == 0 && head_ok && t0 + lane < P.T) P.norms[int64_t(h) * P.nstride + t0 + lane] = nrm;
+                invs[lane] = (nrm > 0.f) ? 1.f / nrm : 0.f;
+                __syncwarp();
+                // everyone has read part[] before it is written again
+                if (lane == 0) mbar_arrive(&rbar[gi]);
+                if (!(ok = mbar_wait(&rbar[gi], ruse & 1, abort_flag, kWaitNs))) break;
+                ++ruse;
+            }
+            if (!glive || !head_ok || R == 0) continue;
+            // codes of 32 tokens (low byte of each word)
+            if (!lm) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = quant_uniform(__uint_as_float(r[i]), qk, cl);
+            } else {
+                const float* tb = th + (b > 0 ? (b - 1) * kLmStride : 0);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float u = __uint_as_float(r[i]) * (rwht ? invs[i] : qk);
+                    r[i] = quant_lm(tb, b, bmax, u);
+                }
+            }
+            uint32_t Y[8];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                Y[2 * m] = low_bytes(r[8 * m], r[8 * m + 1], r[8 * m + 2], r[8 * m + 3]);
+                Y[2 * m + 1] = low_bytes(r[8 * m + 4], r[8 * m + 5], r[8 * m + 6], r[8 * m + 7]);
+                transpose8(Y[2 * m], Y[2 * m + 1]);
+            }
+            const int64_t nt = P.T - t0;
+            const uint32_t live = nt >= 32 ? 0xffffffffu : ((1u << nt) - 1u);
+            uint32_t* dst = out + (int64_t(tile) * 4 + gi) * R + o;
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) {
+                if (kb < bmax) {
+                    const int hs = kb >> 2;
+                    const uint32_t pw = gather_byte(Y[hs], Y[2 + hs], Y[4 + hs], Y[6 + hs], kb & 3) & live;
+                    if (kb < b) dst[kb] = pw;
+                }
+            }
         }
     }
 
@@ -427,7 +423,7 @@ struct DecParams {
 };
 
 struct DecSmem {
-    uint32_t img, as, cs, stg, lv, bars, total;
+    uint32_t img, as, cs, stg, lv, bias, bars, total;
 };
 
 __host__ __device__ inline DecSmem dec_smem_layout(int nterms, int na, int astages, int cstages, uint32_t cbytes,
@@ -441,6 +437,7 @@ __host__ __device__ inline DecSmem dec_smem_layout(int nterms, int na, int astag
     L.cs = o;   o += cstages * cbytes;
     o = (o + 15) & ~15u;
     L.lv = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
+    L.bias = o; o += 4 * D * 4;                   // per epilogue warp: output offsets of the head
     L.bars = o; o += 256;
     L.total = o;
     return L;
@@ -488,12 +485,13 @@ __device__ __forceinline__ float code_byte(const uint32_t (&X)[8], int t)
     return __uint_as_float(__byte_perm(X[t >> 2], 0x4B400000u, 0x7650u | uint32_t(t & 3))) - kMagic;
 }
 
+template <bool LM>
 __global__ void __launch_bounds__(kDecThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const bool lm = P.pv.quant == SPECTRA_Q_LLOYD_GAUSS;
+    constexpr bool lm = LM;
     const bool rwht = P.pv.basis == SPECTRA_BASIS_RWHT;
     const DecSmem L = dec_smem_layout(P.nterms, P.na, P.astages, P.cstages, P.cbytes, lm);
     uint8_t* img = smem + L.img;
@@ -639,6 +637,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         const float* lv = reinterpret_cast<const float*>(smem + L.lv);
         int k = 0, cur_h = -1, R = 0, b0 = 0, b1 = 0, o0 = 0, o1 = 0, bmax = 0;
         float off0 = 0.f, off1 = 0.f;
+        bool code_mode = false;
         for (int w = W.begin; w < W.end; ++w, ++k) {
             const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
             if (h != cur_h) {
@@ -652,6 +651,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 off0 = 1.0f - float(1 << b0);
                 off1 = 1.0f - float(1 << b1);
                 bmax = __reduce_max_sync(0xffffffffu, max(b0, b1));
+                code_mode = !lm && !rwht && P.pv.wmax[h] <= 7;
             }
             const int sc = k % P.cstages, sa = k % P.astages;
             if (!mbar_wait(&cfull[sc], (k / P.cstages) & 1, abort_flag, kWaitNs)) break;
@@ -665,6 +665,25 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 const uint32_t abase = smem_u32(as + sa * P.na * OPND) + hc * KBLK;
                 const float* lv0 = lv + (b0 > 0 ? (b0 - 1) * kLmStride : 0);
                 const float* lv1 = lv + (b1 > 0 ? (b1 - 1) * kLmStride : 0);
+                if (code_mode) {
+                    // (c0, c0+1) of token t as bf16 (128 + code): byte permutes only.
+                    // Row r = 32 gi + t; its swizzled chunk depends on r & 7 = t & 7.
+                    uint32_t rb[8];
+#pragma unroll
+                    for (int r8 = 0; r8 < 8; ++r8)
+                        rb[r8] = abase + uint32_t(gi * 32) * 128u + ((uint32_t(lane >> 2) ^ uint32_t(r8)) << 4) +
+                                 4u * uint32_t(lane & 3);
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const uint32_t lo = __byte_perm(X0[m], X1[m], 0x5140);   // tokens 4m, 4m+1
+                        const uint32_t hi = __byte_perm(X0[m], X1[m], 0x7362);   // tokens 4m+2, 4m+3
+                        const int t = 4 * m;
+                        st_shared_u32(rb[(t + 0) & 7] + uint32_t(t + 0) * 128u, __byte_perm(lo, 0x4343u, 0x5140));
+                        st_shared_u32(rb[(t + 1) & 7] + uint32_t(t + 1) * 128u, __byte_perm(lo, 0x4343u, 0x5342));
+                        st_shared_u32(rb[(t + 2) & 7] + uint32_t(t + 2) * 128u, __byte_perm(hi, 0x4343u, 0x5140));
+                        st_shared_u32(rb[(t + 3) & 7] + uint32_t(t + 3) * 128u, __byte_perm(hi, 0x4343u, 0x5342));
+                    }
+                } else
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
                     const uint32_t row = uint32_t(gi * 32 + t);
@@ -697,8 +716,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
         const bool leader = (warp == 2 + kDecUnpackWarps && lane == 0);
-        int k = 0, euse = 0;
-        bool ok = true;
+        float* bsh = reinterpret_cast<float*>(smem + L.bias) + (warp - 2 - kDecUnpackWarps) * D;
+        int k = 0, euse = 0, cur_h = -1;
+        bool ok = true, code_mode = false;
         auto rendezvous = [&]() -> bool {   // all four epilogue warps
             __syncwarp();
             if (lane == 0) mbar_arrive(ebar);
@@ -708,6 +728,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         };
         for (int w = W.begin; w < W.end && ok; ++w, ++k) {
             const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+            if (h != cur_h) {       // code mode: per-output offsets of this head
+                cur_h = h;
+                code_mode = !lm && !rwht && P.pv.wmax[h] <= 7;
+                __syncwarp();
+                for (int i = lane; i < D; i += 32) bsh[i] = code_mode ? P.pv.dec_bias[size_t(h) * D + i] : 0.f;
+                __syncwarp();
+            }
             const int a = k & 1;
             if (!mbar_wait(&accfull[a], (k >> 1) & 1, abort_flag, kWaitNs)) break;
             tc_fence_after();
@@ -733,10 +760,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4) {
                             uint32_t pk[4];
+                            const float4 bA = *reinterpret_cast<const float4*>(bsh + 32 * j + c4 * 8);
+                            const float4 bB = *reinterpret_cast<const float4*>(bsh + 32 * j + c4 * 8 + 4);
+                            const float bb[8] = {bA.x, bA.y, bA.z, bA.w, bB.x, bB.y, bB.z, bB.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                pk[e] = pack_bf16x2(__uint_as_float(r[c4 * 8 + 2 * e]) * scale,
-                                                    __uint_as_float(r[c4 * 8 + 2 * e + 1]) * scale);
+                                pk[e] = pack_bf16x2(fmaf(__uint_as_float(r[c4 * 8 + 2 * e]), scale, bb[2 * e]),
+                                                    fmaf(__uint_as_float(r[c4 * 8 + 2 * e + 1]), scale, bb[2 * e + 1]));
                             const uint32_t off = (j >> 1) * KBLK + sw128_offset(row, (j & 1) * 64 + c4 * 16);
                             st_shared_v4(sba + off, pk[0], pk[1], pk[2], pk[3]);
                         }
@@ -750,10 +780,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
 #pragma unroll
                         for (int c4 = 0; c4 < 8; ++c4) {
                             const uint32_t off = j * KBLK + sw128_offset(row, c4 * 16);
-                            st_shared_v4(sba + off, __float_as_uint(__uint_as_float(r[4 * c4]) * scale),
-                                         __float_as_uint(__uint_as_float(r[4 * c4 + 1]) * scale),
-                                         __float_as_uint(__uint_as_float(r[4 * c4 + 2]) * scale),
-                                         __float_as_uint(__uint_as_float(r[4 * c4 + 3]) * scale));
+                            const float4 bA = *reinterpret_cast<const float4*>(bsh + 64 * rd + 32 * j + 4 * c4);
+                            st_shared_v4(sba + off, __float_as_uint(fmaf(__uint_as_float(r[4 * c4]), scale, bA.x)),
+                                         __float_as_uint(fmaf(__uint_as_float(r[4 * c4 + 1]), scale, bA.y)),
+                                         __float_as_uint(fmaf(__uint_as_float(r[4 * c4 + 2]), scale, bA.z)),
+                                         __float_as_uint(fmaf(__uint_as_float(r[4 * c4 + 3]), scale, bA.w)));
                         }
                     }
                 }
@@ -799,10 +830,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
 //  decode (B operand, rows = output index i, K = channel c):
 //    EIGEN uniform: basis[i][c] * Delta_c / 2;  EIGEN Lloyd-Max: basis[i][c] *
 //    sigma_c -- two bf16 terms (hi, lo);  RWHT: s_i H[i][c].
-__global__ void tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t* __restrict__ dec)
+// Decode "code mode" (uniform quantizer, every width <= 7): the A operand is
+// the exact bf16 number 128 + code, the image basis[i][c] * Delta_c, and the
+// decode adds dec_bias[i] = sum_c basis[i][c] (Delta_c / 2)(1 - 2^b_c)
+// - 128 sum_c image[i][c]  (so x_i = sum_c image[i][c] code_c + the affine
+// part of the dequantizer).  Otherwise A is the odd integer 2 code + 1 - 2^b
+// and the image basis * Delta / 2.
+__device__ __forceinline__ float dec_image_value(const PlanView& pv, int h, int i, int c, bool code_mode)
+{
+    if (pv.basis == SPECTRA_BASIS_RWHT) return float(pv.signs[size_t(h) * D + i] * hadamard_sign(i, c));
+    const float sc = pv.rscale[size_t(h) * D + c];
+    const float bij = pv.basis_mat[(size_t(h) * D + i) * D + c];
+    if (pv.quant != SPECTRA_Q_UNIFORM3S) return bij * sc;
+    if (code_mode) return pv.bits[size_t(h) * D + c] > 0 ? bij * sc : 0.f;
+    return bij * 0.5f * sc;
+}
+
+__global__ void tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t* __restrict__ dec,
+                                 int32_t* __restrict__ wmax_out, float* __restrict__ bias_out)
 {
     const int h = blockIdx.x;
     const bool rwht = pv.basis == SPECTRA_BASIS_RWHT;
+    __shared__ int wmax_s;
+    if (threadIdx.x == 0) wmax_s = 0;
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += blockDim.x) atomicMax(&wmax_s, int(pv.bits[size_t(h) * D + c]));
+    __syncthreads();
+    const bool code_mode = !rwht && pv.quant == SPECTRA_Q_UNIFORM3S && wmax_s <= 7;
+    if (threadIdx.x == 0) wmax_out[h] = wmax_s;
     uint8_t* e = enc + size_t(h) * enc_img_bytes(D);
     uint8_t* dd = dec + size_t(h) * dec_img_bytes(D);
     for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) {
@@ -823,21 +878,33 @@ __global__ void tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t
         }
         // decode: row = output i = r, K = channel c = kk
         {
-            float v;
-            if (rwht) v = float(pv.signs[size_t(h) * D + r] * hadamard_sign(r, kk));
-            else {
-                const float sc = pv.rscale[size_t(h) * D + kk];
-                v = pv.basis_mat[(size_t(h) * D + r) * D + kk] *
-                    (pv.quant == SPECTRA_Q_UNIFORM3S ? 0.5f * sc : sc);
-            }
             const int nt = rwht ? 1 : 2;
-            float rem = v;
+            float rem = dec_image_value(pv, h, r, kk, code_mode);
             for (int t = 0; t < nt; ++t) {
                 const __nv_bfloat16 b = __float2bfloat16_rn(rem);
                 *reinterpret_cast<__nv_bfloat16*>(dd + t * OPND + off) = b;
                 rem -= __bfloat162float(b);
             }
         }
+    }
+    // per-output offsets of code mode (sums of the rounded image terms)
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        float bias = 0.f;
+        if (code_mode) {
+            float aff = 0.f, img = 0.f;
+            for (int c = 0; c < D; ++c) {
+                const int b = pv.bits[size_t(h) * D + c];
+                if (b == 0) continue;
+                const float v = dec_image_value(pv, h, i, c, true);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+                img += __bfloat162float(hi) + __bfloat162float(lo);
+                aff = fmaf(pv.basis_mat[(size_t(h) * D + i) * D + c] * 0.5f * pv.rscale[size_t(h) * D + c],
+                           1.f - float(1 << b), aff);
+            }
+            bias = aff - 128.f * img;
+        }
+        bias_out[size_t(h) * D + i] = bias;
     }
 }
 
@@ -895,7 +962,8 @@ spectra_status launch_tc_images(const spectra_plan* plan, cudaStream_t s)
 {
     if (plan->head_dim != D) return SPECTRA_OK;
     const PlanView pv = make_view(plan);
-    tc_images_kernel<<<plan->heads, 256, 0, s>>>(pv, const_cast<uint8_t*>(pv.enc_img), const_cast<uint8_t*>(pv.dec_img));
+    tc_images_kernel<<<plan->heads, 256, 0, s>>>(pv, const_cast<uint8_t*>(pv.enc_img), const_cast<uint8_t*>(pv.dec_img),
+                                                  const_cast<int32_t*>(pv.wmax), const_cast<float*>(pv.dec_bias));
     return cuda_status(cudaGetLastError());
 }
 
@@ -923,9 +991,12 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
     P.norms = norms;
     P.nstride = nstride;
     const uint32_t sm = enc_smem_layout(P.nterms, P.stages, lm).total + 1024;
-    cudaFuncSetAttribute(encode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    const bool rw = plan->basis == SPECTRA_BASIS_RWHT;
+    auto kern = lm ? (rw ? encode_tc_kernel<true, true> : encode_tc_kernel<true, false>)
+                   : (rw ? encode_tc_kernel<false, true> : encode_tc_kernel<false, false>);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
     const int grid = min(sm_count(), P.total);
-    encode_tc_kernel<<<grid, kEncThreads, sm, s>>>(m, P);
+    kern<<<grid, kEncThreads, sm, s>>>(m, P);
     *done = true;
     return cuda_status(cudaGetLastError());
 }
@@ -962,9 +1033,10 @@ spectra_status launch_decode_tc(const spectra_plan* plan, const uint8_t* codes, 
     P.norms = norms;
     P.nstride = nstride;
     const uint32_t sm = total();
-    cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    auto kern = lm ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
     const int grid = min(sm_count(), P.total);
-    decode_tc_kernel<<<grid, kDecThreads, sm, s>>>(m, P);
+    kern<<<grid, kDecThreads, sm, s>>>(m, P);
     *done = true;
     return cuda_status(cudaGetLastError());
 }

@@ -25,9 +25,12 @@ constexpr int kLmStride = 256;      // row stride of the Lloyd-Max tables
 // Tensor-core operand images (codec_tc.cu):
 //   enc_img[h]  bf16 basis image for the encode contraction
 //   dec_img[h]  bf16 basis image for the decode contraction
+//   wmax[h]     i32 widest channel of head h
+//   dec_bias[h][i] f32 decode offset of output i (uniform quantizer, widths
+//               <= 7: the decode contraction then takes 128 + code)
 // ---------------------------------------------------------------------------
 struct DerivedLayout {
-    size_t chan_off, qscale, rscale, lm_level, lm_thresh, enc_img, dec_img, total;
+    size_t chan_off, qscale, rscale, lm_level, lm_thresh, enc_img, dec_img, wmax, dec_bias, total;
     size_t enc_img_head_bytes, dec_img_head_bytes;
 };
 
@@ -55,6 +58,8 @@ __host__ __device__ inline DerivedLayout derived_layout(int heads, int d)
     L.dec_img_head_bytes = dec_img_bytes(d);
     L.enc_img = o;   o = align256(o + size_t(heads) * L.enc_img_head_bytes);
     L.dec_img = o;   o = align256(o + size_t(heads) * L.dec_img_head_bytes);
+    L.wmax = o;      o = align256(o + size_t(heads) * sizeof(int32_t));
+    L.dec_bias = o;  o = align256(o + hd * sizeof(float));
     L.total = o;
     return L;
 }
@@ -74,6 +79,8 @@ struct PlanView {
     const float* lm_thresh;
     const uint8_t* enc_img;
     const uint8_t* dec_img;
+    const int32_t* wmax;
+    const float* dec_bias;
     int32_t* status;
 };
 
@@ -99,6 +106,8 @@ inline PlanView make_view(const spectra_plan* p)
     v.lm_thresh = reinterpret_cast<const float*>(base + L.lm_thresh);
     v.enc_img = base + L.enc_img;
     v.dec_img = base + L.dec_img;
+    v.wmax = reinterpret_cast<const int32_t*>(base + L.wmax);
+    v.dec_bias = reinterpret_cast<const float*>(base + L.dec_bias);
     v.status = p->status;
     return v;
 }
