@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=T_TOK,
                     help="tokens per head (default: the Llama-shaped layer's 32768); other values are "
                          "for profiling captures, not bench lines")
+    ap.add_argument("--no-attn-workload", dest="attn_workload", action="store_false",
+                    help="skip the separate compressed-attention measurement")
     ap.add_argument("--copies", type=int, default=NCOPY,
                     help="rotating input/output copies (L2 defeat); fewer for profiling captures")
     return ap.parse_args()
@@ -243,6 +245,8 @@ def run_ours(args, rank, world, local_rank):
             "peak_source": peaks["source"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": None}
 
+    attn = attn_workload(spx, kp, vp, dev, _peaks()) if args.attn_workload else None
+
     tokens = T_TOK * world
     res = {
         "metric": METRIC, "value": round(tokens / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
@@ -256,12 +260,61 @@ def run_ours(args, rank, world, local_rank):
         "jacobi_sweeps": {"min": min(sweeps), "max": max(sweeps)},
         "codec_tokens_per_s": round(T_TOK / ((ph["encode"] + ph["decode"]) * 1e-3), 1),
         "roofline": roof,
+        "attn_decode": attn,
         "clocks": clocks,
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": args.steps * launches_per_step(),
     }
     return res
+
+
+ATTN_B, ATTN_CTX = 16, 65536
+
+
+def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3):
+    """Decode-step attention at the compressed-attention workload: batch 16,
+    32 query heads over 8 kv heads, 65536-token context packed at the plans'
+    2.0 bits/value (K and V streams of 16 x 8 x 65536 tokens).  The stream
+    contents are seeded random words -- every bit pattern is a valid code and
+    the kernel's work does not depend on the values.  Two rotating stream
+    sets (2 x 537 MB) keep each call's reads out of L2.  Timed with CUDA
+    events on the launching stream; GB/s counts the packed bytes read."""
+    import torch
+    R = kp.max_rec_bits
+    sb = spx.spectra_stream_bytes(R, ATTN_CTX)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    sets = []
+    for _ in range(2):
+        kc = torch.randint(0, 256, (ATTN_B * H_KV, sb), dtype=torch.uint8, device=dev, generator=gen)
+        vc = torch.randint(0, 256, (ATTN_B * H_KV, sb), dtype=torch.uint8, device=dev, generator=gen)
+        sets.append((kc, vc))
+    q = torch.randn((ATTN_B, HQ, D), device=dev, generator=gen).mul_(D ** -0.5).to(torch.bfloat16)
+    out = torch.empty((ATTN_B, HQ, D), dtype=torch.float32, device=dev)
+    ws = torch.empty((spx.spectra_attn_workspace_bytes(ATTN_B, HQ, D, ATTN_CTX) + 256,), dtype=torch.uint8,
+                     device=dev)
+    s = torch.cuda.current_stream()
+    for i in range(warm):
+        kc, vc = sets[i % 2]
+        spx.spectra_attn_decode(kp, vp, q, kc, vc, ATTN_CTX, 1.0, out, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(reps):
+        kc, vc = sets[i % 2]
+        spx.spectra_attn_decode(kp, vp, q, kc, vc, ATTN_CTX, 1.0, out, workspace=ws)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = 2 * ATTN_B * H_KV * (ATTN_CTX // 32) * 4 * R      # packed K and V words read
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del sets
+    return {"workload": f"batch {ATTN_B}, {HQ} q heads / {H_KV} kv heads, d {D}, context {ATTN_CTX}, "
+                        f"{R} bits per token and head (K and V)", "ms": round(ms, 4),
+            "packed_bytes": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": peaks["hbm_gbs"],
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "cached_tokens_per_s": round(ATTN_B * ATTN_CTX / (ms * 1e-3), 1),
+            "l2": "2 rotating stream sets (2 x 537 MB) > L2"}
 
 
 def launches_per_step():
@@ -299,11 +352,16 @@ def _max_over_ranks(v, world):
 
 
 # ---------------------------------------------------------------- oracle
-def oracle_sample(seconds_budget: float = 20.0):
-    """Time the CPU oracle on a bounded sample of the workload: calibrate K
-    and V (2048 tokens, 8 heads), allocate, encode+decode a slice of tokens
-    for all heads, attention over that slice; scale the per-token parts to
-    32768 tokens.  Heads run on a thread pool (ctypes releases the GIL)."""
+_ORACLE_INPUTS = {}
+
+
+def oracle_sample(min_seconds: float = 10.0):
+    """Time the CPU oracle (as it stands) on the benchmark workload: whole
+    passes of calibrate K and V (2048 tokens, 8 heads) -> allocate -> encode
+    and decode all 32768 tokens of every head -> attention of the 32 query
+    heads over the whole cache, repeated until at least `min_seconds` of
+    CPU work have run (at least one pass).  Heads run on a thread pool
+    (ctypes releases the GIL); `cores` is the pool size."""
     from concurrent.futures import ThreadPoolExecutor
 
     import numpy as np
@@ -312,52 +370,61 @@ def oracle_sample(seconds_budget: float = 20.0):
     import synth
 
     cores = min(2 * H_KV, os.cpu_count() or 1)
-    n_tok = 8192
-    Kx = synth.to_bf16_exact(synth.spiked_t(7, N_CAL, H_KV, D, role=synth.ROLE_K)).astype(np.float64)
-    Vx = synth.to_bf16_exact(synth.spiked_t(7, N_CAL, H_KV, D, role=synth.ROLE_V)).astype(np.float64)
+    if not _ORACLE_INPUTS:
+        _ORACLE_INPUTS["K"] = synth.to_bf16_exact(synth.spiked_t(7, T_TOK, H_KV, D, role=synth.ROLE_K)).astype(np.float64)
+        _ORACLE_INPUTS["V"] = synth.to_bf16_exact(synth.spiked_t(7, T_TOK, H_KV, D, role=synth.ROLE_V)).astype(np.float64)
+        _ORACLE_INPUTS["q"] = synth.queries(1, 1, HQ, D).astype(np.float64)
+    Kx, Vx, q = _ORACLE_INPUTS["K"], _ORACLE_INPUTS["V"], _ORACLE_INPUTS["q"]
     orc.lloyd_max_tables()
     pool = ThreadPoolExecutor(cores)
-    t0 = time.perf_counter()
-    # calibrate: per head in parallel
+
     def cal(job):
         x, h = job
-        lam, Q, _ = orc.jacobi_eigh(orc.gram(x[:, h, :]))
+        lam, Q, _ = orc.jacobi_eigh(orc.gram(x[:N_CAL, h, :]))
         return lam, Q
-    res = list(pool.map(cal, [(x, h) for x in (Kx, Vx) for h in range(H_KV)]))
-    t_cal = time.perf_counter() - t0
-    t1 = time.perf_counter()
-    plans = []
-    for side in range(2):
-        lam = np.stack([res[side * H_KV + h][0] for h in range(H_KV)]).astype(np.float32).astype(np.float64)
-        Q = np.stack([res[side * H_KV + h][1] for h in range(H_KV)]).astype(np.float32).astype(np.float64)
-        R = orc.total_bits(AVG_BITS, D)
-        bits = np.stack([orc.alloc(lam[h], R) for h in range(H_KV)])
-        plans.append(orc.Plan(orc.BASIS_EIGEN, orc.QUANT_UNIFORM, bits, basis=Q, eigvals=lam))
-    t_alloc = time.perf_counter() - t1
-    t2 = time.perf_counter()
-    xs = (Kx[:n_tok], Vx[:n_tok])
 
-    def encdec(job):
-        side, h = job
-        e = orc.encode_head(plans[side], h, xs[side][:, h, :])
-        return orc.decode_head(plans[side], h, e["stream"], n_tok)
-    rec = list(pool.map(encdec, [(s, h) for s in range(2) for h in range(H_KV)]))
-    t_encdec = time.perf_counter() - t2
-    t3 = time.perf_counter()
-    q = synth.queries(1, 1, HQ, D).astype(np.float64)
-    Kh = np.stack([rec[h] for h in range(H_KV)], 1)[None]
-    Vh = np.stack([rec[H_KV + h] for h in range(H_KV)], 1)[None]
-    orc.attn_decode(q, Kh, Vh, 1.0)
-    t_attn = time.perf_counter() - t3
-    scale = T_TOK / n_tok
-    est = t_cal + t_alloc + (t_encdec + t_attn) * scale
-    return {"value": round(T_TOK / est, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": (f"calibrate K,V (2048 tok x 8 heads) + alloc measured in full; encode+decode "
-                       f"and attention measured on {n_tok} of {T_TOK} tokens (all heads) and scaled "
-                       f"x{scale:g}; wall {t_cal + t_alloc + t_encdec + t_attn:.1f} s"),
-            "seconds": {"calibrate": round(t_cal, 3), "alloc": round(t_alloc, 4),
-                        "encode_decode_sample": round(t_encdec, 3), "attn_sample": round(t_attn, 3)},
-            "est_step_s": round(est, 3)}
+    def one_pass():
+        t = {}
+        t0 = time.perf_counter()
+        res = list(pool.map(cal, [(x, h) for x in (Kx, Vx) for h in range(H_KV)]))
+        t["calibrate"] = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        plans = []
+        for side in range(2):
+            lam = np.stack([res[side * H_KV + h][0] for h in range(H_KV)]).astype(np.float32).astype(np.float64)
+            Q = np.stack([res[side * H_KV + h][1] for h in range(H_KV)]).astype(np.float32).astype(np.float64)
+            R = orc.total_bits(AVG_BITS, D)
+            bits = np.stack([orc.alloc(lam[h], R) for h in range(H_KV)])
+            plans.append(orc.Plan(orc.BASIS_EIGEN, orc.QUANT_UNIFORM, bits, basis=Q, eigvals=lam))
+        t["alloc"] = time.perf_counter() - t1
+        t2 = time.perf_counter()
+        xs = (Kx, Vx)
+
+        def encdec(job):
+            side, h = job
+            e = orc.encode_head(plans[side], h, xs[side][:, h, :])
+            return orc.decode_head(plans[side], h, e["stream"], T_TOK)
+        rec = list(pool.map(encdec, [(sd, h) for sd in range(2) for h in range(H_KV)]))
+        t["encode_decode"] = time.perf_counter() - t2
+        t3 = time.perf_counter()
+        Kh = np.stack([rec[h] for h in range(H_KV)], 1)[None]
+        Vh = np.stack([rec[H_KV + h] for h in range(H_KV)], 1)[None]
+        orc.attn_decode(q, Kh, Vh, 1.0)
+        t["attn"] = time.perf_counter() - t3
+        return t
+
+    passes = []
+    t_all = time.perf_counter()
+    while not passes or time.perf_counter() - t_all < min_seconds:
+        passes.append(one_pass())
+    wall = time.perf_counter() - t_all
+    step_s = wall / len(passes)
+    return {"value": round(T_TOK / step_s, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{len(passes)} whole pass(es) of the workload (calibrate K,V on 2048 tokens x 8 heads, "
+                       f"allocate, encode+decode {T_TOK} tokens x 8 heads x K,V, attention of {HQ} q heads "
+                       f"over the cache); wall {wall:.1f} s"),
+            "seconds_per_pass": {k: round(statistics.mean(p[k] for p in passes), 3) for k in passes[0]},
+            "est_step_s": round(step_s, 3)}
 
 
 def run_reference(args, rank, world):
@@ -368,7 +435,7 @@ def run_reference(args, rank, world):
     vals = []
     t_all = time.perf_counter()
     for i in range(args.warmup + args.steps):
-        r = oracle_sample()
+        r = oracle_sample(min_seconds=0.0)
         if i >= args.warmup:
             vals.append(r)
         if time.perf_counter() - t_all > 240 and len(vals) >= 1:

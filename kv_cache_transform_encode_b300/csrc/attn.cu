@@ -207,58 +207,78 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
     }
 }
 
+// One block per (batch, kv head): merge the context splits of its G query
+// heads, then out[b, j] = B_V latent_j with B_V staged once in shared memory
+// (rows padded to D + 1 floats: conflict-free row reads).
 // code_domain: the partials hold sum_t p_t code_c(t) (tensor-core path,
 // uniform quantizer); the merged value is dequantized as
 // Delta_c (code_mean + (1 - 2^b) / 2) before the rotation.
-__global__ void attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsplit,
-                                    int code_domain, float* __restrict__ out)
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsplit, int code_domain,
+                    float* __restrict__ out)
 {
-    const int D = vp.d;
-    const int bj = blockIdx.x, j = bj % Hq;
-    const int h = j / (Hq / vp.heads);
-    extern __shared__ float os[];
-    __shared__ float sM, sL;
-    const float* pp = part + int64_t(bj) * nsplit * (D + 2);
-    if (threadIdx.x < 32) {
+    const int D = vp.d, Hkv = vp.heads, G = Hq / Hkv;
+    const int bh = blockIdx.x, h = bh % Hkv, b = bh / Hkv;
+    const int LD = D + 1;
+    extern __shared__ float sm[];
+    float* Bs = sm;                     // [D][LD]
+    float* os = Bs + D * LD;            // [G][D]
+    float* stat = os + G * D;           // [G][2]: M, L
+    const bool eig = vp.basis == SPECTRA_BASIS_EIGEN;
+    if (eig) {
+        const float4* src = reinterpret_cast<const float4*>(vp.basis_mat + size_t(h) * D * D);
+        for (int e = threadIdx.x; e < D * D / 4; e += blockDim.x) {
+            const float4 v = src[e];
+            const int i = (4 * e) / D, c = (4 * e) % D;
+            float* d = Bs + i * LD + c;
+            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+        }
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int j = warp; j < G; j += nw) {
+        const float* pp = part + (int64_t(b) * Hq + h * G + j) * nsplit * (D + 2);
         float M = -INFINITY;
-        for (int s = threadIdx.x; s < nsplit; s += 32) M = fmaxf(M, pp[int64_t(s) * (D + 2)]);
+        for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, pp[int64_t(s) * (D + 2)]);
         for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float L = 0.f;
-        for (int s = threadIdx.x; s < nsplit; s += 32) {
+        for (int s = lane; s < nsplit; s += 32) {
             const float m = pp[int64_t(s) * (D + 2)];
             if (m != -INFINITY) L += pp[int64_t(s) * (D + 2) + 1] * __expf(m - M);
         }
         for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (threadIdx.x == 0) { sM = M; sL = L; }
+        if (lane == 0) { stat[2 * j] = M; stat[2 * j + 1] = L; }
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+        const int j = e / D, c = e % D;
+        const float* pp = part + (int64_t(b) * Hq + h * G + j) * nsplit * (D + 2);
+        const float M = stat[2 * j], L = stat[2 * j + 1];
         float a = 0.f;
         for (int s = 0; s < nsplit; ++s) {
             const float m = pp[int64_t(s) * (D + 2)];
-            if (m != -INFINITY) a += pp[int64_t(s) * (D + 2) + 2 + c] * __expf(m - sM);
+            if (m != -INFINITY) a += pp[int64_t(s) * (D + 2) + 2 + c] * __expf(m - M);
         }
-        float y = (sL > 0.f) ? a / sL : 0.f;
+        float y = (L > 0.f) ? a / L : 0.f;
         if (code_domain) {
             const int bc = vp.bits[size_t(h) * D + c];
             y = (bc > 0) ? vp.rscale[size_t(h) * D + c] * (y + 0.5f * (1.f - float(1 << bc))) : 0.f;
         }
-        os[c] = y;
+        os[j * D + c] = y;
     }
     __syncthreads();
-    // out_i = sum_c B_V[i][c] os[c]: one warp per output row (coalesced row reads)
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    for (int i = warp; i < D; i += nw) {
+    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+        const int j = e / D, i = e % D;
         float a = 0.f;
-        for (int c = lane; c < D; c += 32) {
-            const float bic = (vp.basis == SPECTRA_BASIS_EIGEN) ? vp.basis_mat[(size_t(h) * D + i) * D + c]
-                                                                : basis_entry(vp, h, i, c, D);
-            a = fmaf(bic, os[c], a);
+        if (eig) {
+            for (int c = 0; c < D; ++c) a = fmaf(Bs[i * LD + c], os[j * D + c], a);
+        } else {
+            for (int c = 0; c < D; ++c) a = fmaf(basis_entry(vp, h, i, c, D), os[j * D + c], a);
         }
-        for (int o = 16; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        if (lane == 0) out[int64_t(bj) * D + i] = a;
+        out[(int64_t(b) * Hq + h * G + j) * D + i] = a;
     }
 }
+
+size_t combine_smem(int D, int G) { return sizeof(float) * (size_t(D) * (D + 1) + size_t(G) * D + 2 * G); }
 
 template <int D>
 size_t split_smem()
@@ -292,6 +312,14 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
                               float scale, float* part, int nsplit, int split_len, void* extra,
                               cudaStream_t s, bool* done);
 
+void launch_combine(const PlanView& vp, const float* part, int B, int Hq, int nsplit, int code_domain, float* out,
+                    cudaStream_t s)
+{
+    const size_t sm = combine_smem(vp.d, Hq / vp.heads);
+    cudaFuncSetAttribute(attn_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    attn_combine_kernel<<<B * vp.heads, 256, sm, s>>>(vp, part, Hq, nsplit, code_domain, out);
+}
+
 // [qt (B Hq d f32) | split partials | tensor-core operands (sized for Hkv <= Hq)]
 size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx)
 {
@@ -321,7 +349,7 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
                                            split_len, extra, s, &done);
         if (st) return st;
         if (done) {
-            attn_combine_kernel<<<B * Hq, D, D * sizeof(float), s>>>(vp, part, Hq, nsplit, 1, out);
+            launch_combine(vp, part, B, Hq, nsplit, 1, out, s);
             return cuda_status(cudaGetLastError());
         }
         if (attn_path() == 't') return SPECTRA_ERR_UNSUPPORTED;
@@ -339,7 +367,7 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
         attn_split_kernel<64><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
                                                          nstride, nsplit, split_len, part);
     }
-    attn_combine_kernel<<<B * Hq, D, D * sizeof(float), s>>>(vp, part, Hq, nsplit, 0, out);
+    launch_combine(vp, part, B, Hq, nsplit, 0, out, s);
     return cuda_status(cudaGetLastError());
 }
 

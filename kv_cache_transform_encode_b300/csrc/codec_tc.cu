@@ -44,6 +44,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 namespace spectra {
@@ -61,16 +62,50 @@ constexpr int kEncThreads = 576;          // producer, MMA, 16 epilogue warps
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // ------------------------------------------------------------------ helpers
-struct Work {
-    int begin, end;        // this CTA's item range
+// Work schedule of a persistent CTA over the (head, 128-token tile) items.
+// Interleaved (the grid a multiple of the head count): CTA c keeps head
+// c mod H and walks tiles j, j + cph, j + 2 cph, ... (j = c / H, cph = CTAs
+// per head), so the CTAs of all heads move through the same token range
+// together -- each [token][heads][d] row of the cache is read (or written)
+// whole at about the same time, which keeps DRAM pages open -- and every
+// CTA loads its operand image once.  Contiguous (otherwise): one range of
+// the head-major item list per CTA.
+struct Sched {
+    int interleaved, head, j, cph, begin, n, tiles;
+    __device__ __forceinline__ int head_of(int k) const { return interleaved ? head : (begin + k) / tiles; }
+    __device__ __forceinline__ int tile_of(int k) const { return interleaved ? j + k * cph : (begin + k) % tiles; }
 };
 
-__device__ __forceinline__ Work cta_work(int total)
+__device__ __forceinline__ Sched make_sched(int heads, int tiles)
 {
-    Work w;
-    w.begin = int((int64_t(total) * blockIdx.x) / gridDim.x);
-    w.end = int((int64_t(total) * (blockIdx.x + 1)) / gridDim.x);
-    return w;
+    Sched S;
+    S.tiles = tiles;
+    const int G = int(gridDim.x);
+    if (G >= heads && G % heads == 0) {
+        S.interleaved = 1;
+        S.cph = G / heads;
+        S.head = int(blockIdx.x) % heads;
+        S.j = int(blockIdx.x) / heads;
+        S.begin = 0;
+        S.n = (tiles > S.j) ? (tiles - S.j + S.cph - 1) / S.cph : 0;
+    } else {
+        const int64_t total = int64_t(heads) * tiles;
+        S.interleaved = 0;
+        S.cph = S.head = S.j = 0;
+        S.begin = int((total * blockIdx.x) / G);
+        S.n = int((total * (blockIdx.x + 1)) / G) - S.begin;
+    }
+    return S;
+}
+
+// grid of the persistent kernels: interleaved when the heads fit the SMs
+inline int sched_grid(int sms, int heads, int tiles)
+{
+    if (heads <= sms) {
+        const int cph = std::min(sms / heads, tiles);
+        return cph * heads;
+    }
+    return std::min<int64_t>(sms, int64_t(heads) * tiles);
 }
 
 // ------------------------------------------------------------------ pack helpers
@@ -150,7 +185,7 @@ __host__ __device__ inline EncSmem enc_smem_layout(int nterms, int stages, bool 
 {
     EncSmem L;
     uint32_t o = 0;
-    L.img = o;  o += nterms * OPND;
+    L.img = o;  o += 0;                          // the basis image lives in tensor memory
     L.xs = o;   o += stages * OPND;
     L.th = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
     L.red = o;  o += (4 * 4 * 32 + 16 * 32) * 4;     // RWHT norm partials and inverses
@@ -174,28 +209,27 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     constexpr bool lm = LM;
     constexpr bool rwht = RWHT;
     const EncSmem L = enc_smem_layout(P.nterms, P.stages, lm);
-    uint8_t* img = smem + L.img;
     uint8_t* xs = smem + L.xs;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-    uint64_t* full = bars;                 // [stages <= 4]
-    uint64_t* empty = bars + 4;            // [stages]
-    uint64_t* accfull = bars + 8;          // [2]
-    uint64_t* accempty = bars + 10;        // [2]
-    uint64_t* imgfull = bars + 12;
-    uint64_t* imgempty = bars + 13;
-    uint64_t* drain = bars + 14;
-    uint64_t* rbar = bars + 15;            // [4] RWHT norm rendezvous, one per token group
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 20);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
+    uint64_t* full = bars;                 // [stages <= 8]
+    uint64_t* empty = bars + 8;            // [stages]
+    uint64_t* accfull = bars + 16;         // [2]
+    uint64_t* accempty = bars + 18;        // [2]
+    uint64_t* imgfull = bars + 20;
+    uint64_t* imgempty = bars + 21;
+    uint64_t* drain = bars + 22;
+    uint64_t* rbar = bars + 23;            // [4] RWHT norm rendezvous, one per token group
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 28);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 29);
     volatile int* drain_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Work W = cta_work(P.total);
+    const Sched S = make_sched(P.pv.heads, P.tiles_per_head);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P.stages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], 1); mbar_init(&accempty[a], kEncEpiWarps); }
-        mbar_init(imgfull, 1);
+        mbar_init(imgfull, 4);             // the four loader warps (token group 0)
         mbar_init(imgempty, 1);
         mbar_init(drain, 1);
         for (int g = 0; g < 4; ++g) mbar_init(&rbar[g], 4);
@@ -204,7 +238,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, 256);
+        tmem_alloc(tmem_holder, 512);      // accumulators: columns 0..255; basis image: 256..447
         tmem_relinquish();
     }
     if (lm) {
@@ -219,21 +253,10 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            int k = 0, j = 0, cur_h = -1;
-            int last_issued[4] = {-1, -1, -1, -1};
-            int img_issued = 0;
-            for (int w = W.begin; w < W.end; ++w, ++k) {
-                const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
-                if (h != cur_h) {
-                    if (j > 0 && !mbar_wait(imgempty, (j - 1) & 1, abort_flag, kWaitNs)) break;
-                    const uint32_t bytes = P.nterms * OPND;
-                    mbar_arrive_expect_tx(imgfull, bytes);
-                    const uint8_t* src = P.pv.enc_img + size_t(h) * enc_img_bytes(D);
-                    for (uint32_t o = 0; o < bytes; o += 32768u) bulk_load(img + o, src + o, 32768u, imgfull);
-                    img_issued = j + 1;
-                    cur_h = h;
-                    ++j;
-                }
+            int k = 0;
+            int last_issued[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+            for (; k < S.n; ++k) {
+                const int h = S.head_of(k), tile = S.tile_of(k);
                 const int s = k % P.stages;
                 if (k >= P.stages && !mbar_wait(&empty[s], ((k / P.stages) - 1) & 1, abort_flag, kWaitNs)) break;
                 mbar_arrive_expect_tx(&full[s], OPND);
@@ -246,7 +269,6 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                 for (int s = 0; s < P.stages; ++s)
                     if (last_issued[s] >= 0)
                         mbar_wait(&full[s], (last_issued[s] / P.stages) & 1, drain_flag, 100000000ull);
-                if (img_issued > 0) mbar_wait(imgfull, (img_issued - 1) & 1, drain_flag, 100000000ull);
             }
         }
     } else if (warp == 1) {
@@ -254,8 +276,8 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         if (lane == 0) {
             int k = 0, j = 0, cur_h = -1;
             bool issued = false;
-            for (int w = W.begin; w < W.end; ++w, ++k) {
-                const int h = w / P.tiles_per_head;
+            for (; k < S.n; ++k) {
+                const int h = S.head_of(k);
                 if (h != cur_h) {
                     if (!mbar_wait(imgfull, j & 1, abort_flag, kWaitNs)) break;
                     cur_h = h;
@@ -266,19 +288,18 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                 if (k >= 2 && !mbar_wait(&accempty[a], ((k >> 1) - 1) & 1, abort_flag, kWaitNs)) break;
                 tc_fence_after();
                 const uint32_t xa = smem_u32(xs + s * OPND);
-                const uint32_t ia = smem_u32(img);
                 const uint32_t d_tmem = tmem + a * 128;
                 for (int t = 0; t < P.nterms; ++t)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t koff = (kk >> 2) * KBLK + (kk & 3) * 32;
-                        mma_bf16_ss(d_tmem, sdesc_sw128(ia + t * OPND + koff), sdesc_sw128(xa + koff), IDESC,
+                        mma_bf16_ts(d_tmem, tmem + 256 + t * 64 + kk * 8, sdesc_sw128(xa + koff), IDESC,
                                     (t | kk) ? 1u : 0u);
                     }
                 issued = true;
                 mma_commit(&empty[s]);
                 mma_commit(&accfull[a]);
-                const bool head_ends = (w + 1 == W.end) || ((w + 1) / P.tiles_per_head != h);
+                const bool head_ends = (k + 1 == S.n) || (S.head_of(k + 1) != h);
                 if (head_ends) mma_commit(imgempty);
             }
             if (issued) {   // every MMA of this CTA done before TMEM is released
@@ -294,12 +315,35 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         const float* th = reinterpret_cast<const float*>(smem + L.th);
         float* part = reinterpret_cast<float*>(smem + L.red) + gi * (4 * 32);          // [4 q][32 t]
         float* invs = reinterpret_cast<float*>(smem + L.red) + 4 * 4 * 32 + (warp - 2) * 32;
-        int k = 0, cur_h = -1, R = 0, b = 0, o = 0, bmax = 0, ruse = 0;
+        int k = 0, cur_h = -1, R = 0, b = 0, o = 0, bmax = 0, ruse = 0, nimg = 0;
         float qk = 0.f, cl = 0.f;
         bool head_ok = true;
-        for (int w = W.begin; w < W.end; ++w, ++k) {
-            const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+        for (; k < S.n; ++k) {
+            const int h = S.head_of(k), tile = S.tile_of(k);
             if (h != cur_h) {
+                if (gi == 0) {
+                    // the head's basis image -> TMEM columns 256.. (lane = channel):
+                    // after the MMAs of the previous head are done
+                    if (nimg > 0 && !mbar_wait(imgempty, (nimg - 1) & 1, abort_flag, kWaitNs)) break;
+                    tc_fence_after();
+                    const uint4* src = reinterpret_cast<const uint4*>(P.pv.enc_img + size_t(h) * enc_img_bytes(D) +
+                                                                      size_t(c) * 256);
+                    for (int t = 0; t < P.nterms; ++t)
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t r[32];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const uint4 v = src[t * (OPND / 16) + half * 8 + e];
+                                r[4 * e] = v.x; r[4 * e + 1] = v.y; r[4 * e + 2] = v.z; r[4 * e + 3] = v.w;
+                            }
+                            tmem_st32(tmem + (uint32_t(q * 32) << 16) + 256 + t * 64 + half * 32, r);
+                        }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(imgfull);
+                    ++nimg;
+                }
                 cur_h = h;
                 R = P.pv.rec_bits[h];
                 head_ok = R <= P.pv.max_rec_bits;
@@ -394,13 +438,11 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
-        for (int w = W.begin; w < W.end; w += P.tiles_per_head)
-            P.pv.status[w / P.tiles_per_head] = -SPECTRA_ERR_TIMEOUT;
-        if (W.end > W.begin) P.pv.status[(W.end - 1) / P.tiles_per_head] = -SPECTRA_ERR_TIMEOUT;
+        for (int kk = 0; kk < S.n; ++kk) P.pv.status[S.head_of(kk)] = -SPECTRA_ERR_TIMEOUT;
     }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -514,7 +556,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
     volatile int* drain_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Work W = cta_work(P.total);
+    const Sched S = make_sched(P.pv.heads, P.tiles_per_head);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P.cstages; ++s) { mbar_init(&cfull[s], 1); mbar_init(&cempty[s], kDecUnpackWarps); }
@@ -547,8 +589,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             int k = 0, j = 0, cur_h = -1, R = 0;
             int last_issued[4] = {-1, -1, -1, -1};
             int img_issued = 0;
-            for (int w = W.begin; w < W.end; ++w, ++k) {
-                const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+            for (; k < S.n; ++k) {
+                const int h = S.head_of(k), tile = S.tile_of(k);
                 if (h != cur_h) {
                     if (j > 0 && !mbar_wait(imgempty, (j - 1) & 1, abort_flag, kWaitNs)) break;
                     const uint32_t bytes = P.nterms * OPND;
@@ -595,8 +637,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             const int npr = !lm ? P.nterms : (!rwht ? 3 : 2);
             const uint32_t pa = !lm ? 0u : (!rwht ? 0x010u : 0x10u);    // nibble pr: A term
             const uint32_t pb = !lm ? 0x10u : (!rwht ? 0x100u : 0x00u); // nibble pr: image term
-            for (int w = W.begin; w < W.end; ++w, ++k) {
-                const int h = w / P.tiles_per_head;
+            for (; k < S.n; ++k) {
+                const int h = S.head_of(k);
                 if (h != cur_h) {
                     if (!mbar_wait(imgfull, j & 1, abort_flag, kWaitNs)) break;
                     cur_h = h;
@@ -621,7 +663,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 issued = true;
                 mma_commit(&aempty[s]);
                 mma_commit(&accfull[a]);
-                const bool head_ends = (w + 1 == W.end) || ((w + 1) / P.tiles_per_head != h);
+                const bool head_ends = (k + 1 == S.n) || (S.head_of(k + 1) != h);
                 if (head_ends) mma_commit(imgempty);
             }
             if (issued) {
@@ -638,8 +680,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         int k = 0, cur_h = -1, R = 0, b0 = 0, b1 = 0, o0 = 0, o1 = 0, bmax = 0;
         float off0 = 0.f, off1 = 0.f;
         bool code_mode = false;
-        for (int w = W.begin; w < W.end; ++w, ++k) {
-            const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+        for (; k < S.n; ++k) {
+            const int h = S.head_of(k), tile = S.tile_of(k);
             if (h != cur_h) {
                 cur_h = h;
                 R = P.pv.rec_bits[h];
@@ -726,8 +768,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             ++euse;
             return r;
         };
-        for (int w = W.begin; w < W.end && ok; ++w, ++k) {
-            const int h = w / P.tiles_per_head, tile = w % P.tiles_per_head;
+        for (; k < S.n && ok; ++k) {
+            const int h = S.head_of(k), tile = S.tile_of(k);
             if (h != cur_h) {       // code mode: per-output offsets of this head
                 cur_h = h;
                 code_mode = !lm && !rwht && P.pv.wmax[h] <= 7;
@@ -813,9 +855,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
-        for (int w = W.begin; w < W.end; w += P.tiles_per_head)
-            P.pv.status[w / P.tiles_per_head] = -SPECTRA_ERR_TIMEOUT;
-        if (W.end > W.begin) P.pv.status[(W.end - 1) / P.tiles_per_head] = -SPECTRA_ERR_TIMEOUT;
+        for (int kk = 0; kk < S.n; ++kk) P.pv.status[S.head_of(kk)] = -SPECTRA_ERR_TIMEOUT;
     }
     if (warp == 1) {
         tc_fence_after();
@@ -846,10 +886,15 @@ __device__ __forceinline__ float dec_image_value(const PlanView& pv, int h, int 
     return bij * 0.5f * sc;
 }
 
-__global__ void tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t* __restrict__ dec,
-                                 int32_t* __restrict__ wmax_out, float* __restrict__ bias_out)
+// grid (heads, D / 16): block (h, part) writes rows [16 part, 16 part + 16)
+// of both images of head h and the decode offsets of those output rows.
+constexpr int kImgRows = 16;
+
+__global__ void __launch_bounds__(256)
+tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t* __restrict__ dec,
+                 int32_t* __restrict__ wmax_out, float* __restrict__ bias_out)
 {
-    const int h = blockIdx.x;
+    const int h = blockIdx.x, r0 = blockIdx.y * kImgRows;
     const bool rwht = pv.basis == SPECTRA_BASIS_RWHT;
     __shared__ int wmax_s;
     if (threadIdx.x == 0) wmax_s = 0;
@@ -857,11 +902,11 @@ __global__ void tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t
     for (int c = threadIdx.x; c < D; c += blockDim.x) atomicMax(&wmax_s, int(pv.bits[size_t(h) * D + c]));
     __syncthreads();
     const bool code_mode = !rwht && pv.quant == SPECTRA_Q_UNIFORM3S && wmax_s <= 7;
-    if (threadIdx.x == 0) wmax_out[h] = wmax_s;
+    if (threadIdx.x == 0 && blockIdx.y == 0) wmax_out[h] = wmax_s;
     uint8_t* e = enc + size_t(h) * enc_img_bytes(D);
     uint8_t* dd = dec + size_t(h) * dec_img_bytes(D);
-    for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) {
-        const int r = idx / D, kk = idx % D;   // row, K index
+    for (int idx = threadIdx.x; idx < kImgRows * D; idx += blockDim.x) {
+        const int r = r0 + idx / D, kk = idx % D;   // row, K index
         const uint32_t off = (kk >> 6) * KBLK + sw128_offset(r, (kk & 63) * 2);
         // encode: row = channel r, K = input i = kk
         {
@@ -870,9 +915,9 @@ __global__ void tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t
             else v = pv.basis_mat[(size_t(h) * D + kk) * D + r];
             const int nt = rwht ? 1 : 3;
             float rem = v;
-            for (int t = 0; t < nt; ++t) {
+            for (int t = 0; t < nt; ++t) {   // row-major [channel][input] (tensor-memory A operand)
                 const __nv_bfloat16 b = __float2bfloat16_rn(rem);
-                *reinterpret_cast<__nv_bfloat16*>(e + t * OPND + off) = b;
+                *reinterpret_cast<__nv_bfloat16*>(e + t * OPND + size_t(r) * 256 + kk * 2) = b;
                 rem -= __bfloat162float(b);
             }
         }
@@ -887,12 +932,14 @@ __global__ void tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t
             }
         }
     }
-    // per-output offsets of code mode (sums of the rounded image terms)
-    for (int i = threadIdx.x; i < D; i += blockDim.x) {
-        float bias = 0.f;
+    // per-output offsets of code mode (sums of the rounded image terms):
+    // one warp per output row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int ri = warp; ri < kImgRows; ri += blockDim.x >> 5) {
+        const int i = r0 + ri;
+        float aff = 0.f, img = 0.f;
         if (code_mode) {
-            float aff = 0.f, img = 0.f;
-            for (int c = 0; c < D; ++c) {
+            for (int c = lane; c < D; c += 32) {
                 const int b = pv.bits[size_t(h) * D + c];
                 if (b == 0) continue;
                 const float v = dec_image_value(pv, h, i, c, true);
@@ -902,9 +949,12 @@ __global__ void tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t
                 aff = fmaf(pv.basis_mat[(size_t(h) * D + i) * D + c] * 0.5f * pv.rscale[size_t(h) * D + c],
                            1.f - float(1 << b), aff);
             }
-            bias = aff - 128.f * img;
+            for (int o = 16; o; o >>= 1) {
+                aff += __shfl_xor_sync(0xffffffffu, aff, o);
+                img += __shfl_xor_sync(0xffffffffu, img, o);
+            }
         }
-        bias_out[size_t(h) * D + i] = bias;
+        if (lane == 0) bias_out[size_t(h) * D + i] = code_mode ? aff - 128.f * img : 0.f;
     }
 }
 
@@ -962,7 +1012,7 @@ spectra_status launch_tc_images(const spectra_plan* plan, cudaStream_t s)
 {
     if (plan->head_dim != D) return SPECTRA_OK;
     const PlanView pv = make_view(plan);
-    tc_images_kernel<<<plan->heads, 256, 0, s>>>(pv, const_cast<uint8_t*>(pv.enc_img), const_cast<uint8_t*>(pv.dec_img),
+    tc_images_kernel<<<dim3(plan->heads, D / kImgRows), 256, 0, s>>>(pv, const_cast<uint8_t*>(pv.enc_img), const_cast<uint8_t*>(pv.dec_img),
                                                   const_cast<int32_t*>(pv.wmax), const_cast<float*>(pv.dec_bias));
     return cuda_status(cudaGetLastError());
 }
@@ -984,7 +1034,7 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
     P.total = P.tiles_per_head * plan->heads;
     P.nterms = plan->basis == SPECTRA_BASIS_RWHT ? 1 : 3;
     const bool lm = plan->quant == SPECTRA_Q_LLOYD_GAUSS;
-    P.stages = 4;
+    P.stages = 8;
     while (P.stages > 2 && enc_smem_layout(P.nterms, P.stages, lm).total + 1024 > kSmemMax) --P.stages;
     P.codes = codes;
     P.sstride = sstride;
@@ -995,7 +1045,7 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
     auto kern = lm ? (rw ? encode_tc_kernel<true, true> : encode_tc_kernel<true, false>)
                    : (rw ? encode_tc_kernel<false, true> : encode_tc_kernel<false, false>);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-    const int grid = min(sm_count(), P.total);
+    const int grid = sched_grid(sm_count(), plan->heads, P.tiles_per_head);
     kern<<<grid, kEncThreads, sm, s>>>(m, P);
     *done = true;
     return cuda_status(cudaGetLastError());
@@ -1035,7 +1085,7 @@ spectra_status launch_decode_tc(const spectra_plan* plan, const uint8_t* codes, 
     const uint32_t sm = total();
     auto kern = lm ? decode_tc_kernel<true> : decode_tc_kernel<false>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-    const int grid = min(sm_count(), P.total);
+    const int grid = sched_grid(sm_count(), plan->heads, P.tiles_per_head);
     kern<<<grid, kDecThreads, sm, s>>>(m, P);
     *done = true;
     return cuda_status(cudaGetLastError());
