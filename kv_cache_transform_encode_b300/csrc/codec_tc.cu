@@ -58,7 +58,6 @@ constexpr int TILE = 128;                 // tokens per tile (MMA M)
 constexpr uint32_t OPND = TILE * D * 2;   // one bf16 operand tile: 32 KB
 constexpr uint32_t KBLK = TILE * 128;     // one 64-element K block: 16 KB
 constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
-constexpr int kEncThreads = 576;          // producer, MMA, 16 epilogue warps
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // ------------------------------------------------------------------ helpers
@@ -70,18 +69,35 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 // whole at about the same time, which keeps DRAM pages open -- and every
 // CTA loads its operand image once.  Contiguous (otherwise): one range of
 // the head-major item list per CTA.
+// Loops walk the items with first() / next(), which divide only once.
+struct Item {
+    int h, tile;
+};
+
 struct Sched {
     int interleaved, head, j, cph, begin, n, tiles;
     __device__ __forceinline__ int head_of(int k) const { return interleaved ? head : (begin + k) / tiles; }
-    __device__ __forceinline__ int tile_of(int k) const { return interleaved ? j + k * cph : (begin + k) % tiles; }
+    __device__ __forceinline__ Item first() const
+    {
+        return interleaved ? Item{head, j} : Item{begin / tiles, begin % tiles};
+    }
+    __device__ __forceinline__ void next(Item& it) const
+    {
+        if (interleaved) {
+            it.tile += cph;
+        } else if (++it.tile == tiles) {
+            it.tile = 0;
+            ++it.h;
+        }
+    }
 };
 
-__device__ __forceinline__ Sched make_sched(int heads, int tiles)
+__device__ __forceinline__ Sched make_sched(int heads, int tiles, bool contig = false)
 {
     Sched S;
     S.tiles = tiles;
     const int G = int(gridDim.x);
-    if (G >= heads && G % heads == 0) {
+    if (!contig && G >= heads && G % heads == 0) {
         S.interleaved = 1;
         S.cph = G / heads;
         S.head = int(blockIdx.x) % heads;
@@ -164,13 +180,20 @@ __device__ __forceinline__ uint32_t quant_lm(const float* th, int b, int bmax, f
 }
 
 // ------------------------------------------------------------------ encode
+constexpr int ETILE = 256;                        // tokens per encode tile (MMA N)
+constexpr uint32_t ESTAGE = ETILE * D * 2;        // x tile, two K blocks: 64 KB
+constexpr uint32_t EKBLK = ETILE * 128;           // one 64-element K block: 32 KB
+constexpr uint32_t IDESC_E = idesc_bf16_f32(128, ETILE);
+constexpr int kEncEpiWarps = 16;
+constexpr int kEncThreads = 64 + 32 * kEncEpiWarps;   // producer, MMA, epilogue
+constexpr uint32_t kImgCol = 256;                 // TMEM column of the basis image
+
 struct EncParams {
     PlanView pv;
     int64_t T;
     int tiles_per_head;
-    int total;             // heads * tiles_per_head
-    int nterms;            // 3 (EIGEN) or 1 (RWHT)
     int stages;
+    int contig;            // contiguous work ranges (else interleaved)
     uint8_t* codes;
     int64_t sstride;
     float* norms;
@@ -178,58 +201,64 @@ struct EncParams {
 };
 
 struct EncSmem {            // offsets into dynamic shared memory (1024-aligned base)
-    uint32_t img, xs, th, red, bars, total;
+    uint32_t xs, th, red, bars, total;
 };
 
-__host__ __device__ inline EncSmem enc_smem_layout(int nterms, int stages, bool lm)
+__host__ __device__ inline EncSmem enc_smem_layout(int stages, bool lm)
 {
     EncSmem L;
     uint32_t o = 0;
-    L.img = o;  o += 0;                          // the basis image lives in tensor memory
-    L.xs = o;   o += stages * OPND;
+    L.xs = o;   o += stages * ESTAGE;
     L.th = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
-    L.red = o;  o += (4 * 4 * 32 + 16 * 32) * 4;     // RWHT norm partials and inverses
+    L.red = o;  o += (4 * 4 * 32 + kEncEpiWarps * 32) * 4;   // RWHT norm partials and inverses
     L.bars = o; o += 256;
     L.total = o;
     return L;
 }
 
-constexpr int kEncEpiWarps = 16;
-
-// D[c][t] = sum_i img[c][i] x[t][i]: TMEM lane = channel, column = token.
-// Epilogue warp e (warps 2..17): lane quadrant q = warp & 3 (channels
-// 32q .. 32q+31), token group gi = (warp - 2) / 4 of each 128-token tile.
+// D[c][t] = sum_i img[c][i] x[t][i] for a 256-token tile: TMEM lane =
+// channel, column = token (columns 0..255, one accumulator); the basis
+// image (A operand, K-major: lane = channel, two bf16 per column) sits in
+// columns 256.. for the whole head.  Epilogue warp (warps 2..17): lane
+// quadrant q = warp & 3 (channels 32q .. 32q+31), slot gi = (warp - 2) / 4,
+// which takes the 32-token groups gi and gi + 4 of every tile.  The
+// accumulator is read into registers first and released at once, so the
+// MMAs of the next tile overlap the quantize / pack of this one.
 // LM: Lloyd-Max quantizer; RWHT: Hadamard basis (per-token scale).
+// 18 warps put five on two of the four SM sub-partitions, whose register
+// files (16 K each) then allow 96 registers a thread.
 template <bool LM, bool RWHT>
-__global__ void __launch_bounds__(64 + 32 * kEncEpiWarps, 1)
+__global__ void __launch_bounds__(kEncThreads, 1)
 encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr bool lm = LM;
     constexpr bool rwht = RWHT;
-    const EncSmem L = enc_smem_layout(P.nterms, P.stages, lm);
+    constexpr int NT = RWHT ? 1 : 3;       // bf16 terms of the basis image
+    const EncSmem L = enc_smem_layout(P.stages, lm);
     uint8_t* xs = smem + L.xs;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-    uint64_t* full = bars;                 // [stages <= 8]
-    uint64_t* empty = bars + 8;            // [stages]
-    uint64_t* accfull = bars + 16;         // [2]
-    uint64_t* accempty = bars + 18;        // [2]
-    uint64_t* imgfull = bars + 20;
-    uint64_t* imgempty = bars + 21;
-    uint64_t* drain = bars + 22;
-    uint64_t* rbar = bars + 23;            // [4] RWHT norm rendezvous, one per token group
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 28);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 29);
+    uint64_t* full = bars;                 // [stages <= 4]
+    uint64_t* empty = bars + 4;            // [stages]
+    uint64_t* accfull = bars + 8;
+    uint64_t* accempty = bars + 9;
+    uint64_t* imgfull = bars + 10;
+    uint64_t* imgempty = bars + 11;
+    uint64_t* drain = bars + 12;
+    uint64_t* rbar = bars + 13;            // [4] RWHT norm rendezvous, one per slot
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18);
     volatile int* drain_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Sched S = make_sched(P.pv.heads, P.tiles_per_head);
+    const Sched S = make_sched(P.pv.heads, P.tiles_per_head, P.contig != 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P.stages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], 1); mbar_init(&accempty[a], kEncEpiWarps); }
-        mbar_init(imgfull, 4);             // the four loader warps (token group 0)
+        mbar_init(accfull, 1);
+        mbar_init(accempty, kEncEpiWarps);
+        mbar_init(imgfull, kEncEpiWarps);
         mbar_init(imgempty, 1);
         mbar_init(drain, 1);
         for (int g = 0; g < 4; ++g) mbar_init(&rbar[g], 4);
@@ -238,7 +267,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, 512);      // accumulators: columns 0..255; basis image: 256..447
+        tmem_alloc(tmem_holder, 512);      // accumulator: columns 0..255; basis image: 256..447
         tmem_relinquish();
     }
     if (lm) {
@@ -253,54 +282,57 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            int k = 0;
-            int last_issued[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
-            for (; k < S.n; ++k) {
-                const int h = S.head_of(k), tile = S.tile_of(k);
-                const int s = k % P.stages;
-                if (k >= P.stages && !mbar_wait(&empty[s], ((k / P.stages) - 1) & 1, abort_flag, kWaitNs)) break;
-                mbar_arrive_expect_tx(&full[s], OPND);
-                uint8_t* dst = xs + s * OPND;
-                tma_load_3d(dst, &tmap_x, &full[s], 0, h, tile * TILE);
-                tma_load_3d(dst + KBLK, &tmap_x, &full[s], 64, h, tile * TILE);
-                last_issued[s] = k;
+            int s = 0, k = 0;
+            uint32_t ph = 0;
+            Item it = S.first();
+            for (; k < S.n; ++k, S.next(it)) {
+                if (k >= P.stages && !mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitNs)) break;
+                // the first head's basis image is fetched before the x stream
+                // takes the memory system
+                if (k == 1 && !mbar_wait(imgfull, 0, abort_flag, kWaitNs)) break;
+                mbar_arrive_expect_tx(&full[s], ESTAGE);
+                uint8_t* dst = xs + s * ESTAGE;
+                tma_load_3d(dst, &tmap_x, &full[s], 0, it.h, it.tile * ETILE);
+                tma_load_3d(dst + EKBLK, &tmap_x, &full[s], 64, it.h, it.tile * ETILE);
+                if (++s == P.stages) { s = 0; ph ^= 1u; }
             }
             if (*abort_flag) {   // let copies in flight land before the CTA exits
-                for (int s = 0; s < P.stages; ++s)
-                    if (last_issued[s] >= 0)
-                        mbar_wait(&full[s], (last_issued[s] / P.stages) & 1, drain_flag, 100000000ull);
+                for (int i = (k > P.stages ? k - P.stages : 0); i < k; ++i)
+                    mbar_wait(&full[i % P.stages], (i / P.stages) & 1, drain_flag, 100000000ull);
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA
         if (lane == 0) {
-            int k = 0, j = 0, cur_h = -1;
+            int j = 0, cur_h = -1, s = 0;
+            uint32_t ph = 0;
             bool issued = false;
-            for (; k < S.n; ++k) {
-                const int h = S.head_of(k);
+            const uint64_t dbase = sdesc_sw128(smem_u32(xs));
+            Item it = S.first();
+            for (int k = 0; k < S.n; ++k) {
+                const int h = it.h;
+                S.next(it);
                 if (h != cur_h) {
                     if (!mbar_wait(imgfull, j & 1, abort_flag, kWaitNs)) break;
                     cur_h = h;
                     ++j;
                 }
-                const int s = k % P.stages, a = k & 1;
-                if (!mbar_wait(&full[s], (k / P.stages) & 1, abort_flag, kWaitNs)) break;
-                if (k >= 2 && !mbar_wait(&accempty[a], ((k >> 1) - 1) & 1, abort_flag, kWaitNs)) break;
+                if (!mbar_wait(&full[s], ph, abort_flag, kWaitNs)) break;
+                if (k > 0 && !mbar_wait(accempty, (k - 1) & 1, abort_flag, kWaitNs)) break;
                 tc_fence_after();
-                const uint32_t xa = smem_u32(xs + s * OPND);
-                const uint32_t d_tmem = tmem + a * 128;
-                for (int t = 0; t < P.nterms; ++t)
+                // descriptor start addresses advance in 16-byte units
+                const uint64_t db = dbase + uint64_t(s) * (ESTAGE >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * KBLK + (kk & 3) * 32;
-                        mma_bf16_ts(d_tmem, tmem + 256 + t * 64 + kk * 8, sdesc_sw128(xa + koff), IDESC,
-                                    (t | kk) ? 1u : 0u);
-                    }
+                for (int t = 0; t < NT; ++t)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ts(tmem, tmem + kImgCol + t * 64 + kk * 8,
+                                    db + ((kk >> 2) * (EKBLK >> 4) + (kk & 3) * 2), IDESC_E, (t | kk) ? 1u : 0u);
                 issued = true;
                 mma_commit(&empty[s]);
-                mma_commit(&accfull[a]);
-                const bool head_ends = (k + 1 == S.n) || (S.head_of(k + 1) != h);
-                if (head_ends) mma_commit(imgempty);
+                mma_commit(accfull);
+                if ((k + 1 == S.n) || (it.h != h)) mma_commit(imgempty);
+                if (++s == P.stages) { s = 0; ph ^= 1u; }
             }
             if (issued) {   // every MMA of this CTA done before TMEM is released
                 mma_commit(drain);
@@ -310,99 +342,56 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;                        // TMEM lane quadrant: channels 32q..
-        const int gi = (warp - 2) >> 2;                // token group inside each tile
+        const int gi = (warp - 2) >> 2;                // slot: token groups gi and gi + 4
         const int c = q * 32 + lane;                   // this thread's channel
+        const uint32_t tq = tmem + (uint32_t(q * 32) << 16);
         const float* th = reinterpret_cast<const float*>(smem + L.th);
         float* part = reinterpret_cast<float*>(smem + L.red) + gi * (4 * 32);          // [4 q][32 t]
         float* invs = reinterpret_cast<float*>(smem + L.red) + 4 * 4 * 32 + (warp - 2) * 32;
-        int k = 0, cur_h = -1, R = 0, b = 0, o = 0, bmax = 0, ruse = 0, nimg = 0;
+        int cur_h = -1, R = 0, b = 0, o = 0, bmax = 0, ruse = 0, nimg = 0;
         float qk = 0.f, cl = 0.f;
         bool head_ok = true;
-        for (; k < S.n; ++k) {
-            const int h = S.head_of(k), tile = S.tile_of(k);
-            if (h != cur_h) {
-                if (gi == 0) {
-                    // the head's basis image -> TMEM columns 256.. (lane = channel):
-                    // after the MMAs of the previous head are done
-                    if (nimg > 0 && !mbar_wait(imgempty, (nimg - 1) & 1, abort_flag, kWaitNs)) break;
-                    tc_fence_after();
-                    const uint4* src = reinterpret_cast<const uint4*>(P.pv.enc_img + size_t(h) * enc_img_bytes(D) +
-                                                                      size_t(c) * 256);
-                    for (int t = 0; t < P.nterms; ++t)
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t r[32];
+        uint32_t* out = nullptr;
+
+        // RWHT: per-token norms of one 32-token group (r: this channel's 32
+        // values); ||x_t||^2 = (1/d) sum_c D[c][t]^2, reduced over the 32
+        // columns across this warp's lanes (lane t ends with token t), then
+        // over the four lane quadrants through shared memory.  Leaves the
+        // inverse norms in invs[]; false when a rendezvous gave up.
+        auto rwht_norm = [&](const uint32_t (&r)[32], int64_t tile, int g) -> bool {
+            const int64_t t0 = tile * ETILE + g * 32;
+            float v[32];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const uint4 v = src[t * (OPND / 16) + half * 8 + e];
-                                r[4 * e] = v.x; r[4 * e + 1] = v.y; r[4 * e + 2] = v.z; r[4 * e + 3] = v.w;
-                            }
-                            tmem_st32(tmem + (uint32_t(q * 32) << 16) + 256 + t * 64 + half * 32, r);
-                        }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(imgfull);
-                    ++nimg;
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * __uint_as_float(r[i]);
+#pragma unroll
+            for (int sh = 16; sh >= 1; sh >>= 1) {
+                const bool up = lane & sh;
+#pragma unroll
+                for (int i = 0; i < sh; ++i) {
+                    const float send = up ? v[i] : v[i + sh];
+                    const float keep = up ? v[i + sh] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
                 }
-                cur_h = h;
-                R = P.pv.rec_bits[h];
-                head_ok = R <= P.pv.max_rec_bits;
-                if (!head_ok && lane == 0) P.pv.status[h] = -SPECTRA_ERR_BUFFER;
-                b = P.pv.bits[size_t(h) * D + c];
-                o = P.pv.chan_off[size_t(h) * D + c];
-                const float qs = P.pv.qscale[size_t(h) * D + c];
-                // UNIFORM3S: qscale = 2^b / (6 sigma) -> qk = 1 / (6 sigma); LLOYD: 1 / sigma
-                qk = lm ? qs : qs / float(1 << b);
-                cl = float(1 << b) * (1.0f - 0x1p-22f);
-                bmax = __reduce_max_sync(0xffffffffu, b);
             }
-            const int a = k & 1;
-            if (!mbar_wait(&accfull[a], (k >> 1) & 1, abort_flag, kWaitNs)) break;
-            tc_fence_after();
-            uint32_t* out = reinterpret_cast<uint32_t*>(P.codes + int64_t(h) * P.sstride);
-            bool ok = true;
-            const int64_t t0 = int64_t(tile) * TILE + gi * 32;
-            const bool glive = t0 < P.T;
-            uint32_t r[32];
-            tmem_ld32(tmem + a * 128 + (uint32_t(q * 32) << 16) + gi * 32, r);
-            tmem_ld_wait();
-            tc_fence_before();
+            part[q * 32 + lane] = v[0];
             __syncwarp();
-            if (lane == 0) mbar_arrive(&accempty[a]);      // accumulator columns read: MMA may reuse them
-            if (rwht) {
-                // ||x_t||^2 = (1/d) sum_c D[c][t]^2: reduce the 32 columns
-                // over this warp's lanes (lane t ends with token t), then over
-                // the four lane quadrants through shared memory.
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * __uint_as_float(r[i]);
-#pragma unroll
-                for (int s = 16; s >= 1; s >>= 1) {
-                    const bool up = lane & s;
-#pragma unroll
-                    for (int i = 0; i < s; ++i) {
-                        const float send = up ? v[i] : v[i + s];
-                        const float keep = up ? v[i + s] : v[i];
-                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-                    }
-                }
-                part[q * 32 + lane] = v[0];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&rbar[gi]);
-                if (!(ok = mbar_wait(&rbar[gi], ruse & 1, abort_flag, kWaitNs))) break;
-                ++ruse;
-                const float n2 = part[lane] + part[32 + lane] + part[64 + lane] + part[96 + lane];
-                const float nrm = sqrtf(n2 * (1.0f / float(D)));
-                if (q == 0 && head_ok && t0 + lane < P.T) P.norms[int64_t(h) * P.nstride + t0 + lane] = nrm;
-                invs[lane] = (nrm > 0.f) ? 1.f / nrm : 0.f;
-                __syncwarp();
-                // everyone has read part[] before it is written again
-                if (lane == 0) mbar_arrive(&rbar[gi]);
-                if (!(ok = mbar_wait(&rbar[gi], ruse & 1, abort_flag, kWaitNs))) break;
-                ++ruse;
-            }
-            if (!glive || !head_ok || R == 0) continue;
-            // codes of 32 tokens (low byte of each word)
+            if (lane == 0) mbar_arrive(&rbar[gi]);
+            if (!mbar_wait(&rbar[gi], ruse & 1, abort_flag, kWaitNs)) return false;
+            ++ruse;
+            const float n2 = part[lane] + part[32 + lane] + part[64 + lane] + part[96 + lane];
+            const float nrm = sqrtf(n2 * (1.0f / float(D)));
+            if (q == 0 && head_ok && t0 + lane < P.T) P.norms[int64_t(cur_h) * P.nstride + t0 + lane] = nrm;
+            invs[lane] = (nrm > 0.f) ? 1.f / nrm : 0.f;
+            __syncwarp();
+            // everyone has read part[] before it is written again
+            if (lane == 0) mbar_arrive(&rbar[gi]);
+            if (!mbar_wait(&rbar[gi], ruse & 1, abort_flag, kWaitNs)) return false;
+            ++ruse;
+            return true;
+        };
+        // codes of 32 tokens of this channel -> byte i of the 64-bit block
+        // (Y[2m], Y[2m+1]) holds bit i of tokens 8m .. 8m+7
+        auto quant8 = [&](uint32_t (&r)[32], uint32_t (&Y)[8]) {
             if (!lm) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = quant_uniform(__uint_as_float(r[i]), qk, cl);
@@ -414,16 +403,20 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                     r[i] = quant_lm(tb, b, bmax, u);
                 }
             }
-            uint32_t Y[8];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 Y[2 * m] = low_bytes(r[8 * m], r[8 * m + 1], r[8 * m + 2], r[8 * m + 3]);
                 Y[2 * m + 1] = low_bytes(r[8 * m + 4], r[8 * m + 5], r[8 * m + 6], r[8 * m + 7]);
                 transpose8(Y[2 * m], Y[2 * m + 1]);
             }
+        };
+        // the channel's bit-plane words of one group into the stream
+        auto store8 = [&](const uint32_t (&Y)[8], int64_t tile, int g) {
+            const int64_t t0 = tile * ETILE + g * 32;
+            if (t0 >= P.T) return;
             const int64_t nt = P.T - t0;
             const uint32_t live = nt >= 32 ? 0xffffffffu : ((1u << nt) - 1u);
-            uint32_t* dst = out + (int64_t(tile) * 4 + gi) * R + o;
+            uint32_t* dst = out + (tile * 8 + g) * R + o;
 #pragma unroll
             for (int kb = 0; kb < 8; ++kb) {
                 if (kb < bmax) {
@@ -431,6 +424,69 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                     const uint32_t pw = gather_byte(Y[hs], Y[2 + hs], Y[4 + hs], Y[6 + hs], kb & 3) & live;
                     if (kb < b) dst[kb] = pw;
                 }
+            }
+        };
+
+        Item it = S.first();
+        for (int k = 0; k < S.n; ++k, S.next(it)) {
+            const int h = it.h, tile = it.tile;
+            if (h != cur_h) {
+                // the head's basis image -> TMEM columns 256.. (lane = channel),
+                // after the MMAs of the previous head are done; each warp
+                // loads NT * 16 of the NT * 64 columns of its quadrant
+                if (nimg > 0 && !mbar_wait(imgempty, (nimg - 1) & 1, abort_flag, kWaitNs)) break;
+                tc_fence_after();
+                const uint8_t* src = P.pv.enc_img + size_t(h) * enc_img_bytes(D) + size_t(c) * 256;
+                const int col0 = gi * NT * 16;
+                uint32_t r[NT * 16];
+#pragma unroll
+                for (int u = 0; u < NT * 4; ++u) {
+                    const int jc = col0 + u * 4;            // image column (two bf16 each)
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (jc >> 6) * OPND + (jc & 63) * 4));
+                    r[4 * u] = v.x; r[4 * u + 1] = v.y; r[4 * u + 2] = v.z; r[4 * u + 3] = v.w;
+                }
+#pragma unroll
+                for (int u = 0; u < NT; ++u)
+                    tmem_st16(tq + kImgCol + col0 + u * 16, *reinterpret_cast<const uint32_t(*)[16]>(r + 16 * u));
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(imgfull);
+                ++nimg;
+                cur_h = h;
+                R = P.pv.rec_bits[h];
+                head_ok = R <= P.pv.max_rec_bits;
+                if (!head_ok && lane == 0) P.pv.status[h] = -SPECTRA_ERR_BUFFER;
+                b = P.pv.bits[size_t(h) * D + c];
+                o = P.pv.chan_off[size_t(h) * D + c];
+                const float qs = P.pv.qscale[size_t(h) * D + c];
+                // UNIFORM3S: qscale = 2^b / (6 sigma) -> qk = 1 / (6 sigma); LLOYD: 1 / sigma
+                qk = lm ? qs : qs / float(1 << b);
+                cl = float(1 << b) * (1.0f - 0x1p-22f);
+                bmax = __reduce_max_sync(0xffffffffu, b);
+                out = reinterpret_cast<uint32_t*>(P.codes + int64_t(h) * P.sstride);
+            }
+            if (!mbar_wait(accfull, k & 1, abort_flag, kWaitNs)) break;
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tq + gi * 32, r0);
+            tmem_ld32(tq + (gi + 4) * 32, r1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accempty);      // accumulator read: the next tile's MMAs may start
+            if (rwht) {
+                uint32_t Y[8];
+                if (!rwht_norm(r0, tile, gi)) break;
+                if (head_ok && R > 0) { quant8(r0, Y); store8(Y, tile, gi); }
+                if (!rwht_norm(r1, tile, gi + 4)) break;
+                if (head_ok && R > 0) { quant8(r1, Y); store8(Y, tile, gi + 4); }
+            } else if (head_ok && R > 0) {
+                uint32_t Y0[8], Y1[8];
+                quant8(r0, Y0);
+                quant8(r1, Y1);
+                store8(Y0, tile, gi);
+                store8(Y1, tile, gi + 4);
             }
         }
     }
@@ -588,9 +644,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         if (lane == 0) {
             int k = 0, j = 0, cur_h = -1, R = 0;
             int last_issued[4] = {-1, -1, -1, -1};
-            int img_issued = 0;
-            for (; k < S.n; ++k) {
-                const int h = S.head_of(k), tile = S.tile_of(k);
+            int img_issued = 0, cs_i = 0;
+            uint32_t cs_ph = 0;
+            Item it = S.first();
+            for (; k < S.n; ++k, S.next(it)) {
+                const int h = it.h, tile = it.tile;
                 if (h != cur_h) {
                     if (j > 0 && !mbar_wait(imgempty, (j - 1) & 1, abort_flag, kWaitNs)) break;
                     const uint32_t bytes = P.nterms * OPND;
@@ -606,8 +664,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                     }
                     ++j;
                 }
-                const int s = k % P.cstages;
-                if (k >= P.cstages && !mbar_wait(&cempty[s], ((k / P.cstages) - 1) & 1, abort_flag, kWaitNs)) break;
+                const int s = cs_i;
+                if (k >= P.cstages && !mbar_wait(&cempty[s], cs_ph ^ 1u, abort_flag, kWaitNs)) break;
+                if (++cs_i == P.cstages) { cs_i = 0; cs_ph ^= 1u; }
                 const int64_t t0 = int64_t(tile) * TILE;
                 const int64_t ngroups = min(int64_t(4), (P.T - t0 + 31) / 32);
                 const uint32_t bytes = uint32_t((ngroups * 4 * R + 15) / 16 * 16);
@@ -637,15 +696,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             const int npr = !lm ? P.nterms : (!rwht ? 3 : 2);
             const uint32_t pa = !lm ? 0u : (!rwht ? 0x010u : 0x10u);    // nibble pr: A term
             const uint32_t pb = !lm ? 0x10u : (!rwht ? 0x100u : 0x00u); // nibble pr: image term
+            int as_i = 0;
+            uint32_t as_ph = 0;
+            Item it = S.first();
             for (; k < S.n; ++k) {
-                const int h = S.head_of(k);
+                const int h = it.h;
+                S.next(it);
                 if (h != cur_h) {
                     if (!mbar_wait(imgfull, j & 1, abort_flag, kWaitNs)) break;
                     cur_h = h;
                     ++j;
                 }
-                const int s = k % P.astages, a = k & 1;
-                if (!mbar_wait(&afull[s], (k / P.astages) & 1, abort_flag, kWaitNs)) break;
+                const int s = as_i, a = k & 1;
+                if (!mbar_wait(&afull[s], as_ph, abort_flag, kWaitNs)) break;
+                if (++as_i == P.astages) { as_i = 0; as_ph ^= 1u; }
                 if (k >= 2 && !mbar_wait(&accempty[a], ((k >> 1) - 1) & 1, abort_flag, kWaitNs)) break;
                 tc_fence_after();
                 const uint32_t aa = smem_u32(as + s * P.na * OPND);
@@ -663,7 +727,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 issued = true;
                 mma_commit(&aempty[s]);
                 mma_commit(&accfull[a]);
-                const bool head_ends = (k + 1 == S.n) || (S.head_of(k + 1) != h);
+                const bool head_ends = (k + 1 == S.n) || (it.h != h);
                 if (head_ends) mma_commit(imgempty);
             }
             if (issued) {
@@ -680,8 +744,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         int k = 0, cur_h = -1, R = 0, b0 = 0, b1 = 0, o0 = 0, o1 = 0, bmax = 0;
         float off0 = 0.f, off1 = 0.f;
         bool code_mode = false;
-        for (; k < S.n; ++k) {
-            const int h = S.head_of(k), tile = S.tile_of(k);
+        int u_ci = 0, u_ai = 0;
+        uint32_t u_cph = 0, u_aph = 0;
+        Item it = S.first();
+        for (; k < S.n; ++k, S.next(it)) {
+            const int h = it.h, tile = it.tile;
             if (h != cur_h) {
                 cur_h = h;
                 R = P.pv.rec_bits[h];
@@ -695,9 +762,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 bmax = __reduce_max_sync(0xffffffffu, max(b0, b1));
                 code_mode = !lm && !rwht && P.pv.wmax[h] <= 7;
             }
-            const int sc = k % P.cstages, sa = k % P.astages;
-            if (!mbar_wait(&cfull[sc], (k / P.cstages) & 1, abort_flag, kWaitNs)) break;
-            if (k >= P.astages && !mbar_wait(&aempty[sa], ((k / P.astages) - 1) & 1, abort_flag, kWaitNs)) break;
+            const int sc = u_ci, sa = u_ai;
+            if (!mbar_wait(&cfull[sc], u_cph, abort_flag, kWaitNs)) break;
+            if (k >= P.astages && !mbar_wait(&aempty[sa], u_aph ^ 1u, abort_flag, kWaitNs)) break;
+            if (++u_ci == P.cstages) { u_ci = 0; u_cph ^= 1u; }
+            if (++u_ai == P.astages) { u_ai = 0; u_aph ^= 1u; }
             const int64_t t0 = int64_t(tile) * TILE + gi * 32;
             if (t0 < P.T && R > 0) {
                 const uint32_t* words = reinterpret_cast<const uint32_t*>(cs + sc * P.cbytes) + gi * R;
@@ -768,8 +837,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             ++euse;
             return r;
         };
-        for (; k < S.n && ok; ++k) {
-            const int h = S.head_of(k), tile = S.tile_of(k);
+        Item it = S.first();
+        for (; k < S.n && ok; ++k, S.next(it)) {
+            const int h = it.h, tile = it.tile;
             if (h != cur_h) {       // code mode: per-output offsets of this head
                 cur_h = h;
                 code_mode = !lm && !rwht && P.pv.wmax[h] <= 7;
@@ -987,15 +1057,16 @@ int sm_count()
     return n;
 }
 
-// [T][heads][128] cache of 2- or 4-byte elements, box [128 tokens][1][64 or 32]
-bool make_cache_map(CUtensorMap* m, const void* base, bool f32, int heads, int64_t T, int64_t tstride)
+// [T][heads][128] cache of 2- or 4-byte elements, box [rows tokens][1][64 or 32]
+bool make_cache_map(CUtensorMap* m, const void* base, bool f32, int heads, int64_t T, int64_t tstride,
+                    int rows = TILE)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     const int es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(heads), cuuint64_t(T)};
     cuuint64_t strides[2] = {cuuint64_t(D) * es, cuuint64_t(tstride) * es};
-    cuuint32_t box[3] = {cuuint32_t(128 / es), 1u, cuuint32_t(TILE)};
+    cuuint32_t box[3] = {cuuint32_t(128 / es), 1u, cuuint32_t(rows)};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1023,29 +1094,41 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
 {
     *done = false;
     if (dt != SPECTRA_BF16 || plan->head_dim != D || T <= 0) return SPECTRA_OK;
-    if (T > (int64_t(1) << 31) - TILE) return SPECTRA_OK;
+    if (T > (int64_t(1) << 31) - ETILE) return SPECTRA_OK;
     CUtensorMap m;
-    if (!make_cache_map(&m, x, false, plan->heads, T, token_stride)) return SPECTRA_OK;
+    if (!make_cache_map(&m, x, false, plan->heads, T, token_stride, ETILE)) return SPECTRA_OK;
     EncParams P;
     P.pv = make_view(plan);
     P.T = T;
-    P.tiles_per_head = int((T + TILE - 1) / TILE);
-    if (int64_t(P.tiles_per_head) * plan->heads > (int64_t(1) << 31) - 1) return SPECTRA_OK;
-    P.total = P.tiles_per_head * plan->heads;
-    P.nterms = plan->basis == SPECTRA_BASIS_RWHT ? 1 : 3;
+    P.tiles_per_head = int((T + ETILE - 1) / ETILE);
+    const int64_t total = int64_t(P.tiles_per_head) * plan->heads;
+    if (total > (int64_t(1) << 31) - 1) return SPECTRA_OK;
     const bool lm = plan->quant == SPECTRA_Q_LLOYD_GAUSS;
-    P.stages = 8;
-    while (P.stages > 2 && enc_smem_layout(P.nterms, P.stages, lm).total + 1024 > kSmemMax) --P.stages;
+    P.stages = 4;
+    while (P.stages > 2 && enc_smem_layout(P.stages, lm).total + 1024 > kSmemMax) --P.stages;
     P.codes = codes;
     P.sstride = sstride;
     P.norms = norms;
     P.nstride = nstride;
-    const uint32_t sm = enc_smem_layout(P.nterms, P.stages, lm).total + 1024;
+    // interleaved schedule unless contiguous ranges give every CTA fewer tiles
+    const int sms = sm_count();
+    int grid = sched_grid(sms, plan->heads, P.tiles_per_head);
+    P.contig = 0;
+    if (plan->heads <= sms) {
+        const int cph = grid / plan->heads;
+        const int64_t inter_max = (P.tiles_per_head + cph - 1) / cph;
+        const int64_t g2 = std::min<int64_t>(sms, total);
+        const int64_t contig_max = (total + g2 - 1) / g2;
+        if (contig_max < inter_max) {
+            P.contig = 1;
+            grid = int(g2);
+        }
+    }
+    const uint32_t sm = enc_smem_layout(P.stages, lm).total + 1024;
     const bool rw = plan->basis == SPECTRA_BASIS_RWHT;
     auto kern = lm ? (rw ? encode_tc_kernel<true, true> : encode_tc_kernel<true, false>)
                    : (rw ? encode_tc_kernel<false, true> : encode_tc_kernel<false, false>);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-    const int grid = sched_grid(sm_count(), plan->heads, P.tiles_per_head);
     kern<<<grid, kEncThreads, sm, s>>>(m, P);
     *done = true;
     return cuda_status(cudaGetLastError());
