@@ -201,14 +201,19 @@ struct EncParams {
 };
 
 struct EncSmem {            // offsets into dynamic shared memory (1024-aligned base)
-    uint32_t xs, th, red, bars, total;
+    uint32_t xs, img, cb, cbytes, th, red, bars, total;
 };
 
-__host__ __device__ inline EncSmem enc_smem_layout(int stages, bool lm)
+// cbytes: one tile's packed codes (8 groups of R words), double-buffered
+__host__ __device__ inline EncSmem enc_smem_layout(int stages, int max_rec_bits, bool lm)
 {
     EncSmem L;
     uint32_t o = 0;
     L.xs = o;   o += stages * ESTAGE;
+    // the basis image passes through the x stages (all of them idle then)
+    L.img = stages >= 3 ? ESTAGE : 0;
+    L.cbytes = uint32_t((32 * (max_rec_bits > 0 ? max_rec_bits : 1) + 15) / 16 * 16);
+    L.cb = o;   o += 2 * L.cbytes;
     L.th = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
     L.red = o;  o += (4 * 4 * 32 + kEncEpiWarps * 32) * 4;   // RWHT norm partials and inverses
     L.bars = o; o += 256;
@@ -219,11 +224,16 @@ __host__ __device__ inline EncSmem enc_smem_layout(int stages, bool lm)
 // D[c][t] = sum_i img[c][i] x[t][i] for a 256-token tile: TMEM lane =
 // channel, column = token (columns 0..255, one accumulator); the basis
 // image (A operand, K-major: lane = channel, two bf16 per column) sits in
-// columns 256.. for the whole head.  Epilogue warp (warps 2..17): lane
-// quadrant q = warp & 3 (channels 32q .. 32q+31), slot gi = (warp - 2) / 4,
-// which takes the 32-token groups gi and gi + 4 of every tile.  The
-// accumulator is read into registers first and released at once, so the
-// MMAs of the next tile overlap the quantize / pack of this one.
+// columns 256.. for the whole head.  It reaches TMEM by a bulk copy into
+// the idle x stages and tcgen05.cp, issued by the producer and the MMA
+// thread.  Epilogue warp (warps 2..17): lane quadrant q = warp & 3
+// (channels 32q .. 32q+31), slot gi = (warp - 2) / 4, which takes the
+// 32-token groups gi and gi + 4 of every tile.  The accumulator is read
+// into registers and released at once, so the MMAs of the next tile overlap
+// the quantize / pack of this one.  The packed words of a tile are gathered
+// in shared memory (the stream layout of 8 groups) and leave in one bulk
+// store.  One epilogue thread watches the accumulator barrier and a named
+// barrier wakes the rest.
 // LM: Lloyd-Max quantizer; RWHT: Hadamard basis (per-token scale).
 // 18 warps put five on two of the four SM sub-partitions, whose register
 // files (16 K each) then allow 96 registers a thread.
@@ -236,15 +246,15 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     constexpr bool lm = LM;
     constexpr bool rwht = RWHT;
     constexpr int NT = RWHT ? 1 : 3;       // bf16 terms of the basis image
-    const EncSmem L = enc_smem_layout(P.stages, lm);
+    const EncSmem L = enc_smem_layout(P.stages, P.pv.max_rec_bits, lm);
     uint8_t* xs = smem + L.xs;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* full = bars;                 // [stages <= 4]
     uint64_t* empty = bars + 4;            // [stages]
     uint64_t* accfull = bars + 8;
     uint64_t* accempty = bars + 9;
-    uint64_t* imgfull = bars + 10;
-    uint64_t* imgempty = bars + 11;
+    uint64_t* imgsmem = bars + 10;         // basis image landed in shared memory
+    uint64_t* imgcopied = bars + 11;       // ... and copied on to TMEM
     uint64_t* drain = bars + 12;
     uint64_t* rbar = bars + 13;            // [4] RWHT norm rendezvous, one per slot
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
@@ -258,8 +268,8 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         for (int s = 0; s < P.stages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         mbar_init(accfull, 1);
         mbar_init(accempty, kEncEpiWarps);
-        mbar_init(imgfull, kEncEpiWarps);
-        mbar_init(imgempty, 1);
+        mbar_init(imgsmem, 1);
+        mbar_init(imgcopied, 1);
         mbar_init(drain, 1);
         for (int g = 0; g < 4; ++g) mbar_init(&rbar[g], 4);
         *abort_flag = 0;
@@ -282,23 +292,48 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            int s = 0, k = 0;
-            uint32_t ph = 0;
+            int s = 0, k = 0, j = 0, cur_h = -1, last_s = -1, iss = 0;
+            uint32_t ph = 0, last_ph = 0;
+            bool img_pending = false;
             Item it = S.first();
-            for (; k < S.n; ++k, S.next(it)) {
-                if (k >= P.stages && !mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitNs)) break;
-                // the first head's basis image is fetched before the x stream
-                // takes the memory system
-                if (k == 1 && !mbar_wait(imgfull, 0, abort_flag, kWaitNs)) break;
+            auto issue = [&](const Item& t) {
                 mbar_arrive_expect_tx(&full[s], ESTAGE);
                 uint8_t* dst = xs + s * ESTAGE;
-                tma_load_3d(dst, &tmap_x, &full[s], 0, it.h, it.tile * ETILE);
-                tma_load_3d(dst + EKBLK, &tmap_x, &full[s], 64, it.h, it.tile * ETILE);
+                tma_load_3d(dst, &tmap_x, &full[s], 0, t.h, t.tile * ETILE);
+                tma_load_3d(dst + EKBLK, &tmap_x, &full[s], 64, t.h, t.tile * ETILE);
+                last_s = s;
+                last_ph = ph;
+                ++iss;
                 if (++s == P.stages) { s = 0; ph ^= 1u; }
+            };
+            for (; k < S.n; ++k, S.next(it)) {
+                bool pre = false;
+                if (it.h != cur_h) {
+                    // every tile issued so far consumed: the stages are free
+                    if (last_s >= 0 && !mbar_spin(&empty[last_s], last_ph, abort_flag, kWaitNs)) break;
+                    mbar_arrive_expect_tx(imgsmem, NT * OPND);
+                    const uint8_t* src = P.pv.enc_img + size_t(it.h) * enc_img_bytes(D);
+                    for (int t = 0; t < NT; ++t) bulk_load(smem + L.img + t * OPND, src + t * OPND, OPND, imgsmem);
+                    img_pending = true;
+                    // with three stages the image passes through stages 1-2,
+                    // so the first tile streams meanwhile
+                    if (k == 0 && L.img >= ESTAGE) {
+                        issue(it);
+                        pre = true;
+                    }
+                    if (!mbar_spin(imgcopied, j & 1, abort_flag, kWaitNs)) break;
+                    img_pending = false;
+                    ++j;
+                    cur_h = it.h;
+                    if (pre) continue;
+                }
+                if (iss >= P.stages && !mbar_spin(&empty[s], ph ^ 1u, abort_flag, kWaitNs)) break;
+                issue(it);
             }
             if (*abort_flag) {   // let copies in flight land before the CTA exits
-                for (int i = (k > P.stages ? k - P.stages : 0); i < k; ++i)
+                for (int i = (iss > P.stages ? iss - P.stages : 0); i < iss; ++i)
                     mbar_wait(&full[i % P.stages], (i / P.stages) & 1, drain_flag, 100000000ull);
+                if (img_pending) mbar_wait(imgsmem, j & 1, drain_flag, 100000000ull);
             }
         }
     } else if (warp == 1) {
@@ -308,17 +343,29 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
             uint32_t ph = 0;
             bool issued = false;
             const uint64_t dbase = sdesc_sw128(smem_u32(xs));
+            const uint64_t ibase = sdesc_sw128(smem_u32(smem + L.img));
             Item it = S.first();
             for (int k = 0; k < S.n; ++k) {
                 const int h = it.h;
                 S.next(it);
                 if (h != cur_h) {
-                    if (!mbar_wait(imgfull, j & 1, abort_flag, kWaitNs)) break;
+                    // image: shared memory -> TMEM columns 256.. (lane = channel);
+                    // the MMAs below read it after the copies (same issuing thread)
+                    if (!mbar_spin(imgsmem, j & 1, abort_flag, kWaitNs)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int t = 0; t < NT; ++t)
+#pragma unroll
+                        for (int kc = 0; kc < 8; ++kc)
+                            tmem_cp_128x256b(tmem + kImgCol + t * 64 + kc * 8,
+                                             ibase + ((t * OPND + (kc >> 2) * KBLK + (kc & 3) * 32) >> 4));
+                    mma_commit(imgcopied);
+                    issued = true;
                     cur_h = h;
                     ++j;
                 }
-                if (!mbar_wait(&full[s], ph, abort_flag, kWaitNs)) break;
-                if (k > 0 && !mbar_wait(accempty, (k - 1) & 1, abort_flag, kWaitNs)) break;
+                if (!mbar_spin(&full[s], ph, abort_flag, kWaitNs)) break;
+                if (k > 0 && !mbar_spin(accempty, (k - 1) & 1, abort_flag, kWaitNs)) break;
                 tc_fence_after();
                 // descriptor start addresses advance in 16-byte units
                 const uint64_t db = dbase + uint64_t(s) * (ESTAGE >> 4);
@@ -328,13 +375,11 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                     for (int kk = 0; kk < 8; ++kk)
                         mma_bf16_ts(tmem, tmem + kImgCol + t * 64 + kk * 8,
                                     db + ((kk >> 2) * (EKBLK >> 4) + (kk & 3) * 2), IDESC_E, (t | kk) ? 1u : 0u);
-                issued = true;
                 mma_commit(&empty[s]);
                 mma_commit(accfull);
-                if ((k + 1 == S.n) || (it.h != h)) mma_commit(imgempty);
                 if (++s == P.stages) { s = 0; ph ^= 1u; }
             }
-            if (issued) {   // every MMA of this CTA done before TMEM is released
+            if (issued) {   // every tcgen05 operation of this CTA done before TMEM is released
                 mma_commit(drain);
                 mbar_wait(drain, 0, drain_flag, 100000000ull);
             }
@@ -344,14 +389,33 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         const int q = warp & 3;                        // TMEM lane quadrant: channels 32q..
         const int gi = (warp - 2) >> 2;                // slot: token groups gi and gi + 4
         const int c = q * 32 + lane;                   // this thread's channel
+        const bool leader = warp == 2 && lane == 0;    // watches the accumulator, issues the stores
         const uint32_t tq = tmem + (uint32_t(q * 32) << 16);
         const float* th = reinterpret_cast<const float*>(smem + L.th);
         float* part = reinterpret_cast<float*>(smem + L.red) + gi * (4 * 32);          // [4 q][32 t]
         float* invs = reinterpret_cast<float*>(smem + L.red) + 4 * 4 * 32 + (warp - 2) * 32;
-        int cur_h = -1, R = 0, b = 0, o = 0, bmax = 0, ruse = 0, nimg = 0;
+        int cur_h = -1, R = 0, b = 0, o = 0, bmax = 0, ruse = 0;
         float qk = 0.f, cl = 0.f;
         bool head_ok = true;
         uint32_t* out = nullptr;
+        // the tile whose codes wait in shared memory for the bulk store
+        uint32_t* p_out = nullptr;
+        int p_R = 0, p_tile = 0;
+        bool p_live = false;
+
+        // leader: tile p_tile's packed words (buffer pb) -> the stream
+        auto flush = [&](int pb) {
+            if (!p_live) return;
+            uint32_t* cb = reinterpret_cast<uint32_t*>(smem + L.cb + pb * L.cbytes);
+            const int64_t t0 = int64_t(p_tile) * ETILE;
+            const int ng = int(min(int64_t(8), (P.T - t0 + 31) / 32));
+            const uint32_t words = uint32_t(ng * p_R);
+            const uint32_t bytes = (words * 4 + 15) / 16 * 16;
+            for (uint32_t w = words; w < bytes / 4; ++w) cb[w] = 0u;   // stream padding
+            fence_proxy_async_smem();
+            bulk_store(p_out + int64_t(p_tile) * 8 * p_R, cb, bytes);
+            tma_store_commit();
+        };
 
         // RWHT: per-token norms of one 32-token group (r: this channel's 32
         // values); ||x_t||^2 = (1/d) sum_c D[c][t]^2, reduced over the 32
@@ -410,13 +474,13 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                 transpose8(Y[2 * m], Y[2 * m + 1]);
             }
         };
-        // the channel's bit-plane words of one group into the stream
-        auto store8 = [&](const uint32_t (&Y)[8], int64_t tile, int g) {
+        // the channel's bit-plane words of group g into the tile buffer
+        auto store8 = [&](const uint32_t (&Y)[8], uint32_t* cb, int64_t tile, int g) {
             const int64_t t0 = tile * ETILE + g * 32;
             if (t0 >= P.T) return;
             const int64_t nt = P.T - t0;
             const uint32_t live = nt >= 32 ? 0xffffffffu : ((1u << nt) - 1u);
-            uint32_t* dst = out + (tile * 8 + g) * R + o;
+            uint32_t* dst = cb + g * R + o;
 #pragma unroll
             for (int kb = 0; kb < 8; ++kb) {
                 if (kb < bmax) {
@@ -430,29 +494,20 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         Item it = S.first();
         for (int k = 0; k < S.n; ++k, S.next(it)) {
             const int h = it.h, tile = it.tile;
-            if (h != cur_h) {
-                // the head's basis image -> TMEM columns 256.. (lane = channel),
-                // after the MMAs of the previous head are done; each warp
-                // loads NT * 16 of the NT * 64 columns of its quadrant
-                if (nimg > 0 && !mbar_wait(imgempty, (nimg - 1) & 1, abort_flag, kWaitNs)) break;
-                tc_fence_after();
-                const uint8_t* src = P.pv.enc_img + size_t(h) * enc_img_bytes(D) + size_t(c) * 256;
-                const int col0 = gi * NT * 16;
-                uint32_t r[NT * 16];
-#pragma unroll
-                for (int u = 0; u < NT * 4; ++u) {
-                    const int jc = col0 + u * 4;            // image column (two bf16 each)
-                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (jc >> 6) * OPND + (jc & 63) * 4));
-                    r[4 * u] = v.x; r[4 * u + 1] = v.y; r[4 * u + 2] = v.z; r[4 * u + 3] = v.w;
+            // rendezvous: accumulator k complete; the codes of tile k-1 all in
+            // shared memory; the bulk store of tile k-2 done reading its buffer
+            if (warp == 2) {
+                if (lane == 0) {
+                    mbar_spin(accfull, k & 1, abort_flag, kWaitNs);
+                    tma_store_wait_read<0>();
                 }
-#pragma unroll
-                for (int u = 0; u < NT; ++u)
-                    tmem_st16(tq + kImgCol + col0 + u * 16, *reinterpret_cast<const uint32_t(*)[16]>(r + 16 * u));
-                tmem_st_wait();
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(imgfull);
-                ++nimg;
+                tc_fence_before();
+            }
+            if (named_barrier_or(1, 32 * kEncEpiWarps, *abort_flag != 0)) break;
+            tc_fence_after();
+            if (leader) flush((k - 1) & 1);
+            if (h != cur_h) {
                 cur_h = h;
                 R = P.pv.rec_bits[h];
                 head_ok = R <= P.pv.max_rec_bits;
@@ -466,8 +521,6 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                 bmax = __reduce_max_sync(0xffffffffu, b);
                 out = reinterpret_cast<uint32_t*>(P.codes + int64_t(h) * P.sstride);
             }
-            if (!mbar_wait(accfull, k & 1, abort_flag, kWaitNs)) break;
-            tc_fence_after();
             uint32_t r0[32], r1[32];
             tmem_ld32(tq + gi * 32, r0);
             tmem_ld32(tq + (gi + 4) * 32, r1);
@@ -475,19 +528,32 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(accempty);      // accumulator read: the next tile's MMAs may start
+            uint32_t* cb = reinterpret_cast<uint32_t*>(smem + L.cb + (k & 1) * L.cbytes);
+            const bool live = head_ok && R > 0;
             if (rwht) {
                 uint32_t Y[8];
-                if (!rwht_norm(r0, tile, gi)) break;
-                if (head_ok && R > 0) { quant8(r0, Y); store8(Y, tile, gi); }
-                if (!rwht_norm(r1, tile, gi + 4)) break;
-                if (head_ok && R > 0) { quant8(r1, Y); store8(Y, tile, gi + 4); }
-            } else if (head_ok && R > 0) {
+                if (rwht_norm(r0, tile, gi)) {
+                    if (live) { quant8(r0, Y); store8(Y, cb, tile, gi); }
+                    if (rwht_norm(r1, tile, gi + 4) && live) { quant8(r1, Y); store8(Y, cb, tile, gi + 4); }
+                }
+            } else if (live) {
                 uint32_t Y0[8], Y1[8];
                 quant8(r0, Y0);
                 quant8(r1, Y1);
-                store8(Y0, tile, gi);
-                store8(Y1, tile, gi + 4);
+                store8(Y0, cb, tile, gi);
+                store8(Y1, cb, tile, gi + 4);
             }
+            fence_proxy_async_smem();      // this thread's words -> the bulk store
+            p_out = out;
+            p_R = R;
+            p_tile = tile;
+            p_live = live;
+        }
+        // the last tile's codes
+        named_barrier(1, 32 * kEncEpiWarps);
+        if (leader) {
+            if (!*abort_flag && S.n > 0) flush((S.n - 1) & 1);
+            tma_store_wait_all<0>();
         }
     }
 
@@ -985,9 +1051,9 @@ tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t* __restrict__ d
             else v = pv.basis_mat[(size_t(h) * D + kk) * D + r];
             const int nt = rwht ? 1 : 3;
             float rem = v;
-            for (int t = 0; t < nt; ++t) {   // row-major [channel][input] (tensor-memory A operand)
+            for (int t = 0; t < nt; ++t) {
                 const __nv_bfloat16 b = __float2bfloat16_rn(rem);
-                *reinterpret_cast<__nv_bfloat16*>(e + t * OPND + size_t(r) * 256 + kk * 2) = b;
+                *reinterpret_cast<__nv_bfloat16*>(e + t * OPND + off) = b;
                 rem -= __bfloat162float(b);
             }
         }
@@ -1105,7 +1171,8 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
     if (total > (int64_t(1) << 31) - 1) return SPECTRA_OK;
     const bool lm = plan->quant == SPECTRA_Q_LLOYD_GAUSS;
     P.stages = 4;
-    while (P.stages > 2 && enc_smem_layout(P.stages, lm).total + 1024 > kSmemMax) --P.stages;
+    while (P.stages > 2 && enc_smem_layout(P.stages, plan->max_rec_bits, lm).total + 1024 > kSmemMax) --P.stages;
+    if (enc_smem_layout(P.stages, plan->max_rec_bits, lm).total + 1024 > kSmemMax) return SPECTRA_OK;
     P.codes = codes;
     P.sstride = sstride;
     P.norms = norms;
@@ -1124,7 +1191,7 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
             grid = int(g2);
         }
     }
-    const uint32_t sm = enc_smem_layout(P.stages, lm).total + 1024;
+    const uint32_t sm = enc_smem_layout(P.stages, plan->max_rec_bits, lm).total + 1024;
     const bool rw = plan->basis == SPECTRA_BASIS_RWHT;
     auto kern = lm ? (rw ? encode_tc_kernel<true, true> : encode_tc_kernel<true, false>)
                    : (rw ? encode_tc_kernel<false, true> : encode_tc_kernel<false, false>);

@@ -93,6 +93,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Non-blocking probe of the phase (no suspension: the caller spins).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Busy-wait for a phase, for the single threads on the critical path (MMA
+// issuer, producer): reacts within a few cycles where a suspended
+// try_wait can sleep past the completion.  Same limits as mbar_wait.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = 2000000000ull)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1,
                                             int c2)
@@ -137,6 +171,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// plain bulk copy shared -> global, tracked by the issuing thread's bulk
+// groups (16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // make generic-proxy shared-memory writes visible to the async proxy
 // (TMA stores, tcgen05.mma operand reads)
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -147,6 +190,22 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 __device__ __forceinline__ void named_barrier(int id, int nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads:
+// every thread gets the same answer (a uniform exit decision).
+__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n"
+        " setp.ne.u32 q, %1, 0;\n"
+        " bar.red.or.pred p, %2, %3, q;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"(uint32_t(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -194,6 +253,14 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Copy a 128-row x 32-byte matrix from shared memory (described by a
+// matrix descriptor, as an MMA operand) to TMEM lanes 0..127, columns
+// col..col+7 (one thread issues; ordered with this thread's tcgen05.mma).
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // thread i of the warp writes lane (base lane + i), columns col..col+31
