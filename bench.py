@@ -243,7 +243,7 @@ def run_ours(args, rank, world, local_rank):
     achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "peak_source": peaks["source"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": None}
+            "traffic": _traffic(dom)}
 
     attn = attn_workload(spx, kp, vp, dev, _peaks()) if args.attn_workload else None
 
@@ -319,11 +319,36 @@ def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3):
 
 def launches_per_step():
     """Kernels this library launches per step (counted from the dispatch in
-    csrc/api.cu): calibrate = Gram partials + Jacobi; alloc = water-filling +
-    finalize; encode 1; decode 1 -- each for K and V; attention = query
-    rotation + split kernel + combine."""
-    per_side = 2 + 2 + 1 + 1
+    csrc/api.cu and csrc/alloc.cu): calibrate = Gram partials + Jacobi;
+    alloc = water-filling + finalize + tensor-core operand images; encode 1;
+    decode 1 -- each for K and V; attention = query preparation + split
+    kernel + combine."""
+    per_side = 2 + 3 + 1 + 1
     return 2 * per_side + 3
+
+
+def _kernel_sources_sha(names):
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "kv_cache_transform_encode_b300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.json), or None when the kernel sources changed since
+    those counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            t = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not t or t.get("sources_sha") != _kernel_sources_sha(t.get("sources", [])):
+        return None
+    return t.get("dram_bytes_per_launch")
 
 
 def _peaks():

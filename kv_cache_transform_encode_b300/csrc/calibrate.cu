@@ -290,7 +290,7 @@ jacobi_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int 
 // Rutishauser's form (c x - s y evaluated as x - s (y + tau x), tau =
 // s / (1 + c)) keeps the transforms orthogonal to working precision.
 constexpr int kJ2 = 128;
-constexpr int kJacCluster = 8;   // CTAs per head in the cluster Jacobi
+constexpr int kJacCluster = 4;   // CTAs per head in the cluster Jacobi (4 measured fastest: 2 and 8 are slower)
 
 struct Rot { float s, tau, t; };
 
