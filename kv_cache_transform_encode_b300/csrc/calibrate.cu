@@ -11,7 +11,9 @@
 //   matrix of one contiguous token chunk in fp32 registers (8x8 or 4x4 tile
 //   per thread) and writes it to the workspace.  Deterministic: the Jacobi
 //   kernel sums the chunk partials in a fixed order.
-// jacobi_kernel: one block per head.  The matrix and the rotation
+// jacobi1s_kernel (d = 128): one-sided Jacobi on the Cholesky factor of G,
+//   a cluster of CTAs per head; see the comment at the kernel.
+// jacobi_kernel (d = 64): one block per head.  The matrix and the rotation
 //   accumulator live in shared memory (rows padded to d+1 floats so column
 //   accesses are bank-conflict free).  Each round applies d/2 disjoint
 //   rotations chosen by the round-robin ("circle") tournament, so a sweep of
@@ -270,677 +272,401 @@ jacobi_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int 
     if (tid == 0) status[h] = converged ? sweeps : -SPECTRA_ERR_NOT_CONVERGED;
 }
 
-// ---------------------------------------------------------------------------
-// jacobi128_kernel: cyclic Jacobi for head_dim 128 with the odd-even
-// ("caterpillar") ordering, register-blocked.  Round r pairs adjacent
-// positions: (2k, 2k+1) when r is even, (2k+1, 2k+2) when r is odd.  Every
-// pair's transform is the Jacobi rotation that annihilates A[p][q] followed
-// by a swap of the two positions, so after 128 rounds (one sweep) every pair
-// of eigen-indices has met exactly once -- the odd-even transposition
-// network run with every comparator exchanging.  Because pairs are always
-// adjacent, the 128x128 matrix A and the accumulator V stay in registers:
-// thread (warp w, lane l) owns the 4x4 blocks A[4w..4w+3][4l..4l+3] and
-// V[4w..][4l..].  Column rotations that straddle two blocks take the
-// neighbour lane's column by shuffle; row rotations that straddle two warps
-// take the neighbour block row from shared memory.  The 64 rotations of a
-// round come from the diagonal band (A[i][i], A[i][i+1]), which the owners
-// of the diagonal and super-diagonal blocks publish after each round; two
-// warps turn the band into rotations while the other thirty apply the
-// previous round's rotations to V (V trails A by one round).
-// Rutishauser's form (c x - s y evaluated as x - s (y + tau x), tau =
-// s / (1 + c)) keeps the transforms orthogonal to working precision.
 constexpr int kJ2 = 128;
-constexpr int kJacCluster = 4;   // CTAs per head in the cluster Jacobi (4 measured fastest: 2 and 8 are slower)
+#ifndef SPECTRA_J1S_CLUSTER
+#define SPECTRA_J1S_CLUSTER 8
+#endif
+constexpr int kJ1sCluster = SPECTRA_J1S_CLUSTER;   // CTAs per head in the one-sided Jacobi (d = 128)
 
-struct Rot { float s, tau, t; };
+// ------------------------------------------------------------------ one-sided Jacobi
+// jacobi1s_kernel<C>: Hestenes' one-sided cyclic Jacobi, spread over a
+// cluster of C CTAs per head, on the Cholesky factor of the Gram matrix:
+// R^T R = G + delta I (R upper triangular; the small shift delta keeps a
+// singular G positive definite in fp32 and changes no eigenvector).  With
+// X = R V (X = R, V = I at the start), each rotation of the column pair
+// (p, q) makes X_p and X_q orthogonal and applies the same plane rotation
+// to V; when every pair is orthogonal, X^T X = V^T (G + delta I) V is
+// diagonal, so the columns of V are the eigenvectors of G, with eigenvalues
+// lambda_i = |X_i|^2 - delta.  Rotating R rather than G itself keeps the
+// convergence of the two-sided method on G (one-sided Jacobi on G behaves
+// like two-sided Jacobi on G^2: half again as many sweeps).  The pair order is the
+// odd-even ("caterpillar") one with rotation-and-swap: positions (2i, 2i+1)
+// in even rounds, (2i+1, 2i+2) in odd rounds, and the rotated columns trade
+// places, so every pair meets once in d rounds.  CTA r owns positions
+// [r d/C, (r+1) d/C) with their whole columns of Gc and V in shared memory:
+// all rotations are local, and in an odd round only the pair that
+// straddles two CTAs needs a column from the neighbour, which that
+// neighbour pushes into this CTA's shared memory (st.async, counted by an
+// mbarrier) at the end of the even round before.  Both CTAs of a straddling
+// pair compute its rotation from the same two columns in the same order, so
+// they agree bit for bit; each keeps the half that lands in its position.
+// The only cluster-wide barriers are once per sweep (convergence) and at
+// the ends.
+template <int C>
+struct J1s {
+    static constexpr int D = kJ2;
+    static constexpr int PPC = D / C;       // positions (columns) per CTA
+    static constexpr int NP = PPC / 2;      // local pairs in an even round
+    static constexpr int NW = NP + 1;       // warps: one per pair + the left boundary
+};
 
-__device__ __forceinline__ Rot load_rot(const float4* prm, int k)
+__device__ __forceinline__ float warp_sum(float v)
 {
-    const float4 v = prm[k];
-    Rot r;
-    r.s = v.x;
-    r.tau = v.y;
-    r.t = v.z;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(uint32_t(__cvta_generic_to_shared(p))), "r"(rank));
     return r;
 }
 
-// (x, y) <- (s x + c y, c x - s y): rotation then swap, in Rutishauser form
-__device__ __forceinline__ void rotswap(float& x, float& y, float s, float tau)
+// 16 bytes into another CTA's shared memory, counted on its mbarrier
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar)
 {
-    const float xn = fmaf(s, fmaf(-tau, y, x), y);
-    const float yn = fmaf(-s, fmaf(tau, x, y), x);
-    x = xn;
-    y = yn;
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
+                 : "memory");
 }
 
-// the same on two rows at once (packed fp32x2 FMAs)
-__device__ __forceinline__ void rotswap2(float2& x, float2& y, float s, float tau)
+__device__ __forceinline__ void mbar_init_local(uint64_t* bar, uint32_t count)
 {
-    const float2 S = make_float2(s, s), NS = make_float2(-s, -s);
-    const float2 T = make_float2(tau, tau), NT = make_float2(-tau, -tau);
-    const float2 u = __ffma2_rn(NT, y, x);
-    const float2 v = __ffma2_rn(T, x, y);
-    const float2 xn = __ffma2_rn(S, u, y);
-    const float2 yn = __ffma2_rn(NS, v, x);
-    x = xn;
-    y = yn;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(uint32_t(__cvta_generic_to_shared(bar))), "r"(count)
+                 : "memory");
 }
 
-// Rotation of pair (p, q) from the band: fast-math reciprocal and square
-// roots (the rotation only has to be orthogonal, which c = rsqrt(1 + t^2),
-// s = t c guarantees to a few ulp whatever small error t carries).
-__device__ __forceinline__ float4 band_rotation(float app, float aqq, float apq)
+__device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes)
 {
-    float s = 0.f, tau = 0.f, t = 0.f;
-    if (fabsf(apq) > 1e-30f && apq * apq > 1e-20f * fabsf(app * aqq)) {
-        const float theta = __fdividef(aqq - app, 2.f * apq);
-        const float at = fabsf(theta);
-        if (at > 1e18f) {
-            t = __fdividef(0.5f, at);
-        } else {
-            const float q1 = fmaf(at, at, 1.f);
-            t = __fdividef(1.f, fmaf(q1, rsqrtf(q1), at));     // 1 / (|theta| + sqrt(theta^2 + 1))
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(uint32_t(__cvta_generic_to_shared(bar))),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// bounded wait for a phase of a local mbarrier (false after ~2 s)
+__device__ __forceinline__ bool mbar_wait_phase(uint64_t* bar, uint32_t parity)
+{
+    const uint32_t a = uint32_t(__cvta_generic_to_shared(bar));
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((it & 63u) == 0) {
+            uint64_t t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            if (it == 0) t0 = t;
+            else if (t - t0 > 2000000000ull) return false;
         }
-        t = (theta >= 0.f) ? t : -t;
+    }
+}
+
+// Rotation of the column pair (p, q): lane holds rows 4l..4l+3 of both.
+// Returns (s, tau) with tau = s / (1 + c) (Rutishauser's form), or s = 0
+// when the pair is already orthogonal to `tol`.  rel = |g| / sqrt(a b).
+__device__ __forceinline__ float2 pair_rotation(float4 p, float4 q, float tol, float& rel)
+{
+    float a = p.x * p.x, b = q.x * q.x, g = p.x * q.x;
+    a = fmaf(p.y, p.y, a); b = fmaf(q.y, q.y, b); g = fmaf(p.y, q.y, g);
+    a = fmaf(p.z, p.z, a); b = fmaf(q.z, q.z, b); g = fmaf(p.z, q.z, g);
+    a = fmaf(p.w, p.w, a); b = fmaf(q.w, q.w, b); g = fmaf(p.w, q.w, g);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+        g += __shfl_xor_sync(0xffffffffu, g, o);
+    }
+    const float ab = a * b;
+    rel = (ab > 0.f) ? fabsf(g) * rsqrtf(ab) : 0.f;
+    float s = 0.f, tau = 0.f;
+    if (ab > 0.f && g * g > tol * tol * ab) {
+        const float zeta = __fdividef(b - a, 2.f * g);
+        const float az = fabsf(zeta);
+        float t;
+        if (az > 1e18f) {
+            t = __fdividef(0.5f, az);
+        } else {
+            const float q1 = fmaf(az, az, 1.f);
+            t = __fdividef(1.f, fmaf(q1, rsqrtf(q1), az));   // 1 / (|zeta| + sqrt(zeta^2 + 1))
+        }
+        t = (zeta >= 0.f) ? t : -t;
         const float c = rsqrtf(fmaf(t, t, 1.f));
         s = t * c;
         tau = __fdividef(s, 1.f + c);
     }
-    return make_float4(s, tau, t, 0.f);
+    return make_float2(s, tau);
 }
 
-// V <- V Q for round parity `par` (columns only; V rows are independent).
-__device__ __forceinline__ void v_update(float2 (&v)[2][4], const float4* pr, bool E, int l)
+// p' = c p - s q = p - s (q + tau p);  q' = s p + c q = q + s (p - tau q)
+__device__ __forceinline__ float4 rot_p(float4 p, float4 q, float s, float tau)
 {
-    if (E) {
-        const Rot c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
-#pragma unroll
-        for (int ip = 0; ip < 2; ++ip) {
-            rotswap2(v[ip][0], v[ip][1], c0.s, c0.tau);
-            rotswap2(v[ip][2], v[ip][3], c1.s, c1.tau);
-        }
-    } else {
-        const bool lf = l > 0, rt = l < 31;
-        const Rot cm = load_rot(pr, lf ? 2 * l - 1 : 0), c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
-#pragma unroll
-        for (int ip = 0; ip < 2; ++ip) {
-            float2 vr, vl;
-            vr.x = __shfl_down_sync(0xffffffffu, v[ip][0].x, 1);
-            vr.y = __shfl_down_sync(0xffffffffu, v[ip][0].y, 1);
-            vl.x = __shfl_up_sync(0xffffffffu, v[ip][3].x, 1);
-            vl.y = __shfl_up_sync(0xffffffffu, v[ip][3].y, 1);
-            if (rt) {
-                float2 x = v[ip][3], y = vr;
-                rotswap2(x, y, c1.s, c1.tau);
-                v[ip][3] = x;
-            }
-            if (lf) {
-                float2 x = vl, y = v[ip][0];
-                rotswap2(x, y, cm.s, cm.tau);
-                v[ip][0] = y;
-            }
-            rotswap2(v[ip][1], v[ip][2], c0.s, c0.tau);
-        }
-    }
+    return make_float4(fmaf(-s, fmaf(tau, p.x, q.x), p.x), fmaf(-s, fmaf(tau, p.y, q.y), p.y),
+                       fmaf(-s, fmaf(tau, p.z, q.z), p.z), fmaf(-s, fmaf(tau, p.w, q.w), p.w));
 }
-
-__global__ void __launch_bounds__(1024, 1)
-jacobi128_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int max_sweeps,
-                 float* __restrict__ basis_out, float* __restrict__ eig_out, int32_t* __restrict__ status,
-                 float* __restrict__ gram_out)
+__device__ __forceinline__ float4 rot_q(float4 p, float4 q, float s, float tau)
 {
-    constexpr int D = kJ2;
-    extern __shared__ float smem[];
-    float* rowx = smem;                                   // [32][2][D] exchanged block rows
-    float* band = rowx + 32 * 2 * D;                      // [2 parity][2][D]: diag, super-diag
-    float4* prm = reinterpret_cast<float4*>(band + 4 * D);  // [2 parity][64]
-    float* red = reinterpret_cast<float*>(prm + 128);     // [33]
-
-    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, h = blockIdx.x;
-    // a[ip][j] = (A[4w + 2ip][4l + j], A[4w + 2ip + 1][4l + j]); v likewise
-    float2 a[2][4], v[2][4];
-#define AE(i, j) ((i) & 1 ? a[(i) >> 1][j].y : a[(i) >> 1][j].x)
-
-    // 1. G = (1/n) sum of the chunk partials (fixed order), V = I.
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int r = 4 * w + i, c = 4 * l + j;
-            const float* src = partials + size_t(h) * nchunks * D * D + size_t(r) * D + c;
-            float sum = 0.f;
-            for (int ch = 0; ch < nchunks; ++ch) sum += src[size_t(ch) * D * D];
-            sum *= inv_n;
-            AE(i, j) = sum;
-            ((i & 1) ? v[i >> 1][j].y : v[i >> 1][j].x) = (r == c) ? 1.f : 0.f;
-            if (gram_out) gram_out[size_t(h) * D * D + size_t(r) * D + c] = sum;
-            bad |= !isfinite(sum);
-        }
-    if (__syncthreads_or(bad)) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                basis_out[size_t(h) * D * D + size_t(4 * w + i) * D + 4 * l + j] = (4 * w + i == 4 * l + j) ? 1.f : 0.f;
-        if (tid < D) eig_out[size_t(h) * D + tid] = 0.f;
-        if (tid == 0) status[h] = -SPECTRA_ERR_NONFINITE;
-        return;
-    }
-    auto publish_band = [&](int par) {
-        float* dg = band + par * 2 * D;
-        float* sp = dg + D;
-        if (w == l) {
-            dg[4 * w + 0] = a[0][0].x; dg[4 * w + 1] = a[0][1].y;
-            dg[4 * w + 2] = a[1][2].x; dg[4 * w + 3] = a[1][3].y;
-            sp[4 * w + 0] = a[0][1].x; sp[4 * w + 1] = a[0][2].y; sp[4 * w + 2] = a[1][3].x;
-        }
-        if (l == w + 1) sp[4 * w + 3] = a[1][0].y;
-    };
-    publish_band(0);
-
-    float loc = 0.f;
-#pragma unroll
-    for (int ip = 0; ip < 2; ++ip)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) loc += a[ip][j].x * a[ip][j].x + a[ip][j].y * a[ip][j].y;
-    const float fro = sqrtf(block_sum(loc, red));
-
-    int sweeps = 0, converged = 0, rounds = 0;
-    float prev_off = INFINITY;
-    for (;;) {
-        loc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (4 * w + i != 4 * l + j) loc = fmaf(AE(i, j), AE(i, j), loc);
-        const float off = sqrtf(block_sum(loc, red));
-        if (off <= 1e-6f * fro || fro == 0.f || (off > 0.5f * prev_off && off <= 1e-4f * fro)) {
-            converged = 1;
-            break;
-        }
-        if (sweeps >= max_sweeps) break;
-        prev_off = off;
-        ++sweeps;
-        for (int r = 0; r < D; ++r, ++rounds) {
-            const int par = r & 1;
-            const bool E = par == 0;   // pairs (2k, 2k+1)
-            __syncthreads();           // band[par] published
-            if (w < 2) {
-                const int k = tid, p = E ? 2 * k : 2 * k + 1, q = p + 1;
-                float4 rt = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (q < D) {
-                    const float* dg = band + par * 2 * D;
-                    rt = band_rotation(dg[p], dg[q], dg[D + p]);
-                }
-                prm[par * 64 + k] = rt;
-            } else if (rounds > 0) {
-                v_update(v, prm + (par ^ 1) * 64, !E, l);   // previous round's rotations
-            }
-            __syncthreads();
-            if (w < 2 && rounds > 0) v_update(v, prm + (par ^ 1) * 64, !E, l);
-            const float4* pr = prm + par * 64;
-            if (E) {
-                const Rot r0 = load_rot(pr, 2 * w), r1 = load_rot(pr, 2 * w + 1);     // rows
-                const Rot c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);     // columns
-                float d00 = 0.f, d11 = 0.f, d01 = 0.f, d22 = 0.f, d33 = 0.f, d23 = 0.f;
-                if (w == l) {
-                    d00 = a[0][0].x; d11 = a[0][1].y; d01 = a[0][1].x;
-                    d22 = a[1][2].x; d33 = a[1][3].y; d23 = a[1][3].x;
-                }
-#pragma unroll
-                for (int ip = 0; ip < 2; ++ip) {
-                    rotswap2(a[ip][0], a[ip][1], c0.s, c0.tau);
-                    rotswap2(a[ip][2], a[ip][3], c1.s, c1.tau);
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    rotswap(a[0][j].x, a[0][j].y, r0.s, r0.tau);
-                    rotswap(a[1][j].x, a[1][j].y, r1.s, r1.tau);
-                }
-                if (w == l) {   // diagonal sub-blocks: exact values
-                    a[0][0].x = fmaf(r0.t, d01, d11); a[0][1].y = fmaf(-r0.t, d01, d00);
-                    a[0][1].x = 0.f; a[0][0].y = 0.f;
-                    a[1][2].x = fmaf(r1.t, d23, d33); a[1][3].y = fmaf(-r1.t, d23, d22);
-                    a[1][3].x = 0.f; a[1][2].y = 0.f;
-                }
-            } else {
-                const bool up = w > 0, dn = w < 31, lf = l > 0, rt = l < 31;
-                const Rot cm = load_rot(pr, lf ? 2 * l - 1 : 0), c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
-                float d11 = 0.f, d22 = 0.f, d12 = 0.f;
-                if (w == l) { d11 = a[0][1].y; d22 = a[1][2].x; d12 = a[0][2].y; }
-                // columns: (4l-1, 4l) with the left lane, (4l+1, 4l+2) inside, (4l+3, 4l+4) with the right lane
-#pragma unroll
-                for (int ip = 0; ip < 2; ++ip) {
-                    float2 ar, al;
-                    ar.x = __shfl_down_sync(0xffffffffu, a[ip][0].x, 1);
-                    ar.y = __shfl_down_sync(0xffffffffu, a[ip][0].y, 1);
-                    al.x = __shfl_up_sync(0xffffffffu, a[ip][3].x, 1);
-                    al.y = __shfl_up_sync(0xffffffffu, a[ip][3].y, 1);
-                    if (rt) {
-                        float2 x = a[ip][3], y = ar;
-                        rotswap2(x, y, c1.s, c1.tau);
-                        a[ip][3] = x;
-                    }
-                    if (lf) {
-                        float2 x = al, y = a[ip][0];
-                        rotswap2(x, y, cm.s, cm.tau);
-                        a[ip][0] = y;
-                    }
-                    rotswap2(a[ip][1], a[ip][2], c0.s, c0.tau);
-                }
-                // rows: (4w-1, 4w) and (4w+3, 4w+4) through shared memory
-                float* mine = rowx + w * 2 * D + 4 * l;
-                *reinterpret_cast<float4*>(mine) = make_float4(a[0][0].x, a[0][1].x, a[0][2].x, a[0][3].x);
-                *reinterpret_cast<float4*>(mine + D) = make_float4(a[1][0].y, a[1][1].y, a[1][2].y, a[1][3].y);
-                __syncthreads();
-                const Rot rm = load_rot(pr, up ? 2 * w - 1 : 0), r0 = load_rot(pr, 2 * w), r1 = load_rot(pr, 2 * w + 1);
-                if (dn) {
-                    const float4 b4 = *reinterpret_cast<const float4*>(rowx + (w + 1) * 2 * D + 4 * l);
-                    const float bl[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) a[1][j].y = fmaf(r1.s, fmaf(-r1.tau, bl[j], a[1][j].y), bl[j]);
-                }
-                if (up) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(rowx + (w - 1) * 2 * D + D + 4 * l);
-                    const float ab[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) a[0][j].x = fmaf(-rm.s, fmaf(rm.tau, ab[j], a[0][j].x), ab[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) rotswap(a[0][j].y, a[1][j].x, r0.s, r0.tau);
-                if (w == l) {
-                    a[0][1].y = fmaf(r0.t, d12, d22); a[1][2].x = fmaf(-r0.t, d12, d11);
-                    a[0][2].y = 0.f; a[1][1].x = 0.f;
-                }
-            }
-            publish_band(par ^ 1);
-        }
-    }
-    if (rounds > 0) {   // V trails A by one round: apply the last one
-        __syncthreads();
-        v_update(v, prm + ((rounds - 1) & 1) * 64, ((rounds - 1) & 1) == 0, l);
-    }
-
-    // 2. Sort descending (ties: lower position first), sign-fix, write out.
-    __syncthreads();
-    constexpr int LD = D + 1;
-    float* Vs = smem;                 // [D][LD]
-    float* lam = Vs + D * LD;         // [D]
-    int* rank = reinterpret_cast<int*>(lam + D);
-#pragma unroll
-    for (int ip = 0; ip < 2; ++ip)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            Vs[(4 * w + 2 * ip) * LD + 4 * l + j] = v[ip][j].x;
-            Vs[(4 * w + 2 * ip + 1) * LD + 4 * l + j] = v[ip][j].y;
-        }
-    if (w == l) {
-        lam[4 * w + 0] = a[0][0].x; lam[4 * w + 1] = a[0][1].y;
-        lam[4 * w + 2] = a[1][2].x; lam[4 * w + 3] = a[1][3].y;
-    }
-#undef AE
-    __syncthreads();
-    if (tid < D) {
-        const float li = lam[tid];
-        int rk = 0;
-        for (int j = 0; j < D; ++j) {
-            const float lj = lam[j];
-            rk += (lj > li) || (lj == li && j < tid);
-        }
-        rank[tid] = rk;
-    }
-    __syncthreads();
-    for (int i = w; i < D; i += 32) {
-        float best = -1.f;
-        int br = 0;
-        for (int rr = l; rr < D; rr += 32) {
-            const float av = fabsf(Vs[rr * LD + i]);
-            if (av > best) { best = av; br = rr; }
-        }
-        for (int o = 16; o; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int orr = __shfl_xor_sync(0xffffffffu, br, o);
-            if (ob > best || (ob == best && orr < br)) { best = ob; br = orr; }
-        }
-        const float sgn = (Vs[br * LD + i] < 0.f) ? -1.f : 1.f;
-        const int c = rank[i];
-        for (int rr = l; rr < D; rr += 32) basis_out[size_t(h) * D * D + size_t(rr) * D + c] = sgn * Vs[rr * LD + i];
-        if (l == 0) eig_out[size_t(h) * D + c] = lam[i];
-    }
-    if (tid == 0) status[h] = converged ? sweeps : -SPECTRA_ERR_NOT_CONVERGED;
+    return make_float4(fmaf(s, fmaf(-tau, q.x, p.x), q.x), fmaf(s, fmaf(-tau, q.y, p.y), q.y),
+                       fmaf(s, fmaf(-tau, q.z, p.z), q.z), fmaf(s, fmaf(-tau, q.w, p.w), q.w));
 }
 
-size_t jacobi128_smem()
-{
-    const size_t work = sizeof(float) * (32 * 2 * kJ2 + 4 * kJ2) + sizeof(float4) * 128 + sizeof(float) * 33;
-    const size_t fin = sizeof(float) * (kJ2 * (kJ2 + 1) + kJ2) + sizeof(int) * kJ2;
-    return (work > fin ? work : fin) + 16;
-}
-
-// ---------------------------------------------------------------------------
-// jacobi128c_kernel<C>: the same odd-even Jacobi spread over a cluster of C
-// CTAs per head (distributed shared memory).  CTA r owns block rows
-// [NW r, NW r + NW) (NW = 32 / C warps, 4 rows each) of A and V; thread
-// (warp, lane) still owns one 4x4 block of each.  Once per round, after a
-// cluster barrier, every CTA holds the whole diagonal band (each CTA writes
-// its band entries into all CTAs' shared memory) and computes the round's 64
-// rotations itself; the block rows that straddle two CTAs in odd rounds are
-// sent ahead (as they stand after the previous round) and each receiver
-// applies the column rotations to its copy.  Every CTA runs the same rounds
-// and takes the same convergence decision (cluster-reduced in a fixed
-// order), so every barrier is met by all CTAs.
 template <int C>
-__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(1024 / C, 1)
-jacobi128c_kernel(const float* partials, int nchunks, float inv_n, int max_sweeps,
-                  float* __restrict__ basis_out, float* __restrict__ eig_out, int32_t* __restrict__ status,
-                  float* __restrict__ gram_out, float* scratch)
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(32 * J1s<C>::NW, 1)
+jacobi1s_kernel(const float* __restrict__ partials, int nchunks, float inv_n, int max_sweeps,
+                float* __restrict__ basis_out, float* __restrict__ eig_out, int32_t* __restrict__ status,
+                float* __restrict__ gram_out)
 {
     namespace cg = cooperative_groups;
-    constexpr int D = kJ2;
-    constexpr int NW = 32 / C;                // warps per CTA
-    constexpr int NT = 32 * NW;
+    constexpr int D = J1s<C>::D, PPC = J1s<C>::PPC, NP = J1s<C>::NP, NW = J1s<C>::NW;
+    constexpr uint32_t kColBytes = 2 * D * 4;          // one column of Gc and of V
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = int(cluster.block_rank());
     const int hd = blockIdx.x / C;
-
-    extern __shared__ float smem[];
-    float* rowx = smem;                                    // [NW][2][D]
-    float* band = rowx + NW * 2 * D;                       // [2][2][D]
-    float* nbr = band + 4 * D;                             // [2 parity][2: up, down][D]
-    float4* prm = reinterpret_cast<float4*>(nbr + 4 * D);  // [2][64]
-    float* red = reinterpret_cast<float*>(prm + 128);      // [33]
-    float* csum = red + 33;                                // [2][C] cluster partial sums
-    float* lamall = csum + 2 * C;                          // [D]
-    int* cflag = reinterpret_cast<int*>(lamall + D);       // [C]
-
     const int tid = threadIdx.x, wl = tid >> 5, l = tid & 31;
-    const int w = rank * NW + wl;                          // global block row
-    cluster.sync();    // every CTA of the cluster runs before any shared memory is touched remotely
-    float2 a[2][4], v[2][4];
-#define AE(i, j) ((i) & 1 ? a[(i) >> 1][j].y : a[(i) >> 1][j].x)
 
-    // cluster-wide sum of one float per CTA, identical in every CTA
-    int cuse = 0;
-    auto cluster_sum = [&](float part) -> float {
-        const float tot = block_sum(part, red);
-        if (tid < C) *cluster.map_shared_rank(csum + (cuse & 1) * C + rank, tid) = tot;
-        cluster.sync();
-        float s = 0.f;
-        for (int k = 0; k < C; ++k) s += csum[(cuse & 1) * C + k];
-        ++cuse;
-        return s;
-    };
+    extern __shared__ __align__(16) float jsm[];
+    float (*Gc)[D] = reinterpret_cast<float (*)[D]>(jsm);               // [PPC][D] columns of X
+    float (*Vc)[D] = reinterpret_cast<float (*)[D]>(jsm + PPC * D);     // [PPC][D] columns of V
+    float* Am = jsm + 2 * PPC * D;                                      // [D][D + 1] Gram / Cholesky
+    __shared__ __align__(16) float rb[2][2][2][D];     // [side: from left, from right][parity][Gc, V]
+    __shared__ __align__(8) uint64_t rbar[2][2];       // [side][parity]
+    __shared__ float wred[NW];
+    __shared__ float cred[2][C];                       // cluster exchange (two slots)
+    __shared__ float lamall[D];
+    __shared__ int cflag[2][C];
 
+    if (tid == 0) {
+        for (int sd = 0; sd < 2; ++sd)
+            for (int pp = 0; pp < 2; ++pp) mbar_init_local(&rbar[sd][pp], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    constexpr int AS = D + 1;                          // Cholesky row stride (conflict-free columns)
+    // the whole Gram matrix (every CTA), this CTA's columns to gram_out
     bool bad = false;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int r = 4 * w + i, c = 4 * l + j;
-            const float* src = partials + size_t(hd) * nchunks * D * D + size_t(r) * D + c;
-            float sum = 0.f;
-            for (int ch = 0; ch < nchunks; ++ch) sum += src[size_t(ch) * D * D];
-            sum *= inv_n;
-            AE(i, j) = sum;
-            ((i & 1) ? v[i >> 1][j].y : v[i >> 1][j].x) = (r == c) ? 1.f : 0.f;
-            if (gram_out) gram_out[size_t(hd) * D * D + size_t(r) * D + c] = sum;
-            bad |= !isfinite(sum);
-        }
+    for (int e = tid; e < D * D; e += 32 * NW) {
+        const int r = e / D, c = e % D;
+        const float* src = partials + size_t(hd) * nchunks * D * D + e;
+        float sum = 0.f;
+        for (int ch = 0; ch < nchunks; ++ch) sum += src[size_t(ch) * D * D];
+        sum *= inv_n;
+        Am[r * AS + c] = sum;
+        if (gram_out && c / PPC == rank) gram_out[size_t(hd) * D * D + e] = sum;
+        bad |= !isfinite(sum);
+    }
     {
         const int bl = __syncthreads_or(bad);
-        if (tid < C) *cluster.map_shared_rank(cflag + rank, tid) = bl;
-        cluster.sync();
+        if (tid < C) *cluster.map_shared_rank(&cflag[0][rank], tid) = bl;
+        cluster.sync();   // also: every CTA runs (and its barriers exist) before any remote access
         int any = 0;
-        for (int k = 0; k < C; ++k) any |= cflag[k];
+        for (int k = 0; k < C; ++k) any |= cflag[0][k];
         if (any) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    basis_out[size_t(hd) * D * D + size_t(4 * w + i) * D + 4 * l + j] = (4 * w + i == 4 * l + j) ? 1.f : 0.f;
+            for (int e = tid; e < PPC * D; e += 32 * NW) {
+                const int r = e / PPC, c = rank * PPC + e % PPC;
+                basis_out[size_t(hd) * D * D + size_t(r) * D + c] = (r == c) ? 1.f : 0.f;
+            }
             if (rank == 0 && tid < D) eig_out[size_t(hd) * D + tid] = 0.f;
             if (rank == 0 && tid == 0) status[hd] = -SPECTRA_ERR_NONFINITE;
+            cluster.sync();
             return;
         }
     }
-    // publish this CTA's band entries (all CTAs) and, before odd rounds, the
-    // block rows the neighbour CTAs need
-    auto publish = [&](int par, bool rows) {
-        if (w == l) {
-            const float dv[4] = {a[0][0].x, a[0][1].y, a[1][2].x, a[1][3].y};
-            const float sv[3] = {a[0][1].x, a[0][2].y, a[1][3].x};
-            for (int k = 0; k < C; ++k) {
-                float* dg = cluster.map_shared_rank(band + par * 2 * D, k);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dg[4 * w + i] = dv[i];
-#pragma unroll
-                for (int i = 0; i < 3; ++i) dg[D + 4 * w + i] = sv[i];
-            }
-        }
-        if (l == w + 1) {
-            for (int k = 0; k < C; ++k) cluster.map_shared_rank(band + par * 2 * D, k)[D + 4 * w + 3] = a[1][0].y;
-        }
-        if (rows) {
-            if (wl == 0 && rank > 0) {          // my row 0 -> rank-1's "down" row
-                float* dst = cluster.map_shared_rank(nbr + (par * 2 + 1) * D, rank - 1) + 4 * l;
-                *reinterpret_cast<float4*>(dst) = make_float4(a[0][0].x, a[0][1].x, a[0][2].x, a[0][3].x);
-            }
-            if (wl == NW - 1 && rank < C - 1) { // my row 3 -> rank+1's "up" row
-                float* dst = cluster.map_shared_rank(nbr + (par * 2 + 0) * D, rank + 1) + 4 * l;
-                *reinterpret_cast<float4*>(dst) = make_float4(a[1][0].y, a[1][1].y, a[1][2].y, a[1][3].y);
-            }
-        }
-    };
-    publish(0, false);
 
-    float loc = 0.f;
+    // G + delta I = L L^T (L lower triangular, in place), R = L^T.  delta is
+    // a few fp32 rounding units of the largest diagonal entry times d, so a
+    // positive semi-definite G never meets a non-positive pivot.
+    float dmax = 0.f;
+    for (int i = 0; i < D; ++i) dmax = fmaxf(dmax, Am[i * AS + i]);
+    const float delta = 8e-7f * float(D) * dmax;
+    for (int i = tid; i < D; i += 32 * NW) Am[i * AS + i] += delta;
+    // Right-looking, one barrier per step: step j subtracts A[i][j] A[k][j] /
+    // A[j][j] from the trailing lower triangle (rows by warp, columns by
+    // lane) while column j-1, which nobody reads any more, is scaled into L.
+    float prev_d = 1.f;
+    for (int j = 0; j <= D; ++j) {
+        __syncthreads();
+        if (j > 0) {                                   // column j-1 -> L
+            for (int i = j + tid; i < D; i += 32 * NW) Am[i * AS + j - 1] *= 1.f / prev_d;
+            if (tid == 0) Am[(j - 1) * AS + j - 1] = prev_d;
+        }
+        if (j == D) break;
+        const float piv = fmaxf(Am[j * AS + j], 1e-30f);
+        const float inv = 1.f / piv;
+        // this lane's trailing columns k = j+1+l+32u and their multipliers
+        float ak[4];
 #pragma unroll
-    for (int ip = 0; ip < 2; ++ip)
+        for (int u = 0; u < 4; ++u) {
+            const int k = j + 1 + l + 32 * u;
+            ak[u] = (k < D) ? Am[k * AS + j] * inv : 0.f;
+        }
+        for (int i = j + 1 + wl; i < D; i += NW) {
+            const float lij = Am[i * AS + j];
+            float* row = Am + i * AS + j + 1 + l;
+            float v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) loc += a[ip][j].x * a[ip][j].x + a[ip][j].y * a[ip][j].y;
-    const float fro = sqrtf(cluster_sum(loc));
+            for (int u = 0; u < 4; ++u) v[u] = (j + 1 + l + 32 * u <= i) ? row[32 * u] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j + 1 + l + 32 * u <= i) row[32 * u] = fmaf(-lij, ak[u], v[u]);
+        }
+        prev_d = sqrtf(piv);
+    }
+    __syncthreads();
+    // X = R: column c of R is row c of L (zero past the diagonal); V = I
+    for (int e = tid; e < PPC * D; e += 32 * NW) {
+        const int cl = e / D, r = e % D, c = rank * PPC + cl;
+        Gc[cl][r] = (r <= c) ? Am[c * AS + r] : 0.f;
+        Vc[cl][r] = (r == c) ? 1.f : 0.f;
+    }
+    __syncthreads();
 
-    // column rotations of one 4-wide row segment (odd round): (4l-1, 4l) with
-    // the left lane, (4l+1, 4l+2) inside, (4l+3, 4l+4) with the right lane
-    auto col_odd = [&](float (&x)[4], const Rot& cm, const Rot& c0, const Rot& c1) {
-        const float xr = __shfl_down_sync(0xffffffffu, x[0], 1);
-        const float xl = __shfl_up_sync(0xffffffffu, x[3], 1);
-        if (l < 31) x[3] = fmaf(c1.s, fmaf(-c1.tau, xr, x[3]), xr);
-        if (l > 0) x[0] = fmaf(-cm.s, fmaf(cm.tau, xl, x[0]), xl);
-        rotswap(x[1], x[2], c0.s, c0.tau);
-    };
-
-    int sweeps = 0, converged = 0, rounds = 0;
-    float prev_off = INFINITY;
+    constexpr float kTol = 2e-6f;      // |X_p . X_q| / (|X_p| |X_q|) below which a pair counts as orthogonal
+    int sweeps = 0, converged = 0, failed = 0, cuse = 1;
+    uint32_t gr = 0;                   // rounds so far (all sweeps)
+    float4* G4 = reinterpret_cast<float4*>(&Gc[0][0]);
+    float4* V4 = reinterpret_cast<float4*>(&Vc[0][0]);
+    constexpr int Q = D / 4;           // float4 per column
     for (;;) {
-        loc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (4 * w + i != 4 * l + j) loc = fmaf(AE(i, j), AE(i, j), loc);
-        const float off = sqrtf(cluster_sum(loc));
-        if (off <= 1e-6f * fro || fro == 0.f || (off > 0.5f * prev_off && off <= 1e-4f * fro)) {
-            converged = 1;
-            break;
-        }
         if (sweeps >= max_sweeps) break;
-        prev_off = off;
         ++sweeps;
-        for (int r = 0; r < D; ++r, ++rounds) {
-            const int par = r & 1;
-            const bool E = par == 0;
-            cluster.sync();                        // band[par] (and rows) from every CTA visible
-            if (wl < 2) {
-                const int k = tid, p = E ? 2 * k : 2 * k + 1, q = p + 1;
-                float4 rt = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (q < D) {
-                    const float* dg = band + par * 2 * D;
-                    rt = band_rotation(dg[p], dg[q], dg[D + p]);
-                }
-                prm[par * 64 + k] = rt;
-            } else if (rounds > 0) {
-                v_update(v, prm + (par ^ 1) * 64, !E, l);
-            }
-            __syncthreads();
-            if (wl < 2 && rounds > 0) v_update(v, prm + (par ^ 1) * 64, !E, l);
-            const float4* pr = prm + par * 64;
-            if (E) {
-                const Rot r0 = load_rot(pr, 2 * w), r1 = load_rot(pr, 2 * w + 1);
-                const Rot c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
-                float d00 = 0.f, d11 = 0.f, d01 = 0.f, d22 = 0.f, d33 = 0.f, d23 = 0.f;
-                if (w == l) {
-                    d00 = a[0][0].x; d11 = a[0][1].y; d01 = a[0][1].x;
-                    d22 = a[1][2].x; d33 = a[1][3].y; d23 = a[1][3].x;
-                }
-#pragma unroll
-                for (int ip = 0; ip < 2; ++ip) {
-                    rotswap2(a[ip][0], a[ip][1], c0.s, c0.tau);
-                    rotswap2(a[ip][2], a[ip][3], c1.s, c1.tau);
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    rotswap(a[0][j].x, a[0][j].y, r0.s, r0.tau);
-                    rotswap(a[1][j].x, a[1][j].y, r1.s, r1.tau);
-                }
-                if (w == l) {
-                    a[0][0].x = fmaf(r0.t, d01, d11); a[0][1].y = fmaf(-r0.t, d01, d00);
-                    a[0][1].x = 0.f; a[0][0].y = 0.f;
-                    a[1][2].x = fmaf(r1.t, d23, d33); a[1][3].y = fmaf(-r1.t, d23, d22);
-                    a[1][3].x = 0.f; a[1][2].y = 0.f;
+        float mrel = 0.f;
+        for (int r = 0; r < D; ++r, ++gr) {
+            const uint32_t k = gr >> 1, kp = k & 1, ph = (k >> 1) & 1;   // odd-round index, buffer, phase
+            if ((gr & 1) == 0) {
+                // even round: local pairs (2w, 2w+1)
+                if (wl < NP) {
+                    const int P = 2 * wl;
+                    const float4 gp = G4[P * Q + l], gq = G4[(P + 1) * Q + l];
+                    const float4 vp = V4[P * Q + l], vq = V4[(P + 1) * Q + l];
+                    float rel;
+                    const float2 st = pair_rotation(gp, gq, kTol, rel);
+                    mrel = fmaxf(mrel, rel);
+                    const float4 gq2 = rot_q(gp, gq, st.x, st.y), gp2 = rot_p(gp, gq, st.x, st.y);
+                    const float4 vq2 = rot_q(vp, vq, st.x, st.y), vp2 = rot_p(vp, vq, st.x, st.y);
+                    G4[P * Q + l] = gq2;          // swap: position P takes the rotated q
+                    V4[P * Q + l] = vq2;
+                    G4[(P + 1) * Q + l] = gp2;
+                    V4[(P + 1) * Q + l] = vp2;
+                    // the next odd round's straddling pairs need these columns
+                    if (P == 0 && rank > 0) {      // position 0 -> left neighbour, "from right"
+                        const uint32_t rk = uint32_t(rank - 1);
+                        const uint32_t bar = cluster_map(&rbar[1][kp], rk);
+                        st_async_v4(cluster_map(&rb[1][kp][0][4 * l], rk), gq2, bar);
+                        st_async_v4(cluster_map(&rb[1][kp][1][4 * l], rk), vq2, bar);
+                    }
+                    if (P + 1 == PPC - 1 && rank < C - 1) {   // last position -> right neighbour, "from left"
+                        const uint32_t rk = uint32_t(rank + 1);
+                        const uint32_t bar = cluster_map(&rbar[0][kp], rk);
+                        st_async_v4(cluster_map(&rb[0][kp][0][4 * l], rk), gp2, bar);
+                        st_async_v4(cluster_map(&rb[0][kp][1][4 * l], rk), vp2, bar);
+                    }
                 }
             } else {
-                const bool up = w > 0, dn = w < 31, lf = l > 0, rt = l < 31;
-                const Rot cm = load_rot(pr, lf ? 2 * l - 1 : 0), c0 = load_rot(pr, 2 * l), c1 = load_rot(pr, 2 * l + 1);
-                float d11 = 0.f, d22 = 0.f, d12 = 0.f;
-                if (w == l) { d11 = a[0][1].y; d22 = a[1][2].x; d12 = a[0][2].y; }
-#pragma unroll
-                for (int ip = 0; ip < 2; ++ip) {
-                    float2 ar, al;
-                    ar.x = __shfl_down_sync(0xffffffffu, a[ip][0].x, 1);
-                    ar.y = __shfl_down_sync(0xffffffffu, a[ip][0].y, 1);
-                    al.x = __shfl_up_sync(0xffffffffu, a[ip][3].x, 1);
-                    al.y = __shfl_up_sync(0xffffffffu, a[ip][3].y, 1);
-                    if (rt) {
-                        float2 x = a[ip][3], y = ar;
-                        rotswap2(x, y, c1.s, c1.tau);
-                        a[ip][3] = x;
+                // odd round: local pairs (2w+1, 2w+2); warp NP-1 the pair
+                // (last, right neighbour's first), warp NP the pair (left
+                // neighbour's last, first)
+                if (wl < NP - 1) {
+                    const int P = 2 * wl + 1;
+                    const float4 gp = G4[P * Q + l], gq = G4[(P + 1) * Q + l];
+                    const float4 vp = V4[P * Q + l], vq = V4[(P + 1) * Q + l];
+                    float rel;
+                    const float2 st = pair_rotation(gp, gq, kTol, rel);
+                    mrel = fmaxf(mrel, rel);
+                    G4[P * Q + l] = rot_q(gp, gq, st.x, st.y);
+                    V4[P * Q + l] = rot_q(vp, vq, st.x, st.y);
+                    G4[(P + 1) * Q + l] = rot_p(gp, gq, st.x, st.y);
+                    V4[(P + 1) * Q + l] = rot_p(vp, vq, st.x, st.y);
+                } else if (wl == NP - 1) {
+                    if (rank < C - 1) {
+                        if (l == 0) mbar_expect(&rbar[1][kp], kColBytes);
+                        if (!mbar_wait_phase(&rbar[1][kp], ph)) failed = 1;
+                        const int P = PPC - 1;
+                        const float4 gp = G4[P * Q + l], vp = V4[P * Q + l];
+                        const float4 gq = *reinterpret_cast<const float4*>(&rb[1][kp][0][4 * l]);
+                        const float4 vq = *reinterpret_cast<const float4*>(&rb[1][kp][1][4 * l]);
+                        float rel;
+                        const float2 st = pair_rotation(gp, gq, kTol, rel);
+                        mrel = fmaxf(mrel, rel);
+                        G4[P * Q + l] = rot_q(gp, gq, st.x, st.y);
+                        V4[P * Q + l] = rot_q(vp, vq, st.x, st.y);
                     }
-                    if (lf) {
-                        float2 x = al, y = a[ip][0];
-                        rotswap2(x, y, cm.s, cm.tau);
-                        a[ip][0] = y;
+                } else {
+                    if (rank > 0) {
+                        if (l == 0) mbar_expect(&rbar[0][kp], kColBytes);
+                        if (!mbar_wait_phase(&rbar[0][kp], ph)) failed = 1;
+                        const float4 gq = G4[l], vq = V4[l];
+                        const float4 gp = *reinterpret_cast<const float4*>(&rb[0][kp][0][4 * l]);
+                        const float4 vp = *reinterpret_cast<const float4*>(&rb[0][kp][1][4 * l]);
+                        float rel;
+                        const float2 st = pair_rotation(gp, gq, kTol, rel);
+                        mrel = fmaxf(mrel, rel);
+                        G4[l] = rot_p(gp, gq, st.x, st.y);
+                        V4[l] = rot_p(vp, vq, st.x, st.y);
                     }
-                    rotswap2(a[ip][1], a[ip][2], c0.s, c0.tau);
-                }
-                // rows across warps of this CTA: shared memory; across CTAs:
-                // the neighbour's row as it stood, column-rotated here
-                float* mine = rowx + wl * 2 * D + 4 * l;
-                *reinterpret_cast<float4*>(mine) = make_float4(a[0][0].x, a[0][1].x, a[0][2].x, a[0][3].x);
-                *reinterpret_cast<float4*>(mine + D) = make_float4(a[1][0].y, a[1][1].y, a[1][2].y, a[1][3].y);
-                float ab[4] = {0.f, 0.f, 0.f, 0.f}, bl[4] = {0.f, 0.f, 0.f, 0.f};
-                if (wl == 0 && up) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(nbr + (par * 2 + 0) * D + 4 * l);
-                    ab[0] = t4.x; ab[1] = t4.y; ab[2] = t4.z; ab[3] = t4.w;
-                    col_odd(ab, cm, c0, c1);
-                }
-                if (wl == NW - 1 && dn) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(nbr + (par * 2 + 1) * D + 4 * l);
-                    bl[0] = t4.x; bl[1] = t4.y; bl[2] = t4.z; bl[3] = t4.w;
-                    col_odd(bl, cm, c0, c1);
-                }
-                __syncthreads();
-                const Rot rm = load_rot(pr, up ? 2 * w - 1 : 0), r0 = load_rot(pr, 2 * w), r1 = load_rot(pr, 2 * w + 1);
-                if (dn) {
-                    if (wl < NW - 1) {
-                        const float4 b4 = *reinterpret_cast<const float4*>(rowx + (wl + 1) * 2 * D + 4 * l);
-                        bl[0] = b4.x; bl[1] = b4.y; bl[2] = b4.z; bl[3] = b4.w;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) a[1][j].y = fmaf(r1.s, fmaf(-r1.tau, bl[j], a[1][j].y), bl[j]);
-                }
-                if (up) {
-                    if (wl > 0) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(rowx + (wl - 1) * 2 * D + D + 4 * l);
-                        ab[0] = a4.x; ab[1] = a4.y; ab[2] = a4.z; ab[3] = a4.w;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) a[0][j].x = fmaf(-rm.s, fmaf(rm.tau, ab[j], a[0][j].x), ab[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) rotswap(a[0][j].y, a[1][j].x, r0.s, r0.tau);
-                if (w == l) {
-                    a[0][1].y = fmaf(r0.t, d12, d22); a[1][2].x = fmaf(-r0.t, d12, d11);
-                    a[0][2].y = 0.f; a[1][1].x = 0.f;
                 }
             }
-            publish(par ^ 1, E);
+            __syncthreads();
         }
-    }
-    if (rounds > 0) {
+        // sweep done: cluster-wide max of the pair residuals and the failure flag
+        if (l == 0) wred[wl] = failed ? INFINITY : mrel;
         __syncthreads();
-        v_update(v, prm + ((rounds - 1) & 1) * 64, ((rounds - 1) & 1) == 0, l);
+        if (tid < C) {
+            float m = 0.f;
+            for (int w = 0; w < NW; ++w) m = fmaxf(m, wred[w]);
+            *cluster.map_shared_rank(&cred[cuse & 1][rank], tid) = m;
+        }
+        cluster.sync();
+        float m = 0.f;
+        for (int kk = 0; kk < C; ++kk) m = fmaxf(m, cred[cuse & 1][kk]);
+        ++cuse;
+        if (m == INFINITY) { failed = 1; break; }
+        if (m <= kTol) { converged = 1; break; }
     }
 
-    // Sort descending (ties: lower position first), sign-fix, write out.  V
-    // rows go through global scratch, eigenvalues to every CTA.
-    float* Vg = scratch + size_t(hd) * nchunks * D * D;    // [D][D] position-ordered columns
-#pragma unroll
-    for (int ip = 0; ip < 2; ++ip)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            Vg[size_t(4 * w + 2 * ip) * D + 4 * l + j] = v[ip][j].x;
-            Vg[size_t(4 * w + 2 * ip + 1) * D + 4 * l + j] = v[ip][j].y;
-        }
-    if (w == l) {
-        const float dv[4] = {a[0][0].x, a[0][1].y, a[1][2].x, a[1][3].y};
-        for (int k = 0; k < C; ++k) {
-            float* lm = cluster.map_shared_rank(lamall, k);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) lm[4 * w + i] = dv[i];
-        }
+    // eigenvalues (Rayleigh quotients) to every CTA; ranks, sign fix, output
+    for (int P = wl; P < PPC; P += NW) {
+        const float4 g = G4[P * Q + l];
+        const float lam = warp_sum(g.x * g.x + g.y * g.y + g.z * g.z + g.w * g.w) - delta;
+        if (l < C) *cluster.map_shared_rank(&lamall[rank * PPC + P], l) = lam;
     }
-#undef AE
-    __threadfence();
     cluster.sync();
-    constexpr int CPC = D / C;                 // columns per CTA
-    for (int ci = wl; ci < CPC; ci += NW) {
-        const int i = rank * CPC + ci;         // position
+    for (int P = wl; P < PPC; P += NW) {
+        const int i = rank * PPC + P;
         const float li = lamall[i];
         int rk = 0;
         for (int j = l; j < D; j += 32) {
             const float lj = lamall[j];
             rk += (lj > li) || (lj == li && j < i);
         }
-        for (int o = 16; o; o >>= 1) rk += __shfl_xor_sync(0xffffffffu, rk, o);
-        float best = -1.f;
-        int br = 0;
-        for (int rr = l; rr < D; rr += 32) {
-            const float av = fabsf(__ldcg(Vg + size_t(rr) * D + i));   // written by other CTAs: skip L1
-            if (av > best) { best = av; br = rr; }
-        }
+        rk = int(warp_sum(float(rk)) + 0.5f);
+        const float4 v = V4[P * Q + l];
+        float best = fabsf(v.x);
+        int br = 4 * l;
+        if (fabsf(v.y) > best) { best = fabsf(v.y); br = 4 * l + 1; }
+        if (fabsf(v.z) > best) { best = fabsf(v.z); br = 4 * l + 2; }
+        if (fabsf(v.w) > best) { best = fabsf(v.w); br = 4 * l + 3; }
+        float bv = (br == 4 * l) ? v.x : (br == 4 * l + 1) ? v.y : (br == 4 * l + 2) ? v.z : v.w;
         for (int o = 16; o; o >>= 1) {
             const float ob = __shfl_xor_sync(0xffffffffu, best, o);
             const int orr = __shfl_xor_sync(0xffffffffu, br, o);
-            if (ob > best || (ob == best && orr < br)) { best = ob; br = orr; }
+            const float obv = __shfl_xor_sync(0xffffffffu, bv, o);
+            if (ob > best || (ob == best && orr < br)) { best = ob; br = orr; bv = obv; }
         }
-        const float sgn = (__ldcg(Vg + size_t(br) * D + i) < 0.f) ? -1.f : 1.f;
-        for (int rr = l; rr < D; rr += 32)
-            basis_out[size_t(hd) * D * D + size_t(rr) * D + rk] = sgn * __ldcg(Vg + size_t(rr) * D + i);
+        const float sgn = (bv < 0.f) ? -1.f : 1.f;
+        float* dst = basis_out + size_t(hd) * D * D + rk;
+        dst[size_t(4 * l) * D] = sgn * v.x;
+        dst[size_t(4 * l + 1) * D] = sgn * v.y;
+        dst[size_t(4 * l + 2) * D] = sgn * v.z;
+        dst[size_t(4 * l + 3) * D] = sgn * v.w;
         if (l == 0) eig_out[size_t(hd) * D + rk] = li;
     }
-    if (rank == 0 && tid == 0) status[hd] = converged ? sweeps : -SPECTRA_ERR_NOT_CONVERGED;
+    if (rank == 0 && tid == 0)
+        status[hd] = failed ? -SPECTRA_ERR_TIMEOUT : converged ? sweeps : -SPECTRA_ERR_NOT_CONVERGED;
     cluster.sync();   // no CTA leaves while others may still write into its shared memory
-}
-
-template <int C>
-size_t jacobi128c_smem()
-{
-    constexpr int NW = 32 / C;
-    return sizeof(float) * (NW * 2 * kJ2 + 4 * kJ2 + 4 * kJ2) + sizeof(float4) * 128 +
-           sizeof(float) * (33 + 2 * C + kJ2) + sizeof(int) * C + 16;
 }
 
 template <int D>
@@ -977,14 +703,14 @@ spectra_status launch_jacobi(const spectra_plan* plan, const float* partials, in
 {
     const float inv_n = 1.0f / float(n_cal);
     if (plan->head_dim == 128) {
-        // one cluster of kJacCluster CTAs per head; the Gram partials of the
-        // head (at least D x D floats) double as the scratch of the final sort
-        constexpr int C = kJacCluster;
-        const size_t sm = jacobi128c_smem<C>();
-        cudaFuncSetAttribute(jacobi128c_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-        jacobi128c_kernel<C><<<plan->heads * C, 1024 / C, sm, s>>>(partials, nchunks, inv_n, max_sweeps,
-                                                                   plan->basis_mat, plan->eigvals, plan->status,
-                                                                   gram_out, const_cast<float*>(partials));
+        // one cluster of kJ1sCluster CTAs per head (one-sided Jacobi on the
+        // Cholesky factor); d = 64 keeps the one-block two-sided kernel
+        constexpr int C = kJ1sCluster;
+        const size_t sm = sizeof(float) * (2 * J1s<C>::PPC * kJ2 + kJ2 * (kJ2 + 1));
+        cudaFuncSetAttribute(jacobi1s_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        jacobi1s_kernel<C><<<plan->heads * C, 32 * J1s<C>::NW, sm, s>>>(partials, nchunks, inv_n, max_sweeps,
+                                                                      plan->basis_mat, plan->eigvals, plan->status,
+                                                                      gram_out);
     } else {
         const size_t sm = jacobi_smem<64>();
         cudaFuncSetAttribute(jacobi_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
