@@ -147,8 +147,9 @@ def run_ours(args, rank, world, local_rank):
     fork = [torch.cuda.Event() for _ in range(2)]
     phases = ["calibrate", "alloc", "encode", "decode", "attn"]
 
-    def step(i, ev=None):
+    def step(i, ev=None, att_out=None):
         c = i % NCOPY
+        att_o = att if att_out is None else att_out
         mark = (lambda k: ev[k].record(s)) if ev is not None else (lambda k: None)
         mark(0)
         # K and V calibrations are independent (one block per head each):
@@ -169,7 +170,7 @@ def run_ours(args, rank, world, local_rank):
         spx.spectra_decode(kp, kc[c], T_TOK, ko[c])
         spx.spectra_decode(vp, vc[c], T_TOK, vo[c])
         mark(4)
-        spx.spectra_attn_decode(kp, vp, q, kc[c], vc[c], T_TOK, 1.0, att, workspace=aws)
+        spx.spectra_attn_decode(kp, vp, q, kc[c], vc[c], T_TOK, 1.0, att_o, workspace=aws)
         mark(5)
 
     for i in range(args.warmup):
@@ -199,21 +200,41 @@ def run_ours(args, rank, world, local_rank):
     ph = {p: statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evs) for k, p in enumerate(phases)}
 
     # ---- end to end through the API with host buffers (pinned), per step:
-    # H2D of K and V, the whole path, D2H of the packed codes and the output
+    # H2D of K and V, the whole path, D2H of the packed codes and the output.
+    # Copies run on their own streams, one step ahead / behind the compute,
+    # over the rotating copies (a step's slot is reloaded only after the step
+    # that last used it, and overwritten only after its results left).
     hK = K[0].cpu().pin_memory()
     hV = V[0].cpu().pin_memory()
-    hkc = torch.empty_like(kc[0], device="cpu").pin_memory()
-    hvc = torch.empty_like(vc[0], device="cpu").pin_memory()
-    hatt = torch.empty_like(att, device="cpu").pin_memory()
+    hkc = [torch.empty_like(kc[0], device="cpu").pin_memory() for _ in range(NCOPY)]
+    hvc = [torch.empty_like(vc[0], device="cpu").pin_memory() for _ in range(NCOPY)]
+    hatt = [torch.empty_like(att, device="cpu").pin_memory() for _ in range(NCOPY)]
+    atts = [torch.empty_like(att) for _ in range(NCOPY)]
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(NCOPY)]
+    ev_done = [torch.cuda.Event() for _ in range(NCOPY)]
+    ev_out = [torch.cuda.Event() for _ in range(NCOPY)]
+    used = [False] * NCOPY
 
     def e2e_step(i):
         c = i % NCOPY
-        K[c].copy_(hK, non_blocking=True)
-        V[c].copy_(hV, non_blocking=True)
-        step(i)
-        hkc.copy_(kc[c], non_blocking=True)
-        hvc.copy_(vc[c], non_blocking=True)
-        hatt.copy_(att, non_blocking=True)
+        if used[c]:
+            cin.wait_event(ev_done[c])          # the slot's last step has read its inputs
+            s.wait_event(ev_out[c])             # ... and its results have left
+        with torch.cuda.stream(cin):
+            K[c].copy_(hK, non_blocking=True)
+            V[c].copy_(hV, non_blocking=True)
+            ev_in[c].record(cin)
+        s.wait_event(ev_in[c])
+        step(i, att_out=atts[c])
+        ev_done[c].record(s)
+        cout.wait_event(ev_done[c])
+        with torch.cuda.stream(cout):
+            hkc[c].copy_(kc[c], non_blocking=True)
+            hvc[c].copy_(vc[c], non_blocking=True)
+            hatt[c].copy_(atts[c], non_blocking=True)
+            ev_out[c].record(cout)
+        used[c] = True
 
     for i in range(2):
         e2e_step(i)
@@ -222,14 +243,17 @@ def run_ours(args, rank, world, local_rank):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(s)
+    cin.wait_event(e0)
     n_e2e = max(3, args.steps // 2)
     for i in range(n_e2e):
         e2e_step(i)
+    s.wait_stream(cout)
+    s.wait_stream(cin)
     e1.record(s)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
     h2d = hK.numel() * 2 + hV.numel() * 2
-    d2h = hkc.numel() + hvc.numel() + hatt.numel() * 4
+    d2h = hkc[0].numel() + hvc[0].numel() + hatt[0].numel() * 4
 
     # ---- roofline of the dominant HBM kernel (encode or decode, whichever
     # takes longer; each phase is two launches, K and V)
