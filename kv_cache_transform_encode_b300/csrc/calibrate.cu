@@ -384,22 +384,17 @@ __device__ __forceinline__ float2 pair_rotation(float4 p, float4 q, float tol, f
     }
     const float ab = a * b;
     rel = (ab > 0.f) ? fabsf(g) * rsqrtf(ab) : 0.f;
-    float s = 0.f, tau = 0.f;
-    if (ab > 0.f && g * g > tol * tol * ab) {
-        const float zeta = __fdividef(b - a, 2.f * g);
-        const float az = fabsf(zeta);
-        float t;
-        if (az > 1e18f) {
-            t = __fdividef(0.5f, az);
-        } else {
-            const float q1 = fmaf(az, az, 1.f);
-            t = __fdividef(1.f, fmaf(q1, rsqrtf(q1), az));   // 1 / (|zeta| + sqrt(zeta^2 + 1))
-        }
-        t = (zeta >= 0.f) ? t : -t;
-        const float c = rsqrtf(fmaf(t, t, 1.f));
-        s = t * c;
-        tau = __fdividef(s, 1.f + c);
-    }
+    // t = tan(theta) = 2 g sgn(d) / (|d| + sqrt(d^2 + 4 g^2)), d = b - a: the
+    // smaller root, without the 1 / (2 g) of the textbook form
+    const float dd = b - a, g2 = 2.f * g;
+    const float h2 = fmaf(dd, dd, g2 * g2);
+    const float hyp = h2 * rsqrtf(fmaxf(h2, 1e-37f));
+    float t = __fdividef(g2, fabsf(dd) + hyp);
+    t = (dd >= 0.f) ? t : -t;
+    const float c = rsqrtf(fmaf(t, t, 1.f));
+    const bool rot = ab > 0.f && g * g > tol * tol * ab;
+    const float s = rot ? t * c : 0.f;
+    const float tau = rot ? __fdividef(t * c, 1.f + c) : 0.f;
     return make_float2(s, tau);
 }
 
@@ -423,7 +418,6 @@ jacobi1s_kernel(const float* __restrict__ partials, int nchunks, float inv_n, in
 {
     namespace cg = cooperative_groups;
     constexpr int D = J1s<C>::D, PPC = J1s<C>::PPC, NP = J1s<C>::NP, NW = J1s<C>::NW;
-    constexpr uint32_t kColBytes = 2 * D * 4;          // one column of Gc and of V
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = int(cluster.block_rank());
     const int hd = blockIdx.x / C;
@@ -433,35 +427,48 @@ jacobi1s_kernel(const float* __restrict__ partials, int nchunks, float inv_n, in
     float (*Gc)[D] = reinterpret_cast<float (*)[D]>(jsm);               // [PPC][D] columns of X
     float (*Vc)[D] = reinterpret_cast<float (*)[D]>(jsm + PPC * D);     // [PPC][D] columns of V
     float* Am = jsm + 2 * PPC * D;                                      // [D][D + 1] Gram / Cholesky
-    __shared__ __align__(16) float rb[2][2][2][D];     // [side: from left, from right][parity][Gc, V]
-    __shared__ __align__(8) uint64_t rbar[2][2];       // [side][parity]
+    __shared__ __align__(16) float rb[2][2][2][D];     // [X, V][side: from left, from right][parity][D]
+    __shared__ __align__(8) uint64_t rbar[2][2][2];    // [X, V][side][parity]
     __shared__ float wred[NW];
     __shared__ float cred[2][C];                       // cluster exchange (two slots)
     __shared__ float lamall[D];
     __shared__ int cflag[2][C];
+    __shared__ float invd[16];                         // 1 / L[j][j] of the current Cholesky panel
 
     if (tid == 0) {
-        for (int sd = 0; sd < 2; ++sd)
-            for (int pp = 0; pp < 2; ++pp) mbar_init_local(&rbar[sd][pp], 1);
+        for (int xv = 0; xv < 2; ++xv)
+            for (int sd = 0; sd < 2; ++sd)
+                for (int pp = 0; pp < 2; ++pp) mbar_init_local(&rbar[xv][sd][pp], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    cluster.sync();    // every CTA of the cluster runs before any shared memory is touched remotely
     constexpr int AS = D + 1;                          // Cholesky row stride (conflict-free columns)
-    // the whole Gram matrix (every CTA), this CTA's columns to gram_out
+    // the Gram matrix: CTA r sums rows [r d/C, (r+1) d/C) of the chunk
+    // partials (fixed order) and writes them into every CTA's copy
     bool bad = false;
-    for (int e = tid; e < D * D; e += 32 * NW) {
-        const int r = e / D, c = e % D;
-        const float* src = partials + size_t(hd) * nchunks * D * D + e;
-        float sum = 0.f;
-        for (int ch = 0; ch < nchunks; ++ch) sum += src[size_t(ch) * D * D];
-        sum *= inv_n;
-        Am[r * AS + c] = sum;
-        if (gram_out && c / PPC == rank) gram_out[size_t(hd) * D * D + e] = sum;
-        bad |= !isfinite(sum);
+    {
+        const int rb0 = rank * PPC;
+        for (int e = tid; e < PPC * D; e += 32 * NW) {
+            const int r = rb0 + e / D, c = e % D;
+            const float* src = partials + size_t(hd) * nchunks * D * D + size_t(r) * D + c;
+            float sum = 0.f;
+            int ch = 0;
+            for (; ch + 4 <= nchunks; ch += 4) {
+                const float a0 = src[size_t(ch) * D * D], a1 = src[size_t(ch + 1) * D * D];
+                const float a2 = src[size_t(ch + 2) * D * D], a3 = src[size_t(ch + 3) * D * D];
+                sum += a0; sum += a1; sum += a2; sum += a3;
+            }
+            for (; ch < nchunks; ++ch) sum += src[size_t(ch) * D * D];
+            sum *= inv_n;
+            if (gram_out) gram_out[size_t(hd) * D * D + size_t(r) * D + c] = sum;
+            bad |= !isfinite(sum);
+            for (int k = 0; k < C; ++k) *cluster.map_shared_rank(&Am[r * AS + c], k) = sum;
+        }
     }
     {
         const int bl = __syncthreads_or(bad);
         if (tid < C) *cluster.map_shared_rank(&cflag[0][rank], tid) = bl;
-        cluster.sync();   // also: every CTA runs (and its barriers exist) before any remote access
+        cluster.sync();   // also: every CTA's rows of the Gram matrix have landed everywhere
         int any = 0;
         for (int k = 0; k < C; ++k) any |= cflag[0][k];
         if (any) {
@@ -483,37 +490,72 @@ jacobi1s_kernel(const float* __restrict__ partials, int nchunks, float inv_n, in
     for (int i = 0; i < D; ++i) dmax = fmaxf(dmax, Am[i * AS + i]);
     const float delta = 8e-7f * float(D) * dmax;
     for (int i = tid; i < D; i += 32 * NW) Am[i * AS + i] += delta;
-    // Right-looking, one barrier per step: step j subtracts A[i][j] A[k][j] /
-    // A[j][j] from the trailing lower triangle (rows by warp, columns by
-    // lane) while column j-1, which nobody reads any more, is scaled into L.
-    float prev_d = 1.f;
-    for (int j = 0; j <= D; ++j) {
+    // Blocked right-looking factorization, 16-column panels: warp 0 factors
+    // the diagonal block, every thread then solves rows of the panel below
+    // it (forward substitution), and 4x4 register tiles apply the rank-16
+    // update to the trailing lower triangle (the upper triangle of Am is
+    // scratch: it is never read).
+    constexpr int NB = 16;
+    for (int c0 = 0; c0 < D; c0 += NB) {
         __syncthreads();
-        if (j > 0) {                                   // column j-1 -> L
-            for (int i = j + tid; i < D; i += 32 * NW) Am[i * AS + j - 1] *= 1.f / prev_d;
-            if (tid == 0) Am[(j - 1) * AS + j - 1] = prev_d;
+        if (wl == 0) {
+            for (int j = c0; j < c0 + NB; ++j) {
+                const float piv = fmaxf(Am[j * AS + j], 1e-30f);
+                const float rs = rsqrtf(piv);
+                const int i = j + 1 + l;
+                const float lij = (i < c0 + NB) ? Am[i * AS + j] * rs : 0.f;
+                __syncwarp();
+                if (l == 0) {
+                    Am[j * AS + j] = piv * rs;
+                    invd[j - c0] = rs;
+                }
+                if (i < c0 + NB) Am[i * AS + j] = lij;
+                __syncwarp();
+                for (int e = l; e < NB * NB; e += 32) {
+                    const int ii = c0 + e / NB, kk = c0 + e % NB;
+                    if (kk > j && kk <= ii) Am[ii * AS + kk] = fmaf(-Am[ii * AS + j], Am[kk * AS + j], Am[ii * AS + kk]);
+                }
+                __syncwarp();
+            }
         }
-        if (j == D) break;
-        const float piv = fmaxf(Am[j * AS + j], 1e-30f);
-        const float inv = 1.f / piv;
-        // this lane's trailing columns k = j+1+l+32u and their multipliers
-        float ak[4];
+        __syncthreads();
+        for (int i = c0 + NB + tid; i < D; i += 32 * NW) {
+            float x[NB];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int k = j + 1 + l + 32 * u;
-            ak[u] = (k < D) ? Am[k * AS + j] * inv : 0.f;
+            for (int m = 0; m < NB; ++m) {
+                float a = Am[i * AS + c0 + m];
+#pragma unroll
+                for (int q = 0; q < m; ++q) a = fmaf(-x[q], Am[(c0 + m) * AS + c0 + q], a);
+                x[m] = a * invd[m];
+                Am[i * AS + c0 + m] = x[m];
+            }
         }
-        for (int i = j + 1 + wl; i < D; i += NW) {
-            const float lij = Am[i * AS + j];
-            float* row = Am + i * AS + j + 1 + l;
-            float v[4];
+        __syncthreads();
+        const int n4 = (D - c0 - NB) / 4;
+        for (int t = tid; t < n4 * n4; t += 32 * NW) {
+            const int ti = t / n4, tk = t % n4;
+            if (tk > ti) continue;
+            const int i0 = c0 + NB + 4 * ti, k0 = c0 + NB + 4 * tk;
+            float acc[4][4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = (j + 1 + l + 32 * u <= i) ? row[32 * u] : 0.f;
+            for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (j + 1 + l + 32 * u <= i) row[32 * u] = fmaf(-lij, ak[u], v[u]);
+                for (int q = 0; q < 4; ++q) acc[r][q] = Am[(i0 + r) * AS + k0 + q];
+#pragma unroll 4
+            for (int m = 0; m < NB; ++m) {
+                float li[4], lk[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) { li[r] = Am[(i0 + r) * AS + c0 + m]; lk[r] = Am[(k0 + r) * AS + c0 + m]; }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(-li[r], lk[q], acc[r][q]);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) Am[(i0 + r) * AS + k0 + q] = acc[r][q];
         }
-        prev_d = sqrtf(piv);
     }
     __syncthreads();
     // X = R: column c of R is row c of L (zero past the diagonal); V = I
@@ -530,85 +572,108 @@ jacobi1s_kernel(const float* __restrict__ partials, int nchunks, float inv_n, in
     float4* G4 = reinterpret_cast<float4*>(&Gc[0][0]);
     float4* V4 = reinterpret_cast<float4*>(&Vc[0][0]);
     constexpr int Q = D / 4;           // float4 per column
+    constexpr uint32_t kColBytesH = D * 4; // one column
+    // V trails X by one round: in round r a warp rotates the X pair of its
+    // round-r role and applies, in the same instructions stream, the rotation
+    // it found in round r-1 to the V pair of its round-(r-1) role (nothing
+    // reads V before the end, so its updates fill the latency of the X
+    // chain).  (ps, ptau): this warp's rotation of the previous round.
+    float ps = 0.f, ptau = 0.f;
+    auto send_col = [&](int xv, int side, uint32_t kp, uint32_t rk, float4 v) {
+        st_async_v4(cluster_map(&rb[xv][side][kp][4 * l], rk), v, cluster_map(&rbar[xv][side][kp], rk));
+    };
+    auto recv_col = [&](int xv, int side, uint32_t kp, uint32_t ph) -> float4 {
+        if (l == 0) mbar_expect(&rbar[xv][side][kp], kColBytesH);
+        if (!mbar_wait_phase(&rbar[xv][side][kp], ph)) failed = 1;
+        return *reinterpret_cast<const float4*>(&rb[xv][side][kp][4 * l]);
+    };
+    // even round (or the final V-only step when !dox): X pairs (2w, 2w+1);
+    // V of the previous (odd) round: pairs (2w+1, 2w+2), the boundaries
+    auto even_round = [&](bool dox, bool dov, uint32_t kx, uint32_t kv) -> float {
+        float rel = 0.f;
+        const uint32_t kxp = kx & 1, kvp = kv & 1, kvph = (kv >> 1) & 1;
+        float2 st = make_float2(0.f, 0.f);
+        if (wl < NP) {
+            const int P = 2 * wl;
+            if (dox) {
+                const float4 gp = G4[P * Q + l], gq = G4[(P + 1) * Q + l];
+                st = pair_rotation(gp, gq, kTol, rel);
+                const float4 gq2 = rot_q(gp, gq, st.x, st.y), gp2 = rot_p(gp, gq, st.x, st.y);
+                G4[P * Q + l] = gq2;
+                G4[(P + 1) * Q + l] = gp2;
+                if (P == 0 && rank > 0) send_col(0, 1, kxp, uint32_t(rank - 1), gq2);
+                if (P + 1 == PPC - 1 && rank < C - 1) send_col(0, 0, kxp, uint32_t(rank + 1), gp2);
+            }
+            if (dov) {
+                if (wl < NP - 1) {                       // previous odd local pair (2w+1, 2w+2)
+                    const int R = 2 * wl + 1;
+                    const float4 vp = V4[R * Q + l], vq = V4[(R + 1) * Q + l];
+                    V4[R * Q + l] = rot_q(vp, vq, ps, ptau);
+                    V4[(R + 1) * Q + l] = rot_p(vp, vq, ps, ptau);
+                } else if (rank < C - 1) {               // previous right boundary
+                    const float4 vp = V4[(PPC - 1) * Q + l];
+                    const float4 vq = recv_col(1, 1, kvp, kvph);
+                    V4[(PPC - 1) * Q + l] = rot_q(vp, vq, ps, ptau);
+                }
+            }
+        } else if (dov && rank > 0) {                    // previous left boundary
+            const float4 vq = V4[l];
+            const float4 vp = recv_col(1, 0, kvp, kvph);
+            V4[l] = rot_p(vp, vq, ps, ptau);
+        }
+        ps = st.x;
+        ptau = st.y;
+        return rel;
+    };
+    // odd round: X pairs (2w+1, 2w+2) and the boundaries; V of the previous
+    // (even) round: pairs (2w, 2w+1), whose edge columns go to the neighbours
+    auto odd_round = [&](uint32_t kx, uint32_t kv) -> float {
+        float rel = 0.f;
+        const uint32_t kxp = kx & 1, kxph = (kx >> 1) & 1, kvp = kv & 1;
+        float2 st = make_float2(0.f, 0.f);
+        if (wl < NP - 1) {
+            const int P = 2 * wl + 1;
+            const float4 gp = G4[P * Q + l], gq = G4[(P + 1) * Q + l];
+            st = pair_rotation(gp, gq, kTol, rel);
+            G4[P * Q + l] = rot_q(gp, gq, st.x, st.y);
+            G4[(P + 1) * Q + l] = rot_p(gp, gq, st.x, st.y);
+        } else if (wl == NP - 1) {
+            if (rank < C - 1) {
+                const float4 gp = G4[(PPC - 1) * Q + l];
+                const float4 gq = recv_col(0, 1, kxp, kxph);
+                st = pair_rotation(gp, gq, kTol, rel);
+                G4[(PPC - 1) * Q + l] = rot_q(gp, gq, st.x, st.y);
+            }
+        } else {
+            if (rank > 0) {
+                const float4 gq = G4[l];
+                const float4 gp = recv_col(0, 0, kxp, kxph);
+                st = pair_rotation(gp, gq, kTol, rel);
+                G4[l] = rot_p(gp, gq, st.x, st.y);
+            }
+        }
+        if (wl < NP) {                                   // previous even pair (2w, 2w+1)
+            const int P = 2 * wl;
+            const float4 vp = V4[P * Q + l], vq = V4[(P + 1) * Q + l];
+            const float4 vq2 = rot_q(vp, vq, ps, ptau), vp2 = rot_p(vp, vq, ps, ptau);
+            V4[P * Q + l] = vq2;
+            V4[(P + 1) * Q + l] = vp2;
+            if (P == 0 && rank > 0) send_col(1, 1, kvp, uint32_t(rank - 1), vq2);
+            if (P + 1 == PPC - 1 && rank < C - 1) send_col(1, 0, kvp, uint32_t(rank + 1), vp2);
+        }
+        ps = st.x;
+        ptau = st.y;
+        return rel;
+    };
     for (;;) {
         if (sweeps >= max_sweeps) break;
         ++sweeps;
         float mrel = 0.f;
         for (int r = 0; r < D; ++r, ++gr) {
-            const uint32_t k = gr >> 1, kp = k & 1, ph = (k >> 1) & 1;   // odd-round index, buffer, phase
-            if ((gr & 1) == 0) {
-                // even round: local pairs (2w, 2w+1)
-                if (wl < NP) {
-                    const int P = 2 * wl;
-                    const float4 gp = G4[P * Q + l], gq = G4[(P + 1) * Q + l];
-                    const float4 vp = V4[P * Q + l], vq = V4[(P + 1) * Q + l];
-                    float rel;
-                    const float2 st = pair_rotation(gp, gq, kTol, rel);
-                    mrel = fmaxf(mrel, rel);
-                    const float4 gq2 = rot_q(gp, gq, st.x, st.y), gp2 = rot_p(gp, gq, st.x, st.y);
-                    const float4 vq2 = rot_q(vp, vq, st.x, st.y), vp2 = rot_p(vp, vq, st.x, st.y);
-                    G4[P * Q + l] = gq2;          // swap: position P takes the rotated q
-                    V4[P * Q + l] = vq2;
-                    G4[(P + 1) * Q + l] = gp2;
-                    V4[(P + 1) * Q + l] = vp2;
-                    // the next odd round's straddling pairs need these columns
-                    if (P == 0 && rank > 0) {      // position 0 -> left neighbour, "from right"
-                        const uint32_t rk = uint32_t(rank - 1);
-                        const uint32_t bar = cluster_map(&rbar[1][kp], rk);
-                        st_async_v4(cluster_map(&rb[1][kp][0][4 * l], rk), gq2, bar);
-                        st_async_v4(cluster_map(&rb[1][kp][1][4 * l], rk), vq2, bar);
-                    }
-                    if (P + 1 == PPC - 1 && rank < C - 1) {   // last position -> right neighbour, "from left"
-                        const uint32_t rk = uint32_t(rank + 1);
-                        const uint32_t bar = cluster_map(&rbar[0][kp], rk);
-                        st_async_v4(cluster_map(&rb[0][kp][0][4 * l], rk), gp2, bar);
-                        st_async_v4(cluster_map(&rb[0][kp][1][4 * l], rk), vp2, bar);
-                    }
-                }
-            } else {
-                // odd round: local pairs (2w+1, 2w+2); warp NP-1 the pair
-                // (last, right neighbour's first), warp NP the pair (left
-                // neighbour's last, first)
-                if (wl < NP - 1) {
-                    const int P = 2 * wl + 1;
-                    const float4 gp = G4[P * Q + l], gq = G4[(P + 1) * Q + l];
-                    const float4 vp = V4[P * Q + l], vq = V4[(P + 1) * Q + l];
-                    float rel;
-                    const float2 st = pair_rotation(gp, gq, kTol, rel);
-                    mrel = fmaxf(mrel, rel);
-                    G4[P * Q + l] = rot_q(gp, gq, st.x, st.y);
-                    V4[P * Q + l] = rot_q(vp, vq, st.x, st.y);
-                    G4[(P + 1) * Q + l] = rot_p(gp, gq, st.x, st.y);
-                    V4[(P + 1) * Q + l] = rot_p(vp, vq, st.x, st.y);
-                } else if (wl == NP - 1) {
-                    if (rank < C - 1) {
-                        if (l == 0) mbar_expect(&rbar[1][kp], kColBytes);
-                        if (!mbar_wait_phase(&rbar[1][kp], ph)) failed = 1;
-                        const int P = PPC - 1;
-                        const float4 gp = G4[P * Q + l], vp = V4[P * Q + l];
-                        const float4 gq = *reinterpret_cast<const float4*>(&rb[1][kp][0][4 * l]);
-                        const float4 vq = *reinterpret_cast<const float4*>(&rb[1][kp][1][4 * l]);
-                        float rel;
-                        const float2 st = pair_rotation(gp, gq, kTol, rel);
-                        mrel = fmaxf(mrel, rel);
-                        G4[P * Q + l] = rot_q(gp, gq, st.x, st.y);
-                        V4[P * Q + l] = rot_q(vp, vq, st.x, st.y);
-                    }
-                } else {
-                    if (rank > 0) {
-                        if (l == 0) mbar_expect(&rbar[0][kp], kColBytes);
-                        if (!mbar_wait_phase(&rbar[0][kp], ph)) failed = 1;
-                        const float4 gq = G4[l], vq = V4[l];
-                        const float4 gp = *reinterpret_cast<const float4*>(&rb[0][kp][0][4 * l]);
-                        const float4 vp = *reinterpret_cast<const float4*>(&rb[0][kp][1][4 * l]);
-                        float rel;
-                        const float2 st = pair_rotation(gp, gq, kTol, rel);
-                        mrel = fmaxf(mrel, rel);
-                        G4[l] = rot_p(gp, gq, st.x, st.y);
-                        V4[l] = rot_p(vp, vq, st.x, st.y);
-                    }
-                }
-            }
+            // odd-round index of this round (X) and of the previous one (V)
+            const uint32_t kx = gr >> 1, kv = (gr - 1) >> 1;
+            if ((gr & 1) == 0) mrel = fmaxf(mrel, even_round(true, gr > 0, kx, kv));
+            else mrel = fmaxf(mrel, odd_round(kx, kv));
             __syncthreads();
         }
         // sweep done: cluster-wide max of the pair residuals and the failure flag
@@ -625,6 +690,10 @@ jacobi1s_kernel(const float* __restrict__ partials, int nchunks, float inv_n, in
         ++cuse;
         if (m == INFINITY) { failed = 1; break; }
         if (m <= kTol) { converged = 1; break; }
+    }
+    if (gr > 0) {   // the last (odd) round's rotations still owe their V update
+        even_round(false, true, gr >> 1, (gr - 1) >> 1);
+        __syncthreads();
     }
 
     // eigenvalues (Rayleigh quotients) to every CTA; ranks, sign fix, output
