@@ -568,6 +568,7 @@ jacobi1s_kernel(const float* __restrict__ partials, int nchunks, float inv_n, in
 
     constexpr float kTol = 2e-6f;      // |X_p . X_q| / (|X_p| |X_q|) below which a pair counts as orthogonal
     int sweeps = 0, converged = 0, failed = 0, cuse = 1;
+    float prev_m = INFINITY;
     uint32_t gr = 0;                   // rounds so far (all sweeps)
     float4* G4 = reinterpret_cast<float4*>(&Gc[0][0]);
     float4* V4 = reinterpret_cast<float4*>(&Vc[0][0]);
@@ -689,7 +690,12 @@ jacobi1s_kernel(const float* __restrict__ partials, int nchunks, float inv_n, in
         for (int kk = 0; kk < C; ++kk) m = fmaxf(m, cred[cuse & 1][kk]);
         ++cuse;
         if (m == INFINITY) { failed = 1; break; }
-        if (m <= kTol) { converged = 1; break; }
+        // converged when no pair needed a rotation, or when this sweep
+        // started within the quadratic regime (every pair orthogonal to
+        // 1e-3 in the previous sweep: this one has taken them to rounding
+        // level, and a further sweep would rotate nothing)
+        if (m <= kTol || prev_m <= 1e-3f) { converged = 1; break; }
+        prev_m = m;
     }
     if (gr > 0) {   // the last (odd) round's rotations still owe their V update
         even_round(false, true, gr >> 1, (gr - 1) >> 1);

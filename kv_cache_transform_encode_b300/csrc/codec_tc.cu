@@ -672,7 +672,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
     uint64_t* imgfull = bars + 16;
     uint64_t* imgempty = bars + 17;
     uint64_t* drain = bars + 18;
-    uint64_t* ebar = bars + 19;      // epilogue-warp rendezvous (bounded, unlike bar.sync)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 20);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
     volatile int* drain_flag = abort_flag + 1;
@@ -687,7 +686,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         mbar_init(imgfull, 1);
         mbar_init(imgempty, 1);
         mbar_init(drain, 1);
-        mbar_init(ebar, kDecEpiWarps);
         *abort_flag = 0;
         *drain_flag = 0;
         fence_mbar_init();
@@ -731,7 +729,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                     ++j;
                 }
                 const int s = cs_i;
-                if (k >= P.cstages && !mbar_wait(&cempty[s], cs_ph ^ 1u, abort_flag, kWaitNs)) break;
+                if (k >= P.cstages && !mbar_spin(&cempty[s], cs_ph ^ 1u, abort_flag, kWaitNs)) break;
                 if (++cs_i == P.cstages) { cs_i = 0; cs_ph ^= 1u; }
                 const int64_t t0 = int64_t(tile) * TILE;
                 const int64_t ngroups = min(int64_t(4), (P.T - t0 + 31) / 32);
@@ -769,14 +767,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 const int h = it.h;
                 S.next(it);
                 if (h != cur_h) {
-                    if (!mbar_wait(imgfull, j & 1, abort_flag, kWaitNs)) break;
+                    if (!mbar_spin(imgfull, j & 1, abort_flag, kWaitNs)) break;
                     cur_h = h;
                     ++j;
                 }
                 const int s = as_i, a = k & 1;
-                if (!mbar_wait(&afull[s], as_ph, abort_flag, kWaitNs)) break;
+                if (!mbar_spin(&afull[s], as_ph, abort_flag, kWaitNs)) break;
                 if (++as_i == P.astages) { as_i = 0; as_ph ^= 1u; }
-                if (k >= 2 && !mbar_wait(&accempty[a], ((k >> 1) - 1) & 1, abort_flag, kWaitNs)) break;
+                if (k >= 2 && !mbar_spin(&accempty[a], ((k >> 1) - 1) & 1, abort_flag, kWaitNs)) break;
                 tc_fence_after();
                 const uint32_t aa = smem_u32(as + s * P.na * OPND);
                 const uint32_t ia = smem_u32(img);
@@ -894,17 +892,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         const int q = warp & 3;
         const bool leader = (warp == 2 + kDecUnpackWarps && lane == 0);
         float* bsh = reinterpret_cast<float*>(smem + L.bias) + (warp - 2 - kDecUnpackWarps) * D;
-        int k = 0, euse = 0, cur_h = -1;
-        bool ok = true, code_mode = false;
-        auto rendezvous = [&]() -> bool {   // all four epilogue warps
+        int k = 0, cur_h = -1;
+        bool code_mode = false;
+        // all four epilogue warps (named barrier 1); the OR of the abort flag
+        // makes every warp leave at the same point
+        auto rendezvous = [&]() -> bool {
             __syncwarp();
-            if (lane == 0) mbar_arrive(ebar);
-            const bool r = mbar_wait(ebar, euse & 1, abort_flag, kWaitNs);
-            ++euse;
-            return r;
+            return !named_barrier_or(1, 32 * kDecEpiWarps, *abort_flag != 0);
         };
         Item it = S.first();
-        for (; k < S.n && ok; ++k, S.next(it)) {
+        for (; k < S.n; ++k, S.next(it)) {
             const int h = it.h, tile = it.tile;
             if (h != cur_h) {       // code mode: per-output offsets of this head
                 cur_h = h;
@@ -914,8 +911,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 __syncwarp();
             }
             const int a = k & 1;
-            if (!mbar_wait(&accfull[a], (k >> 1) & 1, abort_flag, kWaitNs)) break;
-            tc_fence_after();
+            if (leader) mbar_spin(&accfull[a], (k >> 1) & 1, abort_flag, kWaitNs);
+            bool ok = true;
             const int64_t t = int64_t(tile) * TILE + q * 32 + lane;
             float scale = 1.f;
             if (rwht) scale = (t < P.T) ? P.norms[int64_t(h) * P.nstride + t] * (1.0f / float(D)) : 0.f;
@@ -926,7 +923,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 // staging slot(s) must be free: the stores issued from them earlier have read them
                 const int slot = P.out_f32 ? rd : (k & 1);
                 if (leader) tma_store_wait_read<1>();
+                tc_fence_before();
                 if (!(ok = rendezvous())) break;
+                tc_fence_after();
                 uint8_t* sb = stg + slot * OPND;
                 const uint32_t sba = smem_u32(sb);
                 if (!P.out_f32) {
@@ -935,6 +934,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                         uint32_t r[32];
                         tmem_ld32(tm + 32 * j, r);
                         tmem_ld_wait();
+                        if (j == 3) {   // accumulator read: the MMA may reuse it
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&accempty[a]);
+                        }
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4) {
                             uint32_t pk[4];
@@ -966,7 +970,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                         }
                     }
                 }
-                if (rd == nrounds - 1) {
+                if (P.out_f32 && rd == nrounds - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&accempty[a]);
@@ -984,6 +988,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                     tma_store_commit();
                 }
             }
+            if (!ok) break;
         }
         if (leader) tma_store_wait_all<0>();
     }
