@@ -207,9 +207,11 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
     }
 }
 
-// One block per (batch, kv head): merge the context splits of its G query
-// heads, then out[b, j] = B_V latent_j with B_V staged once in shared memory
-// (rows padded to D + 1 floats: conflict-free row reads).
+// One block per (batch, query head): merge its context splits, then
+// out[b, hq] = B_V latent with B_V staged in shared memory (rows padded to
+// D + 1 floats: conflict-free row reads).  The split weights exp(m_s - M)
+// are computed once; the channel sums read the splits with independent
+// loads in flight (the partials live in L2).
 // code_domain: the partials hold sum_t p_t code_c(t) (tensor-core path,
 // uniform quantizer); the merged value is dequantized as
 // Delta_c (code_mean + (1 - 2^b) / 2) before the rotation.
@@ -218,67 +220,90 @@ attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsp
                     float* __restrict__ out)
 {
     const int D = vp.d, Hkv = vp.heads, G = Hq / Hkv;
-    const int bh = blockIdx.x, h = bh % Hkv, b = bh / Hkv;
+    const int bq = blockIdx.x, hq = bq % Hq, b = bq / Hq, h = hq / G;
     const int LD = D + 1;
     extern __shared__ float sm[];
     float* Bs = sm;                     // [D][LD]
-    float* os = Bs + D * LD;            // [G][D]
-    float* stat = os + G * D;           // [G][2]: M, L
+    float* os = Bs + D * LD;            // [D]
+    float* red = os + D;                // [4][D] partial sums
+    float* stat = red + 4 * D;          // [1]: L
+    float* sc = stat + 4;               // [nsplit] split weights
     const bool eig = vp.basis == SPECTRA_BASIS_EIGEN;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (eig) {
         const float4* src = reinterpret_cast<const float4*>(vp.basis_mat + size_t(h) * D * D);
-        for (int e = threadIdx.x; e < D * D / 4; e += blockDim.x) {
+        for (int e = tid; e < D * D / 4; e += blockDim.x) {
             const float4 v = src[e];
             const int i = (4 * e) / D, c = (4 * e) % D;
             float* d = Bs + i * LD + c;
             d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
         }
     }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    for (int j = warp; j < G; j += nw) {
-        const float* pp = part + (int64_t(b) * Hq + h * G + j) * nsplit * (D + 2);
+    const float* pp = part + (int64_t(b) * Hq + hq) * nsplit * (D + 2);
+    if (warp == 0) {
         float M = -INFINITY;
         for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, pp[int64_t(s) * (D + 2)]);
         for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float L = 0.f;
         for (int s = lane; s < nsplit; s += 32) {
             const float m = pp[int64_t(s) * (D + 2)];
-            if (m != -INFINITY) L += pp[int64_t(s) * (D + 2) + 1] * __expf(m - M);
+            const float w = (m != -INFINITY) ? __expf(m - M) : 0.f;
+            sc[s] = w;
+            L = fmaf(pp[int64_t(s) * (D + 2) + 1], w, L);
         }
         for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (lane == 0) { stat[2 * j] = M; stat[2 * j + 1] = L; }
+        if (lane == 0) stat[0] = L;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-        const int j = e / D, c = e % D;
-        const float* pp = part + (int64_t(b) * Hq + h * G + j) * nsplit * (D + 2);
-        const float M = stat[2 * j], L = stat[2 * j + 1];
-        float a = 0.f;
-        for (int s = 0; s < nsplit; ++s) {
-            const float m = pp[int64_t(s) * (D + 2)];
-            if (m != -INFINITY) a += pp[int64_t(s) * (D + 2) + 2 + c] * __expf(m - M);
+    const int nh = int(blockDim.x) / D;          // split phases (2 for d = 128, 4 for d = 64)
+    {
+        const int c = tid % D, ph = tid / D;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int s = ph;
+        for (; s + 3 * nh < nsplit; s += 4 * nh) {
+            const float v0 = pp[int64_t(s) * (D + 2) + 2 + c], v1 = pp[int64_t(s + nh) * (D + 2) + 2 + c];
+            const float v2 = pp[int64_t(s + 2 * nh) * (D + 2) + 2 + c], v3 = pp[int64_t(s + 3 * nh) * (D + 2) + 2 + c];
+            a0 = fmaf(v0, sc[s], a0);
+            a1 = fmaf(v1, sc[s + nh], a1);
+            a2 = fmaf(v2, sc[s + 2 * nh], a2);
+            a3 = fmaf(v3, sc[s + 3 * nh], a3);
         }
+        for (; s < nsplit; s += nh) a0 = fmaf(pp[int64_t(s) * (D + 2) + 2 + c], sc[s], a0);
+        red[ph * D + c] = (a0 + a1) + (a2 + a3);
+    }
+    __syncthreads();
+    if (tid < D) {
+        const int c = tid;
+        float a = 0.f;
+        for (int k = 0; k < nh; ++k) a += red[k * D + c];
+        const float L = stat[0];
         float y = (L > 0.f) ? a / L : 0.f;
         if (code_domain) {
             const int bc = vp.bits[size_t(h) * D + c];
             y = (bc > 0) ? vp.rscale[size_t(h) * D + c] * (y + 0.5f * (1.f - float(1 << bc))) : 0.f;
         }
-        os[j * D + c] = y;
+        os[c] = y;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-        const int j = e / D, i = e % D;
+    {
+        const int i = tid % D, ph = tid / D, cl = D / nh;   // output i, channel slice ph
         float a = 0.f;
         if (eig) {
-            for (int c = 0; c < D; ++c) a = fmaf(Bs[i * LD + c], os[j * D + c], a);
+            for (int c = ph * cl; c < (ph + 1) * cl; ++c) a = fmaf(Bs[i * LD + c], os[c], a);
         } else {
-            for (int c = 0; c < D; ++c) a = fmaf(basis_entry(vp, h, i, c, D), os[j * D + c], a);
+            for (int c = ph * cl; c < (ph + 1) * cl; ++c) a = fmaf(basis_entry(vp, h, i, c, D), os[c], a);
         }
-        out[(int64_t(b) * Hq + h * G + j) * D + i] = a;
+        red[ph * D + i] = a;
+    }
+    __syncthreads();
+    if (tid < D) {
+        float a = 0.f;
+        for (int k = 0; k < nh; ++k) a += red[k * D + tid];
+        out[(int64_t(b) * Hq + hq) * D + tid] = a;
     }
 }
 
-size_t combine_smem(int D, int G) { return sizeof(float) * (size_t(D) * (D + 1) + size_t(G) * D + 2 * G); }
+size_t combine_smem(int D, int nsplit) { return sizeof(float) * (size_t(D) * (D + 1) + 5 * size_t(D) + 4 + nsplit); }
 
 template <int D>
 size_t split_smem()
@@ -315,9 +340,9 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
 void launch_combine(const PlanView& vp, const float* part, int B, int Hq, int nsplit, int code_domain, float* out,
                     cudaStream_t s)
 {
-    const size_t sm = combine_smem(vp.d, Hq / vp.heads);
+    const size_t sm = combine_smem(vp.d, nsplit);
     cudaFuncSetAttribute(attn_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-    attn_combine_kernel<<<B * vp.heads, 256, sm, s>>>(vp, part, Hq, nsplit, code_domain, out);
+    attn_combine_kernel<<<B * Hq, 256, sm, s>>>(vp, part, Hq, nsplit, code_domain, out);
 }
 
 // [qt (B Hq d f32) | split partials | tensor-core operands (sized for Hkv <= Hq)]

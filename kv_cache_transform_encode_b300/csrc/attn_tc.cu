@@ -113,67 +113,54 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
           "f"(c[3]));
 }
 
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
-{
-    const __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 // ------------------------------------------------------------------ prep
 // Per (batch, kv head): qt_j = scale * B_K^T q_j, W_jc = qt_jc Delta_c as fp16
 // hi/lo rows ([8][D]: rows 0..3 hi, 4..7 lo; heads >= G zero), the sums of
 // each row over every 16-channel chunk (the 1024 offsets removed per MMA
 // step), and K0_j.
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(kGmax * D)
 attn_tc_prep_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, int G, float scale,
                     __half* __restrict__ wimg, float* __restrict__ bias, float* __restrict__ wsum16)
 {
     const int bh = blockIdx.x, Hkv = kp.heads, h = bh % Hkv, b = bh / Hkv;
-    const int c = threadIdx.x;
+    const int tid = threadIdx.x, c = tid % D, j = tid / D;   // channel, query head of the group
     extern __shared__ float Bs[];                 // [D][D] basis of head h (staged: coalesced 16-B loads)
     __shared__ float qs[kGmax][D];
     __shared__ float red[kGmax][4];
     {
         const float4* src = reinterpret_cast<const float4*>(kp.basis_mat + size_t(h) * D * D);
         float4* dst = reinterpret_cast<float4*>(Bs);
-        for (int e = c; e < D * D / 4; e += D) dst[e] = src[e];
+        for (int e = tid; e < D * D / 4; e += kGmax * D) dst[e] = src[e];
     }
-    for (int e = c; e < kGmax * D; e += D)
-        qs[e / D][e % D] = (e / D < G) ? load_elem(q, q_dt, (int64_t(b) * Hq + h * G + e / D) * D + e % D) : 0.f;
+    qs[j][c] = (j < G) ? load_elem(q, q_dt, (int64_t(b) * Hq + h * G + j) * D + c) : 0.f;
     __syncthreads();
-    float qt[kGmax] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = 0; i < D; ++i) {
-        const float bic = Bs[i * D + c];
-#pragma unroll
-        for (int j = 0; j < kGmax; ++j) qt[j] = fmaf(bic, qs[j][i], qt[j]);
-    }
+    float qt = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < D; ++i) qt = fmaf(Bs[i * D + c], qs[j][i], qt);
     const int bits = kp.bits[size_t(h) * D + c];
     const float delta = kp.rscale[size_t(h) * D + c];
     __half* wr = wimg + size_t(bh) * 8 * D;
     float* wsr = wsum16 + size_t(bh) * 8 * 8;           // [kb][n]
-#pragma unroll
-    for (int j = 0; j < kGmax; ++j) {
-        const float qj = qt[j] * scale;
-        const float w = (bits > 0 && j < G) ? qj * delta : 0.f;
-        const __half hi = __float2half_rn(w);
-        const __half lo = __float2half_rn(w - __half2float(hi));
-        wr[j * D + c] = hi;
-        wr[(kGmax + j) * D + c] = lo;
-        float sh = __half2float(hi), sl = __half2float(lo);
-        for (int o = 8; o; o >>= 1) {            // 16-channel chunk sums
-            sh += __shfl_xor_sync(0xffffffffu, sh, o);
-            sl += __shfl_xor_sync(0xffffffffu, sl, o);
-        }
-        if ((c & 15) == 0) {
-            wsr[(c >> 4) * 8 + j] = sh;
-            wsr[(c >> 4) * 8 + kGmax + j] = sl;
-        }
-        float k0 = (bits > 0 && j < G) ? qj * 0.5f * delta * (1.f - float(1 << bits)) : 0.f;
-        for (int o = 16; o; o >>= 1) k0 += __shfl_xor_sync(0xffffffffu, k0, o);
-        if ((c & 31) == 0) red[j][c >> 5] = k0;
+    const float qj = qt * scale;
+    const float w = (bits > 0 && j < G) ? qj * delta : 0.f;
+    const __half hi = __float2half_rn(w);
+    const __half lo = __float2half_rn(w - __half2float(hi));
+    wr[j * D + c] = hi;
+    wr[(kGmax + j) * D + c] = lo;
+    float sh = __half2float(hi), sl = __half2float(lo);
+    for (int o = 8; o; o >>= 1) {                // 16-channel chunk sums
+        sh += __shfl_xor_sync(0xffffffffu, sh, o);
+        sl += __shfl_xor_sync(0xffffffffu, sl, o);
     }
+    if ((c & 15) == 0) {
+        wsr[(c >> 4) * 8 + j] = sh;
+        wsr[(c >> 4) * 8 + kGmax + j] = sl;
+    }
+    float k0 = (bits > 0 && j < G) ? qj * 0.5f * delta * (1.f - float(1 << bits)) : 0.f;
+    for (int o = 16; o; o >>= 1) k0 += __shfl_xor_sync(0xffffffffu, k0, o);
+    if ((c & 31) == 0) red[j][c >> 5] = k0;
     __syncthreads();
-    if (c < kGmax) bias[size_t(bh) * kGmax + c] = red[c][0] + red[c][1] + red[c][2] + red[c][3];
+    if (tid < kGmax) bias[size_t(bh) * kGmax + tid] = red[tid][0] + red[tid][1] + red[tid][2] + red[tid][3];
 }
 
 // ------------------------------------------------------------------ split
@@ -469,7 +456,8 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
     const size_t sm = tc_split_smem(P.kbytes, P.vbytes);
     if (sm > 227 * 1024) return SPECTRA_OK;
     cudaFuncSetAttribute(attn_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(float) * D * D));
-    attn_tc_prep_kernel<<<B * Hkv, D, sizeof(float) * D * D, s>>>(P.kp, q, q_dt, Hq, G, scale, wimg, bias, wsum16);
+    attn_tc_prep_kernel<<<B * Hkv, kGmax * D, sizeof(float) * D * D, s>>>(P.kp, q, q_dt, Hq, G, scale, wimg, bias,
+                                                                         wsum16);
     cudaFuncSetAttribute(attn_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
     dim3 grid(nsplit, Hkv, B);
     attn_tc_split_kernel<<<grid, kThreads, sm, s>>>(P);
