@@ -212,9 +212,9 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
 // D + 1 floats: conflict-free row reads).  The split weights exp(m_s - M)
 // are computed once; the channel sums read the splits with independent
 // loads in flight (the partials live in L2).
-// code_domain: the partials hold sum_t p_t code_c(t) (tensor-core path,
-// uniform quantizer); the merged value is dequantized as
-// Delta_c (code_mean + (1 - 2^b) / 2) before the rotation.
+// code_domain: the partials hold sum_t p_t z_c(t) with z = code - 2^(b-1)
+// (tensor-core path, uniform quantizer); the merged value is dequantized as
+// Delta_c (z_mean + 1/2) before the rotation.
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsplit, int code_domain,
                     float* __restrict__ out)
@@ -280,7 +280,7 @@ attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsp
         float y = (L > 0.f) ? a / L : 0.f;
         if (code_domain) {
             const int bc = vp.bits[size_t(h) * D + c];
-            y = (bc > 0) ? vp.rscale[size_t(h) * D + c] * (y + 0.5f * (1.f - float(1 << bc))) : 0.f;
+            y = (bc > 0) ? vp.rscale[size_t(h) * D + c] * (y + 0.5f) : 0.f;
         }
         os[c] = y;
     }

@@ -5,17 +5,17 @@
 // "Sintesi Tecnica: SPECTRA", "Significato e Rivendicazioni": attention
 // computed directly in the latent space.  With the uniform quantizer a
 // latent coordinate is yhat_c = (Delta_c / 2)(2 code_c + 1 - 2^b_c), affine
-// in the code, so
-//   s_j(t) = sum_c qt_jc yhat_c(t) = sum_c W_jc code_c(t) + K0_j,
-//   W_jc = qt_jc Delta_c,   K0_j = sum_c qt_jc (Delta_c / 2)(1 - 2^b_c),
-//   sum_t p_j(t) yhat_c(t) = Delta_c (sum_t p_j(t) code_c(t) + (1 - 2^b_c) l_j / 2),
-// and both contractions run on integer codes.  A code enters the tensor
-// core as the fp16 number 1024 + code (exact: the code lands in the low
-// mantissa bits, one byte-permute per two codes); after every 16-wide MMA
-// step the 1024 offsets are taken out again with the sums of the other
-// operand, so rounding stays relative to a 16-term partial sum.  W and P enter as fp16
-// hi + lo pairs (22 significand bits), so the products carry fp32-grade
-// accuracy.
+// in the code: with z = code - 2^(b-1) (an exact small integer),
+// yhat_c = Delta_c (z_c + 1/2), so
+//   s_j(t) = sum_c qt_jc yhat_c(t) = sum_c W_jc z_c(t) + K0_j,
+//   W_jc = qt_jc Delta_c,   K0_j = (1/2) sum_c W_jc,
+//   sum_t p_j(t) yhat_c(t) = Delta_c (sum_t p_j(t) z_c(t) + l_j / 2),
+// and both contractions run on the small integers z.  A code enters the
+// tensor core as the fp16 number z: the byte-permute trick gives 1024 +
+// code exactly, one packed subtraction of 1024 + 2^(b-1) leaves z, so the
+// fp32 accumulators only ever hold sums of small terms.  W and P enter as
+// fp16 hi + lo pairs (22 significand bits), so the products carry
+// fp32-grade accuracy.
 //
 // One CTA per (context split, kv head, batch).  Per 128-token tile:
 //  1. the tile's K and V code words arrive in shared memory (cp.async,
@@ -28,7 +28,7 @@
 //  4. online softmax per head (warps 0..3);
 //  5. P V: mma.sync, A = L_V (channels x tokens), B = [P_hi; P_lo], one
 //     16-channel slice per warp, accumulated over the split in registers.
-// The split's (m, l, sum_t p code) go to the workspace; the combine kernel
+// The split's (m, l, sum_t p z) go to the workspace; the combine kernel
 // of attn.cu merges splits, dequantizes and rotates by the V basis.
 #include "spectra_internal.cuh"
 
@@ -44,7 +44,6 @@ constexpr int TT = 128;                  // tokens per tile
 constexpr int LROW = TT * 2 + 16;        // bytes per L row (padded: conflict-free ldmatrix)
 constexpr int kThreads = 256;
 constexpr int kGmax = 4;                 // query heads per kv head
-constexpr float kOff = 1024.f;           // fp16 1024 + code
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
 {
@@ -120,7 +119,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 // step), and K0_j.
 __global__ void __launch_bounds__(kGmax * D)
 attn_tc_prep_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, int G, float scale,
-                    __half* __restrict__ wimg, float* __restrict__ bias, float* __restrict__ wsum16)
+                    __half* __restrict__ wimg, float* __restrict__ bias)
 {
     const int bh = blockIdx.x, Hkv = kp.heads, h = bh % Hkv, b = bh / Hkv;
     const int tid = threadIdx.x, c = tid % D, j = tid / D;   // channel, query head of the group
@@ -140,23 +139,14 @@ attn_tc_prep_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, i
     const int bits = kp.bits[size_t(h) * D + c];
     const float delta = kp.rscale[size_t(h) * D + c];
     __half* wr = wimg + size_t(bh) * 8 * D;
-    float* wsr = wsum16 + size_t(bh) * 8 * 8;           // [kb][n]
     const float qj = qt * scale;
     const float w = (bits > 0 && j < G) ? qj * delta : 0.f;
     const __half hi = __float2half_rn(w);
     const __half lo = __float2half_rn(w - __half2float(hi));
     wr[j * D + c] = hi;
     wr[(kGmax + j) * D + c] = lo;
-    float sh = __half2float(hi), sl = __half2float(lo);
-    for (int o = 8; o; o >>= 1) {                // 16-channel chunk sums
-        sh += __shfl_xor_sync(0xffffffffu, sh, o);
-        sl += __shfl_xor_sync(0xffffffffu, sl, o);
-    }
-    if ((c & 15) == 0) {
-        wsr[(c >> 4) * 8 + j] = sh;
-        wsr[(c >> 4) * 8 + kGmax + j] = sl;
-    }
-    float k0 = (bits > 0 && j < G) ? qj * 0.5f * delta * (1.f - float(1 << bits)) : 0.f;
+    // yhat = Delta (z + 1/2): the 1/2 terms of the score, summed over channels
+    float k0 = 0.5f * w;
     for (int o = 16; o; o >>= 1) k0 += __shfl_xor_sync(0xffffffffu, k0, o);
     if ((c & 31) == 0) red[j][c >> 5] = k0;
     __syncthreads();
@@ -173,7 +163,6 @@ struct AttnTcParams {
     int64_t sstride;
     const __half* wimg;
     const float* bias;
-    const float* wsum16;
     float* part;
     uint32_t kbytes, vbytes;   // code-word bytes of one tile (16 R)
 };
@@ -197,7 +186,6 @@ attn_tc_split_kernel(AttnTcParams P)
     float* st_m = reinterpret_cast<float*>(Pm + 8 * (TT + 8));   // [kGmax]
     float* st_l = st_m + kGmax;
     float* st_a = st_l + kGmax;                                  // alpha of this tile
-    float* ps16 = st_a + kGmax;                                  // [8 chunks][8 rows] p sums
 
     const int64_t t_begin = int64_t(split) * P.split_len;
     const int64_t t_end = min(P.ctx, t_begin + P.split_len);
@@ -259,15 +247,37 @@ attn_tc_split_kernel(AttnTcParams P)
             const uint32_t* words = reinterpret_cast<const uint32_t*>(cw + buf * cwb + (side ? P.kbytes : 0));
             uint8_t* L = side ? Lv : Lk;
             uint8_t* row = L + uc * LROW;
+            // z = code - 2^(b-1) (0 for dropped channels): (1024 + code) - (1024 + 2^(b-1)), exact in fp16
+            const __half2 cz = __float2half2_rn(1024.f + (ub > 0 ? float(1 << (ub - 1)) : 0.f));
 #pragma unroll 1
             for (int g = 0; g < 4; ++g) {
                 uint32_t X[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                if (t0 + 32 * g < t_end && uR > 0) planes_to_codes(words + g * uR, uo, ub, ubmax, X);
+                if (t0 + 32 * g < t_end && uR > 0) {
+                    if (ubmax <= 2) {
+                        // widths <= 2 (the warp's widest channel): spread each
+                        // 4-token nibble of the two planes into bytes with one
+                        // multiply (bit i -> bit 8i) instead of the transposes
+                        const uint32_t* wg = words + g * uR + uo;
+                        const uint32_t w0 = ub > 0 ? wg[0] : 0u, w1 = ub > 1 ? wg[1] : 0u;
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) {
+                            const uint32_t s0 = (((w0 >> (4 * m)) & 0xFu) * 0x00204081u) & 0x01010101u;
+                            const uint32_t s1 = (((w1 >> (4 * m)) & 0xFu) * 0x00204081u) & 0x01010101u;
+                            X[m] = s0 | (s1 << 1);
+                        }
+                    } else {
+                        planes_to_codes(words + g * uR, uo, ub, ubmax, X);
+                    }
+                }
                 uint32_t v[16];
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
-                    v[2 * m] = __byte_perm(X[m], 0x6464u, 0x5140);       // tokens 4m, 4m+1 -> fp16 1024 + code
-                    v[2 * m + 1] = __byte_perm(X[m], 0x6464u, 0x5342);   // tokens 4m+2, 4m+3
+                    const uint32_t p0 = __byte_perm(X[m], 0x6464u, 0x5140);   // tokens 4m, 4m+1 -> fp16 1024 + code
+                    const uint32_t p1 = __byte_perm(X[m], 0x6464u, 0x5342);   // tokens 4m+2, 4m+3
+                    const __half2 z0 = __hsub2(*reinterpret_cast<const __half2*>(&p0), cz);
+                    const __half2 z1 = __hsub2(*reinterpret_cast<const __half2*>(&p1), cz);
+                    v[2 * m] = *reinterpret_cast<const uint32_t*>(&z0);
+                    v[2 * m + 1] = *reinterpret_cast<const uint32_t*>(&z1);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(row + g * 64);
 #pragma unroll
@@ -280,16 +290,12 @@ attn_tc_split_kernel(AttnTcParams P)
         {
             float sacc[4] = {0.f, 0.f, 0.f, 0.f};
             const int mi = lane >> 3, ri = lane & 7;
-            const float* wsr = P.wsum16 + size_t(bh) * 64;
 #pragma unroll
             for (int kb = 0; kb < 8; ++kb) {
                 uint32_t a[4];
                 const int k = kb * 16 + (mi >> 1) * 8 + ri, m = warp * 16 + (mi & 1) * 8;
                 ldsm_x4_t(smem_addr(Lk + k * LROW + m * 2), a);
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                mma16816(d, a, wf[kb][0], wf[kb][1], d);
-                const float o0 = kOff * wsr[kb * 8 + 2 * tig], o1 = kOff * wsr[kb * 8 + 2 * tig + 1];
-                sacc[0] += d[0] - o0; sacc[1] += d[1] - o1; sacc[2] += d[2] - o0; sacc[3] += d[3] - o1;
+                mma16816(sacc, a, wf[kb][0], wf[kb][1], sacc);
             }
             // lanes tig 0/1 hold hi heads 2 tig, 2 tig + 1; lanes tig 2/3 the lo parts
 #pragma unroll
@@ -333,17 +339,7 @@ attn_tc_split_kernel(AttnTcParams P)
                 const int t = lane + 32 * i;
                 Pm[j * (TT + 8) + t] = ph;
                 Pm[(kGmax + j) * (TT + 8) + t] = pl;
-                float sh = __half2float(ph), sl = __half2float(pl);
-                ptot += sh + sl;
-                // per 16-token chunk sums of the hi and lo rows (chunk = t / 16)
-                for (int o = 8; o; o >>= 1) {
-                    sh += __shfl_xor_sync(0xffffffffu, sh, o);
-                    sl += __shfl_xor_sync(0xffffffffu, sl, o);
-                }
-                if ((lane & 15) == 0) {
-                    ps16[(2 * i + (lane >> 4)) * 8 + j] = sh;
-                    ps16[(2 * i + (lane >> 4)) * 8 + kGmax + j] = sl;
-                }
+                ptot += __half2float(ph) + __half2float(pl);
             }
             for (int o = 16; o; o >>= 1) ptot += __shfl_xor_sync(0xffffffffu, ptot, o);
             if (lane == 0) {
@@ -359,7 +355,6 @@ attn_tc_split_kernel(AttnTcParams P)
                     Pm[j * (TT + 8) + t] = __float2half_rn(0.f);
                     Pm[(kGmax + j) * (TT + 8) + t] = __float2half_rn(0.f);
                 }
-                if (lane < 8) { ps16[lane * 8 + j] = 0.f; ps16[lane * 8 + kGmax + j] = 0.f; }
                 if (lane == 0) st_a[j] = 0.f;
             }
         }
@@ -378,10 +373,7 @@ attn_tc_split_kernel(AttnTcParams P)
                 ldsm_x4(smem_addr(Lv + m * LROW + k * 2), a);
                 const uint32_t b0 = *reinterpret_cast<const uint32_t*>(Pm + g8 * (TT + 8) + kb * 16 + 2 * tig);
                 const uint32_t b1 = *reinterpret_cast<const uint32_t*>(Pm + g8 * (TT + 8) + kb * 16 + 8 + 2 * tig);
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                mma16816(d, a, b0, b1, d);
-                const float s0 = kOff * ps16[kb * 8 + 2 * tig], s1 = kOff * ps16[kb * 8 + 2 * tig + 1];
-                oacc[0] += d[0] - s0; oacc[1] += d[1] - s1; oacc[2] += d[2] - s0; oacc[3] += d[3] - s1;
+                mma16816(oacc, a, b0, b1, oacc);
             }
         }
     }
@@ -407,17 +399,16 @@ attn_tc_split_kernel(AttnTcParams P)
 size_t tc_split_smem(uint32_t kbytes, uint32_t vbytes)
 {
     return 2 * size_t(kbytes + vbytes) + 2 * size_t(D) * LROW + sizeof(float) * kGmax * TT +
-           sizeof(__half) * 8 * (TT + 8) + sizeof(float) * (3 * kGmax + 8 * 8) + 64;
+           sizeof(__half) * 8 * (TT + 8) + sizeof(float) * 3 * kGmax + 64;
 }
 
 }  // namespace
 
 // Workspace layout of the tensor-core path (inside attn_workspace_bytes):
-// [partials | wimg (B Hkv 8 D fp16) | bias (B Hkv 4 f32) | wsum16 (B Hkv 64 f32)].
+// [partials | wimg (B Hkv 8 D fp16) | bias (B Hkv 4 f32)].
 size_t attn_tc_extra_bytes(int B, int Hkv)
 {
-    return align256(sizeof(__half) * size_t(B) * Hkv * 8 * D) + align256(sizeof(float) * size_t(B) * Hkv * kGmax) +
-           align256(sizeof(float) * size_t(B) * Hkv * 64);
+    return align256(sizeof(__half) * size_t(B) * Hkv * 8 * D) + align256(sizeof(float) * size_t(B) * Hkv * kGmax);
 }
 
 spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vplan, const void* q, int q_dt, int B,
@@ -445,19 +436,15 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
     __half* wimg = static_cast<__half*>(extra);
     float* bias = reinterpret_cast<float*>(static_cast<uint8_t*>(extra) +
                                            align256(sizeof(__half) * size_t(B) * Hkv * 8 * D));
-    float* wsum16 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bias) +
-                                             align256(sizeof(float) * size_t(B) * Hkv * kGmax));
     P.wimg = wimg;
     P.bias = bias;
-    P.wsum16 = wsum16;
     P.part = part;
     P.kbytes = uint32_t(16 * (kplan->max_rec_bits > 0 ? kplan->max_rec_bits : 1));
     P.vbytes = uint32_t(16 * (vplan->max_rec_bits > 0 ? vplan->max_rec_bits : 1));
     const size_t sm = tc_split_smem(P.kbytes, P.vbytes);
     if (sm > 227 * 1024) return SPECTRA_OK;
     cudaFuncSetAttribute(attn_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(float) * D * D));
-    attn_tc_prep_kernel<<<B * Hkv, kGmax * D, sizeof(float) * D * D, s>>>(P.kp, q, q_dt, Hq, G, scale, wimg, bias,
-                                                                         wsum16);
+    attn_tc_prep_kernel<<<B * Hkv, kGmax * D, sizeof(float) * D * D, s>>>(P.kp, q, q_dt, Hq, G, scale, wimg, bias);
     cudaFuncSetAttribute(attn_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
     dim3 grid(nsplit, Hkv, B);
     attn_tc_split_kernel<<<grid, kThreads, sm, s>>>(P);
