@@ -643,6 +643,19 @@ __device__ __forceinline__ void unpack_channel(const uint32_t* words, int o, int
     }
 }
 
+// The same for widths <= 2: each 4-token nibble of the two planes spreads
+// into bytes with one multiply (bit i -> bit 8i), no transposes.
+__device__ __forceinline__ void unpack_narrow(const uint32_t* words, int o, int b, uint32_t (&X)[8])
+{
+    const uint32_t w0 = b > 0 ? words[o] : 0u, w1 = b > 1 ? words[o + 1] : 0u;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t s0 = (((w0 >> (4 * m)) & 0xFu) * 0x00204081u) & 0x01010101u;
+        const uint32_t s1 = (((w1 >> (4 * m)) & 0xFu) * 0x00204081u) & 0x01010101u;
+        X[m] = s0 | (s1 << 1);
+    }
+}
+
 // byte i of the 32 codes in X as a float (exact): M + code - M
 __device__ __forceinline__ float code_byte(const uint32_t (&X)[8], int t)
 {
@@ -835,8 +848,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             if (t0 < P.T && R > 0) {
                 const uint32_t* words = reinterpret_cast<const uint32_t*>(cs + sc * P.cbytes) + gi * R;
                 uint32_t X0[8], X1[8];
-                unpack_channel(words, o0, b0, bmax, X0);
-                unpack_channel(words, o1, b1, bmax, X1);
+                if (bmax <= 2) {
+                    unpack_narrow(words, o0, b0, X0);
+                    unpack_narrow(words, o1, b1, X1);
+                } else {
+                    unpack_channel(words, o0, b0, bmax, X0);
+                    unpack_channel(words, o1, b1, bmax, X1);
+                }
                 const uint32_t abase = smem_u32(as + sa * P.na * OPND) + hc * KBLK;
                 const float* lv0 = lv + (b0 > 0 ? (b0 - 1) * kLmStride : 0);
                 const float* lv1 = lv + (b1 > 0 ? (b1 - 1) * kLmStride : 0);
