@@ -161,8 +161,13 @@ def run_ours(args, rank, world, local_rank):
         fork[1].record(s2)
         s.wait_event(fork[1])
         mark(1)
+        # the two allocations are independent as well
+        fork[0].record(s)
+        s2.wait_event(fork[0])
         spx.spectra_alloc_bits(kp, AVG_BITS)
-        spx.spectra_alloc_bits(vp, AVG_BITS)
+        spx.spectra_alloc_bits(vp, AVG_BITS, stream=s2)
+        fork[1].record(s2)
+        s.wait_event(fork[1])
         mark(2)
         spx.spectra_encode(kp, K[c], kc[c])
         spx.spectra_encode(vp, V[c], vc[c])

@@ -165,20 +165,6 @@ __device__ __forceinline__ uint32_t quant_uniform(float y, float qk, float cl)
     return __float_as_uint(__fmaf_rd(s, cl, kMagic));
 }
 
-// Lloyd-Max code: number of thresholds <= u among th[1 .. 2^b - 1]
-// (ascending), for a per-lane width b <= bmax (bmax warp-uniform).
-__device__ __forceinline__ uint32_t quant_lm(const float* th, int b, int bmax, float u)
-{
-    int lo = 0;
-    for (int s = bmax - 1; s >= 0; --s) {
-        if (s < b) {
-            const int step = 1 << s;
-            if (th[lo + step] <= u) lo += step;
-        }
-    }
-    return uint32_t(lo);
-}
-
 // ------------------------------------------------------------------ encode
 constexpr int ETILE = 256;                        // tokens per encode tile (MMA N)
 constexpr uint32_t ESTAGE = ETILE * D * 2;        // x tile, two K blocks: 64 KB
@@ -187,6 +173,7 @@ constexpr uint32_t IDESC_E = idesc_bf16_f32(128, ETILE);
 constexpr int kEncEpiWarps = 16;
 constexpr int kEncThreads = 64 + 32 * kEncEpiWarps;   // producer, MMA, epilogue
 constexpr uint32_t kImgCol = 256;                 // TMEM column of the basis image
+constexpr int kLmGroup = 8;   // Lloyd-Max values searched together
 
 struct EncParams {
     PlanView pv;
@@ -460,11 +447,28 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = quant_uniform(__uint_as_float(r[i]), qk, cl);
             } else {
+                // binary search over the thresholds, kLmGroup values at a time with the
+                // search steps outermost: kLmGroup independent shared-memory loads per step
                 const float* tb = th + (b > 0 ? (b - 1) * kLmStride : 0);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float u = __uint_as_float(r[i]) * (rwht ? invs[i] : qk);
-                    r[i] = quant_lm(tb, b, bmax, u);
+                for (int h16 = 0; h16 < 32; h16 += kLmGroup) {
+                    float u[kLmGroup];
+                    int lo[kLmGroup];
+#pragma unroll
+                    for (int i = 0; i < kLmGroup; ++i) {
+                        u[i] = __uint_as_float(r[h16 + i]) * (rwht ? invs[h16 + i] : qk);
+                        lo[i] = 0;
+                    }
+                    for (int sb = bmax - 1; sb >= 0; --sb) {
+                        const int step = sb < b ? (1 << sb) : 0;
+#pragma unroll
+                        for (int i = 0; i < kLmGroup; ++i) {
+                            const bool up = step != 0 && tb[lo[i] + step] <= u[i];
+                            lo[i] += up ? step : 0;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < kLmGroup; ++i) r[h16 + i] = uint32_t(lo[i]);
                 }
             }
 #pragma unroll

@@ -1,6 +1,6 @@
 """Shared pytest setup.
 
-Markers: ``gpu`` -- needs a CUDA device (runs on the GPU machine only).
+Markers: ``gpu`` -- needs a CUDA device.
 """
 import os
 import sys
