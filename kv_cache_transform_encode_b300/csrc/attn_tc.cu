@@ -23,11 +23,13 @@
 //  2. eight warps unpack them, one channel per lane (the bit-plane words of
 //     a 32-token group become 32 code bytes through four 8x8 bit
 //     transposes), into fp16 tiles L[c][t];
-//  3. scores: mma.sync m16n8k16, A = L_K^T (ldmatrix.trans), B = [W_hi; W_lo]
-//     (n = head, hi/lo), one 16-token slice per warp;
-//  4. online softmax per head (warps 0..3);
-//  5. P V: mma.sync, A = L_V (channels x tokens), B = [P_hi; P_lo], one
-//     16-channel slice per warp, accumulated over the split in registers.
+//  3. each warp then owns 16 tokens of the tile end to end: scores by
+//     mma.sync m16n8k16 (A = L_K^T via ldmatrix.trans, B = [W_hi; W_lo],
+//     n = head, hi/lo), an online softmax over its own slice (its running
+//     max and sum per head in registers), and P V (A = L_V, channels x the
+//     slice's tokens, B = [P_hi; P_lo]) into its own accumulators for all
+//     128 channels.  Two block barriers per tile (codes landed, tiles
+//     unpacked); the eight slices merge in shared memory at the end.
 // The split's (m, l, sum_t p z) go to the workspace; the combine kernel
 // of attn.cu merges splits, dequantizes and rotates by the V basis.
 #include "spectra_internal.cuh"
@@ -44,6 +46,7 @@ constexpr int TT = 128;                  // tokens per tile
 constexpr int LROW = TT * 2 + 16;        // bytes per L row (padded: conflict-free ldmatrix)
 constexpr int kThreads = 256;
 constexpr int kGmax = 4;                 // query heads per kv head
+constexpr int PROW = 24;                 // halves per row of a warp's P tile (conflict-free B loads)
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
 {
@@ -181,11 +184,9 @@ attn_tc_split_kernel(AttnTcParams P)
     const uint32_t cwb = P.kbytes + P.vbytes;
     uint8_t* Lk = cw + 2 * cwb;                                  // [D][LROW]
     uint8_t* Lv = Lk + D * LROW;                                 // [D][LROW]
-    float* S = reinterpret_cast<float*>(Lv + D * LROW);          // [kGmax][TT]
-    __half* Pm = reinterpret_cast<__half*>(S + kGmax * TT);      // [8][TT + 8]
-    float* st_m = reinterpret_cast<float*>(Pm + 8 * (TT + 8));   // [kGmax]
-    float* st_l = st_m + kGmax;
-    float* st_a = st_l + kGmax;                                  // alpha of this tile
+    __half* Pw = reinterpret_cast<__half*>(Lv + D * LROW);      // per warp [8][PROW]: P of its 16 tokens
+    float* mw = reinterpret_cast<float*>(Pw + 8 * 8 * PROW);     // [8 warps][kGmax] running max
+    float* lw = mw + 8 * kGmax;                                  // [8 warps][kGmax] running sum
 
     const int64_t t_begin = int64_t(split) * P.split_len;
     const int64_t t_end = min(P.ctx, t_begin + P.split_len);
@@ -217,8 +218,15 @@ attn_tc_split_kernel(AttnTcParams P)
     }
     const float bias0 = P.bias[size_t(bh) * kGmax + ((2 * tig) & 3)];
     const float bias1 = P.bias[size_t(bh) * kGmax + ((2 * tig + 1) & 3)];
-    float oacc[4] = {0.f, 0.f, 0.f, 0.f};     // (channel g8 / g8+8, column n = 2 tig / 2 tig + 1)
-    if (tid < kGmax) { st_m[tid] = -INFINITY; st_l[tid] = 0.f; }
+    // this warp's share of the output, all 128 channels: m-tile mt holds
+    // channels 16 mt + g8 (+8), columns n = 2 tig, 2 tig + 1 (head hi / lo)
+    float oacc[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+    // online-softmax state of the warp's token slice, heads j0 = 2 (tig & 1), j0 + 1
+    const int j0 = 2 * (tig & 1), j1 = j0 + 1;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    __half* pw = Pw + warp * 8 * PROW;
 
     auto issue_load = [&](int tile, int buf) {
         const int64_t t0 = t_begin + int64_t(tile) * TT;
@@ -286,120 +294,137 @@ attn_tc_split_kernel(AttnTcParams P)
         }
         __syncthreads();
 
-        // ---- scores: warp -> tokens 16 warp .. +15
-        {
-            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-            const int mi = lane >> 3, ri = lane & 7;
+        // ---- per warp, tokens 16 warp .. +15 of the tile: scores, online
+        // softmax and P V, with no block barrier in between
+        const int mi = lane >> 3, ri = lane & 7;
+        const int tw = warp * 16;
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kb = 0; kb < 8; ++kb) {
-                uint32_t a[4];
-                const int k = kb * 16 + (mi >> 1) * 8 + ri, m = warp * 16 + (mi & 1) * 8;
-                ldsm_x4_t(smem_addr(Lk + k * LROW + m * 2), a);
-                mma16816(sacc, a, wf[kb][0], wf[kb][1], sacc);
-            }
-            // lanes tig 0/1 hold hi heads 2 tig, 2 tig + 1; lanes tig 2/3 the lo parts
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[e] += __shfl_xor_sync(0xffffffffu, sacc[e], 2);
-            if (tig < 2) {
-                const int j0 = 2 * tig, j1 = 2 * tig + 1;
-                const int ta = warp * 16 + g8, tb = ta + 8;
-                const bool la = t0 + ta < t_end, lb = t0 + tb < t_end;
-                if (j0 < G) {
-                    S[j0 * TT + ta] = la ? sacc[0] + bias0 : -INFINITY;
-                    S[j0 * TT + tb] = lb ? sacc[2] + bias0 : -INFINITY;
-                }
-                if (j1 < G) {
-                    S[j1 * TT + ta] = la ? sacc[1] + bias1 : -INFINITY;
-                    S[j1 * TT + tb] = lb ? sacc[3] + bias1 : -INFINITY;
-                }
-            }
+        for (int kb = 0; kb < 8; kb += 2) {
+            uint32_t a[4], a2[4];
+            const int k = kb * 16 + (mi >> 1) * 8 + ri, m = tw + (mi & 1) * 8;
+            ldsm_x4_t(smem_addr(Lk + k * LROW + m * 2), a);
+            ldsm_x4_t(smem_addr(Lk + (k + 16) * LROW + m * 2), a2);
+            mma16816(sa, a, wf[kb][0], wf[kb][1], sa);
+            mma16816(sb, a2, wf[kb + 1][0], wf[kb + 1][1], sb);
         }
-        __syncthreads();
-
-        // ---- online softmax: warp j < G handles head j
-        if (warp < kGmax) {
-            const int j = warp;
-            float s[4];
-            float mx = -INFINITY;
+        float sc[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                s[i] = (j < G) ? S[j * TT + lane + 32 * i] : -INFINITY;
-                mx = fmaxf(mx, s[i]);
-            }
-            for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float mold = st_m[j];
-            const float mnew = fmaxf(mold, mx);
-            const float alpha = (mold == -INFINITY) ? 0.f : __expf(mold - mnew);
-            float ptot = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float p = (s[i] == -INFINITY) ? 0.f : __expf(s[i] - mnew);
-                const __half ph = __float2half_rn(p);
-                const __half pl = __float2half_rn(p - __half2float(ph));
-                const int t = lane + 32 * i;
-                Pm[j * (TT + 8) + t] = ph;
-                Pm[(kGmax + j) * (TT + 8) + t] = pl;
-                ptot += __half2float(ph) + __half2float(pl);
-            }
-            for (int o = 16; o; o >>= 1) ptot += __shfl_xor_sync(0xffffffffu, ptot, o);
-            if (lane == 0) {
-                st_l[j] = st_l[j] * alpha + ptot;
-                st_m[j] = mnew;
-                st_a[j] = alpha;
-            }
-        } else if (warp < 2 * kGmax && warp - kGmax >= 0) {
-            // zero P rows of absent heads (G < 4) so the MMA sees zeros
-            const int j = warp - kGmax;
-            if (j >= G) {
-                for (int t = lane; t < TT; t += 32) {
-                    Pm[j * (TT + 8) + t] = __float2half_rn(0.f);
-                    Pm[(kGmax + j) * (TT + 8) + t] = __float2half_rn(0.f);
-                }
-                if (lane == 0) st_a[j] = 0.f;
-            }
+        for (int e = 0; e < 4; ++e) {
+            sc[e] = sa[e] + sb[e];
+            sc[e] += __shfl_xor_sync(0xffffffffu, sc[e], 2);   // hi + lo columns
         }
-        __syncthreads();
-
-        // ---- P V: warp -> channels 16 warp .. +15; each column n (head hi/lo)
-        // accumulated on its own, offsets removed per 16-token chunk
         {
-            const int mi = lane >> 3, ri = lane & 7;
-            const float a0 = st_a[(2 * tig) & 3], a1 = st_a[(2 * tig + 1) & 3];
-            oacc[0] *= a0; oacc[1] *= a1; oacc[2] *= a0; oacc[3] *= a1;
+            const bool la = t0 + tw + g8 < t_end, lb = t0 + tw + g8 + 8 < t_end;
+            const bool h0 = j0 < G, h1 = j1 < G;
+            sc[0] = (la && h0) ? sc[0] + bias0 : -INFINITY;
+            sc[1] = (la && h1) ? sc[1] + bias1 : -INFINITY;
+            sc[2] = (lb && h0) ? sc[2] + bias0 : -INFINITY;
+            sc[3] = (lb && h1) ? sc[3] + bias1 : -INFINITY;
+        }
+        float x0 = fmaxf(sc[0], sc[2]), x1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-            for (int kb = 0; kb < 8; ++kb) {
-                uint32_t a[4];
-                const int m = warp * 16 + (mi & 1) * 8 + ri, k = kb * 16 + (mi >> 1) * 8;
-                ldsm_x4(smem_addr(Lv + m * LROW + k * 2), a);
-                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(Pm + g8 * (TT + 8) + kb * 16 + 2 * tig);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(Pm + g8 * (TT + 8) + kb * 16 + 8 + 2 * tig);
-                mma16816(oacc, a, b0, b1, oacc);
-            }
+        for (int o = 4; o < 32; o <<= 1) {
+            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+        }
+        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+        const float al0 = (m0 == -INFINITY) ? 0.f : __expf(m0 - n0);
+        const float al1 = (m1 == -INFINITY) ? 0.f : __expf(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        __half ph[4], pl[4];
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float pe = (sc[e] == -INFINITY) ? 0.f : __expf(sc[e] - ((e & 1) ? n1 : n0));
+            ph[e] = __float2half_rn(pe);
+            pl[e] = __float2half_rn(pe - __half2float(ph[e]));
+            const float pq = __half2float(ph[e]) + __half2float(pl[e]);
+            if (e & 1) ps1 += pq; else ps0 += pq;
+        }
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            ps0 += __shfl_xor_sync(0xffffffffu, ps0, o);
+            ps1 += __shfl_xor_sync(0xffffffffu, ps1, o);
+        }
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
+        // P of the slice as the B operand [n = head hi 0..3 / lo 4..7][k = token]:
+        // lanes tig 0/1 write the hi parts of their heads, tig 2/3 the lo parts
+        {
+            const __half* pv = tig < 2 ? ph : pl;
+            const int r0 = (tig < 2 ? 0 : kGmax) + j0;
+            pw[r0 * PROW + g8] = pv[0];
+            pw[(r0 + 1) * PROW + g8] = pv[1];
+            pw[r0 * PROW + g8 + 8] = pv[2];
+            pw[(r0 + 1) * PROW + g8 + 8] = pv[3];
+        }
+        __syncwarp();
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(pw + g8 * PROW + 2 * tig);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(pw + g8 * PROW + 8 + 2 * tig);
+        // columns n = 2 tig, 2 tig + 1 are heads j0, j1 (hi for tig < 2, lo otherwise)
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            oacc[mt][0] *= al0; oacc[mt][1] *= al1; oacc[mt][2] *= al0; oacc[mt][3] *= al1;
+            uint32_t a[4];
+            const int m = mt * 16 + (mi & 1) * 8 + ri, k = tw + (mi >> 1) * 8;
+            ldsm_x4(smem_addr(Lv + m * LROW + k * 2), a);
+            mma16816(oacc[mt], a, b0, b1, oacc[mt]);
+        }
+    }
+    __syncthreads();   // every warp is past its last read of Lk / Lv
+
+    // merge the eight warps' slices: warp w's partial scaled by exp(m_w - M)
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[mt][e] += __shfl_xor_sync(0xffffffffu, oacc[mt][e], 2);   // hi + lo
+    float* Ow = reinterpret_cast<float*>(Lk);                    // [8 warps][kGmax][D]
+    if (g8 == 0 && tig < 2) {
+        mw[warp * kGmax + j0] = m0; mw[warp * kGmax + j1] = m1;
+        lw[warp * kGmax + j0] = l0; lw[warp * kGmax + j1] = l1;
+    }
+    if (tig < 2) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int c0 = mt * 16 + g8, c1 = c0 + 8;
+            Ow[(warp * kGmax + j0) * D + c0] = oacc[mt][0];
+            Ow[(warp * kGmax + j1) * D + c0] = oacc[mt][1];
+            Ow[(warp * kGmax + j0) * D + c1] = oacc[mt][2];
+            Ow[(warp * kGmax + j1) * D + c1] = oacc[mt][3];
         }
     }
     __syncthreads();
-#pragma unroll
-    for (int e = 0; e < 4; ++e) oacc[e] += __shfl_xor_sync(0xffffffffu, oacc[e], 2);   // hi + lo
 
     // partials: [(b Hq + h G + j) nsplit + split][2 + D]: m, l, sum_t p code
-    if (tig < 2) {
-        const int j0 = 2 * tig, j1 = 2 * tig + 1;
-        const int c0 = warp * 16 + g8, c1 = c0 + 8;
-        auto base = [&](int j) { return P.part + ((int64_t(b) * P.Hq + h * G + j) * P.nsplit + split) * (D + 2); };
-        if (j0 < G) { base(j0)[2 + c0] = oacc[0]; base(j0)[2 + c1] = oacc[2]; }
-        if (j1 < G) { base(j1)[2 + c0] = oacc[1]; base(j1)[2 + c1] = oacc[3]; }
-    }
-    if (tid < G) {
-        float* bp = P.part + ((int64_t(b) * P.Hq + h * G + tid) * P.nsplit + split) * (D + 2);
-        bp[0] = ntiles > 0 ? st_m[tid] : -INFINITY;
-        bp[1] = ntiles > 0 ? st_l[tid] : 0.f;
+    for (int i = tid; i < kGmax * D; i += kThreads) {
+        const int j = i / D, c = i % D;
+        if (j >= G) continue;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) M = fmaxf(M, mw[w * kGmax + j]);
+        float o = 0.f, l = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const float mv = mw[w * kGmax + j];
+            const float f = (mv == -INFINITY) ? 0.f : __expf(mv - M);
+            o = fmaf(f, Ow[(w * kGmax + j) * D + c], o);
+            l = fmaf(f, lw[w * kGmax + j], l);
+        }
+        float* bp = P.part + ((int64_t(b) * P.Hq + h * G + j) * P.nsplit + split) * (D + 2);
+        bp[2 + c] = o;
+        if (c == 0) {
+            bp[0] = M;
+            bp[1] = l;
+        }
     }
 }
 
 size_t tc_split_smem(uint32_t kbytes, uint32_t vbytes)
 {
-    return 2 * size_t(kbytes + vbytes) + 2 * size_t(D) * LROW + sizeof(float) * kGmax * TT +
-           sizeof(__half) * 8 * (TT + 8) + sizeof(float) * 3 * kGmax + 64;
+    return 2 * size_t(kbytes + vbytes) + 2 * size_t(D) * LROW + sizeof(__half) * 8 * 8 * PROW +
+           sizeof(float) * 2 * 8 * kGmax + 64;
 }
 
 }  // namespace
