@@ -20,9 +20,13 @@
 // One CTA per (context split, kv head, batch).  Per 128-token tile:
 //  1. the tile's K and V code words arrive in shared memory (cp.async,
 //     double-buffered);
-//  2. eight warps unpack them, one channel per lane (the bit-plane words of
-//     a 32-token group become 32 code bytes through four 8x8 bit
-//     transposes), into fp16 tiles L[c][t];
+//  2. eight warps unpack them (per side, warp = 32-token group, lane =
+//     channel, over four blocks of 32 channels: the bit-plane words of a
+//     group become 32 code bytes through four 8x8 bit transposes, or, where
+//     a block is at most 2 bits wide, the two planes are interleaved into
+//     even- and odd-token words and each fp16 pair is one shift and one
+//     mask), into fp16 tiles L[c][p]; within a 32-token group position
+//     2s holds token s and 2s + 1 token s + 16;
 //  3. each warp then owns 16 tokens of the tile end to end: scores by
 //     mma.sync m16n8k16 (A = L_K^T via ldmatrix.trans, B = [W_hi; W_lo],
 //     n = head, hi/lo), an online softmax over its own slice (its running
@@ -198,12 +202,24 @@ attn_tc_split_kernel(AttnTcParams P)
     const uint8_t* ks = P.kc + sid * P.sstride;
     const uint8_t* vs = P.vc + sid * P.sstride;
 
-    // unpack role: side (K for warps 0-3, V for 4-7), channel
-    const int side = warp >> 2, uc = (warp & 3) * 32 + lane;
+    // unpack role: side (K for warps 0-3, V for 4-7) and 32-token group
+    // ug = warp & 3 of the tile, over all 128 channels in four blocks of 32
+    // (channel 32 cb + lane).  The wide channels (the leading eigen-
+    // directions) sit in block 0, so every warp gets the same mix of one
+    // wide and three narrow blocks.  Per block: widths packed 8 bits each
+    // (ubp), the widest in the block (ubm), and word offsets 16 bits each.
+    const int side = warp >> 2, ug = warp & 3;
     const PlanView& up = side ? P.vp : P.kp;
-    const int ub = up.bits[size_t(h) * D + uc];
-    const int uo = up.chan_off[size_t(h) * D + uc];
-    const int ubmax = __reduce_max_sync(0xffffffffu, ub);
+    uint32_t ubp = 0, ubm = 0, uop01 = 0, uop23 = 0;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        const int c = cb * 32 + lane;
+        const uint32_t wb = uint32_t(up.bits[size_t(h) * D + c]);
+        const uint32_t wo = uint32_t(up.chan_off[size_t(h) * D + c]);
+        ubp |= wb << (8 * cb);
+        ubm |= uint32_t(__reduce_max_sync(0xffffffffu, wb)) << (8 * cb);
+        if (cb < 2) uop01 |= wo << (16 * cb); else uop23 |= wo << (16 * (cb - 2));
+    }
     const int uR = side ? RV : RK;
 
     // score operand B: W rows (n = g8: 0..3 hi, 4..7 lo), k = 16 kb + 2 tig (+8)
@@ -250,51 +266,60 @@ attn_tc_split_kernel(AttnTcParams P)
         __syncthreads();                                   // code words landed; previous tile done
         if (tile + 1 < ntiles) issue_load(tile + 1, buf ^ 1);
 
-        // ---- unpack: one channel per lane, four 32-token groups
+        // ---- unpack: one 32-token group per warp, one channel per lane, four channel blocks
         {
             const uint32_t* words = reinterpret_cast<const uint32_t*>(cw + buf * cwb + (side ? P.kbytes : 0));
             uint8_t* L = side ? Lv : Lk;
-            uint8_t* row = L + uc * LROW;
-            // z = code - 2^(b-1) (0 for dropped channels): (1024 + code) - (1024 + 2^(b-1)), exact in fp16
-            const __half2 cz = __float2half2_rn(1024.f + (ub > 0 ? float(1 << (ub - 1)) : 0.f));
+            const bool live = t0 + 32 * ug < t_end && uR > 0;
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
-                uint32_t X[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                if (t0 + 32 * g < t_end && uR > 0) {
-                    if (ubmax <= 2) {
-                        // widths <= 2 (the warp's widest channel): spread each
-                        // 4-token nibble of the two planes into bytes with one
-                        // multiply (bit i -> bit 8i) instead of the transposes
-                        const uint32_t* wg = words + g * uR + uo;
-                        const uint32_t w0 = ub > 0 ? wg[0] : 0u, w1 = ub > 1 ? wg[1] : 0u;
+            for (int cb = 0; cb < 4; ++cb) {
+                const int ub = int((ubp >> (8 * cb)) & 0xFFu), ubmax = int((ubm >> (8 * cb)) & 0xFFu);
+                const int uo = int(((cb < 2 ? uop01 : uop23) >> (16 * (cb & 1))) & 0xFFFFu);
+                // v[s] = fp16 pair (1024 + code) for tokens s and s + 16 of the group:
+                // the tile keeps each group in that pair order (positions 2s, 2s + 1),
+                // the same for K and V, so scores and P V see one consistent order
+                uint32_t v[16];
+                if (ubmax <= 2) {
+                    // widths <= 2 (the block's widest channel): interleave the two
+                    // planes once into E (even tokens) and O (odd tokens), 2 bits a
+                    // token; tokens s and s + 16 are then bits s and s + 16 of E (or O)
+                    uint32_t w0 = 0u, w1 = 0u;
+                    if (live) {
+                        const uint32_t* wg = words + ug * uR + uo;
+                        w0 = ub > 0 ? wg[0] : 0u;
+                        w1 = ub > 1 ? wg[1] : 0u;
+                    }
+                    const uint32_t E = (w0 & 0x55555555u) | ((w1 << 1) & 0xAAAAAAAAu);
+                    const uint32_t O = ((w0 >> 1) & 0x55555555u) | (w1 & 0xAAAAAAAAu);
 #pragma unroll
-                        for (int m = 0; m < 8; ++m) {
-                            const uint32_t s0 = (((w0 >> (4 * m)) & 0xFu) * 0x00204081u) & 0x01010101u;
-                            const uint32_t s1 = (((w1 >> (4 * m)) & 0xFu) * 0x00204081u) & 0x01010101u;
-                            X[m] = s0 | (s1 << 1);
-                        }
-                    } else {
-                        planes_to_codes(words + g * uR, uo, ub, ubmax, X);
+                    for (int q = 0; q < 16; ++q) {
+                        const uint32_t x = (q & 1) ? (O >> (q - 1)) : (E >> q);
+                        v[q] = (x & 0x00030003u) | 0x64006400u;
+                    }
+                } else {
+                    uint32_t X[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // byte i of X[m]: code of token 4m + i
+                    if (live) planes_to_codes(words + ug * uR, uo, ub, ubmax, X);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const uint32_t sel = uint32_t(q & 3) | (uint32_t(4 + (q & 3)) << 8);
+                        v[q] = (__byte_perm(X[q >> 2], X[(q >> 2) + 4], sel) & 0x00FF00FFu) | 0x64006400u;
                     }
                 }
-                uint32_t v[16];
+                // z = code - 2^(b-1) (0 for dropped channels): (1024 + code) - (1024 + 2^(b-1)), exact in fp16
+                const __half2 cz = __float2half2_rn(1024.f + (ub > 0 ? float(1 << (ub - 1)) : 0.f));
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const uint32_t p0 = __byte_perm(X[m], 0x6464u, 0x5140);   // tokens 4m, 4m+1 -> fp16 1024 + code
-                    const uint32_t p1 = __byte_perm(X[m], 0x6464u, 0x5342);   // tokens 4m+2, 4m+3
-                    const __half2 z0 = __hsub2(*reinterpret_cast<const __half2*>(&p0), cz);
-                    const __half2 z1 = __hsub2(*reinterpret_cast<const __half2*>(&p1), cz);
-                    v[2 * m] = *reinterpret_cast<const uint32_t*>(&z0);
-                    v[2 * m + 1] = *reinterpret_cast<const uint32_t*>(&z1);
+                for (int q = 0; q < 16; ++q) {
+                    const __half2 z = __hsub2(*reinterpret_cast<const __half2*>(&v[q]), cz);
+                    v[q] = *reinterpret_cast<const uint32_t*>(&z);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(row + g * 64);
+                uint4* dst = reinterpret_cast<uint4*>(L + (cb * 32 + lane) * LROW + ug * 64);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
             }
         }
         __syncthreads();
 
-        // ---- per warp, tokens 16 warp .. +15 of the tile: scores, online
+        // ---- per warp, positions 16 warp .. +15 of the tile: scores, online
         // softmax and P V, with no block barrier in between
         const int mi = lane >> 3, ri = lane & 7;
         const int tw = warp * 16;
@@ -315,7 +340,11 @@ attn_tc_split_kernel(AttnTcParams P)
             sc[e] += __shfl_xor_sync(0xffffffffu, sc[e], 2);   // hi + lo columns
         }
         {
-            const bool la = t0 + tw + g8 < t_end, lb = t0 + tw + g8 + 8 < t_end;
+            // positions tw + g8 (+8) hold tokens 32 (warp / 2) + (q >> 1) + 16 (q & 1), q the position in the group
+            const int qa = (warp & 1) * 16 + g8, qb = qa + 8;
+            const int gbase = (warp >> 1) * 32;
+            const bool la = t0 + gbase + (qa >> 1) + (qa & 1) * 16 < t_end;
+            const bool lb = t0 + gbase + (qb >> 1) + (qb & 1) * 16 < t_end;
             const bool h0 = j0 < G, h1 = j1 < G;
             sc[0] = (la && h0) ? sc[0] + bias0 : -INFINITY;
             sc[1] = (la && h1) ? sc[1] + bias1 : -INFINITY;
