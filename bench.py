@@ -276,9 +276,8 @@ def run_ours(args, rank, world, local_rank):
 
     attn = attn_workload(spx, kp, vp, dev, _peaks()) if args.attn_workload else None
 
-    tokens = T_TOK * world
     res = {
-        "metric": METRIC, "value": round(tokens / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(_whole_job_rate(T_TOK, world, ms), 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded spiked-covariance multivariate Student-t, bf16)",
@@ -291,7 +290,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "attn_decode": attn,
         "clocks": clocks,
-        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(_whole_job_rate(T_TOK, world, e2e_ms), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": args.steps * launches_per_step(),
     }
@@ -396,13 +395,21 @@ def _barrier(world):
 
 
 def _max_over_ranks(v, world):
+    """The largest of the ranks' values (the slowest rank's time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _whole_job_rate(units_per_rank, world, ms_max):
+    """Units every rank processed, over the slowest rank's time (weak scaling:
+    each replica processes the same workload)."""
+    return units_per_rank * world / (ms_max * 1e-3)
 
 
 # ---------------------------------------------------------------- oracle
