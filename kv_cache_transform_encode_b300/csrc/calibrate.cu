@@ -783,6 +783,7 @@ spectra_status launch_jacobi(const spectra_plan* plan, const float* partials, in
         constexpr int C = kJ1sCluster;
         const size_t sm = sizeof(float) * (2 * J1s<C>::PPC * kJ2 + kJ2 * (kJ2 + 1));
         cudaFuncSetAttribute(jacobi1s_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        if (C > 8) cudaFuncSetAttribute(jacobi1s_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         jacobi1s_kernel<C><<<plan->heads * C, 32 * J1s<C>::NW, sm, s>>>(partials, nchunks, inv_n, max_sweeps,
                                                                       plan->basis_mat, plan->eigvals, plan->status,
                                                                       gram_out);
