@@ -302,6 +302,7 @@ def run_ours(args, rank, world, local_rank):
         "jacobi_sweeps": {"min": min(sweeps), "max": max(sweeps)},
         "codec_tokens_per_s": round(T_TOK / ((ph["encode"] + ph["decode"]) * 1e-3), 1),
         "roofline": roof,
+        "rotation": _rotation_rate(T_TOK, H_KV, D, 3, ph["encode"] / 2, peaks["bf16_tflops"]),
         "attn_decode": attn,
         "clocks": clocks,
         "e2e": {"value": round(_whole_job_rate(T_TOK, world, e2e_ms), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -418,6 +419,17 @@ def _max_over_ranks(v, world):
     t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _rotation_rate(tokens, heads, d, terms, launch_ms, peak_tflops):
+    """Tensor-core rate of the encode's rotation contraction: each of the
+    `terms` bf16 basis terms costs 2 d^2 flops per (token, head) vector; the
+    algorithmic rate counts the contraction once."""
+    executed = terms * 2.0 * d * d * tokens * heads / (launch_ms * 1e-3) / 1e12
+    algorithmic = executed / terms
+    return {"executed_tflops": round(executed, 1), "algorithmic_tflops": round(algorithmic, 1),
+            "terms": terms, "peak_tflops": peak_tflops, "frac_executed": round(executed / peak_tflops, 4),
+            "unit": "TFLOP/s"}
 
 
 def _whole_job_rate(units_per_rank, world, ms_max):

@@ -68,3 +68,15 @@ def test_single_rank_helpers_need_no_process_group():
     bench._barrier(1)
     assert bench._max_over_ranks(3.5, 1) == 3.5
     assert bench._whole_job_rate(32768, 1, 2.0) == pytest.approx(32768 / 2e-3)
+
+
+def test_rotation_rate_arithmetic():
+    """The bench's tensor-rate line: terms x 2 d^2 flops per vector over the launch time."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    r = bench._rotation_rate(1000, 2, 4, 3, 1.0, 100.0)        # 3 * 2 * 16 * 2000 flops in 1 ms
+    assert r["executed_tflops"] == pytest.approx(3 * 2 * 16 * 2000 / 1e-3 / 1e12, abs=0.05)
+    assert r["algorithmic_tflops"] == pytest.approx(r["executed_tflops"] / 3, abs=0.05)
+    r = bench._rotation_rate(32768, 8, 128, 3, 0.0349, 1810.1)
+    assert r["frac_executed"] == pytest.approx(r["executed_tflops"] / 1810.1, rel=1e-3)
