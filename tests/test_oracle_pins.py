@@ -455,3 +455,89 @@ def test_bruteforce_2x16x32_pipeline(orc):
         if B == 16.0:
             xs = orc.decode(plan, [orc.encode_head(plan, h, x[:, h, :])["stream"] for h in range(2)], 32)
             assert orc.relmse(x, xs) <= 1e-3
+
+
+# ---------------------------------------------------------------- RWHT branch of the codec
+def _sphere_coordinate_mse(orc, d, b):
+    """MSE of the width-b Gaussian Lloyd-Max quantizer on u = sqrt(d) y_c /
+    ||y|| for isotropic Gaussian y in d dimensions (a coordinate of a
+    uniformly random point on the sphere of radius sqrt(d): density
+    proportional to (1 - u^2/d)^((d-3)/2) on |u| < sqrt(d)), by quadrature."""
+    levels, thresh = orc.lloyd_max_tables()
+    L = 1 << b
+    lv, th = levels[b - 1, :L], thresh[b - 1, 1:L]
+    r = np.sqrt(d)
+    f = lambda u: (1.0 - u * u / d) ** ((d - 3) / 2.0)
+    Z = scipy.integrate.quad(f, -r, r, limit=200)[0]
+    edges = np.concatenate([[-r], th, [r]])
+    return sum(scipy.integrate.quad(lambda u, k=k: (u - lv[k]) ** 2 * f(u), edges[k], edges[k + 1],
+                                    limit=200)[0] for k in range(L)) / Z
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_rwht_per_token_sigma_branch(orc, seed):
+    """The data-independent variant ("Technisch Overzicht ...", "Experimentele
+    Opstelling": randomized WHT, then a fixed Lloyd-Max codebook), with the
+    per-token scale sigma = ||x|| / sqrt(d) read for it.  For Gaussian x the
+    rotation keeps ||y|| = ||x|| and y/sigma is a coordinate of a random point
+    on the sphere of radius sqrt(d), independent of ||x||, so the relative
+    reconstruction MSE equals that coordinate's 3-bit quantizer MSE (0.03398
+    at d = 128, by quadrature; 0.03455 in the Gaussian limit).  A scale of
+    ||x|| instead (or ||x|| / d, or swapped strides) misses it by orders of
+    magnitude.  The stored norm is ||x|| rounded to fp32, and the decode
+    scales linearly with it."""
+    d, T = 128, 4096
+    x = np.random.default_rng(100 + seed).standard_normal((T, d))
+    plan = orc.make_rwht_plan(synth.rwht_signs(seed, 1, d), 3)
+    enc = orc.encode_head(plan, 0, x)
+    assert enc["norms"].dtype == np.float32
+    assert np.array_equal(enc["norms"], np.linalg.norm(x, axis=1).astype(np.float32))
+    np.testing.assert_allclose(enc["sigma"][:, 0], enc["norms"].astype(np.float64) / np.sqrt(d), rtol=0)
+    xh = orc.decode_head(plan, 0, enc["stream"], T, enc["norms"])
+    want = _sphere_coordinate_mse(orc, d, 3)
+    assert abs(want - 0.03398) < 5e-5
+    assert abs(orc.relmse(x, xh) - want) <= 0.01 * want, (orc.relmse(x, xh), want)
+    xh2 = orc.decode_head(plan, 0, enc["stream"], T, 2 * enc["norms"])
+    np.testing.assert_allclose(xh2, 2 * xh, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- decision margin
+def test_decision_margin_worked_example(orc):
+    """Distances to the nearest decision boundary in units of sigma, against
+    tests/golden/decision_margin_worked_example.txt (computed by hand; the
+    Lloyd-Max rows use Max's 4-digit thresholds, hence the 1e-4 tolerance)."""
+    for r in _golden_lines("decision_margin_worked_example.txt"):
+        kind, b, y, want = r[0], int(r[1]), float(r[2]), float(r[3])
+        quant = orc.QUANT_UNIFORM if kind == "u" else orc.QUANT_LLOYD
+        plan = orc.Plan(orc.BASIS_EIGEN, quant, np.array([[b]], dtype=np.uint8),
+                        basis=np.eye(1)[None], eigvals=np.array([[4.0]]))
+        enc = orc.encode_head(plan, 0, np.array([[y]]))
+        got = orc.decision_margin(plan, 0, enc)[0, 0]
+        if np.isinf(want):
+            assert np.isinf(got)
+        else:
+            assert abs(got - want) <= (1e-12 if kind == "u" else 1e-4), (r, got)
+
+
+# ---------------------------------------------------------------- GQA head map
+def test_attn_decode_gqa_head_map(orc):
+    """Grouped-query attention: query head j reads kv head j // (Hq / Hkv).
+    Every kv head holds a constant value vector (h + 1) * 1 and distinct
+    random keys, so each output names the kv head it read: with Hq = 8 and
+    Hkv = 4, heads (0..7) read kv (0,0,1,1,2,2,3,3); a j % Hkv map would read
+    (0,1,2,3,0,1,2,3)."""
+    g = np.random.default_rng(6)
+    B, Hq, Hkv, ctx, d = 2, 8, 4, 9, 16
+    K = g.standard_normal((B, ctx, Hkv, d))
+    V = np.zeros((B, ctx, Hkv, d))
+    for h in range(Hkv):
+        V[:, :, h, :] = h + 1.0
+    q = g.standard_normal((B, Hq, d))
+    out = orc.attn_decode(q, K, V, 0.5)
+    for b in range(B):
+        for j in range(Hq):
+            np.testing.assert_allclose(out[b, j], np.full(d, j // 2 + 1.0), rtol=1e-13)
+    # and per head: the same as single-query attention over the mapped kv head
+    for j in range(Hq):
+        np.testing.assert_allclose(out[1, j], orc.attention(q[1, j], K[1, :, j // 2], V[1, :, j // 2], 0.5),
+                                   rtol=1e-14)
