@@ -114,6 +114,28 @@ typedef struct {
 /* Library version (major*10000 + minor*100 + patch). */
 SPECTRA_API int spectra_version(void);
 
+/*
+ * Kernel family for spectra_encode, spectra_decode and spectra_attn_decode
+ * (a process-wide setting; not part of the method, which both families
+ * compute in full).  AUTO: the tensor-core kernels where they cover the call
+ * (bf16 caches with head_dim 128 for the codec; head_dim 128 with at most 4
+ * query heads per kv head for attention), the CUDA-core kernels elsewhere.
+ * CUDA_CORE: the CUDA-core kernels only.  TENSOR_CORE: the tensor-core
+ * kernels only; a call they do not cover returns SPECTRA_ERR_UNSUPPORTED.
+ * The initial value comes from the environment variable SPECTRA_PATH, read
+ * once on first use ("generic" -> CUDA_CORE, "tc" -> TENSOR_CORE, unset or
+ * anything else -> AUTO).  spectra_set_kernel_family returns
+ * SPECTRA_ERR_INVALID_ARG for an unknown value; it is not synchronised with
+ * calls in flight on other host threads.
+ */
+typedef enum {
+    SPECTRA_KERNELS_AUTO = 0,
+    SPECTRA_KERNELS_CUDA_CORE = 1,
+    SPECTRA_KERNELS_TENSOR_CORE = 2
+} spectra_kernel_family;
+SPECTRA_API spectra_status spectra_set_kernel_family(int family);
+SPECTRA_API int spectra_get_kernel_family(void);
+
 /* Human-readable name of a status code (static string, never NULL). */
 SPECTRA_API const char* spectra_status_string(spectra_status st);
 

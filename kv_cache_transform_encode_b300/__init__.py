@@ -30,7 +30,10 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error
                 4: "eigensolve not converged", 5: "bounded wait timed out",
                 6: "non-finite input", 7: "stream buffer too small"}
 
-EXPORTS = ("spectra_version", "spectra_status_string", "spectra_plan_derived_bytes",
+SPECTRA_KERNELS_AUTO, SPECTRA_KERNELS_CUDA_CORE, SPECTRA_KERNELS_TENSOR_CORE = 0, 1, 2
+
+EXPORTS = ("spectra_version", "spectra_set_kernel_family", "spectra_get_kernel_family",
+           "spectra_status_string", "spectra_plan_derived_bytes",
            "spectra_stream_bytes", "spectra_calibrate_workspace_bytes", "spectra_calibrate",
            "spectra_alloc_bits", "spectra_plan_finalize", "spectra_encode", "spectra_decode",
            "spectra_attn_workspace_bytes", "spectra_attn_decode", "spectra_attn_decode_noalloc")
@@ -70,6 +73,8 @@ def lib() -> C.CDLL:
         P = C.POINTER(spectra_plan)
         sig = {
             "spectra_version": (C.c_int, []),
+            "spectra_set_kernel_family": (C.c_int, [C.c_int]),
+            "spectra_get_kernel_family": (C.c_int, []),
             "spectra_status_string": (C.c_char_p, [C.c_int]),
             "spectra_plan_derived_bytes": (sz, [C.c_int, C.c_int]),
             "spectra_stream_bytes": (sz, [i32, i64]),
@@ -157,6 +162,16 @@ class Plan:
 # ----------------------------------------------------------------- C ABI
 def spectra_version() -> int:
     return lib().spectra_version()
+
+
+def spectra_set_kernel_family(family: int):
+    """Process-wide kernel family: SPECTRA_KERNELS_AUTO, _CUDA_CORE or
+    _TENSOR_CORE (initially from the SPECTRA_PATH environment variable)."""
+    _check(lib().spectra_set_kernel_family(int(family)), "spectra_set_kernel_family")
+
+
+def spectra_get_kernel_family() -> int:
+    return lib().spectra_get_kernel_family()
 
 
 def spectra_status_string(st: int) -> str:

@@ -6,6 +6,8 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <atomic>
+
 using namespace spectra;
 
 namespace spectra {
@@ -67,27 +69,52 @@ spectra_status check_streams(const spectra_plan* p, const uint8_t* codes, int64_
     return SPECTRA_OK;
 }
 
-// Kernel-family selection for encode/decode, read on every call so a test
-// process can switch it: SPECTRA_PATH=generic sends every call to the
-// CUDA-core kernels; SPECTRA_PATH=tc requires the tensor-core kernels (a call
-// they do not cover returns SPECTRA_ERR_UNSUPPORTED); unset = tensor cores
-// where they apply (bf16 cache, head_dim 128), CUDA cores elsewhere.
-enum PathChoice { PATH_AUTO, PATH_GENERIC, PATH_TC };
+// Kernel-family selection for encode, decode and attention.  The process-
+// wide value starts from the environment variable SPECTRA_PATH, read once
+// (generic = CUDA-core kernels only; tc = tensor-core kernels required, a
+// call they do not cover returns SPECTRA_ERR_UNSUPPORTED; unset = tensor
+// cores where they apply), and spectra_set_kernel_family changes it.
+std::atomic<int> g_family{-1};
 
-PathChoice path_choice()
+int family_from_env()
 {
     const char* e = getenv("SPECTRA_PATH");
-    if (!e) return PATH_AUTO;
-    if (e[0] == 'g') return PATH_GENERIC;
-    if (e[0] == 't') return PATH_TC;
-    return PATH_AUTO;
+    if (e && e[0] == 'g') return SPECTRA_KERNELS_CUDA_CORE;
+    if (e && e[0] == 't') return SPECTRA_KERNELS_TENSOR_CORE;
+    return SPECTRA_KERNELS_AUTO;
 }
+
+}  // namespace
+
+int spectra::kernel_family()
+{
+    int f = g_family.load(std::memory_order_relaxed);
+    if (f < 0) {
+        int expect = -1;
+        g_family.compare_exchange_strong(expect, family_from_env());
+        f = g_family.load(std::memory_order_relaxed);
+    }
+    return f;
+}
+
+namespace {
 
 }  // namespace
 
 extern "C" {
 
-int spectra_version(void) { return 100; }
+int spectra_version(void) { return 200; }
+
+spectra_status spectra_set_kernel_family(int family)
+{
+    if (family != SPECTRA_KERNELS_AUTO && family != SPECTRA_KERNELS_CUDA_CORE &&
+        family != SPECTRA_KERNELS_TENSOR_CORE)
+        return SPECTRA_ERR_INVALID_ARG;
+    g_family.store(family, std::memory_order_relaxed);
+    return SPECTRA_OK;
+}
+
+int spectra_get_kernel_family(void) { return kernel_family(); }
 
 const char* spectra_status_string(spectra_status st)
 {
@@ -181,13 +208,13 @@ spectra_status spectra_encode(const spectra_plan* plan, const void* x, spectra_d
         if (plan->basis != SPECTRA_BASIS_RWHT || T == 0) return SPECTRA_OK;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const PathChoice pc = path_choice();
-    if (pc != PATH_GENERIC) {
+    const int fam = kernel_family();
+    if (fam != SPECTRA_KERNELS_CUDA_CORE) {
         bool done = false;
         st = launch_encode_tc(plan, x, dt, T, token_stride, codes, stream_stride_bytes, norms,
                               norms_stride, s, &done);
         if (st || done) return st;
-        if (pc == PATH_TC) return SPECTRA_ERR_UNSUPPORTED;
+        if (fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
     }
     return launch_encode_generic(plan, x, dt, T, token_stride, codes, stream_stride_bytes, norms,
                                  norms_stride, s);
@@ -206,13 +233,13 @@ spectra_status spectra_decode(const spectra_plan* plan, const uint8_t* codes, in
     }
     if (T == 0) return SPECTRA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const PathChoice pc = path_choice();
-    if (pc != PATH_GENERIC) {
+    const int fam = kernel_family();
+    if (fam != SPECTRA_KERNELS_CUDA_CORE) {
         bool done = false;
         st = launch_decode_tc(plan, codes, stream_stride_bytes, norms, norms_stride, T, x_out, out_dt,
                               token_stride, s, &done);
         if (st || done) return st;
-        if (pc == PATH_TC) return SPECTRA_ERR_UNSUPPORTED;
+        if (fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
     }
     return launch_decode_generic(plan, codes, stream_stride_bytes, norms, norms_stride, T, x_out,
                                  out_dt, token_stride, s);

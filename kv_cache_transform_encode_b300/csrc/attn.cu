@@ -322,13 +322,6 @@ int nsplit_of(int B, int Hq, int64_t ctx)
     return int((ctx + L - 1) / L);
 }
 
-// kernel family, as for encode/decode: SPECTRA_PATH=generic / tc / unset
-char attn_path()
-{
-    const char* e = getenv("SPECTRA_PATH");
-    return (e && (e[0] == 'g' || e[0] == 't')) ? e[0] : 'a';
-}
-
 }  // namespace
 
 size_t attn_tc_extra_bytes(int B, int Hkv);   // attn_tc.cu
@@ -337,12 +330,13 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
                               float scale, float* part, int nsplit, int split_len, void* extra,
                               cudaStream_t s, bool* done);
 
-void launch_combine(const PlanView& vp, const float* part, int B, int Hq, int nsplit, int code_domain, float* out,
-                    cudaStream_t s)
+spectra_status launch_combine(const PlanView& vp, const float* part, int B, int Hq, int nsplit, int code_domain,
+                              float* out, cudaStream_t s)
 {
     const size_t sm = combine_smem(vp.d, nsplit);
-    cudaFuncSetAttribute(attn_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    if (spectra_status st = set_smem(attn_combine_kernel, sm)) return st;
     attn_combine_kernel<<<B * Hq, 256, sm, s>>>(vp, part, Hq, nsplit, code_domain, out);
+    return cuda_status(cudaGetLastError());
 }
 
 // [qt (B Hq d f32) | split partials | tensor-core operands (sized for Hkv <= Hq)]
@@ -368,32 +362,30 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                            align256(sizeof(float) * size_t(B) * Hq * D));
     void* extra = reinterpret_cast<uint8_t*>(part) + align256(sizeof(float) * size_t(B) * Hq * nsplit * (D + 2));
-    if (attn_path() != 'g') {
+    const int fam = kernel_family();
+    if (fam != SPECTRA_KERNELS_CUDA_CORE) {
         bool done = false;
         spectra_status st = launch_attn_tc(kplan, vplan, q, q_dt, B, Hq, kc, vc, sstride, ctx, scale, part, nsplit,
                                            split_len, extra, s, &done);
         if (st) return st;
-        if (done) {
-            launch_combine(vp, part, B, Hq, nsplit, 1, out, s);
-            return cuda_status(cudaGetLastError());
-        }
-        if (attn_path() == 't') return SPECTRA_ERR_UNSUPPORTED;
+        if (done) return launch_combine(vp, part, B, Hq, nsplit, 1, out, s);
+        if (fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
     }
     attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt);
     dim3 grid(nsplit, Hkv, B);
     if (D == 128) {
         const size_t sm = split_smem<128>();
-        cudaFuncSetAttribute(attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        if (spectra_status st = set_smem(attn_split_kernel<128>, sm)) return st;
         attn_split_kernel<128><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
                                                           nstride, nsplit, split_len, part);
     } else {
         const size_t sm = split_smem<64>();
-        cudaFuncSetAttribute(attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        if (spectra_status st = set_smem(attn_split_kernel<64>, sm)) return st;
         attn_split_kernel<64><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
                                                          nstride, nsplit, split_len, part);
     }
-    launch_combine(vp, part, B, Hq, nsplit, 0, out, s);
-    return cuda_status(cudaGetLastError());
+    if (spectra_status st = cuda_status(cudaGetLastError())) return st;
+    return launch_combine(vp, part, B, Hq, nsplit, 0, out, s);
 }
 
 }  // namespace spectra

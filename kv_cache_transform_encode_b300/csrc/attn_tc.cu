@@ -497,9 +497,9 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
     P.vbytes = uint32_t(16 * (vplan->max_rec_bits > 0 ? vplan->max_rec_bits : 1));
     const size_t sm = tc_split_smem(P.kbytes, P.vbytes);
     if (sm > 227 * 1024) return SPECTRA_OK;
-    cudaFuncSetAttribute(attn_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(float) * D * D));
+    if (spectra_status st = set_smem(attn_tc_prep_kernel, sizeof(float) * D * D)) return st;
     attn_tc_prep_kernel<<<B * Hkv, kGmax * D, sizeof(float) * D * D, s>>>(P.kp, q, q_dt, Hq, G, scale, wimg, bias);
-    cudaFuncSetAttribute(attn_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    if (spectra_status st = set_smem(attn_tc_split_kernel, sm)) return st;
     dim3 grid(nsplit, Hkv, B);
     attn_tc_split_kernel<<<grid, kThreads, sm, s>>>(P);
     *done = true;

@@ -782,14 +782,15 @@ spectra_status launch_jacobi(const spectra_plan* plan, const float* partials, in
         // Cholesky factor); d = 64 keeps the one-block two-sided kernel
         constexpr int C = kJ1sCluster;
         const size_t sm = sizeof(float) * (2 * J1s<C>::PPC * kJ2 + kJ2 * (kJ2 + 1));
-        cudaFuncSetAttribute(jacobi1s_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-        if (C > 8) cudaFuncSetAttribute(jacobi1s_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (spectra_status st = set_smem(jacobi1s_kernel<C>, sm)) return st;
+        if (C > 8 && cudaFuncSetAttribute(jacobi1s_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1))
+            return SPECTRA_ERR_CUDA;
         jacobi1s_kernel<C><<<plan->heads * C, 32 * J1s<C>::NW, sm, s>>>(partials, nchunks, inv_n, max_sweeps,
                                                                       plan->basis_mat, plan->eigvals, plan->status,
                                                                       gram_out);
     } else {
         const size_t sm = jacobi_smem<64>();
-        cudaFuncSetAttribute(jacobi_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        if (spectra_status st = set_smem(jacobi_kernel<64>, sm)) return st;
         jacobi_kernel<64><<<plan->heads, kJacobiThreads, sm, s>>>(
             partials, nchunks, inv_n, max_sweeps, plan->basis_mat, plan->eigvals, plan->status, gram_out);
     }

@@ -218,12 +218,12 @@ spectra_status launch_encode_generic(const spectra_plan* plan, const void* x, in
     dim3 grid(unsigned((ngroups + kWarps - 1) / kWarps), plan->heads);
     if (plan->head_dim == 128) {
         const size_t sm = enc_smem<128>();
-        cudaFuncSetAttribute(encode_generic_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        if (spectra_status st = set_smem(encode_generic_kernel<128>, sm)) return st;
         encode_generic_kernel<128><<<grid, kWarps * 32, sm, s>>>(pv, x, dt, T, token_stride, codes,
                                                                  sstride, norms, nstride);
     } else {
         const size_t sm = enc_smem<64>();
-        cudaFuncSetAttribute(encode_generic_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        if (spectra_status st = set_smem(encode_generic_kernel<64>, sm)) return st;
         encode_generic_kernel<64><<<grid, kWarps * 32, sm, s>>>(pv, x, dt, T, token_stride, codes,
                                                                 sstride, norms, nstride);
     }
@@ -240,12 +240,12 @@ spectra_status launch_decode_generic(const spectra_plan* plan, const uint8_t* co
     dim3 grid(unsigned((ngroups + kDecWarps - 1) / kDecWarps), plan->heads);
     if (plan->head_dim == 128) {
         const size_t sm = dec_smem<128>();
-        cudaFuncSetAttribute(decode_generic_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        if (spectra_status st = set_smem(decode_generic_kernel<128>, sm)) return st;
         decode_generic_kernel<128><<<grid, kDecWarps * 32, sm, s>>>(pv, codes, sstride, norms, nstride, T,
                                                                  x_out, out_dt, token_stride);
     } else {
         const size_t sm = dec_smem<64>();
-        cudaFuncSetAttribute(decode_generic_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+        if (spectra_status st = set_smem(decode_generic_kernel<64>, sm)) return st;
         decode_generic_kernel<64><<<grid, kDecWarps * 32, sm, s>>>(pv, codes, sstride, norms, nstride, T,
                                                                 x_out, out_dt, token_stride);
     }

@@ -1222,7 +1222,7 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
     const bool rw = plan->basis == SPECTRA_BASIS_RWHT;
     auto kern = lm ? (rw ? encode_tc_kernel<true, true> : encode_tc_kernel<true, false>)
                    : (rw ? encode_tc_kernel<false, true> : encode_tc_kernel<false, false>);
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    if (spectra_status st = set_smem(kern, sm)) return st;
     kern<<<grid, kEncThreads, sm, s>>>(m, P);
     *done = true;
     return cuda_status(cudaGetLastError());
@@ -1261,7 +1261,7 @@ spectra_status launch_decode_tc(const spectra_plan* plan, const uint8_t* codes, 
     P.nstride = nstride;
     const uint32_t sm = total();
     auto kern = lm ? decode_tc_kernel<true> : decode_tc_kernel<false>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    if (spectra_status st = set_smem(kern, sm)) return st;
     const int grid = sched_grid(sm_count(), plan->heads, P.tiles_per_head);
     kern<<<grid, kDecThreads, sm, s>>>(m, P);
     *done = true;

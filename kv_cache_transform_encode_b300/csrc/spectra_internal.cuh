@@ -165,4 +165,16 @@ inline spectra_status cuda_status(cudaError_t e)
     return e == cudaSuccess ? SPECTRA_OK : SPECTRA_ERR_CUDA;
 }
 
+// Dynamic shared-memory opt-in of a kernel; a refused size is reported here
+// (SPECTRA_ERR_CUDA) instead of surfacing later as a launch failure.
+template <typename Kernel>
+inline spectra_status set_smem(Kernel kern, size_t bytes)
+{
+    return cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)));
+}
+
+// Kernel family chosen for encode, decode and attention (process-wide; see
+// spectra_set_kernel_family): SPECTRA_KERNELS_AUTO, _CUDA_CORE or _TENSOR_CORE.
+int kernel_family();
+
 }  // namespace spectra

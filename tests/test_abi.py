@@ -110,3 +110,18 @@ def test_no_cpu_fallback_in_binding():
     src = open(os.path.join(ROOT, "kv_cache_transform_encode_b300", "__init__.py")).read()
     assert "oracle" not in src.replace("no CPU fallback", "")
     assert "numpy" not in src
+
+
+def test_kernel_family_setting(spx):
+    """The process-wide kernel family: settable, read back, unknown values
+    refused (host logic only, no launch)."""
+    prev = spx.spectra_get_kernel_family()
+    try:
+        for f in (spx.SPECTRA_KERNELS_CUDA_CORE, spx.SPECTRA_KERNELS_TENSOR_CORE, spx.SPECTRA_KERNELS_AUTO):
+            spx.spectra_set_kernel_family(f)
+            assert spx.spectra_get_kernel_family() == f
+        assert spx.lib().spectra_set_kernel_family(3) == 1
+        assert spx.lib().spectra_set_kernel_family(-1) == 1
+        assert spx.spectra_get_kernel_family() == spx.SPECTRA_KERNELS_AUTO
+    finally:
+        spx.spectra_set_kernel_family(prev)

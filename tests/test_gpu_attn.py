@@ -11,13 +11,18 @@ from parity import ATTN_TOL, gpu_plan, rel_l2
 
 pytestmark = pytest.mark.gpu
 
+FAMILY = {"tc": 2, "generic": 1}
+
 
 @pytest.fixture(params=["tc", "generic"])
-def path(request, monkeypatch):
+def path(request):
     """Kernel family for uniform-quantizer eigenbasis plans: the tensor-core
     kernels (required) or the CUDA-core kernels."""
-    monkeypatch.setenv("SPECTRA_PATH", request.param)
-    return request.param
+    import kv_cache_transform_encode_b300 as spx
+    prev = spx.spectra_get_kernel_family()
+    spx.spectra_set_kernel_family(FAMILY[request.param])
+    yield request.param
+    spx.spectra_set_kernel_family(prev)
 
 
 @pytest.fixture(scope="module")
@@ -115,11 +120,19 @@ def test_attn_peaky_scores(spx, orc, path):
     assert rel_l2(got, want) <= ATTN_TOL
 
 
-def test_attn_full_layer_sampled(spx, orc, monkeypatch):
+@pytest.fixture
+def tc_only():
+    import kv_cache_transform_encode_b300 as spx
+    prev = spx.spectra_get_kernel_family()
+    spx.spectra_set_kernel_family(FAMILY["tc"])
+    yield
+    spx.spectra_set_kernel_family(prev)
+
+
+def test_attn_full_layer_sampled(spx, orc, tc_only):
     """The benchmark's attention launch (1 x 32 query heads over 8 kv heads,
     32768 tokens at 2.0 bits/value) on the tensor-core kernels; the oracle's
     fp64 attention checked on the query heads of kv heads 0 and 5."""
-    monkeypatch.setenv("SPECTRA_PATH", "tc")
     B, Hq, Hkv, ctx = 1, 32, 8, 32768
     kx = [synth.to_bf16_exact(synth.spiked_t(31, ctx, Hkv, 128, role=synth.ROLE_K)).astype(np.float64)]
     vx = [synth.to_bf16_exact(synth.spiked_t(31, ctx, Hkv, 128, role=synth.ROLE_V)).astype(np.float64)]
@@ -156,3 +169,75 @@ def test_attn_empty_context(spx, orc):
     spx.spectra_attn_decode(gk, gv, torch.zeros((1, 4, 128), device="cuda"), codes, codes, 0, 1.0, out)
     torch.cuda.synchronize()
     assert out.abs().max().item() == 0.0
+
+
+def _single_head_cache(seed, ctx, role):
+    return synth.to_bf16_exact(synth.spiked_t(seed, ctx, 1, 128, role=role))[:, 0, :].astype(np.float64)
+
+
+def _batched_case(spx, orc, B, Hq, Hkv, ctx, checked, seed=71, B_bits=2.0, quant=0):
+    """Plans per kv head from their own first 2048 tokens; the streams of the
+    (batch, kv head) pairs in `checked` hold oracle-encoded synthetic caches,
+    every other stream seeded random code words (every bit pattern is a valid
+    code, so the kernels do the full work everywhere).  Returns the device
+    output and, for each checked pair, the oracle's reconstruction."""
+    cal_k = np.stack([_single_head_cache(seed * 100 + h, 2048, synth.ROLE_K) for h in range(Hkv)], 1)
+    cal_v = np.stack([_single_head_cache(seed * 100 + h, 2048, synth.ROLE_V) for h in range(Hkv)], 1)
+    kp = orc.make_eigen_plan(cal_k, B_bits, quant)
+    vp = orc.make_eigen_plan(cal_v, B_bits, quant)
+    sb = max(orc.stream_bytes(ctx, int(kp.rec_bits().max())), orc.stream_bytes(ctx, int(vp.rec_bits().max())), 16)
+    g = np.random.default_rng(seed)
+    ks = g.integers(0, 256, (B * Hkv, sb), dtype=np.uint8)
+    vs = g.integers(0, 256, (B * Hkv, sb), dtype=np.uint8)
+    rec = {}
+    for (b, h) in checked:
+        xk = _single_head_cache(seed * 1000 + 17 * b + h, ctx, synth.ROLE_K)
+        xv = _single_head_cache(seed * 1000 + 17 * b + h, ctx, synth.ROLE_V)
+        ek, ev = orc.encode_head(kp, h, xk), orc.encode_head(vp, h, xv)
+        ks[b * Hkv + h] = 0
+        vs[b * Hkv + h] = 0
+        ks[b * Hkv + h, : len(ek["stream"])] = ek["stream"]
+        vs[b * Hkv + h, : len(ev["stream"])] = ev["stream"]
+        rec[(b, h)] = (orc.decode_head(kp, h, ek["stream"], ctx), orc.decode_head(vp, h, ev["stream"], ctx))
+    # tails of random streams past the last token are never read; the
+    # oracle-encoded ones are zero-padded like the library's
+    q = synth.to_bf16_exact(synth.queries(seed, B, Hq, 128))
+    gk, gv = gpu_plan(spx, kp), gpu_plan(spx, vp)
+    out = torch.zeros((B, Hq, 128), device="cuda")
+    spx.spectra_attn_decode(gk, gv, torch.from_numpy(q).to(torch.bfloat16).cuda(), torch.from_numpy(ks).cuda(),
+                            torch.from_numpy(vs).cuda(), ctx, 1.0, out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), q, rec
+
+
+def _check_batched(orc, got, q, rec, Hq, Hkv):
+    G = Hq // Hkv
+    for (b, h), (kr, vr) in rec.items():
+        for j in range(G):
+            want = orc.attention(q[b, h * G + j].astype(np.float64), kr, vr, 1.0)
+            err = rel_l2(got[b, h * G + j], want)
+            assert err <= ATTN_TOL, ((b, h, j), err)
+
+
+def test_attn_batched_many_splits(spx, orc, path):
+    """Batch 8 x 32 query heads over 8 kv heads (256 (batch, query head)
+    pairs, the long-split branch), 8192 + 37 tokens: five context splits
+    with a ragged last one, merged per query head; checked on the query heads
+    of four (batch, kv head) pairs."""
+    B, Hq, Hkv, ctx = 8, 32, 8, 8192 + 37
+    checked = [(0, 0), (3, 5), (7, 7), (5, 2)]
+    got, q, rec = _batched_case(spx, orc, B, Hq, Hkv, ctx, checked)
+    _check_batched(orc, got, q, rec, Hq, Hkv)
+
+
+def test_attn_compressed_attention_workload_sampled(spx, orc):
+    """The compressed-attention workload the benchmark times, at full size:
+    batch 16, 32 query heads over 8 kv heads, 65536-token context at 2.0
+    bits/value, on the default kernel family; the oracle's fp64 attention
+    over its own reconstruction checked on three (batch, kv head) pairs
+    (12 query heads), the other streams random code words."""
+    B, Hq, Hkv, ctx = 16, 32, 8, 65536
+    checked = [(0, 0), (15, 5), (7, 3)]
+    got, q, rec = _batched_case(spx, orc, B, Hq, Hkv, ctx, checked, seed=73)
+    _check_batched(orc, got, q, rec, Hq, Hkv)
+    assert np.all(np.isfinite(got))

@@ -14,14 +14,19 @@ from parity import (ATTN_TOL, BAND_SIGMA, FLIP_FRAC, REC_TOL, bf16, compare_code
 
 pytestmark = pytest.mark.gpu
 
+FAMILY = {"tc": 2, "generic": 1}
+
 
 @pytest.fixture(params=["tc", "generic"])
-def path(request, monkeypatch):
+def path(request):
     """Kernel family for bf16 head_dim-128 encode/decode: the tensor-core
     kernels (required: a call they do not cover fails) or the CUDA-core
     kernels."""
-    monkeypatch.setenv("SPECTRA_PATH", request.param)
-    return request.param
+    import kv_cache_transform_encode_b300 as spx
+    prev = spx.spectra_get_kernel_family()
+    spx.spectra_set_kernel_family(FAMILY[request.param])
+    yield request.param
+    spx.spectra_set_kernel_family(prev)
 
 
 @pytest.fixture(scope="module")
@@ -238,7 +243,30 @@ def test_end_to_end_device_plan(spx, orc, path):
     torch.cuda.synchronize()
     assert np.all(p.status.cpu().numpy() >= 0)
     bits = p.bits.cpu().numpy()
-    assert (bits != oplan.bits).sum() <= 8
+    lam_g = p.eigvals.cpu().numpy().astype(np.float64)
+    R = orc.total_bits(2.0, 128)
+    for h in range(8):
+        # bit-exact on the device's own eigenvalues ...
+        assert np.array_equal(bits[h], orc.alloc(lam_g[h], R)), h
+        # ... and every width that differs from the oracle's end-to-end plan
+        # sits at a near-tie of the greedy order: the one-bit step one side
+        # took and the other did not has a key lam_c 4^-j within the two
+        # sides' eigenvalue difference of the cut between taken and untaken
+        # keys (reported in the message)
+        lam_o = oplan.eigvals[h]
+        keys = np.sort(np.concatenate([np.maximum(lam_o, 0) * 4.0 ** -j for j in range(8)]))[::-1]
+        cut = np.sqrt(keys[R - 1] * keys[R])
+        for c in np.nonzero(bits[h] != oplan.bits[h])[0]:
+            j = int(min(bits[h, c], oplan.bits[h, c]))
+            margin = abs(np.log(lam_o[c] * 4.0 ** -j / cut))
+            # channels whose last taken or first untaken key sits near the cut
+            lo = np.maximum(lam_o, 1e-30) * 4.0 ** -oplan.bits[h].astype(float)
+            near = (np.abs(np.log(4 * lo / cut)) < 0.05) | (np.abs(np.log(lo / cut)) < 0.05)
+            lam_err = np.max(np.abs(np.log(np.maximum(lam_g[h][near | (np.arange(128) == c)], 1e-30)
+                                           / np.maximum(lam_o[near | (np.arange(128) == c)], 1e-30))))
+            assert margin <= 2 * lam_err + 1e-6, (h, c, bits[h, c], oplan.bits[h, c], margin, lam_err)
+            print(f"head {h} channel {c}: width {bits[h, c]} vs {oplan.bits[h, c]}, "
+                  f"relative distance to the greedy cut {margin:.2e} (eigenvalue difference {lam_err:.2e})")
     xo = orc.decode(oplan, [e["stream"] for e in orc.encode(oplan, x64)], 4096)
     e_gpu, e_orc = orc.relmse(x64, out.cpu().numpy()), orc.relmse(x64, xo)
     assert abs(e_gpu - e_orc) <= 0.05 * e_orc, (e_gpu, e_orc)
@@ -291,3 +319,57 @@ def test_codec_full_size_sampled(spx, orc, path):
         want = synth.to_bf16_exact(xh.astype(np.float32))
         assert rel_l2(outn[idx, h, :], want) <= REC_TOL
     assert flips <= FLIP_FRAC * total, (flips, total)
+
+
+# ---------------------------------------------------------------- device status words
+@pytest.mark.parametrize("case", ["tiny", "llama"])
+def test_calibrate_not_converged_status(spx, case):
+    """One Jacobi sweep cannot converge on these spectra: every head reports
+    -SPECTRA_ERR_NOT_CONVERGED through plan.status (no trap, no hang), and the
+    next call with the default sweep budget converges on the same plan."""
+    if case == "tiny":
+        _, xd, _ = tiny_case()
+        n = 128
+    else:
+        _, xd, _ = llama_case(T=2048)
+        n = 2048
+    H, d = xd.shape[1], xd.shape[2]
+    p = spx.Plan(H, d)
+    spx.spectra_calibrate(p, xd, n_cal=n, max_sweeps=1)
+    torch.cuda.synchronize()
+    assert np.all(p.status.cpu().numpy() == -4), p.status.cpu().numpy()
+    spx.spectra_calibrate(p, xd, n_cal=n)
+    torch.cuda.synchronize()
+    assert np.all(p.status.cpu().numpy() > 0)
+
+
+def test_buffer_status(spx, orc, path):
+    """A head whose record is longer than plan.max_rec_bits (the bound the
+    streams were sized by) is refused on the device: plan_finalize and the
+    encode report -SPECTRA_ERR_BUFFER for it and write none of its codes; the
+    other head is encoded and decoded normally."""
+    T = 300
+    x, xd, x64 = llama_case(T=T, H=2)
+    oplan = orc.make_eigen_plan(x64, 2.0)
+    oplan.bits[1] = np.minimum(oplan.bits[1], 1)
+    R1 = int(oplan.rec_bits()[1])
+    assert R1 < int(oplan.rec_bits()[0])
+    p = gpu_plan(spx, oplan)
+    p.max_rec_bits = R1
+    spx.spectra_plan_finalize(p)
+    torch.cuda.synchronize()
+    st = p.status.cpu().numpy()
+    assert st[0] == -7 and st[1] >= 0, st
+    codes = p.new_streams(T)
+    spx.spectra_encode(p, xd, codes)
+    out = torch.full((T, 2, 128), 5.0, device="cuda")
+    spx.spectra_decode(p, codes, T, out)
+    torch.cuda.synchronize()
+    st = p.status.cpu().numpy()
+    assert st[0] == -7 and st[1] >= 0, st
+    cc = codes.cpu().numpy()
+    assert not cc[0].any()
+    enc = orc.encode_head(oplan, 1, x64[:, 1, :])
+    compare_codes(orc, oplan, 1, enc, cc[1], T)
+    want = orc.decode_head(oplan, 1, enc["stream"], T)
+    assert rel_l2(out[:, 1, :].cpu().numpy(), want) <= 5 * REC_TOL
