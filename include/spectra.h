@@ -271,11 +271,19 @@ SPECTRA_API spectra_status spectra_attn_decode(const spectra_plan* kplan, const 
  *   exits.  A call whose spectra_attn_workspace_bytes(B, Hq, d, ctx) exceeds
  *   it returns SPECTRA_ERR_UNSUPPORTED and launches nothing.  Nothing in the
  *   array needs clearing between calls.
+ * Arguments are checked exactly as by spectra_attn_decode (same statuses);
+ *   then a call whose spectra_attn_workspace_bytes(B, Hq, d, ctx) exceeds
+ *   the array returns SPECTRA_ERR_UNSUPPORTED (ctx == 0 needs no scratch).
  * The first call on a device looks up the array's device address and caches
- *   it (make that first call before any stream capture).  Every call shares
- *   the one array: calls whose kernels overlap on the GPU race on it.
- * This call allocates nothing (no cudaMalloc / cudaFree, no allocating
- *   library routine).
+ *   it.  CUDA may load the library's device code lazily, so that first call
+ *   can be the moment the array is created on the device: make it at
+ *   start-up, outside any allocator callback and before any stream capture
+ *   (a call refused for its size still does the lookup).  The cached address
+ *   assumes the device's context lasts as long as the process (no
+ *   cudaDeviceReset in between).  Every call shares the one array: calls
+ *   whose kernels overlap on the GPU race on it.
+ * After that first call on a device, this call allocates nothing (no
+ *   cudaMalloc / cudaFree, no allocating library routine).
  */
 #define SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 SPECTRA_API spectra_status spectra_attn_decode_noalloc(const spectra_plan* kplan, const spectra_plan* vplan,

@@ -86,6 +86,27 @@ int family_from_env()
 
 }  // namespace
 
+spectra_status spectra::attn_validate(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
+                                      int q_dt, int B, int Hq, const uint8_t* k_codes, const uint8_t* v_codes,
+                                      int64_t stream_stride_bytes, const float* k_norms, const float* v_norms,
+                                      int64_t norms_stride, int64_t ctx, float softmax_scale, const float* out)
+{
+    spectra_status st;
+    if ((st = check_plan(kplan, true))) return st;
+    if ((st = check_plan(vplan, true))) return st;
+    if (kplan->heads != vplan->heads || kplan->head_dim != vplan->head_dim) return SPECTRA_ERR_INVALID_ARG;
+    const int Hkv = kplan->heads;
+    if (B <= 0 || Hq <= 0 || Hq % Hkv != 0 || ctx < 0) return SPECTRA_ERR_INVALID_ARG;
+    if (!q || !out || !valid_dtype(q_dt) || !isfinite(softmax_scale)) return SPECTRA_ERR_INVALID_ARG;
+    if ((st = check_streams(kplan, k_codes, stream_stride_bytes, ctx, int64_t(B) * Hkv))) return st;
+    if ((st = check_streams(vplan, v_codes, stream_stride_bytes, ctx, int64_t(B) * Hkv))) return st;
+    if (kplan->basis == SPECTRA_BASIS_RWHT && ctx > 0 && (!k_norms || norms_stride < ctx))
+        return SPECTRA_ERR_INVALID_ARG;
+    if (vplan->basis == SPECTRA_BASIS_RWHT && ctx > 0 && (!v_norms || norms_stride < ctx))
+        return SPECTRA_ERR_INVALID_ARG;
+    return SPECTRA_OK;
+}
+
 int spectra::kernel_family()
 {
     int f = g_family.load(std::memory_order_relaxed);
@@ -258,19 +279,10 @@ spectra_status spectra_attn_decode(const spectra_plan* kplan, const spectra_plan
                                    int64_t ctx, float softmax_scale, float* out, void* workspace,
                                    size_t workspace_bytes, spectra_stream_t stream)
 {
-    spectra_status st;
-    if ((st = check_plan(kplan, true))) return st;
-    if ((st = check_plan(vplan, true))) return st;
-    if (kplan->heads != vplan->heads || kplan->head_dim != vplan->head_dim) return SPECTRA_ERR_INVALID_ARG;
-    const int Hkv = kplan->heads, d = kplan->head_dim;
-    if (B <= 0 || Hq <= 0 || Hq % Hkv != 0 || ctx < 0) return SPECTRA_ERR_INVALID_ARG;
-    if (!q || !out || !valid_dtype(q_dt) || !isfinite(softmax_scale)) return SPECTRA_ERR_INVALID_ARG;
-    if ((st = check_streams(kplan, k_codes, stream_stride_bytes, ctx, int64_t(B) * Hkv))) return st;
-    if ((st = check_streams(vplan, v_codes, stream_stride_bytes, ctx, int64_t(B) * Hkv))) return st;
-    if (kplan->basis == SPECTRA_BASIS_RWHT && ctx > 0 && (!k_norms || norms_stride < ctx))
-        return SPECTRA_ERR_INVALID_ARG;
-    if (vplan->basis == SPECTRA_BASIS_RWHT && ctx > 0 && (!v_norms || norms_stride < ctx))
-        return SPECTRA_ERR_INVALID_ARG;
+    spectra_status st = attn_validate(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes,
+                                      k_norms, v_norms, norms_stride, ctx, softmax_scale, out);
+    if (st) return st;
+    const int d = kplan->head_dim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (ctx == 0)
         return cuda_status(cudaMemsetAsync(out, 0, sizeof(float) * size_t(B) * Hq * d, s));

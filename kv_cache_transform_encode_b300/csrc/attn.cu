@@ -23,7 +23,6 @@ namespace spectra {
 
 namespace {
 
-constexpr int kSplitLen = 2048;     // tokens per context split
 constexpr int kTile = 64;           // tokens per tile (two bit-plane groups)
 constexpr int kThreads = 256;
 constexpr int kMaxGroup = 8;        // query heads per kv head
@@ -313,12 +312,22 @@ size_t split_smem()
            sizeof(int) * 4 * D + sizeof(uint32_t) * 2 * 2 * 8 * D;
 }
 
-// context split length: 2048 tokens, or 1024 when few (batch, query head)
-// pairs would leave SMs idle
-int split_len_of(int B, int Hq) { return (int64_t(B) * Hq >= 256) ? kSplitLen : kSplitLen / 2; }
+// Context split length, a multiple of 256 tokens (the tensor-core tile):
+// about 2048 blocks over the (batch, kv head) pairs -- counted as one kv
+// head per four query heads, so the size of the workspace depends on
+// (B, Hq, ctx) alone -- and at least 1024 tokens per split.
+int split_len_of(int B, int Hq, int64_t ctx)
+{
+    const int64_t pairs = (int64_t(B) * Hq + 3) / 4;
+    int64_t L = (ctx * pairs + 2047) / 2048;
+    L = (L + 255) / 256 * 256;
+    if (L < 1024) L = 1024;
+    if (L > (int64_t(1) << 30)) L = int64_t(1) << 30;
+    return int(L);
+}
 int nsplit_of(int B, int Hq, int64_t ctx)
 {
-    const int L = split_len_of(B, Hq);
+    const int64_t L = split_len_of(B, Hq, ctx);
     return int((ctx + L - 1) / L);
 }
 
@@ -357,7 +366,7 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
     if (Hq / Hkv > kMaxGroup) return SPECTRA_ERR_UNSUPPORTED;
     const PlanView kp = make_view(kplan), vp = make_view(vplan);
     const int nsplit = nsplit_of(B, Hq, ctx);
-    const int split_len = split_len_of(B, Hq);
+    const int split_len = split_len_of(B, Hq, ctx);
     float* qt = static_cast<float*>(ws);
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                            align256(sizeof(float) * size_t(B) * Hq * D));

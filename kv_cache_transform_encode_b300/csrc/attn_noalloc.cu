@@ -9,8 +9,13 @@
 // is part of the library image, so the call itself allocates nothing.
 //
 // The first call on each device looks up the array's device address
-// (cudaGetSymbolAddress, with that device current) and caches it; make that
-// first call before any stream capture.
+// (cudaGetSymbolAddress, with that device current) and caches it.  CUDA may
+// load this file's module lazily, so that first lookup can be the moment
+// the array is created on the device: make the first call on each device at
+// start-up, outside any allocator callback and before any stream capture
+// (a call that is refused for its size still does the lookup).  Every later
+// call allocates nothing.  The cached address assumes the device's context
+// lives as long as the process (no cudaDeviceReset in between).
 //
 // The array (SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES) is created with the
 // library's module on every GPU that loads it and stays resident until the
@@ -57,12 +62,17 @@ extern "C" spectra_status spectra_attn_decode_noalloc(
     const float* k_norms, const float* v_norms, int64_t norms_stride, int64_t ctx,
     float softmax_scale, float* out, spectra_stream_t stream)
 {
-    if (!kplan || !vplan) return SPECTRA_ERR_INVALID_ARG;
-    const size_t need = spectra_attn_workspace_bytes(B, Hq, kplan->head_dim, ctx);
-    if (need > size_t(SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES)) return SPECTRA_ERR_UNSUPPORTED;
-    void* scratch = nullptr;
-    const spectra_status st = scratch_address(&scratch);
+    // the same argument checks, in the same order, as spectra_attn_decode
+    spectra_status st = spectra::attn_validate(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes,
+                                               stream_stride_bytes, k_norms, v_norms, norms_stride, ctx,
+                                               softmax_scale, out);
     if (st != SPECTRA_OK) return st;
+    void* scratch = nullptr;
+    if ((st = scratch_address(&scratch)) != SPECTRA_OK) return st;
+    if (ctx > 0) {   // an empty context only zeroes `out` and needs no scratch
+        const size_t need = spectra_attn_workspace_bytes(B, Hq, kplan->head_dim, ctx);
+        if (need > size_t(SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES)) return SPECTRA_ERR_UNSUPPORTED;
+    }
     return spectra_attn_decode(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes,
                                k_norms, v_norms, norms_stride, ctx, softmax_scale, out, scratch,
                                size_t(SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES), stream);

@@ -1,138 +1,110 @@
 // attn_tc.cu -- decode-step attention over packed K/V streams on the tensor
-// cores (uniform quantizer, eigenbasis plans, head_dim 128, at most four
-// query heads per kv head).
+// cores, computed on the bit planes themselves (uniform quantizer,
+// eigenbasis plans, head_dim 128, at most four query heads per kv head).
 //
 // "Sintesi Tecnica: SPECTRA", "Significato e Rivendicazioni": attention
 // computed directly in the latent space.  With the uniform quantizer a
-// latent coordinate is yhat_c = (Delta_c / 2)(2 code_c + 1 - 2^b_c), affine
-// in the code: with z = code - 2^(b-1) (an exact small integer),
-// yhat_c = Delta_c (z_c + 1/2), so
-//   s_j(t) = sum_c qt_jc yhat_c(t) = sum_c W_jc z_c(t) + K0_j,
-//   W_jc = qt_jc Delta_c,   K0_j = (1/2) sum_c W_jc,
-//   sum_t p_j(t) yhat_c(t) = Delta_c (sum_t p_j(t) z_c(t) + l_j / 2),
-// and both contractions run on the small integers z.  A code enters the
-// tensor core as the fp16 number z: the byte-permute trick gives 1024 +
-// code exactly, one packed subtraction of 1024 + 2^(b-1) leaves z, so the
-// fp32 accumulators only ever hold sums of small terms.  W and P enter as
-// fp16 hi + lo pairs (22 significand bits), so the products carry
-// fp32-grade accuracy.
+// latent coordinate is yhat_c = Delta_c (code_c - 2^(b-1) + 1/2), and a code
+// is the sum of its bit planes, code_c = sum_k 2^k bit_{c,k}.  So with plane
+// r = (c, k) of the stream (the stream's own word order, o_c + k),
+//   s_j(t) = sum_c qt_jc yhat_c(t) = sum_r V_jr bit_r(t) + C_j,
+//     V_jr = qt_jc Delta_c 2^k,   C_j = sum_c qt_jc Delta_c (1/2 - 2^(b_c-1)),
+//   sum_t p_j(t) code_c(t) = sum_k 2^k S_{j,(c,k)},  S_jr = sum_t p_j(t) bit_r(t),
+// and both contractions are products of a 0/1 matrix -- the packed words
+// exactly as stored -- with dense fp16 operands.  No code is ever unpacked.
 //
-// One CTA per (context split, kv head, batch).  Per 128-token tile:
-//  1. the tile's K and V code words arrive in shared memory (cp.async,
-//     double-buffered);
-//  2. eight warps unpack them (per side, warp = 32-token group, lane =
-//     channel, over four blocks of 32 channels: the bit-plane words of a
-//     group become 32 code bytes through four 8x8 bit transposes, or, where
-//     a block is at most 2 bits wide, the two planes are interleaved into
-//     even- and odd-token words and each fp16 pair is one shift and one
-//     mask), into fp16 tiles L[c][p]; within a 32-token group position
-//     2s holds token s and 2s + 1 token s + 16;
-//  3. each warp then owns 16 tokens of the tile end to end: scores by
-//     mma.sync m16n8k16 (A = L_K^T via ldmatrix.trans, B = [W_hi; W_lo],
-//     n = head, hi/lo), an online softmax over its own slice (its running
-//     max and sum per head in registers), and P V (A = L_V, channels x the
-//     slice's tokens, B = [P_hi; P_lo]) into its own accumulators for all
-//     128 channels.  Two block barriers per tile (codes landed, tiles
-//     unpacked); the eight slices merge in shared memory at the end.
-// The split's (m, l, sum_t p z) go to the workspace; the combine kernel
-// of attn.cu merges splits, dequantizes and rotates by the V basis.
+// A bit enters the tensor core as an fp16 number by masking: a 32-bit word
+// ANDed with (1 << p) | (1 << (p + 16)) is a pair of fp16 values, each either
+// 0 or the value of the lone bit p -- 2^(p-24) (a subnormal) for p <= 9, a
+// power of two for the exponent bits p = 10..14.  Bit 15 (the sign) is
+// ORed with 1.0, giving 1 - 2 bit.  Every row of a product then carries one
+// known per-position factor, removed after the MMA (scores) or folded into
+// the other operand beforehand (P V).
+//
+//  * Scores (per 32-token group, one warp): m16n8k16 with M = 16 tokens,
+//    K = 16 planes, N = 8 = 4 query heads x (hi, lo) fp16 halves of V.  An A
+//    register holds two planes of one token: the two plane words are merged
+//    by one byte permute (low halves or high halves), then each register is
+//    one mask.  Row p of the tile is token p of the half-group, scaled by
+//    1 / value(bit p).
+//  * P V: m16n8k16 with M = 16 planes, K = 16 tokens, N = 8 = heads x (hi,
+//    lo) of P.  An A register holds one plane of two tokens, s and s + 16,
+//    straight from one stream word: one mask (bits 0..7) or one shift and a
+//    mask (bits 8..15, taken from the word shifted right by 8).  The token
+//    at position p then enters as 2^(p-24); P carries 2^(9-p) instead of 1,
+//    so every product is bit * p * 2^-15.
+//
+// One CTA (8 warps) per (context split, kv head, batch).  Tiles of 256
+// tokens (one 32-token group per warp) arrive by bulk copy (the group
+// records of K and V, 32 R bytes each) into a ring of shared-memory stages.
+// Per tile: each warp scores its group over all K planes; the block takes
+// the running maximum per head (barrier 1); each warp writes its tokens'
+// probabilities as fp16 hi/lo pairs (barrier 2); each warp then accumulates
+// P V for its own slice of the V planes (m-tiles w, w + 8, ...) over the
+// whole tile.  The split's (m, l, sum_t p z) per head go to the workspace
+// (z = code - 2^(b-1)); the combine kernel of attn.cu merges splits,
+// dequantizes and rotates by the V basis.
 #include "spectra_internal.cuh"
+#include "tc_common.cuh"
 
 #include <cuda_fp16.h>
 #include <math.h>
+
+#include <type_traits>
 
 namespace spectra {
 
 namespace {
 
+using namespace tc;
+
 constexpr int D = 128;
-constexpr int TT = 128;                  // tokens per tile
-constexpr int LROW = TT * 2 + 16;        // bytes per L row (padded: conflict-free ldmatrix)
-constexpr int kThreads = 256;
-constexpr int kGmax = 4;                 // query heads per kv head
-constexpr int PROW = 24;                 // halves per row of a warp's P tile (conflict-free B loads)
+constexpr int kGmax = 4;                  // query heads per kv head
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int TT = 32 * kWarps;           // tokens per tile: one group per warp
+constexpr int kMaxStages = 4;
+constexpr int PSTR = 24;                  // u32 per (group, column) row of the P tile
+constexpr int kImgKb = 8 * D / 16;        // k-blocks of the score weights at the widest record
+constexpr uint32_t kImgBytesPerHead = kImgKb * 32 * 8;
+constexpr uint64_t kWaitNs = 2000000000ull;
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void transpose8(uint32_t& lo, uint32_t& hi)
-{
-    uint32_t t;
-    t = (lo ^ (lo >> 7)) & 0x00AA00AAu;  lo ^= t ^ (t << 7);
-    t = (hi ^ (hi >> 7)) & 0x00AA00AAu;  hi ^= t ^ (t << 7);
-    t = (lo ^ (lo >> 14)) & 0x0000CCCCu; lo ^= t ^ (t << 14);
-    t = (hi ^ (hi >> 14)) & 0x0000CCCCu; hi ^= t ^ (t << 14);
-    t = (lo ^ (hi << 4)) & 0xF0F0F0F0u;  lo ^= t;  hi ^= t >> 4;
-}
-
-__device__ __forceinline__ uint32_t gather_byte(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int k)
-{
-    const uint32_t sel = ((4u + k) << 4) | uint32_t(k);
-    return __byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410);
-}
-
-// bit planes of one channel for a 32-token group -> 32 code bytes
-__device__ __forceinline__ void planes_to_codes(const uint32_t* words, int o, int b, int bmax, uint32_t (&X)[8])
-{
-    uint32_t pl[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) pl[k] = (k < bmax && k < b) ? words[o + k] : 0u;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        X[2 * m] = gather_byte(pl[0], pl[1], pl[2], pl[3], m);
-        X[2 * m + 1] = gather_byte(pl[4], pl[5], pl[6], pl[7], m);
-        transpose8(X[2 * m], X[2 * m + 1]);
-    }
-}
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-// D (16x8 f32) = A (16x16 f16, row) * B (16x8 f16, col) + C
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
-                                         const float (&c)[4])
+// D (16x8 f32) += A (16x16 f16, row) * B (16x8 f16, col)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%10, %11, %12, %13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
-          "f"(c[3]));
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // ------------------------------------------------------------------ prep
-// Per (batch, kv head): qt_j = scale * B_K^T q_j, W_jc = qt_jc Delta_c as fp16
-// hi/lo rows ([8][D]: rows 0..3 hi, 4..7 lo; heads >= G zero), the sums of
-// each row over every 16-channel chunk (the 1024 offsets removed per MMA
-// step), and K0_j.
+// Per (batch, kv head): qt_j = scale * B_K^T q_j; W_jc = qt_jc Delta_c;
+// the score weights V_jr = W_jc 2^k of every plane r = (c, k) as fp16 hi and
+// lo parts, laid out as the m16n8k16 B fragments of each 16-plane k-block
+// ([kb][lane][b0, b1], column n = 2 j + (0 hi, 1 lo), zero for planes past
+// the record and for heads >= G); bias[8] = {C_0..3, sum_r V_0r..V_3r}
+// (the sums taken over the fp16 parts exactly as the MMA sees them).
 __global__ void __launch_bounds__(kGmax * D)
 attn_tc_prep_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, int G, float scale,
-                    __half* __restrict__ wimg, float* __restrict__ bias)
+                    uint32_t* __restrict__ img, float* __restrict__ bias)
 {
     const int bh = blockIdx.x, Hkv = kp.heads, h = bh % Hkv, b = bh / Hkv;
     const int tid = threadIdx.x, c = tid % D, j = tid / D;   // channel, query head of the group
-    extern __shared__ float Bs[];                 // [D][D] basis of head h (staged: coalesced 16-B loads)
+    extern __shared__ float Bs[];                 // [D][D] basis of head h
     __shared__ float qs[kGmax][D];
-    __shared__ float red[kGmax][4];
+    __shared__ float red[2][kGmax][4];
+    const int R = min(kp.rec_bits[h], kp.max_rec_bits);
+    const int nkb = (max(R, 1) + 15) / 16;
+    uint32_t* im = img + size_t(bh) * (kImgBytesPerHead / 4);
+    for (int e = tid; e < nkb * 64; e += kGmax * D) im[e] = 0u;
     {
         const float4* src = reinterpret_cast<const float4*>(kp.basis_mat + size_t(h) * D * D);
         float4* dst = reinterpret_cast<float4*>(Bs);
@@ -144,36 +116,74 @@ attn_tc_prep_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, i
 #pragma unroll 8
     for (int i = 0; i < D; ++i) qt = fmaf(Bs[i * D + c], qs[j][i], qt);
     const int bits = kp.bits[size_t(h) * D + c];
+    const int off = kp.chan_off[size_t(h) * D + c];
     const float delta = kp.rscale[size_t(h) * D + c];
-    __half* wr = wimg + size_t(bh) * 8 * D;
-    const float qj = qt * scale;
-    const float w = (bits > 0 && j < G) ? qj * delta : 0.f;
-    const __half hi = __float2half_rn(w);
-    const __half lo = __float2half_rn(w - __half2float(hi));
-    wr[j * D + c] = hi;
-    wr[(kGmax + j) * D + c] = lo;
-    // yhat = Delta (z + 1/2): the 1/2 terms of the score, summed over channels
-    float k0 = 0.5f * w;
-    for (int o = 16; o; o >>= 1) k0 += __shfl_xor_sync(0xffffffffu, k0, o);
-    if ((c & 31) == 0) red[j][c >> 5] = k0;
+    const float w = (bits > 0 && j < G && kp.rec_bits[h] <= kp.max_rec_bits) ? qt * scale * delta : 0.f;
+    float cj = (bits > 0) ? w * (0.5f - float(1 << (bits - 1))) : 0.f;
+    float vs = 0.f;
+    __half* ih = reinterpret_cast<__half*>(im);
+    for (int k = 0; k < bits && w != 0.f; ++k) {
+        const float v = w * float(1 << k);
+        const __half hi = __float2half_rn(v);
+        const __half lo = __float2half_rn(v - __half2float(hi));
+        vs += __half2float(hi) + __half2float(lo);
+        const int r = off + k, kb = r >> 4, kk = r & 15;
+        const int reg = kk >> 3, tg = (kk & 7) >> 1, hf = kk & 1;
+        const int lane_hi = (2 * j) * 4 + tg, lane_lo = (2 * j + 1) * 4 + tg;
+        ih[((kb * 32 + lane_hi) * 2 + reg) * 2 + hf] = hi;
+        ih[((kb * 32 + lane_lo) * 2 + reg) * 2 + hf] = lo;
+    }
+    for (int o = 16; o; o >>= 1) {
+        cj += __shfl_xor_sync(0xffffffffu, cj, o);
+        vs += __shfl_xor_sync(0xffffffffu, vs, o);
+    }
+    if ((c & 31) == 0) {
+        red[0][j][c >> 5] = cj;
+        red[1][j][c >> 5] = vs;
+    }
     __syncthreads();
-    if (tid < kGmax) bias[size_t(bh) * kGmax + tid] = red[tid][0] + red[tid][1] + red[tid][2] + red[tid][3];
+    if (tid < 2 * kGmax) {
+        const int which = tid / kGmax, jj = tid % kGmax;
+        bias[size_t(bh) * 8 + tid] = red[which][jj][0] + red[which][jj][1] + red[which][jj][2] + red[which][jj][3];
+    }
 }
 
 // ------------------------------------------------------------------ split
 struct AttnTcParams {
     PlanView kp, vp;
-    int Hq, G, nsplit, split_len;
+    int Hq, G, nsplit, split_len, stages;
     int64_t ctx;
     const uint8_t* kc;
     const uint8_t* vc;
     int64_t sstride;
-    const __half* wimg;
+    const uint32_t* img;
     const float* bias;
     float* part;
-    uint32_t kbytes, vbytes;   // code-word bytes of one tile (16 R)
+    uint32_t kst, vst;       // bytes of one stage's K / V words (32 R, rounded to 16) plus padding
 };
 
+struct TcSmem {
+    uint32_t img, stage, pt, wmax, red, bars, total;
+};
+
+__host__ __device__ inline TcSmem tc_smem_layout(int stages, uint32_t kst, uint32_t vst, int nkb)
+{
+    TcSmem L;
+    uint32_t o = 0;
+    L.img = o;   o += uint32_t(nkb) * 256;
+    L.stage = o; o += uint32_t(stages) * (kst + vst);
+    L.pt = o;    o += kWarps * 8 * PSTR * 4;
+    L.wmax = o;  o += kWarps * kGmax * 4;
+    L.red = o;   o += kWarps * kGmax * 4;
+    L.bars = o;  o += 8 * kMaxStages + 16;
+    L.total = o;
+    return L;
+}
+
+// MTV: V m-tiles per warp (ceil(R_V / 128)).  A record with an even number
+// of words starts every group's words 8-byte aligned in shared memory (64-bit
+// loads); odd records take 32-bit loads.
+template <int MTV>
 __global__ void __launch_bounds__(kThreads, 2)
 attn_tc_split_kernel(AttnTcParams P)
 {
@@ -183,286 +193,270 @@ attn_tc_split_kernel(AttnTcParams P)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g8 = lane >> 2, tig = lane & 3;
     const int bh = b * Hkv + h;
+    const int S = P.stages;
 
-    uint8_t* cw = smem;                                          // [2][kbytes + vbytes]
-    const uint32_t cwb = P.kbytes + P.vbytes;
-    uint8_t* Lk = cw + 2 * cwb;                                  // [D][LROW]
-    uint8_t* Lv = Lk + D * LROW;                                 // [D][LROW]
-    __half* Pw = reinterpret_cast<__half*>(Lv + D * LROW);      // per warp [8][PROW]: P of its 16 tokens
-    float* mw = reinterpret_cast<float*>(Pw + 8 * 8 * PROW);     // [8 warps][kGmax] running max
-    float* lw = mw + 8 * kGmax;                                  // [8 warps][kGmax] running sum
+    const int nkb = (P.kp.max_rec_bits + 15) / 16;
+    const TcSmem L = tc_smem_layout(S, P.kst, P.vst, max(nkb, 1));
+    uint2* wimg = reinterpret_cast<uint2*>(smem + L.img);
+    uint8_t* stage = smem + L.stage;
+    uint32_t* pt = reinterpret_cast<uint32_t*>(smem + L.pt);
+    float* wmax = reinterpret_cast<float*>(smem + L.wmax);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kMaxStages);
 
     const int64_t t_begin = int64_t(split) * P.split_len;
     const int64_t t_end = min(P.ctx, t_begin + P.split_len);
     const int ntiles = int((t_end - t_begin + TT - 1) / TT);
-    // records larger than the plans' bound are not read (their streams were sized by the bound)
+    // records longer than the plans' bound are not read (the streams were sized by the bound)
     const int RK0 = P.kp.rec_bits[h], RV0 = P.vp.rec_bits[h];
     const int RK = RK0 <= P.kp.max_rec_bits ? RK0 : 0, RV = RV0 <= P.vp.max_rec_bits ? RV0 : 0;
+    const int nkbh = (RK + 15) / 16, nmtv = (RV + 15) / 16;
     const int64_t sid = int64_t(b) * Hkv + h;
     const uint8_t* ks = P.kc + sid * P.sstride;
     const uint8_t* vs = P.vc + sid * P.sstride;
 
-    // unpack role: side (K for warps 0-3, V for 4-7) and 32-token group
-    // ug = warp & 3 of the tile, over all 128 channels in four blocks of 32
-    // (channel 32 cb + lane).  The wide channels (the leading eigen-
-    // directions) sit in block 0, so every warp gets the same mix of one
-    // wide and three narrow blocks.  Per block: widths packed 8 bits each
-    // (ubp), the widest in the block (ubm), and word offsets 16 bits each.
-    const int side = warp >> 2, ug = warp & 3;
-    const PlanView& up = side ? P.vp : P.kp;
-    uint32_t ubp = 0, ubm = 0, uop01 = 0, uop23 = 0;
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-        const int c = cb * 32 + lane;
-        const uint32_t wb = uint32_t(up.bits[size_t(h) * D + c]);
-        const uint32_t wo = uint32_t(up.chan_off[size_t(h) * D + c]);
-        ubp |= wb << (8 * cb);
-        ubm |= uint32_t(__reduce_max_sync(0xffffffffu, wb)) << (8 * cb);
-        if (cb < 2) uop01 |= wo << (16 * cb); else uop23 |= wo << (16 * (cb - 2));
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        abort_flag[0] = 0;
+        abort_flag[1] = 0;
+        fence_mbar_init();
     }
-    const int uR = side ? RV : RK;
-
-    // score operand B: W rows (n = g8: 0..3 hi, 4..7 lo), k = 16 kb + 2 tig (+8)
-    uint32_t wf[8][2];
     {
-        const __half* wr = P.wimg + size_t(bh) * 8 * D + g8 * D;
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-            wf[kb][0] = *reinterpret_cast<const uint32_t*>(wr + kb * 16 + 2 * tig);
-            wf[kb][1] = *reinterpret_cast<const uint32_t*>(wr + kb * 16 + 8 + 2 * tig);
-        }
-    }
-    const float bias0 = P.bias[size_t(bh) * kGmax + ((2 * tig) & 3)];
-    const float bias1 = P.bias[size_t(bh) * kGmax + ((2 * tig + 1) & 3)];
-    // this warp's share of the output, all 128 channels: m-tile mt holds
-    // channels 16 mt + g8 (+8), columns n = 2 tig, 2 tig + 1 (head hi / lo)
-    float oacc[8][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
-    // online-softmax state of the warp's token slice, heads j0 = 2 (tig & 1), j0 + 1
-    const int j0 = 2 * (tig & 1), j1 = j0 + 1;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    __half* pw = Pw + warp * 8 * PROW;
-
-    auto issue_load = [&](int tile, int buf) {
-        const int64_t t0 = t_begin + int64_t(tile) * TT;
-        const int64_t ng = min(int64_t(4), (t_end - t0 + 31) / 32);
-        const uint32_t nk = uint32_t((ng * 4 * RK + 15) / 16), nv = uint32_t((ng * 4 * RV + 15) / 16);
-        uint8_t* dst = cw + buf * cwb;
-        const uint8_t* srck = ks + (t0 / 32) * 4 * RK;
-        const uint8_t* srcv = vs + (t0 / 32) * 4 * RV;
-        for (uint32_t i = tid; i < nk + nv; i += kThreads) {
-            if (i < nk) cp_async16(dst + 16 * i, srck + 16 * i);
-            else cp_async16(dst + P.kbytes + 16 * (i - nk), srcv + 16 * (i - nk));
-        }
-        cp_async_commit();
-    };
-    if (ntiles > 0) issue_load(0, 0);
-
-    for (int tile = 0; tile < ntiles; ++tile) {
-        const int buf = tile & 1;
-        const int64_t t0 = t_begin + int64_t(tile) * TT;
-        cp_async_wait_all();
-        __syncthreads();                                   // code words landed; previous tile done
-        if (tile + 1 < ntiles) issue_load(tile + 1, buf ^ 1);
-
-        // ---- unpack: one 32-token group per warp, one channel per lane, four channel blocks
-        {
-            const uint32_t* words = reinterpret_cast<const uint32_t*>(cw + buf * cwb + (side ? P.kbytes : 0));
-            uint8_t* L = side ? Lv : Lk;
-            const bool live = t0 + 32 * ug < t_end && uR > 0;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                const int ub = int((ubp >> (8 * cb)) & 0xFFu), ubmax = int((ubm >> (8 * cb)) & 0xFFu);
-                const int uo = int(((cb < 2 ? uop01 : uop23) >> (16 * (cb & 1))) & 0xFFFFu);
-                // v[s] = fp16 pair (1024 + code) for tokens s and s + 16 of the group:
-                // the tile keeps each group in that pair order (positions 2s, 2s + 1),
-                // the same for K and V, so scores and P V see one consistent order
-                uint32_t v[16];
-                if (ubmax <= 2) {
-                    // widths <= 2 (the block's widest channel): interleave the two
-                    // planes once into E (even tokens) and O (odd tokens), 2 bits a
-                    // token; tokens s and s + 16 are then bits s and s + 16 of E (or O)
-                    uint32_t w0 = 0u, w1 = 0u;
-                    if (live) {
-                        const uint32_t* wg = words + ug * uR + uo;
-                        w0 = ub > 0 ? wg[0] : 0u;
-                        w1 = ub > 1 ? wg[1] : 0u;
-                    }
-                    const uint32_t E = (w0 & 0x55555555u) | ((w1 << 1) & 0xAAAAAAAAu);
-                    const uint32_t O = ((w0 >> 1) & 0x55555555u) | (w1 & 0xAAAAAAAAu);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const uint32_t x = (q & 1) ? (O >> (q - 1)) : (E >> q);
-                        v[q] = (x & 0x00030003u) | 0x64006400u;
-                    }
-                } else {
-                    uint32_t X[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // byte i of X[m]: code of token 4m + i
-                    if (live) planes_to_codes(words + ug * uR, uo, ub, ubmax, X);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const uint32_t sel = uint32_t(q & 3) | (uint32_t(4 + (q & 3)) << 8);
-                        v[q] = (__byte_perm(X[q >> 2], X[(q >> 2) + 4], sel) & 0x00FF00FFu) | 0x64006400u;
-                    }
-                }
-                // z = code - 2^(b-1) (0 for dropped channels): (1024 + code) - (1024 + 2^(b-1)), exact in fp16
-                const __half2 cz = __float2half2_rn(1024.f + (ub > 0 ? float(1 << (ub - 1)) : 0.f));
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const __half2 z = __hsub2(*reinterpret_cast<const __half2*>(&v[q]), cz);
-                    v[q] = *reinterpret_cast<const uint32_t*>(&z);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(L + (cb * 32 + lane) * LROW + ug * 64);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-            }
-        }
-        __syncthreads();
-
-        // ---- per warp, positions 16 warp .. +15 of the tile: scores, online
-        // softmax and P V, with no block barrier in between
-        const int mi = lane >> 3, ri = lane & 7;
-        const int tw = warp * 16;
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kb = 0; kb < 8; kb += 2) {
-            uint32_t a[4], a2[4];
-            const int k = kb * 16 + (mi >> 1) * 8 + ri, m = tw + (mi & 1) * 8;
-            ldsm_x4_t(smem_addr(Lk + k * LROW + m * 2), a);
-            ldsm_x4_t(smem_addr(Lk + (k + 16) * LROW + m * 2), a2);
-            mma16816(sa, a, wf[kb][0], wf[kb][1], sa);
-            mma16816(sb, a2, wf[kb + 1][0], wf[kb + 1][1], sb);
-        }
-        float sc[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            sc[e] = sa[e] + sb[e];
-            sc[e] += __shfl_xor_sync(0xffffffffu, sc[e], 2);   // hi + lo columns
-        }
-        {
-            // positions tw + g8 (+8) hold tokens 32 (warp / 2) + (q >> 1) + 16 (q & 1), q the position in the group
-            const int qa = (warp & 1) * 16 + g8, qb = qa + 8;
-            const int gbase = (warp >> 1) * 32;
-            const bool la = t0 + gbase + (qa >> 1) + (qa & 1) * 16 < t_end;
-            const bool lb = t0 + gbase + (qb >> 1) + (qb & 1) * 16 < t_end;
-            const bool h0 = j0 < G, h1 = j1 < G;
-            sc[0] = (la && h0) ? sc[0] + bias0 : -INFINITY;
-            sc[1] = (la && h1) ? sc[1] + bias1 : -INFINITY;
-            sc[2] = (lb && h0) ? sc[2] + bias0 : -INFINITY;
-            sc[3] = (lb && h1) ? sc[3] + bias1 : -INFINITY;
-        }
-        float x0 = fmaxf(sc[0], sc[2]), x1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
-            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
-        }
-        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-        const float al0 = (m0 == -INFINITY) ? 0.f : __expf(m0 - n0);
-        const float al1 = (m1 == -INFINITY) ? 0.f : __expf(m1 - n1);
-        m0 = n0;
-        m1 = n1;
-        __half ph[4], pl[4];
-        float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float pe = (sc[e] == -INFINITY) ? 0.f : __expf(sc[e] - ((e & 1) ? n1 : n0));
-            ph[e] = __float2half_rn(pe);
-            pl[e] = __float2half_rn(pe - __half2float(ph[e]));
-            const float pq = __half2float(ph[e]) + __half2float(pl[e]);
-            if (e & 1) ps1 += pq; else ps0 += pq;
-        }
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            ps0 += __shfl_xor_sync(0xffffffffu, ps0, o);
-            ps1 += __shfl_xor_sync(0xffffffffu, ps1, o);
-        }
-        l0 = l0 * al0 + ps0;
-        l1 = l1 * al1 + ps1;
-        // P of the slice as the B operand [n = head hi 0..3 / lo 4..7][k = token]:
-        // lanes tig 0/1 write the hi parts of their heads, tig 2/3 the lo parts
-        {
-            const __half* pv = tig < 2 ? ph : pl;
-            const int r0 = (tig < 2 ? 0 : kGmax) + j0;
-            pw[r0 * PROW + g8] = pv[0];
-            pw[(r0 + 1) * PROW + g8] = pv[1];
-            pw[r0 * PROW + g8 + 8] = pv[2];
-            pw[(r0 + 1) * PROW + g8 + 8] = pv[3];
-        }
-        __syncwarp();
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(pw + g8 * PROW + 2 * tig);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(pw + g8 * PROW + 8 + 2 * tig);
-        // columns n = 2 tig, 2 tig + 1 are heads j0, j1 (hi for tig < 2, lo otherwise)
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            oacc[mt][0] *= al0; oacc[mt][1] *= al1; oacc[mt][2] *= al0; oacc[mt][3] *= al1;
-            uint32_t a[4];
-            const int m = mt * 16 + (mi & 1) * 8 + ri, k = tw + (mi >> 1) * 8;
-            ldsm_x4(smem_addr(Lv + m * LROW + k * 2), a);
-            mma16816(oacc[mt], a, b0, b1, oacc[mt]);
-        }
-    }
-    __syncthreads();   // every warp is past its last read of Lk / Lv
-
-    // merge the eight warps' slices: warp w's partial scaled by exp(m_w - M)
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) oacc[mt][e] += __shfl_xor_sync(0xffffffffu, oacc[mt][e], 2);   // hi + lo
-    float* Ow = reinterpret_cast<float*>(Lk);                    // [8 warps][kGmax][D]
-    if (g8 == 0 && tig < 2) {
-        mw[warp * kGmax + j0] = m0; mw[warp * kGmax + j1] = m1;
-        lw[warp * kGmax + j0] = l0; lw[warp * kGmax + j1] = l1;
-    }
-    if (tig < 2) {
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int c0 = mt * 16 + g8, c1 = c0 + 8;
-            Ow[(warp * kGmax + j0) * D + c0] = oacc[mt][0];
-            Ow[(warp * kGmax + j1) * D + c0] = oacc[mt][1];
-            Ow[(warp * kGmax + j0) * D + c1] = oacc[mt][2];
-            Ow[(warp * kGmax + j1) * D + c1] = oacc[mt][3];
-        }
+        const uint2* src = reinterpret_cast<const uint2*>(P.img + size_t(bh) * (kImgBytesPerHead / 4));
+        for (int e = tid; e < nkbh * 32; e += kThreads) wimg[e] = src[e];
     }
     __syncthreads();
 
-    // partials: [(b Hq + h G + j) nsplit + split][2 + D]: m, l, sum_t p code
-    for (int i = tid; i < kGmax * D; i += kThreads) {
-        const int j = i / D, c = i % D;
+    // bulk copies of tile `tile` into its stage: the groups' K and V words
+    auto issue = [&](int tile) {
+        const int s = tile % S;
+        const int64_t t0 = t_begin + int64_t(tile) * TT;
+        const int64_t ng = min(int64_t(TT / 32), (t_end - t0 + 31) / 32);
+        const uint32_t kb = uint32_t((ng * 4 * RK + 15) / 16 * 16), vb = uint32_t((ng * 4 * RV + 15) / 16 * 16);
+        uint8_t* dst = stage + size_t(s) * (P.kst + P.vst);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&full[s], kb + vb);
+        if (kb) bulk_load(dst, ks + (t0 / 32) * 4 * RK, kb, &full[s]);
+        if (vb) bulk_load(dst + P.kst, vs + (t0 / 32) * 4 * RV, vb, &full[s]);
+    };
+    int issued = 0;                            // tiles whose copies were issued (thread 0)
+    if (tid == 0)
+        for (; issued < min(S - 1, ntiles); ++issued) issue(issued);
+
+    // score weights and constants of head tig (this thread's accumulator column pair)
+    const float cj = P.bias[size_t(bh) * 8 + tig];
+    const float vsum = P.bias[size_t(bh) * 8 + 4 + tig];
+    const bool head_ok = tig < G;
+    // rows g8 and g8 + 8 of a score tile: bit positions p0 = g8, p1 = g8 + 8
+    const uint32_t m0 = (1u << g8) | (1u << (g8 + 16));
+    const uint32_t m1 = (1u << (g8 + 8)) | (1u << (g8 + 24));
+    const uint32_t base1 = (g8 == 7) ? 0x3C003C00u : 0u;            // sign bit: 1 - 2 bit
+    const float rs0 = exp2f(float(24 - g8));
+    const float rs1 = g8 <= 3 ? exp2f(float(16 - g8)) : g8 == 4 ? 2048.f : g8 == 5 ? 128.f : g8 == 6 ? 0.5f : -0.5f;
+    const float bs1 = (g8 == 7) ? vsum : 0.f;
+    // P V masks: token pairs (s, s + 16) at bit positions tig and tig + 4
+    const uint32_t mA = (1u << tig) | (1u << (tig + 16));
+    const uint32_t mB = (1u << (tig + 4)) | (1u << (tig + 20));
+    const float pscale = exp2f(float(9 - g8));      // P' = p 2^(9 - position), position = g8
+
+    float acc[MTV][4];
+#pragma unroll
+    for (int i = 0; i < MTV; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m_run = -INFINITY, l_part = 0.f;
+    bool aborted = false;
+
+    for (int tile = 0; tile < ntiles; ++tile) {
+        const int s = tile % S;
+        const int64_t t0 = t_begin + int64_t(tile) * TT;
+        const uint8_t* stg = stage + size_t(s) * (P.kst + P.vst);
+        const bool ok = mbar_wait(&full[s], uint32_t(tile / S) & 1u, abort_flag, kWaitNs);
+
+        // ---- scores of this warp's group (tokens t0 + 32 warp ...)
+        const int64_t tg0 = t0 + 32 * warp;
+        float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // tokens g8, g8+8, 16+g8, 24+g8
+        if (ok && tg0 < t_end && RK > 0) {
+            const uint32_t* kw = reinterpret_cast<const uint32_t*>(stg) + warp * RK;
+            float aA[4] = {0.f, 0.f, 0.f, 0.f}, aB[4] = {0.f, 0.f, 0.f, 0.f};
+            float aA2[4] = {0.f, 0.f, 0.f, 0.f}, aB2[4] = {0.f, 0.f, 0.f, 0.f};
+            auto kloop = [&](auto even_tag) {
+                constexpr bool EV = decltype(even_tag)::value;
+#pragma unroll 2
+                for (int kb = 0; kb < nkbh; ++kb) {
+                    const uint2 wb = wimg[kb * 32 + lane];
+                    uint32_t p0, p1, p8, p9;
+                    if constexpr (EV) {
+                        const uint2 u = *reinterpret_cast<const uint2*>(kw + 16 * kb + 2 * tig);
+                        const uint2 v = *reinterpret_cast<const uint2*>(kw + 16 * kb + 2 * tig + 8);
+                        p0 = u.x; p1 = u.y; p8 = v.x; p9 = v.y;
+                    } else {
+                        p0 = kw[16 * kb + 2 * tig];     p1 = kw[16 * kb + 2 * tig + 1];
+                        p8 = kw[16 * kb + 2 * tig + 8]; p9 = kw[16 * kb + 2 * tig + 9];
+                    }
+                    const uint32_t lo01 = __byte_perm(p0, p1, 0x5410), hi01 = __byte_perm(p0, p1, 0x7632);
+                    const uint32_t lo89 = __byte_perm(p8, p9, 0x5410), hi89 = __byte_perm(p8, p9, 0x7632);
+                    const uint32_t a[4] = {lo01 & m0, (lo01 & m1) | base1, lo89 & m0, (lo89 & m1) | base1};
+                    const uint32_t c[4] = {hi01 & m0, (hi01 & m1) | base1, hi89 & m0, (hi89 & m1) | base1};
+                    if (kb & 1) {
+                        mma16816(aA2, a, wb.x, wb.y);
+                        mma16816(aB2, c, wb.x, wb.y);
+                    } else {
+                        mma16816(aA, a, wb.x, wb.y);
+                        mma16816(aB, c, wb.x, wb.y);
+                    }
+                }
+            };
+            if (RK & 1) kloop(std::false_type{});
+            else kloop(std::true_type{});
+            const float r[4] = {(aA[0] + aA2[0]) + (aA[1] + aA2[1]), (aA[2] + aA2[2]) + (aA[3] + aA2[3]),
+                                (aB[0] + aB2[0]) + (aB[1] + aB2[1]), (aB[2] + aB2[2]) + (aB[3] + aB2[3])};
+            const int tok[4] = {g8, g8 + 8, 16 + g8, 24 + g8};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float v = (e & 1) ? (r[e] - bs1) * rs1 : r[e] * rs0;
+                sc[e] = (head_ok && tg0 + tok[e] < t_end) ? v + cj : -INFINITY;
+            }
+        } else if (ok && tg0 < t_end && head_ok) {
+            // zero-bit K record: every score is the constant C_j
+            const int tok[4] = {g8, g8 + 8, 16 + g8, 24 + g8};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[e] = (tg0 + tok[e] < t_end) ? cj : -INFINITY;
+        }
+        float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (g8 == 0) wmax[warp * kGmax + tig] = mx;
+        if (__syncthreads_or(!ok)) {          // barrier 1: tile maxima; stage of tile - 1 free
+            aborted = true;
+            break;
+        }
+        if (tid == 0 && issued < ntiles) issue(issued++);
+
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) tmax = fmaxf(tmax, wmax[w * kGmax + tig]);
+        const float m_new = fmaxf(m_run, tmax);
+        const float alpha = (m_run == -INFINITY) ? 0.f : __expf(m_run - m_new);
+        m_run = m_new;
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[e] = (sc[e] == -INFINITY) ? 0.f : __expf(sc[e] - m_new);
+        l_part = l_part * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+        {
+            // pairs (g8, 16 + g8) -> k-step 0, (8 + g8, 24 + g8) -> k-step 1; pair index g8
+            uint32_t* prow = pt + (warp * 8 + 2 * tig) * PSTR + (g8 & 3) * 2 + (g8 >> 2);
+#pragma unroll
+            for (int ksp = 0; ksp < 2; ++ksp) {
+                const float x0 = p[ksp] * pscale, x1 = p[2 + ksp] * pscale;
+                const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                prow[ksp * 8] = pack_half2(__half2float(h0), __half2float(h1));
+                prow[PSTR + ksp * 8] = pack_half2(x0 - __half2float(h0), x1 - __half2float(h1));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < MTV; ++i) {
+            acc[i][0] *= alpha; acc[i][1] *= alpha; acc[i][2] *= alpha; acc[i][3] *= alpha;
+        }
+        __syncthreads();                       // barrier 2: the tile's P in shared memory
+
+        // ---- P V over this warp's V planes, all groups of the tile
+        if (RV > 0) {
+            const uint32_t* vwt = reinterpret_cast<const uint32_t*>(stg + P.kst);
+            const int ngv = int(min(int64_t(TT / 32), (t_end - t0 + 31) / 32));
+            auto vloop = [&](auto even_tag) {
+                constexpr bool EV = decltype(even_tag)::value;
+                for (int g = 0; g < ngv; ++g) {
+                    const uint2* pg = reinterpret_cast<const uint2*>(pt + (g * 8 + g8) * PSTR) + tig;
+                    const uint2 pb0 = pg[0], pb1 = pg[4];
+                    const uint32_t* vw = vwt + g * RV;
+#pragma unroll
+                    for (int i = 0; i < MTV; ++i) {
+                        const int mt = warp + kWarps * i;
+                        if (mt < nmtv) {
+                            uint32_t w0, w1;
+                            if constexpr (EV) {
+                                const uint2 u = *reinterpret_cast<const uint2*>(vw + 16 * mt + 2 * g8);
+                                w0 = u.x; w1 = u.y;
+                            } else {
+                                w0 = vw[16 * mt + 2 * g8]; w1 = vw[16 * mt + 2 * g8 + 1];
+                            }
+                            const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
+                            const uint32_t a0[4] = {w0 & mA, w1 & mA, w0 & mB, w1 & mB};
+                            const uint32_t a1[4] = {s0 & mA, s1 & mA, s0 & mB, s1 & mB};
+                            mma16816(acc[i], a0, pb0.x, pb0.y);
+                            mma16816(acc[i], a1, pb1.x, pb1.y);
+                        }
+                    }
+                }
+            };
+            if (RV & 1) vloop(std::false_type{});
+            else vloop(std::true_type{});
+        }
+    }
+
+    if (aborted) {
+        // let the copies in flight land before the CTA exits (each stage's
+        // last issued phase, bounded), then report through the plan's status
+        if (tid == 0) {
+            for (int st = 0; st < S; ++st) {
+                int last = -1;
+                for (int t = st; t < issued; t += S) last = t;
+                if (last >= 0) mbar_wait(&full[st], uint32_t(last / S) & 1u, abort_flag + 1, 100000000ull);
+            }
+            P.kp.status[h] = -SPECTRA_ERR_TIMEOUT;
+        }
+        return;
+    }
+    __syncthreads();   // every warp is past its last read of the stages and the P tile
+
+    // ---- split partials: S_jr (planes), l_j, then o_jc = sum_k 2^k S_j,(c,k) - 2^(b-1) l_j
+    float* Ssm = reinterpret_cast<float*>(stage);           // [kGmax][R_V] (reuses the stages)
+#pragma unroll
+    for (int i = 0; i < MTV; ++i) {
+        const int mt = warp + kWarps * i;
+        if (mt < nmtv) {
+            const int r = 16 * mt + 2 * g8;
+            if (r < RV) Ssm[tig * RV + r] = 32768.f * (acc[i][0] + acc[i][1]);
+            if (r + 1 < RV) Ssm[tig * RV + r + 1] = 32768.f * (acc[i][2] + acc[i][3]);
+        }
+    }
+    float lsum = l_part;
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
+    if (g8 == 0) red[warp * kGmax + tig] = lsum;
+    if (g8 == 0 && warp == 0) wmax[tig] = m_run;
+    __syncthreads();
+    for (int e = tid; e < kGmax * D; e += kThreads) {
+        const int j = e / D, c = e % D;
         if (j >= G) continue;
-        float M = -INFINITY;
+        float l = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) M = fmaxf(M, mw[w * kGmax + j]);
-        float o = 0.f, l = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const float mv = mw[w * kGmax + j];
-            const float f = (mv == -INFINITY) ? 0.f : __expf(mv - M);
-            o = fmaf(f, Ow[(w * kGmax + j) * D + c], o);
-            l = fmaf(f, lw[w * kGmax + j], l);
+        for (int w = 0; w < kWarps; ++w) l += red[w * kGmax + j];
+        const int bc = P.vp.bits[size_t(h) * D + c];
+        float o = 0.f;
+        if (bc > 0 && RV > 0) {
+            const int oc = P.vp.chan_off[size_t(h) * D + c];
+            for (int k = bc - 1; k >= 0; --k) o = fmaf(o, 2.f, Ssm[j * RV + oc + k]);
+            o -= float(1 << (bc - 1)) * l;
         }
         float* bp = P.part + ((int64_t(b) * P.Hq + h * G + j) * P.nsplit + split) * (D + 2);
         bp[2 + c] = o;
         if (c == 0) {
-            bp[0] = M;
+            bp[0] = wmax[j];
             bp[1] = l;
         }
     }
 }
 
-size_t tc_split_smem(uint32_t kbytes, uint32_t vbytes)
-{
-    return 2 * size_t(kbytes + vbytes) + 2 * size_t(D) * LROW + sizeof(__half) * 8 * 8 * PROW +
-           sizeof(float) * 2 * 8 * kGmax + 64;
-}
-
 }  // namespace
 
-// Workspace layout of the tensor-core path (inside attn_workspace_bytes):
-// [partials | wimg (B Hkv 8 D fp16) | bias (B Hkv 4 f32)].
+// Workspace of the tensor-core path (inside attn_workspace_bytes):
+// [score weight images (B Hkv x 16 KB) | constants (B Hkv x 8 f32)].
 size_t attn_tc_extra_bytes(int B, int Hkv)
 {
-    return align256(sizeof(__half) * size_t(B) * Hkv * 8 * D) + align256(sizeof(float) * size_t(B) * Hkv * kGmax);
+    return align256(size_t(kImgBytesPerHead) * B * Hkv) + align256(sizeof(float) * 8 * size_t(B) * Hkv);
 }
 
 spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vplan, const void* q, int q_dt, int B,
@@ -487,23 +481,44 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
     P.kc = kc;
     P.vc = vc;
     P.sstride = sstride;
-    __half* wimg = static_cast<__half*>(extra);
+    uint32_t* img = static_cast<uint32_t*>(extra);
     float* bias = reinterpret_cast<float*>(static_cast<uint8_t*>(extra) +
-                                           align256(sizeof(__half) * size_t(B) * Hkv * 8 * D));
-    P.wimg = wimg;
+                                           align256(size_t(kImgBytesPerHead) * B * Hkv));
+    P.img = img;
     P.bias = bias;
     P.part = part;
-    P.kbytes = uint32_t(16 * (kplan->max_rec_bits > 0 ? kplan->max_rec_bits : 1));
-    P.vbytes = uint32_t(16 * (vplan->max_rec_bits > 0 ? vplan->max_rec_bits : 1));
-    const size_t sm = tc_split_smem(P.kbytes, P.vbytes);
-    if (sm > 227 * 1024) return SPECTRA_OK;
-    if (spectra_status st = set_smem(attn_tc_prep_kernel, sizeof(float) * D * D)) return st;
-    attn_tc_prep_kernel<<<B * Hkv, kGmax * D, sizeof(float) * D * D, s>>>(P.kp, q, q_dt, Hq, G, scale, wimg, bias);
-    if (spectra_status st = set_smem(attn_tc_split_kernel, sm)) return st;
+    const int RKm = kplan->max_rec_bits, RVm = vplan->max_rec_bits;
+    // one stage: 8 groups of each record, rounded to 16 bytes, plus 64 bytes
+    // for the reads of the last k-block / m-tile past the record
+    P.kst = uint32_t((32 * RKm + 15) / 16 * 16 + 64);
+    P.vst = uint32_t((32 * RVm + 15) / 16 * 16 + 64);
+    const int nkb = max((RKm + 15) / 16, 1);
+    // V-side partial sums reuse the stages: kGmax x R_V floats must fit
+    auto total = [&](int st) { return tc_smem_layout(st, P.kst, P.vst, nkb).total; };
+    int st = kMaxStages;
+    while (st > 2 && total(st) > 113 * 1024) --st;
+    if (total(st) > 227 * 1024) return SPECTRA_OK;
+    if (size_t(st) * (P.kst + P.vst) < sizeof(float) * kGmax * size_t(RVm)) return SPECTRA_OK;
+    P.stages = st;
+    const size_t sm = total(st);
+    const int mtv = (((RVm + 15) / 16) + kWarps - 1) / kWarps;
+    if (spectra_status e = set_smem(attn_tc_prep_kernel, sizeof(float) * D * D)) return e;
+    attn_tc_prep_kernel<<<B * Hkv, kGmax * D, sizeof(float) * D * D, s>>>(P.kp, q, q_dt, Hq, G, scale, img, bias);
+    if (spectra_status e = cuda_status(cudaGetLastError())) return e;
     dim3 grid(nsplit, Hkv, B);
-    attn_tc_split_kernel<<<grid, kThreads, sm, s>>>(P);
+    auto launch = [&](auto kern) -> spectra_status {
+        if (spectra_status e = set_smem(kern, sm)) return e;
+        kern<<<grid, kThreads, sm, s>>>(P);
+        return cuda_status(cudaGetLastError());
+    };
+    spectra_status e;
+    if (mtv <= 1) e = launch(attn_tc_split_kernel<1>);
+    else if (mtv <= 2) e = launch(attn_tc_split_kernel<2>);
+    else if (mtv <= 4) e = launch(attn_tc_split_kernel<4>);
+    else e = launch(attn_tc_split_kernel<8>);
+    if (e) return e;
     *done = true;
-    return cuda_status(cudaGetLastError());
+    return SPECTRA_OK;
 }
 
 }  // namespace spectra

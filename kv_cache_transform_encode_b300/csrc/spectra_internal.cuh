@@ -158,6 +158,12 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
                            int64_t ctx, float scale, float* out, void* ws, size_t ws_bytes,
                            cudaStream_t s);
 size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx);
+// Host-side argument checks of spectra_attn_decode (everything but the
+// workspace), shared by the entry points that run it.
+spectra_status attn_validate(const spectra_plan* kplan, const spectra_plan* vplan, const void* q, int q_dt,
+                             int B, int Hq, const uint8_t* k_codes, const uint8_t* v_codes,
+                             int64_t stream_stride_bytes, const float* k_norms, const float* v_norms,
+                             int64_t norms_stride, int64_t ctx, float softmax_scale, const float* out);
 int gram_chunks(int heads, int64_t n_cal);
 
 inline spectra_status cuda_status(cudaError_t e)
