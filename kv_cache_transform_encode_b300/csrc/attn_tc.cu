@@ -13,26 +13,30 @@
 // and both contractions are products of a 0/1 matrix -- the packed words
 // exactly as stored -- with dense fp16 operands.  No code is ever unpacked.
 //
-// A bit enters the tensor core as an fp16 number by masking: a 32-bit word
-// ANDed with (1 << p) | (1 << (p + 16)) is a pair of fp16 values, each either
-// 0 or the value of the lone bit p -- 2^(p-24) (a subnormal) for p <= 9, a
-// power of two for the exponent bits p = 10..14.  Bit 15 (the sign) is
-// ORed with 1.0, giving 1 - 2 bit.  Every row of a product then carries one
-// known per-position factor, removed after the MMA (scores) or folded into
-// the other operand beforehand (P V).
+// A bit enters the tensor core as a normal fp16 number.  One byte permute
+// moves byte b of a stream word into the high byte of a 16-bit half, so
+// token 8 b + j of the word sits at bit q = 8 + j of that half; masking out
+// every other bit and ORing a per-position base leaves base_q + bit * d_q:
+//   q = 8, 9:    base 2^-14 (exponent 1), bit in the mantissa: d = 2^-16, 2^-15
+//   q = 10..14:  base 0, bit alone in the exponent: 2^-14, 2^-13, 2^-11, 2^-7, 2
+//   q = 15:      base 1.0, bit in the sign: 1 - 2 bit
+// (subnormal operands are avoided: the tensor cores round them coarsely).
+// Every row (scores) or token (P V) of a product then carries one known
+// affine map of its bits, undone after the MMA or folded into the other
+// operand beforehand.
 //
 //  * Scores (per 32-token group, one warp): m16n8k16 with M = 16 tokens,
 //    K = 16 planes, N = 8 = 4 query heads x (hi, lo) fp16 halves of V.  An A
-//    register holds two planes of one token: the two plane words are merged
-//    by one byte permute (low halves or high halves), then each register is
-//    one mask.  Row p of the tile is token p of the half-group, scaled by
-//    1 / value(bit p).
+//    register holds two planes of one token: one byte permute of the two
+//    plane words per byte, then one mask-and-base per register.  A thread's
+//    rows are tokens g, 8 + g, 16 + g, 24 + g, all at q = 8 + g, so
+//    sum_r V_r bit_r = (acc - base_q sum_r V_r) / d_q.
 //  * P V: m16n8k16 with M = 16 planes, K = 16 tokens, N = 8 = heads x (hi,
-//    lo) of P.  An A register holds one plane of two tokens, s and s + 16,
-//    straight from one stream word: one mask (bits 0..7) or one shift and a
-//    mask (bits 8..15, taken from the word shifted right by 8).  The token
-//    at position p then enters as 2^(p-24); P carries 2^(9-p) instead of 1,
-//    so every product is bit * p * 2^-15.
+//    lo) of P.  An A register holds one plane of tokens s and s + 16: one
+//    byte permute of the plane word (bytes 0 and 2, or 1 and 3), then one
+//    mask-and-base.  P enters as P' = p c / d_q, so a product is
+//    c (p bit + p base_q / d_q); the second term is the same for every plane
+//    and is removed with kappa = sum_t p base_q / d_q.
 //
 // One CTA (8 warps) per (context split, kv head, batch).  Tiles of 256
 // tokens (one 32-token group per warp) arrive by bulk copy (the group
@@ -174,7 +178,7 @@ __host__ __device__ inline TcSmem tc_smem_layout(int stages, uint32_t kst, uint3
     L.stage = o; o += uint32_t(stages) * (kst + vst);
     L.pt = o;    o += kWarps * 8 * PSTR * 4;
     L.wmax = o;  o += kWarps * kGmax * 4;
-    L.red = o;   o += kWarps * kGmax * 4;
+    L.red = o;   o += 2 * kWarps * kGmax * 4;
     L.bars = o;  o += 8 * kMaxStages + 16;
     L.total = o;
     return L;
@@ -248,22 +252,27 @@ attn_tc_split_kernel(AttnTcParams P)
     const float cj = P.bias[size_t(bh) * 8 + tig];
     const float vsum = P.bias[size_t(bh) * 8 + 4 + tig];
     const bool head_ok = tig < G;
-    // rows g8 and g8 + 8 of a score tile: bit positions p0 = g8, p1 = g8 + 8
-    const uint32_t m0 = (1u << g8) | (1u << (g8 + 16));
-    const uint32_t m1 = (1u << (g8 + 8)) | (1u << (g8 + 24));
-    const uint32_t base1 = (g8 == 7) ? 0x3C003C00u : 0u;            // sign bit: 1 - 2 bit
-    const float rs0 = exp2f(float(24 - g8));
-    const float rs1 = g8 <= 3 ? exp2f(float(16 - g8)) : g8 == 4 ? 2048.f : g8 == 5 ? 128.f : g8 == 6 ? 0.5f : -0.5f;
-    const float bs1 = (g8 == 7) ? vsum : 0.f;
-    // P V masks: token pairs (s, s + 16) at bit positions tig and tig + 4
-    const uint32_t mA = (1u << tig) | (1u << (tig + 16));
-    const uint32_t mB = (1u << (tig + 4)) | (1u << (tig + 20));
-    const float pscale = exp2f(float(9 - g8));      // P' = p 2^(9 - position), position = g8
-
+    // every row of this thread sits at bit q = 8 + g8 of its half
+    const uint32_t mk = (1u << (8 + g8)) | (1u << (24 + g8));
+    const uint32_t bk = g8 < 2 ? 0x04000400u : g8 == 7 ? 0x3C003C00u : 0u;
+    const float dq = g8 == 0 ? 0x1p-16f : g8 == 1 ? 0x1p-15f : g8 == 2 ? 0x1p-14f : g8 == 3 ? 0x1p-13f
+                   : g8 == 4 ? 0x1p-11f : g8 == 5 ? 0x1p-7f : g8 == 6 ? 2.f : -2.f;
+    const float bq = g8 < 2 ? 0x1p-14f : g8 == 7 ? 1.f : 0.f;
+    const float rs = 1.f / dq;                      // exact: powers of two and -1/2
+    const float bsum = bq * vsum;
+    // P V: slot 0 holds token pairs at q = 8 + tig, slot 1 at q = 12 + tig
+    const uint32_t mv0 = (1u << (8 + tig)) | (1u << (24 + tig));
+    const uint32_t mv1 = (1u << (12 + tig)) | (1u << (28 + tig));
+    const uint32_t bv0 = tig < 2 ? 0x04000400u : 0u;
+    const uint32_t bv1 = tig == 3 ? 0x3C003C00u : 0u;
+    // P' = p c / d_q with c = 1/2 for this thread's tokens (q = 8 + g8);
+    // beta_q = base_q / d_q feeds kappa
+    const float pscale = 0.5f * rs;
+    const float beta = bq * rs;
     float acc[MTV][4];
 #pragma unroll
     for (int i = 0; i < MTV; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m_run = -INFINITY, l_part = 0.f;
+    float m_run = -INFINITY, l_part = 0.f, k_part = 0.f;
     bool aborted = false;
 
     for (int tile = 0; tile < ntiles; ++tile) {
@@ -277,8 +286,14 @@ attn_tc_split_kernel(AttnTcParams P)
         float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // tokens g8, g8+8, 16+g8, 24+g8
         if (ok && tg0 < t_end && RK > 0) {
             const uint32_t* kw = reinterpret_cast<const uint32_t*>(stg) + warp * RK;
+            // Three accumulator chains per m-tile: the first k-block (the widest
+            // channels' planes, which carry the largest terms) alone, then odd and
+            // even k-blocks.  The tensor core truncates each accumulation to the
+            // running sum's precision; short chains keep that error relative to
+            // small partial sums.
             float aA[4] = {0.f, 0.f, 0.f, 0.f}, aB[4] = {0.f, 0.f, 0.f, 0.f};
             float aA2[4] = {0.f, 0.f, 0.f, 0.f}, aB2[4] = {0.f, 0.f, 0.f, 0.f};
+            float aA0[4] = {0.f, 0.f, 0.f, 0.f}, aB0[4] = {0.f, 0.f, 0.f, 0.f};
             auto kloop = [&](auto even_tag) {
                 constexpr bool EV = decltype(even_tag)::value;
 #pragma unroll 2
@@ -293,11 +308,15 @@ attn_tc_split_kernel(AttnTcParams P)
                         p0 = kw[16 * kb + 2 * tig];     p1 = kw[16 * kb + 2 * tig + 1];
                         p8 = kw[16 * kb + 2 * tig + 8]; p9 = kw[16 * kb + 2 * tig + 9];
                     }
-                    const uint32_t lo01 = __byte_perm(p0, p1, 0x5410), hi01 = __byte_perm(p0, p1, 0x7632);
-                    const uint32_t lo89 = __byte_perm(p8, p9, 0x5410), hi89 = __byte_perm(p8, p9, 0x7632);
-                    const uint32_t a[4] = {lo01 & m0, (lo01 & m1) | base1, lo89 & m0, (lo89 & m1) | base1};
-                    const uint32_t c[4] = {hi01 & m0, (hi01 & m1) | base1, hi89 & m0, (hi89 & m1) | base1};
-                    if (kb & 1) {
+                    // byte b of both plane words -> high bytes of the two halves
+                    const uint32_t a[4] = {(__byte_perm(p0, p1, 0x4400) & mk) | bk, (__byte_perm(p0, p1, 0x5511) & mk) | bk,
+                                           (__byte_perm(p8, p9, 0x4400) & mk) | bk, (__byte_perm(p8, p9, 0x5511) & mk) | bk};
+                    const uint32_t c[4] = {(__byte_perm(p0, p1, 0x6622) & mk) | bk, (__byte_perm(p0, p1, 0x7733) & mk) | bk,
+                                           (__byte_perm(p8, p9, 0x6622) & mk) | bk, (__byte_perm(p8, p9, 0x7733) & mk) | bk};
+                    if (kb == 0) {
+                        mma16816(aA0, a, wb.x, wb.y);
+                        mma16816(aB0, c, wb.x, wb.y);
+                    } else if (kb & 1) {
                         mma16816(aA2, a, wb.x, wb.y);
                         mma16816(aB2, c, wb.x, wb.y);
                     } else {
@@ -308,12 +327,15 @@ attn_tc_split_kernel(AttnTcParams P)
             };
             if (RK & 1) kloop(std::false_type{});
             else kloop(std::true_type{});
-            const float r[4] = {(aA[0] + aA2[0]) + (aA[1] + aA2[1]), (aA[2] + aA2[2]) + (aA[3] + aA2[3]),
-                                (aB[0] + aB2[0]) + (aB[1] + aB2[1]), (aB[2] + aB2[2]) + (aB[3] + aB2[3])};
+            float r[4];
+            r[0] = aA0[0] + ((aA[0] + aA2[0]) + (aA0[1] + (aA[1] + aA2[1])));
+            r[1] = aA0[2] + ((aA[2] + aA2[2]) + (aA0[3] + (aA[3] + aA2[3])));
+            r[2] = aB0[0] + ((aB[0] + aB2[0]) + (aB0[1] + (aB[1] + aB2[1])));
+            r[3] = aB0[2] + ((aB[2] + aB2[2]) + (aB0[3] + (aB[3] + aB2[3])));
             const int tok[4] = {g8, g8 + 8, 16 + g8, 24 + g8};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float v = (e & 1) ? (r[e] - bs1) * rs1 : r[e] * rs0;
+                const float v = (r[e] - bsum) * rs;
                 sc[e] = (head_ok && tg0 + tok[e] < t_end) ? v + cj : -INFINITY;
             }
         } else if (ok && tg0 < t_end && head_ok) {
@@ -342,7 +364,9 @@ attn_tc_split_kernel(AttnTcParams P)
         float p[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) p[e] = (sc[e] == -INFINITY) ? 0.f : __expf(sc[e] - m_new);
-        l_part = l_part * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+        const float psum = (p[0] + p[1]) + (p[2] + p[3]);
+        l_part = l_part * alpha + psum;
+        k_part = k_part * alpha + beta * psum;
         {
             // pairs (g8, 16 + g8) -> k-step 0, (8 + g8, 24 + g8) -> k-step 1; pair index g8
             uint32_t* prow = pt + (warp * 8 + 2 * tig) * PSTR + (g8 & 3) * 2 + (g8 >> 2);
@@ -381,11 +405,19 @@ attn_tc_split_kernel(AttnTcParams P)
                             } else {
                                 w0 = vw[16 * mt + 2 * g8]; w1 = vw[16 * mt + 2 * g8 + 1];
                             }
-                            const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
-                            const uint32_t a0[4] = {w0 & mA, w1 & mA, w0 & mB, w1 & mB};
-                            const uint32_t a1[4] = {s0 & mA, s1 & mA, s0 & mB, s1 & mB};
-                            mma16816(acc[i], a0, pb0.x, pb0.y);
-                            mma16816(acc[i], a1, pb1.x, pb1.y);
+                            // bytes 0, 2 (tokens s, s + 16 for s < 8) and 1, 3 (s >= 8)
+                            const uint32_t x0 = __byte_perm(w0, w0, 0x2200), x1 = __byte_perm(w1, w1, 0x2200);
+                            const uint32_t y0 = __byte_perm(w0, w0, 0x3311), y1 = __byte_perm(w1, w1, 0x3311);
+                            const uint32_t a0[4] = {(x0 & mv0) | bv0, (x1 & mv0) | bv0, (x0 & mv1) | bv1, (x1 & mv1) | bv1};
+                            const uint32_t a1[4] = {(y0 & mv0) | bv0, (y1 & mv0) | bv0, (y0 & mv1) | bv1, (y1 & mv1) | bv1};
+                            // a fresh accumulator per group, added with rounding: a
+                            // plane's sum is scaled by up to 2^7 in the output, so the
+                            // tensor core's truncating accumulation must not run
+                            // across the whole split
+                            float t[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma16816(t, a0, pb0.x, pb0.y);
+                            mma16816(t, a1, pb1.x, pb1.y);
+                            acc[i][0] += t[0]; acc[i][1] += t[1]; acc[i][2] += t[2]; acc[i][3] += t[3];
                         }
                     }
                 }
@@ -417,29 +449,38 @@ attn_tc_split_kernel(AttnTcParams P)
         const int mt = warp + kWarps * i;
         if (mt < nmtv) {
             const int r = 16 * mt + 2 * g8;
-            if (r < RV) Ssm[tig * RV + r] = 32768.f * (acc[i][0] + acc[i][1]);
-            if (r + 1 < RV) Ssm[tig * RV + r + 1] = 32768.f * (acc[i][2] + acc[i][3]);
+            if (r < RV) Ssm[tig * RV + r] = 2.f * (acc[i][0] + acc[i][1]);
+            if (r + 1 < RV) Ssm[tig * RV + r + 1] = 2.f * (acc[i][2] + acc[i][3]);
         }
     }
-    float lsum = l_part;
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
-    if (g8 == 0) red[warp * kGmax + tig] = lsum;
+    float lsum = l_part, ksum = k_part;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        ksum += __shfl_xor_sync(0xffffffffu, ksum, o);
+    }
+    if (g8 == 0) {
+        red[warp * kGmax + tig] = lsum;
+        red[(kWarps + warp) * kGmax + tig] = ksum;
+    }
     if (g8 == 0 && warp == 0) wmax[tig] = m_run;
     __syncthreads();
     for (int e = tid; e < kGmax * D; e += kThreads) {
         const int j = e / D, c = e % D;
         if (j >= G) continue;
-        float l = 0.f;
+        float l = 0.f, kap = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) l += red[w * kGmax + j];
+        for (int w = 0; w < kWarps; ++w) {
+            l += red[w * kGmax + j];
+            kap += red[(kWarps + w) * kGmax + j];
+        }
         const int bc = P.vp.bits[size_t(h) * D + c];
         float o = 0.f;
         if (bc > 0 && RV > 0) {
             const int oc = P.vp.chan_off[size_t(h) * D + c];
             for (int k = bc - 1; k >= 0; --k) o = fmaf(o, 2.f, Ssm[j * RV + oc + k]);
-            o -= float(1 << (bc - 1)) * l;
+            // each plane sum carries kappa: sum_k 2^k kappa = (2^b - 1) kappa
+            o -= float((1 << bc) - 1) * kap + float(1 << (bc - 1)) * l;
         }
         float* bp = P.part + ((int64_t(b) * P.Hq + h * G + j) * P.nsplit + split) * (D + 2);
         bp[2 + c] = o;

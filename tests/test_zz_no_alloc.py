@@ -68,17 +68,27 @@ def test_noalloc_matches_workspace_entry_point(spx):
 
 
 def test_noalloc_refuses_oversized_requests(spx):
+    """A well-formed call whose scratch need is beyond the static buffer is
+    refused with SPECTRA_ERR_UNSUPPORTED before any launch; malformed calls
+    get the same status as from spectra_attn_decode; an empty context needs
+    no scratch at any batch size and only zeroes the output."""
+    import ctypes as C
     kp, vp, q, kc, vc = _inputs(spx, B=1, Hq=4, ctx=256)
-    big_ctx = 1 << 40                                  # scratch need far beyond the static buffer
-    assert spx.spectra_attn_workspace_bytes(64, 64, 128, big_ctx) > spx.SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES
-    out = torch.zeros((1, 4, 128), device="cuda")
-    with pytest.raises(spx.SpectraError) as e:
-        spx.lib()  # the refusal happens before any launch
-        import ctypes as C
-        kps, vps = kp.c(), vp.c()
-        st = spx.lib().spectra_attn_decode_noalloc(C.byref(kps), C.byref(vps), C.c_void_p(q.data_ptr()), 0,
-                                                   64, 64, C.c_void_p(kc.data_ptr()), C.c_void_p(vc.data_ptr()),
-                                                   kc.stride(0), None, None, 0, big_ctx, 1.0,
-                                                   C.c_void_p(out.data_ptr()), None)
-        spx._check(st, "spectra_attn_decode_noalloc")
-    assert e.value.status == 2
+    B, Hq, big_ctx = 64, 64, 1 << 40                   # scratch need far beyond the static buffer
+    assert spx.spectra_attn_workspace_bytes(B, Hq, 128, big_ctx) > spx.SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES
+    stride = spx.spectra_stream_bytes(max(kp.max_rec_bits, vp.max_rec_bits), big_ctx)
+    out = torch.zeros((B, Hq, 128), device="cuda")
+    kps, vps = kp.c(), vp.c()
+
+    def call(Hq_, ctx_, stride_):
+        return spx.lib().spectra_attn_decode_noalloc(C.byref(kps), C.byref(vps), C.c_void_p(q.data_ptr()), 0,
+                                                      B, Hq_, C.c_void_p(kc.data_ptr()),
+                                                      C.c_void_p(vc.data_ptr()), stride_, None, None, 0, ctx_,
+                                                      1.0, C.c_void_p(out.data_ptr()), None)
+    assert call(Hq, big_ctx, stride) == 2              # well formed, too large: unsupported
+    assert call(Hq + 1, big_ctx, stride) == 1          # query heads not a multiple of kv heads
+    assert call(Hq, big_ctx, 16) == 1                  # streams too short for the context
+    out.fill_(3.0)
+    assert call(Hq, 0, stride) == 0                    # empty context: zeroes the output
+    torch.cuda.synchronize()
+    assert out.abs().max().item() == 0.0
