@@ -57,6 +57,11 @@ def parse():
                     help="skip the separate compressed-attention measurement")
     ap.add_argument("--copies", type=int, default=NCOPY,
                     help="rotating input/output copies (L2 defeat); fewer for profiling captures")
+    ap.add_argument("--attn-only", action="store_true",
+                    help="profiling captures: calibrate one layer, then time only the compressed-attention "
+                         "workload (prints its block, not a bench line)")
+    ap.add_argument("--attn-batch", type=int, default=16,
+                    help="batch of the compressed-attention workload (default 16); smaller for profiling captures")
     return ap.parse_args()
 
 
@@ -178,6 +183,11 @@ def run_ours(args, rank, world, local_rank):
         spx.spectra_attn_decode(kp, vp, q, kc[c], vc[c], T_TOK, 1.0, att_o, workspace=aws)
         mark(5)
 
+    if args.attn_only:
+        step(0)
+        torch.cuda.synchronize()
+        return {"attn_decode": attn_workload(spx, kp, vp, dev, _peaks(), warm=args.warmup, reps=args.steps,
+                                             batch=args.attn_batch)}
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -288,7 +298,7 @@ def run_ours(args, rank, world, local_rank):
             "peak_source": peaks["source"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": _traffic(dom)}
 
-    attn = attn_workload(spx, kp, vp, dev, _peaks()) if args.attn_workload else None
+    attn = attn_workload(spx, kp, vp, dev, _peaks(), batch=args.attn_batch) if args.attn_workload else None
 
     res = {
         "metric": METRIC, "value": round(_whole_job_rate(T_TOK, world, ms), 1), "unit": UNIT, "n_gpus": world,
@@ -315,7 +325,7 @@ def run_ours(args, rank, world, local_rank):
 ATTN_B, ATTN_CTX = 16, 65536
 
 
-def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3):
+def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None):
     """Decode-step attention at the compressed-attention workload: batch 16,
     32 query heads over 8 kv heads, 65536-token context packed at the plans'
     2.0 bits/value (K and V streams of 16 x 8 x 65536 tokens).  The stream
@@ -324,6 +334,7 @@ def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3):
     sets (2 x 537 MB) keep each call's reads out of L2.  Timed with CUDA
     events on the launching stream; GB/s counts the packed bytes read."""
     import torch
+    ATTN_B = batch or globals()["ATTN_B"]
     R = kp.max_rec_bits
     sb = spx.spectra_stream_bytes(R, ATTN_CTX)
     gen = torch.Generator(device=dev)
@@ -558,6 +569,9 @@ def main():
         dist.init_process_group("nccl")
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
+        if args.attn_only:
+            print(json.dumps(res), flush=True)
+            return
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = oracle_sample()
         print(json.dumps(res), flush=True)

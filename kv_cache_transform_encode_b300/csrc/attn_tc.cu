@@ -285,7 +285,20 @@ attn_tc_split_kernel(AttnTcParams P)
         const int64_t tg0 = t0 + 32 * warp;
         float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // tokens g8, g8+8, 16+g8, 24+g8
         if (ok && tg0 < t_end && RK > 0) {
-            const uint32_t* kw = reinterpret_cast<const uint32_t*>(stg) + warp * RK;
+            uint32_t* kwm = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(stg)) + warp * RK;
+            // an even record: merge the group's plane pairs in place, once --
+            // words (2i, 2i + 1) become (low halves of both, high halves of
+            // both), the tokens 0..15 / 16..31 views the score tiles use (an odd
+            // record keeps its words and merges inside the k-loop)
+            if (!(RK & 1)) {
+                for (int pi = lane; pi < RK / 2; pi += 32) {
+                    const uint2 u = reinterpret_cast<const uint2*>(kwm)[pi];
+                    reinterpret_cast<uint2*>(kwm)[pi] = make_uint2(__byte_perm(u.x, u.y, 0x5410),
+                                                                   __byte_perm(u.x, u.y, 0x7632));
+                }
+                __syncwarp();
+            }
+            const uint32_t* kw = kwm;
             // Three accumulator chains per m-tile: the first k-block (the widest
             // channels' planes, which carry the largest terms) alone, then odd and
             // even k-blocks.  The tensor core truncates each accumulation to the
@@ -296,34 +309,39 @@ attn_tc_split_kernel(AttnTcParams P)
             float aA0[4] = {0.f, 0.f, 0.f, 0.f}, aB0[4] = {0.f, 0.f, 0.f, 0.f};
             auto kloop = [&](auto even_tag) {
                 constexpr bool EV = decltype(even_tag)::value;
-#pragma unroll 2
-                for (int kb = 0; kb < nkbh; ++kb) {
+                // one k-block into the chain (ca, cb): l / h hold tokens 0..15 /
+                // 16..31 of planes (2 tig, 2 tig + 1) and (2 tig + 8, 2 tig + 9);
+                // tokens 0..7 (16..23) reach the high bytes of the halves by a left
+                // shift of 8 (a multiply, so it can issue on the FMA pipe), tokens
+                // 8..15 (24..31) are already there
+                auto kstep = [&](int kb, float (&ca)[4], float (&cb)[4]) {
                     const uint2 wb = wimg[kb * 32 + lane];
-                    uint32_t p0, p1, p8, p9;
+                    uint32_t l01, h01, l89, h89;
                     if constexpr (EV) {
                         const uint2 u = *reinterpret_cast<const uint2*>(kw + 16 * kb + 2 * tig);
                         const uint2 v = *reinterpret_cast<const uint2*>(kw + 16 * kb + 2 * tig + 8);
-                        p0 = u.x; p1 = u.y; p8 = v.x; p9 = v.y;
+                        l01 = u.x; h01 = u.y; l89 = v.x; h89 = v.y;
                     } else {
-                        p0 = kw[16 * kb + 2 * tig];     p1 = kw[16 * kb + 2 * tig + 1];
-                        p8 = kw[16 * kb + 2 * tig + 8]; p9 = kw[16 * kb + 2 * tig + 9];
+                        const uint32_t p0 = kw[16 * kb + 2 * tig], p1 = kw[16 * kb + 2 * tig + 1];
+                        const uint32_t p8 = kw[16 * kb + 2 * tig + 8], p9 = kw[16 * kb + 2 * tig + 9];
+                        l01 = __byte_perm(p0, p1, 0x5410); h01 = __byte_perm(p0, p1, 0x7632);
+                        l89 = __byte_perm(p8, p9, 0x5410); h89 = __byte_perm(p8, p9, 0x7632);
                     }
-                    // byte b of both plane words -> high bytes of the two halves
-                    const uint32_t a[4] = {(__byte_perm(p0, p1, 0x4400) & mk) | bk, (__byte_perm(p0, p1, 0x5511) & mk) | bk,
-                                           (__byte_perm(p8, p9, 0x4400) & mk) | bk, (__byte_perm(p8, p9, 0x5511) & mk) | bk};
-                    const uint32_t c[4] = {(__byte_perm(p0, p1, 0x6622) & mk) | bk, (__byte_perm(p0, p1, 0x7733) & mk) | bk,
-                                           (__byte_perm(p8, p9, 0x6622) & mk) | bk, (__byte_perm(p8, p9, 0x7733) & mk) | bk};
-                    if (kb == 0) {
-                        mma16816(aA0, a, wb.x, wb.y);
-                        mma16816(aB0, c, wb.x, wb.y);
-                    } else if (kb & 1) {
-                        mma16816(aA2, a, wb.x, wb.y);
-                        mma16816(aB2, c, wb.x, wb.y);
-                    } else {
-                        mma16816(aA, a, wb.x, wb.y);
-                        mma16816(aB, c, wb.x, wb.y);
-                    }
+                    const uint32_t a[4] = {((l01 * 256u) & mk) | bk, (l01 & mk) | bk,
+                                           ((l89 * 256u) & mk) | bk, (l89 & mk) | bk};
+                    const uint32_t c[4] = {((h01 * 256u) & mk) | bk, (h01 & mk) | bk,
+                                           ((h89 * 256u) & mk) | bk, (h89 & mk) | bk};
+                    mma16816(ca, a, wb.x, wb.y);
+                    mma16816(cb, c, wb.x, wb.y);
+                };
+                kstep(0, aA0, aB0);
+                int kb = 1;
+#pragma unroll 1
+                for (; kb + 1 < nkbh; kb += 2) {
+                    kstep(kb, aA2, aB2);
+                    kstep(kb + 1, aA, aB);
                 }
+                if (kb < nkbh) kstep(kb, aA2, aB2);
             };
             if (RK & 1) kloop(std::false_type{});
             else kloop(std::true_type{});
@@ -388,35 +406,58 @@ attn_tc_split_kernel(AttnTcParams P)
         if (RV > 0) {
             const uint32_t* vwt = reinterpret_cast<const uint32_t*>(stg + P.kst);
             const int ngv = int(min(int64_t(TT / 32), (t_end - t0 + 31) / 32));
+            // two groups at a time into a fresh accumulator per m-tile, added to
+            // the running sums with rounding: a plane's sum is scaled by up to
+            // 2^7 in the output, so the tensor core's truncating accumulation
+            // must not run across the whole split.  Tokens s, s + 16 with s < 8
+            // reach the high bytes of the halves by a left shift of 8 (bytes 0,
+            // 2); s >= 8 are already there (bytes 1, 3).
             auto vloop = [&](auto even_tag) {
                 constexpr bool EV = decltype(even_tag)::value;
-                for (int g = 0; g < ngv; ++g) {
+                auto pfrag = [&](int g, uint2& pb0, uint2& pb1) {
                     const uint2* pg = reinterpret_cast<const uint2*>(pt + (g * 8 + g8) * PSTR) + tig;
-                    const uint2 pb0 = pg[0], pb1 = pg[4];
-                    const uint32_t* vw = vwt + g * RV;
+                    pb0 = pg[0];
+                    pb1 = pg[4];
+                };
+                auto vstep = [&](int g, int i, const uint2& pb0, const uint2& pb1, float (&t)[4]) {
+                    const uint32_t* vw = vwt + g * RV + 16 * (warp + kWarps * i) + 2 * g8;
+                    uint32_t w0, w1;
+                    if constexpr (EV) {
+                        const uint2 u = *reinterpret_cast<const uint2*>(vw);
+                        w0 = u.x; w1 = u.y;
+                    } else {
+                        w0 = vw[0]; w1 = vw[1];
+                    }
+                    const uint32_t x0 = w0 * 256u, x1 = w1 * 256u;
+                    const uint32_t a0[4] = {(x0 & mv0) | bv0, (x1 & mv0) | bv0, (x0 & mv1) | bv1, (x1 & mv1) | bv1};
+                    const uint32_t a1[4] = {(w0 & mv0) | bv0, (w1 & mv0) | bv0, (w0 & mv1) | bv1, (w1 & mv1) | bv1};
+                    mma16816(t, a0, pb0.x, pb0.y);
+                    mma16816(t, a1, pb1.x, pb1.y);
+                };
+                int g = 0;
+#pragma unroll 1
+                for (; g + 1 < ngv; g += 2) {
+                    uint2 pa0, pa1, pc0, pc1;
+                    pfrag(g, pa0, pa1);
+                    pfrag(g + 1, pc0, pc1);
 #pragma unroll
                     for (int i = 0; i < MTV; ++i) {
-                        const int mt = warp + kWarps * i;
-                        if (mt < nmtv) {
-                            uint32_t w0, w1;
-                            if constexpr (EV) {
-                                const uint2 u = *reinterpret_cast<const uint2*>(vw + 16 * mt + 2 * g8);
-                                w0 = u.x; w1 = u.y;
-                            } else {
-                                w0 = vw[16 * mt + 2 * g8]; w1 = vw[16 * mt + 2 * g8 + 1];
-                            }
-                            // bytes 0, 2 (tokens s, s + 16 for s < 8) and 1, 3 (s >= 8)
-                            const uint32_t x0 = __byte_perm(w0, w0, 0x2200), x1 = __byte_perm(w1, w1, 0x2200);
-                            const uint32_t y0 = __byte_perm(w0, w0, 0x3311), y1 = __byte_perm(w1, w1, 0x3311);
-                            const uint32_t a0[4] = {(x0 & mv0) | bv0, (x1 & mv0) | bv0, (x0 & mv1) | bv1, (x1 & mv1) | bv1};
-                            const uint32_t a1[4] = {(y0 & mv0) | bv0, (y1 & mv0) | bv0, (y0 & mv1) | bv1, (y1 & mv1) | bv1};
-                            // a fresh accumulator per group, added with rounding: a
-                            // plane's sum is scaled by up to 2^7 in the output, so the
-                            // tensor core's truncating accumulation must not run
-                            // across the whole split
+                        if (warp + kWarps * i < nmtv) {
                             float t[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma16816(t, a0, pb0.x, pb0.y);
-                            mma16816(t, a1, pb1.x, pb1.y);
+                            vstep(g, i, pa0, pa1, t);
+                            vstep(g + 1, i, pc0, pc1, t);
+                            acc[i][0] += t[0]; acc[i][1] += t[1]; acc[i][2] += t[2]; acc[i][3] += t[3];
+                        }
+                    }
+                }
+                if (g < ngv) {
+                    uint2 pa0, pa1;
+                    pfrag(g, pa0, pa1);
+#pragma unroll
+                    for (int i = 0; i < MTV; ++i) {
+                        if (warp + kWarps * i < nmtv) {
+                            float t[4] = {0.f, 0.f, 0.f, 0.f};
+                            vstep(g, i, pa0, pa1, t);
                             acc[i][0] += t[0]; acc[i][1] += t[1]; acc[i][2] += t[2]; acc[i][3] += t[3];
                         }
                     }
