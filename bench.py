@@ -57,6 +57,8 @@ def parse():
                     help="skip the separate compressed-attention measurement")
     ap.add_argument("--copies", type=int, default=NCOPY,
                     help="rotating input/output copies (L2 defeat); fewer for profiling captures")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip the budget sweep and the Qwen-shaped RWHT workload")
     ap.add_argument("--attn-only", action="store_true",
                     help="profiling captures: calibrate one layer, then time only the compressed-attention "
                          "workload (prints its block, not a bench line)")
@@ -70,7 +72,7 @@ class ClockSampler:
     """nvidia-smi samples during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, index: int):
         self.index = index
@@ -99,22 +101,28 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        sm, smax, busy, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [v.strip() for v in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
                 sm.append(float(f[1]))
                 smax.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                busy.append(float(f[9]) >= 50.0)
+            except ValueError:
+                busy.append(True)
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
+        loaded = [c for c, b in zip(sm, busy) if b] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "busy_samples": sum(busy),
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -298,7 +306,13 @@ def run_ours(args, rank, world, local_rank):
             "peak_source": peaks["source"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": _traffic(dom)}
 
-    attn = attn_workload(spx, kp, vp, dev, _peaks(), batch=args.attn_batch) if args.attn_workload else None
+    attn = None
+    if args.attn_workload:
+        attn = attn_workload(spx, kp, vp, dev, _peaks(), reps=50, batch=args.attn_batch, local_rank=local_rank)
+    sweep = qwen = None
+    if args.workloads:
+        sweep = budget_sweep(spx, K, V, dev, _peaks(), local_rank)
+        qwen = qwen_rwht(spx, dev, _peaks(), local_rank)
 
     res = {
         "metric": METRIC, "value": round(_whole_job_rate(T_TOK, world, ms), 1), "unit": UNIT, "n_gpus": world,
@@ -310,10 +324,14 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"{NCOPY} rotating input/output copies, {NCOPY * 2 * T_TOK * H_KV * D * 2 >> 20} MiB of inputs > L2"},
         "phases_ms": {k: round(v, 4) for k, v in ph.items()},
         "jacobi_sweeps": {"min": min(sweeps), "max": max(sweeps)},
-        "codec_tokens_per_s": round(T_TOK / ((ph["encode"] + ph["decode"]) * 1e-3), 1),
+        "codec_value": round(_whole_job_rate(T_TOK, world, ph["encode"] + ph["decode"]), 1),
+        "codec_value_note": "encode + decode phases only (the codec's rate; value also counts calibration)",
+        "calibrate_ms": round(ph["calibrate"], 4),
         "roofline": roof,
         "rotation": _rotation_rate(T_TOK, H_KV, D, 3, ph["encode"] / 2, peaks["bf16_tflops"]),
         "attn_decode": attn,
+        "budget_sweep": sweep,
+        "qwen_rwht": qwen,
         "clocks": clocks,
         "e2e": {"value": round(_whole_job_rate(T_TOK, world, e2e_ms), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
@@ -325,7 +343,7 @@ def run_ours(args, rank, world, local_rank):
 ATTN_B, ATTN_CTX = 16, 65536
 
 
-def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None):
+def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None, local_rank=None):
     """Decode-step attention at the compressed-attention workload: batch 16,
     32 query heads over 8 kv heads, 65536-token context packed at the plans'
     2.0 bits/value (K and V streams of 16 x 8 x 65536 tokens).  The stream
@@ -349,18 +367,31 @@ def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None):
     ws = torch.empty((spx.spectra_attn_workspace_bytes(ATTN_B, HQ, D, ATTN_CTX) + 256,), dtype=torch.uint8,
                      device=dev)
     s = torch.cuda.current_stream()
+
+    def call(i):
+        kc, vc = sets[i % 2]
+        spx.spectra_attn_decode(kp, vp, q, kc, vc, ATTN_CTX, 1.0, out, workspace=ws)
     for i in range(warm):
-        kc, vc = sets[i % 2]
-        spx.spectra_attn_decode(kp, vp, q, kc, vc, ATTN_CTX, 1.0, out, workspace=ws)
+        call(i)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for i in range(reps):
-        kc, vc = sets[i % 2]
-        spx.spectra_attn_decode(kp, vp, q, kc, vc, ATTN_CTX, 1.0, out, workspace=ws)
-    e1.record(s)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+
+    def timed():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for i in range(reps):
+            call(i)
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def load():
+        for i in range(20):
+            call(i)
+    if local_rank is None:
+        total_ms, clocks = timed(), None
+    else:
+        total_ms, clocks = clocked(local_rank, timed, load, before=0.3, after=0.2)
+    ms = total_ms / reps
     nbytes = 2 * ATTN_B * H_KV * (ATTN_CTX // 32) * 4 * R      # packed K and V words read
     gbs = nbytes / (ms * 1e-3) / 1e9
     del sets
@@ -368,7 +399,258 @@ def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None):
                         f"{R} bits per token and head (K and V)", "ms": round(ms, 4),
             "packed_bytes": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": peaks["hbm_gbs"],
             "frac": round(gbs / peaks["hbm_gbs"], 4), "cached_tokens_per_s": round(ATTN_B * ATTN_CTX / (ms * 1e-3), 1),
-            "l2": "2 rotating stream sets (2 x 537 MB) > L2"}
+            "l2": "2 rotating stream sets (2 x 537 MB) > L2", "clocks": clocks}
+
+
+
+def clocked(local_rank, timed, load, before=0.4, after=0.3):
+    """Run `timed()` with nvidia-smi clock samples around it; `load()` runs
+    the same work untimed for about `before` / `after` seconds so the 100 ms
+    samples see the GPU under this load.  Returns (timed(), clocks)."""
+    import torch
+    clk = ClockSampler(local_rank)
+    clk.start()
+    t_end = time.perf_counter() + before
+    while time.perf_counter() < t_end:
+        load()
+        torch.cuda.synchronize()
+    res = timed()
+    t_end = time.perf_counter() + after
+    while time.perf_counter() < t_end:
+        load()
+        torch.cuda.synchronize()
+    return res, clk.stop()
+
+
+def _events_ms(fn, reps, warm=2):
+    import torch
+    for _ in range(warm):
+        fn(0)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s = torch.cuda.current_stream()
+    e0.record(s)
+    for i in range(reps):
+        fn(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def _relmse_cos(x, xh):
+    """relMSE ||x - xh||^2 / ||x||^2 and mean per-vector cosine (metrics on the
+    device output, in fp64 on the device)."""
+    x64, h64 = x.double(), xh.double()
+    rel = float(((x64 - h64) ** 2).sum() / (x64 ** 2).sum())
+    cos = float(((x64 * h64).sum(-1) / ((x64 * x64).sum(-1) * (h64 * h64).sum(-1)).sqrt().clamp_min(1e-300)).mean())
+    return rel, cos
+
+
+SWEEP_BUDGETS = (4.0, 2.0, 1.33)
+
+
+def budget_sweep(spx, K, V, dev, peaks, local_rank, reps=10):
+    """The Llama-shaped layer swept over budgets of 4.0, 2.0 and 1.33
+    bits/value (4x / 8x / 12x against bf16) with Gaussian Lloyd-Max levels;
+    K and V calibrated (first 2048 tokens) and allocated separately.  Per
+    budget: encode and decode time of K and V (two rotating input copies
+    keep the reads out of L2), the roofline fraction of each, relMSE and
+    cosine of the device reconstruction over the whole layer, and the
+    oracle's own end-to-end relMSE next to the device's on a sampled slice
+    (tokens 2048..4095, all heads)."""
+    import numpy as np
+    import torch
+
+    import oracle as orc
+    T = K[0].shape[0]
+    kp = spx.Plan(H_KV, D, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev)
+    vp = spx.Plan(H_KV, D, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev)
+    spx.spectra_calibrate(kp, K[0], n_cal=N_CAL)
+    spx.spectra_calibrate(vp, V[0], n_cal=N_CAL)
+    sl = slice(N_CAL, 2 * N_CAL)
+    kcal = K[0][:N_CAL].float().cpu().numpy().astype(np.float64)
+    vcal = V[0][:N_CAL].float().cpu().numpy().astype(np.float64)
+    ksl = K[0][sl].float().cpu().numpy().astype(np.float64)
+    vsl = V[0][sl].float().cpu().numpy().astype(np.float64)
+    ko = torch.empty_like(K[0])
+    vo = torch.empty_like(V[0])
+    out = []
+    for B in SWEEP_BUDGETS:
+        spx.spectra_alloc_bits(kp, B)
+        spx.spectra_alloc_bits(vp, B)
+        kc = [kp.new_streams(T) for _ in range(2)]
+        vc = [vp.new_streams(T) for _ in range(2)]
+
+        def enc(i):
+            spx.spectra_encode(kp, K[i % 2], kc[i % 2])
+            spx.spectra_encode(vp, V[i % 2], vc[i % 2])
+
+        def dec(i):
+            spx.spectra_decode(kp, kc[i % 2], T, ko)
+            spx.spectra_decode(vp, vc[i % 2], T, vo)
+        def load():
+            enc(0)
+            dec(0)
+        (enc_ms, dec_ms), clocks = clocked(local_rank, lambda: (_events_ms(enc, reps), _events_ms(dec, reps)),
+                                           load, before=0.3, after=0.2)
+        enc(0)
+        dec(0)
+        torch.cuda.synchronize()
+        R = kp.max_rec_bits
+        launch_bytes = T * H_KV * (2 * D + R / 8)
+        rk, ck = _relmse_cos(K[0], ko)
+        rv, cv = _relmse_cos(V[0], vo)
+        # the oracle's whole path (its own calibration on the same tokens) on the slice
+        okp = orc.make_eigen_plan(kcal, B, orc.QUANT_LLOYD)
+        ovp = orc.make_eigen_plan(vcal, B, orc.QUANT_LLOYD)
+        kh = orc.decode(okp, [e["stream"] for e in orc.encode(okp, ksl)], ksl.shape[0])
+        vh = orc.decode(ovp, [e["stream"] for e in orc.encode(ovp, vsl)], vsl.shape[0])
+        dk, _ = _relmse_cos(K[0][sl], ko[sl])
+        dv, _ = _relmse_cos(V[0][sl], vo[sl])
+        out.append({"avg_bits": B, "rec_bits": R, "compression_vs_bf16": round(16.0 * D / R, 2),
+                    "encode_ms": round(enc_ms, 4), "decode_ms": round(dec_ms, 4),
+                    "encode_frac": round(launch_bytes / (enc_ms / 2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "decode_frac": round(launch_bytes / (dec_ms / 2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "codec_tokens_per_s": round(T / ((enc_ms + dec_ms) * 1e-3), 1),
+                    "relmse_k": round(rk, 6), "relmse_v": round(rv, 6), "cosine_k": round(ck, 6),
+                    "cosine_v": round(cv, 6),
+                    "slice": {"tokens": f"{N_CAL}..{2 * N_CAL - 1}, all heads",
+                              "relmse_k_device": round(dk, 6), "relmse_k_oracle": round(orc.relmse(ksl, kh), 6),
+                              "relmse_v_device": round(dv, 6), "relmse_v_oracle": round(orc.relmse(vsl, vh), 6)},
+                    "clocks": clocks})
+        del kc, vc
+    return {"workload": ("llama3.1-8b-shaped layer (8 kv heads x 32768 tokens, d 128, bf16), Gaussian "
+                         "Lloyd-Max levels, K and V calibrated and allocated separately"),
+            "budgets": out, "l2": "2 rotating input/output copies (128 MiB of inputs per copy)"}
+
+
+QWEN_LAYERS, QWEN_KV, QWEN_T = 28, 4, 131072
+
+
+def qwen_rwht(spx, dev, peaks, local_rank, steps=4, e2e_steps=2, seed=2024):
+    """Data-independent variant at the Qwen2.5-7B shape: 28 layers x 4 kv
+    heads (one call over 112 heads), 131072 tokens per head, bf16 K and V
+    from the spiked + outlier generator; randomized Walsh-Hadamard rotation
+    with seeded +-1 signs, then the fixed 3-bit Gaussian Lloyd-Max codebook
+    on every channel with the per-token fp32 norm.  A step encodes and
+    decodes K and V (9.04 GB of algorithmic traffic each way; inputs far
+    larger than L2).  value = positions per second (a position = all 112
+    heads, K and V)."""
+    import torch
+
+    import synth
+    H = QWEN_LAYERS * QWEN_KV
+    T = QWEN_T
+    K = synth.spiked_t_torch(seed, T, H, D, role=synth.ROLE_K, device=dev)
+    V = synth.spiked_t_torch(seed, T, H, D, role=synth.ROLE_V, device=dev)
+    plans = []
+    for role, sgn_seed in ((synth.ROLE_K, seed), (synth.ROLE_V, seed + 1)):
+        p = spx.Plan(H, D, basis=spx.SPECTRA_BASIS_RWHT, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev)
+        p.signs.copy_(torch.from_numpy(synth.rwht_signs(sgn_seed, H, D)))
+        spx.spectra_alloc_bits(p, 0.0, fixed_bits=3)
+        plans.append(p)
+    kp, vp = plans
+    kc, vc = kp.new_streams(T), vp.new_streams(T)
+    kn = torch.empty((H, T), dtype=torch.float32, device=dev)
+    vn = torch.empty((H, T), dtype=torch.float32, device=dev)
+    ko, vo = torch.empty_like(K), torch.empty_like(V)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step(i=0, mark=False):
+        if mark:
+            ev[0].record()
+        spx.spectra_encode(kp, K, kc, norms=kn)
+        spx.spectra_encode(vp, V, vc, norms=vn)
+        if mark:
+            ev[1].record()
+        spx.spectra_decode(kp, kc, T, ko, norms=kn)
+        spx.spectra_decode(vp, vc, T, vo, norms=vn)
+        if mark:
+            ev[2].record()
+
+    def timed():
+        ms = _events_ms(step, steps)
+        step(mark=True)
+        torch.cuda.synchronize()
+        return ms, ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+    (ms, enc_ms, dec_ms), clocks = clocked(local_rank, timed, lambda: step())
+    rk, ck = _relmse_cos(K[:4096], ko[:4096])
+    rv, cv = _relmse_cos(V[:4096], vo[:4096])
+    per_vec = 2 * D + 3 * D / 8 + 4
+    launch_bytes = T * H * per_vec
+    dom_ms = max(enc_ms, dec_ms) / 2
+    achieved = launch_bytes / (dom_ms * 1e-3) / 1e9
+    res = {"workload": (f"qwen2.5-7b-shaped cache: {QWEN_LAYERS} layers x {QWEN_KV} kv heads, {T} tokens, "
+                        "d 128, bf16 K and V (spiked+outlier Student-t(4) synthetic); RWHT with seeded signs, "
+                        "fixed 3-bit Gaussian Lloyd-Max, fp32 norm per token; encode+decode K,V"),
+           "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s (a token = one position, all 112 heads, K and V)",
+           "ms_per_step": round(ms, 4), "phases_ms": {"encode": round(enc_ms, 4), "decode": round(dec_ms, 4)},
+           "roofline": {"bound": "hbm", "kernel": "encode" if enc_ms >= dec_ms else "decode",
+                        "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                        "bytes_per_vector": per_vec},
+           "relmse_k": round(rk, 6), "relmse_v": round(rv, 6), "cosine_k": round(ck, 6), "cosine_v": round(cv, 6),
+           "clocks": clocks}
+    # end to end: pinned host K, V in, codes and norms out, every step
+    try:
+        hK = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
+        hV = torch.empty(V.shape, dtype=V.dtype, pin_memory=True)
+        hK.copy_(K)
+        hV.copy_(V)
+        hkc = torch.empty(kc.shape, dtype=kc.dtype, pin_memory=True)
+        hvc = torch.empty(vc.shape, dtype=vc.dtype, pin_memory=True)
+        hkn = torch.empty(kn.shape, dtype=kn.dtype, pin_memory=True)
+        hvn = torch.empty(vn.shape, dtype=vn.dtype, pin_memory=True)
+
+        def e2e(i=0):
+            K.copy_(hK, non_blocking=True)
+            V.copy_(hV, non_blocking=True)
+            step()
+            hkc.copy_(kc, non_blocking=True)
+            hvc.copy_(vc, non_blocking=True)
+            hkn.copy_(kn, non_blocking=True)
+            hvn.copy_(vn, non_blocking=True)
+        e_ms = _events_ms(e2e, e2e_steps, warm=1)
+        res["e2e"] = {"value": round(T / (e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e_ms, 2),
+                      "h2d_bytes_per_step": 2 * K.numel() * 2,
+                      "d2h_bytes_per_step": hkc.numel() + hvc.numel() + 4 * (hkn.numel() + hvn.numel())}
+        del hK, hV, hkc, hvc, hkn, hvn
+    except RuntimeError as e:
+        res["e2e"] = {"unavailable": f"pinned host buffers for the 7.5 GB cache: {e}".splitlines()[0]}
+    res["cpu_baseline"] = qwen_oracle_sample()
+    del K, V, ko, vo, kc, vc, kn, vn
+    torch.cuda.empty_cache()
+    return res
+
+
+def qwen_oracle_sample(T=4096, seed=2024):
+    """The oracle's RWHT + 3-bit Lloyd-Max encode and decode of one layer's
+    4 kv heads x T tokens, K and V, threads over heads; scaled to positions
+    of the whole 112-head cache per second."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle as orc
+    import synth
+    H = QWEN_KV
+    xs = [synth.to_bf16_exact(synth.spiked_t(seed, T, H, D, role=r)).astype(np.float64)
+          for r in (synth.ROLE_K, synth.ROLE_V)]
+    plans = [orc.make_rwht_plan(synth.rwht_signs(seed + i, H, D), 3) for i in range(2)]
+    orc.lloyd_max_tables()
+    cores = min(2 * H, os.cpu_count() or 1)
+
+    def job(a):
+        side, h = a
+        e = orc.encode_head(plans[side], h, xs[side][:, h, :])
+        return orc.decode_head(plans[side], h, e["stream"], T, e["norms"])
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(cores) as pool:
+        list(pool.map(job, [(s, h) for s in range(2) for h in range(H)]))
+    wall = time.perf_counter() - t0
+    vec_per_s = 2 * H * T / wall
+    return {"value": round(vec_per_s / (2 * QWEN_LAYERS * QWEN_KV), 2), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle", "sample": f"1 layer x {H} kv heads x {T} tokens, K and V encode+decode; wall {wall:.1f} s"}
 
 
 def launches_per_step():
@@ -440,7 +722,7 @@ def _rotation_rate(tokens, heads, d, terms, launch_ms, peak_tflops):
     algorithmic = executed / terms
     return {"executed_tflops": round(executed, 1), "algorithmic_tflops": round(algorithmic, 1),
             "terms": terms, "peak_tflops": peak_tflops, "frac_executed": round(executed / peak_tflops, 4),
-            "unit": "TFLOP/s"}
+            "frac_algorithmic": round(algorithmic / peak_tflops, 4), "unit": "TFLOP/s"}
 
 
 def _whole_job_rate(units_per_rank, world, ms_max):
