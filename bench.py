@@ -309,9 +309,10 @@ def run_ours(args, rank, world, local_rank):
     attn = None
     if args.attn_workload:
         attn = attn_workload(spx, kp, vp, dev, _peaks(), reps=50, batch=args.attn_batch, local_rank=local_rank)
-    sweep = qwen = None
+    sweep = qwen = var = None
     if args.workloads:
         sweep = budget_sweep(spx, K, V, dev, _peaks(), local_rank)
+        var = variants(spx, K, V, q, dev, local_rank)
         qwen = qwen_rwht(spx, dev, _peaks(), local_rank)
 
     res = {
@@ -331,6 +332,7 @@ def run_ours(args, rank, world, local_rank):
         "rotation": _rotation_rate(T_TOK, H_KV, D, 3, ph["encode"] / 2, peaks["bf16_tflops"]),
         "attn_decode": attn,
         "budget_sweep": sweep,
+        "variants": var,
         "qwen_rwht": qwen,
         "clocks": clocks,
         "e2e": {"value": round(_whole_job_rate(T_TOK, world, e2e_ms), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -500,11 +502,15 @@ def budget_sweep(spx, K, V, dev, peaks, local_rank, reps=10):
         launch_bytes = T * H_KV * (2 * D + R / 8)
         rk, ck = _relmse_cos(K[0], ko)
         rv, cv = _relmse_cos(V[0], vo)
-        # the oracle's whole path (its own calibration on the same tokens) on the slice
+        # CPU baseline leg: the oracle's whole path (its own calibration on the
+        # same 2048 tokens, then encode + decode of the slice), timed, with its
+        # reconstruction error next to the device's on the same tokens
+        t_or = time.perf_counter()
         okp = orc.make_eigen_plan(kcal, B, orc.QUANT_LLOYD)
         ovp = orc.make_eigen_plan(vcal, B, orc.QUANT_LLOYD)
         kh = orc.decode(okp, [e["stream"] for e in orc.encode(okp, ksl)], ksl.shape[0])
         vh = orc.decode(ovp, [e["stream"] for e in orc.encode(ovp, vsl)], vsl.shape[0])
+        wall = time.perf_counter() - t_or
         dk, _ = _relmse_cos(K[0][sl], ko[sl])
         dv, _ = _relmse_cos(V[0][sl], vo[sl])
         out.append({"avg_bits": B, "rec_bits": R, "compression_vs_bf16": round(16.0 * D / R, 2),
@@ -514,14 +520,94 @@ def budget_sweep(spx, K, V, dev, peaks, local_rank, reps=10):
                     "codec_tokens_per_s": round(T / ((enc_ms + dec_ms) * 1e-3), 1),
                     "relmse_k": round(rk, 6), "relmse_v": round(rv, 6), "cosine_k": round(ck, 6),
                     "cosine_v": round(cv, 6),
-                    "slice": {"tokens": f"{N_CAL}..{2 * N_CAL - 1}, all heads",
-                              "relmse_k_device": round(dk, 6), "relmse_k_oracle": round(orc.relmse(ksl, kh), 6),
-                              "relmse_v_device": round(dv, 6), "relmse_v_oracle": round(orc.relmse(vsl, vh), 6)},
+                    "slice_relmse_k": round(dk, 6), "slice_relmse_v": round(dv, 6),
+                    "cpu_baseline": {"value": round(ksl.shape[0] / wall, 2), "unit": "tokens/s", "cores": 1,
+                                     "kind": "oracle",
+                                     "sample": (f"calibrate K,V on {N_CAL} tokens x {H_KV} heads, allocate, encode+"
+                                                f"decode tokens {N_CAL}..{2 * N_CAL - 1} (all heads); wall {wall:.1f} s"),
+                                     "slice_relmse_k": round(orc.relmse(ksl, kh), 6),
+                                     "slice_relmse_v": round(orc.relmse(vsl, vh), 6)},
                     "clocks": clocks})
         del kc, vc
     return {"workload": ("llama3.1-8b-shaped layer (8 kv heads x 32768 tokens, d 128, bf16), Gaussian "
                          "Lloyd-Max levels, K and V calibrated and allocated separately"),
             "budgets": out, "l2": "2 rotating input/output copies (128 MiB of inputs per copy)"}
+
+
+def variants(spx, K, V, q, dev, local_rank, reps=10):
+    """The ablation page's schemes on the Llama-shaped layer at 2.0
+    bits/value (uniform +-3 sigma quantizer): SpectralQuant with
+    water-filling, SQU-KV (one width on every channel), grouped widths of 4
+    and 16 adjacent channels, the gap-pruned effective dimension (energy
+    0.95), and Plain-KV (no rotation).  Per scheme: encode and decode time (K
+    and V), relMSE / cosine / d^2 = relMSE^2 + (1 - cos)^2 of K and V, and the
+    decode-step attention output (32 query heads over the packed cache)
+    against fp32 attention over the uncompressed cache -- the 6-D error
+    geometry (K, V, output)."""
+    import torch
+    T = K[0].shape[0]
+    x = (K[0], V[0])
+    Kf, Vf = K[0].float(), V[0].float()
+    G = HQ // H_KV
+    qf = q.float()[0]
+    ref = torch.empty((HQ, D), device=dev)
+    for j in range(HQ):
+        s_ = Kf[:, j // G, :] @ qf[j]
+        ref[j] = torch.softmax(s_, 0) @ Vf[:, j // G, :]
+
+    def plans(kind):
+        ps = []
+        de = torch.zeros(H_KV, dtype=torch.int32, device=dev)
+        dg = torch.zeros(H_KV, dtype=torch.int32, device=dev)
+        info = {}
+        for side in range(2):
+            p = spx.Plan(H_KV, D, device=dev)
+            if kind == "plain_kv":
+                spx.spectra_calibrate_plain(p, x[side], n_cal=N_CAL)
+            else:
+                spx.spectra_calibrate(p, x[side], n_cal=N_CAL)
+            if kind == "sq_waterfill" or kind == "plain_kv":
+                spx.spectra_alloc_bits(p, AVG_BITS)
+            elif kind == "squ_uniform":
+                spx.spectra_alloc_bits(p, 0.0, fixed_bits=int(AVG_BITS))
+            elif kind.startswith("grouped"):
+                spx.spectra_alloc_bits_ex(p, AVG_BITS, int(kind[7:]))
+            elif kind == "deff_gap":
+                spx.spectra_effective_dim(p, 0.95, de, dg)
+                spx.spectra_alloc_bits_ex(p, AVG_BITS, 1, dg)
+                torch.cuda.synchronize()
+                info["KV"[side]] = {"d_energy": de.tolist(), "d_gap": dg.tolist()}
+            ps.append(p)
+        return ps, info
+
+    def err(a, b):
+        rel, cos = _relmse_cos(a, b)
+        return {"relmse": round(rel, 6), "cosine": round(cos, 6), "d2": round(rel ** 2 + (1 - cos) ** 2, 8)}
+    out = {}
+    att = torch.empty((1, HQ, D), device=dev)
+    for kind in ("sq_waterfill", "squ_uniform", "grouped4", "grouped16", "deff_gap", "plain_kv"):
+        (kp, vp), info = plans(kind)
+        kc, vc = kp.new_streams(T), vp.new_streams(T)
+        ko, vo = torch.empty_like(K[0]), torch.empty_like(V[0])
+
+        def enc(i):
+            spx.spectra_encode(kp, K[0], kc)
+            spx.spectra_encode(vp, V[0], vc)
+
+        def dec(i):
+            spx.spectra_decode(kp, kc, T, ko)
+            spx.spectra_decode(vp, vc, T, vo)
+        enc_ms = _events_ms(enc, reps)
+        dec_ms = _events_ms(dec, reps)
+        spx.spectra_attn_decode(kp, vp, q, kc, vc, T, 1.0, att)
+        torch.cuda.synchronize()
+        out[kind] = {"rec_bits": [kp.max_rec_bits, vp.max_rec_bits], "encode_ms": round(enc_ms, 4),
+                     "decode_ms": round(dec_ms, 4), "K": err(K[0], ko), "V": err(V[0], vo),
+                     "attn_out": err(ref[None], att), **info}
+        del kc, vc, ko, vo
+    return {"workload": "llama3.1-8b-shaped layer, 2.0 bits/value (uniform +-3 sigma), attention of 32 q heads "
+                        "over the 32768-token packed cache against fp32 attention over the bf16 cache",
+            "schemes": out}
 
 
 QWEN_LAYERS, QWEN_KV, QWEN_T = 28, 4, 131072
@@ -623,7 +709,7 @@ def qwen_rwht(spx, dev, peaks, local_rank, steps=4, e2e_steps=2, seed=2024):
     return res
 
 
-def qwen_oracle_sample(T=4096, seed=2024):
+def qwen_oracle_sample(T=16384, seed=2024):
     """The oracle's RWHT + 3-bit Lloyd-Max encode and decode of one layer's
     4 kv heads x T tokens, K and V, threads over heads; scaled to positions
     of the whole 112-head cache per second."""

@@ -186,6 +186,58 @@ SPECTRA_API spectra_status spectra_alloc_bits(spectra_plan* plan, double avg_bit
                                   spectra_stream_t stream);
 
 /*
+ * spectra_alloc_bits_ex -- grouped reverse water-filling over the leading
+ * channels, then finalize.  ("Sintesi Tecnica: SPECTRA", "La Pipeline di
+ * SPECTRA" phase 2, "Raggruppamento": adjacent latent coordinates share one
+ * bit width, keeping the cache append-only and streamable; "Technisch
+ * Overzicht ...", "Regime-Specifieke Prestaties": the effective dimension is
+ * pruned and the channels past it are left out.)
+ * EIGEN plans.  With R_tot = min(floor(avg_bits * d + 1e-9), 8 d): the first
+ *   keep[h] channels of head h form floor(keep[h] / group) groups of `group`
+ *   consecutive channels (eigenvalue-descending order); every other channel
+ *   gets 0 bits.  floor(R_tot / group) one-bit steps (fewer if every kept
+ *   group reaches 8 bits), each giving all channels of the group with the
+ *   largest Lam_G * 4^-b_G one bit (Lam_G = sum of the group's eigenvalues
+ *   clipped at 0, in fp64 in ascending channel order; lowest group on ties).
+ *   group = 1 with keep = NULL is spectra_alloc_bits.
+ * group: a power of two dividing head_dim.  keep: device int32[heads]
+ *   (values clipped to 0..d), or NULL for all channels -- for instance the
+ *   d_gap output of spectra_effective_dim.
+ * Sets plan->max_rec_bits = group * floor(R_tot / group) on the host.
+ */
+SPECTRA_API spectra_status spectra_alloc_bits_ex(spectra_plan* plan, double avg_bits, int group,
+                                     const int32_t* keep, spectra_stream_t stream);
+
+/*
+ * spectra_effective_dim -- effective dimension of each head's spectrum,
+ * with spectral-gap pruning.  ("Technisch Overzicht ...", "Regime-Specifieke
+ * Prestaties": d_eff follows the calibration budget rather than the true
+ * rank, and a single spurious eigenvalue can flip the output, so a spectral-
+ * gap criterion prunes the estimate.  The page gives no formula; this is the
+ * library's reading.)  On plan->eigvals (descending, clipped at 0):
+ *   d_energy[h] = the smallest k with lam_0 + ... + lam_{k-1} >= energy * sum
+ *                 (0 for an all-zero spectrum), sums in fp64;
+ *   d_gap[h]    = the k in 1 .. min(d_energy, d - 1) with the largest
+ *                 lam_{k-1} / lam_k (lam_k = 0 counts as infinite), the
+ *                 smallest such k on ties.
+ * energy in (0, 1]; d_energy, d_gap: device int32[heads].
+ */
+SPECTRA_API spectra_status spectra_effective_dim(const spectra_plan* plan, double energy, int32_t* d_energy,
+                                     int32_t* d_gap, spectra_stream_t stream);
+
+/*
+ * spectra_calibrate_plain -- calibration without rotation (the ablation
+ * page's Plain-KV: "Technisch Overzicht ...", "Belangrijkste Bijdragen" 1,
+ * scalar quantization without rotation).  basis_mat = identity and
+ * eigvals[h][c] = (1/n_cal) sum_t x[t,h,c]^2, the raw coordinates' second
+ * moments in their own order; status[h] = 0 (or -SPECTRA_ERR_NONFINITE).
+ * x, n_cal, token_stride and the workspace as for spectra_calibrate.
+ */
+SPECTRA_API spectra_status spectra_calibrate_plain(spectra_plan* plan, const void* x, spectra_dtype dt,
+                                       int64_t n_cal, int64_t token_stride, void* workspace,
+                                       size_t workspace_bytes, spectra_stream_t stream);
+
+/*
  * spectra_plan_finalize -- recompute rec_bits and the derived tables from a
  * plan whose bits (and eigvals / basis_mat / signs) the caller filled in.
  * plan->max_rec_bits must already bound every R_h.

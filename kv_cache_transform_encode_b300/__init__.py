@@ -35,7 +35,8 @@ SPECTRA_KERNELS_AUTO, SPECTRA_KERNELS_CUDA_CORE, SPECTRA_KERNELS_TENSOR_CORE = 0
 EXPORTS = ("spectra_version", "spectra_set_kernel_family", "spectra_get_kernel_family",
            "spectra_status_string", "spectra_plan_derived_bytes",
            "spectra_stream_bytes", "spectra_calibrate_workspace_bytes", "spectra_calibrate",
-           "spectra_alloc_bits", "spectra_plan_finalize", "spectra_encode", "spectra_decode",
+           "spectra_alloc_bits", "spectra_alloc_bits_ex", "spectra_effective_dim", "spectra_calibrate_plain",
+           "spectra_plan_finalize", "spectra_encode", "spectra_decode",
            "spectra_attn_workspace_bytes", "spectra_attn_decode", "spectra_attn_decode_noalloc")
 
 
@@ -81,6 +82,9 @@ def lib() -> C.CDLL:
             "spectra_calibrate_workspace_bytes": (sz, [C.c_int, C.c_int, i64]),
             "spectra_calibrate": (C.c_int, [P, vp, C.c_int, i64, i64, C.c_int, vp, sz, vp, vp]),
             "spectra_alloc_bits": (C.c_int, [P, f64, C.c_int, vp]),
+            "spectra_alloc_bits_ex": (C.c_int, [P, f64, C.c_int, vp, vp]),
+            "spectra_effective_dim": (C.c_int, [P, f64, vp, vp, vp]),
+            "spectra_calibrate_plain": (C.c_int, [P, vp, C.c_int, i64, i64, vp, sz, vp]),
             "spectra_plan_finalize": (C.c_int, [P, vp]),
             "spectra_encode": (C.c_int, [P, vp, C.c_int, i64, i64, vp, i64, vp, i64, vp]),
             "spectra_decode": (C.c_int, [P, vp, i64, vp, i64, i64, vp, C.c_int, i64, vp]),
@@ -213,6 +217,36 @@ def spectra_alloc_bits(plan: Plan, avg_bits: float, fixed_bits: int = 0, stream=
     st = lib().spectra_alloc_bits(C.byref(p), float(avg_bits), int(fixed_bits), _stream(stream))
     _check(st, "spectra_alloc_bits")
     plan.max_rec_bits = p.max_rec_bits
+
+
+def spectra_alloc_bits_ex(plan: Plan, avg_bits: float, group: int = 1, keep: torch.Tensor | None = None,
+                          stream=None):
+    """Grouped water-filling over the first keep[h] channels (keep: int32
+    cuda tensor [heads] or None)."""
+    p = plan.c()
+    st = lib().spectra_alloc_bits_ex(C.byref(p), float(avg_bits), int(group), _ptr(keep), _stream(stream))
+    _check(st, "spectra_alloc_bits_ex")
+    plan.max_rec_bits = p.max_rec_bits
+
+
+def spectra_effective_dim(plan: Plan, energy: float, d_energy: torch.Tensor, d_gap: torch.Tensor, stream=None):
+    """d_energy, d_gap: int32 cuda tensors [heads] (outputs)."""
+    p = plan.c()
+    _check(lib().spectra_effective_dim(C.byref(p), float(energy), _ptr(d_energy), _ptr(d_gap), _stream(stream)),
+           "spectra_effective_dim")
+
+
+def spectra_calibrate_plain(plan: Plan, x: torch.Tensor, n_cal: int | None = None,
+                            workspace: torch.Tensor | None = None, stream=None):
+    """Identity basis, raw second moments (Plain-KV); x as for spectra_calibrate."""
+    n_cal = x.shape[0] if n_cal is None else n_cal
+    need = spectra_calibrate_workspace_bytes(plan.heads, plan.head_dim, n_cal)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=x.device)
+    p = plan.c()
+    st = lib().spectra_calibrate_plain(C.byref(p), _ptr(x), _dt(x), n_cal, x.stride(0), _ptr(workspace),
+                                       workspace.numel(), _stream(stream))
+    _check(st, "spectra_calibrate_plain")
 
 
 def spectra_plan_finalize(plan: Plan, stream=None):

@@ -66,6 +66,101 @@ alloc_kernel(const float* __restrict__ eig, int R, int fixed_bits, uint8_t* __re
     if (k == 0) bo[c] = uint8_t(__popc((sm >> (lane & ~7)) & 0xFFu));
 }
 
+// Grouped reverse water-filling ("La Pipeline di SPECTRA" phase 2,
+// "Raggruppamento": adjacent latent coordinates share one width), over the
+// first keep[h] channels (the rest get 0 bits: the effective-dimension
+// pruning of "Technisch Overzicht ...", "Regime-Specifieke Prestaties").
+// Groups of g consecutive channels, floor(keep / g) of them; the greedy's
+// steps give a whole group one bit each, on the key Lam_G 4^-b with Lam_G the
+// group's clipped eigenvalues summed in fp64 in ascending channel order.  The
+// same top-`steps` selection as alloc_kernel, over the keys Lam_G 4^-k of the
+// kept groups (thread 8 G + k); keys of groups past the kept ones never
+// count (they are 0 and come after every kept key in thread order, and
+// steps <= 8 * kept groups).
+template <int D>
+__global__ void __launch_bounds__(D * 8)
+alloc_grouped_kernel(const float* __restrict__ eig, int R, int g, const int32_t* __restrict__ keep,
+                     uint8_t* __restrict__ bits_out)
+{
+    __shared__ int warp_tot[32];
+    __shared__ double Lam[D];
+    const int h = blockIdx.x, tid = threadIdx.x;
+    const int G = tid >> 3, k = tid & 7;
+    const int lane = tid & 31, warp = tid >> 5;
+    int kp = keep ? keep[h] : D;
+    kp = kp < 0 ? 0 : (kp > D ? D : kp);
+    const int ng = kp / g;                       // kept groups
+    const int steps = min(R / g, 8 * ng);
+    if (k == 0 && G < ng) {
+        double s = 0.0;
+        for (int c = G * g; c < (G + 1) * g; ++c) {
+            const float lf = eig[size_t(h) * D + c];
+            s += double(lf > 0.f ? lf : 0.f);
+        }
+        Lam[G] = s;
+    }
+    __syncthreads();
+    const double key = (G < ng) ? ldexp(Lam[G], -2 * k) : 0.0;
+    const unsigned long long kb = static_cast<unsigned long long>(__double_as_longlong(key));
+    bool sel = false;
+    if (steps > 0) {
+        unsigned long long lo = 0ull, hi = 0x7FF0000000000000ull;
+        while (lo < hi) {
+            const unsigned long long mid = lo + ((hi - lo) >> 1);
+            const int gt = __syncthreads_count(kb > mid);
+            if (gt < steps) hi = mid; else lo = mid + 1;
+        }
+        const bool gt = kb > lo, eq = kb == lo && G < ng;
+        const int n_gt = __syncthreads_count(gt);
+        const int need = steps - n_gt;
+        const unsigned m = __ballot_sync(0xffffffffu, eq);
+        if (lane == 0) warp_tot[warp] = __popc(m);
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += warp_tot[w];
+        before += __popc(m & ((1u << lane) - 1u));
+        sel = (gt && G < ng) || (eq && before < need);
+    }
+    const unsigned sm = __ballot_sync(0xffffffffu, sel);
+    const int width = __popc((sm >> (lane & ~7)) & 0xFFu);
+    if (G < D / g)
+        for (int c = G * g + k; c < (G + 1) * g; c += 8) bits_out[size_t(h) * D + c] = uint8_t(G < ng ? width : 0);
+}
+
+// Effective dimension with spectral-gap pruning ("Technisch Overzicht ...",
+// "Regime-Specifieke Prestaties"), one warp per head, lane 0 in fp64:
+// d_energy = the smallest k whose leading k clipped eigenvalues hold `energy`
+// of their sum; d_gap = the k in 1 .. min(d_energy, d - 1) with the largest
+// lam_{k-1} / lam_k (exact cross products; smallest k on ties).
+__global__ void effdim_kernel(const float* __restrict__ eig, int d, double energy, int32_t* __restrict__ d_energy,
+                              int32_t* __restrict__ d_gap)
+{
+    const int h = blockIdx.x;
+    if (threadIdx.x != 0) return;
+    const float* l = eig + size_t(h) * d;
+    auto lam = [&](int c) { return double(l[c] > 0.f ? l[c] : 0.f); };
+    double tot = 0.0;
+    for (int c = 0; c < d; ++c) tot += lam(c);
+    int de = 0;
+    if (tot > 0.0) {
+        double cum = 0.0;
+        while (de < d) {
+            cum += lam(de);
+            ++de;
+            if (cum >= energy * tot) break;
+        }
+    }
+    int best = de;
+    if (de > 0 && d > 1) {
+        const int kmax = de < d - 1 ? de : d - 1;
+        best = 1;
+        for (int k = 2; k <= kmax; ++k)
+            if (lam(k - 1) * lam(best) > lam(best - 1) * lam(k)) best = k;
+    }
+    d_energy[h] = de;
+    d_gap[h] = best;
+}
+
 // Per-head offsets, record size and quantizer scales.
 template <int D>
 __global__ void __launch_bounds__(D)
@@ -219,6 +314,23 @@ spectra_status launch_alloc(const spectra_plan* plan, int R_tot, int fixed_bits,
         alloc_kernel<128><<<plan->heads, 128 * 8, 0, s>>>(plan->eigvals, R_tot, fixed_bits, plan->bits);
     else
         alloc_kernel<64><<<plan->heads, 64 * 8, 0, s>>>(plan->eigvals, R_tot, fixed_bits, plan->bits);
+    return cuda_status(cudaGetLastError());
+}
+
+spectra_status launch_alloc_grouped(const spectra_plan* plan, int R_tot, int group, const int32_t* keep,
+                                    cudaStream_t s)
+{
+    if (plan->head_dim == 128)
+        alloc_grouped_kernel<128><<<plan->heads, 128 * 8, 0, s>>>(plan->eigvals, R_tot, group, keep, plan->bits);
+    else
+        alloc_grouped_kernel<64><<<plan->heads, 64 * 8, 0, s>>>(plan->eigvals, R_tot, group, keep, plan->bits);
+    return cuda_status(cudaGetLastError());
+}
+
+spectra_status launch_effdim(const spectra_plan* plan, double energy, int32_t* d_energy, int32_t* d_gap,
+                             cudaStream_t s)
+{
+    effdim_kernel<<<plan->heads, 32, 0, s>>>(plan->eigvals, plan->head_dim, energy, d_energy, d_gap);
     return cuda_status(cudaGetLastError());
 }
 

@@ -214,6 +214,51 @@ spectra_status spectra_alloc_bits(spectra_plan* plan, double avg_bits, int fixed
     return launch_finalize(plan, s);
 }
 
+spectra_status spectra_alloc_bits_ex(spectra_plan* plan, double avg_bits, int group, const int32_t* keep,
+                                     spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, false);
+    if (st) return st;
+    if (!plan->derived || (reinterpret_cast<uintptr_t>(plan->derived) & 255u)) return SPECTRA_ERR_INVALID_ARG;
+    if (plan->basis != SPECTRA_BASIS_EIGEN) return SPECTRA_ERR_INVALID_ARG;
+    const int d = plan->head_dim;
+    if (group < 1 || group > d || (group & (group - 1)) || d % group) return SPECTRA_ERR_INVALID_ARG;
+    if (!(avg_bits >= 0.0) || !isfinite(avg_bits)) return SPECTRA_ERR_INVALID_ARG;
+    const double r = floor(avg_bits * d + 1e-9);
+    const int R = int(r < 8.0 * d ? r : 8.0 * d);
+    plan->max_rec_bits = (R / group) * group;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = launch_alloc_grouped(plan, R, group, keep, s))) return st;
+    return launch_finalize(plan, s);
+}
+
+spectra_status spectra_effective_dim(const spectra_plan* plan, double energy, int32_t* d_energy, int32_t* d_gap,
+                                     spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, false);
+    if (st) return st;
+    if (plan->basis != SPECTRA_BASIS_EIGEN || !d_energy || !d_gap) return SPECTRA_ERR_INVALID_ARG;
+    if (!(energy > 0.0 && energy <= 1.0)) return SPECTRA_ERR_INVALID_ARG;
+    return launch_effdim(plan, energy, d_energy, d_gap, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spectra_status spectra_calibrate_plain(spectra_plan* plan, const void* x, spectra_dtype dt, int64_t n_cal,
+                                       int64_t token_stride, void* workspace, size_t workspace_bytes,
+                                       spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, false);
+    if (st) return st;
+    if (plan->basis != SPECTRA_BASIS_EIGEN) return SPECTRA_ERR_INVALID_ARG;
+    if (n_cal <= 0) return SPECTRA_ERR_INVALID_ARG;
+    if ((st = check_cache(x, dt, n_cal, token_stride, plan->heads, plan->head_dim))) return st;
+    const size_t need = spectra_calibrate_workspace_bytes(plan->heads, plan->head_dim, n_cal);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SPECTRA_ERR_INVALID_ARG;
+    const int nch = gram_chunks(plan->heads, n_cal);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = launch_gram(plan, x, dt, n_cal, token_stride, static_cast<float*>(workspace), nch, s))) return st;
+    return launch_plain_calibrate(plan, static_cast<float*>(workspace), nch, n_cal, s);
+}
+
 spectra_status spectra_encode(const spectra_plan* plan, const void* x, spectra_dtype dt, int64_t T,
                               int64_t token_stride, uint8_t* codes, int64_t stream_stride_bytes,
                               float* norms, int64_t norms_stride, spectra_stream_t stream)

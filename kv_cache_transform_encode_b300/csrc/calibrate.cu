@@ -752,6 +752,38 @@ size_t jacobi_smem()
 
 }  // namespace
 
+// Plain-KV calibration ("Technisch Overzicht ...", "Belangrijkste
+// Bijdragen" 1: scalar quantization without rotation): the identity basis and
+// the raw coordinates' second moments, the Gram diagonal summed from the
+// chunk partials in chunk order.
+template <int D>
+__global__ void __launch_bounds__(D)
+plain_calibrate_kernel(const float* __restrict__ partials, int nchunks, float inv_n, float* __restrict__ basis,
+                       float* __restrict__ eig, int32_t* __restrict__ status)
+{
+    const int h = blockIdx.x, c = threadIdx.x;
+    float s = 0.f;
+    for (int ch = 0; ch < nchunks; ++ch) s += partials[((size_t(h) * nchunks + ch) * D + c) * D + c];
+    const float v = s * inv_n;
+    eig[size_t(h) * D + c] = v;
+    for (int i = 0; i < D; ++i) basis[(size_t(h) * D + i) * D + c] = (i == c) ? 1.f : 0.f;
+    const int bad = __syncthreads_or(!isfinite(v));
+    if (c == 0) status[h] = bad ? -SPECTRA_ERR_NONFINITE : 0;
+}
+
+spectra_status launch_plain_calibrate(const spectra_plan* plan, const float* partials, int nchunks, int64_t n_cal,
+                                      cudaStream_t s)
+{
+    const float inv_n = 1.0f / float(n_cal);
+    if (plan->head_dim == 128)
+        plain_calibrate_kernel<128><<<plan->heads, 128, 0, s>>>(partials, nchunks, inv_n, plan->basis_mat,
+                                                                plan->eigvals, plan->status);
+    else
+        plain_calibrate_kernel<64><<<plan->heads, 64, 0, s>>>(partials, nchunks, inv_n, plan->basis_mat,
+                                                              plan->eigvals, plan->status);
+    return cuda_status(cudaGetLastError());
+}
+
 int gram_chunks(int heads, int64_t n_cal)
 {
     const int64_t want = (2 * 148 + heads - 1) / heads;

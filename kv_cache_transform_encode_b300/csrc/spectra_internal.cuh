@@ -145,6 +145,12 @@ spectra_status launch_gram(const spectra_plan* plan, const void* x, int dt, int6
 spectra_status launch_jacobi(const spectra_plan* plan, const float* partials, int nchunks,
                              int64_t n_cal, int max_sweeps, float* gram_out, cudaStream_t s);
 spectra_status launch_alloc(const spectra_plan* plan, int R_tot, int fixed_bits, cudaStream_t s);
+spectra_status launch_alloc_grouped(const spectra_plan* plan, int R_tot, int group, const int32_t* keep,
+                                    cudaStream_t s);
+spectra_status launch_effdim(const spectra_plan* plan, double energy, int32_t* d_energy, int32_t* d_gap,
+                             cudaStream_t s);
+spectra_status launch_plain_calibrate(const spectra_plan* plan, const float* partials, int nchunks, int64_t n_cal,
+                                      cudaStream_t s);
 spectra_status launch_finalize(const spectra_plan* plan, cudaStream_t s);
 spectra_status launch_encode(const spectra_plan* plan, const void* x, int dt, int64_t T,
                              int64_t token_stride, uint8_t* codes, int64_t sstride, float* norms,

@@ -63,6 +63,8 @@ def lib() -> C.CDLL:
         "orc_gram": (None, [_D, _L, _L, _I, _D]),
         "orc_jacobi": (_I, [_D, _I, C.c_double, _I, _D, _D]),
         "orc_alloc": (_L, [_D, _I, _L, _U8]),
+        "orc_alloc_grouped": (_L, [_D, _I, _L, _I, _I, _U8]),
+        "orc_effective_dim": (None, [_D, _I, C.c_double, C.POINTER(C.c_int), C.POINTER(C.c_int)]),
         "orc_lloyd_max": (_L, [_I, C.c_double, _L, _D, _D]),
         "orc_codebook_mse": (C.c_double, [_I, _D, _D]),
         "orc_project": (None, [_D, _L, _L, _I, _D, _D]),
@@ -146,6 +148,25 @@ def alloc(lam, R_tot: int) -> np.ndarray:
     bits = np.zeros(lam.shape[0], dtype=np.uint8)
     lib().orc_alloc(lam, lam.shape[0], int(R_tot), bits)
     return bits
+
+
+def alloc_grouped(lam, R_tot: int, group: int = 1, keep: int | None = None) -> np.ndarray:
+    """Grouped reverse water-filling over the first `keep` channels
+    ("La Pipeline di SPECTRA" phase 2, "Raggruppamento")."""
+    lam = _f64(lam)
+    d = lam.shape[0]
+    bits = np.zeros(d, dtype=np.uint8)
+    lib().orc_alloc_grouped(lam, d, int(R_tot), int(group), int(d if keep is None else keep), bits)
+    return bits
+
+
+def effective_dim(lam, energy: float = 0.95):
+    """(d_energy, d_gap) of a descending spectrum ("Technisch Overzicht ...",
+    "Regime-Specifieke Prestaties": spectral-gap pruning of d_eff)."""
+    lam = _f64(lam)
+    de, dg = C.c_int(0), C.c_int(0)
+    lib().orc_effective_dim(lam, lam.shape[0], float(energy), C.byref(de), C.byref(dg))
+    return de.value, dg.value
 
 
 # --------------------------------------------------------------------------
@@ -232,6 +253,36 @@ def make_eigen_plan(x_cal: np.ndarray, avg_bits: float, quant: int = QUANT_UNIFO
         bits = np.stack([alloc(lam32[h], R) for h in range(H)])
     return Plan(BASIS_EIGEN, quant, bits, basis=Q32, eigvals=lam32,
                 extra={"lam64": lam, "Q64": Q})
+
+
+def make_grouped_plan(x_cal: np.ndarray, avg_bits: float, group: int = 1, keep=None,
+                      quant: int = QUANT_UNIFORM, plain: bool = False) -> Plan:
+    """Eigenbasis (or, with `plain`, the identity basis with the raw
+    coordinates' second moments -- the ablation page's Plain-KV) rounded to
+    fp32, then grouped water-filling over the first keep[h] channels of each
+    head (keep: None = all, an int, or one value per head)."""
+    if plain:
+        lam, Q = calibrate_plain(x_cal)
+    else:
+        lam, Q = calibrate(x_cal)
+    lam32 = lam.astype(np.float32).astype(np.float64)
+    Q32 = Q.astype(np.float32).astype(np.float64)
+    H, d = lam.shape
+    keeps = [d] * H if keep is None else ([int(keep)] * H if np.isscalar(keep) else [int(k) for k in keep])
+    R = total_bits(avg_bits, d)
+    bits = np.stack([alloc_grouped(lam32[h], R, group, keeps[h]) for h in range(H)])
+    return Plan(BASIS_EIGEN, quant, bits, basis=Q32, eigvals=lam32, extra={"lam64": lam, "Q64": Q})
+
+
+def calibrate_plain(x_cal: np.ndarray):
+    """Plain-KV calibration ("Technisch Overzicht ...", "Belangrijkste
+    Bijdragen" 1: scalar quantization without rotation): the identity basis,
+    the raw coordinates' uncentred second moments (the Gram diagonal) as the
+    channel variances.  Returns (lam[H, d], Q[H, d, d] = I)."""
+    x_cal = np.asarray(x_cal)
+    n, H, d = x_cal.shape
+    lams = np.stack([np.diag(gram(x_cal[:, h, :])) for h in range(H)])
+    return lams, np.broadcast_to(np.eye(d), (H, d, d)).copy()
 
 
 def make_rwht_plan(signs: np.ndarray, width: int = 3) -> Plan:

@@ -176,6 +176,94 @@ long orc_alloc(const double* lam, int d, long R_tot, uint8_t* bits)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Grouped reverse water-filling.  [SPECTRA] "La Pipeline di SPECTRA" phase 2,
+ * "Raggruppamento": adjacent latent coordinates share one bit width, which
+ * keeps the cache append-only and streamable; [ABL] "Regime-Specifieke
+ * Prestaties": the effective dimension is pruned (the channels past it take
+ * no bits).  Readings: groups of g consecutive channels in the eigenvalue-
+ * descending order; only the first `keep` channels take part, in
+ * floor(keep / g) whole groups, every other channel gets 0 bits; a one-bit
+ * step of a group gives all its g channels one bit and costs g bits; the
+ * greedy takes floor(R_tot / g) steps, each to the group with the largest
+ * Lam_G * 4^-b_G among groups below 8 bits (Lam_G = the sum of the group's
+ * eigenvalues clipped at 0, added in ascending channel order in fp64),
+ * lowest group index on ties.  g = 1 with keep = d is orc_alloc.
+ * Returns the bits given. */
+long orc_alloc_grouped(const double* lam, int d, long R_tot, int g, int keep, uint8_t* bits)
+{
+    for (int c = 0; c < d; ++c) bits[c] = 0;
+    if (g < 1 || keep < 0) return 0;
+    if (keep > d) keep = d;
+    const int ng = keep / g;
+    double* Lam = (double*)malloc(sizeof(double) * (ng > 0 ? ng : 1));
+    int* bg = (int*)calloc(ng > 0 ? ng : 1, sizeof(int));
+    for (int G = 0; G < ng; ++G) {
+        double s = 0.0;
+        for (int c = G * g; c < (G + 1) * g; ++c) s += lam[c] > 0.0 ? lam[c] : 0.0;
+        Lam[G] = s;
+    }
+    long given = 0;
+    for (long step = 0; step < R_tot / g; ++step) {
+        int best = -1;
+        double bv = -1.0;
+        for (int G = 0; G < ng; ++G) {
+            if (bg[G] >= 8) continue;
+            const double v = ldexp(Lam[G], -2 * bg[G]);
+            if (v > bv) { bv = v; best = G; }
+        }
+        if (best < 0) break;
+        bg[best] += 1;
+        given += g;
+    }
+    for (int G = 0; G < ng; ++G)
+        for (int c = G * g; c < (G + 1) * g; ++c) bits[c] = (uint8_t)bg[G];
+    free(Lam);
+    free(bg);
+    return given;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Effective dimension with spectral-gap pruning.  [ABL] "Regime-Specifieke
+ * Prestaties": d_eff follows the calibration budget rather than the true
+ * rank, and a single spurious eigenvalue can make the output anti-correlated,
+ * so a spectral-gap criterion prunes the estimated dimension.  The page gives
+ * no formula; readings (eigenvalues descending, clipped at 0):
+ *   d_energy = the smallest k with lam_0 + ... + lam_{k-1} >= energy * sum(lam)
+ *              (0 when the sum is 0), sums in ascending order in fp64;
+ *   d_gap    = the k in 1 .. min(d_energy, d - 1) with the largest ratio
+ *              lam_{k-1} / lam_k (a zero lam_k is an infinite ratio), the
+ *              smallest such k on ties, compared exactly as cross products;
+ *              d_energy when d_energy is 0 or d is 1. */
+void orc_effective_dim(const double* lam_in, int d, double energy, int* d_energy, int* d_gap)
+{
+    double tot = 0.0;
+    for (int c = 0; c < d; ++c) tot += lam_in[c] > 0.0 ? lam_in[c] : 0.0;
+    int de = 0;
+    if (tot > 0.0) {
+        double cum = 0.0;
+        for (de = 0; de < d;) {
+            cum += lam_in[de] > 0.0 ? lam_in[de] : 0.0;
+            ++de;
+            if (cum >= energy * tot) break;
+        }
+    }
+    *d_energy = de;
+    int best = de;
+    if (de > 0 && d > 1) {
+        const int kmax = de < d - 1 ? de : d - 1;
+        best = 1;
+        for (int k = 2; k <= kmax; ++k) {
+            const double a = lam_in[k - 1] > 0.0 ? lam_in[k - 1] : 0.0, b = lam_in[k] > 0.0 ? lam_in[k] : 0.0;
+            const double ab = lam_in[best - 1] > 0.0 ? lam_in[best - 1] : 0.0;
+            const double bb = lam_in[best] > 0.0 ? lam_in[best] : 0.0;
+            /* a / b > ab / bb  <=>  a * bb > ab * b  (b, bb >= 0) */
+            if (a * bb > ab * b) best = k;
+        }
+    }
+    *d_gap = best;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Gaussian Lloyd-Max codebook (the Lloyd-Max codebook family of [ABL]
  * "Experimentele Opstelling", here for N(0,1) as the workload asks).
  * Lloyd's alternation: thresholds at midpoints of adjacent levels; each level

@@ -60,3 +60,13 @@ def compare_codes(orc, oplan, h, enc, gpu_stream, T):
 
 def bf16(x: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def ks_same_distribution(a, b, alpha=0.01):
+    """Two-sample Kolmogorov-Smirnov test of the ablation page's validation
+    methodology ("Technisch Overzicht ...", "Experimentele Opstelling": a
+    systematic difference between two implementations against seed
+    variance).  Returns (no systematic difference at level alpha, p-value)."""
+    import scipy.stats
+    p = float(scipy.stats.ks_2samp(np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)).pvalue)
+    return p > alpha, p

@@ -541,3 +541,115 @@ def test_attn_decode_gqa_head_map(orc):
     for j in range(Hq):
         np.testing.assert_allclose(out[1, j], orc.attention(q[1, j], K[1, :, j // 2], V[1, :, j // 2], 0.5),
                                    rtol=1e-14)
+
+
+# ---------------------------------------------------------------- grouped widths, d_eff, Plain-KV
+def test_grouped_alloc_worked_example(orc):
+    rows = _golden_lines("grouped_alloc_worked_example.txt")
+    lam = np.array([float(v) for v in rows[0][1:]])
+    for r in rows[1:]:
+        g, keep, R = int(r[0]), int(r[1]), int(r[2])
+        assert list(orc.alloc_grouped(lam, R, g, keep)) == [int(v) for v in r[3:]], r
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_grouped_alloc_properties_and_identity(orc, seed):
+    """Group 1 over all channels is the plain greedy; every group shares one
+    width; channels past `keep` get nothing; the total is g * floor(R / g)
+    while groups have room; widths never exceed 8."""
+    g = np.random.default_rng(seed)
+    lam = np.sort(g.gamma(0.7, 3.0, 64))[::-1]
+    lam[-5:] = 0.0
+    for R in (0, 1, 31, 128, 200, 511, 512):
+        assert np.array_equal(orc.alloc_grouped(lam, R, 1, 64), orc.alloc(lam, R))
+        for grp in (2, 4, 8, 16):
+            for keep in (64, 40, 16):
+                b = orc.alloc_grouped(lam, R, grp, keep).astype(int)
+                ng = keep // grp
+                assert np.all(b[ng * grp:] == 0)
+                assert np.all(b[: ng * grp].reshape(ng, grp) == b[: ng * grp: grp][:, None])
+                assert b.max() <= 8
+                assert b.sum() == grp * min(R // grp, 8 * ng)
+
+
+def test_grouped_alloc_optimal_vs_dynamic_programming(orc):
+    """Greedy on the convex high-rate distortion Lam_G 4^-b is optimal: its
+    distortion equals the exhaustive minimum over group widths with at most
+    floor(R / g) steps (d = 16, groups of 2 and 4, every budget 0..64)."""
+    g = np.random.default_rng(9)
+    lam = np.sort(g.gamma(0.5, 2.0, 16))[::-1]
+    for grp in (2, 4):
+        ng = 16 // grp
+        Lam = lam.reshape(ng, grp).sum(1)
+        for R in range(0, 65):
+            steps = R // grp
+            best = {0: 0.0}
+            for G in range(ng):          # DP over groups: minimal distortion per step count
+                nxt = {}
+                for used, dist in best.items():
+                    for b in range(0, 9):
+                        if used + b > steps:
+                            break
+                        v = dist + Lam[G] * 4.0 ** -b
+                        if used + b not in nxt or v < nxt[used + b]:
+                            nxt[used + b] = v
+                best = nxt
+            b = orc.alloc_grouped(lam, R, grp, 16).astype(int)[::grp]
+            greedy = float((Lam * 4.0 ** -b).sum())
+            assert greedy <= min(best.values()) * (1 + 1e-12) + 1e-300, (grp, R)
+
+
+def test_effective_dim_worked_example(orc):
+    for r in _golden_lines("effective_dim_worked_example.txt"):
+        bar = r.index("|")
+        energy, de, dg = float(r[0]), int(r[1]), int(r[2])
+        lam = np.array([float(v) for v in r[bar + 1:]])
+        assert orc.effective_dim(lam, energy) == (de, dg), r
+
+
+def test_effective_dim_spiked_spectrum(orc):
+    """A planted gap: 6 strong directions over a flat noise floor -- at any
+    energy fraction the gap criterion lands on 6, and one spurious large
+    eigenvalue on top (a 20x outlier) moves it to 1 only when that gap is the
+    widest, which it is by construction here."""
+    lam = np.concatenate([np.geomspace(60, 20, 6), np.full(58, 1.0)])
+    for energy in (0.7, 0.9, 0.99):
+        de, dg = orc.effective_dim(lam, energy)
+        assert dg == min(6, de) or (de < 6 and dg <= de)
+    lam2 = np.concatenate([[60 * 20.0], lam[1:]])
+    assert orc.effective_dim(lam2, 0.99)[1] == 1
+
+
+def test_plain_calibration_is_the_gram_diagonal(orc):
+    """Plain-KV ("Technisch Overzicht ...", "Belangrijkste Bijdragen" 1:
+    scalar quantization without rotation): identity basis, channel variances
+    = the raw coordinates' second moments (library matmul's diagonal)."""
+    x = synth.tiny_gaussian(4, T=300, H=2, d=16).astype(np.float64)
+    lam, Q = orc.calibrate_plain(x)
+    for h in range(2):
+        np.testing.assert_allclose(lam[h], np.diag(x[:, h, :].T @ x[:, h, :]) / 300, rtol=1e-13)
+        assert np.array_equal(Q[h], np.eye(16))
+    plan = orc.make_grouped_plan(x, 2.0, plain=True)
+    enc = orc.encode_head(plan, 1, x[:, 1, :])
+    np.testing.assert_allclose(enc["y"], x[:, 1, :], rtol=0, atol=0)
+
+
+def test_ks_harness_power_and_size(orc):
+    """The KS harness (tests/parity.py) on oracle runs alone, on the Tiny
+    Gaussian regime: two independent seed sets of the same codec are not
+    separated; 2.0 against 1.75 bits/value is.  (On the heavy-tailed spiked
+    regime clipping dominates and even 1.0 bits/value is not separated at
+    this sample size -- the ablation page's heavy-tail finding.)"""
+    from parity import ks_same_distribution
+    T, H = 512, 1
+
+    def errs(seeds, B):
+        out = []
+        for s in seeds:
+            x = synth.tiny_gaussian(s, T=T, H=H, d=64).astype(np.float64)
+            op = orc.make_eigen_plan(x[:384], B)
+            out.append(orc.relmse(x, orc.decode(op, [e["stream"] for e in orc.encode(op, x)], T)))
+        return out
+    a, b, c = errs(range(100, 124), 2.0), errs(range(200, 224), 2.0), errs(range(100, 124), 1.75)
+    assert ks_same_distribution(a, b)[0]
+    assert not ks_same_distribution(a, c)[0]
