@@ -539,7 +539,8 @@ def variants(spx, K, V, q, dev, local_rank, reps=10):
     bits/value (uniform +-3 sigma quantizer): SpectralQuant with
     water-filling, SQU-KV (one width on every channel), grouped widths of 4
     and 16 adjacent channels, the gap-pruned effective dimension (energy
-    0.95), and Plain-KV (no rotation).  Per scheme: encode and decode time (K
+    0.95), and Plain-KV (no rotation); SpectralQuant at 8 bits/value as the
+    near-lossless anchor.  Per scheme: encode and decode time (K
     and V), relMSE / cosine / d^2 = relMSE^2 + (1 - cos)^2 of K and V, and the
     decode-step attention output (32 query heads over the packed cache)
     against fp32 attention over the uncompressed cache -- the 6-D error
@@ -568,6 +569,8 @@ def variants(spx, K, V, q, dev, local_rank, reps=10):
                 spx.spectra_calibrate(p, x[side], n_cal=N_CAL)
             if kind == "sq_waterfill" or kind == "plain_kv":
                 spx.spectra_alloc_bits(p, AVG_BITS)
+            elif kind == "sq_8bit":
+                spx.spectra_alloc_bits(p, 8.0)
             elif kind == "squ_uniform":
                 spx.spectra_alloc_bits(p, 0.0, fixed_bits=int(AVG_BITS))
             elif kind.startswith("grouped"):
@@ -576,7 +579,7 @@ def variants(spx, K, V, q, dev, local_rank, reps=10):
                 spx.spectra_effective_dim(p, 0.95, de, dg)
                 spx.spectra_alloc_bits_ex(p, AVG_BITS, 1, dg)
                 torch.cuda.synchronize()
-                info["KV"[side]] = {"d_energy": de.tolist(), "d_gap": dg.tolist()}
+                info["deff_" + "KV"[side]] = {"d_energy": de.tolist(), "d_gap": dg.tolist()}
             ps.append(p)
         return ps, info
 
@@ -585,7 +588,7 @@ def variants(spx, K, V, q, dev, local_rank, reps=10):
         return {"relmse": round(rel, 6), "cosine": round(cos, 6), "d2": round(rel ** 2 + (1 - cos) ** 2, 8)}
     out = {}
     att = torch.empty((1, HQ, D), device=dev)
-    for kind in ("sq_waterfill", "squ_uniform", "grouped4", "grouped16", "deff_gap", "plain_kv"):
+    for kind in ("sq_waterfill", "squ_uniform", "grouped4", "grouped16", "deff_gap", "plain_kv", "sq_8bit"):
         (kp, vp), info = plans(kind)
         kc, vc = kp.new_streams(T), vp.new_streams(T)
         ko, vo = torch.empty_like(K[0]), torch.empty_like(V[0])
