@@ -309,10 +309,11 @@ def run_ours(args, rank, world, local_rank):
     attn = None
     if args.attn_workload:
         attn = attn_workload(spx, kp, vp, dev, _peaks(), reps=50, batch=args.attn_batch, local_rank=local_rank)
-    sweep = qwen = var = None
+    sweep = qwen = var = stream_res = None
     if args.workloads:
         sweep = budget_sweep(spx, K, V, dev, _peaks(), local_rank)
         var = variants(spx, K, V, q, dev, local_rank)
+        stream_res = streaming(spx, kp, vp, K, V, dev, local_rank)
         qwen = qwen_rwht(spx, dev, _peaks(), local_rank)
 
     res = {
@@ -333,6 +334,7 @@ def run_ours(args, rank, world, local_rank):
         "attn_decode": attn,
         "budget_sweep": sweep,
         "variants": var,
+        "streaming": stream_res,
         "qwen_rwht": qwen,
         "clocks": clocks,
         "e2e": {"value": round(_whole_job_rate(T_TOK, world, e2e_ms), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -611,6 +613,61 @@ def variants(spx, K, V, q, dev, local_rank, reps=10):
     return {"workload": "llama3.1-8b-shaped layer, 2.0 bits/value (uniform +-3 sigma), attention of 32 q heads "
                         "over the 32768-token packed cache against fp32 attention over the bf16 cache",
             "schemes": out}
+
+
+def streaming(spx, kp, vp, K, V, dev, local_rank, reps=50):
+    """The append-only path ("La Pipeline di SPECTRA" phases 2-3) on the
+    Llama-shaped layer's plans: a decode step appends one token to each of
+    the 8 kv heads' K and V streams (read-modify-write of the partly filled
+    32-token group), a chunked prefill appends 100 tokens at an unaligned
+    position; and decode-step attention over the batched workload's packed
+    history plus a 128-token uncompressed recent window, against the same
+    call without the window."""
+    import torch
+    T = K[0].shape[0]
+    kc, vc = kp.new_streams(T), vp.new_streams(T)
+    spx.spectra_encode(kp, K[0][:T // 2], kc)
+    spx.spectra_encode(vp, V[0][:T // 2], vc)
+    t1 = T // 2 + 5
+
+    def one(i):
+        t = t1 + i
+        spx.spectra_append(kp, K[0][t:t + 1], t, kc)
+        spx.spectra_append(vp, V[0][t:t + 1], t, vc)
+    one_ms = _events_ms(one, reps)
+
+    def chunk(i):
+        t = t1 + 37 + 100 * (i % 8)
+        spx.spectra_append(kp, K[0][t:t + 100], t, kc)
+        spx.spectra_append(vp, V[0][t:t + 100], t, vc)
+    chunk_ms = _events_ms(chunk, 16)
+    # windowed attention at the batched workload's shape
+    R = kp.max_rec_bits
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77)
+    sb = spx.spectra_stream_bytes(R, ATTN_CTX)
+    kcb = torch.randint(0, 256, (ATTN_B * H_KV, sb), dtype=torch.uint8, device=dev, generator=gen)
+    vcb = torch.randint(0, 256, (ATTN_B * H_KV, sb), dtype=torch.uint8, device=dev, generator=gen)
+    W = 128
+    kw = torch.randn((ATTN_B, W, H_KV, D), device=dev, generator=gen).to(torch.bfloat16)
+    vw = torch.randn((ATTN_B, W, H_KV, D), device=dev, generator=gen).to(torch.bfloat16)
+    q = torch.randn((ATTN_B, HQ, D), device=dev, generator=gen).mul_(D ** -0.5).to(torch.bfloat16)
+    out = torch.empty((ATTN_B, HQ, D), dtype=torch.float32, device=dev)
+    ws = torch.empty((spx.spectra_attn_workspace_bytes(ATTN_B, HQ, D, ATTN_CTX) + 256,), dtype=torch.uint8,
+                     device=dev)
+    win_ms = _events_ms(lambda i: spx.spectra_attn_decode_window(kp, vp, q, kcb, vcb, ATTN_CTX, kw, vw, 1.0, out,
+                                                                 workspace=ws), 10)
+    plain_ms = _events_ms(lambda i: spx.spectra_attn_decode(kp, vp, q, kcb, vcb, ATTN_CTX, 1.0, out,
+                                                            workspace=ws), 10)
+    del kcb, vcb
+    return {"append_one_token": {"us_per_step": round(one_ms * 1e3, 2),
+                                 "note": "1 token x 8 kv heads, K and V (two calls)"},
+            "append_chunk": {"tokens": 100, "us_per_chunk": round(chunk_ms * 1e3, 2),
+                             "tokens_per_s": round(100 / (chunk_ms * 1e-3), 1),
+                             "note": "100 tokens x 8 kv heads at positions 37 mod 128, K and V"},
+            "attn_window": {"window": W, "ms": round(win_ms, 4), "ms_without_window": round(plain_ms, 4),
+                            "workload": f"batch {ATTN_B}, {HQ} q heads / {H_KV} kv heads, context {ATTN_CTX} "
+                                        f"packed + {W} bf16"}}
 
 
 QWEN_LAYERS, QWEN_KV, QWEN_T = 28, 4, 131072

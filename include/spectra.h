@@ -268,6 +268,25 @@ SPECTRA_API spectra_status spectra_encode(const spectra_plan* plan, const void* 
                               spectra_stream_t stream);
 
 /*
+ * spectra_append -- encode n new tokens of every head at stream positions
+ * t0 .. t0+n-1 (any t0: a partly filled 32-token group keeps its earlier
+ * tokens).  ("Sintesi Tecnica: SPECTRA", "La Pipeline di SPECTRA" phase 2,
+ * "Raggruppamento": the latent cache stays append-only and streamable;
+ * phase 3: each new token is projected, quantized and appended.)
+ * The same codes as spectra_encode of the whole sequence, token by token.
+ * x: [n][heads][d] of dt (token_stride as in spectra_encode); codes: the
+ *   streams of spectra_encode (stride >= spectra_stream_bytes(max_rec_bits,
+ *   t0 + n)); bits of tokens t0 .. t0+n-1 are overwritten, every other bit
+ *   of the streams is kept.  norms (RWHT): norms[h * norms_stride + t0 + i].
+ * Tokens up to the next multiple of 128 take a read-modify-write of their
+ *   group on CUDA cores; the rest is an ordinary encode at that boundary.
+ *   Calls that write the same 32-token group must not overlap on the GPU.
+ */
+SPECTRA_API spectra_status spectra_append(const spectra_plan* plan, const void* x, spectra_dtype dt, int64_t n,
+                              int64_t token_stride, int64_t t0, uint8_t* codes, int64_t stream_stride_bytes,
+                              float* norms, int64_t norms_stride, spectra_stream_t stream);
+
+/*
  * spectra_decode -- unpack, dequantize, rotate back.
  * ("Sintesi Tecnica: SPECTRA", "La Pipeline di SPECTRA" phase 3: full keys
  * and values rebuilt on the fly.)
@@ -309,6 +328,30 @@ SPECTRA_API spectra_status spectra_attn_decode(const spectra_plan* kplan, const 
                                    const float* v_norms, int64_t norms_stride, int64_t ctx,
                                    float softmax_scale, float* out, void* workspace,
                                    size_t workspace_bytes, spectra_stream_t stream);
+
+/*
+ * spectra_attn_decode_window -- spectra_attn_decode over a cache whose
+ * newest win_len tokens are not packed yet: the softmax runs over the ctx
+ * packed tokens (reconstructed as by spectra_decode) followed by the win_len
+ * uncompressed tokens, out[b,j] = sum over both of p_t v_t.  ("La Pipeline
+ * di SPECTRA" phase 3: reconstructed keys and values feed standard
+ * attention; the recent window holds tokens not yet appended.)
+ * k_win / v_win: [B][win_len][Hkv][d] of win_dt, element (b, t, h, i) at
+ *   [(b * win_len + t) * win_token_stride + h * d + i] (stride in elements,
+ *   >= Hkv * d); 0 <= win_len <= SPECTRA_ATTN_MAX_WINDOW.  ctx may be 0.
+ * Every other argument, the workspace (spectra_attn_workspace_bytes(B, Hq,
+ *   d, ctx)) and the statuses as for spectra_attn_decode.
+ */
+#define SPECTRA_ATTN_MAX_WINDOW 16384
+SPECTRA_API spectra_status spectra_attn_decode_window(const spectra_plan* kplan, const spectra_plan* vplan,
+                                   const void* q, spectra_dtype q_dt, int B, int Hq,
+                                   const uint8_t* k_codes, const uint8_t* v_codes,
+                                   int64_t stream_stride_bytes, const float* k_norms,
+                                   const float* v_norms, int64_t norms_stride, int64_t ctx,
+                                   const void* k_win, const void* v_win, spectra_dtype win_dt,
+                                   int64_t win_len, int64_t win_token_stride, float softmax_scale,
+                                   float* out, void* workspace, size_t workspace_bytes,
+                                   spectra_stream_t stream);
 
 /*
  * spectra_attn_decode_noalloc -- spectra_attn_decode for callers that cannot

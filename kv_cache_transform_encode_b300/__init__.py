@@ -36,8 +36,8 @@ EXPORTS = ("spectra_version", "spectra_set_kernel_family", "spectra_get_kernel_f
            "spectra_status_string", "spectra_plan_derived_bytes",
            "spectra_stream_bytes", "spectra_calibrate_workspace_bytes", "spectra_calibrate",
            "spectra_alloc_bits", "spectra_alloc_bits_ex", "spectra_effective_dim", "spectra_calibrate_plain",
-           "spectra_plan_finalize", "spectra_encode", "spectra_decode",
-           "spectra_attn_workspace_bytes", "spectra_attn_decode", "spectra_attn_decode_noalloc")
+           "spectra_plan_finalize", "spectra_encode", "spectra_append", "spectra_decode",
+           "spectra_attn_workspace_bytes", "spectra_attn_decode", "spectra_attn_decode_window", "spectra_attn_decode_noalloc")
 
 
 class SpectraError(RuntimeError):
@@ -88,6 +88,9 @@ def lib() -> C.CDLL:
             "spectra_plan_finalize": (C.c_int, [P, vp]),
             "spectra_encode": (C.c_int, [P, vp, C.c_int, i64, i64, vp, i64, vp, i64, vp]),
             "spectra_decode": (C.c_int, [P, vp, i64, vp, i64, i64, vp, C.c_int, i64, vp]),
+            "spectra_append": (C.c_int, [P, vp, C.c_int, i64, i64, i64, vp, i64, vp, i64, vp]),
+            "spectra_attn_decode_window": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp, vp,
+                                                     i64, i64, vp, vp, C.c_int, i64, i64, f32, vp, vp, sz, vp]),
             "spectra_attn_workspace_bytes": (sz, [C.c_int, C.c_int, C.c_int, i64]),
             "spectra_attn_decode": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp, vp,
                                               i64, i64, f32, vp, vp, sz, vp]),
@@ -266,6 +269,17 @@ def spectra_encode(plan: Plan, x: torch.Tensor, codes: torch.Tensor, norms: torc
     _check(st, "spectra_encode")
 
 
+def spectra_append(plan: Plan, x: torch.Tensor, t0: int, codes: torch.Tensor,
+                   norms: torch.Tensor | None = None, stream=None):
+    """Append x [n, H, d] at stream positions t0 .. t0+n-1 of codes
+    [H, stride] (norms [H, >= t0+n] for RWHT)."""
+    p = plan.c()
+    st = lib().spectra_append(C.byref(p), _ptr(x), _dt(x), x.shape[0], x.stride(0), int(t0), _ptr(codes),
+                              codes.stride(0) if codes.dim() > 1 else 0, _ptr(norms),
+                              norms.stride(0) if norms is not None and norms.dim() > 1 else 0, _stream(stream))
+    _check(st, "spectra_append")
+
+
 def spectra_decode(plan: Plan, codes: torch.Tensor, T: int, out: torch.Tensor,
                    norms: torch.Tensor | None = None, stream=None):
     """codes: uint8 [H, stride]; out: [T, H, d] bf16/f32."""
@@ -294,6 +308,29 @@ def spectra_attn_decode(kplan: Plan, vplan: Plan, q: torch.Tensor, k_codes: torc
                                    nstride, ctx, float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(),
                                    _stream(stream))
     _check(st, "spectra_attn_decode")
+
+
+def spectra_attn_decode_window(kplan: Plan, vplan: Plan, q: torch.Tensor, k_codes: torch.Tensor,
+                               v_codes: torch.Tensor, ctx: int, k_win: torch.Tensor, v_win: torch.Tensor,
+                               softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor | None = None,
+                               k_norms: torch.Tensor | None = None, v_norms: torch.Tensor | None = None,
+                               stream=None):
+    """Attention over ctx packed tokens followed by the uncompressed window
+    k_win / v_win [B, W, Hkv, d] (contiguous rows: token stride Hkv * d)."""
+    B, Hq, d = q.shape
+    W = k_win.shape[1]
+    if workspace is None:
+        workspace = torch.empty((max(spectra_attn_workspace_bytes(B, Hq, d, ctx), 16) + 256,),
+                                dtype=torch.uint8, device=q.device)
+    off = (-workspace.data_ptr()) % 256
+    ws = workspace[off:]
+    kp, vp = kplan.c(), vplan.c()
+    nstride = k_norms.stride(0) if k_norms is not None else 0
+    st = lib().spectra_attn_decode_window(C.byref(kp), C.byref(vp), _ptr(q), _dt(q), B, Hq, _ptr(k_codes),
+                                          _ptr(v_codes), k_codes.stride(0), _ptr(k_norms), _ptr(v_norms), nstride,
+                                          ctx, _ptr(k_win), _ptr(v_win), _dt(k_win), W, k_win.stride(1),
+                                          float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "spectra_attn_decode_window")
 
 
 SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -6,17 +6,18 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <algorithm>
 #include <atomic>
 
 using namespace spectra;
 
 namespace spectra {
 spectra_status launch_encode_generic(const spectra_plan*, const void*, int, int64_t, int64_t,
-                                     uint8_t*, int64_t, float*, int64_t, cudaStream_t);
+                                     uint8_t*, int64_t, float*, int64_t, cudaStream_t, int64_t t0 = 0);
 spectra_status launch_decode_generic(const spectra_plan*, const uint8_t*, int64_t, const float*,
                                      int64_t, int64_t, void*, int, int64_t, cudaStream_t);
 spectra_status launch_encode_tc(const spectra_plan*, const void*, int, int64_t, int64_t,
-                                uint8_t*, int64_t, float*, int64_t, cudaStream_t, bool*);
+                                uint8_t*, int64_t, float*, int64_t, cudaStream_t, bool*, int64_t g0 = 0);
 spectra_status launch_decode_tc(const spectra_plan*, const uint8_t*, int64_t, const float*,
                                 int64_t, int64_t, void*, int, int64_t, cudaStream_t, bool*);
 }  // namespace spectra
@@ -286,6 +287,47 @@ spectra_status spectra_encode(const spectra_plan* plan, const void* x, spectra_d
                                  norms_stride, s);
 }
 
+spectra_status spectra_append(const spectra_plan* plan, const void* x, spectra_dtype dt, int64_t n,
+                              int64_t token_stride, int64_t t0, uint8_t* codes, int64_t stream_stride_bytes,
+                              float* norms, int64_t norms_stride, spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, true);
+    if (st) return st;
+    if (t0 < 0) return SPECTRA_ERR_INVALID_ARG;
+    if ((st = check_cache(x, dt, n, token_stride, plan->heads, plan->head_dim))) return st;
+    if ((st = check_streams(plan, codes, stream_stride_bytes, t0 + n, plan->heads))) return st;
+    if (plan->basis == SPECTRA_BASIS_RWHT && n > 0) {
+        if (!norms || (plan->heads > 1 && norms_stride < t0 + n)) return SPECTRA_ERR_INVALID_ARG;
+    }
+    if (n == 0 || plan->max_rec_bits == 0) {
+        if (plan->basis != SPECTRA_BASIS_RWHT || n == 0) return SPECTRA_OK;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // tokens up to the next 128-token boundary: read-modify-write of the
+    // partly filled group on CUDA cores; the rest is an ordinary encode at a
+    // tile-aligned stream position (16 R bytes per 128 tokens)
+    const int64_t t_al = std::min<int64_t>(t0 + n, (t0 + 127) / 128 * 128);
+    const int fam = kernel_family();
+    if (t_al > t0 || fam == SPECTRA_KERNELS_CUDA_CORE) {
+        const int64_t nh = fam == SPECTRA_KERNELS_CUDA_CORE ? n : t_al - t0;
+        if ((st = launch_encode_generic(plan, x, dt, nh, token_stride, codes, stream_stride_bytes, norms,
+                                        norms_stride, s, t0)))
+            return st;
+        if (nh == n) return SPECTRA_OK;
+    }
+    const int64_t rest = t0 + n - t_al;
+    const size_t esz = dt == SPECTRA_BF16 ? 2 : 4;
+    const void* xr = static_cast<const uint8_t*>(x) + size_t(t_al - t0) * size_t(token_stride) * esz;
+    bool done = false;
+    if ((st = launch_encode_tc(plan, xr, dt, rest, token_stride, codes, stream_stride_bytes, norms, norms_stride, s,
+                               &done, t_al / 32)))
+        return st;
+    if (done) return SPECTRA_OK;
+    if (fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
+    return launch_encode_generic(plan, xr, dt, rest, token_stride, codes, stream_stride_bytes, norms, norms_stride,
+                                 s, t_al);
+}
+
 spectra_status spectra_decode(const spectra_plan* plan, const uint8_t* codes, int64_t stream_stride_bytes,
                               const float* norms, int64_t norms_stride, int64_t T, void* x_out,
                               spectra_dtype out_dt, int64_t token_stride, spectra_stream_t stream)
@@ -336,6 +378,35 @@ spectra_status spectra_attn_decode(const spectra_plan* kplan, const spectra_plan
         return SPECTRA_ERR_INVALID_ARG;
     return launch_attn(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes, k_norms,
                        v_norms, norms_stride, ctx, softmax_scale, out, workspace, workspace_bytes, s);
+}
+
+spectra_status spectra_attn_decode_window(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
+                                          spectra_dtype q_dt, int B, int Hq, const uint8_t* k_codes,
+                                          const uint8_t* v_codes, int64_t stream_stride_bytes,
+                                          const float* k_norms, const float* v_norms, int64_t norms_stride,
+                                          int64_t ctx, const void* k_win, const void* v_win, spectra_dtype win_dt,
+                                          int64_t win_len, int64_t win_token_stride, float softmax_scale,
+                                          float* out, void* workspace, size_t workspace_bytes,
+                                          spectra_stream_t stream)
+{
+    spectra_status st = attn_validate(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes,
+                                      k_norms, v_norms, norms_stride, ctx, softmax_scale, out);
+    if (st) return st;
+    const int d = kplan->head_dim;
+    if (win_len < 0 || win_len > SPECTRA_ATTN_MAX_WINDOW) return SPECTRA_ERR_INVALID_ARG;
+    if (win_len > 0) {
+        if (!valid_dtype(win_dt) || !k_win || !v_win) return SPECTRA_ERR_INVALID_ARG;
+        if (win_token_stride < int64_t(kplan->heads) * d) return SPECTRA_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (ctx == 0 && win_len == 0)
+        return cuda_status(cudaMemsetAsync(out, 0, sizeof(float) * size_t(B) * Hq * d, s));
+    const size_t need = attn_workspace_bytes(B, Hq, d, ctx);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return SPECTRA_ERR_INVALID_ARG;
+    AttnWindow w{k_win, v_win, int(win_dt), win_len, win_token_stride};
+    return launch_attn(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes, k_norms, v_norms,
+                       norms_stride, ctx, softmax_scale, out, workspace, workspace_bytes, s, &w);
 }
 
 }  // extern "C"

@@ -216,7 +216,7 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
 // Delta_c (z_mean + 1/2) before the rotation.
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsplit, int code_domain,
-                    float* __restrict__ out)
+                    const float* __restrict__ win, float* __restrict__ out)
 {
     const int D = vp.d, Hkv = vp.heads, G = Hq / Hkv;
     const int bq = blockIdx.x, hq = bq % Hq, b = bq / Hq, h = hq / G;
@@ -243,6 +243,9 @@ attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsp
         float M = -INFINITY;
         for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, pp[int64_t(s) * (D + 2)]);
         for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        // the recent window's partial (m, l, o in the original basis) joins the maximum
+        const float mw = win ? win[(int64_t(b) * Hq + hq) * (D + 2)] : -INFINITY;
+        M = fmaxf(M, mw);
         float L = 0.f;
         for (int s = lane; s < nsplit; s += 32) {
             const float m = pp[int64_t(s) * (D + 2)];
@@ -251,7 +254,13 @@ attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsp
             L = fmaf(pp[int64_t(s) * (D + 2) + 1], w, L);
         }
         for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (lane == 0) stat[0] = L;
+        if (lane == 0) {
+            const float ww = (mw != -INFINITY) ? __expf(mw - M) : 0.f;
+            const float Lw = win ? ww * win[(int64_t(b) * Hq + hq) * (D + 2) + 1] : 0.f;
+            stat[0] = L + Lw;      // all tokens
+            stat[1] = L;           // packed tokens
+            stat[2] = ww;          // window weight
+        }
     }
     __syncthreads();
     const int nh = int(blockDim.x) / D;          // split phases (2 for d = 128, 4 for d = 64)
@@ -275,11 +284,14 @@ attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsp
         const int c = tid;
         float a = 0.f;
         for (int k = 0; k < nh; ++k) a += red[k * D + c];
-        const float L = stat[0];
-        float y = (L > 0.f) ? a / L : 0.f;
+        const float L = stat[0], Lp = stat[1];
+        float y;
         if (code_domain) {
+            // a = sum_t p z: the latent value is Delta (z + 1/2)
             const int bc = vp.bits[size_t(h) * D + c];
-            y = (bc > 0) ? vp.rscale[size_t(h) * D + c] * (y + 0.5f) : 0.f;
+            y = (bc > 0 && L > 0.f) ? vp.rscale[size_t(h) * D + c] * (a + 0.5f * Lp) / L : 0.f;
+        } else {
+            y = (L > 0.f) ? a / L : 0.f;
         }
         os[c] = y;
     }
@@ -298,7 +310,67 @@ attn_combine_kernel(PlanView vp, const float* __restrict__ part, int Hq, int nsp
     if (tid < D) {
         float a = 0.f;
         for (int k = 0; k < nh; ++k) a += red[k * D + tid];
+        if (win) {
+            const float L = stat[0];
+            a += (L > 0.f) ? stat[2] * win[(int64_t(b) * Hq + hq) * (D + 2) + 2 + tid] / L : 0.f;
+        }
         out[(int64_t(b) * Hq + hq) * D + tid] = a;
+    }
+}
+
+// The recent window: per (batch, query head), softmax partials over W
+// uncompressed tokens in the original basis -- s_t = scale <q, k_t>, m, l and
+// o = sum_t exp(s_t - m) v_t -- for the combine, which merges them with the
+// packed history's split partials.  k_t / v_t at
+// win[(b W + t) * win_stride + h d + i] (bf16 or f32).
+__global__ void __launch_bounds__(256)
+attn_window_kernel(const void* __restrict__ q, int q_dt, int Hq, int Hkv, int D, const void* __restrict__ kw,
+                   const void* __restrict__ vw, int w_dt, int64_t W, int64_t wstride, float scale,
+                   float* __restrict__ wpart)
+{
+    extern __shared__ float wsm[];
+    float* qs = wsm;                 // [D]
+    float* sc = qs + D;              // [W]
+    __shared__ float red[8];
+    const int bq = blockIdx.x, hq = bq % Hq, b = bq / Hq, h = hq / (Hq / Hkv);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    for (int i = tid; i < D; i += blockDim.x) qs[i] = scale * load_elem(q, q_dt, int64_t(bq) * D + i);
+    __syncthreads();
+    // one warp per token: lanes over channels
+    float mx = -INFINITY;
+    for (int64_t t = warp; t < W; t += nw) {
+        const int64_t base = (int64_t(b) * W + t) * wstride + int64_t(h) * D;
+        float a = 0.f;
+        for (int i = lane; i < D; i += 32) a = fmaf(qs[i], load_elem(kw, w_dt, base + i), a);
+        for (int o = 16; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) sc[t] = a;
+        mx = fmaxf(mx, a);
+    }
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    float M = -INFINITY;
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
+    float ls = 0.f;
+    for (int64_t t = tid; t < W; t += blockDim.x) {
+        const float p = __expf(sc[t] - M);
+        sc[t] = p;
+        ls += p;
+    }
+    for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    if (lane == 0) red[warp] = ls;
+    __syncthreads();
+    float* wp = wpart + int64_t(bq) * (D + 2);
+    for (int i = tid; i < D; i += blockDim.x) {
+        float o = 0.f;
+        for (int64_t t = 0; t < W; ++t) o = fmaf(sc[t], load_elem(vw, w_dt, (int64_t(b) * W + t) * wstride + int64_t(h) * D + i), o);
+        wp[2 + i] = o;
+    }
+    if (tid == 0) {
+        float L = 0.f;
+        for (int w = 0; w < nw; ++w) L += red[w];
+        wp[0] = M;
+        wp[1] = L;
     }
 }
 
@@ -340,44 +412,57 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
                               cudaStream_t s, bool* done);
 
 spectra_status launch_combine(const PlanView& vp, const float* part, int B, int Hq, int nsplit, int code_domain,
-                              float* out, cudaStream_t s)
+                              const float* win, float* out, cudaStream_t s)
 {
     const size_t sm = combine_smem(vp.d, nsplit);
     if (spectra_status st = set_smem(attn_combine_kernel, sm)) return st;
-    attn_combine_kernel<<<B * Hq, 256, sm, s>>>(vp, part, Hq, nsplit, code_domain, out);
+    attn_combine_kernel<<<B * Hq, 256, sm, s>>>(vp, part, Hq, nsplit, code_domain, win, out);
     return cuda_status(cudaGetLastError());
 }
 
-// [qt (B Hq d f32) | split partials | tensor-core operands (sized for Hkv <= Hq)]
+// [qt (B Hq d f32) | split partials | tensor-core operands (sized for Hkv <= Hq) |
+//  recent-window partials (B Hq (d + 2) f32)]
 size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx)
 {
     const size_t qt = align256(sizeof(float) * size_t(B) * Hq * d);
     const size_t part = align256(sizeof(float) * size_t(B) * Hq * nsplit_of(B, Hq, ctx) * (d + 2));
-    return qt + part + attn_tc_extra_bytes(B, Hq);
+    const size_t win = align256(sizeof(float) * size_t(B) * Hq * (d + 2));
+    return qt + part + attn_tc_extra_bytes(B, Hq) + win;
 }
 
 spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
                            int q_dt, int B, int Hq, const uint8_t* kc, const uint8_t* vc,
                            int64_t sstride, const float* kn, const float* vn, int64_t nstride,
                            int64_t ctx, float scale, float* out, void* ws, size_t ws_bytes,
-                           cudaStream_t s)
+                           cudaStream_t s, const AttnWindow* window)
 {
     const int D = kplan->head_dim, Hkv = kplan->heads;
     if (Hq / Hkv > kMaxGroup) return SPECTRA_ERR_UNSUPPORTED;
     const PlanView kp = make_view(kplan), vp = make_view(vplan);
-    const int nsplit = nsplit_of(B, Hq, ctx);
+    const int nsplit = ctx > 0 ? nsplit_of(B, Hq, ctx) : 0;
     const int split_len = split_len_of(B, Hq, ctx);
     float* qt = static_cast<float*>(ws);
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                            align256(sizeof(float) * size_t(B) * Hq * D));
-    void* extra = reinterpret_cast<uint8_t*>(part) + align256(sizeof(float) * size_t(B) * Hq * nsplit * (D + 2));
+    void* extra = reinterpret_cast<uint8_t*>(part) + align256(sizeof(float) * size_t(B) * Hq * nsplit_of(B, Hq, ctx) * (D + 2));
+    float* wpart = nullptr;
+    if (window && window->W > 0) {
+        wpart = reinterpret_cast<float*>(static_cast<uint8_t*>(extra) + attn_tc_extra_bytes(B, Hq));
+        const size_t sm = sizeof(float) * (size_t(D) + size_t(window->W));
+        if (sm > 227 * 1024) return SPECTRA_ERR_UNSUPPORTED;
+        if (spectra_status st = set_smem(attn_window_kernel, sm)) return st;
+        attn_window_kernel<<<B * Hq, 256, sm, s>>>(q, q_dt, Hq, Hkv, D, window->k, window->v, window->dt,
+                                                   window->W, window->stride, scale, wpart);
+        if (spectra_status st = cuda_status(cudaGetLastError())) return st;
+    }
+    if (nsplit == 0) return launch_combine(vp, part, B, Hq, 0, 0, wpart, out, s);
     const int fam = kernel_family();
     if (fam != SPECTRA_KERNELS_CUDA_CORE) {
         bool done = false;
         spectra_status st = launch_attn_tc(kplan, vplan, q, q_dt, B, Hq, kc, vc, sstride, ctx, scale, part, nsplit,
                                            split_len, extra, s, &done);
         if (st) return st;
-        if (done) return launch_combine(vp, part, B, Hq, nsplit, 1, out, s);
+        if (done) return launch_combine(vp, part, B, Hq, nsplit, 1, wpart, out, s);
         if (fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
     }
     attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt);
@@ -394,7 +479,7 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
                                                          nstride, nsplit, split_len, part);
     }
     if (spectra_status st = cuda_status(cudaGetLastError())) return st;
-    return launch_combine(vp, part, B, Hq, nsplit, 0, out, s);
+    return launch_combine(vp, part, B, Hq, nsplit, 0, wpart, out, s);
 }
 
 }  // namespace spectra

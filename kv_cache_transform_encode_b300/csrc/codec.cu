@@ -51,11 +51,15 @@ __device__ __forceinline__ int lm_code(const float* th, int b, float u)
     return lo;
 }
 
+// t0: stream position of row 0 of x (an append; 0 for a whole encode).
+// Rows 0..T-1 go to stream tokens t0..t0+T-1; a first group that starts
+// before t0 keeps the bits of its earlier tokens (read-modify-write of its
+// words), every other group is written whole.
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32)
 encode_generic_kernel(PlanView pv, const void* __restrict__ x, int dt, int64_t T, int64_t tstride,
                       uint8_t* __restrict__ codes, int64_t sstride, float* __restrict__ norms,
-                      int64_t nstride)
+                      int64_t nstride, int64_t t0)
 {
     constexpr int LD = D + 1;
     extern __shared__ float smem[];
@@ -80,28 +84,35 @@ encode_generic_kernel(PlanView pv, const void* __restrict__ x, int dt, int64_t T
     }
     __syncthreads();
 
-    const int64_t ngroups = (T + kGroup - 1) / kGroup;
-    const int64_t g = int64_t(blockIdx.x) * kWarps + warp;
-    if (g >= ngroups) return;
+    const int64_t g0 = t0 / kGroup;
+    const int64_t ngroups = (t0 + T + kGroup - 1) / kGroup - g0;
+    const int64_t gi = int64_t(blockIdx.x) * kWarps + warp;
+    if (gi >= ngroups) return;
+    const int64_t g = g0 + gi;                     // stream group
     float* xw = xs + warp * 32 * LD;
     for (int r = 0; r < 32; ++r) {
-        const int64_t t = g * kGroup + r;
+        const int64_t t = g * kGroup + r - t0;     // row of x
         for (int i = lane; i < D; i += 32)
-            xw[r * LD + i] = (t < T) ? load_elem(x, dt, t * tstride + int64_t(h) * D + i) : 0.f;
+            xw[r * LD + i] = (t >= 0 && t < T) ? load_elem(x, dt, t * tstride + int64_t(h) * D + i) : 0.f;
     }
     __syncwarp();
-    const int64_t t = g * kGroup + lane;
-    const bool live = t < T;
+    const int64_t t = g * kGroup + lane - t0;
+    const bool live = t >= 0 && t < T;
+    // lanes of earlier tokens whose bits stay (first group of an unaligned append)
+    const uint32_t keep = (gi == 0 && (t0 % kGroup)) ? ((1u << (t0 % kGroup)) - 1u) : 0u;
     float inv_sig = 0.f;
     if (pv.basis == SPECTRA_BASIS_RWHT) {
         float n2 = 0.f;
         for (int i = 0; i < D; ++i) n2 = fmaf(xw[lane * LD + i], xw[lane * LD + i], n2);
         const float nrm = sqrtf(n2);
-        if (live) norms[int64_t(h) * nstride + t] = nrm;
+        if (live) norms[int64_t(h) * nstride + t0 + t] = nrm;
         const float sig = nrm * rsqrtf(float(D));
         inv_sig = (sig > 0.f) ? 1.f / sig : 0.f;
     }
     uint32_t* out = reinterpret_cast<uint32_t*>(codes + int64_t(h) * sstride) + g * R;
+    auto put = [&](int w, uint32_t v) {
+        out[w] = keep ? ((out[w] & keep) | (v & ~keep)) : v;
+    };
     uint32_t myword = 0;
     int bc = 0;
     for (int c = 0; c < D; ++c) {
@@ -121,10 +132,10 @@ encode_generic_kernel(PlanView pv, const void* __restrict__ x, int dt, int64_t T
         for (int k = 0; k < b; ++k, ++bc) {
             const uint32_t wv = __ballot_sync(0xffffffffu, (code >> k) & 1);
             if ((bc & 31) == lane) myword = wv;
-            if ((bc & 31) == 31) out[(bc & ~31) + lane] = myword;
+            if ((bc & 31) == 31) put((bc & ~31) + lane, myword);
         }
     }
-    if ((bc & 31) != 0 && lane < (bc & 31)) out[(bc & ~31) + lane] = myword;
+    if ((bc & 31) != 0 && lane < (bc & 31)) put((bc & ~31) + lane, myword);
 }
 
 template <int D>
@@ -210,22 +221,22 @@ size_t dec_smem()
 
 spectra_status launch_encode_generic(const spectra_plan* plan, const void* x, int dt, int64_t T,
                                      int64_t token_stride, uint8_t* codes, int64_t sstride,
-                                     float* norms, int64_t nstride, cudaStream_t s)
+                                     float* norms, int64_t nstride, cudaStream_t s, int64_t t0)
 {
     const PlanView pv = make_view(plan);
-    const int64_t ngroups = (T + kGroup - 1) / kGroup;
+    const int64_t ngroups = (t0 + T + kGroup - 1) / kGroup - t0 / kGroup;
     if (ngroups == 0) return SPECTRA_OK;
     dim3 grid(unsigned((ngroups + kWarps - 1) / kWarps), plan->heads);
     if (plan->head_dim == 128) {
         const size_t sm = enc_smem<128>();
         if (spectra_status st = set_smem(encode_generic_kernel<128>, sm)) return st;
         encode_generic_kernel<128><<<grid, kWarps * 32, sm, s>>>(pv, x, dt, T, token_stride, codes,
-                                                                 sstride, norms, nstride);
+                                                                 sstride, norms, nstride, t0);
     } else {
         const size_t sm = enc_smem<64>();
         if (spectra_status st = set_smem(encode_generic_kernel<64>, sm)) return st;
         encode_generic_kernel<64><<<grid, kWarps * 32, sm, s>>>(pv, x, dt, T, token_stride, codes,
-                                                                sstride, norms, nstride);
+                                                                sstride, norms, nstride, t0);
     }
     return cuda_status(cudaGetLastError());
 }

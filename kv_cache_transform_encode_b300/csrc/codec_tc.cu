@@ -178,6 +178,7 @@ constexpr int kLmGroup = 8;   // Lloyd-Max values searched together
 struct EncParams {
     PlanView pv;
     int64_t T;
+    int64_t g0;            // stream group of token 0 (an append at a 128-token boundary; 0 otherwise)
     int tiles_per_head;
     int stages;
     int contig;            // contiguous work ranges (else interleaved)
@@ -431,7 +432,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
             ++ruse;
             const float n2 = part[lane] + part[32 + lane] + part[64 + lane] + part[96 + lane];
             const float nrm = sqrtf(n2 * (1.0f / float(D)));
-            if (q == 0 && head_ok && t0 + lane < P.T) P.norms[int64_t(cur_h) * P.nstride + t0 + lane] = nrm;
+            if (q == 0 && head_ok && t0 + lane < P.T) P.norms[int64_t(cur_h) * P.nstride + 32 * P.g0 + t0 + lane] = nrm;
             invs[lane] = (nrm > 0.f) ? 1.f / nrm : 0.f;
             __syncwarp();
             // everyone has read part[] before it is written again
@@ -523,7 +524,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                 qk = lm ? qs : qs / float(1 << b);
                 cl = float(1 << b) * (1.0f - 0x1p-22f);
                 bmax = __reduce_max_sync(0xffffffffu, b);
-                out = reinterpret_cast<uint32_t*>(P.codes + int64_t(h) * P.sstride);
+                out = reinterpret_cast<uint32_t*>(P.codes + int64_t(h) * P.sstride) + P.g0 * R;
             }
             uint32_t r0[32], r1[32];
             tmem_ld32(tq + gi * 32, r0);
@@ -1183,7 +1184,7 @@ spectra_status launch_tc_images(const spectra_plan* plan, cudaStream_t s)
 
 spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt, int64_t T, int64_t token_stride,
                                 uint8_t* codes, int64_t sstride, float* norms, int64_t nstride, cudaStream_t s,
-                                bool* done)
+                                bool* done, int64_t g0)
 {
     *done = false;
     if (dt != SPECTRA_BF16 || plan->head_dim != D || T <= 0) return SPECTRA_OK;
@@ -1193,6 +1194,7 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
     EncParams P;
     P.pv = make_view(plan);
     P.T = T;
+    P.g0 = g0;
     P.tiles_per_head = int((T + ETILE - 1) / ETILE);
     const int64_t total = int64_t(P.tiles_per_head) * plan->heads;
     if (total > (int64_t(1) << 31) - 1) return SPECTRA_OK;

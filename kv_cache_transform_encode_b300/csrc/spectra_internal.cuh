@@ -158,11 +158,18 @@ spectra_status launch_encode(const spectra_plan* plan, const void* x, int dt, in
 spectra_status launch_decode(const spectra_plan* plan, const uint8_t* codes, int64_t sstride,
                              const float* norms, int64_t nstride, int64_t T, void* x_out,
                              int out_dt, int64_t token_stride, cudaStream_t s);
+// The uncompressed recent window of spectra_attn_decode_window.
+struct AttnWindow {
+    const void* k;
+    const void* v;
+    int dt;
+    int64_t W, stride;
+};
 spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
                            int q_dt, int B, int Hq, const uint8_t* kc, const uint8_t* vc,
                            int64_t sstride, const float* kn, const float* vn, int64_t nstride,
                            int64_t ctx, float scale, float* out, void* ws, size_t ws_bytes,
-                           cudaStream_t s);
+                           cudaStream_t s, const AttnWindow* window = nullptr);
 size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx);
 // Host-side argument checks of spectra_attn_decode (everything but the
 // workspace), shared by the entry points that run it.

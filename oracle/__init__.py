@@ -78,6 +78,7 @@ def lib() -> C.CDLL:
         "orc_stream_bytes": (_L, [_L, _L]),
         "orc_pack": (None, [_I32, _L, _I, _U8, _U8]),
         "orc_unpack": (None, [_U8, _L, _I, _U8, _I32]),
+        "orc_pack_into": (None, [_I32, _L, _I, _U8, _L, _U8]),
         "orc_attention": (None, [_D, _D, _D, _L, _I, C.c_double, _D]),
     }
     for name, (res, args) in sig.items():
@@ -310,6 +311,19 @@ def pack(codes: np.ndarray, bits: np.ndarray) -> np.ndarray:
     return out
 
 
+def pack_into(stream: np.ndarray, codes: np.ndarray, bits: np.ndarray, t0: int) -> np.ndarray:
+    """Write the codes of tokens t0 .. t0+n-1 into `stream` (in place, every
+    other bit kept) -- the append-only latent cache ("La Pipeline di
+    SPECTRA" phases 2-3).  Returns the stream."""
+    codes = np.ascontiguousarray(codes, dtype=np.int32)
+    n, d = codes.shape
+    bits = np.ascontiguousarray(bits, dtype=np.uint8)
+    assert stream.dtype == np.uint8 and stream.flags["C_CONTIGUOUS"]
+    assert len(stream) >= stream_bytes(t0 + n, int(bits.astype(np.int64).sum()))
+    lib().orc_pack_into(codes, n, d, bits, int(t0), stream)
+    return stream
+
+
 def unpack(stream: np.ndarray, T: int, bits: np.ndarray) -> np.ndarray:
     bits = np.ascontiguousarray(bits, dtype=np.uint8)
     d = bits.shape[0]
@@ -428,6 +442,16 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.n
     out = np.zeros(q.shape[0])
     lib().orc_attention(q, K, V, K.shape[0], q.shape[0], float(scale), out)
     return out
+
+
+def attn_decode_window(q, Khat, Vhat, Kwin, Vwin, scale: float) -> np.ndarray:
+    """Decode-step GQA attention over a cache that holds a packed history
+    (Khat, Vhat [B, ctx, Hkv, d], reconstructed) followed by a recent window
+    kept uncompressed (Kwin, Vwin [B, W, Hkv, d]): the softmax runs over the
+    concatenation of both ("La Pipeline di SPECTRA" phase 3: reconstructed
+    keys and values feed standard attention; the newest tokens are the ones
+    not yet appended)."""
+    return attn_decode(q, np.concatenate([Khat, Kwin], axis=1), np.concatenate([Vhat, Vwin], axis=1), scale)
 
 
 def attn_decode(q: np.ndarray, Khat: np.ndarray, Vhat: np.ndarray, scale: float) -> np.ndarray:

@@ -526,6 +526,32 @@ void orc_unpack(const uint8_t* stream, long T, int d, const uint8_t* bits, int32
     }
 }
 
+/* Append to a stream.  [SPECTRA] "La Pipeline di SPECTRA" phase 2
+ * ("Raggruppamento": the latent cache stays append-only and streamable) and
+ * phase 3 (each new token is projected, quantized and appended): the codes of
+ * n tokens are written at stream positions t0 .. t0+n-1, each bit of theirs
+ * set or cleared one by one, every other bit of the stream left as it was.
+ * The stream must hold at least t0 + n tokens. */
+void orc_pack_into(const int32_t* codes, long n, int d, const uint8_t* bits, long t0, uint8_t* stream)
+{
+    long R = 0;
+    for (int c = 0; c < d; ++c) R += bits[c];
+    for (long i = 0; i < n; ++i) {
+        const long t = t0 + i;
+        long off = 0;
+        for (int c = 0; c < d; ++c) {
+            for (int k = 0; k < bits[c]; ++k) {
+                const long word = (t / 32) * R + off + k;
+                const long bitpos = word * 32 + (t % 32);
+                const uint8_t m = (uint8_t)(1u << (bitpos % 8));
+                if ((codes[i * d + c] >> k) & 1) stream[bitpos / 8] |= m;
+                else stream[bitpos / 8] &= (uint8_t)~m;
+            }
+            off += bits[c];
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Decode-step attention over reconstructed keys/values (the standard
  * attention that [SPECTRA] pipeline phase 3 feeds with rebuilt K/V):

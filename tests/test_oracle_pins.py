@@ -653,3 +653,53 @@ def test_ks_harness_power_and_size(orc):
     a, b, c = errs(range(100, 124), 2.0), errs(range(200, 224), 2.0), errs(range(100, 124), 1.75)
     assert ks_same_distribution(a, b)[0]
     assert not ks_same_distribution(a, c)[0]
+
+
+# ---------------------------------------------------------------- append and the recent window
+def test_append_worked_example(orc):
+    rows = {r[0]: r[1:] for r in _golden_lines("append_worked_example.txt")}
+    base = {r[0]: r[1:] for r in _golden_lines("pack_worked_example.txt")}
+    stream = np.array([int(b, 16) for b in base["bytes"]], dtype=np.uint8)
+    bits = np.array([int(v) for v in rows["bits"]], dtype=np.uint8)
+    codes = np.array([int(v) for v in rows["codes"]], dtype=np.int32).reshape(-1, 3)
+    orc.pack_into(stream, codes, bits, int(rows["t0"][0]))
+    assert list(stream) == [int(b, 16) for b in rows["bytes"]]
+
+
+def test_append_in_pieces_equals_one_shot(orc):
+    """Appending a token sequence in pieces at arbitrary positions (inside a
+    group, at its end, across groups and 128-token tiles) gives the bytes of
+    the one-shot pack, whatever the stream held at those positions before."""
+    g = np.random.default_rng(8)
+    bits = g.integers(0, 9, 24).astype(np.uint8)
+    T = 700
+    codes = (g.integers(0, 256, (T, 24)) & ((1 << bits.astype(int)) - 1)[None, :]).astype(np.int32)
+    want = orc.pack(codes, bits)
+    stream = g.integers(0, 256, len(want)).astype(np.uint8)      # stale contents
+    cuts = [0, 1, 31, 32, 33, 127, 128, 129, 400, 641, T]
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        orc.pack_into(stream, codes[a:b], bits, a)
+    n_bytes = orc.stream_bytes(T, int(bits.astype(int).sum()))
+    # bytes holding only tokens >= T (zero in the one-shot pack) keep their stale values
+    assert np.array_equal(orc.unpack(stream, T, bits), codes)
+    assert np.array_equal(orc.unpack(stream[:n_bytes], T, bits), orc.unpack(want, T, bits))
+
+
+def test_attention_window_is_concatenation(orc):
+    """A bf16 recent window joins the softmax: attention over (history,
+    window) equals textbook softmax attention over the concatenated keys and
+    values (scipy), and an empty window reduces to attn_decode."""
+    g = np.random.default_rng(15)
+    B, Hq, Hkv, ctx, W, d = 2, 4, 2, 40, 7, 16
+    K, V = g.standard_normal((B, ctx, Hkv, d)), g.standard_normal((B, ctx, Hkv, d))
+    Kw, Vw = g.standard_normal((B, W, Hkv, d)), g.standard_normal((B, W, Hkv, d))
+    q = g.standard_normal((B, Hq, d))
+    got = orc.attn_decode_window(q, K, V, Kw, Vw, 0.7)
+    for b in range(B):
+        for j in range(Hq):
+            h = j // (Hq // Hkv)
+            Kc = np.concatenate([K[b, :, h], Kw[b, :, h]])
+            Vc = np.concatenate([V[b, :, h], Vw[b, :, h]])
+            np.testing.assert_allclose(got[b, j], scipy.special.softmax(0.7 * Kc @ q[b, j]) @ Vc, rtol=1e-12)
+    np.testing.assert_allclose(orc.attn_decode_window(q, K, V, Kw[:, :0], Vw[:, :0], 0.7),
+                               orc.attn_decode(q, K, V, 0.7), rtol=1e-14)
