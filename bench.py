@@ -541,8 +541,10 @@ def variants(spx, K, V, q, dev, local_rank, reps=10):
     bits/value (uniform +-3 sigma quantizer): SpectralQuant with
     water-filling, SQU-KV (one width on every channel), grouped widths of 4
     and 16 adjacent channels, the gap-pruned effective dimension (energy
-    0.95), and Plain-KV (no rotation); SpectralQuant at 8 bits/value as the
-    near-lossless anchor.  Per scheme: encode and decode time (K
+    0.95), and Plain-KV (no rotation); SpectralQuant at 8 bits/value, and
+    TQ-KV (randomized Walsh-Hadamard rotation, 3-bit Gaussian Lloyd-Max,
+    per-token norm: 3.25 bits/value), which the page finds robust on
+    heavy-tailed caches.  Per scheme: encode and decode time (K
     and V), relMSE / cosine / d^2 = relMSE^2 + (1 - cos)^2 of K and V, and the
     decode-step attention output (32 query heads over the packed cache)
     against fp32 attention over the uncompressed cache -- the 6-D error
@@ -560,6 +562,14 @@ def variants(spx, K, V, q, dev, local_rank, reps=10):
 
     def plans(kind):
         ps = []
+        if kind == "tq_kv_3bit":
+            import synth
+            for side in range(2):
+                p = spx.Plan(H_KV, D, basis=spx.SPECTRA_BASIS_RWHT, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev)
+                p.signs.copy_(torch.from_numpy(synth.rwht_signs(600 + side, H_KV, D)))
+                spx.spectra_alloc_bits(p, 0.0, fixed_bits=3)
+                ps.append(p)
+            return ps, {}
         de = torch.zeros(H_KV, dtype=torch.int32, device=dev)
         dg = torch.zeros(H_KV, dtype=torch.int32, device=dev)
         info = {}
@@ -590,26 +600,30 @@ def variants(spx, K, V, q, dev, local_rank, reps=10):
         return {"relmse": round(rel, 6), "cosine": round(cos, 6), "d2": round(rel ** 2 + (1 - cos) ** 2, 8)}
     out = {}
     att = torch.empty((1, HQ, D), device=dev)
-    for kind in ("sq_waterfill", "squ_uniform", "grouped4", "grouped16", "deff_gap", "plain_kv", "sq_8bit"):
+    for kind in ("sq_waterfill", "squ_uniform", "grouped4", "grouped16", "deff_gap", "plain_kv", "sq_8bit",
+                 "tq_kv_3bit"):
         (kp, vp), info = plans(kind)
         kc, vc = kp.new_streams(T), vp.new_streams(T)
         ko, vo = torch.empty_like(K[0]), torch.empty_like(V[0])
+        rw = kind == "tq_kv_3bit"
+        kn = torch.empty((H_KV, T), device=dev) if rw else None
+        vn = torch.empty((H_KV, T), device=dev) if rw else None
 
         def enc(i):
-            spx.spectra_encode(kp, K[0], kc)
-            spx.spectra_encode(vp, V[0], vc)
+            spx.spectra_encode(kp, K[0], kc, norms=kn)
+            spx.spectra_encode(vp, V[0], vc, norms=vn)
 
         def dec(i):
-            spx.spectra_decode(kp, kc, T, ko)
-            spx.spectra_decode(vp, vc, T, vo)
+            spx.spectra_decode(kp, kc, T, ko, norms=kn)
+            spx.spectra_decode(vp, vc, T, vo, norms=vn)
         enc_ms = _events_ms(enc, reps)
         dec_ms = _events_ms(dec, reps)
-        spx.spectra_attn_decode(kp, vp, q, kc, vc, T, 1.0, att)
+        spx.spectra_attn_decode(kp, vp, q, kc, vc, T, 1.0, att, k_norms=kn, v_norms=vn)
         torch.cuda.synchronize()
         out[kind] = {"rec_bits": [kp.max_rec_bits, vp.max_rec_bits], "encode_ms": round(enc_ms, 4),
                      "decode_ms": round(dec_ms, 4), "K": err(K[0], ko), "V": err(V[0], vo),
                      "attn_out": err(ref[None], att), **info}
-        del kc, vc, ko, vo
+        del kc, vc, ko, vo, kn, vn
     return {"workload": "llama3.1-8b-shaped layer, 2.0 bits/value (uniform +-3 sigma), attention of 32 q heads "
                         "over the 32768-token packed cache against fp32 attention over the bf16 cache",
             "schemes": out}

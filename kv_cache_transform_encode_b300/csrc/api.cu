@@ -14,6 +14,8 @@ using namespace spectra;
 namespace spectra {
 spectra_status launch_encode_generic(const spectra_plan*, const void*, int, int64_t, int64_t,
                                      uint8_t*, int64_t, float*, int64_t, cudaStream_t, int64_t t0 = 0);
+spectra_status launch_append_small(const spectra_plan*, const void*, int, int64_t, int64_t, uint8_t*, int64_t,
+                                   float*, int64_t, int64_t, cudaStream_t);
 spectra_status launch_decode_generic(const spectra_plan*, const uint8_t*, int64_t, const float*,
                                      int64_t, int64_t, void*, int, int64_t, cudaStream_t);
 spectra_status launch_encode_tc(const spectra_plan*, const void*, int, int64_t, int64_t,
@@ -25,6 +27,8 @@ spectra_status launch_decode_tc(const spectra_plan*, const uint8_t*, int64_t, co
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kSmallAppend = 8;   // appends of at most this many tokens take the channel-parallel kernel
 
 int elem_size(int dt) { return dt == SPECTRA_BF16 ? 2 : 4; }
 
@@ -310,9 +314,13 @@ spectra_status spectra_append(const spectra_plan* plan, const void* x, spectra_d
     const int fam = kernel_family();
     if (t_al > t0 || fam == SPECTRA_KERNELS_CUDA_CORE) {
         const int64_t nh = fam == SPECTRA_KERNELS_CUDA_CORE ? n : t_al - t0;
-        if ((st = launch_encode_generic(plan, x, dt, nh, token_stride, codes, stream_stride_bytes, norms,
-                                        norms_stride, s, t0)))
-            return st;
+        // a few tokens (decode steps): channel-parallel, token by token
+        st = nh <= kSmallAppend
+                 ? launch_append_small(plan, x, dt, nh, token_stride, codes, stream_stride_bytes, norms,
+                                       norms_stride, t0, s)
+                 : launch_encode_generic(plan, x, dt, nh, token_stride, codes, stream_stride_bytes, norms,
+                                         norms_stride, s, t0);
+        if (st) return st;
         if (nh == n) return SPECTRA_OK;
     }
     const int64_t rest = t0 + n - t_al;

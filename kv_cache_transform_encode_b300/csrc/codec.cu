@@ -138,6 +138,86 @@ encode_generic_kernel(PlanView pv, const void* __restrict__ x, int dt, int64_t T
     if ((bc & 31) != 0 && lane < (bc & 31)) put((bc & ~31) + lane, myword);
 }
 
+// A few tokens (decode-step appends): one block per head, thread = channel
+// for the rotation and the quantizer (the same arithmetic, in the same order,
+// as encode_generic_kernel), then thread = plane word for the read-modify-
+// write of bit (t mod 32) of each word of the token's group.  Tokens run one
+// after another, so a group shared by several of them is never raced.
+template <int D>
+__global__ void __launch_bounds__(D)
+append_small_kernel(PlanView pv, const void* __restrict__ x, int dt, int64_t n, int64_t tstride,
+                    uint8_t* __restrict__ codes, int64_t sstride, float* __restrict__ norms, int64_t nstride,
+                    int64_t t0)
+{
+    __shared__ float xs[D];
+    __shared__ int code_s[D];
+    __shared__ short plane_c[8 * D];
+    __shared__ unsigned char plane_k[8 * D];
+    __shared__ float red[D / 32];
+    const int h = blockIdx.x, c = threadIdx.x, lane = c & 31, warp = c >> 5;
+    const int R = pv.rec_bits[h];
+    if (R > pv.max_rec_bits) {
+        if (c == 0) pv.status[h] = -SPECTRA_ERR_BUFFER;
+        return;
+    }
+    const int b = pv.bits[size_t(h) * D + c];
+    const int o = pv.chan_off[size_t(h) * D + c];
+    for (int k = 0; k < b; ++k) {
+        plane_c[o + k] = short(c);
+        plane_k[o + k] = (unsigned char)k;
+    }
+    const float qsc = pv.qscale[size_t(h) * D + c];
+    uint32_t* words = reinterpret_cast<uint32_t*>(codes + int64_t(h) * sstride);
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t t = t0 + i;
+        xs[c] = load_elem(x, dt, i * tstride + int64_t(h) * D + c);
+        __syncthreads();
+        float inv_sig = 0.f;
+        if (pv.basis == SPECTRA_BASIS_RWHT) {
+            // the generic kernel's sequential sum of squares, by one thread
+            if (c == 0) {
+                float n2 = 0.f;
+                for (int j = 0; j < D; ++j) n2 = fmaf(xs[j], xs[j], n2);
+                red[0] = n2;
+            }
+            __syncthreads();
+            const float nrm = sqrtf(red[0]);
+            if (c == 0) norms[int64_t(h) * nstride + t] = nrm;
+            const float sig = nrm * rsqrtf(float(D));
+            inv_sig = (sig > 0.f) ? 1.f / sig : 0.f;
+        }
+        int code = 0;
+        if (b > 0) {
+            float y = 0.f;
+            if (pv.basis == SPECTRA_BASIS_EIGEN) {
+                for (int j = 0; j < D; ++j) y = fmaf(pv.basis_mat[(size_t(h) * D + j) * D + c], xs[j], y);
+            } else {
+                const float inv = rsqrtf(float(D));
+                for (int j = 0; j < D; ++j)
+                    y = fmaf(float(pv.signs[size_t(h) * D + j] * hadamard_sign(j, c)) * inv, xs[j], y);
+            }
+            if (pv.quant == SPECTRA_Q_UNIFORM3S) {
+                const float u = fmaf(y, qsc, float(1 << (b - 1)));
+                code = min(max(__float2int_rd(u), 0), (1 << b) - 1);
+            } else {
+                const float sc = (pv.basis == SPECTRA_BASIS_RWHT) ? inv_sig : qsc;
+                code = lm_code(pv.lm_thresh + (b - 1) * kLmStride, b, y * sc);
+            }
+        }
+        code_s[c] = code;
+        __syncthreads();
+        const uint32_t bitm = 1u << (t % kGroup);
+        uint32_t* gw = words + (t / kGroup) * R;
+        for (int r = c; r < R; r += D) {
+            const uint32_t v = (code_s[plane_c[r]] >> plane_k[r]) & 1u;
+            gw[r] = v ? (gw[r] | bitm) : (gw[r] & ~bitm);
+        }
+        __syncthreads();
+    }
+    (void)lane;
+    (void)warp;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecWarps * 32)
 decode_generic_kernel(PlanView pv, const uint8_t* __restrict__ codes, int64_t sstride,
@@ -238,6 +318,20 @@ spectra_status launch_encode_generic(const spectra_plan* plan, const void* x, in
         encode_generic_kernel<64><<<grid, kWarps * 32, sm, s>>>(pv, x, dt, T, token_stride, codes,
                                                                 sstride, norms, nstride, t0);
     }
+    return cuda_status(cudaGetLastError());
+}
+
+spectra_status launch_append_small(const spectra_plan* plan, const void* x, int dt, int64_t n, int64_t token_stride,
+                                   uint8_t* codes, int64_t sstride, float* norms, int64_t nstride, int64_t t0,
+                                   cudaStream_t s)
+{
+    const PlanView pv = make_view(plan);
+    if (plan->head_dim == 128)
+        append_small_kernel<128><<<plan->heads, 128, 0, s>>>(pv, x, dt, n, token_stride, codes, sstride, norms,
+                                                             nstride, t0);
+    else
+        append_small_kernel<64><<<plan->heads, 64, 0, s>>>(pv, x, dt, n, token_stride, codes, sstride, norms,
+                                                           nstride, t0);
     return cuda_status(cudaGetLastError());
 }
 
