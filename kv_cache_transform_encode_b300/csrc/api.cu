@@ -14,6 +14,9 @@ using namespace spectra;
 namespace spectra {
 spectra_status launch_encode_generic(const spectra_plan*, const void*, int, int64_t, int64_t,
                                      uint8_t*, int64_t, float*, int64_t, cudaStream_t, int64_t t0 = 0);
+spectra_status launch_gram_tc(const spectra_plan*, const void*, int, int64_t, int64_t, float*, int, cudaStream_t,
+                              bool*);
+int gram_tc_chunks(int heads, int64_t n_cal);
 spectra_status launch_append_small(const spectra_plan*, const void*, int, int64_t, int64_t, uint8_t*, int64_t,
                                    float*, int64_t, int64_t, cudaStream_t);
 spectra_status launch_decode_generic(const spectra_plan*, const uint8_t*, int64_t, const float*,
@@ -125,6 +128,22 @@ int spectra::kernel_family()
 
 namespace {
 
+// Gram partials: tcgen05 for bf16 caches with head_dim 128 (unless the
+// CUDA-core family is selected), the CUDA-core kernel otherwise.  Returns
+// the chunk count through *nch.
+spectra_status run_gram(const spectra_plan* plan, const void* x, int dt, int64_t n_cal, int64_t token_stride,
+                        float* partials, int* nch, cudaStream_t s)
+{
+    if (spectra::kernel_family() != SPECTRA_KERNELS_CUDA_CORE) {
+        bool done = false;
+        *nch = gram_tc_chunks(plan->heads, n_cal);
+        spectra_status st = launch_gram_tc(plan, x, dt, n_cal, token_stride, partials, *nch, s, &done);
+        if (st || done) return st;
+    }
+    *nch = gram_chunks(plan->heads, n_cal);
+    return launch_gram(plan, x, dt, n_cal, token_stride, partials, *nch, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -182,10 +201,9 @@ spectra_status spectra_calibrate(spectra_plan* plan, const void* x, spectra_dtyp
     if ((st = check_cache(x, dt, n_cal, token_stride, plan->heads, plan->head_dim))) return st;
     const size_t need = spectra_calibrate_workspace_bytes(plan->heads, plan->head_dim, n_cal);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SPECTRA_ERR_INVALID_ARG;
-    const int nch = gram_chunks(plan->heads, n_cal);
+    int nch = 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if ((st = launch_gram(plan, x, dt, n_cal, token_stride, static_cast<float*>(workspace), nch, s)))
-        return st;
+    if ((st = run_gram(plan, x, dt, n_cal, token_stride, static_cast<float*>(workspace), &nch, s))) return st;
     return launch_jacobi(plan, static_cast<float*>(workspace), nch, n_cal, max_sweeps, gram_out, s);
 }
 
@@ -258,9 +276,9 @@ spectra_status spectra_calibrate_plain(spectra_plan* plan, const void* x, spectr
     if ((st = check_cache(x, dt, n_cal, token_stride, plan->heads, plan->head_dim))) return st;
     const size_t need = spectra_calibrate_workspace_bytes(plan->heads, plan->head_dim, n_cal);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SPECTRA_ERR_INVALID_ARG;
-    const int nch = gram_chunks(plan->heads, n_cal);
+    int nch = 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if ((st = launch_gram(plan, x, dt, n_cal, token_stride, static_cast<float*>(workspace), nch, s))) return st;
+    if ((st = run_gram(plan, x, dt, n_cal, token_stride, static_cast<float*>(workspace), &nch, s))) return st;
     return launch_plain_calibrate(plan, static_cast<float*>(workspace), nch, n_cal, s);
 }
 

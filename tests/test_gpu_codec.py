@@ -50,7 +50,9 @@ def llama_case(T=1000, H=8, seed=1, role=synth.ROLE_K):
 
 # ---------------------------------------------------------------- calibrate
 @pytest.mark.parametrize("case", ["tiny", "llama"])
-def test_calibrate_matches_oracle(spx, orc, case):
+def test_calibrate_matches_oracle(spx, orc, path, case):
+    """Gram (tcgen05 for the bf16 d = 128 cache on the tensor-core family,
+    CUDA cores otherwise) and Jacobi eigenbasis against the oracle."""
     if case == "tiny":
         x, xd, x64 = tiny_case()
         n = 128
