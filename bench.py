@@ -623,6 +623,20 @@ def variants(spx, K, V, q, dev, local_rank, reps=10):
         out[kind] = {"rec_bits": [kp.max_rec_bits, vp.max_rec_bits], "encode_ms": round(enc_ms, 4),
                      "decode_ms": round(dec_ms, 4), "K": err(K[0], ko), "V": err(V[0], vo),
                      "attn_out": err(ref[None], att), **info}
+        if kind in ("sq_waterfill", "tq_kv_3bit"):
+            # the 1-bit QJL sketch of the key residuals (TQ-QKV / SQ with QJL on K)
+            gS = torch.Generator(device=dev)
+            gS.manual_seed(4100)
+            Sk = torch.randn((D, D), device=dev, generator=gS)
+            qb = torch.zeros((H_KV, spx.spectra_stream_bytes(D, T)), dtype=torch.uint8, device=dev)
+            qn = torch.zeros((H_KV, T), device=dev)
+            qjl_ms = _events_ms(lambda i: spx.spectra_qjl_encode(kp, Sk, K[0], kc, qb, qn, norms=kn), 3, warm=1)
+            attq = torch.empty_like(att)
+            aq_ms = _events_ms(lambda i: spx.spectra_attn_decode_qjl(kp, vp, q, kc, vc, T, Sk, qb, qn, 1.0, attq,
+                                                                     k_norms=kn, v_norms=vn), 3, warm=1)
+            torch.cuda.synchronize()
+            out[kind]["qjl_k"] = {"encode_ms": round(qjl_ms, 4), "attn_ms": round(aq_ms, 4),
+                                  "attn_out": err(ref[None], attq), "bits_per_value_extra": 1 + 32 / D}
         del kc, vc, ko, vo, kn, vn
     return {"workload": "llama3.1-8b-shaped layer, 2.0 bits/value (uniform +-3 sigma), attention of 32 q heads "
                         "over the 32768-token packed cache against fp32 attention over the bf16 cache",

@@ -354,6 +354,49 @@ SPECTRA_API spectra_status spectra_attn_decode_window(const spectra_plan* kplan,
                                    spectra_stream_t stream);
 
 /*
+ * spectra_qjl_encode -- 1-bit Johnson-Lindenstrauss sketch of the key
+ * residuals.  ("Technisch Overzicht ...", "Experimentele Opstelling" and
+ * "Belangrijkste Bijdragen" 1: TQ-QKV, a 1-bit QJL residual sketch on the
+ * key path; section 2: on the key path its variance is amplified by the
+ * softmax.)  For token t of head h: y = the latent coordinates of x[t,h,:]
+ * (as spectra_encode computes them), yhat = the dequantized codes already in
+ * the stream, r = y - yhat; bit j = (<s_j, r> >= 0) for the rows s_j of
+ * `sketch`, and qjl_norms[h * qjl_norms_stride + t] = ||r||.
+ * sketch: device f32 [d][d], row j = s_j, a Gaussian matrix (i.i.d. N(0,1)
+ *   entries: the random draw is the caller's).
+ * qjl_bits: head h at qjl_bits + h * qjl_stride_bytes, the packed-stream
+ *   layout with R = d "planes" (word g*d + j, bit t mod 32 = bit j of token
+ *   g*32 + t); stride >= spectra_stream_bytes(d, T).  x, codes, norms as for
+ *   spectra_encode; CUDA-core kernel.
+ */
+SPECTRA_API spectra_status spectra_qjl_encode(const spectra_plan* plan, const float* sketch, const void* x,
+                                  spectra_dtype dt, int64_t T, int64_t token_stride, const uint8_t* codes,
+                                  int64_t stream_stride_bytes, const float* norms, int64_t norms_stride,
+                                  uint8_t* qjl_bits, int64_t qjl_stride_bytes, float* qjl_norms,
+                                  int64_t qjl_norms_stride, spectra_stream_t stream);
+
+/*
+ * spectra_attn_decode_qjl -- spectra_attn_decode whose key scores carry the
+ * QJL estimate of the residual's inner product:
+ *   s_t = softmax_scale * (<q, khat_t> + sqrt(pi/2)/d ||r_t|| sum_j <s_j, qt> z_j(t)),
+ * qt = the query in the K latent coordinates, z_j = +1 for a set bit, -1
+ * otherwise (an unbiased estimate of <q, k_t - khat_t>).
+ * k_qjl_bits / k_qjl_norms: the spectra_qjl_encode outputs of every (b, kv
+ *   head) stream, at + (b * Hkv + h) * qjl_stride_bytes / qjl_norms_stride.
+ * CUDA-core kernels (SPECTRA_ERR_UNSUPPORTED when the tensor-core family is
+ *   required); everything else as for spectra_attn_decode.
+ */
+SPECTRA_API spectra_status spectra_attn_decode_qjl(const spectra_plan* kplan, const spectra_plan* vplan,
+                                   const void* q, spectra_dtype q_dt, int B, int Hq,
+                                   const uint8_t* k_codes, const uint8_t* v_codes,
+                                   int64_t stream_stride_bytes, const float* k_norms,
+                                   const float* v_norms, int64_t norms_stride, int64_t ctx,
+                                   const float* sketch, const uint8_t* k_qjl_bits, int64_t qjl_stride_bytes,
+                                   const float* k_qjl_norms, int64_t qjl_norms_stride, float softmax_scale,
+                                   float* out, void* workspace, size_t workspace_bytes,
+                                   spectra_stream_t stream);
+
+/*
  * spectra_attn_decode_noalloc -- spectra_attn_decode for callers that cannot
  * allocate device memory when they run a decode step (code inside an
  * allocator or memory-pool callback, hosts whose device memory belongs to

@@ -37,7 +37,8 @@ EXPORTS = ("spectra_version", "spectra_set_kernel_family", "spectra_get_kernel_f
            "spectra_stream_bytes", "spectra_calibrate_workspace_bytes", "spectra_calibrate",
            "spectra_alloc_bits", "spectra_alloc_bits_ex", "spectra_effective_dim", "spectra_calibrate_plain",
            "spectra_plan_finalize", "spectra_encode", "spectra_append", "spectra_decode",
-           "spectra_attn_workspace_bytes", "spectra_attn_decode", "spectra_attn_decode_window", "spectra_attn_decode_noalloc")
+           "spectra_attn_workspace_bytes", "spectra_attn_decode", "spectra_attn_decode_window",
+           "spectra_qjl_encode", "spectra_attn_decode_qjl", "spectra_attn_decode_noalloc")
 
 
 class SpectraError(RuntimeError):
@@ -88,6 +89,10 @@ def lib() -> C.CDLL:
             "spectra_plan_finalize": (C.c_int, [P, vp]),
             "spectra_encode": (C.c_int, [P, vp, C.c_int, i64, i64, vp, i64, vp, i64, vp]),
             "spectra_decode": (C.c_int, [P, vp, i64, vp, i64, i64, vp, C.c_int, i64, vp]),
+            "spectra_qjl_encode": (C.c_int, [P, vp, vp, C.c_int, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                             vp]),
+            "spectra_attn_decode_qjl": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp, vp, i64,
+                                                  i64, vp, vp, i64, vp, i64, f32, vp, vp, sz, vp]),
             "spectra_append": (C.c_int, [P, vp, C.c_int, i64, i64, i64, vp, i64, vp, i64, vp]),
             "spectra_attn_decode_window": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp, vp,
                                                      i64, i64, vp, vp, C.c_int, i64, i64, f32, vp, vp, sz, vp]),
@@ -331,6 +336,41 @@ def spectra_attn_decode_window(kplan: Plan, vplan: Plan, q: torch.Tensor, k_code
                                           ctx, _ptr(k_win), _ptr(v_win), _dt(k_win), W, k_win.stride(1),
                                           float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "spectra_attn_decode_window")
+
+
+def spectra_qjl_encode(plan: Plan, sketch: torch.Tensor, x: torch.Tensor, codes: torch.Tensor,
+                       qjl_bits: torch.Tensor, qjl_norms: torch.Tensor, norms: torch.Tensor | None = None,
+                       stream=None):
+    """sketch f32 [d, d]; x [T, H, d]; codes [H, stride]; qjl_bits uint8
+    [H, >= spectra_stream_bytes(d, T)]; qjl_norms f32 [H, >= T]."""
+    p = plan.c()
+    T = x.shape[0]
+    st = lib().spectra_qjl_encode(C.byref(p), _ptr(sketch), _ptr(x), _dt(x), T, x.stride(0), _ptr(codes),
+                                  codes.stride(0), _ptr(norms), norms.stride(0) if norms is not None else 0,
+                                  _ptr(qjl_bits), qjl_bits.stride(0), _ptr(qjl_norms), qjl_norms.stride(0),
+                                  _stream(stream))
+    _check(st, "spectra_qjl_encode")
+
+
+def spectra_attn_decode_qjl(kplan: Plan, vplan: Plan, q: torch.Tensor, k_codes: torch.Tensor,
+                            v_codes: torch.Tensor, ctx: int, sketch: torch.Tensor, k_qjl_bits: torch.Tensor,
+                            k_qjl_norms: torch.Tensor, softmax_scale: float, out: torch.Tensor,
+                            workspace: torch.Tensor | None = None, k_norms: torch.Tensor | None = None,
+                            v_norms: torch.Tensor | None = None, stream=None):
+    B, Hq, d = q.shape
+    if workspace is None:
+        workspace = torch.empty((max(spectra_attn_workspace_bytes(B, Hq, d, ctx), 16) + 256,),
+                                dtype=torch.uint8, device=q.device)
+    off = (-workspace.data_ptr()) % 256
+    ws = workspace[off:]
+    kp, vp = kplan.c(), vplan.c()
+    nstride = k_norms.stride(0) if k_norms is not None else 0
+    st = lib().spectra_attn_decode_qjl(C.byref(kp), C.byref(vp), _ptr(q), _dt(q), B, Hq, _ptr(k_codes),
+                                       _ptr(v_codes), k_codes.stride(0), _ptr(k_norms), _ptr(v_norms), nstride, ctx,
+                                       _ptr(sketch), _ptr(k_qjl_bits), k_qjl_bits.stride(0), _ptr(k_qjl_norms),
+                                       k_qjl_norms.stride(0), float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    _check(st, "spectra_attn_decode_qjl")
 
 
 SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -17,6 +17,9 @@ spectra_status launch_encode_generic(const spectra_plan*, const void*, int, int6
 spectra_status launch_gram_tc(const spectra_plan*, const void*, int, int64_t, int64_t, float*, int, cudaStream_t,
                               bool*);
 int gram_tc_chunks(int heads, int64_t n_cal);
+spectra_status launch_qjl_encode(const spectra_plan*, const float*, const void*, int, int64_t, int64_t,
+                                 const uint8_t*, int64_t, const float*, int64_t, uint8_t*, int64_t, float*,
+                                 int64_t, cudaStream_t);
 spectra_status launch_append_small(const spectra_plan*, const void*, int, int64_t, int64_t, uint8_t*, int64_t,
                                    float*, int64_t, int64_t, cudaStream_t);
 spectra_status launch_decode_generic(const spectra_plan*, const uint8_t*, int64_t, const float*,
@@ -433,6 +436,53 @@ spectra_status spectra_attn_decode_window(const spectra_plan* kplan, const spect
     AttnWindow w{k_win, v_win, int(win_dt), win_len, win_token_stride};
     return launch_attn(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes, k_norms, v_norms,
                        norms_stride, ctx, softmax_scale, out, workspace, workspace_bytes, s, &w);
+}
+
+spectra_status spectra_qjl_encode(const spectra_plan* plan, const float* sketch, const void* x, spectra_dtype dt,
+                                  int64_t T, int64_t token_stride, const uint8_t* codes,
+                                  int64_t stream_stride_bytes, const float* norms, int64_t norms_stride,
+                                  uint8_t* qjl_bits, int64_t qjl_stride_bytes, float* qjl_norms,
+                                  int64_t qjl_norms_stride, spectra_stream_t stream)
+{
+    spectra_status st = check_plan(plan, true);
+    if (st) return st;
+    if ((st = check_cache(x, dt, T, token_stride, plan->heads, plan->head_dim))) return st;
+    if ((st = check_streams(plan, codes, stream_stride_bytes, T, plan->heads))) return st;
+    if (T == 0) return SPECTRA_OK;
+    if (!sketch || !qjl_bits || !qjl_norms || !aligned16(qjl_bits)) return SPECTRA_ERR_INVALID_ARG;
+    const int64_t need = stream_bytes(plan->head_dim, T);
+    if (plan->heads > 1 && (qjl_stride_bytes < need || qjl_stride_bytes % 16 != 0)) return SPECTRA_ERR_INVALID_ARG;
+    if (plan->heads > 1 && qjl_norms_stride < T) return SPECTRA_ERR_INVALID_ARG;
+    if (plan->basis == SPECTRA_BASIS_RWHT && (!norms || (plan->heads > 1 && norms_stride < T)))
+        return SPECTRA_ERR_INVALID_ARG;
+    return launch_qjl_encode(plan, sketch, x, dt, T, token_stride, codes, stream_stride_bytes, norms, norms_stride,
+                             qjl_bits, qjl_stride_bytes, qjl_norms, qjl_norms_stride,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+spectra_status spectra_attn_decode_qjl(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
+                                       spectra_dtype q_dt, int B, int Hq, const uint8_t* k_codes,
+                                       const uint8_t* v_codes, int64_t stream_stride_bytes, const float* k_norms,
+                                       const float* v_norms, int64_t norms_stride, int64_t ctx,
+                                       const float* sketch, const uint8_t* k_qjl_bits, int64_t qjl_stride_bytes,
+                                       const float* k_qjl_norms, int64_t qjl_norms_stride, float softmax_scale,
+                                       float* out, void* workspace, size_t workspace_bytes, spectra_stream_t stream)
+{
+    spectra_status st = attn_validate(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes,
+                                      k_norms, v_norms, norms_stride, ctx, softmax_scale, out);
+    if (st) return st;
+    const int d = kplan->head_dim;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (ctx == 0) return cuda_status(cudaMemsetAsync(out, 0, sizeof(float) * size_t(B) * Hq * d, s));
+    if (!sketch || !k_qjl_bits || !k_qjl_norms || !aligned16(k_qjl_bits)) return SPECTRA_ERR_INVALID_ARG;
+    if (qjl_stride_bytes < stream_bytes(d, ctx) || qjl_stride_bytes % 16 != 0 || qjl_norms_stride < ctx)
+        return SPECTRA_ERR_INVALID_ARG;
+    const size_t need = attn_workspace_bytes(B, Hq, d, ctx);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return SPECTRA_ERR_INVALID_ARG;
+    AttnQjl qj{sketch, k_qjl_bits, qjl_stride_bytes, k_qjl_norms, qjl_norms_stride};
+    return launch_attn(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes, k_norms, v_norms,
+                       norms_stride, ctx, softmax_scale, out, workspace, workspace_bytes, s, nullptr, &qj);
 }
 
 }  // extern "C"

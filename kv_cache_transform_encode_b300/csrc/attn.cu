@@ -33,8 +33,20 @@ __device__ __forceinline__ float basis_entry(const PlanView& pv, int h, int i, i
     return float(pv.signs[size_t(h) * D + i] * hadamard_sign(i, c)) * rsqrtf(float(D));
 }
 
+// Optional 1-bit JL sketch of the key residuals ("Technisch Overzicht ...",
+// TQ-QKV): per (b, kv head) stream, bit-plane words of D sketch bits per
+// 32-token group and one residual norm per token; w = S qt per query head.
+struct QjlArgs {
+    const float* sketch;     // [D][D] Gaussian matrix (row j = s_j), latent coordinates
+    const uint8_t* bits;
+    int64_t stride;          // bytes between the (b, kv head) bit streams
+    const float* norms;
+    int64_t nstride;
+    float* w;                // [B Hq][D] workspace
+};
+
 __global__ void attn_qrot_kernel(PlanView kp, const void* __restrict__ q, int q_dt, int Hq, int Hkv,
-                                 float scale, float* __restrict__ qt)
+                                 float scale, float* __restrict__ qt, QjlArgs qj)
 {
     const int D = kp.d;
     const int bj = blockIdx.x, j = bj % Hq;
@@ -46,6 +58,14 @@ __global__ void attn_qrot_kernel(PlanView kp, const void* __restrict__ q, int q_
         float a = 0.f;
         for (int i = 0; i < D; ++i) a = fmaf(basis_entry(kp, h, i, c, D), qs[i], a);
         qt[int64_t(bj) * D + c] = scale * a;
+    }
+    if (qj.bits) {
+        __syncthreads();
+        for (int j = threadIdx.x; j < D; j += blockDim.x) {
+            float a = 0.f;
+            for (int c = 0; c < D; ++c) a = fmaf(qj.sketch[j * D + c], qt[int64_t(bj) * D + c], a);
+            qj.w[int64_t(bj) * D + j] = a;
+        }
     }
 }
 
@@ -94,7 +114,7 @@ __global__ void __launch_bounds__(kThreads)
 attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq, int64_t ctx,
                   const uint8_t* __restrict__ kc, const uint8_t* __restrict__ vc, int64_t sstride,
                   const float* __restrict__ kn, const float* __restrict__ vn, int64_t nstride,
-                  int nsplit, int split_len, float* __restrict__ part)
+                  int nsplit, int split_len, float* __restrict__ part, QjlArgs qj)
 {
     constexpr int LD = D + 1;
     extern __shared__ float smem[];
@@ -161,6 +181,31 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
             S[j * kTile + t] = (t0 + t < s1) ? a : -INFINITY;
         }
         __syncthreads();
+        if (qj.bits) {
+            // QJL correction: + sqrt(pi/2)/D ||r_t|| sum_i w_ji (2 b_i(t) - 1), w = S_jl qt
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(qj.bits + sid * qj.stride);
+            const float* qnr = qj.norms + sid * qj.nstride;
+            float* zs = yv;                         // [kTile][LD] signs, free until the V unpack
+            const int64_t g0 = t0 / kGroup;
+            for (int e = threadIdx.x; e < kTile * D; e += blockDim.x) {
+                const int t = e / D, i = e % D;
+                const int64_t gg = g0 + t / kGroup;
+                const bool in = t0 + t < s1;
+                const uint32_t w = in ? qw[gg * D + i] : 0u;
+                zs[t * LD + i] = ((w >> (t & 31)) & 1u) ? 1.f : -1.f;
+            }
+            __syncthreads();
+            const float cst = 1.25331413731550025f / float(D);   // sqrt(pi / 2) / m, m = d
+            for (int e = threadIdx.x; e < G * kTile; e += blockDim.x) {
+                const int j = e / kTile, t = e % kTile;
+                if (t0 + t >= s1) continue;
+                const float* wj = qj.w + (int64_t(b) * Hq + h * G + j) * D;
+                float a = 0.f;
+                for (int i = 0; i < D; ++i) a = fmaf(wj[i], zs[t * LD + i], a);
+                S[j * kTile + t] += cst * qnr[t0 + t] * a;
+            }
+            __syncthreads();
+        }
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         if (warp < G) {
             float mx = fmaxf(S[warp * kTile + lane], S[warp * kTile + lane + 32]);
@@ -427,14 +472,15 @@ size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx)
     const size_t qt = align256(sizeof(float) * size_t(B) * Hq * d);
     const size_t part = align256(sizeof(float) * size_t(B) * Hq * nsplit_of(B, Hq, ctx) * (d + 2));
     const size_t win = align256(sizeof(float) * size_t(B) * Hq * (d + 2));
-    return qt + part + attn_tc_extra_bytes(B, Hq) + win;
+    const size_t qjw = align256(sizeof(float) * size_t(B) * Hq * d);
+    return qt + part + attn_tc_extra_bytes(B, Hq) + win + qjw;
 }
 
 spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
                            int q_dt, int B, int Hq, const uint8_t* kc, const uint8_t* vc,
                            int64_t sstride, const float* kn, const float* vn, int64_t nstride,
                            int64_t ctx, float scale, float* out, void* ws, size_t ws_bytes,
-                           cudaStream_t s, const AttnWindow* window)
+                           cudaStream_t s, const AttnWindow* window, const AttnQjl* qjl)
 {
     const int D = kplan->head_dim, Hkv = kplan->heads;
     if (Hq / Hkv > kMaxGroup) return SPECTRA_ERR_UNSUPPORTED;
@@ -456,8 +502,18 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
         if (spectra_status st = cuda_status(cudaGetLastError())) return st;
     }
     if (nsplit == 0) return launch_combine(vp, part, B, Hq, 0, 0, wpart, out, s);
+    QjlArgs qj{nullptr, nullptr, 0, nullptr, 0, nullptr};
+    if (qjl) {
+        qj.sketch = qjl->sketch;
+        qj.bits = qjl->bits;
+        qj.stride = qjl->stride;
+        qj.norms = qjl->norms;
+        qj.nstride = qjl->nstride;
+        qj.w = reinterpret_cast<float*>(static_cast<uint8_t*>(extra) + attn_tc_extra_bytes(B, Hq) +
+                                        align256(sizeof(float) * size_t(B) * Hq * (D + 2)));
+    }
     const int fam = kernel_family();
-    if (fam != SPECTRA_KERNELS_CUDA_CORE) {
+    if (fam != SPECTRA_KERNELS_CUDA_CORE && !qjl) {
         bool done = false;
         spectra_status st = launch_attn_tc(kplan, vplan, q, q_dt, B, Hq, kc, vc, sstride, ctx, scale, part, nsplit,
                                            split_len, extra, s, &done);
@@ -465,18 +521,19 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
         if (done) return launch_combine(vp, part, B, Hq, nsplit, 1, wpart, out, s);
         if (fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
     }
-    attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt);
+    if (qjl && fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
+    attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt, qj);
     dim3 grid(nsplit, Hkv, B);
     if (D == 128) {
         const size_t sm = split_smem<128>();
         if (spectra_status st = set_smem(attn_split_kernel<128>, sm)) return st;
         attn_split_kernel<128><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
-                                                          nstride, nsplit, split_len, part);
+                                                          nstride, nsplit, split_len, part, qj);
     } else {
         const size_t sm = split_smem<64>();
         if (spectra_status st = set_smem(attn_split_kernel<64>, sm)) return st;
         attn_split_kernel<64><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
-                                                         nstride, nsplit, split_len, part);
+                                                         nstride, nsplit, split_len, part, qj);
     }
     if (spectra_status st = cuda_status(cudaGetLastError())) return st;
     return launch_combine(vp, part, B, Hq, nsplit, 0, wpart, out, s);

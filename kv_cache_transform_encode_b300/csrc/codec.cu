@@ -321,6 +321,111 @@ spectra_status launch_encode_generic(const spectra_plan* plan, const void* x, in
     return cuda_status(cudaGetLastError());
 }
 
+// 1-bit JL sketch of the key residuals ("Technisch Overzicht ...", TQ-QKV:
+// a 1-bit QJL residual sketch on the key path).  One warp per 32-token group
+// (lane = token): y = the latent coordinates of x, yhat = the dequantized
+// codes already in the stream, r = y - yhat; bit j of the token is
+// (<s_j, r> >= 0) for the rows s_j of the caller's Gaussian matrix S (D x D,
+// latent coordinates), written as the group's D bit-plane words (word j, bit
+// t mod 32); the residual norm ||r|| per token.
+constexpr int kQjlWarps = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kQjlWarps * 32)
+qjl_encode_kernel(PlanView pv, const float* __restrict__ S, const void* __restrict__ x, int dt, int64_t T,
+                  int64_t tstride, const uint8_t* __restrict__ codes, int64_t sstride,
+                  const float* __restrict__ norms, int64_t nstride, uint8_t* __restrict__ qbits, int64_t qstride,
+                  float* __restrict__ qnorms, int64_t qnstride)
+{
+    constexpr int LD = D + 1;
+    extern __shared__ float smem[];
+    float* M = smem;                                 // [D][LD]
+    float* xs = M + D * LD;                          // [kQjlWarps][32][LD]  x, then r
+    float* lv = xs + kQjlWarps * 32 * LD;            // [8][256] Lloyd-Max levels
+    float* rsc = lv + kMaxBits * kLmStride;          // [D]
+    int* bsh = reinterpret_cast<int*>(rsc + D);      // [D]
+    int* osh = bsh + D;                              // [D]
+    const int h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = pv.rec_bits[h];
+    if (R > pv.max_rec_bits) return;
+    load_matrix<D>(pv, h, M);
+    for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) lv[e] = pv.lm_level[e];
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        rsc[c] = pv.rscale[size_t(h) * D + c];
+        bsh[c] = pv.bits[size_t(h) * D + c];
+        osh[c] = pv.chan_off[size_t(h) * D + c];
+    }
+    __syncthreads();
+    const int64_t ngroups = (T + kGroup - 1) / kGroup;
+    const int64_t g = int64_t(blockIdx.x) * kQjlWarps + warp;
+    if (g >= ngroups) return;
+    float* xw = xs + warp * 32 * LD;
+    for (int r = 0; r < 32; ++r) {
+        const int64_t t = g * kGroup + r;
+        for (int i = lane; i < D; i += 32)
+            xw[r * LD + i] = (t < T) ? load_elem(x, dt, t * tstride + int64_t(h) * D + i) : 0.f;
+    }
+    __syncwarp();
+    const int64_t t = g * kGroup + lane;
+    const bool live = t < T;
+    const uint32_t* words = reinterpret_cast<const uint32_t*>(codes + int64_t(h) * sstride) + g * R;
+    float ysig = 0.f;                                // RWHT: the token's scale ||x|| / sqrt(d)
+    if (pv.basis == SPECTRA_BASIS_RWHT && live) ysig = norms[int64_t(h) * nstride + t] * rsqrtf(float(D));
+    float r[D];
+#pragma unroll 4
+    for (int c = 0; c < D; ++c) {
+        float y = 0.f;
+        for (int i = 0; i < D; ++i) y = fmaf(M[i * LD + c], xw[lane * LD + i], y);
+        const int b = bsh[c];
+        float yh = 0.f;
+        if (b > 0) {
+            int code = 0;
+            for (int k = 0; k < b; ++k) code |= int((words[osh[c] + k] >> lane) & 1u) << k;
+            if (pv.quant == SPECTRA_Q_UNIFORM3S) yh = rsc[c] * (float(code) + 0.5f - float(1 << (b - 1)));
+            else yh = ((pv.basis == SPECTRA_BASIS_RWHT) ? ysig : rsc[c]) * lv[(b - 1) * kLmStride + code];
+        }
+        r[c] = y - yh;
+    }
+    float n2 = 0.f;
+#pragma unroll
+    for (int c = 0; c < D; ++c) n2 = fmaf(r[c], r[c], n2);
+    if (live) qnorms[int64_t(h) * qnstride + t] = sqrtf(n2);
+    uint32_t* out = reinterpret_cast<uint32_t*>(qbits + int64_t(h) * qstride) + g * D;
+    for (int j = 0; j < D; ++j) {
+        float a = 0.f;
+#pragma unroll
+        for (int c = 0; c < D; ++c) a = fmaf(S[j * D + c], r[c], a);
+        const uint32_t wv = __ballot_sync(0xffffffffu, live && a >= 0.f);
+        if (lane == (j & 31)) out[j] = wv;
+    }
+}
+
+spectra_status launch_qjl_encode(const spectra_plan* plan, const float* S, const void* x, int dt, int64_t T,
+                                 int64_t token_stride, const uint8_t* codes, int64_t sstride, const float* norms,
+                                 int64_t nstride, uint8_t* qbits, int64_t qstride, float* qnorms, int64_t qnstride,
+                                 cudaStream_t s)
+{
+    const PlanView pv = make_view(plan);
+    const int64_t ngroups = (T + kGroup - 1) / kGroup;
+    if (ngroups == 0) return SPECTRA_OK;
+    dim3 grid(unsigned((ngroups + kQjlWarps - 1) / kQjlWarps), plan->heads);
+    auto sm = [](int D) {
+        return sizeof(float) * (size_t(D) * (D + 1) + size_t(kQjlWarps) * 32 * (D + 1) + kMaxBits * kLmStride + D) +
+               sizeof(int) * 2 * D;
+    };
+    if (plan->head_dim == 128) {
+        if (spectra_status st = set_smem(qjl_encode_kernel<128>, sm(128))) return st;
+        qjl_encode_kernel<128><<<grid, kQjlWarps * 32, sm(128), s>>>(pv, S, x, dt, T, token_stride, codes, sstride,
+                                                                      norms, nstride, qbits, qstride, qnorms, qnstride);
+    } else {
+        if (spectra_status st = set_smem(qjl_encode_kernel<64>, sm(64))) return st;
+        qjl_encode_kernel<64><<<grid, kQjlWarps * 32, sm(64), s>>>(pv, S, x, dt, T, token_stride, codes, sstride,
+                                                                    norms, nstride, qbits, qstride, qnorms, qnstride);
+    }
+    return cuda_status(cudaGetLastError());
+}
+
 spectra_status launch_append_small(const spectra_plan* plan, const void* x, int dt, int64_t n, int64_t token_stride,
                                    uint8_t* codes, int64_t sstride, float* norms, int64_t nstride, int64_t t0,
                                    cudaStream_t s)

@@ -165,11 +165,19 @@ struct AttnWindow {
     int dt;
     int64_t W, stride;
 };
+// The key-residual sketch of spectra_attn_decode_qjl.
+struct AttnQjl {
+    const float* sketch;
+    const uint8_t* bits;
+    int64_t stride;
+    const float* norms;
+    int64_t nstride;
+};
 spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan, const void* q,
                            int q_dt, int B, int Hq, const uint8_t* kc, const uint8_t* vc,
                            int64_t sstride, const float* kn, const float* vn, int64_t nstride,
                            int64_t ctx, float scale, float* out, void* ws, size_t ws_bytes,
-                           cudaStream_t s, const AttnWindow* window = nullptr);
+                           cudaStream_t s, const AttnWindow* window = nullptr, const AttnQjl* qjl = nullptr);
 size_t attn_workspace_bytes(int B, int Hq, int d, int64_t ctx);
 // Host-side argument checks of spectra_attn_decode (everything but the
 // workspace), shared by the entry points that run it.

@@ -79,6 +79,8 @@ def lib() -> C.CDLL:
         "orc_pack": (None, [_I32, _L, _I, _U8, _U8]),
         "orc_unpack": (None, [_U8, _L, _I, _U8, _I32]),
         "orc_pack_into": (None, [_I32, _L, _I, _U8, _L, _U8]),
+        "orc_qjl_sketch": (None, [_D, _L, _I, _D, _I, _U8, _D]),
+        "orc_qjl_estimate": (C.c_double, [_D, _I, _D, _I, _U8, C.c_double]),
         "orc_attention": (None, [_D, _D, _D, _L, _I, C.c_double, _D]),
     }
     for name, (res, args) in sig.items():
@@ -441,6 +443,80 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.n
     q, K, V = _f64(q), _f64(K), _f64(V)
     out = np.zeros(q.shape[0])
     lib().orc_attention(q, K, V, K.shape[0], q.shape[0], float(scale), out)
+    return out
+
+
+def dequant_head(plan: Plan, h: int, codes: np.ndarray, norms=None) -> np.ndarray:
+    """Latent reconstruction yhat[T, d] of head h from its codes (the decode's
+    dequantization step alone)."""
+    codes = np.ascontiguousarray(codes, dtype=np.int32)
+    T, d = codes.shape
+    bits = np.ascontiguousarray(plan.bits[h], dtype=np.uint8)
+    yh = np.zeros((T, d))
+    levels, _ = lloyd_max_tables()
+    if plan.basis_kind == BASIS_EIGEN and plan.quant == QUANT_UNIFORM:
+        lib().orc_dequant_uniform(codes, T, d, _f64(plan.eigvals[h]), bits, yh)
+    elif plan.basis_kind == BASIS_EIGEN:
+        lib().orc_dequant_lm(codes, T, d, _sig_channel(plan.eigvals[h]), 0, 1, bits, _f64(levels), yh)
+    else:
+        sig = _f64(np.asarray(norms, dtype=np.float32)) / np.sqrt(d)
+        lib().orc_dequant_lm(codes, T, d, sig, 1, 0, bits, _f64(levels), yh)
+    return yh
+
+
+def qjl_sketch(r: np.ndarray, S: np.ndarray):
+    """1-bit JL sketch of residuals r[T, d] with the Gaussian S[m, d]
+    ("Technisch Overzicht ...", TQ-QKV).  Returns (bits[T, m] 0/1, norms[T])."""
+    r, S = _f64(r), _f64(S)
+    T, d = r.shape
+    m = S.shape[0]
+    bits = np.zeros((T, m), dtype=np.uint8)
+    norms = np.zeros(T)
+    lib().orc_qjl_sketch(r, T, d, S, m, bits, norms)
+    return bits, norms
+
+
+def qjl_estimate(q: np.ndarray, S: np.ndarray, bits: np.ndarray, norm: float) -> float:
+    S = _f64(S)
+    return float(lib().orc_qjl_estimate(_f64(q), S.shape[1], S, S.shape[0],
+                                        np.ascontiguousarray(bits, dtype=np.uint8), float(norm)))
+
+
+def qjl_encode_head(plan: Plan, h: int, x: np.ndarray, stream: np.ndarray, S: np.ndarray, norms=None):
+    """Sketch of head h's key residuals: r = y - yhat in the latent basis, y
+    the projection of x, yhat the dequantized codes of `stream`.  Returns
+    (bits[T, m], residual norms[T])."""
+    x = _f64(x)
+    T, d = x.shape
+    y = np.zeros((T, d))
+    if plan.basis_kind == BASIS_EIGEN:
+        lib().orc_project(x, T, d, d, _f64(plan.basis[h]), y)
+    else:
+        lib().orc_rwht(x, T, d, d, np.ascontiguousarray(plan.signs[h], dtype=np.int8), y)
+    yh = dequant_head(plan, h, unpack(stream, T, plan.bits[h]), norms)
+    return qjl_sketch(y - yh, S)
+
+
+def attn_decode_qjl(q, Khat, Vhat, kbits, knorm, S, rot, scale: float) -> np.ndarray:
+    """Decode-step GQA attention whose key scores carry the QJL correction:
+    s_t = scale (<q, khat_t> + qjl_estimate(B_K^T q, bits_t, ||r_t||)).
+    q[B, Hq, d]; Khat, Vhat[B, ctx, Hkv, d]; kbits[B, Hkv, ctx, m]; knorm[B,
+    Hkv, ctx]; rot[Hkv] maps q to the latent coordinates of kv head h."""
+    B, Hq, d = q.shape
+    Hkv = Khat.shape[2]
+    g = Hq // Hkv
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        for j in range(Hq):
+            h = j // g
+            qt = rot[h](_f64(q[b, j]))
+            s = Khat[b, :, h, :] @ _f64(q[b, j])
+            # qjl_estimate for every token at once: sqrt(pi/2)/m ||r_t|| sum_j <s_j, qt> z_j(t)
+            z = 2.0 * kbits[b, h].astype(np.float64) - 1.0
+            s = s + np.sqrt(np.pi / 2) / S.shape[0] * _f64(knorm[b, h]) * (z @ (_f64(S) @ qt))
+            s = scale * s
+            p = np.exp(s - s.max())
+            out[b, j] = (p / p.sum()) @ Vhat[b, :, h, :]
     return out
 
 

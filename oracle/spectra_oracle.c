@@ -553,6 +553,45 @@ void orc_pack_into(const int32_t* codes, long n, int d, const uint8_t* bits, lon
 }
 
 /* ------------------------------------------------------------------------ */
+/* 1-bit Johnson-Lindenstrauss sketch of the key residual.  [ABL]
+ * "Experimentele Opstelling" and "Belangrijkste Bijdragen" 1 (TQ-QKV: a 1-bit
+ * QJL residual sketch on the key path): with a Gaussian matrix S (m x d,
+ * i.i.d. N(0,1) entries, supplied by the caller), a residual r is kept as the
+ * m signs z_j = sign(<s_j, r>) and its norm; an inner product with it is
+ * estimated as
+ *     <q, r>  ~  sqrt(pi / 2) / m * ||r|| * sum_j <s_j, q> z_j,
+ * unbiased because E[<s, q> sign(<s, r>)] = sqrt(2 / pi) <q, r> / ||r|| for
+ * Gaussian s.  Reading: the residual is taken in the latent coordinates
+ * (r = y - yhat, the rotation is orthonormal so inner products and norms are
+ * those of k - khat), sign(0) = +1, bits b_j = (z_j > 0).
+ * r[T][d] -> bits[T][m] (0/1), norms[T]. */
+void orc_qjl_sketch(const double* r, long T, int d, const double* S, int m, uint8_t* bits, double* norms)
+{
+    for (long t = 0; t < T; ++t) {
+        double n2 = 0.0;
+        for (int i = 0; i < d; ++i) n2 += r[t * d + i] * r[t * d + i];
+        norms[t] = sqrt(n2);
+        for (int j = 0; j < m; ++j) {
+            double a = 0.0;
+            for (int i = 0; i < d; ++i) a += S[(long)j * d + i] * r[t * d + i];
+            bits[t * m + j] = (uint8_t)(a >= 0.0);
+        }
+    }
+}
+
+/* The estimate of <q, r> from a sketch (definition above). */
+double orc_qjl_estimate(const double* q, int d, const double* S, int m, const uint8_t* bits, double norm)
+{
+    double acc = 0.0;
+    for (int j = 0; j < m; ++j) {
+        double sq = 0.0;
+        for (int i = 0; i < d; ++i) sq += S[(long)j * d + i] * q[i];
+        acc += bits[j] ? sq : -sq;
+    }
+    return sqrt(M_PI / 2.0) / (double)m * norm * acc;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Decode-step attention over reconstructed keys/values (the standard
  * attention that [SPECTRA] pipeline phase 3 feeds with rebuilt K/V):
  *   s_t = scale * <q, k_t>,  p = softmax(s) (max subtracted),

@@ -703,3 +703,73 @@ def test_attention_window_is_concatenation(orc):
             np.testing.assert_allclose(got[b, j], scipy.special.softmax(0.7 * Kc @ q[b, j]) @ Vc, rtol=1e-12)
     np.testing.assert_allclose(orc.attn_decode_window(q, K, V, Kw[:, :0], Vw[:, :0], 0.7),
                                orc.attn_decode(q, K, V, 0.7), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- QJL residual sketch
+def test_qjl_worked_example(orc):
+    for r in _golden_lines("qjl_worked_example.txt"):
+        v = [float(a) for a in r]
+        S = np.array(v[0:4]).reshape(2, 2)
+        res, q = np.array(v[4:6]), np.array(v[6:8])
+        bits, norms = orc.qjl_sketch(res[None], S)
+        assert list(bits[0]) == [int(v[8]), int(v[9])]
+        assert norms[0] == v[10]
+        assert abs(orc.qjl_estimate(q, S, bits[0], norms[0]) - v[11]) < 1e-12
+
+
+def test_qjl_unbiased_and_variance(orc):
+    """Over independent Gaussian sketch matrices the estimate of <q, r> is
+    unbiased, with variance ((pi/2) |q|^2 |r|^2 - <q, r>^2) / m (the
+    moments of <s, q> sign(<s, r>) for Gaussian s)."""
+    g = np.random.default_rng(31)
+    d, m, n = 16, 32, 6000
+    q, r = g.standard_normal(d), g.standard_normal(d)
+    est = np.empty(n)
+    for i in range(n):
+        S = g.standard_normal((m, d))
+        bits, norms = orc.qjl_sketch(r[None], S)
+        est[i] = orc.qjl_estimate(q, S, bits[0], norms[0])
+    true = float(q @ r)
+    var = ((np.pi / 2) * (q @ q) * (r @ r) - true ** 2) / m
+    assert abs(est.mean() - true) < 4 * np.sqrt(var / n)
+    assert abs(est.var() / var - 1) < 0.1
+
+
+def test_qjl_residual_is_the_reconstruction_error(orc):
+    """The sketched residual is the key's reconstruction error: its norm is
+    ||x - xhat|| (the rotation is orthonormal), and with m large the
+    corrected score <q, xhat> + estimate approaches <q, x>."""
+    x = synth.tiny_gaussian(3, T=64, H=1, d=16)[:, 0, :].astype(np.float64)
+    plan = orc.make_eigen_plan(x[:, None, :], 1.0)
+    enc = orc.encode_head(plan, 0, x)
+    xh = orc.decode_head(plan, 0, enc["stream"], 64)
+    S = np.random.default_rng(2).standard_normal((20000, 16))
+    bits, norms = orc.qjl_encode_head(plan, 0, x, enc["stream"], S)
+    np.testing.assert_allclose(norms, np.linalg.norm(x - xh, axis=1), rtol=1e-6)   # the fp32 plan basis
+    q = np.random.default_rng(4).standard_normal(16)
+    qt = plan.basis[0].T @ q
+    corr = np.array([orc.qjl_estimate(qt, S, bits[t], norms[t]) for t in range(64)])
+    err_plain = np.abs(xh @ q - x @ q).mean()
+    err_qjl = np.abs(xh @ q + corr - x @ q).mean()
+    assert err_qjl < 0.1 * err_plain
+
+
+def test_qjl_attention_uses_the_estimate(orc):
+    """The attention's vectorised correction is qjl_estimate token by token,
+    and with a zero residual sketch norm it is plain attention."""
+    g = np.random.default_rng(33)
+    B, Hq, Hkv, ctx, d, m = 1, 2, 1, 12, 8, 8
+    K, V = g.standard_normal((B, ctx, Hkv, d)), g.standard_normal((B, ctx, Hkv, d))
+    S = g.standard_normal((m, d))
+    bits = g.integers(0, 2, (B, Hkv, ctx, m)).astype(np.uint8)
+    nrm = g.uniform(0.1, 1.0, (B, Hkv, ctx))
+    q = g.standard_normal((B, Hq, d))
+    Qb = np.linalg.qr(g.standard_normal((d, d)))[0]
+    rot = [lambda v: Qb.T @ v]
+    got = orc.attn_decode_qjl(q, K, V, bits, nrm, S, rot, 0.5)
+    for j in range(Hq):
+        s = np.array([K[0, t, 0] @ q[0, j] + orc.qjl_estimate(Qb.T @ q[0, j], S, bits[0, 0, t], nrm[0, 0, t])
+                      for t in range(ctx)])
+        np.testing.assert_allclose(got[0, j], scipy.special.softmax(0.5 * s) @ V[0, :, 0], rtol=1e-12)
+    np.testing.assert_allclose(orc.attn_decode_qjl(q, K, V, bits, 0 * nrm, S, rot, 0.5),
+                               orc.attn_decode(q, K, V, 0.5), rtol=1e-13)
