@@ -306,6 +306,14 @@ def run_ours(args, rank, world, local_rank):
             "peak_source": peaks["source"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": _traffic(dom)}
 
+    # the encode's contraction with its operands resident in L2: the same
+    # 64 MiB layer encoded back to back (no rotating copies)
+    def l2_enc(i):
+        spx.spectra_encode(kp, K[0], kc[0])
+    l2_ms = _events_ms(l2_enc, 40, warm=5)
+    rot_l2 = _rotation_rate(T_TOK, H_KV, D, 3, l2_ms, _peaks()["bf16_tflops"])
+    rot_l2["launch_ms"] = round(l2_ms, 4)
+    rot_l2["note"] = "one 32768-token x 8-head K encode repeated on the same (L2-resident) input"
     attn = None
     if args.attn_workload:
         attn = attn_workload(spx, kp, vp, dev, _peaks(), reps=50, batch=args.attn_batch, local_rank=local_rank)
@@ -331,6 +339,7 @@ def run_ours(args, rank, world, local_rank):
         "calibrate_ms": round(ph["calibrate"], 4),
         "roofline": roof,
         "rotation": _rotation_rate(T_TOK, H_KV, D, 3, ph["encode"] / 2, peaks["bf16_tflops"]),
+        "rotation_l2": rot_l2,
         "attn_decode": attn,
         "budget_sweep": sweep,
         "variants": var,
