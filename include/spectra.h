@@ -397,6 +397,22 @@ SPECTRA_API spectra_status spectra_attn_decode_qjl(const spectra_plan* kplan, co
                                    spectra_stream_t stream);
 
 /*
+ * spectra_selftest_wait -- exercises, on the device, the bounded waits that
+ * every kernel of the library uses for its pipeline barriers (not part of
+ * the method).  A one-block kernel waits for an mbarrier that nothing ever
+ * arrives on: one thread with the busy-spin form, one warp with the
+ * suspending form, under one shared abort flag.  After limit_ns the first
+ * waiter gives up and raises the flag, and the rest give up on it; the kernel
+ * then returns normally, so the context stays usable.
+ * status: device int32[2] -- status[0] = -SPECTRA_ERR_TIMEOUT when the wait
+ *   gave up (0 if the barrier had completed), status[1] = the number of the
+ *   33 waiters that gave up.  elapsed_ns: device uint64 -- how long the
+ *   spinning thread waited.  limit_ns in 1 .. 10^10.
+ */
+SPECTRA_API spectra_status spectra_selftest_wait(uint64_t limit_ns, int32_t* status, uint64_t* elapsed_ns,
+                                     spectra_stream_t stream);
+
+/*
  * spectra_attn_decode_noalloc -- spectra_attn_decode for callers that cannot
  * allocate device memory when they run a decode step (code inside an
  * allocator or memory-pool callback, hosts whose device memory belongs to

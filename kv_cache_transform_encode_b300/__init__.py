@@ -38,7 +38,7 @@ EXPORTS = ("spectra_version", "spectra_set_kernel_family", "spectra_get_kernel_f
            "spectra_alloc_bits", "spectra_alloc_bits_ex", "spectra_effective_dim", "spectra_calibrate_plain",
            "spectra_plan_finalize", "spectra_encode", "spectra_append", "spectra_decode",
            "spectra_attn_workspace_bytes", "spectra_attn_decode", "spectra_attn_decode_window",
-           "spectra_qjl_encode", "spectra_attn_decode_qjl", "spectra_attn_decode_noalloc")
+           "spectra_qjl_encode", "spectra_attn_decode_qjl", "spectra_selftest_wait", "spectra_attn_decode_noalloc")
 
 
 class SpectraError(RuntimeError):
@@ -93,6 +93,7 @@ def lib() -> C.CDLL:
                                              vp]),
             "spectra_attn_decode_qjl": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp, vp, i64,
                                                   i64, vp, vp, i64, vp, i64, f32, vp, vp, sz, vp]),
+            "spectra_selftest_wait": (C.c_int, [C.c_uint64, vp, vp, vp]),
             "spectra_append": (C.c_int, [P, vp, C.c_int, i64, i64, i64, vp, i64, vp, i64, vp]),
             "spectra_attn_decode_window": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp, vp,
                                                      i64, i64, vp, vp, C.c_int, i64, i64, f32, vp, vp, sz, vp]),
@@ -371,6 +372,12 @@ def spectra_attn_decode_qjl(kplan: Plan, vplan: Plan, q: torch.Tensor, k_codes: 
                                        k_qjl_norms.stride(0), float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(),
                                        _stream(stream))
     _check(st, "spectra_attn_decode_qjl")
+
+
+def spectra_selftest_wait(limit_ns: int, status: torch.Tensor, elapsed_ns: torch.Tensor, stream=None):
+    """status: int32 cuda [2]; elapsed_ns: int64 cuda [1] (see spectra.h)."""
+    _check(lib().spectra_selftest_wait(int(limit_ns), _ptr(status), _ptr(elapsed_ns), _stream(stream)),
+           "spectra_selftest_wait")
 
 
 SPECTRA_ATTN_NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -17,6 +17,7 @@ spectra_status launch_encode_generic(const spectra_plan*, const void*, int, int6
 spectra_status launch_gram_tc(const spectra_plan*, const void*, int, int64_t, int64_t, float*, int, cudaStream_t,
                               bool*);
 int gram_tc_chunks(int heads, int64_t n_cal);
+spectra_status launch_wait_selftest(uint64_t limit_ns, int32_t* out, uint64_t* t_out, cudaStream_t s);
 spectra_status launch_qjl_encode(const spectra_plan*, const float*, const void*, int, int64_t, int64_t,
                                  const uint8_t*, int64_t, const float*, int64_t, uint8_t*, int64_t, float*,
                                  int64_t, cudaStream_t);
@@ -483,6 +484,15 @@ spectra_status spectra_attn_decode_qjl(const spectra_plan* kplan, const spectra_
     AttnQjl qj{sketch, k_qjl_bits, qjl_stride_bytes, k_qjl_norms, qjl_norms_stride};
     return launch_attn(kplan, vplan, q, q_dt, B, Hq, k_codes, v_codes, stream_stride_bytes, k_norms, v_norms,
                        norms_stride, ctx, softmax_scale, out, workspace, workspace_bytes, s, nullptr, &qj);
+}
+
+spectra_status spectra_selftest_wait(uint64_t limit_ns, int32_t* status, uint64_t* elapsed_ns,
+                                    spectra_stream_t stream)
+{
+    if (!status || !elapsed_ns || limit_ns == 0 || limit_ns > 10000000000ull) return SPECTRA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(elapsed_ns) & 7u) || (reinterpret_cast<uintptr_t>(status) & 3u))
+        return SPECTRA_ERR_INVALID_ARG;
+    return launch_wait_selftest(limit_ns, status, elapsed_ns, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -279,7 +279,9 @@ attn_tc_split_kernel(AttnTcParams P)
         const int s = tile % S;
         const int64_t t0 = t_begin + int64_t(tile) * TT;
         const uint8_t* stg = stage + size_t(s) * (P.kst + P.vst);
-        const bool ok = mbar_wait(&full[s], uint32_t(tile / S) & 1u, abort_flag, kWaitNs);
+        // a give-up is made warp-uniform: the warp-synchronous MMAs below run
+        // on whole warps or not at all
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], uint32_t(tile / S) & 1u, abort_flag, kWaitNs));
 
         // ---- scores of this warp's group (tokens t0 + 32 warp ...)
         const int64_t tg0 = t0 + 32 * warp;

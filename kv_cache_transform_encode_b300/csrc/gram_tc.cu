@@ -155,6 +155,45 @@ gram_tc_kernel(const uint16_t* __restrict__ x, int64_t n_cal, int64_t token_stri
     }
 }
 
+// Self-test of the bounded waits every kernel of the library uses: an
+// mbarrier that nothing ever arrives on.  Thread 0 spins on it (the single-
+// thread form), warp 1 waits on it (the suspending form), under one shared
+// abort flag: the first waiter to pass `limit_ns` raises the flag and every
+// other one gives up on it.  out[0] = -SPECTRA_ERR_TIMEOUT when thread 0 gave
+// up (0 otherwise), out[1] = how many of the 33 waiters gave up; t_out =
+// thread 0's wait in ns.
+__global__ void wait_selftest_kernel(uint64_t limit_ns, int32_t* out, uint64_t* t_out)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_s;
+    __shared__ int gave_up;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_s = 0;
+        gave_up = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    volatile int* abort_flag = &abort_s;
+    const int warp = threadIdx.x >> 5;
+    bool ok = true;
+    uint64_t t0 = 0, t1 = 0;
+    if (threadIdx.x == 0) {
+        t0 = globaltimer_ns();
+        ok = mbar_spin(&bar, 0u, abort_flag, limit_ns);
+        t1 = globaltimer_ns();
+    } else if (warp == 1) {
+        ok = mbar_wait(&bar, 0u, abort_flag, limit_ns);
+    }
+    if ((threadIdx.x == 0 || warp == 1) && !ok) atomicAdd(&gave_up, 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        out[0] = ok ? 0 : -SPECTRA_ERR_TIMEOUT;
+        out[1] = gave_up;
+        *t_out = t1 - t0;
+    }
+}
+
 }  // namespace
 
 // Chunks of whole 128-token tiles, at most gram_chunks(heads, n_cal) of them
@@ -165,6 +204,12 @@ int gram_tc_chunks(int heads, int64_t n_cal)
     const int64_t maxc = (n_cal + TILE - 1) / TILE;
     const int64_t c = want < maxc ? want : maxc;
     return int(c < 1 ? 1 : c);
+}
+
+spectra_status launch_wait_selftest(uint64_t limit_ns, int32_t* out, uint64_t* t_out, cudaStream_t s)
+{
+    wait_selftest_kernel<<<1, 64, 0, s>>>(limit_ns, out, t_out);
+    return cuda_status(cudaGetLastError());
 }
 
 spectra_status launch_gram_tc(const spectra_plan* plan, const void* x, int dt, int64_t n_cal, int64_t token_stride,

@@ -375,3 +375,20 @@ def test_buffer_status(spx, orc, path):
     compare_codes(orc, oplan, 1, enc, cc[1], T)
     want = orc.decode_head(oplan, 1, enc["stream"], T)
     assert rel_l2(out[:, 1, :].cpu().numpy(), want) <= 5 * REC_TOL
+
+
+def test_bounded_wait_gives_up_and_context_survives(spx, orc):
+    """The library's bounded waits on a barrier that nothing arrives on: every
+    waiter gives up with SPECTRA_ERR_TIMEOUT after the limit (the single-thread
+    spin and a suspending warp, through the shared abort flag), the kernel
+    returns, and the context keeps working (an ordinary encode/decode after
+    it is still exact against the oracle)."""
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    el = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for limit in (2_000, 200_000):
+        spx.spectra_selftest_wait(limit, st, el)
+        torch.cuda.synchronize()
+        assert st[0].item() == -5 and st[1].item() == 33, st.tolist()
+        assert limit // 2 <= el.item() < limit + 5_000_000, (limit, el.item())
+    x, xd, x64 = llama_case(T=300, H=2, seed=2)
+    _check_codec(spx, orc, orc.make_eigen_plan(x64, 2.0), x64, xd, 300)
