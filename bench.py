@@ -62,6 +62,11 @@ def parse():
     ap.add_argument("--attn-only", action="store_true",
                     help="profiling captures: calibrate one layer, then time only the compressed-attention "
                          "workload (prints its block, not a bench line)")
+    ap.add_argument("--codec-only", choices=["uniform", "lloyd", "rwht"], default=None,
+                    help="profiling captures: one K plan of the given kind on the layer (eigenbasis with uniform "
+                         "or Lloyd-Max levels at --avg-bits, or RWHT with 3-bit Lloyd-Max), then time only its "
+                         "encode and decode (prints their block, not a bench line)")
+    ap.add_argument("--avg-bits", type=float, default=2.0, help="budget of --codec-only (bits/value)")
     ap.add_argument("--attn-batch", type=int, default=16,
                     help="batch of the compressed-attention workload (default 16); smaller for profiling captures")
     return ap.parse_args()
@@ -191,6 +196,8 @@ def run_ours(args, rank, world, local_rank):
         spx.spectra_attn_decode(kp, vp, q, kc[c], vc[c], T_TOK, 1.0, att_o, workspace=aws)
         mark(5)
 
+    if args.codec_only:
+        return {"codec": codec_only(spx, args, K, dev, _peaks())}
     if args.attn_only:
         step(0)
         torch.cuda.synchronize()
@@ -460,6 +467,42 @@ def _relmse_cos(x, xh):
 
 
 SWEEP_BUDGETS = (4.0, 2.0, 1.33)
+
+
+def codec_only(spx, args, K, dev, peaks):
+    """Encode and decode of one K plan on the layer's inputs, for profiling
+    captures and quick timings: eigenbasis calibrated on the first 2048
+    tokens with uniform or Lloyd-Max levels at --avg-bits, or RWHT with the
+    fixed 3-bit Lloyd-Max codebook.  --warmup calls, then --steps timed
+    calls of each, rotating over the input copies."""
+    import torch
+
+    import synth
+    T = K[0].shape[0]
+    if args.codec_only == "rwht":
+        p = spx.Plan(H_KV, D, basis=spx.SPECTRA_BASIS_RWHT, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev)
+        p.signs.copy_(torch.from_numpy(synth.rwht_signs(7, H_KV, D)))
+        spx.spectra_alloc_bits(p, 0.0, fixed_bits=3)
+    else:
+        quant = spx.SPECTRA_Q_LLOYD_GAUSS if args.codec_only == "lloyd" else spx.SPECTRA_Q_UNIFORM3S
+        p = spx.Plan(H_KV, D, quant=quant, device=dev)
+        spx.spectra_calibrate(p, K[0], n_cal=N_CAL)
+        spx.spectra_alloc_bits(p, args.avg_bits)
+    n = len(K)
+    codes = [p.new_streams(T) for _ in range(n)]
+    norms = [torch.zeros((H_KV, T), device=dev) for _ in range(n)] if args.codec_only == "rwht" else [None] * n
+    xo = torch.empty_like(K[0])
+    enc = lambda i: spx.spectra_encode(p, K[i % n], codes[i % n], norms=norms[i % n])
+    dec = lambda i: spx.spectra_decode(p, codes[i % n], T, xo, norms=norms[i % n])
+    enc_ms = _events_ms(enc, args.steps, warm=args.warmup)
+    dec_ms = _events_ms(dec, args.steps, warm=args.warmup)
+    R = p.max_rec_bits
+    nb = 4 if args.codec_only == "rwht" else 0
+    launch_bytes = T * H_KV * (2 * D + R / 8 + nb)
+    return {"kind": args.codec_only, "avg_bits": args.avg_bits, "rec_bits": R, "encode_ms": round(enc_ms, 4),
+            "decode_ms": round(dec_ms, 4),
+            "encode_frac": round(launch_bytes / (enc_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "decode_frac": round(launch_bytes / (dec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
 
 
 def budget_sweep(spx, K, V, dev, peaks, local_rank, reps=10):
@@ -1034,7 +1077,7 @@ def main():
         dist.init_process_group("nccl")
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
-        if args.attn_only:
+        if args.attn_only or args.codec_only:
             print(json.dumps(res), flush=True)
             return
         if not args.no_cpu_baseline:

@@ -306,6 +306,35 @@ lm_tables_kernel(float* __restrict__ levels, float* __restrict__ thresh)
     }
 }
 
+// The bucket table of the Lloyd-Max encode (layout in spectra_internal.cuh)
+// from the thresholds, with a check of its premise: no threshold below the
+// inner grid or above it, at most one inside any bucket.  One block.
+__global__ void __launch_bounds__(256)
+lm_bucket_kernel(const float* __restrict__ thresh, float2* __restrict__ tab, int32_t* __restrict__ bad)
+{
+    bool ok = true;
+    for (int e = threadIdx.x; e < kBkEntries; e += blockDim.x) {
+        int b = 1;
+        while (b < kMaxBits && e >= bk_off(b + 1)) ++b;
+        const int j = e - bk_off(b), NB = 1 << bk_log(b), L = 1 << b;
+        const float w = ldexpf(1.f, -bk_shift(b));
+        const float ej = float(j - NB / 2) * w;                 // left edge (exact)
+        const float* tt = thresh + (b - 1) * kLmStride;         // tt[1 .. L-1] ascending
+        int cnt = 0;
+        for (int step = L >> 1; step; step >>= 1)
+            if (tt[cnt + step] <= ej) cnt += step;
+        const float hi = cnt + 1 <= L - 1 ? tt[cnt + 1] : INFINITY;
+        bool e_ok = hi == hi && hi > ej;
+        if (cnt + 2 <= L - 1 && !(tt[cnt + 2] >= ej + w)) e_ok = false;   // two thresholds in one bucket
+        if (j == 0 && (cnt != 0 || !(hi >= ej + w))) e_ok = false;          // none below the inner grid
+        if (j >= NB - 1 && cnt != L - 1) e_ok = false;                      // none above it
+        tab[e] = make_float2(hi, __int_as_float(cnt));
+        ok = ok && e_ok;
+    }
+    const int any_bad = __syncthreads_or(!ok);
+    if (threadIdx.x == 0) *bad = any_bad ? 1 : 0;
+}
+
 }  // namespace
 
 spectra_status launch_alloc(const spectra_plan* plan, int R_tot, int fixed_bits, cudaStream_t s)
@@ -354,6 +383,8 @@ spectra_status launch_finalize(const spectra_plan* plan, cudaStream_t s)
     if (st != SPECTRA_OK) return st;
     if (plan->quant == SPECTRA_Q_LLOYD_GAUSS) {
         lm_tables_kernel<<<kMaxBits, 32, 0, s>>>(const_cast<float*>(v.lm_level), const_cast<float*>(v.lm_thresh));
+        lm_bucket_kernel<<<1, 256, 0, s>>>(v.lm_thresh, const_cast<float2*>(v.lm_bucket),
+                                           const_cast<int32_t*>(v.lm_bucket_bad));
         st = cuda_status(cudaGetLastError());
         if (st != SPECTRA_OK) return st;
     }

@@ -165,6 +165,19 @@ __device__ __forceinline__ uint32_t quant_uniform(float y, float qk, float cl)
     return __float_as_uint(__fmaf_rd(s, cl, kMagic));
 }
 
+// Lloyd-Max code by the plan's bucket table (exact, one shared-memory
+// load): s = RD_sat(u 2^(k-p) + 1/2) and floor(s 2^p) (a round-down FMA
+// with a magic addend) give the exact bucket of u -- both scales are powers
+// of two and rounding down never crosses a multiple of 2^-p -- and then
+// code(u) = #{tau <= u} = cnt + (u >= hi): the same count as a search over
+// the thresholds, in the same fp32 comparisons.
+__device__ __forceinline__ float fma_rm_sat(float a, float b, float c)
+{
+    float d;
+    asm("fma.rm.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // ------------------------------------------------------------------ encode
 constexpr int ETILE = 256;                        // tokens per encode tile (MMA N)
 constexpr uint32_t ESTAGE = ETILE * D * 2;        // x tile, two K blocks: 64 KB
@@ -173,7 +186,6 @@ constexpr uint32_t IDESC_E = idesc_bf16_f32(128, ETILE);
 constexpr int kEncEpiWarps = 16;
 constexpr int kEncThreads = 64 + 32 * kEncEpiWarps;   // producer, MMA, epilogue
 constexpr uint32_t kImgCol = 256;                 // TMEM column of the basis image
-constexpr int kLmGroup = 8;   // Lloyd-Max values searched together
 
 struct EncParams {
     PlanView pv;
@@ -202,7 +214,7 @@ __host__ __device__ inline EncSmem enc_smem_layout(int stages, int max_rec_bits,
     L.img = stages >= 3 ? ESTAGE : 0;
     L.cbytes = uint32_t((32 * (max_rec_bits > 0 ? max_rec_bits : 1) + 15) / 16 * 16);
     L.cb = o;   o += 2 * L.cbytes;
-    L.th = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
+    L.th = o;   o += lm ? (kBkEntries * 8 + 15) / 16 * 16 : 0;   // Lloyd-Max bucket table
     L.red = o;  o += (4 * 4 * 32 + kEncEpiWarps * 32) * 4;   // RWHT norm partials and inverses
     L.bars = o; o += 256;
     L.total = o;
@@ -268,9 +280,12 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         tmem_alloc(tmem_holder, 512);      // accumulator: columns 0..255; basis image: 256..447
         tmem_relinquish();
     }
+    bool bk_bad = false;            // the plan's tables break the buckets' premise
     if (lm) {
-        float* th = reinterpret_cast<float*>(smem + L.th);
-        for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) th[e] = P.pv.lm_thresh[e];
+        const float4* src = reinterpret_cast<const float4*>(P.pv.lm_bucket);
+        float4* dst = reinterpret_cast<float4*>(smem + L.th);
+        for (int e = threadIdx.x; e < kBkEntries / 2; e += blockDim.x) dst[e] = src[e];
+        bk_bad = *P.pv.lm_bucket_bad != 0;
     }
     tc_fence_before();
     __syncthreads();
@@ -379,11 +394,15 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         const int c = q * 32 + lane;                   // this thread's channel
         const bool leader = warp == 2 && lane == 0;    // watches the accumulator, issues the stores
         const uint32_t tq = tmem + (uint32_t(q * 32) << 16);
-        const float* th = reinterpret_cast<const float*>(smem + L.th);
+        const float2* tab = reinterpret_cast<const float2*>(smem + L.th);
         float* part = reinterpret_cast<float*>(smem + L.red) + gi * (4 * 32);          // [4 q][32 t]
         float* invs = reinterpret_cast<float*>(smem + L.red) + 4 * 4 * 32 + (warp - 2) * 32;
         int cur_h = -1, R = 0, b = 0, o = 0, bmax = 0, ruse = 0;
         float qk = 0.f, cl = 0.f;
+        // Lloyd-Max bucket grid of this channel's width: clamp range, 2^k,
+        // m + magic, table offset - the magic's bit pattern
+        float bk_a = 0.f, bk_sc = 0.f;
+        int bk_base = 0;
         bool head_ok = true;
         uint32_t* out = nullptr;
         // the tile whose codes wait in shared memory for the bulk store
@@ -447,29 +466,31 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
             if (!lm) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = quant_uniform(__uint_as_float(r[i]), qk, cl);
+            } else if (!bk_bad) {
+                // eight lookups in flight at a time (the memory clobber keeps the
+                // compiler from hoisting all 32 loads, which needs 64 registers)
+#pragma unroll
+                for (int i0 = 0; i0 < 32; i0 += 8) {
+#pragma unroll
+                    for (int i = i0; i < i0 + 8; ++i) {
+                        const float u = __uint_as_float(r[i]) * (rwht ? invs[i] : qk);
+                        const float sv = fma_rm_sat(u, bk_a, 0.5f);
+                        const float2 e = tab[__float_as_int(__fmaf_rd(sv, bk_sc, kMagic)) + bk_base];
+                        r[i] = uint32_t(__float_as_int(e.y) + (u >= e.x ? 1 : 0));
+                    }
+                    asm volatile("" ::: "memory");
+                }
             } else {
-                // binary search over the thresholds, kLmGroup values at a time with the
-                // search steps outermost: kLmGroup independent shared-memory loads per step
-                const float* tb = th + (b > 0 ? (b - 1) * kLmStride : 0);
+                // a table whose premise failed: a binary search over the thresholds
+                const float* tb = P.pv.lm_thresh + (b > 0 ? (b - 1) * kLmStride : 0);
 #pragma unroll
-                for (int h16 = 0; h16 < 32; h16 += kLmGroup) {
-                    float u[kLmGroup];
-                    int lo[kLmGroup];
-#pragma unroll
-                    for (int i = 0; i < kLmGroup; ++i) {
-                        u[i] = __uint_as_float(r[h16 + i]) * (rwht ? invs[h16 + i] : qk);
-                        lo[i] = 0;
-                    }
-                    for (int sb = bmax - 1; sb >= 0; --sb) {
-                        const int step = sb < b ? (1 << sb) : 0;
-#pragma unroll
-                        for (int i = 0; i < kLmGroup; ++i) {
-                            const bool up = step != 0 && tb[lo[i] + step] <= u[i];
-                            lo[i] += up ? step : 0;
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < kLmGroup; ++i) r[h16 + i] = uint32_t(lo[i]);
+                for (int i = 0; i < 32; ++i) {
+                    const float u = __uint_as_float(r[i]) * (rwht ? invs[i] : qk);
+                    int lo = 0;
+#pragma unroll 1
+                    for (int step = b > 0 ? 1 << (b - 1) : 0; step; step >>= 1)
+                        if (tb[lo + step] <= u) lo += step;
+                    r[i] = uint32_t(lo);
                 }
             }
 #pragma unroll
@@ -524,29 +545,49 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                 qk = lm ? qs : qs / float(1 << b);
                 cl = float(1 << b) * (1.0f - 0x1p-22f);
                 bmax = __reduce_max_sync(0xffffffffu, b);
+                if (lm) {
+                    const int bw = b > 0 ? b : 1;
+                    bk_a = __int_as_float((127 + bk_shift(bw) - bk_log(bw)) << 23);      // 2^(k-p)
+                    bk_sc = __int_as_float((127 + bk_log(bw)) << 23);                    // 2^p
+                    bk_base = bk_off(bw) - __float_as_int(kMagic);
+                }
                 out = reinterpret_cast<uint32_t*>(P.codes + int64_t(h) * P.sstride) + P.g0 * R;
             }
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tq + gi * 32, r0);
-            tmem_ld32(tq + (gi + 4) * 32, r1);
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(accempty);      // accumulator read: the next tile's MMAs may start
             uint32_t* cb = reinterpret_cast<uint32_t*>(smem + L.cb + (k & 1) * L.cbytes);
             const bool live = head_ok && R > 0;
-            if (rwht) {
-                uint32_t Y[8];
-                if (rwht_norm(r0, tile, gi)) {
-                    if (live) { quant8(r0, Y); store8(Y, cb, tile, gi); }
-                    if (rwht_norm(r1, tile, gi + 4) && live) { quant8(r1, Y); store8(Y, cb, tile, gi + 4); }
+            if (rwht || lm) {
+                // one group at a time (the per-token norms and the table
+                // lookups need the registers); the accumulator is released
+                // after the second read -- these epilogues are longer than the MMAs
+                uint32_t r[32], Y[8];
+                tmem_ld32(tq + gi * 32, r);
+                tmem_ld_wait();
+                const bool ok0 = !rwht || rwht_norm(r, tile, gi);
+                if (ok0 && live) { quant8(r, Y); store8(Y, cb, tile, gi); }
+                tmem_ld32(tq + (gi + 4) * 32, r);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty);
+                if (ok0 && (!rwht || rwht_norm(r, tile, gi + 4)) && live) {
+                    quant8(r, Y);
+                    store8(Y, cb, tile, gi + 4);
                 }
-            } else if (live) {
-                uint32_t Y0[8], Y1[8];
-                quant8(r0, Y0);
-                quant8(r1, Y1);
-                store8(Y0, cb, tile, gi);
-                store8(Y1, cb, tile, gi + 4);
+            } else {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tq + gi * 32, r0);
+                tmem_ld32(tq + (gi + 4) * 32, r1);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty);      // accumulator read: the next tile's MMAs may start
+                if (live) {
+                    uint32_t Y[8];
+                    quant8(r0, Y);
+                    store8(Y, cb, tile, gi);
+                    quant8(r1, Y);
+                    store8(Y, cb, tile, gi + 4);
+                }
             }
             fence_proxy_async_smem();      // this thread's words -> the bulk store
             p_out = out;

@@ -13,6 +13,21 @@ constexpr int kGroup = 32;          // tokens per bit-plane group (one warp)
 constexpr int kMaxBits = 8;         // widest channel code
 constexpr int kLmStride = 256;      // row stride of the Lloyd-Max tables
 
+// Bucket grids of the Lloyd-Max encode (codec_tc.cu): width b splits
+// [-U_b, U_b) into NB_b = 2^p_b buckets of w_b = 2^-k_b, no wider than the
+// smallest gap between two thresholds of the Gaussian tables (0.98, 0.50,
+// 0.26, 0.13, 0.067, 0.034, 0.017 for b = 2..8), so a bucket holds at most
+// one threshold; every threshold lies in the inner buckets (U_b = 2, 2, 4,
+// 4, 4, 4, 4, 8 against largest thresholds 0, 0.98, 1.75, 2.40, 2.98, 3.49,
+// 3.96, 4.40).  Entry j of width b (j = 0..NB_b, entry NB_b taking u >= U_b)
+// holds (hi, cnt): cnt = #{tau <= left edge j}, hi = the first threshold
+// above that edge (+inf if none); code(u) = cnt + (u >= hi).
+__host__ __device__ constexpr int bk_shift(int b) { return b <= 1 ? 0 : (b <= 3 ? 1 : b - 2); }   // k_b
+__host__ __device__ constexpr int bk_log(int b) { return b <= 7 ? b + 1 : 10; }                       // p_b
+__host__ __device__ constexpr int bk_off(int b) { return b <= kMaxBits ? (1 << (b + 1)) - 4 + (b - 1) : 1540; }
+constexpr int kBkEntries = 1540;   // sum over b of NB_b + 1
+static_assert(bk_off(kMaxBits) + (1 << bk_log(kMaxBits)) + 1 == kBkEntries, "bucket table size");
+
 // ---------------------------------------------------------------------------
 // Layout of a plan's `derived` buffer.  Each table starts on a 256-byte
 // boundary.  Per head h:
@@ -22,6 +37,8 @@ constexpr int kLmStride = 256;      // row stride of the Lloyd-Max tables
 // Shared by every head:
 //   lm_level[b-1][k] f32 Gaussian Lloyd-Max level k of width b (ascending)
 //   lm_thresh[b-1][k] f32 threshold between levels k-1 and k (k >= 1)
+//   lm_bucket[e]     (f32 hi, i32 cnt) bucket table of the Lloyd-Max encode
+//   lm_bucket_bad    i32 nonzero when the tables break the buckets' premise
 // Tensor-core operand images (codec_tc.cu):
 //   enc_img[h]  bf16 basis image for the encode contraction
 //   dec_img[h]  bf16 basis image for the decode contraction
@@ -30,7 +47,8 @@ constexpr int kLmStride = 256;      // row stride of the Lloyd-Max tables
 //               <= 7: the decode contraction then takes 128 + code)
 // ---------------------------------------------------------------------------
 struct DerivedLayout {
-    size_t chan_off, qscale, rscale, lm_level, lm_thresh, enc_img, dec_img, wmax, dec_bias, total;
+    size_t chan_off, qscale, rscale, lm_level, lm_thresh, lm_bucket, lm_bucket_bad, enc_img, dec_img, wmax, dec_bias,
+        total;
     size_t enc_img_head_bytes, dec_img_head_bytes;
 };
 
@@ -54,6 +72,8 @@ __host__ __device__ inline DerivedLayout derived_layout(int heads, int d)
     L.rscale = o;    o = align256(o + hd * sizeof(float));
     L.lm_level = o;  o = align256(o + kMaxBits * kLmStride * sizeof(float));
     L.lm_thresh = o; o = align256(o + kMaxBits * kLmStride * sizeof(float));
+    L.lm_bucket = o; o = align256(o + kBkEntries * 2 * sizeof(float));
+    L.lm_bucket_bad = o; o = align256(o + sizeof(int32_t));
     L.enc_img_head_bytes = enc_img_bytes(d);
     L.dec_img_head_bytes = dec_img_bytes(d);
     L.enc_img = o;   o = align256(o + size_t(heads) * L.enc_img_head_bytes);
@@ -77,6 +97,8 @@ struct PlanView {
     const float* rscale;
     const float* lm_level;
     const float* lm_thresh;
+    const float2* lm_bucket;
+    const int32_t* lm_bucket_bad;
     const uint8_t* enc_img;
     const uint8_t* dec_img;
     const int32_t* wmax;
@@ -104,6 +126,8 @@ inline PlanView make_view(const spectra_plan* p)
     v.rscale = reinterpret_cast<const float*>(base + L.rscale);
     v.lm_level = reinterpret_cast<const float*>(base + L.lm_level);
     v.lm_thresh = reinterpret_cast<const float*>(base + L.lm_thresh);
+    v.lm_bucket = reinterpret_cast<const float2*>(base + L.lm_bucket);
+    v.lm_bucket_bad = reinterpret_cast<const int32_t*>(base + L.lm_bucket_bad);
     v.enc_img = base + L.enc_img;
     v.dec_img = base + L.dec_img;
     v.wmax = reinterpret_cast<const int32_t*>(base + L.wmax);
