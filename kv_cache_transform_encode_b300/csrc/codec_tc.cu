@@ -280,6 +280,9 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         tmem_alloc(tmem_holder, 512);      // accumulator: columns 0..255; basis image: 256..447
         tmem_relinquish();
     }
+    // the prologue above overlaps the previous kernel; global reads wait for it
+    pdl_trigger();
+    pdl_wait();
     bool bk_bad = false;            // the plan's tables break the buckets' premise
     if (lm) {
         const float4* src = reinterpret_cast<const float4*>(P.pv.lm_bucket);
@@ -753,6 +756,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         tmem_alloc(tmem_holder, 256);
         tmem_relinquish();
     }
+    // the prologue above overlaps the previous kernel; global reads wait for it
+    pdl_trigger();
+    pdl_wait();
     if (lm) {
         float* lv = reinterpret_cast<float*>(smem + L.lv);
         for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) lv[e] = P.pv.lm_level[e];
@@ -1266,7 +1272,7 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
     auto kern = lm ? (rw ? encode_tc_kernel<true, true> : encode_tc_kernel<true, false>)
                    : (rw ? encode_tc_kernel<false, true> : encode_tc_kernel<false, false>);
     if (spectra_status st = set_smem(kern, sm)) return st;
-    kern<<<grid, kEncThreads, sm, s>>>(m, P);
+    if (cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kEncThreads), sm, s, m, P)) return cuda_status(e);
     *done = true;
     return cuda_status(cudaGetLastError());
 }
@@ -1306,7 +1312,7 @@ spectra_status launch_decode_tc(const spectra_plan* plan, const uint8_t* codes, 
     auto kern = lm ? decode_tc_kernel<true> : decode_tc_kernel<false>;
     if (spectra_status st = set_smem(kern, sm)) return st;
     const int grid = sched_grid(sm_count(), plan->heads, P.tiles_per_head);
-    kern<<<grid, kDecThreads, sm, s>>>(m, P);
+    if (cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kDecThreads), sm, s, m, P)) return cuda_status(e);
     *done = true;
     return cuda_status(cudaGetLastError());
 }

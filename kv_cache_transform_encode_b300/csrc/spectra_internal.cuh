@@ -52,6 +52,26 @@ struct DerivedLayout {
     size_t enc_img_head_bytes, dec_img_head_bytes;
 };
 
+// Launch with programmatic dependent launch allowed: the kernel's CTAs may
+// start (and run their prologue) while the previous kernel in the stream
+// finishes; such a kernel calls pdl_wait() before its first global read.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Per-head tensor-core operand images (bytes; head_dim 128 only, the
