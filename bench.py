@@ -187,11 +187,10 @@ def run_ours(args, rank, world, local_rank):
         fork[1].record(s2)
         s.wait_event(fork[1])
         mark(2)
-        spx.spectra_encode(kp, K[c], kc[c])
-        spx.spectra_encode(vp, V[c], vc[c])
+        # K and V of the layer in one call (one launch) each way
+        spx.spectra_encode_kv(kp, vp, K[c], V[c], kc[c], vc[c])
         mark(3)
-        spx.spectra_decode(kp, kc[c], T_TOK, ko[c])
-        spx.spectra_decode(vp, vc[c], T_TOK, vo[c])
+        spx.spectra_decode_kv(kp, vp, kc[c], vc[c], T_TOK, ko[c], vo[c])
         mark(4)
         spx.spectra_attn_decode(kp, vp, q, kc[c], vc[c], T_TOK, 1.0, att_o, workspace=aws)
         mark(5)
@@ -300,14 +299,14 @@ def run_ours(args, rank, world, local_rank):
     d2h = hkc[0].numel() + hvc[0].numel() + hatt[0].numel() * 4
 
     # ---- roofline of the dominant HBM kernel (encode or decode, whichever
-    # takes longer; each phase is two launches, K and V)
+    # takes longer; each phase is one launch over K and V)
     import json as _json
     peaks = _peaks()
     enc_bytes = 2 * (T_TOK * H_KV * D * 2 + H_KV * sbytes)      # per phase (K+V)
     dec_bytes = enc_bytes
     dom = "encode" if ph["encode"] >= ph["decode"] else "decode"
-    per_launch_bytes = (enc_bytes if dom == "encode" else dec_bytes) / 2
-    per_launch_ms = ph[dom] / 2
+    per_launch_bytes = enc_bytes if dom == "encode" else dec_bytes
+    per_launch_ms = ph[dom]
     achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "peak_source": peaks["source"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -345,7 +344,7 @@ def run_ours(args, rank, world, local_rank):
         "codec_value_note": "encode + decode phases only (the codec's rate; value also counts calibration)",
         "calibrate_ms": round(ph["calibrate"], 4),
         "roofline": roof,
-        "rotation": _rotation_rate(T_TOK, H_KV, D, 3, ph["encode"] / 2, peaks["bf16_tflops"]),
+        "rotation": _rotation_rate(T_TOK, 2 * H_KV, D, 3, ph["encode"], peaks["bf16_tflops"]),
         "rotation_l2": rot_l2,
         "attn_decode": attn,
         "budget_sweep": sweep,
@@ -538,12 +537,10 @@ def budget_sweep(spx, K, V, dev, peaks, local_rank, reps=10):
         vc = [vp.new_streams(T) for _ in range(2)]
 
         def enc(i):
-            spx.spectra_encode(kp, K[i % 2], kc[i % 2])
-            spx.spectra_encode(vp, V[i % 2], vc[i % 2])
+            spx.spectra_encode_kv(kp, vp, K[i % 2], V[i % 2], kc[i % 2], vc[i % 2])
 
         def dec(i):
-            spx.spectra_decode(kp, kc[i % 2], T, ko)
-            spx.spectra_decode(vp, vc[i % 2], T, vo)
+            spx.spectra_decode_kv(kp, vp, kc[i % 2], vc[i % 2], T, ko, vo)
         def load():
             enc(0)
             dec(0)
@@ -569,8 +566,8 @@ def budget_sweep(spx, K, V, dev, peaks, local_rank, reps=10):
         dv, _ = _relmse_cos(V[0][sl], vo[sl])
         out.append({"avg_bits": B, "rec_bits": R, "compression_vs_bf16": round(16.0 * D / R, 2),
                     "encode_ms": round(enc_ms, 4), "decode_ms": round(dec_ms, 4),
-                    "encode_frac": round(launch_bytes / (enc_ms / 2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                    "decode_frac": round(launch_bytes / (dec_ms / 2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "encode_frac": round(2 * launch_bytes / (enc_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "decode_frac": round(2 * launch_bytes / (dec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                     "codec_tokens_per_s": round(T / ((enc_ms + dec_ms) * 1e-3), 1),
                     "relmse_k": round(rk, 6), "relmse_v": round(rv, 6), "cosine_k": round(ck, 6),
                     "cosine_v": round(cv, 6),
@@ -785,12 +782,10 @@ def qwen_rwht(spx, dev, peaks, local_rank, steps=4, e2e_steps=2, seed=2024):
     def step(i=0, mark=False):
         if mark:
             ev[0].record()
-        spx.spectra_encode(kp, K, kc, norms=kn)
-        spx.spectra_encode(vp, V, vc, norms=vn)
+        spx.spectra_encode_kv(kp, vp, K, V, kc, vc, k_norms=kn, v_norms=vn)
         if mark:
             ev[1].record()
-        spx.spectra_decode(kp, kc, T, ko, norms=kn)
-        spx.spectra_decode(vp, vc, T, vo, norms=vn)
+        spx.spectra_decode_kv(kp, vp, kc, vc, T, ko, vo, k_norms=kn, v_norms=vn)
         if mark:
             ev[2].record()
 
@@ -803,8 +798,8 @@ def qwen_rwht(spx, dev, peaks, local_rank, steps=4, e2e_steps=2, seed=2024):
     rk, ck = _relmse_cos(K[:4096], ko[:4096])
     rv, cv = _relmse_cos(V[:4096], vo[:4096])
     per_vec = 2 * D + 3 * D / 8 + 4
-    launch_bytes = T * H * per_vec
-    dom_ms = max(enc_ms, dec_ms) / 2
+    launch_bytes = 2 * T * H * per_vec          # one launch: K and V
+    dom_ms = max(enc_ms, dec_ms)
     achieved = launch_bytes / (dom_ms * 1e-3) / 1e9
     res = {"workload": (f"qwen2.5-7b-shaped cache: {QWEN_LAYERS} layers x {QWEN_KV} kv heads, {T} tokens, "
                         "d 128, bf16 K and V (spiked+outlier Student-t(4) synthetic); RWHT with seeded signs, "
@@ -882,11 +877,11 @@ def qwen_oracle_sample(T=16384, seed=2024):
 def launches_per_step():
     """Kernels this library launches per step (counted from the dispatch in
     csrc/api.cu and csrc/alloc.cu): calibrate = Gram partials + Jacobi;
-    alloc = water-filling + finalize + tensor-core operand images; encode 1;
-    decode 1 -- each for K and V; attention = query preparation + split
-    kernel + combine."""
-    per_side = 2 + 3 + 1 + 1
-    return 2 * per_side + 3
+    alloc = water-filling + finalize + tensor-core operand images -- each for
+    K and V; encode 1 and decode 1 for K and V together; attention = query
+    preparation + split kernel + combine."""
+    per_side = 2 + 3
+    return 2 * per_side + 1 + 1 + 3
 
 
 def _kernel_sources_sha(names):

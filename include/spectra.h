@@ -268,6 +268,25 @@ SPECTRA_API spectra_status spectra_encode(const spectra_plan* plan, const void* 
                               spectra_stream_t stream);
 
 /*
+ * spectra_encode_kv -- spectra_encode of a layer's keys and values in one
+ * call: exactly spectra_encode(kplan, k, ..., k_codes, ..., k_norms, ...)
+ * followed by spectra_encode(vplan, v, ..., v_codes, ..., v_norms, ...) on
+ * the same stream, with the same codes.  ("Sintesi Tecnica: SPECTRA", "La
+ * Pipeline di SPECTRA" phase 3: each token's key and value are projected,
+ * quantized and appended.)  kplan and vplan must have the same heads and
+ * head_dim (else SPECTRA_ERR_INVALID_ARG); k and v share dt, T and
+ * token_stride, the two stream sets share stream_stride_bytes, the norms
+ * (RWHT plans) share norms_stride.  When both plans take the tensor-core
+ * encode (bf16, d = 128, the same basis and quantizer) the two halves run as
+ * one launch, so its fixed cost is paid once; otherwise as two.  Every
+ * argument of both halves is checked before anything is launched.
+ */
+SPECTRA_API spectra_status spectra_encode_kv(const spectra_plan* kplan, const spectra_plan* vplan, const void* k,
+                                 const void* v, spectra_dtype dt, int64_t T, int64_t token_stride,
+                                 uint8_t* k_codes, uint8_t* v_codes, int64_t stream_stride_bytes,
+                                 float* k_norms, float* v_norms, int64_t norms_stride, spectra_stream_t stream);
+
+/*
  * spectra_append -- encode n new tokens of every head at stream positions
  * t0 .. t0+n-1 (any t0: a partly filled 32-token group keeps its earlier
  * tokens).  ("Sintesi Tecnica: SPECTRA", "La Pipeline di SPECTRA" phase 2,
@@ -300,6 +319,23 @@ SPECTRA_API spectra_status spectra_decode(const spectra_plan* plan, const uint8_
                               int64_t stream_stride_bytes, const float* norms,
                               int64_t norms_stride, int64_t T, void* x_out, spectra_dtype out_dt,
                               int64_t token_stride, spectra_stream_t stream);
+
+/*
+ * spectra_decode_kv -- spectra_decode of a layer's keys and values in one
+ * call: exactly spectra_decode(kplan, k_codes, ..., k_norms, ..., k_out, ...)
+ * followed by spectra_decode(vplan, v_codes, ..., v_norms, ..., v_out, ...)
+ * on the same stream.  kplan and vplan must have the same heads and
+ * head_dim (else SPECTRA_ERR_INVALID_ARG); the stream sets share
+ * stream_stride_bytes, the norms norms_stride, the outputs out_dt and
+ * token_stride.  One launch when both plans take the tensor-core decode (d =
+ * 128, the same basis and quantizer), else two.  Every argument of both
+ * halves is checked before anything is launched.
+ */
+SPECTRA_API spectra_status spectra_decode_kv(const spectra_plan* kplan, const spectra_plan* vplan,
+                                 const uint8_t* k_codes, const uint8_t* v_codes, int64_t stream_stride_bytes,
+                                 const float* k_norms, const float* v_norms, int64_t norms_stride, int64_t T,
+                                 void* k_out, void* v_out, spectra_dtype out_dt, int64_t token_stride,
+                                 spectra_stream_t stream);
 
 /*
  * spectra_attn_decode -- one decode step of grouped-query attention read

@@ -36,7 +36,8 @@ EXPORTS = ("spectra_version", "spectra_set_kernel_family", "spectra_get_kernel_f
            "spectra_status_string", "spectra_plan_derived_bytes",
            "spectra_stream_bytes", "spectra_calibrate_workspace_bytes", "spectra_calibrate",
            "spectra_alloc_bits", "spectra_alloc_bits_ex", "spectra_effective_dim", "spectra_calibrate_plain",
-           "spectra_plan_finalize", "spectra_encode", "spectra_append", "spectra_decode",
+           "spectra_plan_finalize", "spectra_encode", "spectra_encode_kv", "spectra_append", "spectra_decode",
+           "spectra_decode_kv",
            "spectra_attn_workspace_bytes", "spectra_attn_decode", "spectra_attn_decode_window",
            "spectra_qjl_encode", "spectra_attn_decode_qjl", "spectra_selftest_wait", "spectra_attn_decode_noalloc")
 
@@ -88,7 +89,9 @@ def lib() -> C.CDLL:
             "spectra_calibrate_plain": (C.c_int, [P, vp, C.c_int, i64, i64, vp, sz, vp]),
             "spectra_plan_finalize": (C.c_int, [P, vp]),
             "spectra_encode": (C.c_int, [P, vp, C.c_int, i64, i64, vp, i64, vp, i64, vp]),
+            "spectra_encode_kv": (C.c_int, [P, P, vp, vp, C.c_int, i64, i64, vp, vp, i64, vp, vp, i64, vp]),
             "spectra_decode": (C.c_int, [P, vp, i64, vp, i64, i64, vp, C.c_int, i64, vp]),
+            "spectra_decode_kv": (C.c_int, [P, P, vp, vp, i64, vp, vp, i64, i64, vp, vp, C.c_int, i64, vp]),
             "spectra_qjl_encode": (C.c_int, [P, vp, vp, C.c_int, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                              vp]),
             "spectra_attn_decode_qjl": (C.c_int, [P, P, vp, C.c_int, C.c_int, C.c_int, vp, vp, i64, vp, vp, i64,
@@ -275,6 +278,27 @@ def spectra_encode(plan: Plan, x: torch.Tensor, codes: torch.Tensor, norms: torc
     _check(st, "spectra_encode")
 
 
+def spectra_encode_kv(kplan: Plan, vplan: Plan, k: torch.Tensor, v: torch.Tensor, k_codes: torch.Tensor,
+                      v_codes: torch.Tensor, k_norms: torch.Tensor | None = None,
+                      v_norms: torch.Tensor | None = None, T: int | None = None, stream=None):
+    """k, v: [T, H, d] (same dtype and token stride); k_codes, v_codes: uint8
+    [H, stride] (same stride); norms (RWHT): f32 [H, >=T] (same stride)."""
+    T = k.shape[0] if T is None else T
+    if v.stride(0) != k.stride(0) or v.dtype != k.dtype:
+        raise ValueError("spectra_encode_kv: k and v need the same dtype and token stride")
+    ss = k_codes.stride(0) if k_codes.dim() > 1 else 0
+    if (v_codes.stride(0) if v_codes.dim() > 1 else 0) != ss:
+        raise ValueError("spectra_encode_kv: k_codes and v_codes need the same stride")
+    ns = k_norms.stride(0) if k_norms is not None and k_norms.dim() > 1 else 0
+    if v_norms is not None and v_norms.dim() > 1 and v_norms.stride(0) != ns:
+        raise ValueError("spectra_encode_kv: k_norms and v_norms need the same stride")
+    kp, vp = kplan.c(), vplan.c()
+    st = lib().spectra_encode_kv(C.byref(kp), C.byref(vp), _ptr(k), _ptr(v), _dt(k), T, k.stride(0),
+                                 _ptr(k_codes), _ptr(v_codes), ss, _ptr(k_norms), _ptr(v_norms), ns,
+                                 _stream(stream))
+    _check(st, "spectra_encode_kv")
+
+
 def spectra_append(plan: Plan, x: torch.Tensor, t0: int, codes: torch.Tensor,
                    norms: torch.Tensor | None = None, stream=None):
     """Append x [n, H, d] at stream positions t0 .. t0+n-1 of codes
@@ -294,6 +318,26 @@ def spectra_decode(plan: Plan, codes: torch.Tensor, T: int, out: torch.Tensor,
                               _ptr(norms), norms.stride(0) if norms is not None and norms.dim() > 1 else 0,
                               T, _ptr(out), _dt(out), out.stride(0), _stream(stream))
     _check(st, "spectra_decode")
+
+
+def spectra_decode_kv(kplan: Plan, vplan: Plan, k_codes: torch.Tensor, v_codes: torch.Tensor, T: int,
+                      k_out: torch.Tensor, v_out: torch.Tensor, k_norms: torch.Tensor | None = None,
+                      v_norms: torch.Tensor | None = None, stream=None):
+    """k_codes, v_codes: uint8 [H, stride] (same stride); k_out, v_out: [T, H, d]
+    (same dtype and token stride); norms (RWHT): f32 [H, >=T] (same stride)."""
+    ss = k_codes.stride(0) if k_codes.dim() > 1 else 0
+    if (v_codes.stride(0) if v_codes.dim() > 1 else 0) != ss:
+        raise ValueError("spectra_decode_kv: k_codes and v_codes need the same stride")
+    if v_out.stride(0) != k_out.stride(0) or v_out.dtype != k_out.dtype:
+        raise ValueError("spectra_decode_kv: k_out and v_out need the same dtype and token stride")
+    ns = k_norms.stride(0) if k_norms is not None and k_norms.dim() > 1 else 0
+    if v_norms is not None and v_norms.dim() > 1 and v_norms.stride(0) != ns:
+        raise ValueError("spectra_decode_kv: k_norms and v_norms need the same stride")
+    kp, vp = kplan.c(), vplan.c()
+    st = lib().spectra_decode_kv(C.byref(kp), C.byref(vp), _ptr(k_codes), _ptr(v_codes), ss, _ptr(k_norms),
+                                 _ptr(v_norms), ns, T, _ptr(k_out), _ptr(v_out), _dt(k_out), k_out.stride(0),
+                                 _stream(stream))
+    _check(st, "spectra_decode_kv")
 
 
 def spectra_attn_decode(kplan: Plan, vplan: Plan, q: torch.Tensor, k_codes: torch.Tensor,

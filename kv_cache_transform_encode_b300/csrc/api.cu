@@ -27,6 +27,12 @@ spectra_status launch_decode_generic(const spectra_plan*, const uint8_t*, int64_
                                      int64_t, int64_t, void*, int, int64_t, cudaStream_t);
 spectra_status launch_encode_tc(const spectra_plan*, const void*, int, int64_t, int64_t,
                                 uint8_t*, int64_t, float*, int64_t, cudaStream_t, bool*, int64_t g0 = 0);
+spectra_status launch_encode_tc_kv(const spectra_plan*, const spectra_plan*, const void*, const void*, int, int64_t,
+                                   int64_t, uint8_t*, uint8_t*, int64_t, float*, float*, int64_t, cudaStream_t,
+                                   bool*);
+spectra_status launch_decode_tc_kv(const spectra_plan*, const spectra_plan*, const uint8_t*, const uint8_t*, int64_t,
+                                   const float*, const float*, int64_t, int64_t, void*, void*, int, int64_t,
+                                   cudaStream_t, bool*);
 spectra_status launch_decode_tc(const spectra_plan*, const uint8_t*, int64_t, const float*,
                                 int64_t, int64_t, void*, int, int64_t, cudaStream_t, bool*);
 }  // namespace spectra
@@ -313,6 +319,42 @@ spectra_status spectra_encode(const spectra_plan* plan, const void* x, spectra_d
                                  norms_stride, s);
 }
 
+spectra_status spectra_encode_kv(const spectra_plan* kplan, const spectra_plan* vplan, const void* k, const void* v,
+                                 spectra_dtype dt, int64_t T, int64_t token_stride, uint8_t* k_codes,
+                                 uint8_t* v_codes, int64_t stream_stride_bytes, float* k_norms, float* v_norms,
+                                 int64_t norms_stride, spectra_stream_t stream)
+{
+    // every argument of both halves is checked before anything is launched
+    const spectra_plan* plans[2] = {kplan, vplan};
+    const void* xs[2] = {k, v};
+    uint8_t* cs[2] = {k_codes, v_codes};
+    float* ns[2] = {k_norms, v_norms};
+    spectra_status st;
+    for (int i = 0; i < 2; ++i) {
+        if ((st = check_plan(plans[i], true))) return st;
+        if ((st = check_cache(xs[i], dt, T, token_stride, plans[i]->heads, plans[i]->head_dim))) return st;
+        if ((st = check_streams(plans[i], cs[i], stream_stride_bytes, T, plans[i]->heads))) return st;
+        if (plans[i]->basis == SPECTRA_BASIS_RWHT && T > 0) {
+            if (!ns[i] || (plans[i]->heads > 1 && norms_stride < T)) return SPECTRA_ERR_INVALID_ARG;
+        }
+    }
+    if (kplan->heads != vplan->heads || kplan->head_dim != vplan->head_dim) return SPECTRA_ERR_INVALID_ARG;
+    if (T == 0) return SPECTRA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (kernel_family() != SPECTRA_KERNELS_CUDA_CORE) {
+        bool done = false;
+        st = launch_encode_tc_kv(kplan, vplan, k, v, dt, T, token_stride, k_codes, v_codes, stream_stride_bytes,
+                                 k_norms, v_norms, norms_stride, s, &done);
+        if (st || done) return st;
+    }
+    // not one launch: the two encodes in turn
+    if ((st = spectra_encode(kplan, k, dt, T, token_stride, k_codes, stream_stride_bytes, k_norms, norms_stride,
+                             stream)))
+        return st;
+    return spectra_encode(vplan, v, dt, T, token_stride, v_codes, stream_stride_bytes, v_norms, norms_stride,
+                          stream);
+}
+
 spectra_status spectra_append(const spectra_plan* plan, const void* x, spectra_dtype dt, int64_t n,
                               int64_t token_stride, int64_t t0, uint8_t* codes, int64_t stream_stride_bytes,
                               float* norms, int64_t norms_stride, spectra_stream_t stream)
@@ -381,6 +423,40 @@ spectra_status spectra_decode(const spectra_plan* plan, const uint8_t* codes, in
     }
     return launch_decode_generic(plan, codes, stream_stride_bytes, norms, norms_stride, T, x_out,
                                  out_dt, token_stride, s);
+}
+
+spectra_status spectra_decode_kv(const spectra_plan* kplan, const spectra_plan* vplan, const uint8_t* k_codes,
+                                 const uint8_t* v_codes, int64_t stream_stride_bytes, const float* k_norms,
+                                 const float* v_norms, int64_t norms_stride, int64_t T, void* k_out, void* v_out,
+                                 spectra_dtype out_dt, int64_t token_stride, spectra_stream_t stream)
+{
+    const spectra_plan* plans[2] = {kplan, vplan};
+    const uint8_t* cs[2] = {k_codes, v_codes};
+    const float* ns[2] = {k_norms, v_norms};
+    void* outs[2] = {k_out, v_out};
+    spectra_status st;
+    for (int i = 0; i < 2; ++i) {
+        if ((st = check_plan(plans[i], true))) return st;
+        if ((st = check_cache(outs[i], out_dt, T, token_stride, plans[i]->heads, plans[i]->head_dim))) return st;
+        if ((st = check_streams(plans[i], cs[i], stream_stride_bytes, T, plans[i]->heads))) return st;
+        if (plans[i]->basis == SPECTRA_BASIS_RWHT && T > 0) {
+            if (!ns[i] || (plans[i]->heads > 1 && norms_stride < T)) return SPECTRA_ERR_INVALID_ARG;
+        }
+    }
+    if (kplan->heads != vplan->heads || kplan->head_dim != vplan->head_dim) return SPECTRA_ERR_INVALID_ARG;
+    if (T == 0) return SPECTRA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (kernel_family() != SPECTRA_KERNELS_CUDA_CORE) {
+        bool done = false;
+        st = launch_decode_tc_kv(kplan, vplan, k_codes, v_codes, stream_stride_bytes, k_norms, v_norms,
+                                 norms_stride, T, k_out, v_out, out_dt, token_stride, s, &done);
+        if (st || done) return st;
+    }
+    if ((st = spectra_decode(kplan, k_codes, stream_stride_bytes, k_norms, norms_stride, T, k_out, out_dt,
+                             token_stride, stream)))
+        return st;
+    return spectra_decode(vplan, v_codes, stream_stride_bytes, v_norms, norms_stride, T, v_out, out_dt,
+                          token_stride, stream);
 }
 
 size_t spectra_attn_workspace_bytes(int B, int Hq, int head_dim, int64_t ctx)

@@ -187,8 +187,14 @@ constexpr int kEncEpiWarps = 16;
 constexpr int kEncThreads = 64 + 32 * kEncEpiWarps;   // producer, MMA, epilogue
 constexpr uint32_t kImgCol = 256;                 // TMEM column of the basis image
 
+// One launch encodes one or two segments (the K and V caches of a layer:
+// the same shapes, basis and quantizer, each with its own plan, input and
+// streams).  Work units are (segment, head) = seg * heads + h.
 struct EncParams {
-    PlanView pv;
+    PlanView pv;           // segment 0
+    PlanView pv2;          // segment 1 (nseg == 2)
+    int nseg;
+    int max_rec;           // widest record over the segments (shared-memory layout)
     int64_t T;
     int64_t g0;            // stream group of token 0 (an append at a 128-token boundary; 0 otherwise)
     int tiles_per_head;
@@ -198,6 +204,10 @@ struct EncParams {
     int64_t sstride;
     float* norms;
     int64_t nstride;
+    uint8_t* codes2;
+    int64_t sstride2;
+    float* norms2;
+    int64_t nstride2;
 };
 
 struct EncSmem {            // offsets into dynamic shared memory (1024-aligned base)
@@ -239,14 +249,15 @@ __host__ __device__ inline EncSmem enc_smem_layout(int stages, int max_rec_bits,
 // files (16 K each) then allow 96 registers a thread.
 template <bool LM, bool RWHT>
 __global__ void __launch_bounds__(kEncThreads, 1)
-encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
+encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x2,
+                 EncParams P)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr bool lm = LM;
     constexpr bool rwht = RWHT;
     constexpr int NT = RWHT ? 1 : 3;       // bf16 terms of the basis image
-    const EncSmem L = enc_smem_layout(P.stages, P.pv.max_rec_bits, lm);
+    const EncSmem L = enc_smem_layout(P.stages, P.max_rec, lm);
     uint8_t* xs = smem + L.xs;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* full = bars;                 // [stages <= 4]
@@ -262,7 +273,8 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     volatile int* drain_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Sched S = make_sched(P.pv.heads, P.tiles_per_head, P.contig != 0);
+    const int H = P.pv.heads;
+    const Sched S = make_sched(P.nseg * H, P.tiles_per_head, P.contig != 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P.stages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -305,8 +317,11 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
             auto issue = [&](const Item& t) {
                 mbar_arrive_expect_tx(&full[s], ESTAGE);
                 uint8_t* dst = xs + s * ESTAGE;
-                tma_load_3d(dst, &tmap_x, &full[s], 0, t.h, t.tile * ETILE);
-                tma_load_3d(dst + EKBLK, &tmap_x, &full[s], 64, t.h, t.tile * ETILE);
+                const bool s1 = t.h >= H;
+                const CUtensorMap* tm = s1 ? &tmap_x2 : &tmap_x;
+                const int hh = s1 ? t.h - H : t.h;
+                tma_load_3d(dst, tm, &full[s], 0, hh, t.tile * ETILE);
+                tma_load_3d(dst + EKBLK, tm, &full[s], 64, hh, t.tile * ETILE);
                 last_s = s;
                 last_ph = ph;
                 ++iss;
@@ -318,7 +333,8 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                     // every tile issued so far consumed: the stages are free
                     if (last_s >= 0 && !mbar_spin(&empty[last_s], last_ph, abort_flag, kWaitNs)) break;
                     mbar_arrive_expect_tx(imgsmem, NT * OPND);
-                    const uint8_t* src = P.pv.enc_img + size_t(it.h) * enc_img_bytes(D);
+                    const uint8_t* src = it.h >= H ? P.pv2.enc_img + size_t(it.h - H) * enc_img_bytes(D)
+                                                   : P.pv.enc_img + size_t(it.h) * enc_img_bytes(D);
                     for (int t = 0; t < NT; ++t) bulk_load(smem + L.img + t * OPND, src + t * OPND, OPND, imgsmem);
                     img_pending = true;
                     // with three stages the image passes through stages 1-2,
@@ -408,6 +424,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
         int bk_base = 0;
         bool head_ok = true;
         uint32_t* out = nullptr;
+        float* cur_norms = nullptr;            // RWHT: this unit's norms
         // the tile whose codes wait in shared memory for the bulk store
         uint32_t* p_out = nullptr;
         int p_R = 0, p_tile = 0;
@@ -454,7 +471,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
             ++ruse;
             const float n2 = part[lane] + part[32 + lane] + part[64 + lane] + part[96 + lane];
             const float nrm = sqrtf(n2 * (1.0f / float(D)));
-            if (q == 0 && head_ok && t0 + lane < P.T) P.norms[int64_t(cur_h) * P.nstride + 32 * P.g0 + t0 + lane] = nrm;
+            if (q == 0 && head_ok && t0 + lane < P.T) cur_norms[32 * P.g0 + t0 + lane] = nrm;
             invs[lane] = (nrm > 0.f) ? 1.f / nrm : 0.f;
             __syncwarp();
             // everyone has read part[] before it is written again
@@ -538,12 +555,16 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
             if (leader) flush((k - 1) & 1);
             if (h != cur_h) {
                 cur_h = h;
-                R = P.pv.rec_bits[h];
-                head_ok = R <= P.pv.max_rec_bits;
-                if (!head_ok && lane == 0) P.pv.status[h] = -SPECTRA_ERR_BUFFER;
-                b = P.pv.bits[size_t(h) * D + c];
-                o = P.pv.chan_off[size_t(h) * D + c];
-                const float qs = P.pv.qscale[size_t(h) * D + c];
+                const bool s1 = h >= H;                // segment of the unit
+                const int hh = s1 ? h - H : h;
+                const int32_t* rb = s1 ? P.pv2.rec_bits : P.pv.rec_bits;
+                int32_t* st = s1 ? P.pv2.status : P.pv.status;
+                R = rb[hh];
+                head_ok = R <= (s1 ? P.pv2.max_rec_bits : P.pv.max_rec_bits);
+                if (!head_ok && lane == 0) st[hh] = -SPECTRA_ERR_BUFFER;
+                b = (s1 ? P.pv2.bits : P.pv.bits)[size_t(hh) * D + c];
+                o = (s1 ? P.pv2.chan_off : P.pv.chan_off)[size_t(hh) * D + c];
+                const float qs = (s1 ? P.pv2.qscale : P.pv.qscale)[size_t(hh) * D + c];
                 // UNIFORM3S: qscale = 2^b / (6 sigma) -> qk = 1 / (6 sigma); LLOYD: 1 / sigma
                 qk = lm ? qs : qs / float(1 << b);
                 cl = float(1 << b) * (1.0f - 0x1p-22f);
@@ -554,7 +575,9 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
                     bk_sc = __int_as_float((127 + bk_log(bw)) << 23);                    // 2^p
                     bk_base = bk_off(bw) - __float_as_int(kMagic);
                 }
-                out = reinterpret_cast<uint32_t*>(P.codes + int64_t(h) * P.sstride) + P.g0 * R;
+                out = reinterpret_cast<uint32_t*>(s1 ? P.codes2 + int64_t(hh) * P.sstride2
+                                                      : P.codes + int64_t(hh) * P.sstride) + P.g0 * R;
+                if (rwht) cur_norms = s1 ? P.norms2 + int64_t(hh) * P.nstride2 : P.norms + int64_t(hh) * P.nstride;
             }
             uint32_t* cb = reinterpret_cast<uint32_t*>(smem + L.cb + (k & 1) * L.cbytes);
             const bool live = head_ok && R > 0;
@@ -609,7 +632,10 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
-        for (int kk = 0; kk < S.n; ++kk) P.pv.status[S.head_of(kk)] = -SPECTRA_ERR_TIMEOUT;
+        for (int kk = 0; kk < S.n; ++kk) {
+            const int u = S.head_of(kk);
+            (u >= H ? P.pv2.status : P.pv.status)[u >= H ? u - H : u] = -SPECTRA_ERR_TIMEOUT;
+        }
     }
     if (warp == 1) {
         tc_fence_after();
@@ -618,8 +644,12 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, EncParams P)
 }
 
 // ------------------------------------------------------------------ decode
+// Like the encode: one or two segments (a layer's K and V streams), work
+// units (segment, head) = seg * heads + h.
 struct DecParams {
-    PlanView pv;
+    PlanView pv;           // segment 0
+    PlanView pv2;          // segment 1 (nseg == 2)
+    int nseg;
     int64_t T;
     int tiles_per_head;
     int total;
@@ -633,6 +663,8 @@ struct DecParams {
     int64_t sstride;
     const float* norms;
     int64_t nstride;
+    const uint8_t* codes2;
+    const float* norms2;
 };
 
 struct DecSmem {
@@ -713,7 +745,8 @@ __device__ __forceinline__ float code_byte(const uint32_t (&X)[8], int t)
 
 template <bool LM>
 __global__ void __launch_bounds__(kDecThreads, 1)
-decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, const __grid_constant__ CUtensorMap tmap_out2,
+                 DecParams P)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -739,7 +772,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
     volatile int* drain_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Sched S = make_sched(P.pv.heads, P.tiles_per_head);
+    const int H = P.pv.heads;
+    const Sched S = make_sched(P.nseg * H, P.tiles_per_head);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P.cstages; ++s) { mbar_init(&cfull[s], 1); mbar_init(&cempty[s], kDecUnpackWarps); }
@@ -775,6 +809,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             int last_issued[4] = {-1, -1, -1, -1};
             int img_issued = 0, cs_i = 0;
             uint32_t cs_ph = 0;
+            const uint8_t* hcodes = nullptr;     // this unit's stream
             Item it = S.first();
             for (; k < S.n; ++k, S.next(it)) {
                 const int h = it.h, tile = it.tile;
@@ -782,15 +817,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                     if (j > 0 && !mbar_wait(imgempty, (j - 1) & 1, abort_flag, kWaitNs)) break;
                     const uint32_t bytes = P.nterms * OPND;
                     mbar_arrive_expect_tx(imgfull, bytes);
-                    const uint8_t* src = P.pv.dec_img + size_t(h) * dec_img_bytes(D);
+                    const bool s1 = h >= H;
+                    const int hh = s1 ? h - H : h;
+                    const uint8_t* src = (s1 ? P.pv2.dec_img : P.pv.dec_img) + size_t(hh) * dec_img_bytes(D);
                     for (uint32_t o = 0; o < bytes; o += 32768u) bulk_load(img + o, src + o, 32768u, imgfull);
                     img_issued = j + 1;
                     cur_h = h;
-                    R = P.pv.rec_bits[h];
-                    if (R > P.pv.max_rec_bits) {
-                        P.pv.status[h] = -SPECTRA_ERR_BUFFER;
+                    R = (s1 ? P.pv2.rec_bits : P.pv.rec_bits)[hh];
+                    if (R > (s1 ? P.pv2.max_rec_bits : P.pv.max_rec_bits)) {
+                        (s1 ? P.pv2.status : P.pv.status)[hh] = -SPECTRA_ERR_BUFFER;
                         R = 0;
                     }
+                    hcodes = s1 ? P.codes2 + int64_t(hh) * P.sstride : P.codes + int64_t(hh) * P.sstride;
                     ++j;
                 }
                 const int s = cs_i;
@@ -801,8 +839,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 const uint32_t bytes = uint32_t((ngroups * 4 * R + 15) / 16 * 16);
                 if (bytes > 0) {
                     mbar_arrive_expect_tx(&cfull[s], bytes);
-                    bulk_load(cs + s * P.cbytes, P.codes + int64_t(h) * P.sstride + (t0 / 32) * 4 * R, bytes,
-                              &cfull[s]);
+                    bulk_load(cs + s * P.cbytes, hcodes + (t0 / 32) * 4 * R, bytes, &cfull[s]);
                     last_issued[s] = k;
                 } else {
                     mbar_arrive(&cfull[s]);
@@ -880,16 +917,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             const int h = it.h, tile = it.tile;
             if (h != cur_h) {
                 cur_h = h;
-                R = P.pv.rec_bits[h];
-                if (R > P.pv.max_rec_bits) R = 0;
-                b0 = P.pv.bits[size_t(h) * D + c0];
-                b1 = P.pv.bits[size_t(h) * D + c0 + 1];
-                o0 = P.pv.chan_off[size_t(h) * D + c0];
-                o1 = P.pv.chan_off[size_t(h) * D + c0 + 1];
+                const bool s1 = h >= H;
+                const int hh = s1 ? h - H : h;
+                R = (s1 ? P.pv2.rec_bits : P.pv.rec_bits)[hh];
+                if (R > (s1 ? P.pv2.max_rec_bits : P.pv.max_rec_bits)) R = 0;
+                const uint8_t* bts = s1 ? P.pv2.bits : P.pv.bits;
+                const uint16_t* cof = s1 ? P.pv2.chan_off : P.pv.chan_off;
+                b0 = bts[size_t(hh) * D + c0];
+                b1 = bts[size_t(hh) * D + c0 + 1];
+                o0 = cof[size_t(hh) * D + c0];
+                o1 = cof[size_t(hh) * D + c0 + 1];
                 off0 = 1.0f - float(1 << b0);
                 off1 = 1.0f - float(1 << b1);
                 bmax = __reduce_max_sync(0xffffffffu, max(b0, b1));
-                code_mode = !lm && !rwht && P.pv.wmax[h] <= 7;
+                code_mode = !lm && !rwht && (s1 ? P.pv2.wmax : P.pv.wmax)[hh] <= 7;
             }
             const int sc = u_ci, sa = u_ai;
             if (!mbar_wait(&cfull[sc], u_cph, abort_flag, kWaitNs)) break;
@@ -962,8 +1003,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
         const int q = warp & 3;
         const bool leader = (warp == 2 + kDecUnpackWarps && lane == 0);
         float* bsh = reinterpret_cast<float*>(smem + L.bias) + (warp - 2 - kDecUnpackWarps) * D;
-        int k = 0, cur_h = -1;
-        bool code_mode = false;
+        int k = 0, cur_h = -1, hh = 0;
+        bool code_mode = false, s1 = false;   // s1: the unit's segment
         // all four epilogue warps (named barrier 1); the OR of the abort flag
         // makes every warp leave at the same point
         auto rendezvous = [&]() -> bool {
@@ -975,9 +1016,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             const int h = it.h, tile = it.tile;
             if (h != cur_h) {       // code mode: per-output offsets of this head
                 cur_h = h;
-                code_mode = !lm && !rwht && P.pv.wmax[h] <= 7;
+                s1 = h >= H;
+                hh = s1 ? h - H : h;
+                code_mode = !lm && !rwht && (s1 ? P.pv2.wmax : P.pv.wmax)[hh] <= 7;
+                const float* db = s1 ? P.pv2.dec_bias : P.pv.dec_bias;
                 __syncwarp();
-                for (int i = lane; i < D; i += 32) bsh[i] = code_mode ? P.pv.dec_bias[size_t(h) * D + i] : 0.f;
+                for (int i = lane; i < D; i += 32) bsh[i] = code_mode ? db[size_t(hh) * D + i] : 0.f;
                 __syncwarp();
             }
             const int a = k & 1;
@@ -985,7 +1029,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
             bool ok = true;
             const int64_t t = int64_t(tile) * TILE + q * 32 + lane;
             float scale = 1.f;
-            if (rwht) scale = (t < P.T) ? P.norms[int64_t(h) * P.nstride + t] * (1.0f / float(D)) : 0.f;
+            if (rwht) scale = (t < P.T) ? (s1 ? P.norms2 : P.norms)[int64_t(hh) * P.nstride + t] * (1.0f / float(D)) : 0.f;
             const uint32_t tm = tmem + a * 128 + (uint32_t(q * 32) << 16);
             const uint32_t row = uint32_t(q * 32 + lane);
             const int nrounds = P.out_f32 ? 2 : 1;
@@ -1048,12 +1092,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
                 fence_proxy_async_smem();
                 if (!(ok = rendezvous())) break;
                 if (leader) {
+                    const CUtensorMap* tmo = s1 ? &tmap_out2 : &tmap_out;
                     if (!P.out_f32) {
-                        tma_store_3d(&tmap_out, sb, 0, h, tile * TILE);
-                        tma_store_3d(&tmap_out, sb + KBLK, 64, h, tile * TILE);
+                        tma_store_3d(tmo, sb, 0, hh, tile * TILE);
+                        tma_store_3d(tmo, sb + KBLK, 64, hh, tile * TILE);
                     } else {
-                        tma_store_3d(&tmap_out, sb, 64 * rd, h, tile * TILE);
-                        tma_store_3d(&tmap_out, sb + KBLK, 64 * rd + 32, h, tile * TILE);
+                        tma_store_3d(tmo, sb, 64 * rd, hh, tile * TILE);
+                        tma_store_3d(tmo, sb + KBLK, 64 * rd + 32, hh, tile * TILE);
                     }
                     tma_store_commit();
                 }
@@ -1066,7 +1111,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, DecParams P)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
-        for (int kk = 0; kk < S.n; ++kk) P.pv.status[S.head_of(kk)] = -SPECTRA_ERR_TIMEOUT;
+        for (int kk = 0; kk < S.n; ++kk) {
+            const int u = S.head_of(kk);
+            (u >= H ? P.pv2.status : P.pv.status)[u >= H ? u - H : u] = -SPECTRA_ERR_TIMEOUT;
+        }
     }
     if (warp == 1) {
         tc_fence_after();
@@ -1229,36 +1277,56 @@ spectra_status launch_tc_images(const spectra_plan* plan, cudaStream_t s)
     return cuda_status(cudaGetLastError());
 }
 
-spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt, int64_t T, int64_t token_stride,
-                                uint8_t* codes, int64_t sstride, float* norms, int64_t nstride, cudaStream_t s,
-                                bool* done, int64_t g0)
+namespace {
+
+// One launch over nseg (1 or 2) segments; returns with *done false (nothing
+// launched) when the tensor-core path does not cover the call.
+spectra_status encode_tc_segs(const spectra_plan* const* plans, const void* const* xs, int nseg, int dt, int64_t T,
+                              int64_t token_stride, uint8_t* const* codes, const int64_t* sstride,
+                              float* const* norms, const int64_t* nstride, cudaStream_t s, bool* done, int64_t g0)
 {
     *done = false;
+    const spectra_plan* plan = plans[0];
     if (dt != SPECTRA_BF16 || plan->head_dim != D || T <= 0) return SPECTRA_OK;
     if (T > (int64_t(1) << 31) - ETILE) return SPECTRA_OK;
-    CUtensorMap m;
-    if (!make_cache_map(&m, x, false, plan->heads, T, token_stride, ETILE)) return SPECTRA_OK;
+    if (nseg == 2) {
+        const spectra_plan* p2 = plans[1];
+        if (p2->head_dim != D || p2->heads != plan->heads || p2->basis != plan->basis || p2->quant != plan->quant)
+            return SPECTRA_OK;
+    }
+    CUtensorMap m[2];
+    for (int i = 0; i < nseg; ++i)
+        if (!make_cache_map(&m[i], xs[i], false, plan->heads, T, token_stride, ETILE)) return SPECTRA_OK;
+    if (nseg == 1) m[1] = m[0];
     EncParams P;
     P.pv = make_view(plan);
+    P.pv2 = nseg == 2 ? make_view(plans[1]) : P.pv;
+    P.nseg = nseg;
+    P.max_rec = std::max(plan->max_rec_bits, nseg == 2 ? plans[1]->max_rec_bits : 0);
     P.T = T;
     P.g0 = g0;
     P.tiles_per_head = int((T + ETILE - 1) / ETILE);
-    const int64_t total = int64_t(P.tiles_per_head) * plan->heads;
+    const int units = nseg * plan->heads;
+    const int64_t total = int64_t(P.tiles_per_head) * units;
     if (total > (int64_t(1) << 31) - 1) return SPECTRA_OK;
     const bool lm = plan->quant == SPECTRA_Q_LLOYD_GAUSS;
     P.stages = 4;
-    while (P.stages > 2 && enc_smem_layout(P.stages, plan->max_rec_bits, lm).total + 1024 > kSmemMax) --P.stages;
-    if (enc_smem_layout(P.stages, plan->max_rec_bits, lm).total + 1024 > kSmemMax) return SPECTRA_OK;
-    P.codes = codes;
-    P.sstride = sstride;
-    P.norms = norms;
-    P.nstride = nstride;
+    while (P.stages > 2 && enc_smem_layout(P.stages, P.max_rec, lm).total + 1024 > kSmemMax) --P.stages;
+    if (enc_smem_layout(P.stages, P.max_rec, lm).total + 1024 > kSmemMax) return SPECTRA_OK;
+    P.codes = codes[0];
+    P.sstride = sstride[0];
+    P.norms = norms[0];
+    P.nstride = nstride[0];
+    P.codes2 = codes[nseg - 1];
+    P.sstride2 = sstride[nseg - 1];
+    P.norms2 = norms[nseg - 1];
+    P.nstride2 = nstride[nseg - 1];
     // interleaved schedule unless contiguous ranges give every CTA fewer tiles
     const int sms = sm_count();
-    int grid = sched_grid(sms, plan->heads, P.tiles_per_head);
+    int grid = sched_grid(sms, units, P.tiles_per_head);
     P.contig = 0;
-    if (plan->heads <= sms) {
-        const int cph = grid / plan->heads;
+    if (units <= sms) {
+        const int cph = grid / units;
         const int64_t inter_max = (P.tiles_per_head + cph - 1) / cph;
         const int64_t g2 = std::min<int64_t>(sms, total);
         const int64_t contig_max = (total + g2 - 1) / g2;
@@ -1267,36 +1335,75 @@ spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt,
             grid = int(g2);
         }
     }
-    const uint32_t sm = enc_smem_layout(P.stages, plan->max_rec_bits, lm).total + 1024;
+    const uint32_t sm = enc_smem_layout(P.stages, P.max_rec, lm).total + 1024;
     const bool rw = plan->basis == SPECTRA_BASIS_RWHT;
     auto kern = lm ? (rw ? encode_tc_kernel<true, true> : encode_tc_kernel<true, false>)
                    : (rw ? encode_tc_kernel<false, true> : encode_tc_kernel<false, false>);
     if (spectra_status st = set_smem(kern, sm)) return st;
-    if (cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kEncThreads), sm, s, m, P)) return cuda_status(e);
+    if (cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kEncThreads), sm, s, m[0], m[1], P)) return cuda_status(e);
     *done = true;
     return cuda_status(cudaGetLastError());
 }
 
-spectra_status launch_decode_tc(const spectra_plan* plan, const uint8_t* codes, int64_t sstride, const float* norms,
-                                int64_t nstride, int64_t T, void* x_out, int out_dt, int64_t token_stride,
-                                cudaStream_t s, bool* done)
+}  // namespace
+
+spectra_status launch_encode_tc(const spectra_plan* plan, const void* x, int dt, int64_t T, int64_t token_stride,
+                                uint8_t* codes, int64_t sstride, float* norms, int64_t nstride, cudaStream_t s,
+                                bool* done, int64_t g0)
+{
+    return encode_tc_segs(&plan, &x, 1, dt, T, token_stride, &codes, &sstride, &norms, &nstride, s, done, g0);
+}
+
+spectra_status launch_encode_tc_kv(const spectra_plan* kplan, const spectra_plan* vplan, const void* k,
+                                   const void* v, int dt, int64_t T, int64_t token_stride, uint8_t* k_codes,
+                                   uint8_t* v_codes, int64_t sstride, float* k_norms, float* v_norms,
+                                   int64_t nstride, cudaStream_t s, bool* done)
+{
+    const spectra_plan* plans[2] = {kplan, vplan};
+    const void* xs[2] = {k, v};
+    uint8_t* cs[2] = {k_codes, v_codes};
+    const int64_t ss[2] = {sstride, sstride};
+    float* ns[2] = {k_norms, v_norms};
+    const int64_t nss[2] = {nstride, nstride};
+    return encode_tc_segs(plans, xs, 2, dt, T, token_stride, cs, ss, ns, nss, s, done, 0);
+}
+
+namespace {
+
+// One launch over nseg (1 or 2) segments; *done false when the tensor-core
+// path does not cover the call.
+spectra_status decode_tc_segs(const spectra_plan* const* plans, const uint8_t* const* codes, int nseg,
+                              int64_t sstride, const float* const* norms, int64_t nstride, int64_t T,
+                              void* const* outs, int out_dt, int64_t token_stride, cudaStream_t s, bool* done)
 {
     *done = false;
+    const spectra_plan* plan = plans[0];
     if (plan->head_dim != D || T <= 0) return SPECTRA_OK;
     if (T > (int64_t(1) << 31) - TILE) return SPECTRA_OK;
+    if (nseg == 2) {
+        const spectra_plan* p2 = plans[1];
+        if (p2->head_dim != D || p2->heads != plan->heads || p2->basis != plan->basis || p2->quant != plan->quant)
+            return SPECTRA_OK;
+    }
     const bool f32 = out_dt == SPECTRA_F32;
-    CUtensorMap m;
-    if (!make_cache_map(&m, x_out, f32, plan->heads, T, token_stride)) return SPECTRA_OK;
+    CUtensorMap m[2];
+    for (int i = 0; i < nseg; ++i)
+        if (!make_cache_map(&m[i], outs[i], f32, plan->heads, T, token_stride)) return SPECTRA_OK;
+    if (nseg == 1) m[1] = m[0];
     DecParams P;
     P.pv = make_view(plan);
+    P.pv2 = nseg == 2 ? make_view(plans[1]) : P.pv;
+    P.nseg = nseg;
     P.T = T;
     P.tiles_per_head = int((T + TILE - 1) / TILE);
-    if (int64_t(P.tiles_per_head) * plan->heads > (int64_t(1) << 31) - 1) return SPECTRA_OK;
-    P.total = P.tiles_per_head * plan->heads;
+    const int units = nseg * plan->heads;
+    if (int64_t(P.tiles_per_head) * units > (int64_t(1) << 31) - 1) return SPECTRA_OK;
+    P.total = P.tiles_per_head * units;
     const bool lm = plan->quant == SPECTRA_Q_LLOYD_GAUSS;
     P.nterms = plan->basis == SPECTRA_BASIS_RWHT ? 1 : 2;
     P.na = lm ? 2 : 1;
-    P.cbytes = uint32_t(16 * ((plan->max_rec_bits > 0) ? plan->max_rec_bits : 1));
+    const int max_rec = std::max(plan->max_rec_bits, nseg == 2 ? plans[1]->max_rec_bits : 0);
+    P.cbytes = uint32_t(16 * (max_rec > 0 ? max_rec : 1));
     P.astages = 2;
     P.cstages = 3;
     auto total = [&] { return dec_smem_layout(P.nterms, P.na, P.astages, P.cstages, P.cbytes, lm).total + 1024; };
@@ -1304,17 +1411,41 @@ spectra_status launch_decode_tc(const spectra_plan* plan, const uint8_t* codes, 
     while (total() > kSmemMax && P.astages > 1) --P.astages;
     if (total() > kSmemMax) return SPECTRA_OK;
     P.out_f32 = f32 ? 1 : 0;
-    P.codes = codes;
+    P.codes = codes[0];
     P.sstride = sstride;
-    P.norms = norms;
+    P.norms = norms[0];
     P.nstride = nstride;
+    P.codes2 = codes[nseg - 1];
+    P.norms2 = norms[nseg - 1];
     const uint32_t sm = total();
     auto kern = lm ? decode_tc_kernel<true> : decode_tc_kernel<false>;
     if (spectra_status st = set_smem(kern, sm)) return st;
-    const int grid = sched_grid(sm_count(), plan->heads, P.tiles_per_head);
-    if (cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kDecThreads), sm, s, m, P)) return cuda_status(e);
+    const int grid = sched_grid(sm_count(), units, P.tiles_per_head);
+    if (cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kDecThreads), sm, s, m[0], m[1], P))
+        return cuda_status(e);
     *done = true;
     return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+spectra_status launch_decode_tc(const spectra_plan* plan, const uint8_t* codes, int64_t sstride, const float* norms,
+                                int64_t nstride, int64_t T, void* x_out, int out_dt, int64_t token_stride,
+                                cudaStream_t s, bool* done)
+{
+    return decode_tc_segs(&plan, &codes, 1, sstride, &norms, nstride, T, &x_out, out_dt, token_stride, s, done);
+}
+
+spectra_status launch_decode_tc_kv(const spectra_plan* kplan, const spectra_plan* vplan, const uint8_t* k_codes,
+                                   const uint8_t* v_codes, int64_t sstride, const float* k_norms,
+                                   const float* v_norms, int64_t nstride, int64_t T, void* k_out, void* v_out,
+                                   int out_dt, int64_t token_stride, cudaStream_t s, bool* done)
+{
+    const spectra_plan* plans[2] = {kplan, vplan};
+    const uint8_t* cs[2] = {k_codes, v_codes};
+    const float* ns[2] = {k_norms, v_norms};
+    void* outs[2] = {k_out, v_out};
+    return decode_tc_segs(plans, cs, 2, sstride, ns, nstride, T, outs, out_dt, token_stride, s, done);
 }
 
 }  // namespace spectra

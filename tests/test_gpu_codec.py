@@ -216,6 +216,58 @@ def test_codec_ragged_lengths(spx, orc, path, T):
     _check_codec(spx, orc, oplan, x64, xd, T)
 
 
+@pytest.mark.parametrize("kind", ["uniform", "lloyd", "rwht", "mixed"])
+def test_encode_decode_kv_matches_oracle(spx, orc, path, kind):
+    """spectra_encode_kv / spectra_decode_kv (K and V of a layer in one call; one launch on the
+    tensor-core family when both plans share basis and quantizer, two
+    otherwise -- "mixed" pairs a uniform K plan with a Lloyd-Max V plan):
+    each half's codes against the oracle under the band rule, and byte for
+    byte against two spectra_encode calls."""
+    T, H = 1000, 3
+    xk, kd, k64 = llama_case(T=T, H=H, seed=11, role=synth.ROLE_K)
+    xv, vd, v64 = llama_case(T=T, H=H, seed=11, role=synth.ROLE_V)
+    if kind == "rwht":
+        kpl = orc.make_rwht_plan(synth.rwht_signs(11, H, 128), 3)
+        vpl = orc.make_rwht_plan(synth.rwht_signs(12, H, 128), 3)
+    else:
+        kpl = orc.make_eigen_plan(k64[:512], 2.0, 1 if kind == "lloyd" else 0)
+        vpl = orc.make_eigen_plan(v64[:512], 1.33, 0 if kind == "uniform" else 1)
+    kp, vp = gpu_plan(spx, kpl), gpu_plan(spx, vpl)
+    sb = max(kp.stream_bytes(T), vp.stream_bytes(T), 16)
+    kc, vc, kc1, vc1 = (torch.zeros((H, sb), dtype=torch.uint8, device="cuda") for _ in range(4))
+    rw = kind == "rwht"
+    kn, vn, kn1, vn1 = ((torch.zeros((H, T), device="cuda") if rw else None) for _ in range(4))
+    spx.spectra_encode_kv(kp, vp, kd, vd, kc, vc, k_norms=kn, v_norms=vn)
+    spx.spectra_encode(kp, kd, kc1, norms=kn1)
+    spx.spectra_encode(vp, vd, vc1, norms=vn1)
+    torch.cuda.synchronize()
+    assert torch.equal(kc, kc1) and torch.equal(vc, vc1)
+    if rw:
+        assert torch.equal(kn, kn1) and torch.equal(vn, vn1)
+    # decode_kv of the same streams: equal to two spectra_decode calls, and to
+    # the oracle's reconstruction within the decode bar
+    for dt in (torch.float32, torch.bfloat16):
+        ko, vo, ko1, vo1 = (torch.zeros((T, H, 128), device="cuda", dtype=dt) for _ in range(4))
+        spx.spectra_decode_kv(kp, vp, kc, vc, T, ko, vo, k_norms=kn, v_norms=vn)
+        spx.spectra_decode(kp, kc, T, ko1, norms=kn)
+        spx.spectra_decode(vp, vc, T, vo1, norms=vn)
+        torch.cuda.synchronize()
+        assert torch.equal(ko, ko1) and torch.equal(vo, vo1)
+    for opl, out, codes, nrm in ((kpl, ko, kc, kn), (vpl, vo, vc, vn)):
+        streams = [codes[h].cpu().numpy() for h in range(H)]
+        want = orc.decode(opl, streams, T, None if nrm is None else [nrm[h].cpu().numpy() for h in range(H)])
+        assert rel_l2(out.float().cpu().numpy(), bf16(want).float().numpy()) <= REC_TOL
+    for opl, x64, codes, nrm in ((kpl, k64, kc, kn), (vpl, v64, vc, vn)):
+        encs = orc.encode(opl, x64)
+        flips = total = 0
+        for h in range(H):
+            f, n = compare_codes(orc, opl, h, encs[h], codes[h].cpu().numpy(), T)
+            flips, total = flips + f, total + n
+            if rw:
+                np.testing.assert_allclose(nrm[h].cpu().numpy(), encs[h]["norms"], rtol=1e-5)
+        assert flips <= FLIP_FRAC * max(total, 1), (flips, total)
+
+
 def test_codec_empty(spx, orc, path):
     x, xd, x64 = llama_case(T=64, H=2)
     oplan = orc.make_eigen_plan(x64, 2.0)
