@@ -650,6 +650,7 @@ struct DecParams {
     PlanView pv;           // segment 0
     PlanView pv2;          // segment 1 (nseg == 2)
     int nseg;
+    int contig;            // contiguous work ranges (else interleaved)
     int64_t T;
     int tiles_per_head;
     int total;
@@ -773,7 +774,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, const __grid_cons
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = P.pv.heads;
-    const Sched S = make_sched(P.nseg * H, P.tiles_per_head);
+    const Sched S = make_sched(P.nseg * H, P.tiles_per_head, P.contig != 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P.cstages; ++s) { mbar_init(&cfull[s], 1); mbar_init(&cempty[s], kDecUnpackWarps); }
@@ -1043,16 +1044,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, const __grid_cons
                 uint8_t* sb = stg + slot * OPND;
                 const uint32_t sba = smem_u32(sb);
                 if (!P.out_f32) {
-#pragma unroll 1
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t r[32];
-                        tmem_ld32(tm + 32 * j, r);
-                        tmem_ld_wait();
-                        if (j == 3) {   // accumulator read: the MMA may reuse it
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&accempty[a]);
-                        }
+                    // 32 columns at a time; the load of the next 32 is in flight
+                    // while these are converted (one wait covers both loads)
+                    auto convert = [&](const uint32_t (&r)[32], int j) {
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4) {
                             uint32_t pk[4];
@@ -1066,7 +1060,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, const __grid_cons
                             const uint32_t off = (j >> 1) * KBLK + sw128_offset(row, (j & 1) * 64 + c4 * 16);
                             st_shared_v4(sba + off, pk[0], pk[1], pk[2], pk[3]);
                         }
-                    }
+                    };
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32(tm, ra);
+                    tmem_ld_wait();
+                    tmem_ld32(tm + 32, rb);
+                    convert(ra, 0);
+                    tmem_ld_wait();
+                    tmem_ld32(tm + 64, ra);
+                    convert(rb, 1);
+                    tmem_ld_wait();
+                    tmem_ld32(tm + 96, rb);
+                    convert(ra, 2);
+                    tmem_ld_wait();
+                    // accumulator read: the MMA may reuse it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&accempty[a]);
+                    convert(rb, 3);
                 } else {
 #pragma unroll 1
                     for (int j = 0; j < 2; ++j) {
@@ -1420,7 +1431,20 @@ spectra_status decode_tc_segs(const spectra_plan* const* plans, const uint8_t* c
     const uint32_t sm = total();
     auto kern = lm ? decode_tc_kernel<true> : decode_tc_kernel<false>;
     if (spectra_status st = set_smem(kern, sm)) return st;
-    const int grid = sched_grid(sm_count(), units, P.tiles_per_head);
+    // interleaved schedule unless contiguous ranges give every CTA fewer tiles
+    const int sms = sm_count();
+    int grid = sched_grid(sms, units, P.tiles_per_head);
+    P.contig = 0;
+    if (units <= sms) {
+        const int cph = grid / units;
+        const int64_t inter_max = (P.tiles_per_head + cph - 1) / cph;
+        const int64_t g2 = std::min<int64_t>(sms, P.total);
+        const int64_t contig_max = (P.total + g2 - 1) / g2;
+        if (contig_max < inter_max) {
+            P.contig = 1;
+            grid = int(g2);
+        }
+    }
     if (cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kDecThreads), sm, s, m[0], m[1], P))
         return cuda_status(e);
     *done = true;
