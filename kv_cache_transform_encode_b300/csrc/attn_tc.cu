@@ -187,8 +187,10 @@ __host__ __device__ inline TcSmem tc_smem_layout(int stages, uint32_t kst, uint3
 // MTV: V m-tiles per warp (ceil(R_V / 128)).  A record with an even number
 // of words starts every group's words 8-byte aligned in shared memory (64-bit
 // loads); odd records take 32-bit loads.
+// Records up to 256 V planes (MTV <= 2) run three CTAs per SM (24 warps hide
+// the latency of the shared-memory loads and MMAs), wider ones two.
 template <int MTV>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, MTV <= 2 ? 3 : 2)
 attn_tc_split_kernel(AttnTcParams P)
 {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -579,13 +581,15 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
     const int nkb = max((RKm + 15) / 16, 1);
     // V-side partial sums reuse the stages: kGmax x R_V floats must fit
     auto total = [&](int st) { return tc_smem_layout(st, P.kst, P.vst, nkb).total; };
+    const int mtv = (((RVm + 15) / 16) + kWarps - 1) / kWarps;
+    // stages that let the kernel's CTAs per SM fit (228 KB per SM, 1 KB of it per CTA reserved)
+    const uint32_t fit = mtv <= 2 ? 75 * 1024 : 113 * 1024;
     int st = kMaxStages;
-    while (st > 2 && total(st) > 113 * 1024) --st;
+    while (st > 2 && total(st) > fit) --st;
     if (total(st) > 227 * 1024) return SPECTRA_OK;
     if (size_t(st) * (P.kst + P.vst) < sizeof(float) * kGmax * size_t(RVm)) return SPECTRA_OK;
     P.stages = st;
     const size_t sm = total(st);
-    const int mtv = (((RVm + 15) / 16) + kWarps - 1) / kWarps;
     if (spectra_status e = set_smem(attn_tc_prep_kernel, sizeof(float) * D * D)) return e;
     attn_tc_prep_kernel<<<B * Hkv, kGmax * D, sizeof(float) * D * D, s>>>(P.kp, q, q_dt, Hq, G, scale, img, bias);
     if (spectra_status e = cuda_status(cudaGetLastError())) return e;
