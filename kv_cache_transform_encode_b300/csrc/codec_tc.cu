@@ -644,6 +644,10 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
 }
 
 // ------------------------------------------------------------------ decode
+constexpr int kDecUnpackWarps = 8;
+constexpr int kDecEpiWarps = 8;   // two per TMEM lane quadrant, one column half each
+constexpr int kDecThreads = 32 * (2 + kDecUnpackWarps + kDecEpiWarps);
+
 // Like the encode: one or two segments (a layer's K and V streams), work
 // units (segment, head) = seg * heads + h.
 struct DecParams {
@@ -683,7 +687,7 @@ __host__ __device__ inline DecSmem dec_smem_layout(int nterms, int na, int astag
     L.cs = o;   o += cstages * cbytes;
     o = (o + 15) & ~15u;
     L.lv = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
-    L.bias = o; o += 4 * D * 4;                   // per epilogue warp: output offsets of the head
+    L.bias = o; o += kDecEpiWarps * D * 4;        // per epilogue warp: output offsets of the head
     L.bars = o; o += 256;
     L.total = o;
     return L;
@@ -706,9 +710,6 @@ __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-constexpr int kDecUnpackWarps = 8;
-constexpr int kDecEpiWarps = 4;
-constexpr int kDecThreads = 32 * (2 + kDecUnpackWarps + kDecEpiWarps);
 
 // Unpack one channel's codes of a 32-token group: planes -> code bytes.
 // X[2m], X[2m+1] hold the codes of tokens 8m .. 8m+7, one per byte.
@@ -1001,12 +1002,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, const __grid_cons
         }
     } else {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;
+        // warp e = warp - 2 - unpack warps: TMEM lane quadrant q = warp & 3
+        // (tokens 32q ..), column half ch = e / 4 (outputs 64 ch ..)
+        const int q = warp & 3, ch = (warp - 2 - kDecUnpackWarps) >> 2;
         const bool leader = (warp == 2 + kDecUnpackWarps && lane == 0);
         float* bsh = reinterpret_cast<float*>(smem + L.bias) + (warp - 2 - kDecUnpackWarps) * D;
         int k = 0, cur_h = -1, hh = 0;
         bool code_mode = false, s1 = false;   // s1: the unit's segment
-        // all four epilogue warps (named barrier 1); the OR of the abort flag
+        // all the epilogue warps (named barrier 1); the OR of the abort flag
         // makes every warp leave at the same point
         auto rendezvous = [&]() -> bool {
             __syncwarp();
@@ -1062,25 +1065,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, const __grid_cons
                         }
                     };
                     uint32_t ra[32], rb[32];
-                    tmem_ld32(tm, ra);
+                    tmem_ld32(tm + 64 * ch, ra);
                     tmem_ld_wait();
-                    tmem_ld32(tm + 32, rb);
-                    convert(ra, 0);
-                    tmem_ld_wait();
-                    tmem_ld32(tm + 64, ra);
-                    convert(rb, 1);
-                    tmem_ld_wait();
-                    tmem_ld32(tm + 96, rb);
-                    convert(ra, 2);
+                    tmem_ld32(tm + 64 * ch + 32, rb);
+                    convert(ra, 2 * ch);
                     tmem_ld_wait();
                     // accumulator read: the MMA may reuse it
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&accempty[a]);
-                    convert(rb, 3);
+                    convert(rb, 2 * ch + 1);
                 } else {
-#pragma unroll 1
-                    for (int j = 0; j < 2; ++j) {
+                    {
+                        const int j = ch;
                         uint32_t r[32];
                         tmem_ld32(tm + 64 * rd + 32 * j, r);
                         tmem_ld_wait();
