@@ -672,6 +672,10 @@ struct DecParams {
     const float* norms2;
 };
 
+// Lloyd-Max levels in shared memory: one row per width, 257 floats apart, so
+// lanes of different widths reading the same code hit different banks
+constexpr int kLvStride = kLmStride + 1;
+
 struct DecSmem {
     uint32_t img, as, cs, stg, lv, bias, bars, total;
 };
@@ -686,7 +690,7 @@ __host__ __device__ inline DecSmem dec_smem_layout(int nterms, int na, int astag
     L.stg = o;  o += 2 * OPND;
     L.cs = o;   o += cstages * cbytes;
     o = (o + 15) & ~15u;
-    L.lv = o;   o += lm ? kMaxBits * kLmStride * 4 : 0;
+    L.lv = o;   o += lm ? kMaxBits * kLvStride * 4 : 0;
     L.bias = o; o += kDecEpiWarps * D * 4;        // per epilogue warp: output offsets of the head
     L.bars = o; o += 256;
     L.total = o;
@@ -737,6 +741,12 @@ __device__ __forceinline__ void unpack_narrow(const uint32_t* words, int o, int 
         const uint32_t s1 = (((w1 >> (4 * m)) & 0xFu) * 0x00204081u) & 0x01010101u;
         X[m] = s0 | (s1 << 1);
     }
+}
+
+// byte t of the 32 codes in X as an integer
+__device__ __forceinline__ int code_int(const uint32_t (&X)[8], int t)
+{
+    return int(__byte_perm(X[t >> 2], 0u, 0x4440u | uint32_t(t & 3)));
 }
 
 // byte i of the 32 codes in X as a float (exact): M + code - M
@@ -797,7 +807,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, const __grid_cons
     pdl_wait();
     if (lm) {
         float* lv = reinterpret_cast<float*>(smem + L.lv);
-        for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) lv[e] = P.pv.lm_level[e];
+        // each level as its bf16 pair (hi = RN(level), lo = RN(level - hi)) in one word
+        uint32_t* lvp = reinterpret_cast<uint32_t*>(lv);
+        for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) {
+            const float v = P.pv.lm_level[e];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+            lvp[(e / kLmStride) * kLvStride + e % kLmStride] =
+                uint32_t(__bfloat16_as_ushort(hi)) | (uint32_t(__bfloat16_as_ushort(lo)) << 16);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -951,8 +969,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, const __grid_cons
                     unpack_channel(words, o1, b1, bmax, X1);
                 }
                 const uint32_t abase = smem_u32(as + sa * P.na * OPND) + hc * KBLK;
-                const float* lv0 = lv + (b0 > 0 ? (b0 - 1) * kLmStride : 0);
-                const float* lv1 = lv + (b1 > 0 ? (b1 - 1) * kLmStride : 0);
+                const uint32_t* lv0 = reinterpret_cast<const uint32_t*>(lv) + (b0 > 0 ? (b0 - 1) * kLvStride : 0);
+                const uint32_t* lv1 = reinterpret_cast<const uint32_t*>(lv) + (b1 > 0 ? (b1 - 1) * kLvStride : 0);
                 if (code_mode) {
                     // (c0, c0+1) of token t as bf16 (128 + code): byte permutes only.
                     // Row r = 32 gi + t; its swizzled chunk depends on r & 7 = t & 7.
@@ -977,19 +995,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_out, const __grid_cons
                     const uint32_t row = uint32_t(gi * 32 + t);
                     const uint32_t addr = abase + row * 128u + ((uint32_t(lane >> 2) ^ (row & 7u)) << 4) +
                                           4u * uint32_t(lane & 3);
-                    const float k0 = code_byte(X0, t), k1 = code_byte(X1, t);
                     if (!lm) {
+                        const float k0 = code_byte(X0, t), k1 = code_byte(X1, t);
                         // 2 code + 1 - 2^b (odd integer, exact in bf16); 0 for dropped channels
                         const float v0 = b0 ? fmaf(k0, 2.f, off0) : 0.f;
                         const float v1 = b1 ? fmaf(k1, 2.f, off1) : 0.f;
                         st_shared_u32(addr, pack_bf16x2(v0, v1));
                     } else {
-                        const float v0 = b0 ? lv0[int(k0)] : 0.f;
-                        const float v1 = b1 ? lv1[int(k1)] : 0.f;
-                        const uint32_t hv = pack_bf16x2(v0, v1);
-                        const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hv);
-                        st_shared_u32(addr, hv);
-                        st_shared_u32(addr + OPND, pack_bf16x2(v0 - __low2float(hb), v1 - __high2float(hb)));
+                        // the levels' (hi, lo) pairs of channels c0, c0 + 1 -> the hi and lo tiles
+                        const uint32_t e0 = b0 ? lv0[code_int(X0, t)] : 0u;
+                        const uint32_t e1 = b1 ? lv1[code_int(X1, t)] : 0u;
+                        st_shared_u32(addr, __byte_perm(e0, e1, 0x5410));
+                        st_shared_u32(addr + OPND, __byte_perm(e0, e1, 0x7632));
                     }
                 }
             }
