@@ -69,93 +69,114 @@ __global__ void attn_qrot_kernel(PlanView kp, const void* __restrict__ q, int q_
     }
 }
 
-struct Side {            // per-plan tables staged in shared memory
-    int* bits;
-    int* off;
-    float* rsc;
-    uint32_t* words;     // [2][R]
-};
-
+// Split-context attention on CUDA cores (every plan the tensor-core kernel
+// does not cover: Lloyd-Max and RWHT plans, head_dim 64, the QJL
+// correction).  One block of 256 threads per (split, kv head, batch); per
+// 64-token tile (two bit-plane groups):
+//  * unpack: a thread per (group, channel) turns its b plane words into the
+//    32 tokens' dequantized latent values y[t][c];
+//  * scores: four threads per token, each over a quarter of the channels
+//    (c = 4 i + quarter) for all GM query heads at once, reduced by shuffles;
+//  * the QJL correction (optional) the same way over the tile's sign bits;
+//  * P V: a thread per (channel, token subset) for all GM heads at once.
+// Rows of y are D + 4 floats apart (4 mod 32 words): the score reads of a
+// warp (8 tokens x 4 quarters) and the unpack / P V accesses (consecutive
+// channels) are all free of bank conflicts.  K, the signs and V take turns
+// in the one y buffer.
 template <int D>
-__device__ void unpack_tile(const PlanView& pv, const Side& sd, int h, int R, const uint32_t* stream,
-                            const float* norms, int64_t t0, int64_t tend, float* y, const float* lv)
+constexpr int ystride() { return D + 4; }
+constexpr int kLvs = kLmStride + 1;   // level-table rows 257 floats apart (lanes of different widths)
+
+template <int D, int GM>
+size_t split_smem_t()
 {
-    constexpr int LD = D + 1;
-    // stage the two groups' words
-    const int64_t g0 = t0 / kGroup;
-    for (int e = threadIdx.x; e < 2 * R; e += blockDim.x) {
-        const int64_t gg = g0 + e / R;
-        sd.words[e] = (gg * kGroup < tend) ? stream[gg * R + (e % R)] : 0u;
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < kTile * D; e += blockDim.x) {
-        const int t = e / D, c = e % D;
-        const int b = sd.bits[c];
-        float v = 0.f;
-        if (b > 0 && t0 + t < tend) {
-            const uint32_t* w = sd.words + (t >> 5) * R + sd.off[c];
-            int code = 0;
-            for (int k = 0; k < b; ++k) code |= int((w[k] >> (t & 31)) & 1u) << k;
-            if (pv.quant == SPECTRA_Q_UNIFORM3S)
-                v = sd.rsc[c] * (float(code) + 0.5f - float(1 << (b - 1)));
-            else {
-                const float s = (pv.basis == SPECTRA_BASIS_RWHT)
-                                    ? norms[t0 + t] * rsqrtf(float(D)) : sd.rsc[c];
-                v = s * lv[(b - 1) * kLmStride + code];
-            }
-        }
-        y[t * LD + c] = v;
-    }
-    __syncthreads();
+    return sizeof(float) * (size_t(2) * D * GM + size_t(kTile) * ystride<D>() + kTile * GM + 3 * GM +
+                            kMaxBits * kLvs + 2 * kTile + D) +
+           sizeof(int) * 2 * D + sizeof(uint32_t) * 2 * 8 * D;
 }
 
+// the 32 tokens of group g (stream group g0 + g) of channel c into y[32 g + t][c]
 template <int D>
+__device__ __forceinline__ void unpack_channel_group(const PlanView& pv, int c, int g, int R, const uint32_t* words,
+                                                     const int* bits, const int* off, const float* rsc,
+                                                     const float* lv, const float* nrm, int ntok, float* y)
+{
+    constexpr int LD = ystride<D>();
+    const int b = bits[c];
+    float* yc = y + (32 * g) * LD + c;
+    if (b == 0) {
+#pragma unroll 4
+        for (int t = 0; t < 32; ++t) yc[t * LD] = 0.f;
+        return;
+    }
+    // the 32 codes as bytes: gather each plane's byte m, then 8 x 8 bit
+    // transposes -- X[j] holds the codes of tokens 4 j .. 4 j + 3
+    uint32_t pl[kMaxBits];
+    const uint32_t* wp = words + g * R + off[c];
+#pragma unroll
+    for (int k = 0; k < kMaxBits; ++k) pl[k] = k < b ? wp[k] : 0u;
+    uint32_t X[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        X[2 * m] = gather_byte(pl[0], pl[1], pl[2], pl[3], m);
+        X[2 * m + 1] = gather_byte(pl[4], pl[5], pl[6], pl[7], m);
+        transpose8(X[2 * m], X[2 * m + 1]);
+    }
+    const bool uni = pv.quant == SPECTRA_Q_UNIFORM3S;
+    const bool rw = pv.basis == SPECTRA_BASIS_RWHT;
+    const float sc = rsc[c], mid = 0.5f - float(1 << (b - 1));
+    const float* lvb = lv + (b - 1) * kLvs;
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+        const int code = int(__byte_perm(X[t >> 2], 0u, 0x4440u | uint32_t(t & 3)));
+        float v;
+        if (uni) v = sc * (float(code) + mid);
+        else v = (rw ? nrm[32 * g + t] : sc) * lvb[code];
+        yc[t * LD] = (32 * g + t < ntok) ? v : 0.f;
+    }
+}
+
+template <int D, int GM>
 __global__ void __launch_bounds__(kThreads)
 attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq, int64_t ctx,
                   const uint8_t* __restrict__ kc, const uint8_t* __restrict__ vc, int64_t sstride,
                   const float* __restrict__ kn, const float* __restrict__ vn, int64_t nstride,
                   int nsplit, int split_len, float* __restrict__ part, QjlArgs qj)
 {
-    constexpr int LD = D + 1;
-    extern __shared__ float smem[];
+    constexpr int LD = ystride<D>();
+    extern __shared__ __align__(16) float smem[];
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int Hkv = kp.heads, G = Hq / Hkv;
     const int RK = kp.rec_bits[h], RV = vp.rec_bits[h];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    float* qs = smem;                       // [G][D]
-    float* yk = qs + kMaxGroup * D;         // [kTile][LD]
-    float* yv = yk + kTile * LD;            // [kTile][LD]
-    float* S = yv + kTile * LD;             // [G][kTile]
-    float* mrow = S + kMaxGroup * kTile;    // [G]
-    float* lrow = mrow + kMaxGroup;         // [G]
-    float* alpha = lrow + kMaxGroup;        // [G]
-    float* lvK = alpha + kMaxGroup;         // [8][256]
-    float* lvV = lvK + kMaxBits * kLmStride;
-    Side sk, sv;
-    sk.rsc = lvV + kMaxBits * kLmStride;
-    sv.rsc = sk.rsc + D;
-    sk.bits = reinterpret_cast<int*>(sv.rsc + D);
-    sv.bits = sk.bits + D;
-    sk.off = sv.bits + D;
-    sv.off = sk.off + D;
-    sk.words = reinterpret_cast<uint32_t*>(sv.off + D);
-    sv.words = sk.words + 2 * 8 * D;
+    float* qT = smem;                       // [D][GM] q~ transposed (heads >= G zero)
+    float* wT = qT + D * GM;                // [D][GM] QJL w = S q~, transposed
+    float* y = wT + D * GM;                 // [kTile][LD] K, then the signs, then V
+    float* St = y + kTile * LD;             // [kTile][GM] scores, then probabilities
+    float* mrow = St + kTile * GM;          // [GM]
+    float* lrow = mrow + GM;                // [GM]
+    float* alpha = lrow + GM;               // [GM]
+    float* lv = alpha + GM;                 // [8][kLvs] Gaussian levels (both plans share them)
+    float* nrm = lv + kMaxBits * kLvs;      // [kTile] RWHT norms / sqrt(d) of the tile
+    float* qnr = nrm + kTile;               // [kTile] QJL residual norms of the tile
+    float* rscK = qnr + kTile;              // [D] (K side; V's staged in turn over it -- see below)
+    int* bitsS = reinterpret_cast<int*>(rscK + D);   // [D]
+    int* offS = bitsS + D;                            // [D]
+    uint32_t* words = reinterpret_cast<uint32_t*>(offS + D);   // [2 groups][R]
 
-    for (int e = threadIdx.x; e < G * D; e += blockDim.x)
-        qs[e] = qt[(int64_t(b) * Hq + h * G) * D + e];
-    for (int c = threadIdx.x; c < D; c += blockDim.x) {
-        sk.bits[c] = kp.bits[size_t(h) * D + c];
-        sv.bits[c] = vp.bits[size_t(h) * D + c];
-        sk.off[c] = kp.chan_off[size_t(h) * D + c];
-        sv.off[c] = vp.chan_off[size_t(h) * D + c];
-        sk.rsc[c] = kp.rscale[size_t(h) * D + c];
-        sv.rsc[c] = vp.rscale[size_t(h) * D + c];
+    for (int e = tid; e < D * GM; e += kThreads) {
+        const int c = e / GM, j = e % GM;
+        qT[e] = j < G ? qt[(int64_t(b) * Hq + h * G + j) * D + c] : 0.f;
+        wT[e] = (qj.bits && j < G) ? qj.w[(int64_t(b) * Hq + h * G + j) * D + c] : 0.f;
     }
-    for (int e = threadIdx.x; e < kMaxBits * kLmStride; e += blockDim.x) {
-        lvK[e] = kp.lm_level[e];
-        lvV[e] = vp.lm_level[e];
+    {
+        // the Gaussian levels, from whichever plan has them (the tables are the same)
+        const float* lsrc = kp.quant == SPECTRA_Q_LLOYD_GAUSS ? kp.lm_level : vp.lm_level;
+        for (int e = tid; e < kMaxBits * kLmStride; e += kThreads)
+            lv[(e / kLmStride) * kLvs + e % kLmStride] = lsrc[e];
     }
-    if (threadIdx.x < kMaxGroup) { mrow[threadIdx.x] = -INFINITY; lrow[threadIdx.x] = 0.f; }
+    if (tid < GM) { mrow[tid] = -INFINITY; lrow[tid] = 0.f; }
 
     const int64_t sid = int64_t(b) * Hkv + h;
     const uint32_t* ks = reinterpret_cast<const uint32_t*>(kc + sid * sstride);
@@ -165,89 +186,179 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
     const int64_t s0 = int64_t(split) * split_len;
     const int64_t s1 = min(ctx, s0 + split_len);
 
-    // each thread owns outputs (j, c) for e = tid + k*blockDim
-    constexpr int kOwn = kMaxGroup * D / kThreads;
-    float acc[kOwn];
+    // stage one side's tables and the tile's words (and RWHT norms)
+    auto stage = [&](const PlanView& pv, int R, const uint32_t* stream, const float* norms, int64_t t0) {
+        for (int c = tid; c < D; c += kThreads) {
+            bitsS[c] = pv.bits[size_t(h) * D + c];
+            offS[c] = pv.chan_off[size_t(h) * D + c];
+            rscK[c] = pv.rscale[size_t(h) * D + c];
+        }
+        const int64_t g0 = t0 / kGroup;
+        for (int e = tid; e < 2 * R; e += kThreads) {
+            const int64_t gg = g0 + e / R;
+            words[e] = (gg * kGroup < s1) ? stream[gg * R + (e % R)] : 0u;
+        }
+        if (pv.basis == SPECTRA_BASIS_RWHT)
+            for (int t = tid; t < kTile; t += kThreads)
+                nrm[t] = (t0 + t < s1) ? norms[t0 + t] * rsqrtf(float(D)) : 0.f;
+    };
+    auto unpack = [&](const PlanView& pv, int R, int ntok) {
+        for (int e = tid; e < 2 * D; e += kThreads)
+            unpack_channel_group<D>(pv, e % D, e / D, R, words, bitsS, offS, rscK, lv, nrm, ntok, y);
+    };
+
+    // P V: thread = (channel c, token subset); GM heads at once
+    constexpr int kSub = kThreads / D;             // token subsets (2 for d = 128, 4 for 64)
+    constexpr int kSubTok = kTile / kSub;
+    const int pc = tid % D, psub = tid / D;
+    float acc[GM];
 #pragma unroll
-    for (int k = 0; k < kOwn; ++k) acc[k] = 0.f;
+    for (int j = 0; j < GM; ++j) acc[j] = 0.f;
     __syncthreads();
 
     for (int64_t t0 = s0; t0 < s1; t0 += kTile) {
-        unpack_tile<D>(kp, sk, h, RK, ks, knr, t0, s1, yk, lvK);
-        for (int e = threadIdx.x; e < G * kTile; e += blockDim.x) {
-            const int j = e / kTile, t = e % kTile;
-            float a = 0.f;
-            for (int c = 0; c < D; ++c) a = fmaf(qs[j * D + c], yk[t * LD + c], a);
-            S[j * kTile + t] = (t0 + t < s1) ? a : -INFINITY;
-        }
+        const int ntok = int(min(int64_t(kTile), s1 - t0));
+        // ---- K: unpack, scores
+        stage(kp, RK, ks, knr, t0);
         __syncthreads();
-        if (qj.bits) {
-            // QJL correction: + sqrt(pi/2)/D ||r_t|| sum_i w_ji (2 b_i(t) - 1), w = S_jl qt
-            const uint32_t* qw = reinterpret_cast<const uint32_t*>(qj.bits + sid * qj.stride);
-            const float* qnr = qj.norms + sid * qj.nstride;
-            float* zs = yv;                         // [kTile][LD] signs, free until the V unpack
-            const int64_t g0 = t0 / kGroup;
-            for (int e = threadIdx.x; e < kTile * D; e += blockDim.x) {
-                const int t = e / D, i = e % D;
-                const int64_t gg = g0 + t / kGroup;
-                const bool in = t0 + t < s1;
-                const uint32_t w = in ? qw[gg * D + i] : 0u;
-                zs[t * LD + i] = ((w >> (t & 31)) & 1u) ? 1.f : -1.f;
+        unpack(kp, RK, ntok);
+        __syncthreads();
+        const int st = tid >> 2, qd = tid & 3;     // token, channel quarter
+        {
+            float a[GM];
+#pragma unroll
+            for (int j = 0; j < GM; ++j) a[j] = 0.f;
+            const float* yr = y + st * LD;
+#pragma unroll 4
+            for (int i = 0; i < D / 4; ++i) {
+                const int c = 4 * i + qd;
+                const float yv = yr[c];
+                const float4* qv = reinterpret_cast<const float4*>(qT + c * GM);
+#pragma unroll
+                for (int j4 = 0; j4 < GM / 4; ++j4) {
+                    const float4 q4 = qv[j4];
+                    a[4 * j4] = fmaf(q4.x, yv, a[4 * j4]);
+                    a[4 * j4 + 1] = fmaf(q4.y, yv, a[4 * j4 + 1]);
+                    a[4 * j4 + 2] = fmaf(q4.z, yv, a[4 * j4 + 2]);
+                    a[4 * j4 + 3] = fmaf(q4.w, yv, a[4 * j4 + 3]);
+                }
             }
-            __syncthreads();
-            const float cst = 1.25331413731550025f / float(D);   // sqrt(pi / 2) / m, m = d
-            for (int e = threadIdx.x; e < G * kTile; e += blockDim.x) {
-                const int j = e / kTile, t = e % kTile;
-                if (t0 + t >= s1) continue;
-                const float* wj = qj.w + (int64_t(b) * Hq + h * G + j) * D;
-                float a = 0.f;
-                for (int i = 0; i < D; ++i) a = fmaf(wj[i], zs[t * LD + i], a);
-                S[j * kTile + t] += cst * qnr[t0 + t] * a;
+#pragma unroll
+            for (int j = 0; j < GM; ++j) {
+                a[j] += __shfl_xor_sync(0xffffffffu, a[j], 1);
+                a[j] += __shfl_xor_sync(0xffffffffu, a[j], 2);
             }
-            __syncthreads();
+            if (qd == 0) {
+#pragma unroll
+                for (int j = 0; j < GM; ++j) St[st * GM + j] = (st < ntok) ? a[j] : -INFINITY;
+            }
         }
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (qj.bits) {
+            // QJL correction: + sqrt(pi/2)/d ||r_t|| sum_i w_ji (2 b_i(t) - 1)
+            __syncthreads();                          // the scores have read y
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(qj.bits + sid * qj.stride);
+            const int64_t g0 = t0 / kGroup;
+            for (int e = tid; e < 2 * D; e += kThreads) {
+                const int g = e / D, i = e % D;
+                const uint32_t w = (32 * g < ntok) ? qw[(g0 + g) * D + i] : 0u;
+                float* yc = y + (32 * g) * LD + i;
+#pragma unroll 4
+                for (int t = 0; t < 32; ++t) yc[t * LD] = ((w >> t) & 1u) ? 1.f : -1.f;
+            }
+            for (int t = tid; t < kTile; t += kThreads)
+                qnr[t] = (t0 + t < s1) ? qj.norms[sid * qj.nstride + t0 + t] : 0.f;
+            __syncthreads();
+            float a[GM];
+#pragma unroll
+            for (int j = 0; j < GM; ++j) a[j] = 0.f;
+            const float* yr = y + st * LD;
+#pragma unroll 4
+            for (int i = 0; i < D / 4; ++i) {
+                const int c = 4 * i + qd;
+                const float zv = yr[c];
+                const float4* wv = reinterpret_cast<const float4*>(wT + c * GM);
+#pragma unroll
+                for (int j4 = 0; j4 < GM / 4; ++j4) {
+                    const float4 w4 = wv[j4];
+                    a[4 * j4] = fmaf(w4.x, zv, a[4 * j4]);
+                    a[4 * j4 + 1] = fmaf(w4.y, zv, a[4 * j4 + 1]);
+                    a[4 * j4 + 2] = fmaf(w4.z, zv, a[4 * j4 + 2]);
+                    a[4 * j4 + 3] = fmaf(w4.w, zv, a[4 * j4 + 3]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < GM; ++j) {
+                a[j] += __shfl_xor_sync(0xffffffffu, a[j], 1);
+                a[j] += __shfl_xor_sync(0xffffffffu, a[j], 2);
+            }
+            const float cst = 1.25331413731550025f / float(D);   // sqrt(pi / 2) / m, m = d
+            if (qd == 0 && st < ntok) {
+#pragma unroll
+                for (int j = 0; j < GM; ++j) St[st * GM + j] += cst * qnr[st] * a[j];
+            }
+        }
+        __syncthreads();                              // scores complete; y free
+        // ---- softmax over the tile, one warp per query head
         if (warp < G) {
-            float mx = fmaxf(S[warp * kTile + lane], S[warp * kTile + lane + 32]);
+            const int j = warp;
+            const float x0 = St[lane * GM + j], x1 = St[(lane + 32) * GM + j];
+            float mx = fmaxf(x0, x1);
             for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float mold = mrow[warp];
+            const float mold = mrow[j];
             const float mnew = fmaxf(mold, mx);
-            const float p0 = __expf(S[warp * kTile + lane] - mnew);
-            const float p1 = __expf(S[warp * kTile + lane + 32] - mnew);
-            S[warp * kTile + lane] = p0;
-            S[warp * kTile + lane + 32] = p1;
+            const float p0 = __expf(x0 - mnew), p1 = __expf(x1 - mnew);
+            St[lane * GM + j] = p0;
+            St[(lane + 32) * GM + j] = p1;
             float ps = p0 + p1;
             for (int o = 16; o; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
             if (lane == 0) {
                 const float al = (mold == -INFINITY) ? 0.f : __expf(mold - mnew);
-                alpha[warp] = al;
-                lrow[warp] = lrow[warp] * al + ps;
-                mrow[warp] = mnew;
+                alpha[j] = al;
+                lrow[j] = lrow[j] * al + ps;
+                mrow[j] = mnew;
             }
         }
-        unpack_tile<D>(vp, sv, h, RV, vs, vnr, t0, s1, yv, lvV);   // syncs inside
-#pragma unroll
-        for (int k = 0; k < kOwn; ++k) {
-            const int e = threadIdx.x + k * kThreads;
-            const int j = e / D, c = e % D;
-            if (j < G) {
-                float a = acc[k] * alpha[j];
-                for (int t = 0; t < kTile; ++t) a = fmaf(S[j * kTile + t], yv[t * LD + c], a);
-                acc[k] = a;
-            }
-        }
+        // ---- V: unpack, P V
+        stage(vp, RV, vs, vnr, t0);
         __syncthreads();
-    }
-    float* out = part + ((int64_t(b) * Hq + h * G) * nsplit + split) * (D + 2);
+        unpack(vp, RV, ntok);
+        __syncthreads();
+        {
 #pragma unroll
-    for (int k = 0; k < kOwn; ++k) {
-        const int e = threadIdx.x + k * kThreads;
-        const int j = e / D, c = e % D;
-        if (j < G) out[int64_t(j) * nsplit * (D + 2) + 2 + c] = acc[k];
+            for (int j = 0; j < GM; ++j) acc[j] *= (j < G) ? alpha[j] : 0.f;
+            const int tb = psub * kSubTok;
+#pragma unroll 4
+            for (int t = tb; t < tb + kSubTok; ++t) {
+                const float yv = y[t * LD + pc];
+                const float4* pv4 = reinterpret_cast<const float4*>(St + t * GM);
+#pragma unroll
+                for (int j4 = 0; j4 < GM / 4; ++j4) {
+                    const float4 p4 = pv4[j4];
+                    acc[4 * j4] = fmaf(p4.x, yv, acc[4 * j4]);
+                    acc[4 * j4 + 1] = fmaf(p4.y, yv, acc[4 * j4 + 1]);
+                    acc[4 * j4 + 2] = fmaf(p4.z, yv, acc[4 * j4 + 2]);
+                    acc[4 * j4 + 3] = fmaf(p4.w, yv, acc[4 * j4 + 3]);
+                }
+            }
+        }
+        __syncthreads();                              // y, St, the tables free for the next tile
     }
-    if (threadIdx.x < G) {
-        out[int64_t(threadIdx.x) * nsplit * (D + 2) + 0] = mrow[threadIdx.x];
-        out[int64_t(threadIdx.x) * nsplit * (D + 2) + 1] = lrow[threadIdx.x];
+    // token subsets -> one sum per (head, channel), through the y buffer
+    float* red = y;                                   // [kSub][GM][D]
+#pragma unroll
+    for (int j = 0; j < GM; ++j) red[(psub * GM + j) * D + pc] = acc[j];
+    __syncthreads();
+    float* out = part + ((int64_t(b) * Hq + h * G) * nsplit + split) * (D + 2);
+    for (int e = tid; e < G * D; e += kThreads) {
+        const int j = e / D, c = e % D;
+        float a = 0.f;
+#pragma unroll
+        for (int u = 0; u < kSub; ++u) a += red[(u * GM + j) * D + c];
+        out[int64_t(j) * nsplit * (D + 2) + 2 + c] = a;
+    }
+    if (tid < G) {
+        out[int64_t(tid) * nsplit * (D + 2) + 0] = mrow[tid];
+        out[int64_t(tid) * nsplit * (D + 2) + 1] = lrow[tid];
     }
 }
 
@@ -421,13 +532,6 @@ attn_window_kernel(const void* __restrict__ q, int q_dt, int Hq, int Hkv, int D,
 
 size_t combine_smem(int D, int nsplit) { return sizeof(float) * (size_t(D) * (D + 1) + 5 * size_t(D) + 4 + nsplit); }
 
-template <int D>
-size_t split_smem()
-{
-    return sizeof(float) * (kMaxGroup * D + 2 * kTile * (D + 1) + kMaxGroup * kTile + 3 * kMaxGroup +
-                            2 * kMaxBits * kLmStride + 2 * D) +
-           sizeof(int) * 4 * D + sizeof(uint32_t) * 2 * 2 * 8 * D;
-}
 
 // Context split length, a multiple of 256 tokens (the tensor-core tile):
 // about 2048 blocks over the (batch, kv head) pairs -- counted as one kv
@@ -524,17 +628,20 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
     if (qjl && fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
     attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt, qj);
     dim3 grid(nsplit, Hkv, B);
-    if (D == 128) {
-        const size_t sm = split_smem<128>();
-        if (spectra_status st = set_smem(attn_split_kernel<128>, sm)) return st;
-        attn_split_kernel<128><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
-                                                          nstride, nsplit, split_len, part, qj);
-    } else {
-        const size_t sm = split_smem<64>();
-        if (spectra_status st = set_smem(attn_split_kernel<64>, sm)) return st;
-        attn_split_kernel<64><<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn,
-                                                         nstride, nsplit, split_len, part, qj);
-    }
+    auto go = [&](auto kern, size_t sm) -> spectra_status {
+        if (spectra_status st = set_smem(kern, sm)) return st;
+        kern<<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn, nstride, nsplit, split_len,
+                                        part, qj);
+        return SPECTRA_OK;
+    };
+    spectra_status gst;
+    if (D == 128)
+        gst = Hq / Hkv <= 4 ? go(attn_split_kernel<128, 4>, split_smem_t<128, 4>())
+                     : go(attn_split_kernel<128, 8>, split_smem_t<128, 8>());
+    else
+        gst = Hq / Hkv <= 4 ? go(attn_split_kernel<64, 4>, split_smem_t<64, 4>())
+                     : go(attn_split_kernel<64, 8>, split_smem_t<64, 8>());
+    if (gst) return gst;
     if (spectra_status st = cuda_status(cudaGetLastError())) return st;
     return launch_combine(vp, part, B, Hq, nsplit, 0, wpart, out, s);
 }

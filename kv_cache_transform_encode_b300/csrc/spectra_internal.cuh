@@ -52,6 +52,27 @@ struct DerivedLayout {
     size_t enc_img_head_bytes, dec_img_head_bytes;
 };
 
+// ---------------------------------------------------------------------------
+// Bit-plane helpers shared by the codec and attention kernels.
+// 8x8 bit transpose of a 64-bit block held as (lo, hi): byte i, bit j
+// <-> byte j, bit i.  Three delta swaps (exchange distances 7, 14, 28).
+__device__ __forceinline__ void transpose8(uint32_t& lo, uint32_t& hi)
+{
+    uint32_t t;
+    t = (lo ^ (lo >> 7)) & 0x00AA00AAu;  lo ^= t ^ (t << 7);
+    t = (hi ^ (hi >> 7)) & 0x00AA00AAu;  hi ^= t ^ (t << 7);
+    t = (lo ^ (lo >> 14)) & 0x0000CCCCu; lo ^= t ^ (t << 14);
+    t = (hi ^ (hi >> 14)) & 0x0000CCCCu; hi ^= t ^ (t << 14);
+    t = (lo ^ (hi << 4)) & 0xF0F0F0F0u;  lo ^= t;  hi ^= t >> 4;
+}
+
+// bytes k of four words, in order, as one word
+__device__ __forceinline__ uint32_t gather_byte(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int k)
+{
+    const uint32_t sel = ((4u + k) << 4) | uint32_t(k);
+    return __byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410);
+}
+
 // Launch with programmatic dependent launch allowed: the kernel's CTAs may
 // start (and run their prologue) while the previous kernel in the stream
 // finishes; such a kernel calls pdl_wait() before its first global read.
