@@ -19,6 +19,8 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <algorithm>
+
 namespace spectra {
 
 namespace {
@@ -87,13 +89,23 @@ template <int D>
 constexpr int ystride() { return D + 4; }
 constexpr int kLvs = kLmStride + 1;   // level-table rows 257 floats apart (lanes of different widths)
 
+// rkm, rvm: the plans' widest records (the double-buffered word stages)
 template <int D, int GM>
-size_t split_smem_t()
+size_t split_smem_t(int rkm, int rvm)
 {
     return sizeof(float) * (size_t(2) * D * GM + size_t(kTile) * ystride<D>() + kTile * GM + 3 * GM +
-                            kMaxBits * kLvs + 2 * kTile + D) +
-           sizeof(int) * 2 * D + sizeof(uint32_t) * 2 * 8 * D;
+                            kMaxBits * kLvs + 2 * kTile + 2 * D) +
+           sizeof(int) * 4 * D + sizeof(uint32_t) * 2 * (2 * size_t(rkm) + 2 * size_t(rvm));
 }
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(uint32_t(__cvta_generic_to_shared(dst))), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // the 32 tokens of group g (stream group g0 + g) of channel c into y[32 g + t][c]
 template <int D>
@@ -137,7 +149,7 @@ __device__ __forceinline__ void unpack_channel_group(const PlanView& pv, int c, 
 }
 
 template <int D, int GM>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq, int64_t ctx,
                   const uint8_t* __restrict__ kc, const uint8_t* __restrict__ vc, int64_t sstride,
                   const float* __restrict__ kn, const float* __restrict__ vn, int64_t nstride,
@@ -147,7 +159,9 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
     extern __shared__ __align__(16) float smem[];
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int Hkv = kp.heads, G = Hq / Hkv;
-    const int RK = kp.rec_bits[h], RV = vp.rec_bits[h];
+    // records wider than the plans' bound are not read (the streams were sized by it)
+    const int RKm = kp.max_rec_bits, RVm = vp.max_rec_bits;
+    const int RK = kp.rec_bits[h] <= RKm ? kp.rec_bits[h] : 0, RV = vp.rec_bits[h] <= RVm ? vp.rec_bits[h] : 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     float* qT = smem;                       // [D][GM] q~ transposed (heads >= G zero)
@@ -160,10 +174,16 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
     float* lv = alpha + GM;                 // [8][kLvs] Gaussian levels (both plans share them)
     float* nrm = lv + kMaxBits * kLvs;      // [kTile] RWHT norms / sqrt(d) of the tile
     float* qnr = nrm + kTile;               // [kTile] QJL residual norms of the tile
-    float* rscK = qnr + kTile;              // [D] (K side; V's staged in turn over it -- see below)
-    int* bitsS = reinterpret_cast<int*>(rscK + D);   // [D]
-    int* offS = bitsS + D;                            // [D]
-    uint32_t* words = reinterpret_cast<uint32_t*>(offS + D);   // [2 groups][R]
+    float* rscK = qnr + kTile;              // [D] per-channel tables of the two plans
+    float* rscV = rscK + D;
+    int* bitsK = reinterpret_cast<int*>(rscV + D);
+    int* bitsV = bitsK + D;
+    int* offK = bitsV + D;
+    int* offV = offK + D;
+    // [2 buffers][2 groups x RKm K words, then 2 groups x RVm V words]: the
+    // next tile's words arrive (cp.async) while this tile is computed
+    uint32_t* wb = reinterpret_cast<uint32_t*>(offV + D);
+    const int WB = 2 * RKm + 2 * RVm;
 
     for (int e = tid; e < D * GM; e += kThreads) {
         const int c = e / GM, j = e % GM;
@@ -186,25 +206,41 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
     const int64_t s0 = int64_t(split) * split_len;
     const int64_t s1 = min(ctx, s0 + split_len);
 
-    // stage one side's tables and the tile's words (and RWHT norms)
-    auto stage = [&](const PlanView& pv, int R, const uint32_t* stream, const float* norms, int64_t t0) {
-        for (int c = tid; c < D; c += kThreads) {
-            bitsS[c] = pv.bits[size_t(h) * D + c];
-            offS[c] = pv.chan_off[size_t(h) * D + c];
-            rscK[c] = pv.rscale[size_t(h) * D + c];
-        }
+    for (int c = tid; c < D; c += kThreads) {
+        bitsK[c] = kp.bits[size_t(h) * D + c];
+        offK[c] = kp.chan_off[size_t(h) * D + c];
+        rscK[c] = kp.rscale[size_t(h) * D + c];
+        bitsV[c] = vp.bits[size_t(h) * D + c];
+        offV[c] = vp.chan_off[size_t(h) * D + c];
+        rscV[c] = vp.rscale[size_t(h) * D + c];
+    }
+    // the K and V words of the tile at t0 into buffer buf, asynchronously
+    auto prefetch = [&](int64_t t0, int buf) {
+        uint32_t* wk = wb + buf * WB;
+        uint32_t* wv = wk + 2 * RKm;
         const int64_t g0 = t0 / kGroup;
-        for (int e = tid; e < 2 * R; e += kThreads) {
-            const int64_t gg = g0 + e / R;
-            words[e] = (gg * kGroup < s1) ? stream[gg * R + (e % R)] : 0u;
+        for (int e = tid; e < 2 * RK; e += kThreads) {
+            const int64_t gg = g0 + e / RK;
+            if (gg * kGroup < s1) cp_async4(wk + e, ks + gg * RK + (e % RK));
+            else wk[e] = 0u;
         }
+        for (int e = tid; e < 2 * RV; e += kThreads) {
+            const int64_t gg = g0 + e / RV;
+            if (gg * kGroup < s1) cp_async4(wv + e, vs + gg * RV + (e % RV));
+            else wv[e] = 0u;
+        }
+        cp_async_commit();
+    };
+    // RWHT: the tile's norms / sqrt(d)
+    auto stage_norms = [&](const PlanView& pv, const float* norms, int64_t t0) {
         if (pv.basis == SPECTRA_BASIS_RWHT)
             for (int t = tid; t < kTile; t += kThreads)
                 nrm[t] = (t0 + t < s1) ? norms[t0 + t] * rsqrtf(float(D)) : 0.f;
     };
-    auto unpack = [&](const PlanView& pv, int R, int ntok) {
+    auto unpack = [&](const PlanView& pv, int R, int ntok, const uint32_t* words, const int* bits, const int* off,
+                      const float* rsc) {
         for (int e = tid; e < 2 * D; e += kThreads)
-            unpack_channel_group<D>(pv, e % D, e / D, R, words, bitsS, offS, rscK, lv, nrm, ntok, y);
+            unpack_channel_group<D>(pv, e % D, e / D, R, words, bits, off, rsc, lv, nrm, ntok, y);
     };
 
     // P V: thread = (channel c, token subset); GM heads at once
@@ -216,12 +252,22 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
     for (int j = 0; j < GM; ++j) acc[j] = 0.f;
     __syncthreads();
 
-    for (int64_t t0 = s0; t0 < s1; t0 += kTile) {
+    if (s0 < s1) prefetch(s0, 0);
+    int buf = 0;
+    for (int64_t t0 = s0; t0 < s1; t0 += kTile, buf ^= 1) {
         const int ntok = int(min(int64_t(kTile), s1 - t0));
+        const uint32_t* wk = wb + buf * WB;
+        const uint32_t* wv = wk + 2 * RKm;
+        if (t0 + kTile < s1) {
+            prefetch(t0 + kTile, buf ^ 1);   // the buffer tile - 1 used: free since its last barrier
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
         // ---- K: unpack, scores
-        stage(kp, RK, ks, knr, t0);
+        stage_norms(kp, knr, t0);
         __syncthreads();
-        unpack(kp, RK, ntok);
+        unpack(kp, RK, ntok, wk, bitsK, offK, rscK);
         __syncthreads();
         const int st = tid >> 2, qd = tid & 3;     // token, channel quarter
         {
@@ -319,9 +365,9 @@ attn_split_kernel(PlanView kp, PlanView vp, const float* __restrict__ qt, int Hq
             }
         }
         // ---- V: unpack, P V
-        stage(vp, RV, vs, vnr, t0);
+        stage_norms(vp, vnr, t0);
         __syncthreads();
-        unpack(vp, RV, ntok);
+        unpack(vp, RV, ntok, wv, bitsV, offV, rscV);
         __syncthreads();
         {
 #pragma unroll
@@ -628,6 +674,7 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
     if (qjl && fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
     attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt, qj);
     dim3 grid(nsplit, Hkv, B);
+    const int rkm = std::max(kplan->max_rec_bits, 1), rvm = std::max(vplan->max_rec_bits, 1);
     auto go = [&](auto kern, size_t sm) -> spectra_status {
         if (spectra_status st = set_smem(kern, sm)) return st;
         kern<<<grid, kThreads, sm, s>>>(kp, vp, qt, Hq, ctx, kc, vc, sstride, kn, vn, nstride, nsplit, split_len,
@@ -636,11 +683,11 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
     };
     spectra_status gst;
     if (D == 128)
-        gst = Hq / Hkv <= 4 ? go(attn_split_kernel<128, 4>, split_smem_t<128, 4>())
-                     : go(attn_split_kernel<128, 8>, split_smem_t<128, 8>());
+        gst = Hq / Hkv <= 4 ? go(attn_split_kernel<128, 4>, split_smem_t<128, 4>(rkm, rvm))
+                            : go(attn_split_kernel<128, 8>, split_smem_t<128, 8>(rkm, rvm));
     else
-        gst = Hq / Hkv <= 4 ? go(attn_split_kernel<64, 4>, split_smem_t<64, 4>())
-                     : go(attn_split_kernel<64, 8>, split_smem_t<64, 8>());
+        gst = Hq / Hkv <= 4 ? go(attn_split_kernel<64, 4>, split_smem_t<64, 4>(rkm, rvm))
+                            : go(attn_split_kernel<64, 8>, split_smem_t<64, 8>(rkm, rvm));
     if (gst) return gst;
     if (spectra_status st = cuda_status(cudaGetLastError())) return st;
     return launch_combine(vp, part, B, Hq, nsplit, 0, wpart, out, s);
