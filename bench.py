@@ -362,7 +362,7 @@ def run_ours(args, rank, world, local_rank):
 ATTN_B, ATTN_CTX = 16, 65536
 
 
-def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None, local_rank=None):
+def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None, local_rank=None, rwht_norms=False):
     """Decode-step attention at the compressed-attention workload: batch 16,
     32 query heads over 8 kv heads, 65536-token context packed at the plans'
     2.0 bits/value (K and V streams of 16 x 8 x 65536 tokens).  The stream
@@ -382,6 +382,11 @@ def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None, local_ra
         vc = torch.randint(0, 256, (ATTN_B * H_KV, sb), dtype=torch.uint8, device=dev, generator=gen)
         sets.append((kc, vc))
     q = torch.randn((ATTN_B, HQ, D), device=dev, generator=gen).mul_(D ** -0.5).to(torch.bfloat16)
+    # RWHT plans: per-token norms of K and V (seeded, in [1, 10))
+    kn = vn = None
+    if rwht_norms:
+        kn = torch.rand((ATTN_B * H_KV, ATTN_CTX), device=dev, generator=gen).mul_(9).add_(1)
+        vn = torch.rand((ATTN_B * H_KV, ATTN_CTX), device=dev, generator=gen).mul_(9).add_(1)
     out = torch.empty((ATTN_B, HQ, D), dtype=torch.float32, device=dev)
     ws = torch.empty((spx.spectra_attn_workspace_bytes(ATTN_B, HQ, D, ATTN_CTX) + 256,), dtype=torch.uint8,
                      device=dev)
@@ -389,7 +394,7 @@ def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None, local_ra
 
     def call(i):
         kc, vc = sets[i % 2]
-        spx.spectra_attn_decode(kp, vp, q, kc, vc, ATTN_CTX, 1.0, out, workspace=ws)
+        spx.spectra_attn_decode(kp, vp, q, kc, vc, ATTN_CTX, 1.0, out, workspace=ws, k_norms=kn, v_norms=vn)
     for i in range(warm):
         call(i)
     torch.cuda.synchronize()
@@ -412,13 +417,15 @@ def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None, local_ra
         total_ms, clocks = clocked(local_rank, timed, load, before=0.3, after=0.2)
     ms = total_ms / reps
     nbytes = 2 * ATTN_B * H_KV * (ATTN_CTX // 32) * 4 * R      # packed K and V words read
+    if rwht_norms:
+        nbytes += 2 * ATTN_B * H_KV * ATTN_CTX * 4               # and the fp32 norms
     gbs = nbytes / (ms * 1e-3) / 1e9
-    del sets
+    del sets, kn, vn
     return {"workload": f"batch {ATTN_B}, {HQ} q heads / {H_KV} kv heads, d {D}, context {ATTN_CTX}, "
                         f"{R} bits per token and head (K and V)", "ms": round(ms, 4),
             "packed_bytes": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": peaks["hbm_gbs"],
             "frac": round(gbs / peaks["hbm_gbs"], 4), "cached_tokens_per_s": round(ATTN_B * ATTN_CTX / (ms * 1e-3), 1),
-            "l2": "2 rotating stream sets (2 x 537 MB) > L2", "clocks": clocks}
+            "l2": f"2 rotating stream sets (2 x {nbytes / 1e6:.0f} MB) > L2", "clocks": clocks}
 
 
 
@@ -579,6 +586,9 @@ def budget_sweep(spx, K, V, dev, peaks, local_rank, reps=10):
                                      "slice_relmse_k": round(orc.relmse(ksl, kh), 6),
                                      "slice_relmse_v": round(orc.relmse(vsl, vh), 6)},
                     "clocks": clocks})
+        if abs(B - 2.0) < 1e-9:
+            # decode-step attention over Lloyd-Max streams (the CUDA-core kernel)
+            out[-1]["attn_decode"] = attn_workload(spx, kp, vp, dev, peaks, reps=5, warm=2, local_rank=local_rank)
         del kc, vc
     return {"workload": ("llama3.1-8b-shaped layer (8 kv heads x 32768 tokens, d 128, bf16), Gaussian "
                          "Lloyd-Max levels, K and V calibrated and allocated separately"),
@@ -812,6 +822,16 @@ def qwen_rwht(spx, dev, peaks, local_rank, steps=4, e2e_steps=2, seed=2024):
                         "bytes_per_vector": per_vec},
            "relmse_k": round(rk, 6), "relmse_v": round(rv, 6), "cosine_k": round(ck, 6), "cosine_v": round(cv, 6),
            "clocks": clocks}
+    # decode-step attention over RWHT + 3-bit Lloyd-Max streams at the
+    # compressed-attention workload's shape (the CUDA-core kernel; 8 kv heads)
+    aps = []
+    for side in range(2):
+        ap = spx.Plan(H_KV, D, basis=spx.SPECTRA_BASIS_RWHT, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev)
+        ap.signs.copy_(torch.from_numpy(synth.rwht_signs(seed + 7 + side, H_KV, D)))
+        spx.spectra_alloc_bits(ap, 0.0, fixed_bits=3)
+        aps.append(ap)
+    res["attn_decode"] = attn_workload(spx, aps[0], aps[1], dev, peaks, reps=5, warm=2, local_rank=local_rank,
+                                       rwht_norms=True)
     # end to end: pinned host K, V in, codes and norms out, every step
     try:
         hK = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
