@@ -241,3 +241,11 @@ def test_attn_compressed_attention_workload_sampled(spx, orc):
     got, q, rec = _batched_case(spx, orc, B, Hq, Hkv, ctx, checked, seed=73)
     _check_batched(orc, got, q, rec, Hq, Hkv)
     assert np.all(np.isfinite(got))
+
+
+@pytest.mark.parametrize("kind,quant,G", [("eigen", 1, 4), ("rwht", 1, 4), ("eigen", 1, 8)])
+def test_attn_cuda_core_plans_multi_split(spx, orc, kind, quant, G):
+    """Lloyd-Max and RWHT plans (the CUDA-core kernel) over several context
+    splits with a ragged last tile, 4 and 8 query heads per kv head."""
+    got, want = _run(spx, orc, B=2, Hq=2 * G, Hkv=2, ctx=5000 + 29, kind=kind, quant=quant, B_bits=2.0)
+    assert rel_l2(got, want) <= ATTN_TOL, rel_l2(got, want)
