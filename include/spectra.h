@@ -118,8 +118,9 @@ SPECTRA_API int spectra_version(void);
  * Kernel family for spectra_encode, spectra_decode and spectra_attn_decode
  * (a process-wide setting; not part of the method, which both families
  * compute in full).  AUTO: the tensor-core kernels where they cover the call
- * (bf16 caches with head_dim 128 for the codec; head_dim 128 with at most 4
- * query heads per kv head for attention), the CUDA-core kernels elsewhere.
+ * (bf16 caches with head_dim 128 for the codec; head_dim 128 with at most 8
+ * query heads per kv head, and no key-residual sketch, for attention), the
+ * CUDA-core kernels elsewhere.
  * CUDA_CORE: the CUDA-core kernels only.  TENSOR_CORE: the tensor-core
  * kernels only; a call they do not cover returns SPECTRA_ERR_UNSUPPORTED.
  * The initial value comes from the environment variable SPECTRA_PATH, read

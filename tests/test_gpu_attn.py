@@ -16,8 +16,9 @@ FAMILY = {"tc": 2, "generic": 1}
 
 @pytest.fixture(params=["tc", "generic"])
 def path(request):
-    """Kernel family for uniform-quantizer eigenbasis plans: the tensor-core
-    kernels (required) or the CUDA-core kernels."""
+    """Kernel family: the tensor-core kernels (required: bit-plane for
+    uniform eigenbasis plans with <= 4 query heads per kv head, level-table
+    otherwise) or the CUDA-core kernels."""
     import kv_cache_transform_encode_b300 as spx
     prev = spx.spectra_get_kernel_family()
     spx.spectra_set_kernel_family(FAMILY[request.param])
@@ -90,7 +91,7 @@ def test_attn_uniform_gqa(spx, orc, path, ctx):
     assert rel_l2(got, want) <= ATTN_TOL, rel_l2(got, want)
 
 
-def test_attn_lloyd(spx, orc):
+def test_attn_lloyd(spx, orc, path):
     got, want = _run(spx, orc, B=1, Hq=4, Hkv=1, ctx=3000, quant=1, B_bits=1.33)
     assert rel_l2(got, want) <= ATTN_TOL
 
@@ -109,7 +110,7 @@ def test_attn_small_groups(spx, orc, path, G):
     assert rel_l2(got, want) <= ATTN_TOL
 
 
-def test_attn_rwht(spx, orc):
+def test_attn_rwht(spx, orc, path):
     got, want = _run(spx, orc, B=2, Hq=4, Hkv=2, ctx=1200, kind="rwht")
     assert rel_l2(got, want) <= ATTN_TOL
 
@@ -243,9 +244,21 @@ def test_attn_compressed_attention_workload_sampled(spx, orc):
     assert np.all(np.isfinite(got))
 
 
-@pytest.mark.parametrize("kind,quant,G", [("eigen", 1, 4), ("rwht", 1, 4), ("eigen", 1, 8)])
-def test_attn_cuda_core_plans_multi_split(spx, orc, kind, quant, G):
-    """Lloyd-Max and RWHT plans (the CUDA-core kernel) over several context
-    splits with a ragged last tile, 4 and 8 query heads per kv head."""
+@pytest.mark.parametrize("kind,quant,G", [("eigen", 1, 4), ("rwht", 1, 4), ("eigen", 1, 8), ("rwht", 1, 7),
+                                          ("eigen", 0, 8), ("eigen", 0, 5)])
+def test_attn_plans_multi_split(spx, orc, path, kind, quant, G):
+    """Lloyd-Max and RWHT plans, and uniform plans with more than four query
+    heads per kv head (the level-table tensor-core kernel, or the CUDA-core
+    one), over several context splits with a ragged last group."""
     got, want = _run(spx, orc, B=2, Hq=2 * G, Hkv=2, ctx=5000 + 29, kind=kind, quant=quant, B_bits=2.0)
     assert rel_l2(got, want) <= ATTN_TOL, rel_l2(got, want)
+
+
+def test_attn_lloyd_batched_many_splits(spx, orc, path):
+    """Lloyd-Max plans at 2.0 bits/value on the long-split branch: batch 8 x
+    32 query heads over 8 kv heads, 8192 + 37 tokens, checked on four
+    (batch, kv head) pairs."""
+    B, Hq, Hkv, ctx = 8, 32, 8, 8192 + 37
+    checked = [(0, 0), (3, 5), (7, 7), (5, 2)]
+    got, q, rec = _batched_case(spx, orc, B, Hq, Hkv, ctx, checked, seed=79, quant=1)
+    _check_batched(orc, got, q, rec, Hq, Hkv)
