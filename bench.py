@@ -67,6 +67,9 @@ def parse():
                          "or Lloyd-Max levels at --avg-bits, or RWHT with 3-bit Lloyd-Max), then time only its "
                          "encode and decode (prints their block, not a bench line)")
     ap.add_argument("--avg-bits", type=float, default=2.0, help="budget of --codec-only (bits/value)")
+    ap.add_argument("--attn-plans", choices=["uniform", "lloyd", "rwht"], default="uniform",
+                    help="plans of --attn-only: the layer's uniform plans, eigenbasis Lloyd-Max plans at "
+                         "--avg-bits, or RWHT plans with 3-bit Lloyd-Max levels (with per-token norms)")
     ap.add_argument("--attn-batch", type=int, default=16,
                     help="batch of the compressed-attention workload (default 16); smaller for profiling captures")
     return ap.parse_args()
@@ -199,9 +202,23 @@ def run_ours(args, rank, world, local_rank):
         return {"codec": codec_only(spx, args, K, dev, _peaks())}
     if args.attn_only:
         step(0)
+        ap_, rw = (kp, vp), False
+        if args.attn_plans == "lloyd":
+            ap_ = tuple(spx.Plan(H_KV, D, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev) for _ in range(2))
+            for p_, x_ in zip(ap_, (K[0], V[0])):
+                spx.spectra_calibrate(p_, x_, n_cal=N_CAL)
+                spx.spectra_alloc_bits(p_, args.avg_bits)
+        elif args.attn_plans == "rwht":
+            ap_ = tuple(spx.Plan(H_KV, D, basis=spx.SPECTRA_BASIS_RWHT, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev)
+                        for _ in range(2))
+            for side, p_ in enumerate(ap_):
+                p_.signs.copy_(torch.from_numpy(synth.rwht_signs(600 + side, H_KV, D)))
+                spx.spectra_alloc_bits(p_, 0.0, fixed_bits=3)
+            rw = True
         torch.cuda.synchronize()
-        return {"attn_decode": attn_workload(spx, kp, vp, dev, _peaks(), warm=args.warmup, reps=args.steps,
-                                             batch=args.attn_batch)}
+        return {"attn_decode": attn_workload(spx, ap_[0], ap_[1], dev, _peaks(), warm=args.warmup, reps=args.steps,
+                                             batch=args.attn_batch, rwht_norms=rw),
+                "plans": args.attn_plans}
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
