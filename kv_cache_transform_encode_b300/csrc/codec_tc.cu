@@ -402,7 +402,8 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
         // Lloyd-Max bucket grid of this channel's width: clamp range, 2^k,
         // m + magic, table offset - the magic's bit pattern
         float bk_a = 0.f, bk_sc = 0.f;
-        int bk_base = 0;
+        int bk_base = 0;         // table offset of the width minus the magic's bit pattern
+        uint32_t bk_addr = 0u;   // the same as a shared address: first entry - 8 x the magic's bits (wraps)
         bool head_ok = true;
         uint32_t* out = nullptr;
         float* cur_norms = nullptr;            // RWHT: this unit's norms
@@ -470,23 +471,44 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
             } else if (!bk_bad) {
                 // eight lookups in flight at a time (the memory clobber keeps the
                 // compiler from hoisting all 32 loads, which needs 64 registers)
+                if (rwht) {
 #pragma unroll
-                for (int i0 = 0; i0 < 32; i0 += 8) {
+                    for (int i0 = 0; i0 < 32; i0 += 8) {
 #pragma unroll
-                    for (int i = i0; i < i0 + 8; ++i) {
-                        const float u = __uint_as_float(r[i]) * (rwht ? invs[i] : qk);
-                        const float sv = fma_rm_sat(u, bk_a, 0.5f);
-                        const float2 e = tab[__float_as_int(__fmaf_rd(sv, bk_sc, kMagic)) + bk_base];
-                        r[i] = uint32_t(__float_as_int(e.y) + (u >= e.x ? 1 : 0));
+                        for (int i = i0; i < i0 + 8; ++i) {
+                            const float u = __uint_as_float(r[i]) * invs[i];
+                            const float sv = fma_rm_sat(u, bk_a, 0.5f);
+                            const float2 e = tab[__float_as_int(__fmaf_rd(sv, bk_sc, kMagic)) + bk_base];
+                            r[i] = uint32_t(__float_as_int(e.y) + (u >= e.x ? 1 : 0));
+                        }
+                        asm volatile("" ::: "memory");
                     }
-                    asm volatile("" ::: "memory");
+                } else {
+                    // eigenbasis: the image already carries 1 / sigma_c, and the
+                    // entry's address is the bucket value's bit pattern times 8
+                    // plus one per-width base
+#pragma unroll
+                    for (int i0 = 0; i0 < 32; i0 += 8) {
+#pragma unroll
+                        for (int i = i0; i < i0 + 8; ++i) {
+                            const float u = __uint_as_float(r[i]);
+                            const float sv = fma_rm_sat(u, bk_a, 0.5f);
+                            const uint32_t bits = __float_as_uint(__fmaf_rd(sv, bk_sc, kMagic));
+                            float hi, cnt;
+                            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                                         : "=f"(hi), "=f"(cnt)
+                                         : "r"(bk_addr + (bits << 3)));
+                            r[i] = uint32_t(__float_as_int(cnt) + (u >= hi ? 1 : 0));
+                        }
+                        asm volatile("" ::: "memory");
+                    }
                 }
             } else {
                 // a table whose premise failed: a binary search over the thresholds
                 const float* tb = P.pv.lm_thresh + (b > 0 ? (b - 1) * kLmStride : 0);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float u = __uint_as_float(r[i]) * (rwht ? invs[i] : qk);
+                    const float u = rwht ? __uint_as_float(r[i]) * invs[i] : __uint_as_float(r[i]);
                     int lo = 0;
 #pragma unroll 1
                     for (int step = b > 0 ? 1 << (b - 1) : 0; step; step >>= 1)
@@ -555,6 +577,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
                     bk_a = __int_as_float((127 + bk_shift(bw) - bk_log(bw)) << 23);      // 2^(k-p)
                     bk_sc = __int_as_float((127 + bk_log(bw)) << 23);                    // 2^p
                     bk_base = bk_off(bw) - __float_as_int(kMagic);
+                    bk_addr = smem_u32(tab) + 8u * uint32_t(bk_base);
                 }
                 out = reinterpret_cast<uint32_t*>(s1 ? P.codes2 + int64_t(hh) * P.sstride2
                                                       : P.codes + int64_t(hh) * P.sstride) + P.g0 * R;
@@ -1178,6 +1201,8 @@ tc_images_kernel(PlanView pv, uint8_t* __restrict__ enc, uint8_t* __restrict__ d
             float v;
             if (rwht) v = float(pv.signs[size_t(h) * D + kk] * hadamard_sign(kk, r));
             else v = pv.basis_mat[(size_t(h) * D + kk) * D + r];
+            // Lloyd-Max on an eigenbasis: the contraction yields u = y / sigma_c directly
+            if (!rwht && pv.quant == SPECTRA_Q_LLOYD_GAUSS) v *= pv.qscale[size_t(h) * D + r];
             const int nt = rwht ? 1 : 3;
             float rem = v;
             for (int t = 0; t < nt; ++t) {
