@@ -40,8 +40,10 @@
 // plain codes and a computed address.
 //
 // The warps are independent: warp w of a CTA takes every eighth 32-token
-// group of the CTA's context split, stages each group's K and V records
-// (and RWHT norms) through its own cp.async ring, and keeps its own online
+// group of the CTA's context split and stages its records through two
+// cp.async slots of its own, K in one and V in the other: the next group's K
+// record (and RWHT norms) lands during this group's softmax and P V, its V
+// record during the next group's scores.  Each warp keeps its own online
 // softmax (m, l) and value sums (in shared memory, updated once per 16
 // channels with the softmax rescale folded in).  The eight states merge once,
 // at the end of the split, into the partials the combine kernel of attn.cu
@@ -52,6 +54,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
 #include <type_traits>
 
 namespace spectra {
@@ -216,13 +219,13 @@ struct LvParams {
     int Hq, G, nsplit, split_len;
     int64_t ctx;
     float* part;
-    int rks, rvs, sw;         // stage layout (words): K record, V record, whole stage of one warp
+    int sw;                   // words of one record slot (widest record, padding, norms)
 };
 
 // Shared memory (after aligning the start to 256 bytes): level tables,
 // channel descriptors (word offset, table address, code masks), per-step
 // widest widths, the score weights as B fragments, each warp's P tile and
-// value sums, the merge scalars, then the warps' stage rings.
+// value sums, the merge scalars, then the warps' record slots (two each).
 template <int NT>
 struct LvSmem {
     static constexpr int PS = NT == 1 ? 8 : 24;   // u32 per token row of a P tile (conflict-free reads)
@@ -230,10 +233,10 @@ struct LvSmem {
                             descV = descK + 16 * D, bmK = descV + 16 * D, bmV = bmK + 64, wf = bmV + 64,
                             pw = wf + size_t(8) * NT * 16 * 32, ob = pw + size_t(4) * kWarps * 32 * PS,
                             mw = ob + size_t(8) * kWarps * NT * 8 * 32, lw = mw + 4 * 64, ring = lw + 4 * 64;
-    static size_t total(int S, int sw) { return 256 + ring + size_t(4) * kWarps * S * sw; }
+    static size_t total(int sw) { return 256 + ring + size_t(4) * kWarps * 2 * sw; }
 };
 
-template <int NT, int S>
+template <int NT>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kernel(const LvParams P)
 {
     using L = LvSmem<NT>;
@@ -329,26 +332,24 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
     const int64_t s1 = min(P.ctx, s0 + P.split_len);
     const int ng = int((s1 - s0 + kGroup - 1) / kGroup);   // s0 is a multiple of 32
     const int64_t g0 = s0 / kGroup;
-    uint32_t* wring = ring + size_t(warp) * S * P.sw;
-    const int voff = P.rks + kPad, noff = voff + P.rvs + kPad;
+    uint32_t* const slotK = ring + size_t(warp) * 2 * P.sw;
+    uint32_t* const slotV = slotK + P.sw;
+    const int noff = P.sw - 32;      // the record's per-token norms (RWHT Lloyd-Max plans)
 
-    // the records of the warp's it-th group into stage it % S; always commits
-    auto issue = [&](int it) {
+    // one record (K: side 0, V: side 1) of the warp's it-th group into its
+    // slot, with the norms where the plan has them; always commits
+    auto issue = [&](int it, int side) {
         const int gi = warp + kWarps * it;
         if (gi < ng) {
-            uint32_t* st = wring + (it % S) * P.sw;
+            uint32_t* st = side ? slotV : slotK;
             const int64_t grp = g0 + gi;
-            copy_record(st, ks + grp * RK * 4, RK, lane);
-            copy_record(st + voff, vs + grp * RV * 4, RV, lane);
-            float* nst = reinterpret_cast<float*>(st + noff);
-            const int64_t t = grp * kGroup + lane;
-            if (ktok) {
-                if (t < s1) cp_async4(smem_u32(nst + lane), knr + t);
+            if (side) copy_record(st, vs + grp * RV * 4, RV, lane);
+            else copy_record(st, ks + grp * RK * 4, RK, lane);
+            if (side ? vtok : ktok) {
+                float* nst = reinterpret_cast<float*>(st + noff);
+                const int64_t t = grp * kGroup + lane;
+                if (t < s1) cp_async4(smem_u32(nst + lane), (side ? vnr : knr) + t);
                 else nst[lane] = 0.f;
-            }
-            if (vtok) {
-                if (t < s1) cp_async4(smem_u32(nst + 32 + lane), vnr + t);
-                else nst[32 + lane] = 0.f;
             }
         }
         cp_async_commit();
@@ -363,18 +364,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
     uint32_t* pw = Pw + warp * 32 * PS;
     float2* ow = Ob + warp * NT * 8 * 32 + lane;
 
-#pragma unroll
-    for (int it = 0; it < S - 1; ++it) issue(it);
+    issue(0, 0);
+    issue(0, 1);
 #pragma unroll 1
     for (int it = 0; warp + kWarps * it < ng; ++it) {
-        __syncwarp();                 // every lane is past its reads of the stage refilled next
-        issue(it + S - 1);
-        cp_async_wait<S - 1>();
-        __syncwarp();                 // the group's words, copied by every lane, are visible
-        const uint32_t* wk = wring + (it % S) * P.sw;
-        const uint32_t* wv = wk + voff;
-        const float* nk = reinterpret_cast<const float*>(wk + noff);
-        const float* nv = nk + 32;
+        cp_async_wait<1>();           // K of this group (its V may still be in flight)
+        __syncwarp();                 // the words, copied by every lane, are visible
+        const uint32_t* wk = slotK;
+        const uint32_t* wv = slotV;
+        const float* nk = reinterpret_cast<const float*>(slotK + noff);
+        const float* nv = reinterpret_cast<const float*>(slotV + noff);
         const int64_t tb = (g0 + warp + kWarps * it) * kGroup + g;   // token of byte 0
 
         // ---- scores of the group's 32 tokens
@@ -410,19 +409,30 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
             else score_step(std::integral_constant<int, 0>{}, kb, bm);
         }
 
+        // scores of this thread's tokens (g + 8 m), scaled by the K norms
+        float s[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            s[nt][0] = sc[nt][0][0] + sc[nt][0][1];
+            s[nt][1] = sc[nt][0][2] + sc[nt][0][3];
+            s[nt][2] = sc[nt][1][0] + sc[nt][1][1];
+            s[nt][3] = sc[nt][1][2] + sc[nt][1][3];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                if (ktok) s[nt][m] *= nk[g + 8 * m];
+                s[nt][m] = (tb + 8 * m < s1) ? s[nt][m] : -INFINITY;
+            }
+        }
+        __syncwarp();                 // every lane is past its reads of the K slot
+        issue(it + 1, 0);             // the next group's K lands during this softmax and P V
+        cp_async_wait<1>();           // this group's V
+        __syncwarp();
+
         // ---- online softmax of the warp's own tokens; P tile for P V
         float alpha[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            float s[4] = {sc[nt][0][0] + sc[nt][0][1], sc[nt][0][2] + sc[nt][0][3], sc[nt][1][0] + sc[nt][1][1],
-                          sc[nt][1][2] + sc[nt][1][3]};
-            float mx = -INFINITY;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (ktok) s[m] *= nk[g + 8 * m];
-                s[m] = (tb + 8 * m < s1) ? s[m] : -INFINITY;
-                mx = fmaxf(mx, s[m]);
-            }
+            float mx = fmaxf(fmaxf(s[nt][0], s[nt][1]), fmaxf(s[nt][2], s[nt][3]));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -433,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
             float ps = 0.f;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                const float p = exp2f(s[m] - mnew);
+                const float p = exp2f(s[nt][m] - mnew);
                 ps += p;
                 const float pv = vtok ? p * nv[g + 8 * m] : p;
                 const uint32_t hi = bf16_bits(pv), lo = bf16_bits(pv - bf16_val(hi));
@@ -489,6 +499,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
             if (bm <= 6) value_step(std::integral_constant<int, 2>{}, mt, bm);
             else value_step(std::integral_constant<int, 0>{}, mt, bm);
         }
+        __syncwarp();                 // every lane is past its reads of the V slot
+        issue(it + 1, 1);             // the next group's V lands during its scores
     }
     cp_async_wait<0>();               // (only empty groups can remain)
 
@@ -563,11 +575,9 @@ spectra_status launch_attn_lv(const spectra_plan* kplan, const spectra_plan* vpl
     P.split_len = split_len;
     P.ctx = ctx;
     P.part = part;
-    P.rks = (RKm + 3) & ~3;
-    P.rvs = (RVm + 3) & ~3;
-    const bool norms = (kplan->quant == SPECTRA_Q_LLOYD_GAUSS && kplan->basis == SPECTRA_BASIS_RWHT) ||
-                       (vplan->quant == SPECTRA_Q_LLOYD_GAUSS && vplan->basis == SPECTRA_BASIS_RWHT);
-    P.sw = P.rks + kPad + P.rvs + kPad + (norms ? 64 : 0);
+    // a slot: the widest record (16-byte multiple), the padding the plane
+    // reads may run into, then 32 norms
+    P.sw = ((std::max(RKm, RVm) + 3) & ~3) + kPad + 32;
     dim3 grid(nsplit, Hkv, B);
     auto go = [&](auto kern, size_t sm) -> spectra_status {
         if (spectra_status e = set_smem(kern, sm)) return e;
@@ -576,18 +586,12 @@ spectra_status launch_attn_lv(const spectra_plan* kplan, const spectra_plan* vpl
         *done = true;
         return SPECTRA_OK;
     };
-    // the most CTAs per SM (228 KB, 1 KB of it per CTA reserved), then the
-    // deeper ring
-    const int per_sm = G <= 4 ? 3 : 2;
-    for (int cap : {per_sm, 2, 1}) {
+    // as many CTAs per SM as the registers allow, if the shared memory does
+    // (228 KB per SM, 1 KB of it per CTA reserved)
+    for (int cap : {G <= 4 ? 3 : 2, 2, 1}) {
         const size_t lim = size_t(228 * 1024) / cap - 1024;
-        if (G <= 4) {
-            if (LvSmem<1>::total(3, P.sw) <= lim) return go(attn_lv_split_kernel<1, 3>, LvSmem<1>::total(3, P.sw));
-            if (LvSmem<1>::total(2, P.sw) <= lim) return go(attn_lv_split_kernel<1, 2>, LvSmem<1>::total(2, P.sw));
-        } else {
-            if (LvSmem<2>::total(3, P.sw) <= lim) return go(attn_lv_split_kernel<2, 3>, LvSmem<2>::total(3, P.sw));
-            if (LvSmem<2>::total(2, P.sw) <= lim) return go(attn_lv_split_kernel<2, 2>, LvSmem<2>::total(2, P.sw));
-        }
+        if (G <= 4 && LvSmem<1>::total(P.sw) <= lim) return go(attn_lv_split_kernel<1>, LvSmem<1>::total(P.sw));
+        if (G > 4 && LvSmem<2>::total(P.sw) <= lim) return go(attn_lv_split_kernel<2>, LvSmem<2>::total(P.sw));
     }
     return SPECTRA_OK;
 }
