@@ -119,8 +119,8 @@ SPECTRA_API int spectra_version(void);
  * (a process-wide setting; not part of the method, which both families
  * compute in full).  AUTO: the tensor-core kernels where they cover the call
  * (bf16 caches with head_dim 128 for the codec; head_dim 128 with at most 8
- * query heads per kv head, and no key-residual sketch, for attention), the
- * CUDA-core kernels elsewhere.
+ * query heads per kv head for attention, with or without the key-residual
+ * sketch), the CUDA-core kernels elsewhere.
  * CUDA_CORE: the CUDA-core kernels only.  TENSOR_CORE: the tensor-core
  * kernels only; a call they do not cover returns SPECTRA_ERR_UNSUPPORTED.
  * The initial value comes from the environment variable SPECTRA_PATH, read
@@ -420,8 +420,9 @@ SPECTRA_API spectra_status spectra_qjl_encode(const spectra_plan* plan, const fl
  * otherwise (an unbiased estimate of <q, k_t - khat_t>).
  * k_qjl_bits / k_qjl_norms: the spectra_qjl_encode outputs of every (b, kv
  *   head) stream, at + (b * Hkv + h) * qjl_stride_bytes / qjl_norms_stride.
- * CUDA-core kernels (SPECTRA_ERR_UNSUPPORTED when the tensor-core family is
- *   required); everything else as for spectra_attn_decode.
+ * Kernels as for spectra_attn_decode (the sketch term is one more tensor-core
+ *   contraction of the level-table kernel); everything else as for
+ *   spectra_attn_decode.
  */
 SPECTRA_API spectra_status spectra_attn_decode_qjl(const spectra_plan* kplan, const spectra_plan* vplan,
                                    const void* q, spectra_dtype q_dt, int B, int Hq,

@@ -608,7 +608,8 @@ spectra_status launch_attn_tc(const spectra_plan* kplan, const spectra_plan* vpl
 spectra_status launch_attn_lv(const spectra_plan* kplan, const spectra_plan* vplan, const float* qt, int B, int Hq,
                               const uint8_t* kc, const uint8_t* vc, int64_t sstride, const float* kn,
                               const float* vn, int64_t nstride, int64_t ctx, float* part, int nsplit, int split_len,
-                              cudaStream_t s, bool* done);   // attn_lv.cu
+                              const uint8_t* qbits, int64_t qstride, const float* qnorms, int64_t qnstride,
+                              const float* qw, cudaStream_t s, bool* done);   // attn_lv.cu
 
 spectra_status launch_combine(const PlanView& vp, const float* part, int B, int Hq, int nsplit, int code_domain,
                               const float* win, float* out, cudaStream_t s)
@@ -668,24 +669,27 @@ spectra_status launch_attn(const spectra_plan* kplan, const spectra_plan* vplan,
     }
     const int fam = kernel_family();
     bool have_qt = false;
-    if (fam != SPECTRA_KERNELS_CUDA_CORE && !qjl) {
+    if (fam != SPECTRA_KERNELS_CUDA_CORE) {
         // the bit-plane kernel (uniform quantizer, eigenbasis, <= 4 query
-        // heads per kv head), else the level-table kernel (any plan pair)
+        // heads per kv head, no sketch), else the level-table kernel (any
+        // plan pair, with or without the sketch correction)
         bool done = false;
-        spectra_status st = launch_attn_tc(kplan, vplan, q, q_dt, B, Hq, kc, vc, sstride, ctx, scale, part, nsplit,
-                                           split_len, extra, s, &done);
-        if (st) return st;
-        if (done) return launch_combine(vp, part, B, Hq, nsplit, 1, wpart, out, s);
+        spectra_status st = SPECTRA_OK;
+        if (!qjl) {
+            st = launch_attn_tc(kplan, vplan, q, q_dt, B, Hq, kc, vc, sstride, ctx, scale, part, nsplit, split_len,
+                                extra, s, &done);
+            if (st) return st;
+            if (done) return launch_combine(vp, part, B, Hq, nsplit, 1, wpart, out, s);
+        }
         attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt, qj);
         if (spectra_status e = cuda_status(cudaGetLastError())) return e;
         have_qt = true;
         st = launch_attn_lv(kplan, vplan, qt, B, Hq, kc, vc, sstride, kn, vn, nstride, ctx, part, nsplit, split_len,
-                            s, &done);
+                            qj.bits, qj.stride, qj.norms, qj.nstride, qj.w, s, &done);
         if (st) return st;
         if (done) return launch_combine(vp, part, B, Hq, nsplit, 0, wpart, out, s);
         if (fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
     }
-    if (qjl && fam == SPECTRA_KERNELS_TENSOR_CORE) return SPECTRA_ERR_UNSUPPORTED;
     if (!have_qt) attn_qrot_kernel<<<B * Hq, D, D * sizeof(float), s>>>(kp, q, q_dt, Hq, Hkv, scale, qt, qj);
     dim3 grid(nsplit, Hkv, B);
     const int rkm = std::max(kplan->max_rec_bits, 1), rvm = std::max(vplan->max_rec_bits, 1);

@@ -69,6 +69,7 @@ constexpr int kTabWords = 13 * kSlot;      // widths 0..6 one slot each, width 7
 constexpr int kPad = 8;                    // stage words past each record (reads up to 7 past a channel)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kQjlScale = 1.25331413731550025f / float(D);   // sqrt(pi / 2) / m, m = d sketch rows
 
 // first word of width w's table (width 0: one zero entry)
 __host__ __device__ constexpr int tab_word(int w) { return w <= 7 ? w * kSlot : 9 * kSlot; }
@@ -219,27 +220,37 @@ struct LvParams {
     int Hq, G, nsplit, split_len;
     int64_t ctx;
     float* part;
-    int sw;                   // words of one record slot (widest record, padding, norms)
+    int sw;                   // words of one record slot
+    int nofs;                 // slot offset of the record's norms (after the widest record and its padding)
+    // the 1-bit key-residual sketch (kernels with QJ): per (b, kv head) a
+    // bit-plane stream of D one-bit rows, the residual norms, and the
+    // per-query weights w = S qt
+    const uint8_t* qbits;
+    int64_t qstride;
+    const float* qnorms;
+    int64_t qnstride;
+    const float* qw;          // [B Hq][D]
 };
 
 // Shared memory (after aligning the start to 256 bytes): level tables,
 // channel descriptors (word offset, table address, code masks), per-step
 // widest widths, the score weights as B fragments, each warp's P tile and
 // value sums, the merge scalars, then the warps' record slots (two each).
-template <int NT>
+template <int NT, bool QJ>
 struct LvSmem {
     static constexpr int PS = NT == 1 ? 8 : 24;   // u32 per token row of a P tile (conflict-free reads)
-    static constexpr size_t tabK = 0, tabV = tabK + 4 * kTabWords, descK = tabV + 4 * kTabWords,
-                            descV = descK + 16 * D, bmK = descV + 16 * D, bmV = bmK + 64, wf = bmV + 64,
-                            pw = wf + size_t(8) * NT * 16 * 32, ob = pw + size_t(4) * kWarps * 32 * PS,
+    static constexpr size_t tabK = 0, tabV = tabK + 4 * kTabWords, tabS = tabV + 4 * kTabWords,
+                            descK = tabS + 4 * kSlot, descV = descK + 16 * D, bmK = descV + 16 * D,
+                            bmV = bmK + 64, wf = bmV + 64, wfq = wf + size_t(8) * NT * 16 * 32,
+                            pw = wfq + (QJ ? size_t(8) * NT * 16 * 32 : 0), ob = pw + size_t(4) * kWarps * 32 * PS,
                             mw = ob + size_t(8) * kWarps * NT * 8 * 32, lw = mw + 4 * 64, ring = lw + 4 * 64;
     static size_t total(int sw) { return 256 + ring + size_t(4) * kWarps * 2 * sw; }
 };
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kernel(const LvParams P)
+template <int NT, bool QJ>
+__global__ void __launch_bounds__(kThreads, (NT == 1 && !QJ) ? 3 : 2) attn_lv_split_kernel(const LvParams P)
 {
-    using L = LvSmem<NT>;
+    using L = LvSmem<NT, QJ>;
     constexpr int PS = L::PS;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((256u - (smem_u32(smem_raw) & 255u)) & 255u);
@@ -250,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
     int* bmK = reinterpret_cast<int*>(smem + L::bmK);     // [16] widest width of channels 8 kb .. 8 kb + 7
     int* bmV = reinterpret_cast<int*>(smem + L::bmV);     // [8] widest width of channels 16 mt .. 16 mt + 15
     uint2* Wf = reinterpret_cast<uint2*>(smem + L::wf);   // [NT][16][32] score-weight fragments
+    uint2* Wq = reinterpret_cast<uint2*>(smem + L::wfq);  // [NT][16][32] sketch-weight fragments (QJ)
+    uint32_t* tabS = reinterpret_cast<uint32_t*>(smem + L::tabS);   // the sketch's levels -1, +1
     uint32_t* Pw = reinterpret_cast<uint32_t*>(smem + L::pw);
     float2* Ob = reinterpret_cast<float2*>(smem + L::ob); // [8 warps][NT][8 m-tiles][32 lanes]
     float* mw = reinterpret_cast<float*>(smem + L::mw);   // [8 warps][8 heads]
@@ -309,6 +322,21 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
         }
         Wf[e] = v;
     }
+    if (QJ) {
+        // sketch weights w_ji log2(e), laid out like the score weights (row i = sketch row)
+        for (int e = tid; e < NT * 16 * 32; e += kThreads) {
+            const int nt = e / 512, kb = (e / 32) % 16, ln = e % 32;
+            const int gg = ln >> 2, tt = ln & 3, j = 4 * nt + (gg >> 1), y = gg & 1;
+            uint2 v = make_uint2(0u, 0u);
+            if (j < G) {
+                const float* w = P.qw + (int64_t(b) * P.Hq + h * G + j) * D;
+                v.x = bf16_part_dup(w[8 * kb + tt] * kLog2e, y);
+                v.y = bf16_part_dup(w[8 * kb + tt + 4] * kLog2e, y);
+            }
+            Wq[e] = v;
+        }
+        if (tid < kSlot) tabS[tid] = tid == 0 ? bf16_pair(-1.f) : (tid == 1 ? bf16_pair(1.f) : 0u);
+    }
     for (int e = tid; e < kWarps * NT * 8 * 32; e += kThreads) Ob[e] = make_float2(0.f, 0.f);
     __syncthreads();
     if (tid < 16) {
@@ -334,7 +362,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
     const int64_t g0 = s0 / kGroup;
     uint32_t* const slotK = ring + size_t(warp) * 2 * P.sw;
     uint32_t* const slotV = slotK + P.sw;
-    const int noff = P.sw - 32;      // the record's per-token norms (RWHT Lloyd-Max plans)
+    const int noff = P.nofs;         // the record's per-token norms (RWHT Lloyd-Max plans)
+    const int qoff = noff + 32;      // K slot (QJ): the sketch record (D words), then its norms
+    const float* qnr = QJ ? P.qnorms + sid * P.qnstride : nullptr;
+    const uint8_t* qs = QJ ? P.qbits + sid * P.qstride : nullptr;
 
     // one record (K: side 0, V: side 1) of the warp's it-th group into its
     // slot, with the norms where the plan has them; always commits
@@ -345,6 +376,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
             const int64_t grp = g0 + gi;
             if (side) copy_record(st, vs + grp * RV * 4, RV, lane);
             else copy_record(st, ks + grp * RK * 4, RK, lane);
+            if (QJ && !side) {
+                copy_record(st + qoff, qs + grp * D * 4, D, lane);
+                const int64_t t = grp * kGroup + lane;
+                float* qn = reinterpret_cast<float*>(st + qoff + D);
+                if (t < s1) cp_async4(smem_u32(qn + lane), qnr + t);
+                else qn[lane] = 0.f;
+            }
             if (side ? vtok : ktok) {
                 float* nst = reinterpret_cast<float*>(st + noff);
                 const int64_t t = grp * kGroup + lane;
@@ -409,7 +447,34 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
             else score_step(std::integral_constant<int, 0>{}, kb, bm);
         }
 
-        // scores of this thread's tokens (g + 8 m), scaled by the K norms
+        // the sketch correction: sum_i w_ji z_i(t), z = -1 / +1 for a clear / set bit
+        float sq[NT][2][4];
+        if (QJ) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sq[nt][0][r] = sq[nt][1][r] = 0.f;
+            const uint32_t* wq = wk + qoff;
+            const uint32_t ts = smem_u32(tabS);
+#pragma unroll 2
+            for (int kb = 0; kb < 16; ++kb) {
+                const uint32_t v0 = wq[8 * kb + tg], v1 = wq[8 * kb + 4 + tg];
+                const uint32_t x0 = __funnelshift_r(v0, v0, g - 2) & 0x04040404u;
+                const uint32_t x1 = __funnelshift_r(v1, v1, g - 2) & 0x04040404u;
+                const uint32_t a00 = level<2>(x0, ts, 0), a01 = level<2>(x0, ts, 1), a02 = level<2>(x0, ts, 2),
+                               a03 = level<2>(x0, ts, 3);
+                const uint32_t a10 = level<2>(x1, ts, 0), a11 = level<2>(x1, ts, 1), a12 = level<2>(x1, ts, 2),
+                               a13 = level<2>(x1, ts, 3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint2 wf = Wq[(nt * 16 + kb) * 32 + lane];
+                    mma_bf16(sq[nt][0], a00, a01, a10, a11, wf.x, wf.y);
+                    mma_bf16(sq[nt][1], a02, a03, a12, a13, wf.x, wf.y);
+                }
+            }
+        }
+        // scores of this thread's tokens (g + 8 m), scaled by the K norms,
+        // plus sqrt(pi/2)/d ||r_t|| times the sketch correction
         float s[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -420,6 +485,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 if (ktok) s[nt][m] *= nk[g + 8 * m];
+                if (QJ) {
+                    const float* qn = reinterpret_cast<const float*>(wk + qoff + D);
+                    const float c = sq[nt][m >> 1][2 * (m & 1)] + sq[nt][m >> 1][2 * (m & 1) + 1];
+                    s[nt][m] = fmaf(kQjlScale * qn[g + 8 * m], c, s[nt][m]);
+                }
                 s[nt][m] = (tb + 8 * m < s1) ? s[nt][m] : -INFINITY;
             }
         }
@@ -546,12 +616,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) attn_lv_split_kerne
 }  // namespace
 
 // Attention of any plan pair with head_dim 128 and at most eight query heads
-// per kv head, after attn_qrot_kernel has written qt; *done is false when
-// the shapes are not covered (nothing launched).
+// per kv head, after attn_qrot_kernel has written qt (and, with the sketch,
+// qw = S qt); *done is false when the shapes are not covered (nothing
+// launched).  qbits null: no sketch correction.
 spectra_status launch_attn_lv(const spectra_plan* kplan, const spectra_plan* vplan, const float* qt, int B, int Hq,
                               const uint8_t* kc, const uint8_t* vc, int64_t sstride, const float* kn,
                               const float* vn, int64_t nstride, int64_t ctx, float* part, int nsplit, int split_len,
-                              cudaStream_t s, bool* done)
+                              const uint8_t* qbits, int64_t qstride, const float* qnorms, int64_t qnstride,
+                              const float* qw, cudaStream_t s, bool* done)
 {
     *done = false;
     const int Hkv = kplan->heads, G = Hq / Hkv;
@@ -576,8 +648,15 @@ spectra_status launch_attn_lv(const spectra_plan* kplan, const spectra_plan* vpl
     P.ctx = ctx;
     P.part = part;
     // a slot: the widest record (16-byte multiple), the padding the plane
-    // reads may run into, then 32 norms
-    P.sw = ((std::max(RKm, RVm) + 3) & ~3) + kPad + 32;
+    // reads may run into, 32 norms; with the sketch, its record and norms
+    const bool qj = qbits != nullptr;
+    P.nofs = ((std::max(RKm, RVm) + 3) & ~3) + kPad;
+    P.sw = P.nofs + 32 + (qj ? D + 32 : 0);
+    P.qbits = qbits;
+    P.qstride = qstride;
+    P.qnorms = qnorms;
+    P.qnstride = qnstride;
+    P.qw = qw;
     dim3 grid(nsplit, Hkv, B);
     auto go = [&](auto kern, size_t sm) -> spectra_status {
         if (spectra_status e = set_smem(kern, sm)) return e;
@@ -588,10 +667,19 @@ spectra_status launch_attn_lv(const spectra_plan* kplan, const spectra_plan* vpl
     };
     // as many CTAs per SM as the registers allow, if the shared memory does
     // (228 KB per SM, 1 KB of it per CTA reserved)
-    for (int cap : {G <= 4 ? 3 : 2, 2, 1}) {
+    for (int cap : {(G <= 4 && !qj) ? 3 : 2, 2, 1}) {
         const size_t lim = size_t(228 * 1024) / cap - 1024;
-        if (G <= 4 && LvSmem<1>::total(P.sw) <= lim) return go(attn_lv_split_kernel<1>, LvSmem<1>::total(P.sw));
-        if (G > 4 && LvSmem<2>::total(P.sw) <= lim) return go(attn_lv_split_kernel<2>, LvSmem<2>::total(P.sw));
+        if (!qj) {
+            if (G <= 4 && LvSmem<1, false>::total(P.sw) <= lim)
+                return go(attn_lv_split_kernel<1, false>, LvSmem<1, false>::total(P.sw));
+            if (G > 4 && LvSmem<2, false>::total(P.sw) <= lim)
+                return go(attn_lv_split_kernel<2, false>, LvSmem<2, false>::total(P.sw));
+        } else {
+            if (G <= 4 && LvSmem<1, true>::total(P.sw) <= lim)
+                return go(attn_lv_split_kernel<1, true>, LvSmem<1, true>::total(P.sw));
+            if (G > 4 && LvSmem<2, true>::total(P.sw) <= lim)
+                return go(attn_lv_split_kernel<2, true>, LvSmem<2, true>::total(P.sw));
+        }
     }
     return SPECTRA_OK;
 }

@@ -73,8 +73,19 @@ def test_qjl_encode_matches_oracle(spx, orc, kind):
     assert flips <= 1e-3 * total, (flips, total)
 
 
-def test_attn_qjl_matches_oracle(spx, orc):
-    B, Hq, Hkv, ctx = 2, 8, 2, 1500
+@pytest.fixture(params=["tc", "generic"])
+def path(request):
+    """Kernel family: the level-table tensor-core kernel (required) or the
+    CUDA-core kernel."""
+    import kv_cache_transform_encode_b300 as spx
+    prev = spx.spectra_get_kernel_family()
+    spx.spectra_set_kernel_family({"tc": 2, "generic": 1}[request.param])
+    yield request.param
+    spx.spectra_set_kernel_family(prev)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,ctx", [(2, 8, 2, 1500), (2, 14, 2, 2048 + 1029)])
+def test_attn_qjl_matches_oracle(spx, orc, path, B, Hq, Hkv, ctx):
     S = np.random.default_rng(7).standard_normal((128, 128))
     S32 = S.astype(np.float32).astype(np.float64)
     kx = [synth.to_bf16_exact(synth.spiked_t(51 + b, ctx, Hkv, 128, role=synth.ROLE_K)).astype(np.float64)
