@@ -379,16 +379,22 @@ def run_ours(args, rank, world, local_rank):
 ATTN_B, ATTN_CTX = 16, 65536
 
 
-def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None, local_rank=None, rwht_norms=False):
+def attn_workload(spx, kp, vp, dev, peaks, reps=10, warm=3, batch=None, local_rank=None, rwht_norms=False,
+                  hq=None, ctx=None):
     """Decode-step attention at the compressed-attention workload: batch 16,
     32 query heads over 8 kv heads, 65536-token context packed at the plans'
     2.0 bits/value (K and V streams of 16 x 8 x 65536 tokens).  The stream
     contents are seeded random words -- every bit pattern is a valid code and
     the kernel's work does not depend on the values.  Two rotating stream
     sets (2 x 537 MB) keep each call's reads out of L2.  Timed with CUDA
-    events on the launching stream; GB/s counts the packed bytes read."""
+    events on the launching stream; GB/s counts the packed bytes read.
+    hq / ctx (and the plans' kv heads) give other head configurations and
+    context lengths."""
     import torch
     ATTN_B = batch or globals()["ATTN_B"]
+    HQ = hq or globals()["HQ"]
+    ATTN_CTX = ctx or globals()["ATTN_CTX"]
+    H_KV = kp.heads
     R = kp.max_rec_bits
     sb = spx.spectra_stream_bytes(R, ATTN_CTX)
     gen = torch.Generator(device=dev)
@@ -839,16 +845,26 @@ def qwen_rwht(spx, dev, peaks, local_rank, steps=4, e2e_steps=2, seed=2024):
                         "bytes_per_vector": per_vec},
            "relmse_k": round(rk, 6), "relmse_v": round(rv, 6), "cosine_k": round(ck, 6), "cosine_v": round(cv, 6),
            "clocks": clocks}
-    # decode-step attention over RWHT + 3-bit Lloyd-Max streams at the
-    # compressed-attention workload's shape (the CUDA-core kernel; 8 kv heads)
-    aps = []
-    for side in range(2):
-        ap = spx.Plan(H_KV, D, basis=spx.SPECTRA_BASIS_RWHT, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev)
-        ap.signs.copy_(torch.from_numpy(synth.rwht_signs(seed + 7 + side, H_KV, D)))
-        spx.spectra_alloc_bits(ap, 0.0, fixed_bits=3)
-        aps.append(ap)
+    # decode-step attention over RWHT + 3-bit Lloyd-Max streams (the
+    # level-table tensor-core kernel): at the compressed-attention workload's
+    # shape (32 query heads over 8 kv heads, 65536 tokens), and at the Qwen
+    # model's own head configuration (28 query heads over 4 kv heads, 7 per kv
+    # head) over its 131072-token context, batch 16
+    def rwht_plans(hkv):
+        ps = []
+        for side in range(2):
+            ap = spx.Plan(hkv, D, basis=spx.SPECTRA_BASIS_RWHT, quant=spx.SPECTRA_Q_LLOYD_GAUSS, device=dev)
+            ap.signs.copy_(torch.from_numpy(synth.rwht_signs(seed + 7 + side, hkv, D)))
+            spx.spectra_alloc_bits(ap, 0.0, fixed_bits=3)
+            ps.append(ap)
+        return ps
+    aps = rwht_plans(H_KV)
     res["attn_decode"] = attn_workload(spx, aps[0], aps[1], dev, peaks, reps=5, warm=2, local_rank=local_rank,
                                        rwht_norms=True)
+    aps = rwht_plans(QWEN_KV)
+    res["attn_decode_qwen_heads"] = attn_workload(spx, aps[0], aps[1], dev, peaks, reps=5, warm=2,
+                                                  local_rank=local_rank, rwht_norms=True, hq=28, ctx=QWEN_T)
+    del aps
     # end to end: pinned host K, V in, codes and norms out, every step
     try:
         hK = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
