@@ -35,7 +35,7 @@
 // single byte permute of (codes, slot address) is the lookup address.  The
 // planes of a step (8 or 16 channels) are read by one straight-line chain
 // for the step's widest width, entered by a single jump; a narrower
-// channel's extra words (its neighbour's planes, or the stage padding) are
+// channel's extra words (its neighbour's planes, or the slot padding) are
 // masked off.  Steps with a 7- or 8-bit channel take the same chain with
 // plain codes and a computed address.
 //
@@ -66,7 +66,7 @@ constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kSlot = 64;                  // words of a 256-byte table slot
 constexpr int kTabWords = 13 * kSlot;      // widths 0..6 one slot each, width 7 two, width 8 four
-constexpr int kPad = 8;                    // stage words past each record (reads up to 7 past a channel)
+constexpr int kPad = 8;                    // slot words past each record (reads up to 7 past a channel)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kQjlScale = 1.25331413731550025f / float(D);   // sqrt(pi / 2) / m, m = d sketch rows
@@ -232,10 +232,11 @@ struct LvParams {
     const float* qw;          // [B Hq][D]
 };
 
-// Shared memory (after aligning the start to 256 bytes): level tables,
-// channel descriptors (word offset, table address, code masks), per-step
-// widest widths, the score weights as B fragments, each warp's P tile and
-// value sums, the merge scalars, then the warps' record slots (two each).
+// Shared memory (after aligning the start to 256 bytes): level tables (K,
+// V, and the sketch's -1 / +1), channel descriptors (word offset, table
+// address, code masks), per-step widest widths, the score weights (and the
+// sketch weights) as B fragments, each warp's P tile and value sums, the
+// merge scalars, then the warps' record slots (two each).
 template <int NT, bool QJ>
 struct LvSmem {
     static constexpr int PS = NT == 1 ? 8 : 24;   // u32 per token row of a P tile (conflict-free reads)
@@ -243,8 +244,8 @@ struct LvSmem {
                             descK = tabS + 4 * kSlot, descV = descK + 16 * D, bmK = descV + 16 * D,
                             bmV = bmK + 64, wf = bmV + 64, wfq = wf + size_t(8) * NT * 16 * 32,
                             pw = wfq + (QJ ? size_t(8) * NT * 16 * 32 : 0), ob = pw + size_t(4) * kWarps * 32 * PS,
-                            mw = ob + size_t(8) * kWarps * NT * 8 * 32, lw = mw + 4 * 64, ring = lw + 4 * 64;
-    static size_t total(int sw) { return 256 + ring + size_t(4) * kWarps * 2 * sw; }
+                            mw = ob + size_t(8) * kWarps * NT * 8 * 32, lw = mw + 4 * 64, slots = lw + 4 * 64;
+    static size_t total(int sw) { return 256 + slots + size_t(4) * kWarps * 2 * sw; }
 };
 
 template <int NT, bool QJ>
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && !QJ) ? 3 : 2) attn_lv_sp
     float2* Ob = reinterpret_cast<float2*>(smem + L::ob); // [8 warps][NT][8 m-tiles][32 lanes]
     float* mw = reinterpret_cast<float*>(smem + L::mw);   // [8 warps][8 heads]
     float* lw = reinterpret_cast<float*>(smem + L::lw);
-    uint32_t* ring = reinterpret_cast<uint32_t*>(smem + L::ring);
+    uint32_t* slots = reinterpret_cast<uint32_t*>(smem + L::slots);   // [8 warps][K, V][sw]
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tg = lane & 3;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && !QJ) ? 3 : 2) attn_lv_sp
     const int64_t s1 = min(P.ctx, s0 + P.split_len);
     const int ng = int((s1 - s0 + kGroup - 1) / kGroup);   // s0 is a multiple of 32
     const int64_t g0 = s0 / kGroup;
-    uint32_t* const slotK = ring + size_t(warp) * 2 * P.sw;
+    uint32_t* const slotK = slots + size_t(warp) * 2 * P.sw;
     uint32_t* const slotV = slotK + P.sw;
     const int noff = P.nofs;         // the record's per-token norms (RWHT Lloyd-Max plans)
     const int qoff = noff + 32;      // K slot (QJ): the sketch record (D words), then its norms
