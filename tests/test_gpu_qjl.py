@@ -127,3 +127,62 @@ def test_attn_qjl_matches_oracle(spx, orc, path, B, Hq, Hkv, ctx):
     # the correction changes the result (it is not silently skipped)
     plain = orc.attn_decode(q.astype(np.float64), krec, vrec, 1.0)
     assert rel_l2(plain, want) > 10 * ATTN_TOL
+
+
+def test_attn_qjl_rwht_matches_oracle(spx, orc, path):
+    """TQ-KV with the QJL key sketch: RWHT + 3-bit Lloyd-Max plans (per-token
+    norms on both sides) and the sketch correction in the same scores, over
+    three context splits with a ragged last group."""
+    B, Hq, Hkv, ctx, d = 2, 8, 2, 2048 + 77, 128
+    S = np.random.default_rng(9).standard_normal((d, d))
+    S32 = S.astype(np.float32).astype(np.float64)
+    kx = [synth.to_bf16_exact(synth.spiked_t(61 + b, ctx, Hkv, d, role=synth.ROLE_K)).astype(np.float64)
+          for b in range(B)]
+    vx = [synth.to_bf16_exact(synth.spiked_t(61 + b, ctx, Hkv, d, role=synth.ROLE_V)).astype(np.float64)
+          for b in range(B)]
+    kp = orc.make_rwht_plan(synth.rwht_signs(63, Hkv, d), 3)
+    vp = orc.make_rwht_plan(synth.rwht_signs(64, Hkv, d), 3)
+    sb = orc.stream_bytes(ctx, 3 * d)
+    ks = np.zeros((B * Hkv, sb), np.uint8)
+    vs = np.zeros((B * Hkv, sb), np.uint8)
+    kn = np.zeros((B * Hkv, ctx), np.float32)
+    vn = np.zeros((B * Hkv, ctx), np.float32)
+    qbs = np.zeros((B * Hkv, orc.stream_bytes(ctx, d)), np.uint8)
+    qns = np.zeros((B * Hkv, ctx), np.float32)
+    kbits = np.zeros((B, Hkv, ctx, d), np.uint8)
+    knorm = np.zeros((B, Hkv, ctx))
+    krec = np.zeros((B, ctx, Hkv, d))
+    vrec = np.zeros((B, ctx, Hkv, d))
+    for b in range(B):
+        ek, ev = orc.encode(kp, kx[b]), orc.encode(vp, vx[b])
+        for h in range(Hkv):
+            i = b * Hkv + h
+            ks[i, : len(ek[h]["stream"])] = ek[h]["stream"]
+            vs[i, : len(ev[h]["stream"])] = ev[h]["stream"]
+            kn[i], vn[i] = ek[h]["norms"], ev[h]["norms"]
+            bits, nrm = orc.qjl_encode_head(kp, h, kx[b][:, h, :], ek[h]["stream"], S32, norms=ek[h]["norms"])
+            kbits[b, h], knorm[b, h] = bits, nrm.astype(np.float32)
+            qbs[i] = orc.pack(bits.astype(np.int32), np.ones(d, np.uint8))
+            qns[i] = nrm
+        krec[b] = orc.decode(kp, [e["stream"] for e in ek], ctx, [e["norms"] for e in ek])
+        vrec[b] = orc.decode(vp, [e["stream"] for e in ev], ctx, [e["norms"] for e in ev])
+    q = synth.to_bf16_exact(synth.queries(67, B, Hq, d))
+
+    def rot(v, h):
+        y = np.zeros((1, d))
+        orc.lib().orc_rwht(np.ascontiguousarray(v[None, :], dtype=np.float64), 1, d, d,
+                           np.ascontiguousarray(kp.signs[h], dtype=np.int8), y)
+        return y[0]
+    want = orc.attn_decode_qjl(q.astype(np.float64), krec, vrec, kbits, knorm, S32,
+                               [lambda v, h=h: rot(v, h) for h in range(Hkv)], 1.0)
+    gk, gv = gpu_plan(spx, kp), gpu_plan(spx, vp)
+    out = torch.zeros((B, Hq, d), device="cuda")
+    spx.spectra_attn_decode_qjl(gk, gv, torch.from_numpy(q).to(torch.bfloat16).cuda(), torch.from_numpy(ks).cuda(),
+                                torch.from_numpy(vs).cuda(), ctx, torch.from_numpy(S.astype(np.float32)).cuda(),
+                                torch.from_numpy(qbs).cuda(), torch.from_numpy(qns).cuda(), 1.0, out,
+                                k_norms=torch.from_numpy(kn).cuda(), v_norms=torch.from_numpy(vn).cuda())
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert rel_l2(got, want) <= ATTN_TOL, rel_l2(got, want)
+    plain = orc.attn_decode(q.astype(np.float64), krec, vrec, 1.0)
+    assert rel_l2(plain, want) > 10 * ATTN_TOL
